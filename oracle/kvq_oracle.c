@@ -1,0 +1,447 @@
+/*
+ * kvq_oracle.c — scalar CPU oracle for the FlashLoop packed-KV path.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may include, link,
+ * load or execute this file or the library built from it: only tests/,
+ * __graft_entry__.smoke() and the cpu_baseline / reference leg of bench.py use
+ * it. It shares no source with the CUDA path (own format indexing, own
+ * FP16/BF16 rounding written from IEEE-754, own group loops).
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fPIC -shared
+ *        (no SIMD intrinsics, no FMA contraction, IEEE single precision).
+ *
+ * Sources ("RFC" = "[RFC]: FlashLoop integration — token-sparse prefill,
+ * sparse decode attention, and KV residual quantization", vllm-rlt issue #156;
+ * "PR" = "INT4 KV packing/unpacking and cross-loop residual reconstruction",
+ * vllm-rlt pull #166):
+ *   - residual chain X̂1 = deq(q(X1)), δr = Xr − X̂(r−1), X̂r = X̂(r−1) + deq(q(δr)),
+ *     subtracting the reconstructed predecessor:            RFC §3.3 (first two paragraphs)
+ *   - affine INT4 group: scale = (max−min)/15, code = rounded/clipped
+ *     (x−min)/scale, decode = min + scale·code; constant groups explicit;
+ *     group size 64; FP16 params; K across token rows per channel, V across
+ *     channels per token; BF16 compute dtype:               RFC §3.3 (third paragraph)
+ *   - codes computed in FP32 before the FP16 metadata is rounded; nibble
+ *     order; compact-row K groups for sparse residuals:      PR, review by 0z5a
+ *   - two codes per uint8, FP16 min and scale, partial groups supported,
+ *     subtraction/addition in the input compute dtype:       PR, "Purpose"
+ *   - compact sparse residual rows, explicit logical→compact maps, absent
+ *     residual = inherit (not code 0); loop-4 read example:  RFC §3.3 (fourth paragraph)
+ *   - decode attention at the requested depth, scale 1/sqrt(head_dim):
+ *                                                           RFC §3.2
+ *
+ * Readings taken where the pages are silent (each also listed in the design doc):
+ *   - code rounding: round half to even, then clamp to [0, 15];
+ *   - division: IEEE-correct FP32 '/', no reciprocal;
+ *   - constant group (max == min): scale stored as +0, every code 0, min
+ *     stored as RN16(min); decoding gives min16;
+ *   - nibble order: the even channel sits in the low nibble;
+ *   - packing axis: channel pairs within one (row, head);
+ *   - dequantisation rounds to BF16: RN_bf16(RN32(min16 + RN32(scale16·c)));
+ *     each chain addition rounds to BF16: RN_bf16(RN32(X̂ + deq));
+ *   - residual: δ = RN_bf16(RN32(X_r − X̂_{r−1})) at the stored rows;
+ *   - GQA head mapping kv_head = q_head / (Hq / H);
+ *   - plane layout (head-major): codes u8[H][n][D/2]; K params f16[H][⌈n/G⌉][D];
+ *     V params f16[H][n][⌈D/G⌉]; sparse index int32[n] ascending.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_KIND_K 0
+#define ORC_KIND_V 1
+
+#define ORC_OK 0
+#define ORC_EINVAL (-1)
+#define ORC_ENOMEM (-2)
+
+/* ------------------------------------------------------------------------ */
+/* IEEE-754 conversions, written from the binary16 / bfloat16 definitions.   */
+/* ------------------------------------------------------------------------ */
+
+static uint32_t f32_bits(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return u;
+}
+
+static float bits_f32(uint32_t u) {
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* binary32 -> binary16, round to nearest, ties to even. Overflow gives ±inf,
+ * underflow goes through the binary16 subnormal range, NaN stays NaN. */
+uint16_t orc_f32_to_f16(float f) {
+  uint32_t x = f32_bits(f);
+  uint32_t sign = (x >> 16) & 0x8000u;
+  uint32_t exp = (x >> 23) & 0xFFu;
+  uint32_t man = x & 0x7FFFFFu;
+  if (exp == 0xFFu) {
+    if (man != 0) return (uint16_t)(sign | 0x7E00u);
+    return (uint16_t)(sign | 0x7C00u);
+  }
+  if (exp == 0) return (uint16_t)sign; /* |f| < 2^-126: far below half of the smallest f16 subnormal */
+  int e16 = (int)exp - 127 + 15;
+  if (e16 >= 31) return (uint16_t)(sign | 0x7C00u);
+  if (e16 <= 0) {
+    /* Result is a binary16 subnormal m * 2^-24 (or rounds up to the smallest normal).
+     * The binary32 significand with its hidden bit is sig * 2^(exp-150);
+     * m = sig * 2^(exp-150+24) = sig >> (126 - exp). */
+    int shift = 126 - (int)exp;
+    if (shift > 24) return (uint16_t)sign; /* |f| < 2^-25: rounds to zero */
+    uint32_t sig = man | 0x800000u;
+    uint32_t m = sig >> shift;
+    uint32_t rem = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (m & 1u))) m += 1u;
+    return (uint16_t)(sign | m);
+  }
+  uint32_t h = sign | ((uint32_t)e16 << 10) | (man >> 13);
+  uint32_t rem = man & 0x1FFFu;
+  if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h += 1u; /* a carry may roll into the exponent (and to inf) */
+  return (uint16_t)h;
+}
+
+float orc_f16_to_f32(uint16_t h) {
+  uint32_t sign = ((uint32_t)h & 0x8000u) << 16;
+  uint32_t exp = ((uint32_t)h >> 10) & 0x1Fu;
+  uint32_t man = (uint32_t)h & 0x3FFu;
+  if (exp == 0x1Fu) return bits_f32(sign | 0x7F800000u | (man << 13));
+  if (exp == 0) {
+    /* zero or subnormal: man * 2^-24, exact in binary32 */
+    float v = (float)man * 5.9604644775390625e-8f; /* 2^-24 */
+    return sign ? -v : v;
+  }
+  return bits_f32(sign | ((exp - 15u + 127u) << 23) | (man << 13));
+}
+
+/* binary32 -> bfloat16 (the upper half of binary32), round to nearest, ties to even. */
+uint16_t orc_f32_to_bf16(float f) {
+  uint32_t x = f32_bits(f);
+  if ((x & 0x7F800000u) == 0x7F800000u && (x & 0x7FFFFFu) != 0) return (uint16_t)((x >> 16) | 0x0040u);
+  uint32_t hi = x >> 16;
+  uint32_t rem = x & 0xFFFFu;
+  if (rem > 0x8000u || (rem == 0x8000u && (hi & 1u))) hi += 1u;
+  return (uint16_t)hi;
+}
+
+float orc_bf16_to_f32(uint16_t b) { return bits_f32((uint32_t)b << 16); }
+
+/* Batch forms of the conversions, for the tests that pin them. */
+void orc_f32_to_f16_n(const float* x, uint16_t* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = orc_f32_to_f16(x[i]);
+}
+void orc_f32_to_bf16_n(const float* x, uint16_t* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = orc_f32_to_bf16(x[i]);
+}
+void orc_f16_to_f32_n(const uint16_t* x, float* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = orc_f16_to_f32(x[i]);
+}
+
+/* Round half to even for 0 <= v < 2^22 (the quantiser's ratio lies in [0, 15]). */
+static float round_half_even(float v) {
+  float fl = floorf(v);
+  float frac = v - fl; /* exact: both lie in the same binade range below 2^23 */
+  if (frac > 0.5f) return fl + 1.0f;
+  if (frac < 0.5f) return fl;
+  return (fmodf(fl, 2.0f) == 0.0f) ? fl : fl + 1.0f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Affine INT4 group quantiser (RFC §3.3; FP32 codes before FP16 rounding,    */
+/* PR review by 0z5a).                                                        */
+/* ------------------------------------------------------------------------ */
+
+/* Quantise n values v[0], v[step], ... (each a BF16 value widened to FP32).
+ * Writes n codes in [0, 15] to code[0..n-1] and the FP16 min and scale. */
+static void quantize_group(const float* v, int n, int step, uint8_t* code, uint16_t* min16, uint16_t* scale16) {
+  float mn = v[0], mx = v[0];
+  for (int i = 1; i < n; ++i) {
+    float x = v[(int64_t)i * step];
+    if (x < mn) mn = x;
+    if (x > mx) mx = x;
+  }
+  *min16 = orc_f32_to_f16(mn);
+  if (mx == mn) { /* constant group: defined explicitly, no division */
+    *scale16 = orc_f32_to_f16(0.0f);
+    for (int i = 0; i < n; ++i) code[i] = 0;
+    return;
+  }
+  float range = mx - mn;      /* RN32 */
+  float s32 = range / 15.0f;  /* RN32, IEEE division */
+  *scale16 = orc_f32_to_f16(s32);
+  for (int i = 0; i < n; ++i) {
+    float x = v[(int64_t)i * step];
+    float diff = x - mn;      /* RN32, >= 0 */
+    float ratio = diff / s32; /* RN32, IEEE division */
+    float r = round_half_even(ratio);
+    if (r < 0.0f) r = 0.0f;
+    if (r > 15.0f) r = 15.0f;
+    code[i] = (uint8_t)r;
+  }
+}
+
+/* Decode one code: RN_bf16(RN32(f32(min16) + RN32(f32(scale16) * c))). */
+static float dequant(uint16_t min16, uint16_t scale16, int c) {
+  float m = orc_f16_to_f32(min16);
+  float s = orc_f16_to_f32(scale16);
+  float prod = s * (float)c;
+  float sum = m + prod;
+  return orc_bf16_to_f32(orc_f32_to_bf16(sum));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Plane geometry (head-major).                                              */
+/* ------------------------------------------------------------------------ */
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+/* Byte-exact sizes of the planes of one stream with n stored rows. */
+int64_t orc_codes_bytes(int n, int H, int D) { return (int64_t)H * n * (D / 2); }
+int64_t orc_param_count(int kind, int n, int H, int D, int G) {
+  if (kind == ORC_KIND_K) return (int64_t)H * ceil_div(n, G) * D;
+  return (int64_t)H * n * ceil_div(D, G);
+}
+int64_t orc_stream_bytes(int kind, int n, int H, int D, int G, int sparse) {
+  return orc_codes_bytes(n, H, D) + 2 * 2 * orc_param_count(kind, n, H, D, G) + (sparse ? 4 * (int64_t)n : 0);
+}
+
+static int64_t code_byte_index(int n, int D, int h, int row, int d) {
+  return ((int64_t)h * n + row) * (D / 2) + d / 2;
+}
+static int64_t param_index(int kind, int n, int D, int G, int h, int row, int d) {
+  if (kind == ORC_KIND_K) return ((int64_t)h * ceil_div(n, G) + row / G) * D + d;
+  return ((int64_t)h * n + row) * ceil_div(D, G) + d / G;
+}
+
+static int get_code(const uint8_t* codes, int n, int D, int h, int row, int d) {
+  uint8_t b = codes[code_byte_index(n, D, h, row, d)];
+  return (d & 1) ? (b >> 4) : (b & 0x0F);
+}
+
+/* An ascending, duplicate-free index list inside [0, T). */
+static int check_active(const int32_t* a, int n, int T) {
+  for (int i = 0; i < n; ++i) {
+    if (a[i] < 0 || a[i] >= T) return 0;
+    if (i > 0 && a[i] <= a[i - 1]) return 0;
+  }
+  return 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Encode one stream.                                                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * x    : BF16 bits [T][H][D], the loop-r source in logical token order.
+ * pred : BF16 bits [T][H][D], X̂_{r-1} in logical order; NULL encodes the base (loop 1).
+ * active, n : sorted logical rows to store (NULL: dense, n must equal T).
+ * Outputs use the head-major planes described at the top of the file.
+ */
+int orc_encode(int kind, int T, int H, int D, int G, const uint16_t* x, const uint16_t* pred, const int32_t* active,
+               int n, uint8_t* codes, uint16_t* mins, uint16_t* scales) {
+  if (T < 0 || H <= 0 || D <= 0 || (D & 1) || G <= 0) return ORC_EINVAL;
+  if (kind != ORC_KIND_K && kind != ORC_KIND_V) return ORC_EINVAL;
+  if (active == NULL) {
+    if (n != T) return ORC_EINVAL;
+  } else if (n < 0 || n > T || !check_active(active, n, T)) {
+    return ORC_EINVAL;
+  }
+  if (n == 0) return ORC_OK;
+
+  /* Values to quantise, in compact row order: v[row][h][d] (FP32 from BF16). */
+  float* v = (float*)malloc(sizeof(float) * (size_t)n * H * D);
+  uint8_t* c = (uint8_t*)malloc((size_t)n * H * D);
+  if (!v || !c) {
+    free(v);
+    free(c);
+    return ORC_ENOMEM;
+  }
+  for (int row = 0; row < n; ++row) {
+    int t = active ? active[row] : row;
+    for (int h = 0; h < H; ++h) {
+      for (int d = 0; d < D; ++d) {
+        int64_t li = ((int64_t)t * H + h) * D + d;
+        float xv = orc_bf16_to_f32(x[li]);
+        float val;
+        if (pred == NULL) {
+          val = xv;
+        } else {
+          float diff = xv - orc_bf16_to_f32(pred[li]); /* RN32 */
+          val = orc_bf16_to_f32(orc_f32_to_bf16(diff)); /* residual in the BF16 compute dtype */
+        }
+        v[((int64_t)row * H + h) * D + d] = val;
+      }
+    }
+  }
+
+  if (kind == ORC_KIND_K) {
+    /* K: per (head, channel), groups of G consecutive stored rows. */
+    int ng = (int)ceil_div(n, G);
+    uint8_t gc[4096];
+    for (int h = 0; h < H; ++h) {
+      for (int d = 0; d < D; ++d) {
+        for (int g = 0; g < ng; ++g) {
+          int r0 = g * G;
+          int len = (r0 + G <= n) ? G : n - r0;
+          const float* base = v + ((int64_t)r0 * H + h) * D + d;
+          uint16_t m16, s16;
+          quantize_group(base, len, H * D, gc, &m16, &s16);
+          for (int i = 0; i < len; ++i) c[((int64_t)(r0 + i) * H + h) * D + d] = gc[i];
+          int64_t pi = param_index(kind, n, D, G, h, r0, d);
+          mins[pi] = m16;
+          scales[pi] = s16;
+        }
+      }
+    }
+  } else {
+    /* V: per (stored row, head), groups of G consecutive channels. */
+    int ngc = (int)ceil_div(D, G);
+    uint8_t gc[4096];
+    for (int row = 0; row < n; ++row) {
+      for (int h = 0; h < H; ++h) {
+        for (int k = 0; k < ngc; ++k) {
+          int d0 = k * G;
+          int len = (d0 + G <= D) ? G : D - d0;
+          const float* base = v + ((int64_t)row * H + h) * D + d0;
+          uint16_t m16, s16;
+          quantize_group(base, len, 1, gc, &m16, &s16);
+          for (int i = 0; i < len; ++i) c[((int64_t)row * H + h) * D + d0 + i] = gc[i];
+          int64_t pi = param_index(kind, n, D, G, h, row, d0);
+          mins[pi] = m16;
+          scales[pi] = s16;
+        }
+      }
+    }
+  }
+
+  /* Pack: byte (h, row, k) = code(row, h, 2k) | code(row, h, 2k+1) << 4. */
+  for (int h = 0; h < H; ++h) {
+    for (int row = 0; row < n; ++row) {
+      for (int k = 0; k < D / 2; ++k) {
+        uint8_t lo = c[((int64_t)row * H + h) * D + 2 * k];
+        uint8_t hi = c[((int64_t)row * H + h) * D + 2 * k + 1];
+        codes[code_byte_index(n, D, h, row, 2 * k)] = (uint8_t)(lo | (hi << 4));
+      }
+    }
+  }
+  free(v);
+  free(c);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Reconstruct the chain to a requested depth (RFC §3.3).                     */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  int32_t n;              /* stored rows */
+  int32_t _pad;
+  const int32_t* active;  /* NULL: dense (n == T) */
+  const uint8_t* codes;
+  const uint16_t* mins;
+  const uint16_t* scales;
+} orc_stream;
+
+/*
+ * loops[0] is the base, loops[j-1] the residual of loop j. out: BF16 bits
+ * [T][H][D] in logical order. A token absent from loop j keeps its value
+ * (inheritance); it is never decoded from a code.
+ */
+int orc_reconstruct(int kind, int T, int H, int D, int G, int depth, const orc_stream* loops, uint16_t* out) {
+  if (T < 0 || H <= 0 || D <= 0 || (D & 1) || G <= 0 || depth < 1) return ORC_EINVAL;
+  if (loops[0].active != NULL || loops[0].n != T) return ORC_EINVAL;
+  for (int j = 1; j < depth; ++j) {
+    if (loops[j].active == NULL) {
+      if (loops[j].n != T) return ORC_EINVAL;
+    } else if (loops[j].n < 0 || loops[j].n > T || !check_active(loops[j].active, loops[j].n, T)) {
+      return ORC_EINVAL;
+    }
+  }
+  int32_t* rowmap = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+  if (!rowmap) return ORC_ENOMEM;
+
+  /* Base. */
+  const orc_stream* b = &loops[0];
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h)
+      for (int d = 0; d < D; ++d) {
+        int64_t pi = param_index(kind, T, D, G, h, t, d);
+        float val = dequant(b->mins[pi], b->scales[pi], get_code(b->codes, T, D, h, t, d));
+        out[((int64_t)t * H + h) * D + d] = orc_f32_to_bf16(val);
+      }
+
+  /* Residual loops 2..depth. */
+  for (int j = 1; j < depth; ++j) {
+    const orc_stream* s = &loops[j];
+    for (int t = 0; t < T; ++t) rowmap[t] = -1;
+    for (int i = 0; i < s->n; ++i) rowmap[s->active ? s->active[i] : i] = i;
+    for (int t = 0; t < T; ++t) {
+      int row = rowmap[t];
+      if (row < 0) continue; /* absent: inherit */
+      for (int h = 0; h < H; ++h)
+        for (int d = 0; d < D; ++d) {
+          int64_t pi = param_index(kind, s->n, D, G, h, row, d);
+          float dq = dequant(s->mins[pi], s->scales[pi], get_code(s->codes, s->n, D, h, row, d));
+          int64_t li = ((int64_t)t * H + h) * D + d;
+          float sum = orc_bf16_to_f32(out[li]) + dq; /* RN32 */
+          out[li] = orc_f32_to_bf16(sum);
+        }
+    }
+  }
+  free(rowmap);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention in FP32 on reconstructed K̂, V̂ (RFC §3.2, §5).             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * q: BF16 bits [Hq][D]; khat, vhat: BF16 bits [T][H][D]; out: FP32 [Hq][D].
+ * One query token attends to all T stored tokens (no mask: in decode the
+ * query follows every stored position). kv_head = q_head / (Hq / H).
+ * s_t = (sum_d q_d k_td, in channel order) * scale; p_t = exp(s_t - max s);
+ * o_d = (sum_t p_t v_td, in token order) / (sum_t p_t).
+ */
+int orc_attention(int T, int H, int Hq, int D, const uint16_t* q, const uint16_t* khat, const uint16_t* vhat,
+                  float scale, float* out) {
+  if (T <= 0 || H <= 0 || Hq <= 0 || D <= 0 || Hq % H != 0) return ORC_EINVAL;
+  int g = Hq / H;
+  float* s = (float*)malloc(sizeof(float) * (size_t)T);
+  float* acc = (float*)malloc(sizeof(float) * (size_t)D);
+  if (!s || !acc) {
+    free(s);
+    free(acc);
+    return ORC_ENOMEM;
+  }
+  for (int hq = 0; hq < Hq; ++hq) {
+    int h = hq / g;
+    float mx = -INFINITY;
+    for (int t = 0; t < T; ++t) {
+      float dot = 0.0f;
+      for (int d = 0; d < D; ++d) {
+        float prod = orc_bf16_to_f32(q[(int64_t)hq * D + d]) * orc_bf16_to_f32(khat[((int64_t)t * H + h) * D + d]);
+        dot = dot + prod;
+      }
+      s[t] = dot * scale;
+      if (s[t] > mx) mx = s[t];
+    }
+    float L = 0.0f;
+    for (int d = 0; d < D; ++d) acc[d] = 0.0f;
+    for (int t = 0; t < T; ++t) {
+      float p = expf(s[t] - mx);
+      L = L + p;
+      for (int d = 0; d < D; ++d) {
+        float prod = p * orc_bf16_to_f32(vhat[((int64_t)t * H + h) * D + d]);
+        acc[d] = acc[d] + prod;
+      }
+    }
+    for (int d = 0; d < D; ++d) out[(int64_t)hq * D + d] = acc[d] / L;
+  }
+  free(s);
+  free(acc);
+  return ORC_OK;
+}

@@ -1,0 +1,219 @@
+"""Python wrapper around the scalar CPU oracle (kvq_oracle.c).
+
+TEST INFRASTRUCTURE ONLY. Only tests/, ``__graft_entry__.smoke()`` and the
+cpu_baseline / reference leg of ``bench.py`` may import this module. It imports
+nothing from the product package; the product package never imports it.
+
+Arrays are numpy: BF16 and FP16 values travel as their uint16 bit patterns.
+Layouts (head-major planes) are those written in kvq_oracle.c's header.
+
+The chain helpers follow the FlashLoop RFC (vllm-rlt issue #156) §3.3: the
+base is encoded from X1; loop r encodes X_r minus the reconstruction at depth
+r-1, over all rows (dense) or over the sorted active rows (compact sparse).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvq_oracle.c")
+_LIB = os.path.join(_HERE, "liborc.so")
+_lock = threading.Lock()
+_lib = None
+
+KIND_K = 0
+KIND_V = 1
+GROUP = 64
+
+
+def build(force: bool = False) -> str:
+    """Compile kvq_oracle.c into liborc.so (plain scalar C, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = [
+            "gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+            "-Wall", "-Wextra", "-Wno-unused-parameter", _SRC, "-o", tmp, "-lm",
+        ]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Stream(ctypes.Structure):
+    _fields_ = [
+        ("n", ctypes.c_int32),
+        ("_pad", ctypes.c_int32),
+        ("active", ctypes.c_void_p),
+        ("codes", ctypes.c_void_p),
+        ("mins", ctypes.c_void_p),
+        ("scales", ctypes.c_void_p),
+    ]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+            L.orc_encode.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp, vp]
+            L.orc_encode.restype = i32
+            L.orc_reconstruct.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(_Stream), vp]
+            L.orc_reconstruct.restype = i32
+            L.orc_attention.argtypes = [i32, i32, i32, i32, vp, vp, vp, ctypes.c_float, vp]
+            L.orc_attention.restype = i32
+            L.orc_stream_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+            L.orc_stream_bytes.restype = i64
+            for name in ("orc_f32_to_f16_n", "orc_f32_to_bf16_n", "orc_f16_to_f32_n"):
+                getattr(L, name).argtypes = [vp, vp, i64]
+                getattr(L, name).restype = None
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+# --------------------------------------------------------------------------- rounding helpers
+
+
+def f32_to_f16_bits(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint16)
+    lib().orc_f32_to_f16_n(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def f32_to_bf16_bits(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint16)
+    lib().orc_f32_to_bf16_n(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def f16_bits_to_f32(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    y = np.empty(x.shape, dtype=np.float32)
+    lib().orc_f16_to_f32_n(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def bf16_bits_to_f32(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    return (x.astype(np.uint32) << 16).view(np.float32)
+
+
+# --------------------------------------------------------------------------- codec
+
+
+@dataclass
+class Stream:
+    """One encoded loop (base or residual) of K or V for one request/layer."""
+
+    kind: int
+    T: int
+    H: int
+    D: int
+    n: int
+    active: np.ndarray | None  # int32 [n] ascending, or None (dense)
+    codes: np.ndarray  # uint8 [H, n, D/2]
+    mins: np.ndarray  # uint16 (f16 bits): K [H, ceil(n/G), D]; V [H, n, ceil(D/G)]
+    scales: np.ndarray
+
+    def c_struct(self) -> _Stream:
+        s = _Stream()
+        s.n = self.n
+        s.active = None if self.active is None else self.active.ctypes.data
+        s.codes = self.codes.ctypes.data
+        s.mins = self.mins.ctypes.data
+        s.scales = self.scales.ctypes.data
+        return s
+
+
+def param_shape(kind: int, n: int, H: int, D: int, G: int = GROUP):
+    if kind == KIND_K:
+        return (H, -(-n // G), D)
+    return (H, n, -(-D // G))
+
+
+def encode(kind: int, x: np.ndarray, pred: np.ndarray | None = None, active: np.ndarray | None = None,
+           G: int = GROUP) -> Stream:
+    """Encode one stream. x, pred: uint16 BF16 bits [T, H, D] (logical order)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T, H, D = x.shape
+    if pred is not None:
+        pred = np.ascontiguousarray(pred, dtype=np.uint16)
+        assert pred.shape == x.shape
+    if active is not None:
+        active = np.ascontiguousarray(active, dtype=np.int32)
+        n = int(active.size)
+    else:
+        n = T
+    codes = np.zeros((H, n, D // 2), dtype=np.uint8)
+    mins = np.zeros(param_shape(kind, n, H, D, G), dtype=np.uint16)
+    scales = np.zeros_like(mins)
+    rc = lib().orc_encode(kind, T, H, D, G, _ptr(x), _ptr(pred), _ptr(active), n, _ptr(codes), _ptr(mins),
+                          _ptr(scales))
+    if rc != 0:
+        raise ValueError(f"orc_encode failed with status {rc}")
+    return Stream(kind, T, H, D, n, active, codes, mins, scales)
+
+
+def reconstruct(streams: list[Stream], depth: int, G: int = GROUP) -> np.ndarray:
+    """BF16 bits [T, H, D] of the chain summed to `depth` (1 = base only)."""
+    s0 = streams[0]
+    arr = (_Stream * depth)(*[s.c_struct() for s in streams[:depth]])
+    out = np.empty((s0.T, s0.H, s0.D), dtype=np.uint16)
+    rc = lib().orc_reconstruct(s0.kind, s0.T, s0.H, s0.D, G, depth, arr, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"orc_reconstruct failed with status {rc}")
+    return out
+
+
+def encode_chain(kind: int, xs: list[np.ndarray], actives: list[np.ndarray | None], G: int = GROUP) -> list[Stream]:
+    """Loop 1 encodes X1; loop r encodes X_r minus reconstruct(r-1) at its rows."""
+    streams = [encode(kind, xs[0], None, None, G)]
+    for r in range(1, len(xs)):
+        pred = reconstruct(streams, r, G)
+        streams.append(encode(kind, xs[r], pred, actives[r], G))
+    return streams
+
+
+def attention(q: np.ndarray, khat: np.ndarray, vhat: np.ndarray, scale: float) -> np.ndarray:
+    """FP32 decode attention of q [Hq, D] over K̂, V̂ [T, H, D] (all BF16 bits)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    khat = np.ascontiguousarray(khat, dtype=np.uint16)
+    vhat = np.ascontiguousarray(vhat, dtype=np.uint16)
+    Hq, D = q.shape
+    T, H, D2 = khat.shape
+    assert D2 == D and vhat.shape == khat.shape
+    out = np.empty((Hq, D), dtype=np.float32)
+    rc = lib().orc_attention(T, H, Hq, D, _ptr(q), _ptr(khat), _ptr(vhat), ctypes.c_float(scale), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"orc_attention failed with status {rc}")
+    return out
+
+
+def stream_bytes(kind: int, n: int, H: int, D: int, G: int = GROUP, sparse: bool = False) -> int:
+    return int(lib().orc_stream_bytes(kind, n, H, D, G, int(sparse)))
+
+
+def request_path(xk: list[np.ndarray], xv: list[np.ndarray], actives: list[np.ndarray | None], q: np.ndarray,
+                 depth: int, scale: float):
+    """The whole path for one request: encode both chains, reconstruct to
+    `depth`, attend. Returns (k_streams, v_streams, khat, vhat, out)."""
+    ks = encode_chain(KIND_K, xk, actives)
+    vs = encode_chain(KIND_V, xv, actives)
+    khat = reconstruct(ks, depth)
+    vhat = reconstruct(vs, depth)
+    out = attention(q, khat, vhat, scale)
+    return ks, vs, khat, vhat, out

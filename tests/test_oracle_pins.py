@@ -1,0 +1,454 @@
+"""Pins for the CPU oracle: facts fixed by the pages, by IEEE-754 and by
+mathematics, checked without reusing the oracle's own formulas.
+
+Page titles used below: "FlashLoop RFC" = "[RFC]: FlashLoop integration —
+token-sparse prefill, sparse decode attention, and KV residual quantization"
+(vllm-rlt issue #156); "codec PR" = "INT4 KV packing/unpacking and cross-loop
+residual reconstruction" (vllm-rlt pull #166).
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16(a) -> np.ndarray:
+    """float values -> BF16 bits via torch's cast (a library routine)."""
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def f32(bits) -> np.ndarray:
+    return O.bf16_bits_to_f32(bits)
+
+
+def f16_to_f32(bits) -> np.ndarray:
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def unpack(codes: np.ndarray) -> np.ndarray:
+    """uint8 [H, n, D/2] -> int codes [n, H, D]: the low nibble holds the even channel."""
+    H, n, half = codes.shape
+    out = np.empty((n, H, 2 * half), dtype=np.int64)
+    out[:, :, 0::2] = np.transpose(codes & 0x0F, (1, 0, 2))
+    out[:, :, 1::2] = np.transpose(codes >> 4, (1, 0, 2))
+    return out
+
+
+# ---------------------------------------------------------------- IEEE rounding helpers
+
+
+def _sample_f32_bits(n: int, seed: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    r = rng.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
+    # add every pattern whose low 16 bits sit at or next to a rounding tie, and special values
+    hi = rng.integers(0, 2**16, size=4096, dtype=np.uint64).astype(np.uint32) << 16
+    low = np.array([0x0000, 0x0001, 0x7FFF, 0x8000, 0x8001, 0xFFFF, 0x1000, 0x0FFF, 0x1001, 0x2000, 0x3000],
+                   dtype=np.uint32)
+    ties = (hi[:, None] | low[None, :]).ravel()
+    special = np.array([0, 0x80000000, 0x7F800000, 0xFF800000, 0x7F7FFFFF, 0x477FEFFF, 0x477FF000, 0x477FF001,
+                        0x38800000, 0x387FFFFF, 0x33800000, 0x33000000, 0x33000001, 0x00000001, 0x80000001],
+                       dtype=np.uint32)
+    # the whole binary16 subnormal/normal boundary region, densely
+    dense = (np.arange(0x33000000, 0x38900000, 97, dtype=np.uint64)).astype(np.uint32)
+    return np.concatenate([r, ties, special, dense])
+
+
+def test_f32_to_f16_matches_numpy_cast():
+    bits = _sample_f32_bits(1 << 22, 1)
+    x = bits.view(np.float32)
+    ours = O.f32_to_f16_bits(x)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    nan = np.isnan(x)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.all(np.isnan(ours[nan].view(np.float16)))
+
+
+def test_f16_to_f32_exhaustive():
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = O.f16_bits_to_f32(h)
+    ref = h.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+    assert np.all(np.isnan(ours[nan]))
+
+
+def test_f32_to_bf16_matches_torch_cast():
+    bits = _sample_f32_bits(1 << 22, 2)
+    x = bits.view(np.float32)
+    ours = O.f32_to_bf16_bits(x)
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(x)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.all(np.isnan(f32(ours[nan])))
+
+
+# ---------------------------------------------------------------- the INT4 group quantiser
+
+
+def _k_stream_of_columns(cols: np.ndarray):
+    """Encode columns cols[:, j] (each one K group over rows) as a K base stream."""
+    n, m = cols.shape
+    assert m % 2 == 0
+    x = bf16(cols.reshape(n, 1, m))
+    return x, O.encode(O.KIND_K, x)
+
+
+def _check_group_brute(xs: np.ndarray, codes: np.ndarray, min16: int, scale16: int):
+    """Exact-rational check of one group (xs: FP32 values of the BF16 inputs).
+
+    FlashLoop RFC §3.3: scale = (max - min)/15, code = rounded/clipped
+    (x - min)/scale; codec PR review by 0z5a: codes come from the FP32 scale,
+    the FP16 metadata is rounded afterwards.
+    """
+    mn, mx = float(np.min(xs)), float(np.max(xs))
+    assert codes.min() >= 0 and codes.max() <= 15
+    assert min16 == int(np.float16(np.float32(mn)).view(np.uint16))
+    if mx == mn:  # constant group: explicit, every code 0, scale stored as 0
+        assert np.all(codes == 0) and scale16 == 0
+        return
+    s32 = np.float32(np.float32(np.float32(mx) - np.float32(mn)) / np.float32(15.0))
+    assert scale16 == int(np.float16(s32).view(np.uint16))
+    S = Fraction(float(s32))
+    slack = Fraction(1, 1 << 19)  # FP32 rounding of (x - min) and of the ratio, in units of the scale
+    for x, c in zip(xs.tolist(), codes.tolist()):
+        r = (Fraction(x) - Fraction(mn)) / S
+        dist = abs(r - c)
+        assert dist <= Fraction(1, 2) + slack, (x, c, float(r))
+        for c2 in range(16):  # no other level is clearly closer
+            assert abs(r - c2) >= dist - 2 * slack, (x, c, c2)
+    # the group's minimum maps to code 0 and its maximum to code 15
+    assert codes[int(np.argmin(xs))] == 0
+    assert codes[int(np.argmax(xs))] == 15
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 17, 64])
+def test_quantiser_brute_force_random(n):
+    rng = np.random.default_rng(100 + n)
+    for trial in range(20):
+        cols = rng.standard_normal((n, 4)).astype(np.float32) * rng.choice([1e-3, 0.1, 1.0, 30.0])
+        cols[:, 3] = cols[0, 3]  # one constant column
+        x, s = _k_stream_of_columns(cols)
+        c = unpack(s.codes)[:, 0, :]
+        xs = f32(x)[:, 0, :]
+        for j in range(4):
+            _check_group_brute(xs[:, j], c[:, j], int(s.mins[0, 0, j]), int(s.scales[0, 0, j]))
+
+
+def test_quantiser_ties_round_half_even():
+    # min 0 and max 15 make the scale exactly 1, so (x - min)/scale is exact
+    col = np.array([0.0, 15.0, 0.5, 1.5, 2.5, 3.5, 6.5, 7.5, 14.5, 13.5], dtype=np.float32)
+    cols = np.stack([col, col], axis=1)
+    _, s = _k_stream_of_columns(cols)
+    c = unpack(s.codes)[:, 0, 0]
+    assert c.tolist() == [0, 15, 0, 2, 2, 4, 6, 8, 14, 14]
+
+
+def test_codes_use_fp32_scale_not_fp16_scale():
+    """Codec PR review by 0z5a: codes come from the FP32 scale before the FP16
+    metadata is rounded. Find a BF16 value whose code differs under the two."""
+    cand = None
+    for mx in (1.0078125, 1.0234375, 1.3671875, 1.6328125, 1.8828125, 2.0625, 3.8125):
+        mx = np.float32(mx)
+        s32 = np.float32(mx / np.float32(15.0))
+        s16 = np.float32(np.float16(s32))
+        if s16 == s32:
+            continue
+        vals = torch.arange(1, 1 << 15, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float().numpy()
+        vals = vals[(vals > 0) & (vals < mx)]
+        r32 = np.rint((vals / s32).astype(np.float32))
+        r16 = np.rint((vals / s16).astype(np.float32))
+        hit = np.nonzero(r32 != r16)[0]
+        if hit.size:
+            cand = (mx, np.float32(vals[hit[0]]), int(r32[hit[0]]), int(r16[hit[0]]))
+            break
+    assert cand is not None
+    mx, v, code32, code16 = cand
+    col = np.array([0.0, mx, v, v], dtype=np.float32)
+    _, s = _k_stream_of_columns(np.stack([col, col], axis=1))
+    c = unpack(s.codes)[2, 0, 0]
+    assert c == code32 and c != code16
+
+
+def test_constant_group_decodes_to_min16():
+    # FlashLoop RFC §3.3 and §9: constant groups are defined explicitly (no division by zero)
+    cols = np.full((64, 2), 3.140625, dtype=np.float32)
+    x, s = _k_stream_of_columns(cols)
+    assert np.all(unpack(s.codes) == 0) and np.all(s.scales == 0)
+    out = O.reconstruct([s], 1)
+    expect = bf16(f16_to_f32(s.mins[0, 0, 0]))
+    assert np.all(out == expect[()])
+    v = O.encode(O.KIND_V, bf16(np.full((3, 2, 128), -0.75, dtype=np.float32)))
+    assert np.all(v.scales == 0)
+    assert np.all(O.reconstruct([v], 1) == bf16(np.float32(-0.75))[()])
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_round_trip_bound(seed):
+    """|x - decode| <= scale/2 plus the FP16 metadata and BF16 output roundings."""
+    rng = np.random.default_rng(seed)
+    T, H, D = 70, 2, 96  # a partial K row group (6 rows) and a partial V channel group (32)
+    x = bf16(rng.standard_normal((T, H, D)) * 2.0)
+    xf = f32(x).astype(np.float64)
+    for kind in (O.KIND_K, O.KIND_V):
+        s = O.encode(kind, x)
+        dec = f32(O.reconstruct([s], 1)).astype(np.float64)
+        for t in range(T):
+            for h in range(H):
+                for d in range(D):
+                    if kind == O.KIND_K:
+                        rows = slice((t // 64) * 64, min((t // 64) * 64 + 64, T))
+                        grp = xf[rows, h, d]
+                        p = (h, t // 64, d)
+                    else:
+                        c0 = (d // 64) * 64
+                        grp = xf[t, h, c0:min(c0 + 64, D)]
+                        p = (h, t, d // 64)
+                    mn, mx = grp.min(), grp.max()
+                    s32 = float(np.float32(np.float32(mx - mn) / np.float32(15)))
+                    m16 = float(f16_to_f32(s.mins[p]))
+                    sc16 = float(f16_to_f32(s.scales[p]))
+                    bound = (s32 / 2 * (1 + 2**-18) + abs(mn - m16) + 15 * abs(s32 - sc16)
+                             + 2.0 ** (math.frexp(abs(dec[t, h, d]) or 1e-30)[1] - 9) + 1e-30)
+                    assert abs(xf[t, h, d] - dec[t, h, d]) <= bound, (kind, t, h, d)
+
+
+# ---------------------------------------------------------------- group geometry and packing
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 129, 1000])
+def test_group_boundaries_and_partial_tails(T):
+    """K groups hold <= 64 consecutive rows per (head, channel); V groups 64
+    channels per (row, head); tails hold only their true rows (codec PR, Purpose)."""
+    rng = np.random.default_rng(T)
+    H, D = 2, 128
+    x = bf16(rng.standard_normal((T, H, D)))
+    xf = f32(x)
+    k = O.encode(O.KIND_K, x)
+    assert k.mins.shape == (H, -(-T // 64), D)
+    for g in range(-(-T // 64)):
+        rows = xf[g * 64:min(g * 64 + 64, T)]
+        mn = rows.min(axis=0)  # [H, D]
+        assert np.array_equal(k.mins[:, g, :], mn.astype(np.float16).view(np.uint16))
+        mx = rows.max(axis=0)
+        s32 = ((mx - mn).astype(np.float32) / np.float32(15)).astype(np.float32)
+        s32[mx == mn] = 0
+        assert np.array_equal(k.scales[:, g, :], s32.astype(np.float16).view(np.uint16))
+    v = O.encode(O.KIND_V, x)
+    assert v.mins.shape == (H, T, 2)
+    for c in range(2):
+        grp = xf[:, :, c * 64:(c + 1) * 64]
+        assert np.array_equal(v.mins[:, :, c], grp.min(axis=2).T.astype(np.float16).view(np.uint16))
+
+
+def test_v_partial_channel_group():
+    rng = np.random.default_rng(7)
+    x = bf16(rng.standard_normal((5, 1, 80)))
+    xf = f32(x)
+    v = O.encode(O.KIND_V, x)
+    assert v.mins.shape == (1, 5, 2)
+    assert np.array_equal(v.mins[0, :, 1], xf[:, 0, 64:80].min(axis=1).astype(np.float16).view(np.uint16))
+
+
+def test_nibble_order_fixture():
+    gold = json.load(open(os.path.join(GOLD, "nibble_order.json")))
+    vc = gold["v_case"]
+    v = O.encode(O.KIND_V, bf16(np.array(vc["x"], dtype=np.float32).reshape(1, 1, 4)))
+    assert v.codes.ravel().tolist() == vc["bytes"]
+    assert unpack(v.codes).ravel().tolist() == vc["codes"]
+    kc = gold["k_case"]
+    k = O.encode(O.KIND_K, bf16(np.array(kc["x"], dtype=np.float32).reshape(4, 1, 2)))
+    assert k.codes.ravel().tolist() == kc["bytes_by_row"]
+
+
+def test_head_major_plane_layout():
+    """Byte (h, row, k) holds channels 2k, 2k+1 of (row, head h)."""
+    T, H, D = 3, 2, 4
+    x = np.zeros((T, H, D), dtype=np.float32)
+    x[:, :, 0] = 0.0
+    x[:, :, 1] = 15.0  # each V group: min 0 (channel 0), max 15 (channel 1), scale 1
+    x[1, 1, 2] = 7.0
+    x[2, 0, 3] = 9.0
+    v = O.encode(O.KIND_V, bf16(x))
+    assert v.codes.shape == (H, T, 2)
+    assert v.codes[1, 1, 1] == 7 and v.codes[0, 2, 1] == 9 << 4
+    assert np.all(v.codes[:, :, 0] == 0xF0)
+
+
+# ---------------------------------------------------------------- residual chains
+
+
+def test_residual_subtracts_reconstructed_predecessor():
+    """FlashLoop RFC §3.3 worked example: the residual is X[2] - X̂[1]; a raw
+    difference X[2] - X[1] would keep the first loop's error. With X2 == X1 the
+    raw difference is zero, while the right residual cancels most of the base error."""
+    rng = np.random.default_rng(11)
+    T, H, D = 128, 2, 128
+    x1 = bf16(rng.standard_normal((T, H, D)) * 3.0)
+    for kind in (O.KIND_K, O.KIND_V):
+        ks = O.encode_chain(kind, [x1, x1], [None, None])
+        e1 = np.abs(f32(O.reconstruct(ks, 1)) - f32(x1)).max()
+        e2 = np.abs(f32(O.reconstruct(ks, 2)) - f32(x1)).max()
+        assert e1 > 0.05
+        assert e2 < e1 / 6, (kind, e1, e2)
+        # the stored residual is exactly the quantisation of RN_bf16(X2 - X̂1)
+        xhat1 = f32(O.reconstruct(ks, 1))
+        delta = bf16(f32(x1) - xhat1)
+        ref = O.encode(kind, delta)
+        assert np.array_equal(ref.codes, ks[1].codes)
+        assert np.array_equal(ref.mins, ks[1].mins) and np.array_equal(ref.scales, ks[1].scales)
+
+
+def _offset_chain(T, H, D, seed):
+    rng = np.random.default_rng(seed)
+    xs = [rng.standard_normal((T, H, D)).astype(np.float32)]
+    for r in range(1, 4):
+        # a positive drift, so every residual group has a nonzero FP16 minimum
+        xs.append(xs[-1] + 0.25 + 0.1 * np.abs(rng.standard_normal((T, H, D))).astype(np.float32))
+    return [bf16(x) for x in xs]
+
+
+def test_loop4_read_example_inheritance():
+    """FlashLoop RFC §3.1 eight-token example and §3.3 loop-4 read resolution:
+    an absent residual means inheritance, not an INT4 code 0."""
+    gold = json.load(open(os.path.join(GOLD, "loop4_read_example.json")))
+    T = gold["T"]
+    act = {int(r): np.array(v, dtype=np.int32) - 1 for r, v in gold["active_1based"].items()}
+    xs = _offset_chain(T, 2, 128, 5)
+    actives = [None, None, act[3], act[4]]
+    for kind in (O.KIND_K, O.KIND_V):
+        ks = O.encode_chain(kind, xs, actives)
+        assert ks[2].n == 4 and ks[3].n == 2
+        assert np.all(f16_to_f32(ks[3].mins) > 0)  # a code-0 read would add this minimum
+        rec = {d: O.reconstruct(ks, d) for d in range(1, 5)}
+        for tok1, loops in gold["loop4_read_1based"].items():
+            t = int(tok1) - 1
+            last = max(loops)
+            # the value changes at each listed loop and never after the last one
+            for d in range(2, 5):
+                changed = not np.array_equal(rec[d][t], rec[d - 1][t])
+                assert changed == (d in loops), (kind, tok1, d)
+            assert np.array_equal(rec[4][t], rec[last][t])
+        # every token outside A4 keeps its depth-3 bits at depth 4
+        for t in range(T):
+            if t not in act[4]:
+                assert np.array_equal(rec[4][t], rec[3][t])
+
+
+def test_dense_equals_full_sparse():
+    T, H, D = 200, 2, 128
+    xs = _offset_chain(T, H, D, 9)
+    full = np.arange(T, dtype=np.int32)
+    for kind in (O.KIND_K, O.KIND_V):
+        a = O.encode_chain(kind, xs, [None] * 4)
+        b = O.encode_chain(kind, xs, [None, full, full, full])
+        for sa, sb in zip(a, b):
+            assert np.array_equal(sa.codes, sb.codes)
+            assert np.array_equal(sa.mins, sb.mins) and np.array_equal(sa.scales, sb.scales)
+        assert np.array_equal(O.reconstruct(a, 4), O.reconstruct(b, 4))
+
+
+def test_sparse_k_groups_follow_compact_rows():
+    """Codec PR review by 0z5a: sparse K groups run over compact rows, so one
+    group can mix distant logical positions."""
+    T, H, D = 300, 1, 128
+    xs = _offset_chain(T, H, D, 13)
+    rng = np.random.default_rng(3)
+    a = np.sort(rng.choice(T, 130, replace=False)).astype(np.int32)
+    ks = O.encode_chain(O.KIND_K, xs[:2] + [xs[2]], [None, None, a])
+    s = ks[2]
+    assert s.mins.shape == (H, 3, D)  # ceil(130/64) groups: 64, 64, 2 rows
+    pred = f32(O.reconstruct(ks, 2))
+    delta = f32(bf16(f32(xs[2])[a] - pred[a]))  # [130, H, D]
+    for g, rows in enumerate([slice(0, 64), slice(64, 128), slice(128, 130)]):
+        assert np.array_equal(s.mins[:, g, :], delta[rows].min(axis=0).astype(np.float16).view(np.uint16))
+
+
+def test_rejects_unsorted_or_out_of_range_active():
+    x = bf16(np.zeros((8, 1, 2), dtype=np.float32))
+    for bad in ([3, 1], [1, 1], [-1, 2], [2, 8]):
+        with pytest.raises(ValueError):
+            O.encode(O.KIND_K, x, x, np.array(bad, dtype=np.int32))
+
+
+# ---------------------------------------------------------------- storage accounting
+
+
+def test_storage_sizes_closed_form():
+    gold = json.load(open(os.path.join(GOLD, "storage.json")))
+    H, D = 8, 128
+    for n in (64, 128, 4096):  # full groups: 4 bits of code + 32 bits of params per 64 elements
+        for kind in (O.KIND_K, O.KIND_V):
+            bits = O.stream_bytes(kind, n, H, D) * 8 / (n * H * D)
+            assert bits == gold["bits_per_element_full_groups"]
+    # partial groups pay their padding: ceil(n/64) K groups
+    assert O.stream_bytes(O.KIND_K, 65, H, D) == 65 * H * 64 + 2 * 2 * 2 * H * D
+    assert O.stream_bytes(O.KIND_V, 65, H, D) == 65 * H * 64 + 2 * 2 * 65 * H * 2
+    assert O.stream_bytes(O.KIND_K, 65, H, D, sparse=True) == O.stream_bytes(O.KIND_K, 65, H, D) + 4 * 65
+    # the stored byte arrays have exactly these sizes
+    x = bf16(np.random.default_rng(0).standard_normal((65, H, D)))
+    for kind in (O.KIND_K, O.KIND_V):
+        s = O.encode(kind, x)
+        assert s.codes.nbytes + s.mins.nbytes + s.scales.nbytes == O.stream_bytes(kind, 65, H, D)
+    # payload-only ratio of four BF16 depths vs INT4 at retention [1, 1, 0.25, 0.10]
+    N = 6400
+    code_bytes = sum(O.encode(O.KIND_V, bf16(np.zeros((int(r * N), 1, 2), np.float32))).codes.nbytes
+                     for r in gold["retention"])
+    ratio = (4 * N * 16) / (code_bytes * 8 / 2)  # one code byte holds two channels
+    assert abs(ratio - 64 / 9.4) < 1e-9
+    assert round(ratio, 2) == gold["payload_ratio_about"]
+
+
+# ---------------------------------------------------------------- decode attention
+
+
+def _sdpa64(q, k, v, scale):
+    """Float64 reference through torch's scaled_dot_product_attention (GQA)."""
+    Hq, D = q.shape
+    T, H, _ = k.shape
+    g = Hq // H
+    qt = torch.from_numpy(f32(q).astype(np.float64)).reshape(1, Hq, 1, D)
+    kt = torch.from_numpy(f32(k).astype(np.float64)).permute(1, 0, 2).repeat_interleave(g, 0).unsqueeze(0)
+    vt = torch.from_numpy(f32(v).astype(np.float64)).permute(1, 0, 2).repeat_interleave(g, 0).unsqueeze(0)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+    return o.reshape(Hq, D).numpy()
+
+
+@pytest.mark.parametrize("T,H,Hq", [(1, 2, 8), (7, 2, 8), (300, 8, 32), (513, 8, 64), (100, 4, 4)])
+def test_attention_matches_float64_sdpa(T, H, Hq):
+    rng = np.random.default_rng(T + Hq)
+    D = 128
+    q = bf16(rng.standard_normal((Hq, D)))
+    k = bf16(rng.standard_normal((T, H, D)) * 1.5)
+    v = bf16(rng.standard_normal((T, H, D)))
+    scale = 1.0 / math.sqrt(D)
+    out = O.attention(q, k, v, scale)
+    ref = _sdpa64(q, k, v, scale)
+    assert np.max(np.abs(out - ref)) < 2e-5
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(5)
+    D, H, Hq = 128, 2, 8
+    v1 = bf16(rng.standard_normal((1, H, D)))
+    out = O.attention(bf16(rng.standard_normal((Hq, D))), bf16(rng.standard_normal((1, H, D))), v1, 0.088)
+    for hq in range(Hq):  # one stored token: the output is that token's value
+        assert np.array_equal(out[hq], f32(v1)[0, hq // 4])
+    T = 37
+    v = bf16(rng.standard_normal((T, H, D)))
+    out = O.attention(bf16(np.zeros((Hq, D))), bf16(rng.standard_normal((T, H, D))), v, 0.088)
+    mean = f32(v).astype(np.float64).mean(axis=0)  # equal logits: the plain mean
+    for hq in range(Hq):
+        assert np.max(np.abs(out[hq] - mean[hq // 4])) < 1e-6
