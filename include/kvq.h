@@ -1,0 +1,222 @@
+/*
+ * kvq.h — C ABI of libkvq.so: the FlashLoop packed-KV hot path on one GB300
+ * (sm_103a). INT4 base + cross-loop residual codec, residual-chain
+ * reconstruction, and packed-KV GQA decode attention.
+ *
+ * Pages cited ("RFC" = "[RFC]: FlashLoop integration — token-sparse prefill,
+ * sparse decode attention, and KV residual quantization", vllm-rlt issue #156;
+ * "codec PR" = "INT4 KV packing/unpacking and cross-loop residual
+ * reconstruction", vllm-rlt pull #166).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller. The library
+ *     allocates no device memory and keeps no pointer after a call returns.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: a call returns before the GPU finishes. No
+ *     call reads device data back to the host or synchronises (RFC §6.2).
+ *   - Arguments are checked on the host before anything is launched. A bad
+ *     argument returns a negative kvq_status and launches nothing; there is no
+ *     CPU fallback and no other backend (RFC §4: fail clearly).
+ *     kvq_last_error() gives a one-line reason for the last failure on the
+ *     calling thread.
+ *   - BF16 and FP16 values travel as their 16-bit patterns (uint16_t).
+ *   - The GPU kernels support head_dim == 128 (other sizes: UNSUPPORTED).
+ *
+ * Packed format, version 1 (one stream = one loop of K or V of one
+ * request/layer; RFC §3.3, codec PR "Purpose"):
+ *   codes   uint8  [H][n_rows][D/2]   byte (h,i,k) = code(i,h,2k) | code(i,h,2k+1) << 4
+ *   K mins, scales  FP16 [H][ceil(n_rows/64)][D]   one group = 64 consecutive stored
+ *                                                  rows of one (head, channel)
+ *   V mins, scales  FP16 [H][n_rows][ceil(D/64)]   one group = 64 channels of one
+ *                                                  (stored row, head)
+ *   active_idx int32 [n_rows]  ascending logical rows of a compact sparse
+ *                              residual; NULL for a dense stream (n_rows == n_tokens)
+ *   tile_dir   int32 [ceil(n_tokens/64)+1]  tile_dir[k] = number of active
+ *                              indices below 64k (derived map, see kvq_build_tile_dir)
+ * Quantiser (RFC §3.3; codes from the FP32 scale, then FP16 metadata, codec
+ * PR review by 0z5a): scale = RN32(RN32(max-min)/15); code =
+ * clamp(rint_even(RN32(RN32(x-min)/scale)), 0, 15); a constant group stores
+ * scale 0 and codes 0. Decode: RN_bf16(min16 + scale16*code). Residual loop r:
+ * delta = RN_bf16(X_r - X̂_{r-1}) at the stored rows; X̂_r = RN_bf16(X̂_{r-1} +
+ * decode(delta)) where a token is stored, and X̂_{r-1} (inherited) where it is
+ * absent (RFC §3.3: an absent residual is not an INT4 code 0).
+ *
+ * Alignment: every plane pointer (codes, mins, scales, active_idx) must be
+ * 16-byte aligned and its allocation at least kvq_plane_bytes() long (sizes
+ * are rounded up to 16 bytes so the kernels can move whole 16-byte vectors).
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_FORMAT_VERSION 1u
+#define KVQ_BITS 4
+#define KVQ_GROUP 64
+#define KVQ_TILE 64
+#define KVQ_MAX_LOOPS 8
+#define KVQ_NIBBLE_LO_FIRST 0
+
+typedef int32_t kvq_status;
+#define KVQ_OK 0
+#define KVQ_ERR_BAD_ARG (-1)     /* null pointer, size out of range, inconsistent descriptors */
+#define KVQ_ERR_UNSUPPORTED (-2) /* valid format the kernels do not implement (e.g. head_dim != 128) */
+#define KVQ_ERR_MISALIGNED (-3)  /* a plane pointer is not 16-byte aligned */
+#define KVQ_ERR_WORKSPACE (-4)   /* workspace missing or smaller than required */
+#define KVQ_ERR_CUDA (-5)        /* a CUDA runtime call or kernel launch failed */
+
+/* Opaque CUDA stream handle: identical to cudaStream_t. */
+typedef struct CUstream_st* kvq_cuda_stream;
+
+enum { KVQ_K = 0, KVQ_V = 1 };
+enum { KVQ_PLANE_CODES = 0, KVQ_PLANE_MINS = 1, KVQ_PLANE_SCALES = 2, KVQ_PLANE_INDEX = 3, KVQ_PLANE_TILE_DIR = 4 };
+
+/* Descriptor of one stream (host memory; the pointers inside are device
+ * pointers). The descriptor records format, grouping axis and group size
+ * (codec PR review by 0z5a: put format/axis/group_size in the descriptor). */
+typedef struct kvq_stream {
+  uint32_t version;          /* KVQ_FORMAT_VERSION */
+  uint8_t bits;              /* 4 */
+  uint8_t kind;              /* KVQ_K (groups over rows) or KVQ_V (groups over channels) */
+  uint16_t group;            /* 64 */
+  uint8_t nibble_order;      /* KVQ_NIBBLE_LO_FIRST */
+  uint8_t reserved[3];
+  int32_t n_rows;            /* stored rows: n_tokens if dense, |active set| if sparse */
+  int32_t n_tokens;          /* logical tokens T of the request */
+  int32_t n_heads;           /* KV heads H */
+  int32_t head_dim;          /* channels D */
+  uint8_t* codes;
+  uint16_t* mins;
+  uint16_t* scales;
+  const int32_t* active_idx; /* NULL: dense */
+  int32_t* tile_dir;         /* sparse streams: written by kvq_encode_residual, read by attention/reconstruct */
+} kvq_stream;
+
+/* Fill the format fields of `s` and clear its pointers. */
+kvq_status kvq_stream_init(kvq_stream* s, int kind, int n_rows, int n_tokens, int n_heads, int head_dim);
+
+/* Bytes to allocate for one plane of `s` (KVQ_PLANE_*), rounded up to 16. The
+ * index plane is at least 16 bytes, so that an empty sparse set still has a
+ * non-NULL active_idx (NULL marks a dense stream). */
+size_t kvq_plane_bytes(const kvq_stream* s, int plane);
+
+/* Byte-exact storage of one stream: codes + FP16 mins and scales (+ 4 bytes per
+ * row of sparse index), without the 16-byte allocation rounding and without the
+ * derived tile directory. 4.5 bits per element on full groups (codec PR review
+ * by 0z5a); partial groups pay their padding (RFC §7.4). */
+int64_t kvq_stream_payload_bytes(int kind, int n_rows, int n_heads, int head_dim, int sparse);
+
+/*
+ * Encode the loop-1 base of K or V (RFC §3.3: X̂[1] = deq(q(X[1]))).
+ *   x    BF16 [n_tokens][n_heads][head_dim], logical token-major, device.
+ *   out  dense stream (n_rows == n_tokens, active_idx NULL) whose codes, mins
+ *        and scales planes are written.
+ */
+kvq_status kvq_encode_base(const uint16_t* x, const kvq_stream* out, kvq_cuda_stream stream);
+
+/*
+ * Encode the residual of loop r = n_prev + 1 (RFC §3.3: delta[r] = X[r] -
+ * X̂[r-1], subtracting the reconstructed predecessor, which the kernel rebuilds
+ * from the packed chain at each stored row).
+ *   x_r   BF16 [n_tokens][n_heads][head_dim] source of loop r, logical order.
+ *   prev  n_prev descriptors of loops 1..r-1 (prev[0] the dense base); sparse
+ *         ones must carry their tile_dir.
+ *   out   stream of loop r: dense (active_idx NULL) or compact sparse over the
+ *         ascending active rows in out->active_idx (RFC §3.3: only active tokens
+ *         store a residual; K groups then run over compact rows, codec PR review
+ *         by 0z5a). For a sparse `out`, out->tile_dir must point to
+ *         kvq_plane_bytes(out, KVQ_PLANE_TILE_DIR) bytes and is written too.
+ * Preconditions (not checked on the device): active_idx ascending without
+ * duplicates, inside [0, n_tokens); nested in the previous sparse loop's set
+ * (RFC §3.1). Values |x| <= 65504 so FP16 metadata stays finite.
+ */
+kvq_status kvq_encode_residual(const uint16_t* x_r, const kvq_stream* prev, int n_prev, const kvq_stream* out,
+                               kvq_cuda_stream stream);
+
+/* Build tile_dir[0..ceil(n_tokens/64)] for an ascending active index list:
+ * tile_dir[k] = count of indices < 64k (the compact row where logical tile k
+ * starts; RFC §3.3 explicit logical-to-compact maps). */
+kvq_status kvq_build_tile_dir(const int32_t* active_idx, int n_rows, int n_tokens, int32_t* tile_dir,
+                              kvq_cuda_stream stream);
+
+/*
+ * Reconstruct X̂ at `depth` (1 = base only) into BF16 [n_tokens][n_heads][head_dim]
+ * (RFC §3.3: unpack, dequantise and sum the chain in BF16; absent tokens
+ * inherit). loops[0..depth-1] describe loops 1..depth of one K or V chain.
+ */
+kvq_status kvq_reconstruct(const kvq_stream* loops, int depth, uint16_t* out, kvq_cuda_stream stream);
+
+/* Per-request reference to the packed K and V chains, read by the attention
+ * kernel from DEVICE memory (an array of kvq_request, one per request). */
+typedef struct kvq_loop_ref {
+  int32_t n_rows;
+  int32_t reserved;
+  const int32_t* active_idx; /* NULL: dense */
+  const int32_t* tile_dir;   /* required for sparse loops */
+  const uint8_t* k_codes;
+  const uint16_t* k_mins;
+  const uint16_t* k_scales;
+  const uint8_t* v_codes;
+  const uint16_t* v_mins;
+  const uint16_t* v_scales;
+} kvq_loop_ref;
+
+typedef struct kvq_request {
+  int32_t n_tokens; /* T of this request (>= 0) */
+  int32_t n_loops;  /* loops stored (>= the requested depth) */
+  kvq_loop_ref loop[KVQ_MAX_LOOPS];
+} kvq_request;
+
+/* Host helper: fill one kvq_request from the K and V stream descriptors of a
+ * request (n_loops of each). Checks that K and V agree on rows and sets. */
+kvq_status kvq_request_fill(const kvq_stream* k_loops, const kvq_stream* v_loops, int n_loops, kvq_request* out);
+
+/* Workspace bytes kvq_decode_attn_packed needs on the current device. */
+size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim);
+
+#define KVQ_ATTN_AUTO 0 /* the fastest kernel for the shape (tensor-core MMA) */
+#define KVQ_ATTN_SIMT 1 /* CUDA-core kernel: exact BF16 chain per element, FP32 dot products */
+#define KVQ_ATTN_MMA 2  /* tensor-core kernel: unpack + folded dequant into m16n8k16 MMAs */
+
+/*
+ * Packed-KV GQA decode attention at `depth` (RFC §3.2: historical K/V are read
+ * at the requested depth and reconstructed if compressed; §3.3: readers consume
+ * packed base/residual tiles directly, with no BF16 shadow cache).
+ *   reqs       DEVICE array [n_requests] of kvq_request.
+ *   q          BF16 [n_requests][n_q_heads][head_dim], one decode query per request.
+ *   out        FP32 [n_requests][n_q_heads][head_dim].
+ *   softmax_scale  usually 1/sqrt(head_dim) (RFC §3.2).
+ *   workspace  DEVICE scratch of >= kvq_decode_attn_workspace_bytes(...) bytes,
+ *              16-byte aligned; int32 at offset 0 is an error word the kernels
+ *              set (nonzero) when a request's table entry is inconsistent; that
+ *              request's output is then NaN.
+ * Query head hq reads KV head hq / (n_q_heads / n_heads). Softmax and all
+ * accumulation are FP32. A request with n_tokens == 0 gets a zero output.
+ */
+kvq_status kvq_decode_attn_packed(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads,
+                                  int head_dim, int depth, const uint16_t* q, float softmax_scale, float* out,
+                                  void* workspace, size_t workspace_bytes, kvq_cuda_stream stream);
+
+/* Same, choosing the kernel (KVQ_ATTN_*). */
+kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads,
+                                     int head_dim, int depth, const uint16_t* q, float softmax_scale, float* out,
+                                     void* workspace, size_t workspace_bytes, int algo, kvq_cuda_stream stream);
+
+/* Human-readable name of a status code. */
+const char* kvq_status_string(kvq_status s);
+
+/* One-line reason for the last failing call on this thread ("" if none). */
+const char* kvq_last_error(void);
+
+/* Library and format version: (major << 16) | minor. */
+uint32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H_ */

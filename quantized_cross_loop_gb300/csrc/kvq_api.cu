@@ -1,0 +1,364 @@
+// kvq_api.cu — the extern "C" entry points of libkvq.so (declared in
+// include/kvq.h): host-side argument checks, then asynchronous launches on the
+// caller's stream. Nothing here allocates device memory or synchronises.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "kvq_attn_common.cuh"
+
+using namespace kvq;
+
+namespace {
+
+thread_local char g_err[512] = {0};
+
+kvq_status fail(kvq_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+kvq_status ok() {
+  g_err[0] = 0;
+  return KVQ_OK;
+}
+
+kvq_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(KVQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t round16(size_t x) { return (x + 15) / 16 * 16; }
+
+// Checks the format fields of a descriptor (not its pointers).
+kvq_status check_format(const kvq_stream* s, const char* name) {
+  if (s == nullptr) return fail(KVQ_ERR_BAD_ARG, "%s is NULL", name);
+  if (s->version != KVQ_FORMAT_VERSION) return fail(KVQ_ERR_UNSUPPORTED, "%s: format version %u", name, s->version);
+  if (s->bits != KVQ_BITS || s->group != KVQ_GROUP || s->nibble_order != KVQ_NIBBLE_LO_FIRST)
+    return fail(KVQ_ERR_UNSUPPORTED, "%s: bits %d group %d nibble order %d", name, s->bits, s->group,
+                s->nibble_order);
+  if (s->kind != KVQ_K && s->kind != KVQ_V) return fail(KVQ_ERR_BAD_ARG, "%s: kind %d", name, s->kind);
+  if (s->n_tokens < 0 || s->n_rows < 0 || s->n_rows > s->n_tokens)
+    return fail(KVQ_ERR_BAD_ARG, "%s: n_rows %d n_tokens %d", name, s->n_rows, s->n_tokens);
+  if (s->n_heads < 1 || s->n_heads > 1024) return fail(KVQ_ERR_BAD_ARG, "%s: n_heads %d", name, s->n_heads);
+  if (s->head_dim != kD) return fail(KVQ_ERR_UNSUPPORTED, "%s: head_dim %d (kernels support 128)", name, s->head_dim);
+  if (s->active_idx == nullptr && s->n_rows != s->n_tokens)
+    return fail(KVQ_ERR_BAD_ARG, "%s: dense stream with n_rows %d != n_tokens %d", name, s->n_rows, s->n_tokens);
+  return KVQ_OK;
+}
+
+// Checks pointers of a stream that is read (need_dir: sparse streams must carry tile_dir).
+kvq_status check_planes(const kvq_stream* s, const char* name, bool need_dir) {
+  kvq_status st = check_format(s, name);
+  if (st != KVQ_OK) return st;
+  if (s->n_rows == 0) return KVQ_OK;
+  if (!s->codes || !s->mins || !s->scales) return fail(KVQ_ERR_BAD_ARG, "%s: NULL plane", name);
+  if (!aligned16(s->codes) || !aligned16(s->mins) || !aligned16(s->scales) ||
+      (s->active_idx && !aligned16(s->active_idx)))
+    return fail(KVQ_ERR_MISALIGNED, "%s: planes must be 16-byte aligned", name);
+  if (need_dir && s->active_idx && !s->tile_dir) return fail(KVQ_ERR_BAD_ARG, "%s: sparse stream without tile_dir", name);
+  return KVQ_OK;
+}
+
+void to_planes(const kvq_stream* s, LoopPlanes* p) {
+  p->n_rows = s->n_rows;
+  p->sparse = s->active_idx != nullptr;
+  p->active = s->active_idx;
+  p->tile_dir = s->tile_dir;
+  p->codes = s->codes;
+  p->mins = s->mins;
+  p->scales = s->scales;
+}
+
+kvq_status build_chain(const kvq_stream* loops, int depth, Chain* C, const char* name) {
+  if (depth < 1 || depth > KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "%s: depth %d", name, depth);
+  if (loops == nullptr) return fail(KVQ_ERR_BAD_ARG, "%s is NULL", name);
+  for (int j = 0; j < depth; ++j) {
+    char nm[64];
+    snprintf(nm, sizeof nm, "%s[%d]", name, j);
+    kvq_status st = check_planes(&loops[j], nm, true);
+    if (st != KVQ_OK) return st;
+    if (loops[j].kind != loops[0].kind || loops[j].n_tokens != loops[0].n_tokens ||
+        loops[j].n_heads != loops[0].n_heads)
+      return fail(KVQ_ERR_BAD_ARG, "%s: loops disagree on kind, n_tokens or n_heads", name);
+  }
+  if (loops[0].active_idx != nullptr) return fail(KVQ_ERR_BAD_ARG, "%s[0]: the base must be dense", name);
+  memset(C, 0, sizeof *C);
+  C->depth = depth;
+  C->kind = loops[0].kind;
+  C->n_tokens = loops[0].n_tokens;
+  C->n_heads = loops[0].n_heads;
+  for (int j = 0; j < depth; ++j) to_planes(&loops[j], &C->loop[j]);
+  return KVQ_OK;
+}
+
+int sm_count(int device) {
+  static int cache[64] = {0};
+  if (device < 0 || device >= 64) return 0;
+  if (cache[device] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+    cache[device] = n;
+  }
+  return cache[device];
+}
+
+constexpr int kMaxCtasPerSm = 8;
+
+}  // namespace
+
+namespace kvq {
+int attn_ctas(int algo, int device) {
+  int sms = sm_count(device);
+  if (sms <= 0) return 0;
+  int per_sm = (algo == KVQ_ATTN_SIMT) ? 4 : 2;
+  if (per_sm > kMaxCtasPerSm) per_sm = kMaxCtasPerSm;
+  return sms * per_sm;
+}
+}  // namespace kvq
+
+extern "C" {
+
+uint32_t kvq_version(void) { return (1u << 16) | KVQ_FORMAT_VERSION; }
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_BAD_ARG: return "KVQ_ERR_BAD_ARG";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED";
+    case KVQ_ERR_MISALIGNED: return "KVQ_ERR_MISALIGNED";
+    case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA";
+    default: return "KVQ_ERR_UNKNOWN";
+  }
+}
+
+const char* kvq_last_error(void) { return g_err; }
+
+kvq_status kvq_stream_init(kvq_stream* s, int kind, int n_rows, int n_tokens, int n_heads, int head_dim) {
+  if (s == nullptr) return fail(KVQ_ERR_BAD_ARG, "stream is NULL");
+  memset(s, 0, sizeof *s);
+  s->version = KVQ_FORMAT_VERSION;
+  s->bits = KVQ_BITS;
+  s->kind = uint8_t(kind);
+  s->group = KVQ_GROUP;
+  s->nibble_order = KVQ_NIBBLE_LO_FIRST;
+  s->n_rows = n_rows;
+  s->n_tokens = n_tokens;
+  s->n_heads = n_heads;
+  s->head_dim = head_dim;
+  if (kind != KVQ_K && kind != KVQ_V) return fail(KVQ_ERR_BAD_ARG, "kind %d", kind);
+  if (n_tokens < 0 || n_rows < 0 || n_rows > n_tokens || n_heads < 1 || head_dim < 2 || (head_dim & 1))
+    return fail(KVQ_ERR_BAD_ARG, "sizes n_rows %d n_tokens %d n_heads %d head_dim %d", n_rows, n_tokens, n_heads,
+                head_dim);
+  return ok();
+}
+
+size_t kvq_plane_bytes(const kvq_stream* s, int plane) {
+  if (s == nullptr) return 0;
+  const int64_t n = s->n_rows, H = s->n_heads, D = s->head_dim;
+  switch (plane) {
+    case KVQ_PLANE_CODES: return round16(size_t(H * n * (D / 2)));
+    case KVQ_PLANE_MINS:
+    case KVQ_PLANE_SCALES:
+      if (s->kind == KVQ_K) return round16(size_t(2 * H * cdiv(n, KVQ_GROUP) * D));
+      return round16(size_t(2 * H * n * cdiv(D, KVQ_GROUP)));
+    case KVQ_PLANE_INDEX: return n > 0 ? round16(size_t(4 * n)) : 16;  // never NULL: NULL means dense
+    case KVQ_PLANE_TILE_DIR: return round16(size_t(4 * (cdiv(s->n_tokens, KVQ_TILE) + 1)));
+    default: return 0;
+  }
+}
+
+int64_t kvq_stream_payload_bytes(int kind, int n_rows, int n_heads, int head_dim, int sparse) {
+  const int64_t n = n_rows, H = n_heads, D = head_dim;
+  int64_t params = (kind == KVQ_K) ? H * cdiv(n, KVQ_GROUP) * D : H * n * cdiv(D, KVQ_GROUP);
+  return H * n * (D / 2) + 2 * 2 * params + (sparse ? 4 * n : 0);
+}
+
+kvq_status kvq_encode_base(const uint16_t* x, const kvq_stream* out, kvq_cuda_stream stream) {
+  kvq_status st = check_planes(out, "out", false);
+  if (st != KVQ_OK) return st;
+  if (out->active_idx != nullptr) return fail(KVQ_ERR_BAD_ARG, "out: the base stream must be dense");
+  if (out->n_rows == 0) return ok();
+  if (x == nullptr) return fail(KVQ_ERR_BAD_ARG, "x is NULL");
+  if (!aligned16(x)) return fail(KVQ_ERR_MISALIGNED, "x must be 16-byte aligned");
+  EncodeArgs a;
+  memset(&a, 0, sizeof a);
+  a.prev.depth = 0;
+  a.prev.kind = out->kind;
+  a.prev.n_tokens = out->n_tokens;
+  a.prev.n_heads = out->n_heads;
+  a.x = x;
+  a.n_rows = out->n_rows;
+  a.kind = out->kind;
+  a.active = nullptr;
+  a.codes = out->codes;
+  a.mins = out->mins;
+  a.scales = out->scales;
+  return cuda_status(launch_encode(a, reinterpret_cast<cudaStream_t>(stream)), "encode_base launch");
+}
+
+kvq_status kvq_build_tile_dir(const int32_t* active_idx, int n_rows, int n_tokens, int32_t* tile_dir,
+                              kvq_cuda_stream stream) {
+  if (n_rows < 0 || n_tokens < 0 || n_rows > n_tokens)
+    return fail(KVQ_ERR_BAD_ARG, "n_rows %d n_tokens %d", n_rows, n_tokens);
+  if (tile_dir == nullptr || (n_rows > 0 && active_idx == nullptr))
+    return fail(KVQ_ERR_BAD_ARG, "NULL active_idx or tile_dir");
+  return cuda_status(launch_tile_dir(active_idx, n_rows, n_tokens, tile_dir, reinterpret_cast<cudaStream_t>(stream)),
+                     "tile_dir launch");
+}
+
+kvq_status kvq_encode_residual(const uint16_t* x_r, const kvq_stream* prev, int n_prev, const kvq_stream* out,
+                               kvq_cuda_stream stream) {
+  if (n_prev < 1 || n_prev >= KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "n_prev %d", n_prev);
+  EncodeArgs a;
+  memset(&a, 0, sizeof a);
+  kvq_status st = build_chain(prev, n_prev, &a.prev, "prev");
+  if (st != KVQ_OK) return st;
+  st = check_planes(out, "out", false);
+  if (st != KVQ_OK) return st;
+  if (out->kind != prev[0].kind || out->n_tokens != prev[0].n_tokens || out->n_heads != prev[0].n_heads)
+    return fail(KVQ_ERR_BAD_ARG, "out disagrees with prev on kind, n_tokens or n_heads");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (out->active_idx != nullptr) {
+    if (out->tile_dir == nullptr) return fail(KVQ_ERR_BAD_ARG, "out: sparse stream needs tile_dir storage");
+    cudaError_t e = launch_tile_dir(out->active_idx, out->n_rows, out->n_tokens, out->tile_dir, s);
+    if (e != cudaSuccess) return cuda_status(e, "tile_dir launch");
+  }
+  if (out->n_rows == 0) return ok();
+  if (x_r == nullptr) return fail(KVQ_ERR_BAD_ARG, "x_r is NULL");
+  if (!aligned16(x_r)) return fail(KVQ_ERR_MISALIGNED, "x_r must be 16-byte aligned");
+  a.x = x_r;
+  a.n_rows = out->n_rows;
+  a.kind = out->kind;
+  a.active = out->active_idx;
+  a.codes = out->codes;
+  a.mins = out->mins;
+  a.scales = out->scales;
+  return cuda_status(launch_encode(a, s), "encode_residual launch");
+}
+
+kvq_status kvq_reconstruct(const kvq_stream* loops, int depth, uint16_t* out, kvq_cuda_stream stream) {
+  Chain C;
+  kvq_status st = build_chain(loops, depth, &C, "loops");
+  if (st != KVQ_OK) return st;
+  if (C.n_tokens == 0) return ok();
+  if (out == nullptr) return fail(KVQ_ERR_BAD_ARG, "out is NULL");
+  if (!aligned16(out)) return fail(KVQ_ERR_MISALIGNED, "out must be 16-byte aligned");
+  return cuda_status(launch_reconstruct(C, out, reinterpret_cast<cudaStream_t>(stream)), "reconstruct launch");
+}
+
+kvq_status kvq_request_fill(const kvq_stream* k_loops, const kvq_stream* v_loops, int n_loops, kvq_request* out) {
+  if (out == nullptr || k_loops == nullptr || v_loops == nullptr) return fail(KVQ_ERR_BAD_ARG, "NULL argument");
+  if (n_loops < 1 || n_loops > KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "n_loops %d", n_loops);
+  memset(out, 0, sizeof *out);
+  for (int j = 0; j < n_loops; ++j) {
+    const kvq_stream* k = &k_loops[j];
+    const kvq_stream* v = &v_loops[j];
+    kvq_status st = check_planes(k, "k_loops[j]", true);
+    if (st != KVQ_OK) return st;
+    st = check_planes(v, "v_loops[j]", true);
+    if (st != KVQ_OK) return st;
+    if (k->kind != KVQ_K || v->kind != KVQ_V) return fail(KVQ_ERR_BAD_ARG, "loop %d: kinds must be K and V", j);
+    if (k->n_rows != v->n_rows || k->n_tokens != v->n_tokens || k->n_heads != v->n_heads ||
+        (k->active_idx == nullptr) != (v->active_idx == nullptr))
+      return fail(KVQ_ERR_BAD_ARG, "loop %d: K and V streams disagree", j);
+    if (k->n_tokens != k_loops[0].n_tokens) return fail(KVQ_ERR_BAD_ARG, "loop %d: n_tokens differs", j);
+    if (j == 0 && k->active_idx != nullptr) return fail(KVQ_ERR_BAD_ARG, "loop 1 must be dense");
+    kvq_loop_ref& L = out->loop[j];
+    L.n_rows = k->n_rows;
+    L.active_idx = k->active_idx;
+    L.tile_dir = k->tile_dir ? k->tile_dir : v->tile_dir;
+    L.k_codes = k->codes;
+    L.k_mins = k->mins;
+    L.k_scales = k->scales;
+    L.v_codes = v->codes;
+    L.v_mins = v->mins;
+    L.v_scales = v->scales;
+  }
+  out->n_tokens = k_loops[0].n_tokens;
+  out->n_loops = n_loops;
+  return ok();
+}
+
+size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim) {
+  (void)n_q_heads;
+  (void)head_dim;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int sms = sm_count(dev);
+  if (n_requests < 0 || n_heads < 1 || sms <= 0) return 0;
+  return ws_bytes(n_requests, n_heads, sms * kMaxCtasPerSm);
+}
+
+kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads,
+                                     int head_dim, int depth, const uint16_t* q, float softmax_scale, float* out,
+                                     void* workspace, size_t workspace_bytes, int algo, kvq_cuda_stream stream) {
+  if (n_requests < 0) return fail(KVQ_ERR_BAD_ARG, "n_requests %d", n_requests);
+  if (n_heads < 1 || n_heads > 1024) return fail(KVQ_ERR_BAD_ARG, "n_heads %d", n_heads);
+  if (n_q_heads < n_heads || n_q_heads % n_heads != 0)
+    return fail(KVQ_ERR_BAD_ARG, "n_q_heads %d is not a multiple of n_heads %d", n_q_heads, n_heads);
+  const int g = n_q_heads / n_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8)
+    return fail(KVQ_ERR_UNSUPPORTED, "query heads per KV head %d (supported: 1, 2, 4, 8)", g);
+  if (head_dim != kD) return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d (kernels support 128)", head_dim);
+  if (depth < 1 || depth > KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "depth %d", depth);
+  if (!(softmax_scale > 0.0f) || softmax_scale > 1e30f) return fail(KVQ_ERR_BAD_ARG, "softmax_scale");
+  if (algo < KVQ_ATTN_AUTO || algo > KVQ_ATTN_MMA) return fail(KVQ_ERR_BAD_ARG, "algo %d", algo);
+  if (n_requests == 0) return ok();
+  if (!reqs || !q || !out) return fail(KVQ_ERR_BAD_ARG, "NULL reqs, q or out");
+  if (!aligned16(reqs) || !aligned16(q) || !aligned16(out))
+    return fail(KVQ_ERR_MISALIGNED, "reqs, q and out must be 16-byte aligned");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+  const int sms = sm_count(dev);
+  if (sms <= 0) return fail(KVQ_ERR_CUDA, "cannot read the SM count of device %d", dev);
+  const size_t need = ws_bytes(n_requests, n_heads, sms * kMaxCtasPerSm);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return fail(KVQ_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", need);
+  if (algo == KVQ_ATTN_AUTO) algo = KVQ_ATTN_SIMT;
+  if (algo == KVQ_ATTN_MMA) return fail(KVQ_ERR_UNSUPPORTED, "MMA kernel not built");
+
+  AttnArgs a;
+  memset(&a, 0, sizeof a);
+  a.reqs = reqs;
+  a.n_requests = n_requests;
+  a.H = n_heads;
+  a.Hq = n_q_heads;
+  a.g = g;
+  a.depth = depth;
+  a.n_ctas = attn_ctas(algo, dev);
+  a.q = q;
+  a.scale = softmax_scale;
+  a.out = out;
+  char* ws = static_cast<char*>(workspace);
+  a.err = reinterpret_cast<int32_t*>(ws);
+  a.prefix = reinterpret_cast<int32_t*>(ws + ws_prefix_offset());
+  a.partials = reinterpret_cast<float*>(ws + ws_partials_offset(n_requests));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  e = cudaMemsetAsync(a.err, 0, 16, s);
+  if (e != cudaSuccess) return cuda_status(e, "clear error word");
+  e = launch_plan(a, s);
+  if (e != cudaSuccess) return cuda_status(e, "plan launch");
+  e = (algo == KVQ_ATTN_SIMT) ? launch_attn_simt(a, s) : launch_attn_mma(a, s);
+  if (e != cudaSuccess) return cuda_status(e, "attention launch");
+  e = launch_combine(a, s);
+  if (e != cudaSuccess) return cuda_status(e, "combine launch");
+  return ok();
+}
+
+kvq_status kvq_decode_attn_packed(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads,
+                                  int head_dim, int depth, const uint16_t* q, float softmax_scale, float* out,
+                                  void* workspace, size_t workspace_bytes, kvq_cuda_stream stream) {
+  return kvq_decode_attn_packed_ex(reqs, n_requests, n_heads, n_q_heads, head_dim, depth, q, softmax_scale, out,
+                                   workspace, workspace_bytes, KVQ_ATTN_AUTO, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// kvq_attn_common.cuh — work decomposition shared by the decode-attention
+// kernels: a device-side plan (tile prefix over requests), a flat balanced
+// split of all (request, KV head, 64-token tile) work items over a fixed grid,
+// partial (max, sum, acc) slots, and the log-sum-exp combine.
+//
+// Work order: request b, then KV head h, then logical tile k. Unit u = b*H + h
+// owns tiles [prefix[b] + h*nt_b, prefix[b] + (h+1)*nt_b), nt_b = ceil(T_b/64).
+// CTA c owns the global tile range [floor(c*W/C), floor((c+1)*W/C)). A CTA that
+// covers a whole unit writes its output directly; otherwise it writes a partial
+// to slot c + u (distinct for every (c, u) pair because ranges are ordered and
+// contiguous), and the combine kernel merges the partials of the unit.
+#pragma once
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+constexpr int kMaxG = 8;                          // query heads per KV head
+constexpr int kSlotFloats = kMaxG * (kD + 2);     // m[8], l[8], acc[8][128]
+
+struct AttnArgs {
+  const kvq_request* reqs;
+  int32_t n_requests;
+  int32_t H;
+  int32_t Hq;
+  int32_t g;
+  int32_t depth;
+  int32_t n_ctas;
+  const uint16_t* q;  // BF16 [B][Hq][128]
+  float scale;        // softmax scale (natural-log units)
+  float* out;         // FP32 [B][Hq][128]
+  int32_t* err;       // error word
+  int32_t* prefix;    // [B+1] tile prefix
+  float* partials;    // slots
+};
+
+// Workspace layout: [0,16) error word; then int32 prefix[B+1] (rounded to 16 B);
+// then (n_ctas + B*H) partial slots of kSlotFloats floats.
+__host__ __device__ inline size_t ws_prefix_offset() { return 16; }
+__host__ __device__ inline size_t ws_partials_offset(int B) {
+  return 16 + ((size_t(B) + 1) * 4 + 15) / 16 * 16;
+}
+__host__ __device__ inline size_t ws_bytes(int B, int H, int n_ctas) {
+  return ws_partials_offset(B) + (size_t(n_ctas) + size_t(B) * H) * kSlotFloats * 4;
+}
+
+__device__ __forceinline__ long long cta_start(int c, long long W, int C) { return (long long)c * W / C; }
+
+// Largest c with cta_start(c) <= x, for 0 <= x < W.
+__device__ __forceinline__ int cta_of(long long x, long long W, int C) {
+  long long c = ((x + 1) * C + W - 1) / W - 1;
+  if (c < 0) c = 0;
+  if (c > C - 1) c = C - 1;
+  return int(c);
+}
+
+// Largest b with prefix[b] <= x (prefix is non-decreasing, prefix[0] = 0).
+__device__ __forceinline__ int request_of(const int32_t* prefix, int B, long long x) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int n_tiles_of(int T) { return (T + KVQ_TILE - 1) / KVQ_TILE; }
+
+// A request entry the kernels can read without going out of bounds.
+__device__ __forceinline__ bool request_ok(const kvq_request& r, int depth) {
+  if (r.n_tokens < 0 || r.n_loops < depth || r.n_loops > KVQ_MAX_LOOPS) return false;
+  if (r.n_tokens == 0) return true;
+  if (r.loop[0].active_idx != nullptr || r.loop[0].n_rows != r.n_tokens) return false;
+  for (int j = 0; j < depth; ++j) {
+    const kvq_loop_ref& L = r.loop[j];
+    if (L.n_rows < 0 || L.n_rows > r.n_tokens) return false;
+    if (L.active_idx == nullptr && L.n_rows != r.n_tokens) return false;
+    if (L.active_idx != nullptr && L.tile_dir == nullptr) return false;
+    if (L.n_rows > 0 && (L.k_codes == nullptr || L.v_codes == nullptr || L.k_mins == nullptr || L.k_scales == nullptr ||
+        L.v_mins == nullptr || L.v_scales == nullptr))
+      return false;
+  }
+  return true;
+}
+
+cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
+int attn_ctas(int algo, int device);
+
+}  // namespace kvq

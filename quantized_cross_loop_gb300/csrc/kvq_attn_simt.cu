@@ -1,0 +1,316 @@
+// kvq_attn_simt.cu — plan and combine kernels, and the CUDA-core decode
+// attention kernel over packed K/V.
+//
+// FlashLoop RFC (vllm-rlt issue #156) §3.2: historical K/V are read at the
+// requested depth and reconstructed if compressed; scores use 1/sqrt(head_dim);
+// §5: FP32 mass and accumulation; §3.3: readers consume the packed base and
+// residual tiles directly (no BF16 shadow cache in HBM).
+//
+// The CUDA-core kernel rebuilds each 64-token tile of K̂ and V̂ in shared memory
+// with the exact BF16 chain (bit-identical to the reconstruction), then runs
+// FP32 dot products, an online softmax and the PV sum. It is the reference
+// design the tensor-core kernel is measured against.
+#include "kvq_attn_common.cuh"
+
+namespace kvq {
+
+// ---------------------------------------------------------------- plan
+
+__global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a) {
+  __shared__ long long s_carry;
+  __shared__ int s_warp[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  if (threadIdx.x == 0) {
+    s_carry = 0;
+    a.prefix[0] = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < a.n_requests; base += blockDim.x) {
+    int b = base + threadIdx.x;
+    int v = 0;
+    if (b < a.n_requests) {
+      const kvq_request& r = a.reqs[b];
+      if (!request_ok(r, a.depth)) {
+        atomicOr(a.err, 1);
+      } else {
+        v = a.H * n_tiles_of(r.n_tokens);
+      }
+    }
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, w, off);
+        if (lane >= off) w += y;
+      }
+      s_warp[lane] = w;
+    }
+    __syncthreads();
+    long long incl = s_carry + (warp > 0 ? s_warp[warp - 1] : 0) + x;
+    if (incl > 0x7FFFFFFFLL) {  // more than 2^31 - 1 tiles in one call
+      atomicOr(a.err, 2);
+      incl = 0x7FFFFFFFLL;
+    }
+    if (b < a.n_requests) a.prefix[b + 1] = int(incl);
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_carry = incl;
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream) {
+  plan_kernel<<<1, 1024, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- combine
+
+__global__ void __launch_bounds__(kD) combine_kernel(AttnArgs a) {
+  const int u = blockIdx.x;
+  const int b = u / a.H, h = u % a.H;
+  const int d = threadIdx.x;
+  const int g = a.g;
+  const kvq_request& r = a.reqs[b];
+  float* outp = a.out + ((long long)b * a.Hq + (long long)h * g) * kD;
+  if (!request_ok(r, a.depth)) {
+    for (int i = 0; i < g; ++i) outp[i * kD + d] = __int_as_float(0x7fc00000);
+    return;
+  }
+  const int nt = n_tiles_of(r.n_tokens);
+  if (nt == 0) {
+    for (int i = 0; i < g; ++i) outp[i * kD + d] = 0.0f;
+    return;
+  }
+  const long long W = a.prefix[a.n_requests];
+  const int C = a.n_ctas;
+  const long long s = (long long)a.prefix[b] + (long long)h * nt;
+  const long long e = s + nt;
+  const int c_lo = cta_of(s, W, C), c_hi = cta_of(e - 1, W, C);
+  if (c_lo == c_hi) return;  // written directly by its only CTA
+  for (int i = 0; i < g; ++i) {
+    float M = -INFINITY;
+    for (int c = c_lo; c <= c_hi; ++c) {
+      if (cta_start(c, W, C) == cta_start(c + 1, W, C)) continue;  // empty range
+      const float* slot = a.partials + (size_t)(c + u) * kSlotFloats;
+      M = fmaxf(M, slot[i]);
+    }
+    float L = 0.0f, acc = 0.0f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+      if (cta_start(c, W, C) == cta_start(c + 1, W, C)) continue;
+      const float* slot = a.partials + (size_t)(c + u) * kSlotFloats;
+      float m = slot[i];
+      float w = (m == -INFINITY) ? 0.0f : exp2f(m - M);
+      L += slot[kMaxG + i] * w;
+      acc += slot[2 * kMaxG + i * kD + d] * w;
+    }
+    outp[i * kD + d] = acc / L;
+  }
+}
+
+cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
+  if (a.n_requests == 0) return cudaSuccess;
+  combine_kernel<<<a.n_requests * a.H, kD, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- CUDA-core attention
+
+// Softmax state is kept in the log2 domain: logits are scaled by
+// scale*log2(e) and exponentials are exp2.
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct SimtSmem {
+  float q[kMaxG][kD];
+  uint16_t khat[KVQ_TILE][kD];
+  uint16_t vhat[KVQ_TILE][kD];
+  float p[KVQ_TILE][kMaxG];
+  int map[KVQ_MAX_LOOPS][KVQ_TILE];
+  float m[kMaxG];
+  float l[kMaxG];
+  float alpha[kMaxG];
+  Chain ck;
+  Chain cv;
+};
+
+__device__ void simt_load_unit(const AttnArgs& a, SimtSmem& S, int b, int h) {
+  const int tid = threadIdx.x;
+  for (int k = tid; k < a.g * kD; k += blockDim.x) {
+    int i = k / kD, d = k % kD;
+    S.q[i][d] = bf16_bits_to_f32(a.q[((long long)b * a.Hq + (long long)h * a.g + i) * kD + d]) * (a.scale * kLog2e);
+  }
+  if (tid < kMaxG) {
+    S.m[tid] = -INFINITY;
+    S.l[tid] = 0.0f;
+  }
+  if (tid == 0) {
+    const kvq_request& r = a.reqs[b];
+    for (int kind = 0; kind < 2; ++kind) {
+      Chain& C = kind == 0 ? S.ck : S.cv;
+      C.depth = a.depth;
+      C.kind = kind;
+      C.n_tokens = r.n_tokens;
+      C.n_heads = a.H;
+      for (int j = 0; j < a.depth; ++j) {
+        const kvq_loop_ref& L = r.loop[j];
+        C.loop[j].n_rows = L.n_rows;
+        C.loop[j].sparse = L.active_idx != nullptr;
+        C.loop[j].active = L.active_idx;
+        C.loop[j].tile_dir = L.tile_dir;
+        C.loop[j].codes = kind == 0 ? L.k_codes : L.v_codes;
+        C.loop[j].mins = kind == 0 ? L.k_mins : L.v_mins;
+        C.loop[j].scales = kind == 0 ? L.k_scales : L.v_scales;
+      }
+    }
+  }
+}
+
+__device__ void simt_finish_unit(const AttnArgs& a, SimtSmem& S, float* acc, int b, int h, int u, bool whole) {
+  const int tid = threadIdx.x;
+  const int g = a.g;
+  if (whole) {
+    for (int k = tid, n = 0; k < g * kD; k += blockDim.x, ++n) {
+      int i = k / kD, d = k % kD;
+      a.out[((long long)b * a.Hq + (long long)h * g + i) * kD + d] = acc[n] / S.l[i];
+    }
+  } else {
+    float* slot = a.partials + (size_t)(blockIdx.x + u) * kSlotFloats;
+    if (tid < g) {
+      slot[tid] = S.m[tid];
+      slot[kMaxG + tid] = S.l[tid];
+    }
+    for (int k = tid, n = 0; k < g * kD; k += blockDim.x, ++n) {
+      int i = k / kD, d = k % kD;
+      slot[2 * kMaxG + i * kD + d] = acc[n];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
+  __shared__ SimtSmem S;
+  const int tid = threadIdx.x;
+  const int C = a.n_ctas;
+  const long long W = a.prefix[a.n_requests];
+  const long long s0 = cta_start(blockIdx.x, W, C), e0 = cta_start(blockIdx.x + 1, W, C);
+  if (s0 >= e0) return;
+  const int g = a.g;
+  constexpr int kAccMax = kMaxG * kD / 256;  // pairs (head, channel) per thread
+  float acc[kAccMax];
+
+  int b = request_of(a.prefix, a.n_requests, s0);
+  long long x = s0;
+  while (x < e0) {
+    // advance b to the request that owns tile x (skipping empty requests)
+    while (a.prefix[b + 1] <= x) ++b;
+    const kvq_request& r = a.reqs[b];
+    const int T = r.n_tokens;
+    const int nt = n_tiles_of(T);
+    const long long rb = a.prefix[b];
+    const int h = int((x - rb) / nt);
+    const long long us = rb + (long long)h * nt, ue = us + nt;
+    const int u = b * a.H + h;
+    const long long xe = ue < e0 ? ue : e0;
+
+    __syncthreads();
+    simt_load_unit(a, S, b, h);
+#pragma unroll
+    for (int n = 0; n < kAccMax; ++n) acc[n] = 0.0f;
+    __syncthreads();
+
+    for (; x < xe; ++x) {
+      const int k = int(x - us);
+      const int t0 = k * KVQ_TILE;
+      const int nvalid = min(KVQ_TILE, T - t0);
+      // logical -> stored row for every loop
+      for (int idx = tid; idx < a.depth * KVQ_TILE; idx += blockDim.x) {
+        int j = idx / KVQ_TILE, tt = idx % KVQ_TILE;
+        S.map[j][tt] = (S.ck.loop[j].sparse || tt >= nvalid) ? -1 : t0 + tt;
+      }
+      __syncthreads();
+      for (int j = 1; j < a.depth; ++j) {
+        const LoopPlanes& L = S.ck.loop[j];
+        if (!L.sparse) continue;
+        int c0 = __ldg(L.tile_dir + k), c1 = __ldg(L.tile_dir + k + 1);
+        if (c0 < 0 || c1 > L.n_rows || c1 - c0 > KVQ_TILE || c0 > c1) {
+          if (tid == 0) atomicOr(a.err, 4);
+          continue;
+        }
+        for (int c = c0 + tid; c < c1; c += blockDim.x) {
+          int tt = __ldg(L.active + c) - t0;
+          if (tt >= 0 && tt < KVQ_TILE) S.map[j][tt] = c;
+          else atomicOr(a.err, 4);
+        }
+      }
+      __syncthreads();
+      // exact BF16 chain for the tile's K̂ and V̂ rows
+      for (int idx = tid; idx < KVQ_TILE * (kD / 4); idx += blockDim.x) {
+        int tt = idx / (kD / 4), c0 = (idx % (kD / 4)) * 4;
+        if (tt < nvalid) {
+          int rows[KVQ_MAX_LOOPS];
+          for (int j = 0; j < a.depth; ++j) rows[j] = S.map[j][tt];
+          float kv[4], vv[4];
+          chain4(S.ck, a.depth, rows, h, c0, kv);
+          chain4(S.cv, a.depth, rows, h, c0, vv);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            S.khat[tt][c0 + e] = f32_to_bf16_bits(kv[e]);
+            S.vhat[tt][c0 + e] = f32_to_bf16_bits(vv[e]);
+          }
+        }
+      }
+      __syncthreads();
+      // logits (log2 units)
+      for (int idx = tid; idx < KVQ_TILE * g; idx += blockDim.x) {
+        int tt = idx / g, i = idx % g;
+        float sacc = -INFINITY;
+        if (tt < nvalid) {
+          sacc = 0.0f;
+          for (int d = 0; d < kD; ++d) sacc = fmaf(S.q[i][d], bf16_bits_to_f32(S.khat[tt][d]), sacc);
+        }
+        S.p[tt][i] = sacc;
+      }
+      __syncthreads();
+      if (tid < g) {
+        float mt = -INFINITY;
+        for (int tt = 0; tt < nvalid; ++tt) mt = fmaxf(mt, S.p[tt][tid]);
+        float mn = fmaxf(S.m[tid], mt);
+        float al = (S.m[tid] == -INFINITY) ? 0.0f : exp2f(S.m[tid] - mn);
+        float sum = 0.0f;
+        for (int tt = 0; tt < KVQ_TILE; ++tt) {
+          float p = tt < nvalid ? exp2f(S.p[tt][tid] - mn) : 0.0f;
+          S.p[tt][tid] = p;
+          sum += p;
+        }
+        S.alpha[tid] = al;
+        S.l[tid] = S.l[tid] * al + sum;
+        S.m[tid] = mn;
+      }
+      __syncthreads();
+      {
+        int n = 0;
+        for (int kk = tid; kk < g * kD; kk += blockDim.x, ++n) {
+          int i = kk / kD, d = kk % kD;
+          float s = acc[n] * S.alpha[i];
+          for (int tt = 0; tt < nvalid; ++tt) s = fmaf(S.p[tt][i], bf16_bits_to_f32(S.vhat[tt][d]), s);
+          acc[n] = s;
+        }
+      }
+      __syncthreads();
+    }
+    simt_finish_unit(a, S, acc, b, h, u, us >= s0 && ue <= e0);
+  }
+}
+
+cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream) {
+  attn_simt_kernel<<<a.n_ctas, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,153 @@
+// kvq_internal.cuh — device helpers shared by the codec, reconstruction and
+// attention kernels of libkvq. Codec arithmetic follows the quantiser and the
+// residual chain of the FlashLoop RFC (vllm-rlt issue #156) §3.3 with the FP32
+// codes / FP16 metadata order of the INT4 codec PR (vllm-rlt pull #166, review
+// by 0z5a). Every rounding step is an explicit round-to-nearest intrinsic, so
+// FMA contraction cannot change a codec result.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kD = 128;       // head_dim supported by the kernels
+constexpr int kG = KVQ_GROUP;  // 64
+constexpr int kRowBytes = kD / 2;  // packed bytes per (row, head)
+
+// Per-loop plane pointers as the kernels see them (a trimmed kvq_stream).
+struct LoopPlanes {
+  int32_t n_rows;
+  int32_t sparse;
+  const int32_t* active;
+  const int32_t* tile_dir;
+  const uint8_t* codes;
+  const uint16_t* mins;
+  const uint16_t* scales;
+};
+
+struct Chain {
+  int32_t depth;
+  int32_t kind;
+  int32_t n_tokens;
+  int32_t n_heads;
+  LoopPlanes loop[KVQ_MAX_LOOPS];
+};
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ float round_bf16(float f) { return bf16_bits_to_f32(f32_to_bf16_bits(f)); }
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+// decode(c) = RN_bf16(RN32(min16 + RN32(scale16 * c))).
+__device__ __forceinline__ float dequant(uint16_t min16, uint16_t scale16, int c) {
+  return round_bf16(__fadd_rn(f16_bits_to_f32(min16), __fmul_rn(f16_bits_to_f32(scale16), float(c))));
+}
+
+// Compact row of logical token t in a sparse loop, or -1 if t is absent. The
+// tile directory narrows the search to the <= 64 indices of t's 64-token tile.
+__device__ __forceinline__ int sparse_rank(const LoopPlanes& L, int t) {
+  int lo = __ldg(L.tile_dir + (t >> 6));
+  int hi = __ldg(L.tile_dir + (t >> 6) + 1);
+  if (lo < 0) lo = 0;
+  if (hi > L.n_rows) hi = L.n_rows;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    int v = __ldg(L.active + mid);
+    if (v < t) lo = mid + 1;
+    else hi = mid;
+  }
+  if (lo < L.n_rows && lo < __ldg(L.tile_dir + (t >> 6) + 1) && __ldg(L.active + lo) == t) return lo;
+  return -1;
+}
+
+__device__ __forceinline__ int row_of(const LoopPlanes& L, int t) { return L.sparse ? sparse_rank(L, t) : t; }
+
+__device__ __forceinline__ long long param_index(int kind, int n_rows, int h, int row, int d) {
+  if (kind == KVQ_K) return ((long long)h * ((n_rows + kG - 1) / kG) + row / kG) * kD + d;
+  return ((long long)h * n_rows + row) * (kD / kG) + d / kG;
+}
+
+// Reconstruct 4 consecutive channels c0..c0+3 (c0 % 4 == 0) of token t, head h,
+// through loops 0..depth-1, given each loop's stored row (rows[j] < 0: absent).
+__device__ __forceinline__ void chain4(const Chain& C, int depth, const int* rows, int h, int c0, float out[4]) {
+  {
+    const LoopPlanes& B = C.loop[0];
+    int row = rows[0];
+    uint16_t two = *reinterpret_cast<const uint16_t*>(B.codes + ((long long)h * B.n_rows + row) * kRowBytes + c0 / 2);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int c = (two >> (4 * e)) & 0xF;
+      long long pi = param_index(C.kind, B.n_rows, h, row, c0 + e);
+      out[e] = dequant(__ldg(B.mins + pi), __ldg(B.scales + pi), c);
+    }
+  }
+  for (int j = 1; j < depth; ++j) {
+    int row = rows[j];
+    if (row < 0) continue;  // absent: inherit the predecessor
+    const LoopPlanes& L = C.loop[j];
+    uint16_t two = *reinterpret_cast<const uint16_t*>(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + c0 / 2);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int c = (two >> (4 * e)) & 0xF;
+      long long pi = param_index(C.kind, L.n_rows, h, row, c0 + e);
+      out[e] = round_bf16(__fadd_rn(out[e], dequant(__ldg(L.mins + pi), __ldg(L.scales + pi), c)));
+    }
+  }
+}
+
+// Same for one channel d.
+__device__ __forceinline__ float chain1(const Chain& C, int depth, const int* rows, int h, int d) {
+  float v;
+  {
+    const LoopPlanes& B = C.loop[0];
+    int row = rows[0];
+    uint8_t byte = __ldg(B.codes + ((long long)h * B.n_rows + row) * kRowBytes + d / 2);
+    int c = (d & 1) ? (byte >> 4) : (byte & 0xF);
+    long long pi = param_index(C.kind, B.n_rows, h, row, d);
+    v = dequant(__ldg(B.mins + pi), __ldg(B.scales + pi), c);
+  }
+  for (int j = 1; j < depth; ++j) {
+    int row = rows[j];
+    if (row < 0) continue;
+    const LoopPlanes& L = C.loop[j];
+    uint8_t byte = __ldg(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + d / 2);
+    int c = (d & 1) ? (byte >> 4) : (byte & 0xF);
+    long long pi = param_index(C.kind, L.n_rows, h, row, d);
+    v = round_bf16(__fadd_rn(v, dequant(__ldg(L.mins + pi), __ldg(L.scales + pi), c)));
+  }
+  return v;
+}
+
+struct EncodeArgs {
+  Chain prev;             // loops 1..r-1 (prev.depth of them); depth 0 for the base
+  const uint16_t* x;      // BF16 [T][H][D] logical
+  int32_t n_rows;         // rows of the stream being written
+  int32_t kind;
+  const int32_t* active;  // NULL: dense
+  uint8_t* codes;
+  uint16_t* mins;
+  uint16_t* scales;
+};
+
+cudaError_t launch_encode(const EncodeArgs& a, cudaStream_t stream);
+cudaError_t launch_tile_dir(const int32_t* active, int n, int T, int32_t* dir, cudaStream_t stream);
+cudaError_t launch_reconstruct(const Chain& C, uint16_t* out, cudaStream_t stream);
+
+// Quantise one value against its group's FP32 min and scale (scale 0: constant group).
+__device__ __forceinline__ int quantize(float x, float mn, float s32) {
+  if (s32 == 0.0f) return 0;
+  float r = rintf(__fdiv_rn(__fsub_rn(x, mn), s32));
+  r = fminf(fmaxf(r, 0.0f), 15.0f);
+  return int(r);
+}
+
+}  // namespace kvq

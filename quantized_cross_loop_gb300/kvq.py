@@ -1,0 +1,305 @@
+"""Thin ctypes binding over libkvq.so (include/kvq.h).
+
+Argument marshalling only: PyTorch supplies device memory and the current
+CUDA stream; every step of the path runs in the library's kernels. The
+library is loaded on first use; if it is missing the call raises KvqError.
+There is no CPU fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvq.so")
+
+KVQ_K = 0
+KVQ_V = 1
+KVQ_GROUP = 64
+KVQ_TILE = 64
+KVQ_MAX_LOOPS = 8
+KVQ_FORMAT_VERSION = 1
+PLANE_CODES, PLANE_MINS, PLANE_SCALES, PLANE_INDEX, PLANE_TILE_DIR = range(5)
+ATTN_AUTO, ATTN_SIMT, ATTN_MMA = 0, 1, 2
+
+EXPORTED = (
+    "kvq_stream_init", "kvq_plane_bytes", "kvq_stream_payload_bytes", "kvq_encode_base", "kvq_encode_residual",
+    "kvq_build_tile_dir", "kvq_reconstruct", "kvq_request_fill", "kvq_decode_attn_workspace_bytes",
+    "kvq_decode_attn_packed", "kvq_decode_attn_packed_ex", "kvq_status_string", "kvq_last_error", "kvq_version",
+)
+
+
+class KvqError(RuntimeError):
+    pass
+
+
+class kvq_stream(ctypes.Structure):
+    _fields_ = [
+        ("version", ctypes.c_uint32),
+        ("bits", ctypes.c_uint8),
+        ("kind", ctypes.c_uint8),
+        ("group", ctypes.c_uint16),
+        ("nibble_order", ctypes.c_uint8),
+        ("reserved", ctypes.c_uint8 * 3),
+        ("n_rows", ctypes.c_int32),
+        ("n_tokens", ctypes.c_int32),
+        ("n_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("codes", ctypes.c_void_p),
+        ("mins", ctypes.c_void_p),
+        ("scales", ctypes.c_void_p),
+        ("active_idx", ctypes.c_void_p),
+        ("tile_dir", ctypes.c_void_p),
+    ]
+
+
+class kvq_loop_ref(ctypes.Structure):
+    _fields_ = [
+        ("n_rows", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("active_idx", ctypes.c_void_p),
+        ("tile_dir", ctypes.c_void_p),
+        ("k_codes", ctypes.c_void_p),
+        ("k_mins", ctypes.c_void_p),
+        ("k_scales", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("v_mins", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
+    ]
+
+
+class kvq_request(ctypes.Structure):
+    _fields_ = [
+        ("n_tokens", ctypes.c_int32),
+        ("n_loops", ctypes.c_int32),
+        ("loop", kvq_loop_ref * KVQ_MAX_LOOPS),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """Load libkvq.so (raises KvqError if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise KvqError(f"{LIB_PATH} is missing: build it with quantized_cross_loop_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            P = ctypes.POINTER
+            L.kvq_stream_init.argtypes = [P(kvq_stream), i32, i32, i32, i32, i32]
+            L.kvq_plane_bytes.argtypes = [P(kvq_stream), i32]
+            L.kvq_plane_bytes.restype = sz
+            L.kvq_stream_payload_bytes.argtypes = [i32, i32, i32, i32, i32]
+            L.kvq_stream_payload_bytes.restype = ctypes.c_int64
+            L.kvq_encode_base.argtypes = [vp, P(kvq_stream), vp]
+            L.kvq_encode_residual.argtypes = [vp, P(kvq_stream), i32, P(kvq_stream), vp]
+            L.kvq_build_tile_dir.argtypes = [vp, i32, i32, vp, vp]
+            L.kvq_reconstruct.argtypes = [P(kvq_stream), i32, vp, vp]
+            L.kvq_request_fill.argtypes = [P(kvq_stream), P(kvq_stream), i32, P(kvq_request)]
+            L.kvq_decode_attn_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            L.kvq_decode_attn_workspace_bytes.restype = sz
+            L.kvq_decode_attn_packed.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_float, vp, vp, sz, vp]
+            L.kvq_decode_attn_packed_ex.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_float, vp, vp, sz,
+                                                    i32, vp]
+            L.kvq_status_string.argtypes = [i32]
+            L.kvq_status_string.restype = ctypes.c_char_p
+            L.kvq_last_error.restype = ctypes.c_char_p
+            L.kvq_version.restype = ctypes.c_uint32
+            for name in ("kvq_stream_init", "kvq_encode_base", "kvq_encode_residual", "kvq_build_tile_dir",
+                         "kvq_reconstruct", "kvq_request_fill", "kvq_decode_attn_packed",
+                         "kvq_decode_attn_packed_ex"):
+                getattr(L, name).restype = ctypes.c_int32
+            _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        L = lib()
+        raise KvqError(f"{what}: {L.kvq_status_string(status).decode()} ({L.kvq_last_error().decode()})")
+
+
+def _stream_handle(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _require_cuda(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise KvqError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise KvqError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise KvqError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+class Stream:
+    """One encoded loop of K or V: the planes (torch tensors on the device) and
+    the C descriptor pointing at them."""
+
+    def __init__(self, kind: int, n_rows: int, n_tokens: int, n_heads: int, head_dim: int, device,
+                 active: torch.Tensor | None = None):
+        self.desc = kvq_stream()
+        _check(lib().kvq_stream_init(ctypes.byref(self.desc), kind, n_rows, n_tokens, n_heads, head_dim),
+               "kvq_stream_init")
+        self.kind, self.n_rows, self.n_tokens, self.n_heads, self.head_dim = kind, n_rows, n_tokens, n_heads, head_dim
+
+        def plane(p):
+            return torch.empty(int(lib().kvq_plane_bytes(ctypes.byref(self.desc), p)), dtype=torch.uint8,
+                               device=device)
+
+        self.codes = plane(PLANE_CODES)
+        self.mins = plane(PLANE_MINS)
+        self.scales = plane(PLANE_SCALES)
+        self.active = None
+        self.tile_dir = None
+        if active is not None:
+            buf = plane(PLANE_INDEX)
+            buf.view(torch.int32)[:n_rows].copy_(active.to(device=device, dtype=torch.int32))
+            self.active = buf
+            self.tile_dir = plane(PLANE_TILE_DIR)
+        self.desc.codes = self.codes.data_ptr()
+        self.desc.mins = self.mins.data_ptr()
+        self.desc.scales = self.scales.data_ptr()
+        self.desc.active_idx = None if self.active is None else self.active.data_ptr()
+        self.desc.tile_dir = None if self.tile_dir is None else self.tile_dir.data_ptr()
+
+    @property
+    def sparse(self) -> bool:
+        return self.active is not None
+
+    # views with the logical plane shapes
+    def codes_view(self):
+        return self.codes[: self.n_heads * self.n_rows * self.head_dim // 2].view(self.n_heads, self.n_rows,
+                                                                                  self.head_dim // 2)
+
+    def param_shape(self):
+        if self.kind == KVQ_K:
+            return (self.n_heads, -(-self.n_rows // KVQ_GROUP), self.head_dim)
+        return (self.n_heads, self.n_rows, -(-self.head_dim // KVQ_GROUP))
+
+    def mins_view(self):
+        shp = self.param_shape()
+        return self.mins.view(torch.int16)[: math.prod(shp)].view(shp)
+
+    def scales_view(self):
+        shp = self.param_shape()
+        return self.scales.view(torch.int16)[: math.prod(shp)].view(shp)
+
+    def active_view(self):
+        return None if self.active is None else self.active.view(torch.int32)[: self.n_rows]
+
+    def tile_dir_view(self):
+        if self.tile_dir is None:
+            return None
+        return self.tile_dir.view(torch.int32)[: -(-self.n_tokens // KVQ_TILE) + 1]
+
+
+def payload_bytes(kind: int, n_rows: int, n_heads: int, head_dim: int, sparse: bool) -> int:
+    return int(lib().kvq_stream_payload_bytes(kind, n_rows, n_heads, head_dim, int(sparse)))
+
+
+def kvq_encode_base(x: torch.Tensor, kind: int, stream=None) -> Stream:
+    """Encode the loop-1 base of K (kind=KVQ_K) or V from BF16 x [T, H, D]."""
+    _require_cuda(x, "x", torch.bfloat16)
+    T, H, D = x.shape
+    out = Stream(kind, T, T, H, D, x.device)
+    _check(lib().kvq_encode_base(_dptr(x), ctypes.byref(out.desc), _stream_handle(stream)), "kvq_encode_base")
+    return out
+
+
+def kvq_encode_residual(x_r: torch.Tensor, prev: list, active: torch.Tensor | None = None, stream=None) -> Stream:
+    """Encode loop len(prev)+1 of the chain `prev` from BF16 x_r [T, H, D];
+    `active` (sorted int32 logical rows) makes it a compact sparse residual."""
+    _require_cuda(x_r, "x_r", torch.bfloat16)
+    T, H, D = x_r.shape
+    kind = prev[0].kind
+    n = T if active is None else int(active.numel())
+    out = Stream(kind, n, T, H, D, x_r.device, active)
+    arr = (kvq_stream * len(prev))(*[p.desc for p in prev])
+    _check(lib().kvq_encode_residual(_dptr(x_r), arr, len(prev), ctypes.byref(out.desc), _stream_handle(stream)),
+           "kvq_encode_residual")
+    out._keep = list(prev)  # noqa: the chain must outlive the launch
+    return out
+
+
+def kvq_build_tile_dir(active: torch.Tensor, n_tokens: int, stream=None) -> torch.Tensor:
+    _require_cuda(active, "active", torch.int32)
+    out = torch.empty(-(-n_tokens // KVQ_TILE) + 1, dtype=torch.int32, device=active.device)
+    _check(lib().kvq_build_tile_dir(_dptr(active), active.numel(), n_tokens, _dptr(out), _stream_handle(stream)),
+           "kvq_build_tile_dir")
+    return out
+
+
+def kvq_reconstruct(streams: list, depth: int, stream=None) -> torch.Tensor:
+    """BF16 [T, H, D] reconstruction of the chain at `depth`."""
+    s0 = streams[0]
+    out = torch.empty((s0.n_tokens, s0.n_heads, s0.head_dim), dtype=torch.bfloat16, device=s0.codes.device)
+    arr = (kvq_stream * depth)(*[s.desc for s in streams[:depth]])
+    _check(lib().kvq_reconstruct(arr, depth, _dptr(out), _stream_handle(stream)), "kvq_reconstruct")
+    return out
+
+
+class RequestTable:
+    """Device array of kvq_request for a batch of requests (each a pair of K and
+    V stream lists). Holds references to the streams so their planes outlive it."""
+
+    def __init__(self, k_chains: list, v_chains: list, device=None):
+        n = len(k_chains)
+        host = (kvq_request * max(n, 1))()
+        for b in range(n):
+            ks, vs = k_chains[b], v_chains[b]
+            ka = (kvq_stream * len(ks))(*[s.desc for s in ks])
+            va = (kvq_stream * len(vs))(*[s.desc for s in vs])
+            _check(lib().kvq_request_fill(ka, va, len(ks), ctypes.byref(host[b])), f"kvq_request_fill[{b}]")
+        raw = bytes(memoryview(host).cast("B"))
+        if device is None:
+            device = k_chains[0][0].codes.device if n else torch.device("cuda")
+        self.table = torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(device)
+        self.n_requests = n
+        self._keep = (k_chains, v_chains)
+
+
+def kvq_decode_attn_workspace_bytes(n_requests: int, n_heads: int, n_q_heads: int, head_dim: int) -> int:
+    return int(lib().kvq_decode_attn_workspace_bytes(n_requests, n_heads, n_q_heads, head_dim))
+
+
+def kvq_decode_attn_packed(table: RequestTable, q: torch.Tensor, depth: int, n_heads: int,
+                           softmax_scale: float | None = None, algo: int = ATTN_AUTO, out: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """FP32 [B, Hq, D] decode attention of q [B, Hq, D] (BF16) over the packed
+    chains of `table` at `depth`."""
+    _require_cuda(q, "q", torch.bfloat16)
+    B, Hq, D = q.shape
+    if B != table.n_requests:
+        raise KvqError(f"q has {B} requests, table has {table.n_requests}")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    need = kvq_decode_attn_workspace_bytes(B, n_heads, Hq, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().kvq_decode_attn_packed_ex(_dptr(table.table), B, n_heads, Hq, D, depth, _dptr(q),
+                                           ctypes.c_float(softmax_scale), _dptr(out), _dptr(workspace),
+                                           workspace.numel(), algo, _stream_handle(stream)),
+           "kvq_decode_attn_packed")
+    return out
+
+
+def attn_error_word(workspace: torch.Tensor) -> int:
+    """The error word the attention kernels set in the workspace (reads the device)."""
+    return int(workspace[:4].view(torch.int32).item())
