@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Benchmark of the packed-KV hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic requests:
+batched encode of the loop-1 base and the loop-2..4 residuals of K and V,
+batched reconstruction at depth 4 of K and V, and packed-KV GQA decode
+attention at depth 4. Inputs are resident in HBM before the timed region and
+larger than L2. The reported value is algorithmic bytes per second of the
+whole step (every phase's algorithmic bytes, divided by the step time).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the CPU oracle timed on host cores)
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own independent
+batch (weak scaling), no data-path collective; the timed region is bracketed
+by a barrier and a synchronize, and the max time over ranks is reported.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "packed-KV decode attn GB/s & % of GB300 HBM peak; encode/reconstruct GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# name -> (configuration index, replicate count, description)
+WORKLOADS = {
+    "cfg2x512": (2, 512, "512 independent requests of the partial-group sparse configuration: 1000 tokens each "
+                         "(tail group of 40), H=8 KV heads x D=128, Hq=32, 4 loops, loops 3/4 compact sparse over "
+                         "nested random sets of 50%/25%"),
+    "cfg3": (3, 1, "32 requests x 4096 tokens, H=8 x D=128, Hq=32, 4 dense loops"),
+    "cfg4": (4, 1, "4 requests x 32768 tokens, H=8 x D=128, Hq=64, loops 3/4 sparse 50%/25%, 1% K outlier channels"),
+    "cfg1": (1, 1, "1 request x 256 tokens, H=8 x D=128, Hq=32, 4 dense loops"),
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="cfg2x512")
+    ap.add_argument("--algo", choices=["auto", "simt", "mma"], default="auto")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target wall time of the CPU-oracle sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ algorithmic bytes
+
+
+def request_sizes(req, H):
+    rows = [req.T if a is None else int(a.numel()) for a in req.active]
+    sparse = [a is not None for a in req.active]
+    return rows, sparse
+
+
+def algorithmic_bytes(reqs, H, D, Hq, depth, payload):
+    """Per-phase algorithmic bytes of one step.
+
+    encode (loop r, K or V): read the BF16 source rows (2*n_r*H*D), read the
+    predecessor chain at those rows (each earlier loop's payload scaled by
+    n_r/n_j), write the loop's payload. reconstruct: read the chain payload to
+    the depth, write BF16 [T, H, D]. attention: read the K and V chain payloads
+    (with the shared sparse index once), q (BF16) and the FP32 output."""
+    enc = rec = att = 0
+    tokens = 0
+    for req in reqs:
+        rows, sparse = request_sizes(req, H)
+        tokens += req.T
+        for kind in (0, 1):
+            pl = [payload(kind, rows[j], sparse[j]) for j in range(depth)]
+            for r in range(depth):
+                enc += 2 * rows[r] * H * D + pl[r]
+                for j in range(r):
+                    enc += pl[j] * (rows[r] / rows[j] if rows[j] else 0.0)
+            rec += sum(pl) + 2 * req.T * H * D
+        att += sum(payload(0, rows[j], sparse[j]) + payload(1, rows[j], False) for j in range(depth))
+        att += 2 * Hq * D + 4 * Hq * D
+    return {"encode": enc, "reconstruct": rec, "attention": att, "tokens": tokens}
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        self.gpu = ids[local_rank] if local_rank < len(ids) else str(local_rank)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))[kernel_key]
+    except Exception:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if sha != d.get("source_sha"):
+        return None
+    return d
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+
+def oracle_sample(reqs, q_rows, depth, scale, threads):
+    """Run the CPU oracle over `reqs` with `threads` host threads; returns seconds."""
+    from oracle import oracle as O
+    from quantized_cross_loop_gb300.workloads import bf16_bits
+
+    import numpy as np
+
+    host = []
+    for req, q in zip(reqs, q_rows):
+        host.append(([bf16_bits(x) for x in req.xk], [bf16_bits(x) for x in req.xv],
+                     [None if a is None else a.cpu().numpy().astype(np.int32) for a in req.active], bf16_bits(q)))
+    O.lib()
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda h: O.request_path(h[0], h[1], h[2], h[3], depth, scale), host))
+    return time.perf_counter() - t0
+
+
+# ------------------------------------------------------------------ main
+
+
+def main():
+    args = parse_args()
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg_idx, replicate, desc = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return run_reference(args, world, rank, cfg_idx, replicate, desc)
+
+    from quantized_cross_loop_gb300 import build as kbuild
+    from quantized_cross_loop_gb300 import kvq
+    from quantized_cross_loop_gb300 import workloads as W
+
+    if not os.path.exists(kvq.LIB_PATH):
+        kbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    # ---- workload, resident in HBM (each rank its own independent batch)
+    wl = W.make_workload(cfg_idx, device=dev, layer=rank, replicate=replicate)
+    reqs = wl.requests
+    B, H, D, Hq, depth = wl.n_requests, wl.H, wl.D, wl.Hq, wl.depth
+    lengths = [r.T for r in reqs]
+    pool = kvq.PackedPool(lengths, [r.active for r in reqs], H, D, depth, dev)
+    xk_ptrs = [kvq.pointer_array([r.xk[j] for r in reqs], dev) for j in range(depth)]
+    xv_ptrs = [kvq.pointer_array([r.xv[j] for r in reqs], dev) for j in range(depth)]
+    total_rows = sum(lengths)
+    rk = torch.empty((total_rows, H, D), dtype=torch.bfloat16, device=dev)
+    rv = torch.empty_like(rk)
+    offs = [0]
+    for t in lengths:
+        offs.append(offs[-1] + t)
+    rk_ptrs = kvq.pointer_array([rk[offs[b]:offs[b + 1]] for b in range(B)], dev)
+    rv_ptrs = kvq.pointer_array([rv[offs[b]:offs[b + 1]] for b in range(B)], dev)
+    q = wl.q.contiguous()
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(B, H, Hq, D), dtype=torch.uint8, device=dev)
+    algo = {"auto": kvq.ATTN_AUTO, "simt": kvq.ATTN_SIMT, "mma": kvq.ATTN_MMA}[args.algo]
+    stream = torch.cuda.current_stream()
+
+    def encode_all():
+        for j in range(depth):
+            kvq.kvq_encode_batch(pool, kvq.KVQ_K, j, xk_ptrs[j])
+            kvq.kvq_encode_batch(pool, kvq.KVQ_V, j, xv_ptrs[j])
+
+    def reconstruct_all():
+        kvq.kvq_reconstruct_batch(pool, kvq.KVQ_K, depth, rk_ptrs)
+        kvq.kvq_reconstruct_batch(pool, kvq.KVQ_V, depth, rv_ptrs)
+
+    def attend():
+        kvq.kvq_decode_attn_packed(pool.table, q, depth, H, algo=algo, out=out, workspace=ws)
+
+    n_ev = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+
+    def step(e=None):
+        if e:
+            e[0].record(stream)
+        encode_all()
+        if e:
+            e[1].record(stream)
+        reconstruct_all()
+        if e:
+            e[2].record(stream)
+        attend()
+        if e:
+            e[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    err = kvq.attn_error_word(ws)
+    if err:
+        raise RuntimeError(f"attention error word {err}")
+
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start
+    launches0 = kvq.launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = kvq.launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    enc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    rec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    att_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    ab = algorithmic_bytes(reqs, H, D, Hq, depth, lambda k, n, s: kvq.payload_bytes(k, n, H, D, s))
+    step_bytes = ab["encode"] + ab["reconstruct"] + ab["attention"]
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    phase_ms = {"encode": enc_ms, "reconstruct": rec_ms, "attention": att_ms}
+    phase_gbs = {k: ab[k] / (phase_ms[k] * 1e-3) / 1e9 for k in phase_ms}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, torch, kvq, reqs, q, out, step, stream, world, dev, step_bytes, dist)
+
+    # ---- roofline of the attention kernel call (plan + attention + combine)
+    dominant = max(phase_ms, key=phase_ms.get)
+    att_key = {kvq.ATTN_AUTO: "attn_auto", kvq.ATTN_SIMT: "attn_simt", kvq.ATTN_MMA: "attn_mma"}[algo]
+    tr = kernel_traffic(att_key)
+    traffic = None
+    if tr is not None and tr.get("workload") == args.workload:
+        traffic = tr["dram_bytes_per_launch"]
+    roof = {"bound": "hbm", "kernel": "kvq_decode_attn_packed (" + args.algo + ")", "achieved": phase_gbs["attention"],
+            "peak": peak, "unit": "GB/s", "frac": phase_gbs["attention"] / peak, "peak_source": peak_kind,
+            "frac_of_nominal_8tbs": phase_gbs["attention"] / NOMINAL_HBM_GBS, "traffic": traffic,
+            "algorithmic_bytes_per_launch": ab["attention"], "avg_launch_ms": att_ms,
+            "dominant_phase_of_step": dominant}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded, generated on the device)",
+            "config": {"workload": args.workload, "description": desc, "requests_per_gpu": B,
+                       "tokens_per_request": "ragged" if len(set(lengths)) > 1 else lengths[0], "kv_heads": H,
+                       "head_dim": D, "q_heads": Hq, "loops": depth, "attn_kernel": args.algo,
+                       "l2": "inputs larger than L2 (BF16 sources %.1f GB, packed %.2f GB per GPU), no flush"
+                             % (sum(2 * r.T * H * D * 2 * depth for r in reqs) / 1e9, pool.payload_bytes / 1e9),
+                       "arithmetic": "codec FP32 with BF16/FP16 rounding (bit-exact), attention FP32 accumulate",
+                       "parallelism": f"replicas x{world} (independent batches, no collective)"},
+            "phases": {"encode_gbs": phase_gbs["encode"], "reconstruct_gbs": phase_gbs["reconstruct"],
+                       "attention_gbs": phase_gbs["attention"], "encode_ms": enc_ms, "reconstruct_ms": rec_ms,
+                       "attention_ms": att_ms, "attention_pct_of_measured_hbm": 100 * phase_gbs["attention"] / peak,
+                       "attention_pct_of_8tbs": 100 * phase_gbs["attention"] / NOMINAL_HBM_GBS,
+                       "attended_tokens_per_s": ab["tokens"] / (att_ms * 1e-3),
+                       "encoded_tokens_per_s": ab["tokens"] / (enc_ms * 1e-3)},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clk,
+            "gpu_launches": launches,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, torch, kvq, reqs, q, out, step, stream, world, dev, step_bytes, dist):
+    """Same step through the public API with host inputs: H2D of every BF16
+    source and of q from pinned memory, the step, D2H of the attention output."""
+    host_x = []
+    for r in reqs:
+        for xs in (r.xk, r.xv):
+            for x in xs:
+                host_x.append((x, torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x)))
+    host_q = torch.empty(q.shape, dtype=q.dtype, pin_memory=True).copy_(q)
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(h.numel() * h.element_size() for _, h in host_x) + host_q.numel() * host_q.element_size()
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for d, h in host_x:
+            d.copy_(h, non_blocking=True)
+        q.copy_(host_q, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 10)
+    if world > 1:
+        dist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq):
+    """The CPU oracle as it stands, on the host cores, over a bounded sample of
+    the same requests; same metric and unit."""
+    cores = os.cpu_count() or 1
+    scale = 1.0 / math.sqrt(D)
+    t1 = oracle_sample(reqs[:1], q[:1], depth, scale, 1)
+    n = max(1, min(len(reqs), int(args.cpu_seconds * cores / max(t1, 1e-3))))
+    n = max(1, min(n, cores * 8))
+    sample = reqs[:n]
+    secs = oracle_sample(sample, q[:n], depth, scale, cores)
+    ab = algorithmic_bytes(sample, H, D, Hq, depth, lambda k, nn, s: kvq.payload_bytes(k, nn, H, D, s))
+    tot = ab["encode"] + ab["reconstruct"] + ab["attention"]
+    return {"value": tot / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {len(reqs)} requests of the same workload, whole path (encode K/V 4 loops, "
+                      f"reconstruct, FP32 attention), {secs:.1f} s on {cores} threads"}
+
+
+def run_reference(args, world, rank, cfg_idx, replicate, desc):
+    """--impl reference: the CPU oracle timed on the host cores, each step a
+    bounded sample of the same workload (rank 0 only under torchrun)."""
+    if world > 1 and rank != 0:
+        return
+    from quantized_cross_loop_gb300 import workloads as W
+
+    cores = os.cpu_count() or 1
+    spec = W.CONFIGS[cfg_idx]
+    n = min(cores, spec.n_requests * replicate)
+    if replicate > 1:
+        wl = W.make_workload(cfg_idx, device="cpu", replicate=math.ceil(n / spec.n_requests))
+    else:
+        wl = W.make_workload(cfg_idx, device="cpu", requests=list(range(n)))
+    reqs = wl.requests[:n]
+    q = wl.q[:n]
+    H, D, Hq, depth = wl.H, wl.D, wl.Hq, wl.depth
+    scale = 1.0 / math.sqrt(D)
+
+    def payload(kind, nn, sparse):
+        from oracle import oracle as O
+
+        return O.stream_bytes(kind, nn, H, D, sparse=sparse)
+
+    for _ in range(args.warmup):
+        oracle_sample(reqs[:1], q[:1], depth, scale, 1)
+    times = [oracle_sample(reqs, q, depth, scale, cores) for _ in range(args.steps)]
+    ab = algorithmic_bytes(reqs, H, D, Hq, depth, payload)
+    tot = ab["encode"] + ab["reconstruct"] + ab["attention"]
+    ms = 1e3 * sum(times) / len(times)
+    value = tot / (ms * 1e-3) / 1e9
+    sample = f"{n} requests of {args.workload} per step (whole path) on {cores} threads"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "description": desc, "oracle_requests_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    main()

@@ -151,19 +151,22 @@ kvq_status kvq_build_tile_dir(const int32_t* active_idx, int n_rows, int n_token
  */
 kvq_status kvq_reconstruct(const kvq_stream* loops, int depth, uint16_t* out, kvq_cuda_stream stream);
 
-/* Per-request reference to the packed K and V chains, read by the attention
- * kernel from DEVICE memory (an array of kvq_request, one per request). */
+/* Per-request reference to the packed K and V chains (one entry per loop),
+ * read by the attention kernel and by the batched codec calls from DEVICE
+ * memory (an array of kvq_request, one per request). The batched encode
+ * writes the planes (and, for a sparse loop, the tile_dir) of the loop it
+ * encodes; every other call only reads through these pointers. */
 typedef struct kvq_loop_ref {
   int32_t n_rows;
   int32_t reserved;
   const int32_t* active_idx; /* NULL: dense */
-  const int32_t* tile_dir;   /* required for sparse loops */
-  const uint8_t* k_codes;
-  const uint16_t* k_mins;
-  const uint16_t* k_scales;
-  const uint8_t* v_codes;
-  const uint16_t* v_mins;
-  const uint16_t* v_scales;
+  int32_t* tile_dir;         /* required for sparse loops */
+  uint8_t* k_codes;
+  uint16_t* k_mins;
+  uint16_t* k_scales;
+  uint8_t* v_codes;
+  uint16_t* v_mins;
+  uint16_t* v_scales;
 } kvq_loop_ref;
 
 typedef struct kvq_request {
@@ -175,6 +178,34 @@ typedef struct kvq_request {
 /* Host helper: fill one kvq_request from the K and V stream descriptors of a
  * request (n_loops of each). Checks that K and V agree on rows and sets. */
 kvq_status kvq_request_fill(const kvq_stream* k_loops, const kvq_stream* v_loops, int n_loops, kvq_request* out);
+
+/* Workspace bytes the batched codec calls need for n_requests requests. */
+size_t kvq_batch_workspace_bytes(int n_requests);
+
+/*
+ * Batched encode of loop `loop` (0 = the loop-1 base) of K or V (`kind`) for
+ * n_requests requests, same arithmetic as kvq_encode_base / kvq_encode_residual.
+ *   reqs  DEVICE table [n_requests]: loops 0..loop-1 are read as the
+ *         predecessor chain; loop `loop` gives the rows to store (dense, or
+ *         sparse with its active_idx) and the planes written. For a sparse
+ *         loop its tile_dir is written as well (both kinds write the same
+ *         values; K and V of one request share the active set).
+ *   x     DEVICE array [n_requests] of device pointers to BF16 [T_b][H][D]
+ *         sources of this loop.
+ *   workspace  >= kvq_batch_workspace_bytes(n_requests) bytes, 16-byte aligned.
+ * Table contents are preconditions (as for the single-request calls); an
+ * inconsistent sparse tile map sets bit 4 of the int32 error word at offset 0
+ * of the workspace.
+ */
+kvq_status kvq_encode_batch(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind, int loop,
+                            const uint16_t* const* x, void* workspace, size_t workspace_bytes,
+                            kvq_cuda_stream stream);
+
+/* Batched reconstruction at `depth` of K or V for n_requests requests into
+ * out[b] (DEVICE array of device pointers to BF16 [T_b][H][D]). */
+kvq_status kvq_reconstruct_batch(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind,
+                                 int depth, uint16_t* const* out, void* workspace, size_t workspace_bytes,
+                                 kvq_cuda_stream stream);
 
 /* Workspace bytes kvq_decode_attn_packed needs on the current device. */
 size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim);
@@ -215,6 +246,10 @@ const char* kvq_last_error(void);
 
 /* Library and format version: (major << 16) | minor. */
 uint32_t kvq_version(void);
+
+/* Number of CUDA kernels this library has launched in the calling process
+ * (host-side counter; for accounting launches in timed regions). */
+uint64_t kvq_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -1,6 +1,7 @@
 // kvq_api.cu — the extern "C" entry points of libkvq.so (declared in
 // include/kvq.h): host-side argument checks, then asynchronous launches on the
 // caller's stream. Nothing here allocates device memory or synchronises.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -114,6 +115,9 @@ constexpr int kMaxCtasPerSm = 8;
 }  // namespace
 
 namespace kvq {
+static std::atomic<unsigned long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 int attn_ctas(int algo, int device) {
   int sms = sm_count(device);
   if (sms <= 0) return 0;
@@ -126,6 +130,8 @@ int attn_ctas(int algo, int device) {
 extern "C" {
 
 uint32_t kvq_version(void) { return (1u << 16) | KVQ_FORMAT_VERSION; }
+
+uint64_t kvq_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* kvq_status_string(kvq_status s) {
   switch (s) {
@@ -181,6 +187,38 @@ int64_t kvq_stream_payload_bytes(int kind, int n_rows, int n_heads, int head_dim
   return H * n * (D / 2) + 2 * 2 * params + (sparse ? 4 * n : 0);
 }
 
+// Planes of a stream descriptor as one loop entry of a request.
+static void to_loop_ref(const kvq_stream* s, kvq_loop_ref* L) {
+  L->n_rows = s->n_rows;
+  L->active_idx = s->active_idx;
+  L->tile_dir = s->tile_dir;
+  if (s->kind == KVQ_K) {
+    L->k_codes = s->codes;
+    L->k_mins = s->mins;
+    L->k_scales = s->scales;
+  } else {
+    L->v_codes = s->codes;
+    L->v_mins = s->mins;
+    L->v_scales = s->scales;
+  }
+}
+
+static kvq_status current_sms(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+  *sms = sm_count(dev);
+  if (*sms <= 0) return fail(KVQ_ERR_CUDA, "cannot read the SM count of device %d", dev);
+  return KVQ_OK;
+}
+
+static kvq_status run_single(CodecArgs& a, int mode, cudaStream_t s, const char* what) {
+  int sms = 0;
+  kvq_status st = current_sms(&sms);
+  if (st != KVQ_OK) return st;
+  return cuda_status(launch_codec(a, mode, nullptr, sms, s), what);
+}
+
 kvq_status kvq_encode_base(const uint16_t* x, const kvq_stream* out, kvq_cuda_stream stream) {
   kvq_status st = check_planes(out, "out", false);
   if (st != KVQ_OK) return st;
@@ -188,60 +226,66 @@ kvq_status kvq_encode_base(const uint16_t* x, const kvq_stream* out, kvq_cuda_st
   if (out->n_rows == 0) return ok();
   if (x == nullptr) return fail(KVQ_ERR_BAD_ARG, "x is NULL");
   if (!aligned16(x)) return fail(KVQ_ERR_MISALIGNED, "x must be 16-byte aligned");
-  EncodeArgs a;
+  CodecArgs a;
   memset(&a, 0, sizeof a);
-  a.prev.depth = 0;
-  a.prev.kind = out->kind;
-  a.prev.n_tokens = out->n_tokens;
-  a.prev.n_heads = out->n_heads;
-  a.x = x;
-  a.n_rows = out->n_rows;
+  a.H = out->n_heads;
   a.kind = out->kind;
-  a.active = nullptr;
-  a.codes = out->codes;
-  a.mins = out->mins;
-  a.scales = out->scales;
-  return cuda_status(launch_encode(a, reinterpret_cast<cudaStream_t>(stream)), "encode_base launch");
+  a.loop = 0;
+  a.one.n_tokens = out->n_tokens;
+  a.one.n_loops = 1;
+  to_loop_ref(out, &a.one.loop[0]);
+  a.one_x = x;
+  return run_single(a, out->kind == KVQ_K ? kModeEncK : kModeEncV, reinterpret_cast<cudaStream_t>(stream),
+                    "encode_base launch");
 }
 
 kvq_status kvq_build_tile_dir(const int32_t* active_idx, int n_rows, int n_tokens, int32_t* tile_dir,
                               kvq_cuda_stream stream) {
   if (n_rows < 0 || n_tokens < 0 || n_rows > n_tokens)
     return fail(KVQ_ERR_BAD_ARG, "n_rows %d n_tokens %d", n_rows, n_tokens);
-  if (tile_dir == nullptr || (n_rows > 0 && active_idx == nullptr))
-    return fail(KVQ_ERR_BAD_ARG, "NULL active_idx or tile_dir");
-  return cuda_status(launch_tile_dir(active_idx, n_rows, n_tokens, tile_dir, reinterpret_cast<cudaStream_t>(stream)),
-                     "tile_dir launch");
+  if (tile_dir == nullptr || active_idx == nullptr) return fail(KVQ_ERR_BAD_ARG, "NULL active_idx or tile_dir");
+  CodecArgs a;
+  memset(&a, 0, sizeof a);
+  a.H = 1;
+  a.loop = 0;
+  a.one.n_tokens = n_tokens;
+  a.one.n_loops = 1;
+  a.one.loop[0].n_rows = n_rows;
+  a.one.loop[0].active_idx = active_idx;
+  a.one.loop[0].tile_dir = tile_dir;
+  return run_single(a, kModeTileDir, reinterpret_cast<cudaStream_t>(stream), "tile_dir launch");
 }
 
 kvq_status kvq_encode_residual(const uint16_t* x_r, const kvq_stream* prev, int n_prev, const kvq_stream* out,
                                kvq_cuda_stream stream) {
   if (n_prev < 1 || n_prev >= KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "n_prev %d", n_prev);
-  EncodeArgs a;
-  memset(&a, 0, sizeof a);
-  kvq_status st = build_chain(prev, n_prev, &a.prev, "prev");
+  Chain C;
+  kvq_status st = build_chain(prev, n_prev, &C, "prev");
   if (st != KVQ_OK) return st;
   st = check_planes(out, "out", false);
   if (st != KVQ_OK) return st;
   if (out->kind != prev[0].kind || out->n_tokens != prev[0].n_tokens || out->n_heads != prev[0].n_heads)
     return fail(KVQ_ERR_BAD_ARG, "out disagrees with prev on kind, n_tokens or n_heads");
+  if (out->active_idx != nullptr && out->tile_dir == nullptr)
+    return fail(KVQ_ERR_BAD_ARG, "out: sparse stream needs tile_dir storage");
+  if (out->n_rows > 0 && x_r == nullptr) return fail(KVQ_ERR_BAD_ARG, "x_r is NULL");
+  if (out->n_rows > 0 && !aligned16(x_r)) return fail(KVQ_ERR_MISALIGNED, "x_r must be 16-byte aligned");
+  CodecArgs a;
+  memset(&a, 0, sizeof a);
+  a.H = out->n_heads;
+  a.kind = out->kind;
+  a.loop = n_prev;
+  a.one.n_tokens = out->n_tokens;
+  a.one.n_loops = n_prev + 1;
+  for (int j = 0; j < n_prev; ++j) to_loop_ref(&prev[j], &a.one.loop[j]);
+  to_loop_ref(out, &a.one.loop[n_prev]);
+  a.one_x = x_r;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (out->active_idx != nullptr) {
-    if (out->tile_dir == nullptr) return fail(KVQ_ERR_BAD_ARG, "out: sparse stream needs tile_dir storage");
-    cudaError_t e = launch_tile_dir(out->active_idx, out->n_rows, out->n_tokens, out->tile_dir, s);
-    if (e != cudaSuccess) return cuda_status(e, "tile_dir launch");
+    st = run_single(a, kModeTileDir, s, "tile_dir launch");
+    if (st != KVQ_OK) return st;
   }
-  if (out->n_rows == 0) return ok();
-  if (x_r == nullptr) return fail(KVQ_ERR_BAD_ARG, "x_r is NULL");
-  if (!aligned16(x_r)) return fail(KVQ_ERR_MISALIGNED, "x_r must be 16-byte aligned");
-  a.x = x_r;
-  a.n_rows = out->n_rows;
-  a.kind = out->kind;
-  a.active = out->active_idx;
-  a.codes = out->codes;
-  a.mins = out->mins;
-  a.scales = out->scales;
-  return cuda_status(launch_encode(a, s), "encode_residual launch");
+  return run_single(a, out->kind == KVQ_K ? kModeEncK : kModeEncV, s, "encode_residual launch");
 }
 
 kvq_status kvq_reconstruct(const kvq_stream* loops, int depth, uint16_t* out, kvq_cuda_stream stream) {
@@ -251,7 +295,92 @@ kvq_status kvq_reconstruct(const kvq_stream* loops, int depth, uint16_t* out, kv
   if (C.n_tokens == 0) return ok();
   if (out == nullptr) return fail(KVQ_ERR_BAD_ARG, "out is NULL");
   if (!aligned16(out)) return fail(KVQ_ERR_MISALIGNED, "out must be 16-byte aligned");
-  return cuda_status(launch_reconstruct(C, out, reinterpret_cast<cudaStream_t>(stream)), "reconstruct launch");
+  CodecArgs a;
+  memset(&a, 0, sizeof a);
+  a.H = loops[0].n_heads;
+  a.kind = loops[0].kind;
+  a.loop = depth;
+  a.one.n_tokens = loops[0].n_tokens;
+  a.one.n_loops = depth;
+  for (int j = 0; j < depth; ++j) to_loop_ref(&loops[j], &a.one.loop[j]);
+  a.one_out = out;
+  return run_single(a, kModeRecon, reinterpret_cast<cudaStream_t>(stream), "reconstruct launch");
+}
+
+size_t kvq_batch_workspace_bytes(int n_requests) {
+  if (n_requests < 0) return 0;
+  return 16 + round16(size_t(n_requests + 1) * 4);
+}
+
+static kvq_status check_batch(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind,
+                              const void* ptrs, void* workspace, size_t workspace_bytes) {
+  if (n_requests < 0) return fail(KVQ_ERR_BAD_ARG, "n_requests %d", n_requests);
+  if (n_heads < 1 || n_heads > 1024) return fail(KVQ_ERR_BAD_ARG, "n_heads %d", n_heads);
+  if (head_dim != kD) return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d (kernels support 128)", head_dim);
+  if (kind != KVQ_K && kind != KVQ_V) return fail(KVQ_ERR_BAD_ARG, "kind %d", kind);
+  if (n_requests == 0) return KVQ_OK;
+  if (reqs == nullptr || ptrs == nullptr) return fail(KVQ_ERR_BAD_ARG, "NULL reqs or pointer array");
+  if (!aligned16(reqs)) return fail(KVQ_ERR_MISALIGNED, "reqs must be 16-byte aligned");
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < kvq_batch_workspace_bytes(n_requests))
+    return fail(KVQ_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", kvq_batch_workspace_bytes(n_requests));
+  return KVQ_OK;
+}
+
+kvq_status kvq_encode_batch(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind, int loop,
+                            const uint16_t* const* x, void* workspace, size_t workspace_bytes,
+                            kvq_cuda_stream stream) {
+  kvq_status st = check_batch(reqs, n_requests, n_heads, head_dim, kind, x, workspace, workspace_bytes);
+  if (st != KVQ_OK) return st;
+  if (loop < 0 || loop >= KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "loop %d", loop);
+  if (n_requests == 0) return ok();
+  int sms = 0;
+  st = current_sms(&sms);
+  if (st != KVQ_OK) return st;
+  CodecArgs a;
+  memset(&a, 0, sizeof a);
+  a.reqs = reqs;
+  a.x = x;
+  a.n_requests = n_requests;
+  a.H = n_heads;
+  a.kind = kind;
+  a.loop = loop;
+  char* ws = static_cast<char*>(workspace);
+  a.err = reinterpret_cast<int32_t*>(ws);
+  int32_t* prefix = reinterpret_cast<int32_t*>(ws + 16);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(a.err, 0, 16, s);
+  if (e != cudaSuccess) return cuda_status(e, "clear error word");
+  if (loop > 0) {
+    e = launch_codec(a, kModeTileDir, prefix, sms, s);
+    if (e != cudaSuccess) return cuda_status(e, "tile_dir launch");
+  }
+  return cuda_status(launch_codec(a, kind == KVQ_K ? kModeEncK : kModeEncV, prefix, sms, s), "encode launch");
+}
+
+kvq_status kvq_reconstruct_batch(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind,
+                                 int depth, uint16_t* const* out, void* workspace, size_t workspace_bytes,
+                                 kvq_cuda_stream stream) {
+  kvq_status st = check_batch(reqs, n_requests, n_heads, head_dim, kind, out, workspace, workspace_bytes);
+  if (st != KVQ_OK) return st;
+  if (depth < 1 || depth > KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "depth %d", depth);
+  if (n_requests == 0) return ok();
+  int sms = 0;
+  st = current_sms(&sms);
+  if (st != KVQ_OK) return st;
+  CodecArgs a;
+  memset(&a, 0, sizeof a);
+  a.reqs = reqs;
+  a.out = out;
+  a.n_requests = n_requests;
+  a.H = n_heads;
+  a.kind = kind;
+  a.loop = depth;
+  char* ws = static_cast<char*>(workspace);
+  a.err = reinterpret_cast<int32_t*>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(a.err, 0, 16, s);
+  if (e != cudaSuccess) return cuda_status(e, "clear error word");
+  return cuda_status(launch_codec(a, kModeRecon, reinterpret_cast<int32_t*>(ws + 16), sms, s), "reconstruct launch");
 }
 
 kvq_status kvq_request_fill(const kvq_stream* k_loops, const kvq_stream* v_loops, int n_loops, kvq_request* out) {

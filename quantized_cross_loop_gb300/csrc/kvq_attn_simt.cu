@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a) {
 
 cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream) {
   plan_kernel<<<1, 1024, 0, stream>>>(a);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(kD) combine_kernel(AttnArgs a) {
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
   combine_kernel<<<a.n_requests * a.H, kD, 0, stream>>>(a);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -310,6 +312,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
 
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream) {
   attn_simt_kernel<<<a.n_ctas, 256, 0, stream>>>(a);
+  count_launch();
   return cudaGetLastError();
 }
 

@@ -127,20 +127,31 @@ __device__ __forceinline__ float chain1(const Chain& C, int depth, const int* ro
   return v;
 }
 
-struct EncodeArgs {
-  Chain prev;             // loops 1..r-1 (prev.depth of them); depth 0 for the base
-  const uint16_t* x;      // BF16 [T][H][D] logical
-  int32_t n_rows;         // rows of the stream being written
+// Number of kernels this library has launched in the process (host counter).
+void count_launch();
+
+enum { kModeEncK = 0, kModeEncV = 1, kModeTileDir = 2, kModeRecon = 3 };
+
+// Arguments of the codec kernels: either a batch described by a device table of
+// requests, or one request carried by value in the kernel parameters.
+struct CodecArgs {
+  const kvq_request* reqs;   // device table [n_requests], or nullptr: use `one`
+  const uint16_t* const* x;  // batch encode: device array of BF16 [T_b][H][D] sources
+  uint16_t* const* out;      // batch reconstruct: device array of BF16 [T_b][H][D] outputs
+  int32_t* err;              // error word, or nullptr
+  int32_t n_requests;
+  int32_t H;
   int32_t kind;
-  const int32_t* active;  // NULL: dense
-  uint8_t* codes;
-  uint16_t* mins;
-  uint16_t* scales;
+  int32_t loop;              // encode and tile directory: loop written; reconstruct: depth
+  kvq_request one;
+  const uint16_t* one_x;
+  uint16_t* one_out;
+  int32_t one_prefix[2];
 };
 
-cudaError_t launch_encode(const EncodeArgs& a, cudaStream_t stream);
-cudaError_t launch_tile_dir(const int32_t* active, int n, int T, int32_t* dir, cudaStream_t stream);
-cudaError_t launch_reconstruct(const Chain& C, uint16_t* out, cudaStream_t stream);
+// Launches one codec stage (kMode*) for a batch or a single request; a batch
+// first plans its items into prefix_ws ([n_requests + 1] int32, device).
+cudaError_t launch_codec(const CodecArgs& a, int mode, int32_t* prefix_ws, int sms, cudaStream_t stream);
 
 // Quantise one value against its group's FP32 min and scale (scale 0: constant group).
 __device__ __forceinline__ int quantize(float x, float mn, float s32) {

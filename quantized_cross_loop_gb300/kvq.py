@@ -31,6 +31,7 @@ EXPORTED = (
     "kvq_stream_init", "kvq_plane_bytes", "kvq_stream_payload_bytes", "kvq_encode_base", "kvq_encode_residual",
     "kvq_build_tile_dir", "kvq_reconstruct", "kvq_request_fill", "kvq_decode_attn_workspace_bytes",
     "kvq_decode_attn_packed", "kvq_decode_attn_packed_ex", "kvq_status_string", "kvq_last_error", "kvq_version",
+    "kvq_batch_workspace_bytes", "kvq_encode_batch", "kvq_reconstruct_batch", "kvq_launch_count",
 )
 
 
@@ -114,9 +115,14 @@ def lib():
             L.kvq_status_string.restype = ctypes.c_char_p
             L.kvq_last_error.restype = ctypes.c_char_p
             L.kvq_version.restype = ctypes.c_uint32
+            L.kvq_launch_count.restype = ctypes.c_uint64
+            L.kvq_batch_workspace_bytes.argtypes = [i32]
+            L.kvq_batch_workspace_bytes.restype = sz
+            L.kvq_encode_batch.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, sz, vp]
+            L.kvq_reconstruct_batch.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, sz, vp]
             for name in ("kvq_stream_init", "kvq_encode_base", "kvq_encode_residual", "kvq_build_tile_dir",
                          "kvq_reconstruct", "kvq_request_fill", "kvq_decode_attn_packed",
-                         "kvq_decode_attn_packed_ex"):
+                         "kvq_decode_attn_packed_ex", "kvq_encode_batch", "kvq_reconstruct_batch"):
                 getattr(L, name).restype = ctypes.c_int32
             _lib = L
     return _lib
@@ -151,22 +157,26 @@ class Stream:
     the C descriptor pointing at them."""
 
     def __init__(self, kind: int, n_rows: int, n_tokens: int, n_heads: int, head_dim: int, device,
-                 active: torch.Tensor | None = None):
+                 active: torch.Tensor | None = None, alloc=None, shared_index=None):
         self.desc = kvq_stream()
         _check(lib().kvq_stream_init(ctypes.byref(self.desc), kind, n_rows, n_tokens, n_heads, head_dim),
                "kvq_stream_init")
         self.kind, self.n_rows, self.n_tokens, self.n_heads, self.head_dim = kind, n_rows, n_tokens, n_heads, head_dim
 
         def plane(p):
-            return torch.empty(int(lib().kvq_plane_bytes(ctypes.byref(self.desc), p)), dtype=torch.uint8,
-                               device=device)
+            nbytes = int(lib().kvq_plane_bytes(ctypes.byref(self.desc), p))
+            if alloc is not None:
+                return alloc(nbytes)
+            return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
         self.codes = plane(PLANE_CODES)
         self.mins = plane(PLANE_MINS)
         self.scales = plane(PLANE_SCALES)
         self.active = None
         self.tile_dir = None
-        if active is not None:
+        if shared_index is not None:  # K and V of one loop share the active set and its directory
+            self.active, self.tile_dir = shared_index
+        elif active is not None:
             buf = plane(PLANE_INDEX)
             buf.view(torch.int32)[:n_rows].copy_(active.to(device=device, dtype=torch.int32))
             self.active = buf
@@ -298,6 +308,101 @@ def kvq_decode_attn_packed(table: RequestTable, q: torch.Tensor, depth: int, n_h
                                            workspace.numel(), algo, _stream_handle(stream)),
            "kvq_decode_attn_packed")
     return out
+
+
+def plane_bytes(kind: int, n_rows: int, n_tokens: int, n_heads: int, head_dim: int) -> list:
+    d = kvq_stream()
+    _check(lib().kvq_stream_init(ctypes.byref(d), kind, n_rows, n_tokens, n_heads, head_dim), "kvq_stream_init")
+    return [int(lib().kvq_plane_bytes(ctypes.byref(d), p)) for p in range(5)]
+
+
+class PackedPool:
+    """Device storage for the packed K/V chains of a batch of requests: one
+    allocation, each request's planes contiguous and 256-byte aligned, located
+    through the device request table (kvq_request per request).
+
+    active_sets[b][r] is the sorted int32 active set of loop r of request b, or
+    None for a dense loop (loop 0 must be dense)."""
+
+    ALIGN = 256
+
+    def __init__(self, lengths: list, active_sets: list, n_heads: int, head_dim: int, n_loops: int, device):
+        device = torch.device(device)
+        self.lengths = list(lengths)
+        self.n_heads, self.head_dim, self.n_loops = n_heads, head_dim, n_loops
+        # pass 1: sizes
+        total = 0
+        sizes = []
+        for b, T in enumerate(self.lengths):
+            per = []
+            for r in range(n_loops):
+                act = active_sets[b][r]
+                n = T if act is None else int(act.numel())
+                k = plane_bytes(KVQ_K, n, T, n_heads, head_dim)
+                v = plane_bytes(KVQ_V, n, T, n_heads, head_dim)
+                per.append((n, k, v, act is not None))
+                total += sum(self._up(x) for x in k[:3]) + sum(self._up(x) for x in v[:3])
+                if act is not None:
+                    total += self._up(k[PLANE_INDEX]) + self._up(k[PLANE_TILE_DIR])
+            sizes.append(per)
+        self.storage = torch.empty(max(total, self.ALIGN), dtype=torch.uint8, device=device)
+        self.offset = 0
+        self.payload_bytes = 0
+        # pass 2: carve
+        self.k_streams, self.v_streams = [], []
+        for b, T in enumerate(self.lengths):
+            ks, vs = [], []
+            for r in range(n_loops):
+                n, kb, vb, sparse = sizes[b][r]
+                shared = None
+                if sparse:
+                    idx = self._take(kb[PLANE_INDEX])
+                    idx.view(torch.int32)[:n].copy_(active_sets[b][r].to(device=device, dtype=torch.int32))
+                    shared = (idx, self._take(kb[PLANE_TILE_DIR]))
+                ks.append(Stream(KVQ_K, n, T, n_heads, head_dim, device, alloc=self._take, shared_index=shared))
+                vs.append(Stream(KVQ_V, n, T, n_heads, head_dim, device, alloc=self._take, shared_index=shared))
+                self.payload_bytes += payload_bytes(KVQ_K, n, n_heads, head_dim, sparse)
+                self.payload_bytes += payload_bytes(KVQ_V, n, n_heads, head_dim, False)
+            self.k_streams.append(ks)
+            self.v_streams.append(vs)
+        self.table = RequestTable(self.k_streams, self.v_streams, device)
+        self.workspace = torch.empty(int(lib().kvq_batch_workspace_bytes(len(self.lengths))), dtype=torch.uint8,
+                                     device=device)
+
+    def _up(self, n):
+        return -(-n // self.ALIGN) * self.ALIGN
+
+    def _take(self, nbytes):
+        t = self.storage[self.offset:self.offset + nbytes]
+        self.offset += self._up(nbytes)
+        return t
+
+    @property
+    def n_requests(self):
+        return len(self.lengths)
+
+
+def pointer_array(tensors: list, device) -> torch.Tensor:
+    """Device int64 array of the tensors' data pointers (for the batched calls)."""
+    return torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=device)
+
+
+def kvq_encode_batch(pool: PackedPool, kind: int, loop: int, x_ptrs: torch.Tensor, stream=None):
+    """Encode loop `loop` (0 = base) of `kind` for every request of the pool;
+    x_ptrs: device int64 array of BF16 [T_b, H, D] source pointers."""
+    _check(lib().kvq_encode_batch(_dptr(pool.table.table), pool.n_requests, pool.n_heads, pool.head_dim, kind, loop,
+                                  _dptr(x_ptrs), _dptr(pool.workspace), pool.workspace.numel(),
+                                  _stream_handle(stream)), "kvq_encode_batch")
+
+
+def kvq_reconstruct_batch(pool: PackedPool, kind: int, depth: int, out_ptrs: torch.Tensor, stream=None):
+    _check(lib().kvq_reconstruct_batch(_dptr(pool.table.table), pool.n_requests, pool.n_heads, pool.head_dim, kind,
+                                       depth, _dptr(out_ptrs), _dptr(pool.workspace), pool.workspace.numel(),
+                                       _stream_handle(stream)), "kvq_reconstruct_batch")
+
+
+def launch_count() -> int:
+    return int(lib().kvq_launch_count())
 
 
 def attn_error_word(workspace: torch.Tensor) -> int:

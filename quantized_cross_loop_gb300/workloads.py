@@ -146,9 +146,9 @@ def make_request(spec: ConfigSpec, layer: int, b: int, device="cpu", T: int | No
                  sparse: bool | None = None) -> Request:
     """One request's K/V chains and active sets; reproducible per (config, layer, request)."""
     if T is None:
-        T = request_lengths(spec)[b]
+        T = spec.T if spec.ragged is None else request_lengths(spec)[b % spec.n_requests]
     if sparse is None:
-        sparse = request_is_sparse(spec)[b]
+        sparse = request_is_sparse(spec)[b % spec.n_requests]
     seed = (spec.seed + 1) * 1_000_003 + layer * 10_007 + b
     g = _gen(device, seed)
     gain = None

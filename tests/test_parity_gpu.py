@@ -163,3 +163,46 @@ def test_attention_error_word_for_bad_table():
         assert kvq.attn_error_word(ws) != 0
         o = out.cpu().numpy()
         assert np.all(np.isnan(o[1])) and not np.any(np.isnan(o[0]))
+
+
+def test_batch_api_matches_single_request_api():
+    """The batched encode and reconstruction (device request table, one pool of
+    contiguous per-request planes) give the same bytes as the per-request calls,
+    and the attention over the pool matches the oracle."""
+    spec = W.CONFIGS[2]
+    reqs = [W.make_request(spec, 0, b, "cpu") for b in range(3)]
+    reqs += [W.make_request(W.CONFIGS[1], 0, 0, "cpu")]
+    reqs += [W.make_request(spec, 0, 9, "cpu", T=1, sparse=True), W.make_request(spec, 0, 10, "cpu", T=0)]
+    dev = torch.device("cuda")
+    dreqs = [W.Request(r.T, [x.to(dev) for x in r.xk], [x.to(dev) for x in r.xv],
+                       [None if a is None else a.to(dev) for a in r.active]) for r in reqs]
+    pool = kvq.PackedPool([r.T for r in dreqs], [r.active for r in dreqs], 8, 128, 4, dev)
+    for j in range(4):
+        kvq.kvq_encode_batch(pool, kvq.KVQ_K, j, kvq.pointer_array([r.xk[j] for r in dreqs], dev))
+        kvq.kvq_encode_batch(pool, kvq.KVQ_V, j, kvq.pointer_array([r.xv[j] for r in dreqs], dev))
+    outs = {k: [torch.empty((max(r.T, 1), 8, 128), dtype=torch.bfloat16, device=dev) for r in dreqs] for k in (0, 1)}
+    for kind in (0, 1):
+        kvq.kvq_reconstruct_batch(pool, kind, 4, kvq.pointer_array(outs[kind], dev))
+    torch.cuda.synchronize()
+    assert kvq.attn_error_word(pool.workspace) == 0
+    for b, r in enumerate(dreqs):
+        if r.T == 0:
+            continue
+        k1, v1 = P.gpu_chains(r)
+        for j in range(4):
+            for got, want in ((pool.k_streams[b][j], k1[j]), (pool.v_streams[b][j], v1[j])):
+                assert torch.equal(got.codes_view(), want.codes_view())
+                assert torch.equal(got.mins_view(), want.mins_view())
+                assert torch.equal(got.scales_view(), want.scales_view())
+                if want.sparse:
+                    assert torch.equal(got.tile_dir_view(), want.tile_dir_view())
+        assert torch.equal(outs[0][b][:r.T], kvq.kvq_reconstruct(k1, 4))
+        assert torch.equal(outs[1][b][:r.T], kvq.kvq_reconstruct(v1, 4))
+    q = W.make_queries(spec, 0, len(dreqs)).to(dev)
+    live = [b for b in range(len(reqs)) if reqs[b].T > 0]
+    ref = P.oracle_many([reqs[b] for b in live], q[live].cpu(), 4, P.softmax_scale(128), THREADS)
+    for algo in _algos():
+        out = kvq.kvq_decode_attn_packed(pool.table, q, 4, 8, algo=algo).cpu().numpy()
+        assert np.all(out[[b for b in range(len(reqs)) if reqs[b].T == 0]] == 0)
+        for j, b in enumerate(live):
+            P.assert_attention_close(out[b], ref[j][4], f"pool req {b} algo {algo}")
