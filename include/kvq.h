@@ -238,6 +238,30 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
                                      int head_dim, int depth, const uint16_t* q, float softmax_scale, float* out,
                                      void* workspace, size_t workspace_bytes, int algo, kvq_cuda_stream stream);
 
+/* Bytes of the static device scratch used by kvq_decode_attn_packed_noalloc. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * Packed-KV decode attention that allocates nothing and takes no workspace.
+ * There is no counterpart on the pages: it serves callers that cannot
+ * allocate device memory (code running under CUDA graph capture, plugins in a
+ * serving process that owns all device allocations, hosts whose allocator the
+ * library cannot reach). Arguments, results and errors are those of
+ * kvq_decode_attn_packed; the scratch it needs lives in a file-scope device
+ * array of KVQ_NOALLOC_SCRATCH_BYTES (32 MiB), reserved on every device that
+ * loads it until the process exits.
+ *   - Sizes whose kvq_decode_attn_workspace_bytes() exceed 32 MiB are rejected
+ *     with KVQ_ERR_WORKSPACE before any launch (on a 152-SM GB300 that is about
+ *     6850 request x KV-head pairs per call).
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - Every call shares the array and leaves its contents behind; calls that
+ *     overlap on the GPU race on it and must be serialised by the caller.
+ */
+kvq_status kvq_decode_attn_packed_noalloc(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads,
+                                          int head_dim, int depth, const uint16_t* q, float softmax_scale,
+                                          float* out, kvq_cuda_stream stream);
+
 /* Human-readable name of a status code. */
 const char* kvq_status_string(kvq_status s);
 

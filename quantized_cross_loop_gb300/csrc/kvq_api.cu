@@ -115,6 +115,8 @@ constexpr int kMaxCtasPerSm = 8;
 }  // namespace
 
 namespace kvq {
+void set_error_message(const char* msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
+
 static std::atomic<unsigned long long> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 

@@ -32,6 +32,7 @@ EXPORTED = (
     "kvq_build_tile_dir", "kvq_reconstruct", "kvq_request_fill", "kvq_decode_attn_workspace_bytes",
     "kvq_decode_attn_packed", "kvq_decode_attn_packed_ex", "kvq_status_string", "kvq_last_error", "kvq_version",
     "kvq_batch_workspace_bytes", "kvq_encode_batch", "kvq_reconstruct_batch", "kvq_launch_count",
+    "kvq_decode_attn_packed_noalloc",
 )
 
 
@@ -403,6 +404,27 @@ def kvq_reconstruct_batch(pool: PackedPool, kind: int, depth: int, out_ptrs: tor
 
 def launch_count() -> int:
     return int(lib().kvq_launch_count())
+
+
+def kvq_decode_attn_packed_noalloc(table: RequestTable, q: torch.Tensor, depth: int, n_heads: int,
+                                   softmax_scale: float | None = None, out: torch.Tensor | None = None,
+                                   stream=None) -> torch.Tensor:
+    """Same result as kvq_decode_attn_packed, for callers that cannot allocate:
+    the library's static device scratch replaces the workspace. Calls that
+    overlap on the GPU share that scratch and must be serialised."""
+    _require_cuda(q, "q", torch.bfloat16)
+    B, Hq, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    f = lib().kvq_decode_attn_packed_noalloc
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int32
+    _check(f(_dptr(table.table), B, n_heads, Hq, D, depth, _dptr(q), ctypes.c_float(softmax_scale), _dptr(out),
+             _stream_handle(stream)), "kvq_decode_attn_packed_noalloc")
+    return out
 
 
 def attn_error_word(workspace: torch.Tensor) -> int:
