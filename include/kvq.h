@@ -210,9 +210,9 @@ kvq_status kvq_reconstruct_batch(const kvq_request* reqs, int n_requests, int n_
 /* Workspace bytes kvq_decode_attn_packed needs on the current device. */
 size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim);
 
-#define KVQ_ATTN_AUTO 0 /* the fastest kernel for the shape (tensor-core MMA) */
+#define KVQ_ATTN_AUTO 0 /* tensor-core kernel for depth <= 4, CUDA-core kernel beyond */
 #define KVQ_ATTN_SIMT 1 /* CUDA-core kernel: exact BF16 chain per element, FP32 dot products */
-#define KVQ_ATTN_MMA 2  /* tensor-core kernel: unpack + folded dequant into m16n8k16 MMAs */
+#define KVQ_ATTN_MMA 2  /* tensor-core kernel (depth <= 4): unpack + folded dequant into m16n8k16 MMAs */
 
 /*
  * Packed-KV GQA decode attention at `depth` (RFC §3.2: historical K/V are read

@@ -40,6 +40,9 @@
  *     each chain addition rounds to BF16: RN_bf16(RN32(X̂ + deq));
  *   - residual: δ = RN_bf16(RN32(X_r − X̂_{r−1})) at the stored rows;
  *   - GQA head mapping kv_head = q_head / (Hq / H);
+ *   - the attention reference decodes the packed chain in FP32 (decode and
+ *     chain sums rounded to FP32 only) before FP32 attention: the direct
+ *     packed reader's values; the BF16 reconstruction is a separate output;
  *   - plane layout (head-major): codes u8[H][n][D/2]; K params f16[H][⌈n/G⌉][D];
  *     V params f16[H][n][⌈D/G⌉]; sparse index int32[n] ascending.
  */
@@ -396,7 +399,55 @@ int orc_reconstruct(int kind, int T, int H, int D, int G, int depth, const orc_s
 }
 
 /* ------------------------------------------------------------------------ */
-/* Decode attention in FP32 on reconstructed K̂, V̂ (RFC §3.2, §5).             */
+/* FP32 decode of the packed chain: the values a direct packed reader sees.  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Same chain as orc_reconstruct, evaluated in FP32 without BF16 rounding:
+ * decode = RN32(f32(min16) + RN32(f32(scale16) * c)) and each present loop is
+ * added with one FP32 rounding; absent tokens inherit. This is the reference
+ * of the attention reader, which consumes the packed planes directly (RFC §3.3)
+ * and is compared in FP32 on the same packed data; its distance to the BF16
+ * reconstruction is the direct-reader error that RFC §9 asks to bound.
+ * out: FP32 [T][H][D].
+ */
+int orc_decode_f32(int kind, int T, int H, int D, int G, int depth, const orc_stream* loops, float* out) {
+  if (T < 0 || H <= 0 || D <= 0 || (D & 1) || G <= 0 || depth < 1) return ORC_EINVAL;
+  if (loops[0].active != NULL || loops[0].n != T) return ORC_EINVAL;
+  for (int j = 1; j < depth; ++j) {
+    if (loops[j].active == NULL) {
+      if (loops[j].n != T) return ORC_EINVAL;
+    } else if (loops[j].n < 0 || loops[j].n > T || !check_active(loops[j].active, loops[j].n, T)) {
+      return ORC_EINVAL;
+    }
+  }
+  int32_t* rowmap = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+  if (!rowmap) return ORC_ENOMEM;
+  for (int j = 0; j < depth; ++j) {
+    const orc_stream* s = &loops[j];
+    for (int t = 0; t < T; ++t) rowmap[t] = -1;
+    for (int i = 0; i < s->n; ++i) rowmap[s->active ? s->active[i] : i] = i;
+    for (int t = 0; t < T; ++t) {
+      int row = rowmap[t];
+      if (row < 0) continue;
+      for (int h = 0; h < H; ++h)
+        for (int d = 0; d < D; ++d) {
+          int64_t pi = param_index(kind, s->n, D, G, h, row, d);
+          float m = orc_f16_to_f32(s->mins[pi]);
+          float sc = orc_f16_to_f32(s->scales[pi]);
+          float prod = sc * (float)get_code(s->codes, s->n, D, h, row, d);
+          float dq = m + prod;
+          int64_t li = ((int64_t)t * H + h) * D + d;
+          out[li] = (j == 0) ? dq : out[li] + dq;
+        }
+    }
+  }
+  free(rowmap);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention in FP32 (RFC §3.2, §5).                                   */
 /* ------------------------------------------------------------------------ */
 
 /*
@@ -406,8 +457,8 @@ int orc_reconstruct(int kind, int T, int H, int D, int G, int depth, const orc_s
  * s_t = (sum_d q_d k_td, in channel order) * scale; p_t = exp(s_t - max s);
  * o_d = (sum_t p_t v_td, in token order) / (sum_t p_t).
  */
-int orc_attention(int T, int H, int Hq, int D, const uint16_t* q, const uint16_t* khat, const uint16_t* vhat,
-                  float scale, float* out) {
+static int attention_core(int T, int H, int Hq, int D, const uint16_t* q, const float* kf, const float* vf,
+                          float scale, float* out) {
   if (T <= 0 || H <= 0 || Hq <= 0 || D <= 0 || Hq % H != 0) return ORC_EINVAL;
   int g = Hq / H;
   float* s = (float*)malloc(sizeof(float) * (size_t)T);
@@ -423,7 +474,7 @@ int orc_attention(int T, int H, int Hq, int D, const uint16_t* q, const uint16_t
     for (int t = 0; t < T; ++t) {
       float dot = 0.0f;
       for (int d = 0; d < D; ++d) {
-        float prod = orc_bf16_to_f32(q[(int64_t)hq * D + d]) * orc_bf16_to_f32(khat[((int64_t)t * H + h) * D + d]);
+        float prod = orc_bf16_to_f32(q[(int64_t)hq * D + d]) * kf[((int64_t)t * H + h) * D + d];
         dot = dot + prod;
       }
       s[t] = dot * scale;
@@ -435,7 +486,7 @@ int orc_attention(int T, int H, int Hq, int D, const uint16_t* q, const uint16_t
       float p = expf(s[t] - mx);
       L = L + p;
       for (int d = 0; d < D; ++d) {
-        float prod = p * orc_bf16_to_f32(vhat[((int64_t)t * H + h) * D + d]);
+        float prod = p * vf[((int64_t)t * H + h) * D + d];
         acc[d] = acc[d] + prod;
       }
     }
@@ -444,4 +495,38 @@ int orc_attention(int T, int H, int Hq, int D, const uint16_t* q, const uint16_t
   free(s);
   free(acc);
   return ORC_OK;
+}
+
+/*
+ * q: BF16 bits [Hq][D]; khat, vhat: BF16 bits [T][H][D]; out: FP32 [Hq][D].
+ * One query token attends to all T stored tokens (no mask: in decode the
+ * query follows every stored position). kv_head = q_head / (Hq / H).
+ * s_t = (sum_d q_d k_td, in channel order) * scale; p_t = exp(s_t - max s);
+ * o_d = (sum_t p_t v_td, in token order) / (sum_t p_t).
+ */
+int orc_attention(int T, int H, int Hq, int D, const uint16_t* q, const uint16_t* khat, const uint16_t* vhat,
+                  float scale, float* out) {
+  if (T <= 0 || H <= 0 || D <= 0) return ORC_EINVAL;
+  size_t n = (size_t)T * H * D;
+  float* kf = (float*)malloc(sizeof(float) * n);
+  float* vf = (float*)malloc(sizeof(float) * n);
+  if (!kf || !vf) {
+    free(kf);
+    free(vf);
+    return ORC_ENOMEM;
+  }
+  for (size_t i = 0; i < n; ++i) {
+    kf[i] = orc_bf16_to_f32(khat[i]);
+    vf[i] = orc_bf16_to_f32(vhat[i]);
+  }
+  int rc = attention_core(T, H, Hq, D, q, kf, vf, scale, out);
+  free(kf);
+  free(vf);
+  return rc;
+}
+
+/* Same attention on FP32 K and V (the FP32 decode of the packed chain). */
+int orc_attention_f32(int T, int H, int Hq, int D, const uint16_t* q, const float* kf, const float* vf, float scale,
+                      float* out) {
+  return attention_core(T, H, Hq, D, q, kf, vf, scale, out);
 }

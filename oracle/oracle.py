@@ -70,6 +70,10 @@ def lib():
             L.orc_reconstruct.restype = i32
             L.orc_attention.argtypes = [i32, i32, i32, i32, vp, vp, vp, ctypes.c_float, vp]
             L.orc_attention.restype = i32
+            L.orc_attention_f32.argtypes = [i32, i32, i32, i32, vp, vp, vp, ctypes.c_float, vp]
+            L.orc_attention_f32.restype = i32
+            L.orc_decode_f32.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(_Stream), vp]
+            L.orc_decode_f32.restype = i32
             L.orc_stream_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
             L.orc_stream_bytes.restype = i64
             for name in ("orc_f32_to_f16_n", "orc_f32_to_bf16_n", "orc_f16_to_f32_n"):
@@ -207,13 +211,43 @@ def stream_bytes(kind: int, n: int, H: int, D: int, G: int = GROUP, sparse: bool
     return int(lib().orc_stream_bytes(kind, n, H, D, G, int(sparse)))
 
 
+def decode_f32(streams: list[Stream], depth: int, G: int = GROUP) -> np.ndarray:
+    """FP32 [T, H, D] decode of the chain at `depth` with no BF16 rounding: the
+    values a direct packed reader computes with (see orc_decode_f32)."""
+    s0 = streams[0]
+    arr = (_Stream * depth)(*[s.c_struct() for s in streams[:depth]])
+    out = np.empty((s0.T, s0.H, s0.D), dtype=np.float32)
+    rc = lib().orc_decode_f32(s0.kind, s0.T, s0.H, s0.D, G, depth, arr, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"orc_decode_f32 failed with status {rc}")
+    return out
+
+
+def attention_f32(q: np.ndarray, kf: np.ndarray, vf: np.ndarray, scale: float) -> np.ndarray:
+    """FP32 decode attention of q [Hq, D] (BF16 bits) over FP32 K, V [T, H, D]."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    kf = np.ascontiguousarray(kf, dtype=np.float32)
+    vf = np.ascontiguousarray(vf, dtype=np.float32)
+    Hq, D = q.shape
+    T, H, D2 = kf.shape
+    assert D2 == D and vf.shape == kf.shape
+    out = np.empty((Hq, D), dtype=np.float32)
+    rc = lib().orc_attention_f32(T, H, Hq, D, _ptr(q), _ptr(kf), _ptr(vf), ctypes.c_float(scale), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"orc_attention_f32 failed with status {rc}")
+    return out
+
+
 def request_path(xk: list[np.ndarray], xv: list[np.ndarray], actives: list[np.ndarray | None], q: np.ndarray,
                  depth: int, scale: float):
     """The whole path for one request: encode both chains, reconstruct to
-    `depth`, attend. Returns (k_streams, v_streams, khat, vhat, out)."""
+    `depth` in BF16, and attend. Returns (k_streams, v_streams, khat, vhat,
+    out) where `out` is the FP32 attention on the FP32 decode of the packed
+    chains (the reference of the direct packed reader); the attention on the
+    BF16 reconstruction is attention(q, khat, vhat, scale)."""
     ks = encode_chain(KIND_K, xk, actives)
     vs = encode_chain(KIND_V, xv, actives)
     khat = reconstruct(ks, depth)
     vhat = reconstruct(vs, depth)
-    out = attention(q, khat, vhat, scale)
+    out = attention_f32(q, decode_f32(ks, depth), decode_f32(vs, depth), scale)
     return ks, vs, khat, vhat, out

@@ -123,7 +123,7 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 int attn_ctas(int algo, int device) {
   int sms = sm_count(device);
   if (sms <= 0) return 0;
-  int per_sm = (algo == KVQ_ATTN_SIMT) ? 4 : 2;
+  int per_sm = (algo == KVQ_ATTN_SIMT) ? 4 : 1;
   if (per_sm > kMaxCtasPerSm) per_sm = kMaxCtasPerSm;
   return sms * per_sm;
 }
@@ -454,8 +454,9 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   const size_t need = ws_bytes(n_requests, n_heads, sms * kMaxCtasPerSm);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
     return fail(KVQ_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", need);
-  if (algo == KVQ_ATTN_AUTO) algo = KVQ_ATTN_SIMT;
-  if (algo == KVQ_ATTN_MMA) return fail(KVQ_ERR_UNSUPPORTED, "MMA kernel not built");
+  if (algo == KVQ_ATTN_AUTO) algo = depth <= kMmaMaxDepth ? KVQ_ATTN_MMA : KVQ_ATTN_SIMT;
+  if (algo == KVQ_ATTN_MMA && depth > kMmaMaxDepth)
+    return fail(KVQ_ERR_UNSUPPORTED, "the tensor-core kernel reads depth <= %d (got %d)", kMmaMaxDepth, depth);
 
   AttnArgs a;
   memset(&a, 0, sizeof a);

@@ -16,6 +16,7 @@
 namespace kvq {
 
 constexpr int kMaxG = 8;                          // query heads per KV head
+constexpr int kMmaMaxDepth = 4;                   // loops the tensor-core kernel stages per tile
 constexpr int kSlotFloats = kMaxG * (kD + 2);     // m[8], l[8], acc[8][128]
 
 struct AttnArgs {

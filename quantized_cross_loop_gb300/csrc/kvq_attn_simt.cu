@@ -6,10 +6,10 @@
 // §5: FP32 mass and accumulation; §3.3: readers consume the packed base and
 // residual tiles directly (no BF16 shadow cache in HBM).
 //
-// The CUDA-core kernel rebuilds each 64-token tile of K̂ and V̂ in shared memory
-// with the exact BF16 chain (bit-identical to the reconstruction), then runs
-// FP32 dot products, an online softmax and the PV sum. It is the reference
-// design the tensor-core kernel is measured against.
+// The CUDA-core kernel decodes each 64-token tile of K and V into shared memory
+// with the FP32 chain (dequantised values summed in FP32, the values a direct
+// packed reader works with), then runs FP32 dot products, an online softmax
+// and the PV sum. It is the design the tensor-core kernel is measured against.
 #include "kvq_attn_common.cuh"
 
 namespace kvq {
@@ -131,8 +131,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct SimtSmem {
   float q[kMaxG][kD];
-  uint16_t khat[KVQ_TILE][kD];
-  uint16_t vhat[KVQ_TILE][kD];
+  float khat[KVQ_TILE][kD];
+  float vhat[KVQ_TILE][kD];
   float p[KVQ_TILE][kMaxG];
   int map[KVQ_MAX_LOOPS][KVQ_TILE];
   float m[kMaxG];
@@ -196,7 +196,8 @@ __device__ void simt_finish_unit(const AttnArgs& a, SimtSmem& S, float* acc, int
 }
 
 __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
-  __shared__ SimtSmem S;
+  extern __shared__ __align__(16) uint8_t simt_smem[];
+  SimtSmem& S = *reinterpret_cast<SimtSmem*>(simt_smem);
   const int tid = threadIdx.x;
   const int C = a.n_ctas;
   const long long W = a.prefix[a.n_requests];
@@ -258,12 +259,12 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
           int rows[KVQ_MAX_LOOPS];
           for (int j = 0; j < a.depth; ++j) rows[j] = S.map[j][tt];
           float kv[4], vv[4];
-          chain4(S.ck, a.depth, rows, h, c0, kv);
-          chain4(S.cv, a.depth, rows, h, c0, vv);
+          chain4_f32(S.ck, a.depth, rows, h, c0, kv);
+          chain4_f32(S.cv, a.depth, rows, h, c0, vv);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            S.khat[tt][c0 + e] = f32_to_bf16_bits(kv[e]);
-            S.vhat[tt][c0 + e] = f32_to_bf16_bits(vv[e]);
+            S.khat[tt][c0 + e] = kv[e];
+            S.vhat[tt][c0 + e] = vv[e];
           }
         }
       }
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
         float sacc = -INFINITY;
         if (tt < nvalid) {
           sacc = 0.0f;
-          for (int d = 0; d < kD; ++d) sacc = fmaf(S.q[i][d], bf16_bits_to_f32(S.khat[tt][d]), sacc);
+          for (int d = 0; d < kD; ++d) sacc = fmaf(S.q[i][d], S.khat[tt][d], sacc);
         }
         S.p[tt][i] = sacc;
       }
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
         for (int kk = tid; kk < g * kD; kk += blockDim.x, ++n) {
           int i = kk / kD, d = kk % kD;
           float s = acc[n] * S.alpha[i];
-          for (int tt = 0; tt < nvalid; ++tt) s = fmaf(S.p[tt][i], bf16_bits_to_f32(S.vhat[tt][d]), s);
+          for (int tt = 0; tt < nvalid; ++tt) s = fmaf(S.p[tt][i], S.vhat[tt][d], s);
           acc[n] = s;
         }
       }
@@ -311,7 +312,14 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
 }
 
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream) {
-  attn_simt_kernel<<<a.n_ctas, 256, 0, stream>>>(a);
+  const int smem = int(sizeof(SimtSmem));
+  static int configured = 0;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = 1;
+  }
+  attn_simt_kernel<<<a.n_ctas, 256, smem, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }

@@ -104,6 +104,26 @@ __device__ __forceinline__ void chain4(const Chain& C, int depth, const int* row
   }
 }
 
+// The same chain in FP32: decode = RN32(min16 + RN32(scale16 * c)), loops
+// summed with FP32 rounding only (the values a direct packed reader uses).
+__device__ __forceinline__ void chain4_f32(const Chain& C, int depth, const int* rows, int h, int c0, float out[4]) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) out[e] = 0.0f;
+  for (int j = 0; j < depth; ++j) {
+    int row = rows[j];
+    if (row < 0) continue;
+    const LoopPlanes& L = C.loop[j];
+    uint16_t two = *reinterpret_cast<const uint16_t*>(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + c0 / 2);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int c = (two >> (4 * e)) & 0xF;
+      long long pi = param_index(C.kind, L.n_rows, h, row, c0 + e);
+      float dq = __fadd_rn(f16_bits_to_f32(__ldg(L.mins + pi)), __fmul_rn(f16_bits_to_f32(__ldg(L.scales + pi)), float(c)));
+      out[e] = (j == 0) ? dq : __fadd_rn(out[e], dq);
+    }
+  }
+}
+
 // Same for one channel d.
 __device__ __forceinline__ float chain1(const Chain& C, int depth, const int* rows, int h, int d) {
   float v;

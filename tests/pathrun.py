@@ -88,5 +88,20 @@ def assert_attention_close(out_gpu, out_ref, what=""):
     return float(err.max()), float((err / np.maximum(np.abs(b), 1e-30)).max())
 
 
+# The attention of the direct packed reader against the attention on the BF16
+# reconstruction: their distance is the direct-reader error (FlashLoop RFC §9
+# asks it to be bounded). Measured up to ~4e-3 on the synthetic configurations;
+# the bound below leaves a margin and catches any structural mistake.
+READER_ATOL = 2e-2
+READER_RTOL = 5e-2
+
+
+def assert_reader_error_bounded(out_gpu, khat, vhat, q_bits, scale, what=""):
+    ref = O.attention(q_bits, khat, vhat, scale).astype(np.float64)
+    err = np.abs(np.asarray(out_gpu, dtype=np.float64) - ref)
+    assert np.all(err <= READER_ATOL + READER_RTOL * np.abs(ref)), f"direct-reader error {err.max():.3e} {what}"
+    return float(err.max())
+
+
 def softmax_scale(D):
     return 1.0 / math.sqrt(D)

@@ -452,3 +452,59 @@ def test_attention_special_cases():
     mean = f32(v).astype(np.float64).mean(axis=0)  # equal logits: the plain mean
     for hq in range(Hq):
         assert np.max(np.abs(out[hq] - mean[hq // 4])) < 1e-6
+
+
+# ---------------------------------------------------------------- FP32 decode of the packed chain
+
+
+def test_decode_f32_depth1_is_the_affine_decode():
+    """FlashLoop RFC §3.3: decoding is min + scale * code. At depth 1 the FP32
+    decode is that value rounded once to FP32, and its BF16 rounding is the
+    BF16 reconstruction bit for bit."""
+    rng = np.random.default_rng(21)
+    x = bf16(rng.standard_normal((70, 2, 128)) * 3)
+    for kind in (O.KIND_K, O.KIND_V):
+        s = O.encode(kind, x)
+        f = O.decode_f32([s], 1)
+        assert np.array_equal(O.f32_to_bf16_bits(f), O.reconstruct([s], 1))
+        c = unpack(s.codes)
+        for (t, h, d) in [(0, 0, 0), (5, 1, 77), (69, 0, 127), (64, 1, 63), (33, 0, 64)]:
+            p = (h, t // 64, d) if kind == O.KIND_K else (h, t, d // 64)
+            exact = Fraction(float(f16_to_f32(s.mins[p]))) + Fraction(float(f16_to_f32(s.scales[p]))) * int(c[t, h, d])
+            assert float(f[t, h, d]) == float(np.float32(float(exact)))
+
+
+def test_decode_f32_inherits_absent_tokens_and_tracks_the_bf16_chain():
+    gold = json.load(open(os.path.join(GOLD, "loop4_read_example.json")))
+    act = {int(r): np.array(v, dtype=np.int32) - 1 for r, v in gold["active_1based"].items()}
+    xs = _offset_chain(gold["T"], 2, 128, 6)
+    for kind in (O.KIND_K, O.KIND_V):
+        ks = O.encode_chain(kind, xs, [None, None, act[3], act[4]])
+        f = {d: O.decode_f32(ks, d) for d in range(1, 5)}
+        for tok1, loops in gold["loop4_read_1based"].items():
+            t = int(tok1) - 1
+            for d in range(2, 5):
+                assert (not np.array_equal(f[d][t], f[d - 1][t])) == (d in loops)
+        # the FP32 chain and the BF16 chain differ only by the 2*depth-1 BF16 roundings
+        for d in range(1, 5):
+            bf = f32(O.reconstruct(ks, d)).astype(np.float64)
+            mag = np.maximum(np.abs(bf), np.abs(f[d].astype(np.float64)))
+            assert np.all(np.abs(bf - f[d]) <= (2 * d - 1) * 2.0 ** -8 * (mag + 4.0))
+
+
+def test_attention_f32_matches_float64_sdpa_on_decoded_chain():
+    rng = np.random.default_rng(4)
+    T, H, Hq, D = 333, 4, 16, 128
+    xs = [bf16(rng.standard_normal((T, H, D)) * (0.1 if r else 1.0)) for r in range(4)]
+    xs = [bf16(sum(f32(xs[i]) for i in range(r + 1))) for r in range(4)]
+    ks = O.encode_chain(O.KIND_K, xs, [None] * 4)
+    vs = O.encode_chain(O.KIND_V, xs, [None] * 4)
+    kf, vf = O.decode_f32(ks, 4), O.decode_f32(vs, 4)
+    q = bf16(rng.standard_normal((Hq, D)))
+    out = O.attention_f32(q, kf, vf, 1 / math.sqrt(D))
+    g = Hq // H
+    qt = torch.from_numpy(f32(q).astype(np.float64)).reshape(1, Hq, 1, D)
+    kt = torch.from_numpy(kf.astype(np.float64)).permute(1, 0, 2).repeat_interleave(g, 0).unsqueeze(0)
+    vt = torch.from_numpy(vf.astype(np.float64)).permute(1, 0, 2).repeat_interleave(g, 0).unsqueeze(0)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=1 / math.sqrt(D)).reshape(Hq, D)
+    assert np.max(np.abs(out - ref.numpy())) < 2e-5
