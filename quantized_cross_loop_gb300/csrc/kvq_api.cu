@@ -123,7 +123,8 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 int attn_ctas(int algo, int device) {
   int sms = sm_count(device);
   if (sms <= 0) return 0;
-  int per_sm = (algo == KVQ_ATTN_SIMT) ? 4 : 1;
+  // the tensor-core kernel runs two independent groups (virtual CTAs) per block
+  int per_sm = (algo == KVQ_ATTN_SIMT) ? 4 : 2;
   if (per_sm > kMaxCtasPerSm) per_sm = kMaxCtasPerSm;
   return sms * per_sm;
 }

@@ -7,27 +7,33 @@
 // accumulation. The dequantiser is the affine INT4 group code of §3.3
 // (decode = min + scale * code).
 //
-// Design (ours). One CTA per SM runs over a contiguous range of 64-token tiles
-// of the flat (request, KV head, tile) work list (kvq_attn_common.cuh).
-//   producer warp   one lane issues 1-D bulk TMA copies (cp.async.bulk with
-//                   mbarrier transaction counts) of each tile's packed planes —
-//                   per loop: K and V codes, K and V min/scale planes, and for
-//                   a sparse loop its index slice — into one of kStages stages.
-//   8 consumer warps fold the dequantisation into the contractions, since min
-//                   and scale are constant along each contraction:
+// Design (ours). Each CTA holds two independent groups; a group is a virtual
+// CTA of the flat (request, KV head, 64-token tile) work list of
+// kvq_attn_common.cuh and owns a contiguous tile range.
+//   producer warp   (one per group) one lane issues 1-D bulk TMA copies
+//                   (cp.async.bulk with mbarrier transaction counts) of each
+//                   tile's packed planes — per loop: K and V codes, K and V
+//                   min/scale planes, and for a sparse loop its index slice —
+//                   into the group's two stages.
+//   4 consumer warps a warp owns 16 logical tokens of the tile through QK^T,
+//                   softmax and PV; the dequantisation is folded into the
+//                   contractions, since min and scale are constant along each:
 //       S[t, h]  = sum_j [ sum_d c_j[t,d] * (q[h,d] * sK_j[d]) + sum_d q[h,d] * mK_j[d] ]
 //       O[h, d]  = sum_j [ sum_t c_j[t,d] * (p[t,h] * sV_j[t]) + sum_t p[t,h] * mV_j[t] ]
-//                   Codes are unpacked to exact FP16 integers in registers and
-//                   fed to mma.sync m16n8k16 (FP32 accumulate). q (BF16) is
-//                   exact in FP16; q*sK is carried exactly as the sum of two
-//                   FP16 terms (hi = RN16(q*sK), lo = RN16(q*sK - hi)), so the
-//                   logits are exact up to FP32 accumulation. QK^T runs with
-//                   tokens as M and the 8 query heads of a KV head as N, PV
-//                   with channels as M. Sparse loops are processed over their
-//                   compact rows only; their logits are gathered back to
-//                   logical tokens through a 64-bit presence mask per tile.
-//                   The K min terms of all (loop, group) pairs come from one
-//                   small MMA; the V min terms are FP32 sums.
+//                   Codes enter mma.sync m16n8k16 (FP32 accumulate) as the FP16
+//                   values 64 + c, made by OR-ing the nibble into the mantissa
+//                   of 64.0; the offset is removed exactly: -64 * sum_d q*sK
+//                   rides in the K-min MMA, -64 * sum_t p*sV is added in FP32.
+//                   q (BF16) is exact in FP16; q*sK is carried exactly as the
+//                   sum of two FP16 terms (hi = RN16(q*sK), lo = RN16(q*sK - hi)),
+//                   so logits are exact up to FP32 accumulation. QK^T runs with
+//                   tokens as M and the 8 query heads of a KV head as N; the
+//                   softmax stays in the accumulator registers; p * sV becomes
+//                   the PV B operand through movmatrix.trans; PV runs with
+//                   channels as M. A sparse loop contributes over its compact
+//                   rows only; rows and tokens are matched through a 64-bit
+//                   presence mask of the tile and warp shuffles.
+// Per tile and group: two named barriers (K-min terms ready; max exchange).
 // Softmax is online over tiles in the log2 domain, FP32 throughout.
 #include <cuda_fp16.h>
 
@@ -36,36 +42,24 @@
 namespace kvq {
 namespace mma_attn {
 
-constexpr int kLoops = 4;            // depth handled by this kernel
-constexpr int kStages = 3;
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + producer warp
-constexpr int kMaxPairs = 2 * kLoops;       // (loop, K group) pairs of one tile
+constexpr int kLoops = 4;  // most loops staged per tile
+constexpr int kGroups = 2;
+constexpr int kGroupWarps = 4;
+constexpr int kGroupThreads = kGroupWarps * 32;
+constexpr int kStagesPerGroup = 2;
+constexpr int kStages = kGroups * kStagesPerGroup;
+constexpr int kConsumers = kGroups * kGroupThreads;
+constexpr int kThreads = kConsumers + kGroups * 32;  // + one producer warp per group
+constexpr int kMaxPairs = 2 * kLoops;                // (loop, K group) pairs of one tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitNs = 2000000000LL;  // bounded waits: 2 s, then flag and leave
+constexpr uint32_t kMagic = 0x54005400u;     // FP16 64.0 in both halves
 
-// Per-loop description of a staged tile.
-struct LoopMeta {
-  int32_t nrows;   // stored rows in this tile (logical rows for dense, compact rows for sparse)
-  int32_t c0;      // first stored row (stream row index)
-  int32_t g0;      // K group of row c0
-  int32_t ngrp;    // K groups spanned (1 or 2; 0 if no rows)
-  int32_t vrem;    // half offset of the first V param inside the staged V param chunk
-  int32_t irem;    // int offset of the first index inside the staged index chunk
-  int32_t sparse;
-  int32_t pad;
-};
-
-struct TileMeta {
-  int32_t unit;    // b*H + h
-  int32_t b, h;
-  int32_t t0, nvalid;
-  int32_t whole;   // this CTA covers the unit's whole tile range
-  int32_t last_of_unit;
-  int32_t pad;
-  LoopMeta loop[kLoops];
-};
+// Per-tile metadata written by the producer (int32 words).
+//   [0] unit  [1] b  [2] h  [3] t0  [4] nvalid  [5] whole  [6] npairs  [7] -
+//   pair p (8 words from 8): loop index << 1 | group
+//   loop j (8 words from 16 + 8j): nrows c0 g0 ngrp vrem irem sparse pbase
+constexpr int kMetaWords = 16 + 8 * kLoops;
 
 struct __align__(128) Stage {
   uint8_t kc[kLoops][KVQ_TILE * kRowBytes];
@@ -75,30 +69,28 @@ struct __align__(128) Stage {
   uint16_t vmin[kLoops][144];  // 64 rows x 2 groups + 16 B rounding slack
   uint16_t vsc[kLoops][144];
   int32_t idx[kLoops][80];     // 64 indices + rounding slack
-  TileMeta meta;
+  int32_t meta[kMetaWords];
+};
+
+// Per warp and loop: first staged row of the warp's slice, row count, and the
+// 16-bit presence mask of the slice's tokens (sparse loops).
+struct SliceInfo {
+  int32_t rb, cnt, bits, pad;
+};
+
+struct GroupSmem {
+  __half q16[8][kD];                     // query of the current unit (BF16 values, exact in FP16)
+  float kbias[kMaxPairs][8];             // sum_d q*mK - 64 sum_d q*sK per (pair, head)
+  float red[kGroupWarps][8];             // per-warp max per head
+  float lsum[kGroupWarps][8];
+  float vbs[kGroupWarps][2][8];
+  SliceInfo slice[kGroupWarps][kLoops];
+  float fin[kGroupWarps][kD][8];         // end-of-unit sum of the warps' PV partials
 };
 
 struct Smem {
   Stage st[kStages];
-  // Q' = q * sK per (pair, head) as FP16 hi and lo terms, fragment order: head
-  // stride 160 halves (320 B), then [word i][chunk q][8 channels in the order
-  // 0,4,1,5,2,6,3,7].
-  __half qp[kMaxPairs][2][8 * 160];
-  float kbias[kMaxPairs][8];                // sum_d q * mK per (pair, head)
-  float s[kLoops][KVQ_TILE][8];             // per-loop logits (stream rows), log2 units
-  // P' = p * sV per (loop, V group), FP16, fragment order [k-step][head][16].
-  __half pp[kLoops][2][4][8][16];
-  __half q16[8][kD];                        // query of the current unit (BF16 values, exact in FP16)
-  float fin[4][kD][8];                      // end-of-unit sum of the row-quarter PV partials
-  unsigned long long mask[kLoops];          // presence of logical tokens in a sparse loop
-  float red[kConsumerWarps][8];
-  float alpha[8];
-  float lsum[kConsumerWarps][8];
-  float vbs[kConsumerWarps][8][2];
-  float vbias[8][2];
-  float l_tot[8];
-  int32_t pair_j[kMaxPairs], pair_g[kMaxPairs];
-  int32_t npairs;
+  GroupSmem grp[kGroups];
   unsigned long long full[kStages];
   unsigned long long empty[kStages];
 };
@@ -155,7 +147,10 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+// Named barrier of one consumer group (ids 1, 2).
+__device__ __forceinline__ void group_sync(int grp) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kGroupThreads) : "memory");
+}
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t m, uint32_t o) {
   uint32_t r;
@@ -163,26 +158,16 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t m, uint32_t
   return r;
 }
 
-__device__ __forceinline__ uint32_t h2_sub1024(uint32_t x) {
-  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&x), __half2(__float2half_rn(1024.f), __float2half_rn(1024.f)));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
+// FP16 value 64 + (the nibble at bits 4..7 of each half of x).
+__device__ __forceinline__ uint32_t nib(uint32_t x) { return lop3_and_or(x, 0x00F000F0u, kMagic); }
 
-// (1024 + 16c) / 16 - 64 = c
-__device__ __forceinline__ uint32_t h2_hi_nibble(uint32_t x) {
-  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), __half2(__float2half_rn(0.0625f), __float2half_rn(0.0625f)),
-                      __half2(__float2half_rn(-64.f), __float2half_rn(-64.f)));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
-// Codes of a 32-bit word w (nibbles n0..n7, n0 = lowest channel) as exact FP16 pairs:
-// r[0] = {n0, n4}, r[1] = {n1, n5}, r[2] = {n2, n6}, r[3] = {n3, n7}.
+// Codes of a 32-bit word w (nibbles n0..n7, n0 = lowest channel) as FP16 pairs
+// offset by 64: r[0] = {n0, n4}, r[1] = {n1, n5}, r[2] = {n2, n6}, r[3] = {n3, n7}.
 __device__ __forceinline__ void unpack8(uint32_t w, uint32_t r[4]) {
-  const uint32_t w8 = w >> 8;
-  r[0] = h2_sub1024(lop3_and_or(w, 0x000F000Fu, 0x64006400u));
-  r[1] = h2_hi_nibble(lop3_and_or(w, 0x00F000F0u, 0x64006400u));
-  r[2] = h2_sub1024(lop3_and_or(w8, 0x000F000Fu, 0x64006400u));
-  r[3] = h2_hi_nibble(lop3_and_or(w8, 0x00F000F0u, 0x64006400u));
+  r[0] = nib(w << 4);
+  r[1] = nib(w);
+  r[2] = nib(w >> 4);
+  r[3] = nib(w >> 8);
 }
 
 __device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
@@ -193,138 +178,132 @@ __device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ int popc64(unsigned long long x) { return __popcll(x); }
+// Transpose of an 8x8 matrix of 16-bit values held one row pair per thread.
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ __half2 u2h(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
 
 // ---------------------------------------------------------------- producer
 
-struct UnitPtrs {
-  int T;
-  int nrows[kLoops];
-  const int32_t* active[kLoops];
-  const int32_t* dir[kLoops];
-  const uint8_t* kc[kLoops];
-  const uint16_t* kmin[kLoops];
-  const uint16_t* ksc[kLoops];
-  const uint8_t* vc[kLoops];
-  const uint16_t* vmin[kLoops];
-  const uint16_t* vsc[kLoops];
-};
-
-__device__ void producer(const AttnArgs& a, Smem& S, long long s0, long long e0) {
-  const long long W = a.prefix[a.n_requests];
-  const int C = a.n_ctas;
+template <int DEPTH>
+__device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long long e0) {
   int b = request_of(a.prefix, a.n_requests, s0);
-  int cur_unit = -1;
-  UnitPtrs U;
+  long long us = 0, ue = -1;  // current unit's tile range
+  int h = 0, T = 0, unit = -1;
+  int nr[DEPTH];
+  const int32_t* act[DEPTH];
+  const int32_t* dir[DEPTH];
+  const uint8_t* kc[DEPTH];
+  const uint16_t* kmn[DEPTH];
+  const uint16_t* ksc[DEPTH];
+  const uint8_t* vc[DEPTH];
+  const uint16_t* vmn[DEPTH];
+  const uint16_t* vsc[DEPTH];
   long long it = 0;
   for (long long x = s0; x < e0; ++x, ++it) {
-    const int s = int(it % kStages);
-    const uint32_t ph = uint32_t((it / kStages) & 1);
-    if (it >= kStages && !mbar_wait(&S.empty[s], ph ^ 1u)) {
+    if (x >= ue) {  // next unit: request b (skipping empty ones) and KV head h
+      while (a.prefix[b + 1] <= x) ++b;
+      const kvq_request& R = a.reqs[b];
+      T = R.n_tokens;
+      const int nt = n_tiles_of(T);
+      const long long rb = a.prefix[b];
+      h = int((x - rb) / nt);
+      us = rb + (long long)h * nt;
+      ue = us + nt;
+      unit = b * a.H + h;
+#pragma unroll
+      for (int j = 0; j < DEPTH; ++j) {
+        const kvq_loop_ref& L = R.loop[j];
+        nr[j] = L.n_rows;
+        act[j] = L.active_idx;
+        dir[j] = L.tile_dir;
+        kc[j] = L.k_codes;
+        kmn[j] = L.k_mins;
+        ksc[j] = L.k_scales;
+        vc[j] = L.v_codes;
+        vmn[j] = L.v_mins;
+        vsc[j] = L.v_scales;
+      }
+    }
+    const int k = int(x - us);
+    // directory entries first: their latency overlaps the wait for a free stage
+    int c0s[DEPTH], c1s[DEPTH];
+#pragma unroll
+    for (int j = 0; j < DEPTH; ++j) {
+      if (act[j] == nullptr) {
+        c0s[j] = k * KVQ_TILE;
+        c1s[j] = min(k * KVQ_TILE + KVQ_TILE, T);
+      } else {
+        c0s[j] = __ldg(dir[j] + k);
+        c1s[j] = __ldg(dir[j] + k + 1);
+      }
+    }
+    const int s = grp * kStagesPerGroup + int(it & 1);
+    const uint32_t ph = uint32_t((it >> 1) & 1);
+    if (it >= kStagesPerGroup && !mbar_wait(&S.empty[s], ph ^ 1u)) {
       atomicOr(a.err, 8);
       return;
     }
-    while (a.prefix[b + 1] <= x) ++b;
-    const kvq_request& R = a.reqs[b];
-    const int T = R.n_tokens;
-    const int nt = n_tiles_of(T);
-    const long long rb = a.prefix[b];
-    const int h = int((x - rb) / nt);
-    const int k = int((x - rb) % nt);
-    const int unit = b * a.H + h;
-    if (unit != cur_unit) {
-      cur_unit = unit;
-      U.T = T;
-      for (int j = 0; j < a.depth; ++j) {
-        const kvq_loop_ref& L = R.loop[j];
-        U.nrows[j] = L.n_rows;
-        U.active[j] = L.active_idx;
-        U.dir[j] = L.tile_dir;
-        U.kc[j] = L.k_codes;
-        U.kmin[j] = L.k_mins;
-        U.ksc[j] = L.k_scales;
-        U.vc[j] = L.v_codes;
-        U.vmin[j] = L.v_mins;
-        U.vsc[j] = L.v_scales;
-      }
-    }
     Stage& st = S.st[s];
-    TileMeta& M = st.meta;
-    M.unit = unit;
-    M.b = b;
-    M.h = h;
-    M.t0 = k * KVQ_TILE;
-    M.nvalid = min(KVQ_TILE, T - M.t0);
-    const long long us = rb + (long long)h * nt, ue = us + nt;
-    M.whole = (us >= s0 && ue <= e0) ? 1 : 0;
-    M.last_of_unit = (x == ue - 1 || x == e0 - 1) ? 1 : 0;
-    (void)W;
-    (void)C;
-    // rows of every loop
-    int c0s[kLoops], c1s[kLoops];
-    for (int j = 0; j < a.depth; ++j) {
-      if (U.active[j] == nullptr) {
-        c0s[j] = M.t0;
-        c1s[j] = M.t0 + M.nvalid;
-      } else {
-        c0s[j] = __ldg(U.dir[j] + k);
-        c1s[j] = __ldg(U.dir[j] + k + 1);
-      }
-    }
-    uint32_t bytes = 0;
-    for (int j = 0; j < a.depth; ++j) {
+    int32_t* M = st.meta;
+    M[0] = unit;
+    M[1] = b;
+    M[2] = h;
+    M[3] = k * KVQ_TILE;
+    M[4] = min(KVQ_TILE, T - k * KVQ_TILE);
+    M[5] = (us >= s0 && ue <= e0) ? 1 : 0;
+    int np = 0;
+#pragma unroll
+    for (int j = 0; j < DEPTH; ++j) {
       int c0 = c0s[j], c1 = c1s[j];
-      LoopMeta& LM = M.loop[j];
-      LM.sparse = U.active[j] != nullptr;
-      if (c0 < 0 || c1 > U.nrows[j] || c0 > c1 || c1 - c0 > KVQ_TILE) {
+      int32_t* LM = M + 16 + 8 * j;
+      if (c0 < 0 || c1 > nr[j] || c0 > c1 || c1 - c0 > KVQ_TILE) {
         atomicOr(a.err, 4);
         c0 = c1 = 0;
       }
       const int n = c1 - c0;
-      LM.nrows = n;
-      LM.c0 = c0;
-      LM.g0 = c0 / kG;
-      LM.ngrp = n > 0 ? (c1 - 1) / kG - c0 / kG + 1 : 0;
-      LM.vrem = 0;
-      LM.irem = 0;
+      const int g0 = c0 / kG;
+      const int ngrp = n > 0 ? (c1 - 1) / kG - g0 + 1 : 0;
+      LM[0] = n;
+      LM[1] = c0;
+      LM[2] = g0;
+      LM[3] = ngrp;
+      LM[4] = 0;
+      LM[5] = 0;
+      LM[6] = act[j] != nullptr;
+      LM[7] = np;
+      for (int G = 0; G < ngrp; ++G) M[8 + np++] = (j << 1) | G;
       if (n == 0) continue;
-      const int nr = U.nrows[j];
-      // codes: n rows x 64 B, contiguous in the head-major plane
-      bulk_copy(st.kc[j], U.kc[j] + ((long long)h * nr + c0) * kRowBytes, n * kRowBytes, &S.full[s]);
-      bulk_copy(st.vc[j], U.vc[j] + ((long long)h * nr + c0) * kRowBytes, n * kRowBytes, &S.full[s]);
-      bytes += 2 * n * kRowBytes;
-      // K params: the spanned groups, 256 B per group and plane
-      const int ng = (nr + kG - 1) / kG;
-      const uint16_t* km = U.kmin[j] + ((long long)h * ng + LM.g0) * kD;
-      const uint16_t* ks = U.ksc[j] + ((long long)h * ng + LM.g0) * kD;
-      bulk_copy(st.kmin[j], km, LM.ngrp * kD * 2, &S.full[s]);
-      bulk_copy(st.ksc[j], ks, LM.ngrp * kD * 2, &S.full[s]);
-      bytes += 2 * LM.ngrp * kD * 2;
-      // V params: 4 B per row and plane, copied in 16-byte units (the planes are
-      // allocated to a 16-byte multiple, so the rounded range stays inside)
-      {
-        const long long off = ((long long)h * nr + c0) * 4;  // bytes
+      const long long hr = (long long)h * nr[j] + c0;  // first stored row of this head
+      bulk_copy(st.kc[j], kc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
+      bulk_copy(st.vc[j], vc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
+      const long long gb = ((long long)h * ((nr[j] + kG - 1) / kG) + g0) * kD;
+      bulk_copy(st.kmin[j], kmn[j] + gb, ngrp * kD * 2, &S.full[s]);
+      bulk_copy(st.ksc[j], ksc[j] + gb, ngrp * kD * 2, &S.full[s]);
+      {  // V params: 4 B per row and plane, moved in whole 16-byte units
+        const long long off = hr * 4;
         const long long lo = off & ~15LL;
-        const long long hi = (off + (long long)n * 4 + 15) & ~15LL;
-        const uint32_t nb = uint32_t(hi - lo);
-        bulk_copy(st.vmin[j], reinterpret_cast<const uint8_t*>(U.vmin[j]) + lo, nb, &S.full[s]);
-        bulk_copy(st.vsc[j], reinterpret_cast<const uint8_t*>(U.vsc[j]) + lo, nb, &S.full[s]);
-        bytes += 2 * nb;
-        LM.vrem = int((off - lo) / 2);
+        const uint32_t nb = uint32_t(((off + (long long)n * 4 + 15) & ~15LL) - lo);
+        bulk_copy(st.vmin[j], reinterpret_cast<const uint8_t*>(vmn[j]) + lo, nb, &S.full[s]);
+        bulk_copy(st.vsc[j], reinterpret_cast<const uint8_t*>(vsc[j]) + lo, nb, &S.full[s]);
+        LM[4] = int((off - lo) / 2);
       }
-      if (LM.sparse) {
+      if (act[j] != nullptr) {
         const long long off = (long long)c0 * 4;
         const long long lo = off & ~15LL;
-        const long long hi = (off + (long long)n * 4 + 15) & ~15LL;
-        const uint32_t nb = uint32_t(hi - lo);
-        bulk_copy(st.idx[j], reinterpret_cast<const uint8_t*>(U.active[j]) + lo, nb, &S.full[s]);
-        bytes += nb;
-        LM.irem = int((off - lo) / 4);
+        const uint32_t nb = uint32_t(((off + (long long)n * 4 + 15) & ~15LL) - lo);
+        bulk_copy(st.idx[j], reinterpret_cast<const uint8_t*>(act[j]) + lo, nb, &S.full[s]);
+        LM[5] = int((off - lo) / 4);
       }
     }
-    // The single expected arrival: releases the metadata written above; the phase
-    // completes once every copy has delivered its bytes.
-    (void)bytes;
+    M[6] = np;
+    // the single expected arrival: releases the metadata; the phase completes
+    // once every copy has delivered its bytes
     mbar_arrive(&S.full[s]);
   }
 }
@@ -332,440 +311,485 @@ __device__ void producer(const AttnArgs& a, Smem& S, long long s0, long long e0)
 // ---------------------------------------------------------------- consumers
 
 struct UnitState {
-  float m;       // running max of this thread's head (log2 units)
-  float l;       // partial sum of exp2 for this thread's (head, tokens)
-  float vb[2];   // partial V-min terms per V group
-  float acc[4][4];  // PV accumulators: 4 channel m-tiles x (2 rows x 2 heads)
+  float m[2];       // running max of heads 2q, 2q+1 (log2 units)
+  float l[2];       // partial sums of exp2 of this thread's tokens for heads 2q, 2q+1
+  float vb[2][2];   // partial V-min terms (with the -64 offset correction): [V group][head 2q / 2q+1]
+  float acc[8][4];  // PV accumulators: 8 channel m-tiles x (2 rows x 2 heads)
 };
 
-__device__ void load_unit_query(const AttnArgs& a, Smem& S, int b, int h) {
-  const int tid = threadIdx.x;
-  for (int i = tid; i < 8 * kD; i += kConsumers) {
-    const int hh = i / kD, d = i % kD;
-    float v = 0.0f;
-    if (hh < a.g) v = bf16_bits_to_f32(a.q[((long long)b * a.Hq + (long long)h * a.g + hh) * kD + d]);
-    S.q16[hh][d] = __float2half_rn(v);  // exact: a BF16 value in the FP16 range
-  }
-}
-
-// Writes the unit's result: output rows (whole unit) or a partial slot.
 struct UnitInfo {
   int unit, b, h, whole;
 };
 
-__device__ void finish_unit(const AttnArgs& a, Smem& S, UnitState& U, const UnitInfo& M, int warp, int lane) {
-  const int tid = threadIdx.x;
-  const int hme = tid & 7;
-  // l and V-min terms: reduce over the threads of the same head
-  float l = U.l, v0 = U.vb[0], v1 = U.vb[1];
-#pragma unroll
-  for (int off = 8; off < 32; off <<= 1) {
-    l += __shfl_xor_sync(0xffffffffu, l, off);
-    v0 += __shfl_xor_sync(0xffffffffu, v0, off);
-    v1 += __shfl_xor_sync(0xffffffffu, v1, off);
+__device__ void load_unit_query(const AttnArgs& a, GroupSmem& G, int b, int h, int gt) {
+  for (int i = gt; i < 8 * kD; i += kGroupThreads) {
+    const int hh = i / kD, d = i % kD;
+    float v = 0.0f;
+    if (hh < a.g) v = bf16_bits_to_f32(a.q[((long long)b * a.Hq + (long long)h * a.g + hh) * kD + d]);
+    G.q16[hh][d] = __float2half_rn(v);  // exact: a BF16 value in the FP16 range
   }
-  if (lane < 8) {
-    S.lsum[warp][lane] = l;
-    S.vbs[warp][lane][0] = v0;
-    S.vbs[warp][lane][1] = v1;
-  }
-  // PV partials of this warp: channel group grp, row quarter rq
-  const int grp = warp >> 2, rq = warp & 3;
-  const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-  for (int mt = 0; mt < 4; ++mt) {
-    const int ch_lo = 64 * grp + 8 * g + 2 * mt;
-    S.fin[rq][ch_lo][2 * q] = U.acc[mt][0];
-    S.fin[rq][ch_lo][2 * q + 1] = U.acc[mt][1];
-    S.fin[rq][ch_lo + 1][2 * q] = U.acc[mt][2];
-    S.fin[rq][ch_lo + 1][2 * q + 1] = U.acc[mt][3];
-  }
-  consumer_sync();
-  if (tid < 8) {
-    float lt = 0.f, b0 = 0.f, b1 = 0.f;
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      lt += S.lsum[w][tid];
-      b0 += S.vbs[w][tid][0];
-      b1 += S.vbs[w][tid][1];
-    }
-    S.l_tot[tid] = lt;
-    S.vbias[tid][0] = b0;
-    S.vbias[tid][1] = b1;
-  }
-  consumer_sync();
-  const int g_q = a.g;
-  if (M.whole) {
-    for (int i = tid; i < g_q * kD; i += kConsumers) {
-      const int hh = i / kD, d = i % kD;
-      float o = S.fin[0][d][hh] + S.fin[1][d][hh] + S.fin[2][d][hh] + S.fin[3][d][hh] + S.vbias[hh][d >> 6];
-      a.out[((long long)M.b * a.Hq + (long long)M.h * g_q + hh) * kD + d] = o / S.l_tot[hh];
-    }
-  } else {
-    float* slot = a.partials + (size_t)(blockIdx.x + M.unit) * kSlotFloats;
-    if (tid < g_q) {
-      slot[tid] = U.m;  // every thread tracks the max of head tid & 7; thread tid has head tid
-      slot[kMaxG + tid] = S.l_tot[tid];
-    }
-    for (int i = tid; i < g_q * kD; i += kConsumers) {
-      const int hh = i / kD, d = i % kD;
-      slot[2 * kMaxG + hh * kD + d] =
-          S.fin[0][d][hh] + S.fin[1][d][hh] + S.fin[2][d][hh] + S.fin[3][d][hh] + S.vbias[hh][d >> 6];
-    }
-  }
-  (void)hme;
-  consumer_sync();
 }
 
-__device__ void consumer(const AttnArgs& a, Smem& S, long long s0, long long e0) {
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
+// Writes the unit's result: output rows (whole unit) or the group's partial slot.
+__device__ void finish_unit(const AttnArgs& a, GroupSmem& G, UnitState& U, const UnitInfo& M, int grp, int vcta,
+                            int w, int lane) {
+  const int gt = w * 32 + lane;
   const int g = lane >> 2, q = lane & 3;
-  const int hme = tid & 7;       // head of this thread in the softmax phase
+  float l0 = U.l[0], l1 = U.l[1];
+  float v00 = U.vb[0][0], v01 = U.vb[0][1], v10 = U.vb[1][0], v11 = U.vb[1][1];
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    v00 += __shfl_xor_sync(0xffffffffu, v00, off);
+    v01 += __shfl_xor_sync(0xffffffffu, v01, off);
+    v10 += __shfl_xor_sync(0xffffffffu, v10, off);
+    v11 += __shfl_xor_sync(0xffffffffu, v11, off);
+  }
+  if (g == 0) {
+    G.lsum[w][2 * q] = l0;
+    G.lsum[w][2 * q + 1] = l1;
+    G.vbs[w][0][2 * q] = v00;
+    G.vbs[w][0][2 * q + 1] = v01;
+    G.vbs[w][1][2 * q] = v10;
+    G.vbs[w][1][2 * q + 1] = v11;
+  }
+#pragma unroll
+  for (int vg = 0; vg < 2; ++vg)
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int ch = 64 * vg + 8 * g + 2 * mt;
+      const float* c = U.acc[4 * vg + mt];
+      *reinterpret_cast<float2*>(&G.fin[w][ch][2 * q]) = make_float2(c[0], c[1]);
+      *reinterpret_cast<float2*>(&G.fin[w][ch + 1][2 * q]) = make_float2(c[2], c[3]);
+    }
+  group_sync(grp);
   const int gq = a.g;
+  float* slot = a.partials + (size_t)(vcta + M.unit) * kSlotFloats;
+  for (int i = gt; i < gq * kD; i += kGroupThreads) {
+    const int hh = i / kD, d = i % kD;
+    const float lt = G.lsum[0][hh] + G.lsum[1][hh] + G.lsum[2][hh] + G.lsum[3][hh];
+    const float vb = G.vbs[0][d >> 6][hh] + G.vbs[1][d >> 6][hh] + G.vbs[2][d >> 6][hh] + G.vbs[3][d >> 6][hh];
+    const float o = (G.fin[0][d][hh] + G.fin[1][d][hh]) + (G.fin[2][d][hh] + G.fin[3][d][hh]) + vb;
+    if (M.whole) {
+      a.out[((long long)M.b * a.Hq + (long long)M.h * gq + hh) * kD + d] = o / lt;
+    } else {
+      slot[2 * kMaxG + hh * kD + d] = o;
+      if (d == 0) slot[kMaxG + hh] = lt;
+    }
+  }
+  if (!M.whole && w == 0 && g == 0) {  // the running max is the same in every thread
+    if (2 * q < gq) slot[2 * q] = U.m[0];
+    if (2 * q + 1 < gq) slot[2 * q + 1] = U.m[1];
+  }
+  group_sync(grp);
+}
+
+// Logits of the 16 staged rows (rb + g, rb + g + 8 per thread) of loop j against
+// K group G: Q' = q * sK as exact FP16 hi + lo terms, codes unpacked from the
+// two 16-byte chunks wa (row g) and wb (row g + 8); four accumulation chains.
+__device__ __forceinline__ void qk_pass(const Stage& st, int j, int G, const uint32_t qp[16], const uint4 wa,
+                                        const uint4 wb, int q, float e[4]) {
+  const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w}, wB[4] = {wb.x, wb.y, wb.z, wb.w};
+  float c[4][4] = {};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 sv4 = *reinterpret_cast<const uint4*>(&st.ksc[j][G * kD + 32 * q + 8 * i]);
+    const uint32_t sp[4] = {__byte_perm(sv4.x, sv4.z, 0x5410), __byte_perm(sv4.x, sv4.z, 0x7632),
+                            __byte_perm(sv4.y, sv4.w, 0x5410), __byte_perm(sv4.y, sv4.w, 0x7632)};
+    uint32_t bh[4], bl[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 hv = __hmul2(u2h(qp[4 * i + k]), u2h(sp[k]));               // RN16(q * s)
+      const __half2 lv = __hfma2(u2h(qp[4 * i + k]), u2h(sp[k]), __hneg2(hv));  // RN16(q * s - hi)
+      bh[k] = h2u(hv);
+      bl[k] = h2u(lv);
+    }
+    uint32_t ua[4], ub[4];
+    unpack8(wA[i], ua);
+    unpack8(wB[i], ub);
+    const uint32_t A0[4] = {ua[0], ub[0], ua[1], ub[1]};
+    const uint32_t A1[4] = {ua[2], ub[2], ua[3], ub[3]};
+    mma16816(c[0], A0, bh[0], bh[1]);
+    mma16816(c[1], A1, bh[2], bh[3]);
+    mma16816(c[2], A0, bl[0], bl[1]);
+    mma16816(c[3], A1, bl[2], bl[3]);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) e[k] = (c[0][k] + c[1][k]) + (c[2][k] + c[3][k]);
+}
+
+template <int DEPTH>
+__device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long long s0, long long e0) {
+  const int gt = threadIdx.x - grp * kGroupThreads;  // thread within the group
+  const int w = gt >> 5, lane = gt & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int gq = a.g;
+  const float lsc = a.scale * kLog2e;
+  GroupSmem& Gs = S.grp[grp];
   UnitState U;
   int cur_unit = -1;
   UnitInfo Mprev = {-1, 0, 0, 0};
+  uint32_t qp[16];  // q of head g, channels 32q..32q+31, as FP16 pairs in fragment order
   long long it = 0;
-  // Q' task of this thread: pair offset, head, channel chunk
-  const int qt_pair = tid >> 7, qt_h = (tid >> 4) & 7, qt_chunk = tid & 15;
-  uint32_t qreg[4];  // FP16 pairs of q in the order (0,4),(1,5),(2,6),(3,7) of the chunk
 
   for (long long x = s0; x < e0; ++x, ++it) {
-    const int s = int(it % kStages);
-    const uint32_t ph = uint32_t((it / kStages) & 1);
+    const int s = grp * kStagesPerGroup + int(it & 1);
+    const uint32_t ph = uint32_t((it >> 1) & 1);
     if (!mbar_wait(&S.full[s], ph)) {
       if (lane == 0) atomicOr(a.err, 8);
       return;
     }
-    Stage& st = S.st[s];
-    const TileMeta& M = st.meta;
-    if (M.unit != cur_unit) {
-      if (cur_unit >= 0) finish_unit(a, S, U, Mprev, warp, lane);
-      cur_unit = M.unit;
-      U.m = -INFINITY;
-      U.l = 0.f;
-      U.vb[0] = U.vb[1] = 0.f;
+    const Stage& st = S.st[s];
+    const int4 m0 = *reinterpret_cast<const int4*>(&st.meta[0]);
+    const int4 m1 = *reinterpret_cast<const int4*>(&st.meta[4]);
+    const int unit = m0.x, t0 = m0.w, nvalid = m1.x, npairs = m1.z;
+    if (unit != cur_unit) {
+      if (cur_unit >= 0) finish_unit(a, Gs, U, Mprev, grp, vcta, w, lane);
+      cur_unit = unit;
+      Mprev.unit = unit;
+      Mprev.b = m0.y;
+      Mprev.h = m0.z;
+      Mprev.whole = m1.y;
+      U.m[0] = U.m[1] = -INFINITY;
+      U.l[0] = U.l[1] = 0.f;
+      U.vb[0][0] = U.vb[0][1] = U.vb[1][0] = U.vb[1][1] = 0.f;
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
+      for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) U.acc[mt][e] = 0.f;
-      load_unit_query(a, S, M.b, M.h);
-      consumer_sync();
-      {
-        const __half* qp = &S.q16[qt_h][8 * qt_chunk];
-        const __half o[8] = {qp[0], qp[4], qp[1], qp[5], qp[2], qp[6], qp[3], qp[7]};
+      load_unit_query(a, Gs, Mprev.b, Mprev.h, gt);
+      group_sync(grp);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          __half2 hv = __halves2half2(o[2 * e], o[2 * e + 1]);
-          qreg[e] = *reinterpret_cast<uint32_t*>(&hv);
-        }
+      for (int i = 0; i < 4; ++i) {
+        const __half* qr = &Gs.q16[g][32 * q + 8 * i];
+        qp[4 * i + 0] = h2u(__halves2half2(qr[0], qr[4]));
+        qp[4 * i + 1] = h2u(__halves2half2(qr[1], qr[5]));
+        qp[4 * i + 2] = h2u(__halves2half2(qr[2], qr[6]));
+        qp[4 * i + 3] = h2u(__halves2half2(qr[3], qr[7]));
       }
     }
-    Mprev.unit = M.unit;
-    Mprev.b = M.b;
-    Mprev.h = M.h;
-    Mprev.whole = M.whole;
-    const int depth = a.depth;
 
-    // ---- prep: sparse presence masks, (loop, group) pairs, Q' and the K-min terms
-    if (warp < depth && M.loop[warp].sparse) {
-      const LoopMeta& LM = M.loop[warp];
-      unsigned long long bits = 0;
-      for (int i = lane; i < LM.nrows; i += 32) {
-        const int u = st.idx[warp][LM.irem + i] - M.t0;
-        if (u >= 0 && u < KVQ_TILE) bits |= 1ull << u;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, off);
-      if (lane == 0) S.mask[warp] = bits;
-    }
-    if (tid == 0) {
-      int np = 0;
-      for (int j = 0; j < depth; ++j)
-        for (int G = 0; G < M.loop[j].ngrp; ++G) {
-          S.pair_j[np] = j;
-          S.pair_g[np] = G;
-          ++np;
-        }
-      S.npairs = np;
-    }
-    consumer_sync();
-    const int npairs = S.npairs;
-    for (int p = qt_pair; p < npairs; p += kConsumers / 128) {
-      const int j = S.pair_j[p], G = S.pair_g[p];
-      const uint4 sv = *reinterpret_cast<const uint4*>(&st.ksc[j][G * kD + 8 * qt_chunk]);
-      // scales in the order (0,4),(1,5),(2,6),(3,7)
-      const uint32_t s04 = __byte_perm(sv.x, sv.z, 0x5410), s15 = __byte_perm(sv.x, sv.z, 0x7632);
-      const uint32_t s26 = __byte_perm(sv.y, sv.w, 0x5410), s37 = __byte_perm(sv.y, sv.w, 0x7632);
-      const uint32_t sp[4] = {s04, s15, s26, s37};
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __half2 qv = *reinterpret_cast<const __half2*>(&qreg[e]);
-        const __half2 sv2 = *reinterpret_cast<const __half2*>(&sp[e]);
-        const __half2 h2 = __hmul2(qv, sv2);                 // RN16(q * s)
-        const __half2 l2 = __hfma2(qv, sv2, __hneg2(h2));   // RN16(q * s - hi), exact here
-        hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
-        lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
-      }
-      // chunk c covers channels 8c..8c+7 = 32q' + 8i': store at [head][i'][q']
-      const int qq = qt_chunk >> 2, ii = qt_chunk & 3;
-      *reinterpret_cast<uint4*>(&S.qp[p][0][qt_h * 160 + ii * 32 + qq * 8]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(&S.qp[p][1][qt_h * 160 + ii * 32 + qq * 8]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    // K-min terms of all pairs in one MMA chain: rows = pairs, K = channels, N = heads
-    if (warp == kConsumerWarps - 1) {
+    // ---- K-min terms of every (loop, group) pair, by warp 0 of the group, in one
+    // MMA chain: rows 0..7 = the pairs' mins, rows 8..15 = their scales times
+    // -64 (removing the code offset); K = channels, N = heads.
+    if (w == 0) {
       float c[4] = {0.f, 0.f, 0.f, 0.f};
+      const bool live = g < npairs;
+      const int pj = live ? st.meta[8 + g] : 0;
+      const uint16_t* mrow = &st.kmin[pj >> 1][(pj & 1) * kD];
+      const uint16_t* srow = &st.ksc[pj >> 1][(pj & 1) * kD];
+      const __half2 m64 = __float2half2_rn(-64.f);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         uint32_t av[4] = {0u, 0u, 0u, 0u};
-        if (g < npairs) {
-          const uint16_t* mrow = &st.kmin[S.pair_j[g]][S.pair_g[g] * kD + 16 * kk];
-          av[0] = *reinterpret_cast<const uint32_t*>(mrow + 2 * q);
-          av[2] = *reinterpret_cast<const uint32_t*>(mrow + 2 * q + 8);
+        if (live) {
+          av[0] = *reinterpret_cast<const uint32_t*>(mrow + 16 * kk + 2 * q);
+          av[1] = h2u(__hmul2(u2h(*reinterpret_cast<const uint32_t*>(srow + 16 * kk + 2 * q)), m64));
+          av[2] = *reinterpret_cast<const uint32_t*>(mrow + 16 * kk + 2 * q + 8);
+          av[3] = h2u(__hmul2(u2h(*reinterpret_cast<const uint32_t*>(srow + 16 * kk + 2 * q + 8)), m64));
         }
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&S.q16[g][16 * kk + 2 * q]);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&S.q16[g][16 * kk + 2 * q + 8]);
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&Gs.q16[g][16 * kk + 2 * q]);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&Gs.q16[g][16 * kk + 2 * q + 8]);
         mma16816(c, av, b0, b1);
       }
-      if (g < npairs) {
-        S.kbias[g][2 * q] = c[0];
-        S.kbias[g][2 * q + 1] = c[1];
-      }
+      if (live) *reinterpret_cast<float2*>(&Gs.kbias[g][2 * q]) = make_float2(c[0] + c[2], c[1] + c[3]);
     }
-    consumer_sync();
 
-    // ---- QK^T over the stored rows of every loop: item = (loop, 16-row m-tile)
-    {
-      int item = 0;
-      int pbase = 0;
-      for (int j = 0; j < depth; ++j) {
-        const LoopMeta& LM = M.loop[j];
-        const int nmt = (LM.nrows + 15) >> 4;
-        for (int mt = 0; mt < nmt; ++mt, ++item) {
-          if ((item % kConsumerWarps) != warp) continue;
-          const int r0 = 16 * mt + g, r1 = r0 + 8;
-          // K group of each row (relative to the tile's first group)
-          const int ga = (LM.c0 + 16 * mt) / kG - LM.g0;
-          const int gb = (LM.c0 + 16 * mt + 15) / kG - LM.g0;
-          const bool split = ga != gb && gb < LM.ngrp;
-          float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-          const uint4 wa = *reinterpret_cast<const uint4*>(&st.kc[j][r0 * kRowBytes + 16 * q]);
-          const uint4 wb = *reinterpret_cast<const uint4*>(&st.kc[j][r1 * kRowBytes + 16 * q]);
-          const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w}, wB[4] = {wb.x, wb.y, wb.z, wb.w};
-          const __half* qpa = &S.qp[pbase + ga][0][g * 160 + q * 8];
-          const __half* qpb = &S.qp[pbase + (split ? gb : ga)][0][g * 160 + q * 8];
-          constexpr int kLo = 8 * 160;  // offset of the lo terms
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t ua[4], ub[4];
-            unpack8(wA[i], ua);
-            unpack8(wB[i], ub);
-            const uint32_t A0[4] = {ua[0], ub[0], ua[1], ub[1]};
-            const uint32_t A1[4] = {ua[2], ub[2], ua[3], ub[3]};
-            const uint4 bh = *reinterpret_cast<const uint4*>(qpa + i * 32);
-            const uint4 bl = *reinterpret_cast<const uint4*>(qpa + kLo + i * 32);
-            mma16816(c0, A0, bh.x, bh.y);
-            mma16816(c0, A1, bh.z, bh.w);
-            mma16816(c0, A0, bl.x, bl.y);
-            mma16816(c0, A1, bl.z, bl.w);
-            if (split) {
-              const uint4 bh2 = *reinterpret_cast<const uint4*>(qpb + i * 32);
-              const uint4 bl2 = *reinterpret_cast<const uint4*>(qpb + kLo + i * 32);
-              mma16816(c1, A0, bh2.x, bh2.y);
-              mma16816(c1, A1, bh2.z, bh2.w);
-              mma16816(c1, A0, bl2.x, bl2.y);
-              mma16816(c1, A1, bl2.z, bl2.w);
-            }
-          }
-          // rows r0 / r1 of this m-tile: pick the accumulator of their K group, add its min term
-          const int gr0 = (LM.c0 + r0) / kG - LM.g0;
-          const int gr1 = (LM.c0 + r1) / kG - LM.g0;
-          const float* e0v = (split && gr0 != ga) ? c1 : c0;
-          const float* e1v = (split && gr1 != ga) ? c1 : c0;
-          const int p0 = pbase + min(gr0, LM.ngrp - 1), p1 = pbase + min(gr1, LM.ngrp - 1);
-          *reinterpret_cast<float2*>(&S.s[j][r0][2 * q]) =
-              make_float2(e0v[0] + S.kbias[p0][2 * q], e0v[1] + S.kbias[p0][2 * q + 1]);
-          *reinterpret_cast<float2*>(&S.s[j][r1][2 * q]) =
-              make_float2(e1v[2] + S.kbias[p1][2 * q], e1v[3] + S.kbias[p1][2 * q + 1]);
+    // ---- QK^T of the warp's 16 tokens [16w, 16w + 16) over every loop
+    // logits in the accumulator layout: sv[0] (token g, head 2q), sv[1] (g, 2q+1),
+    // sv[2] (g + 8, 2q), sv[3] (g + 8, 2q + 1)
+    float sv[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t pinfo = 0;  // per loop 4 bits: tokens g / g+8 present, and their K group
+    for (int j = 0; j < DEPTH; ++j) {
+      const int4 la = *reinterpret_cast<const int4*>(&st.meta[16 + 8 * j]);
+      const int4 lb = *reinterpret_cast<const int4*>(&st.meta[20 + 8 * j]);
+      const int c0 = la.y, g0 = la.z, ngrp = la.w, irem = lb.y, sparse = lb.z, pbase = lb.w;
+      int rb, cnt, bits;
+      if (!sparse) {
+        rb = 16 * w;
+        cnt = max(0, min(16, nvalid - 16 * w));
+        bits = cnt >= 16 ? 0xFFFF : ((1 << cnt) - 1);
+      } else {
+        // presence of the tile's tokens in this loop, from its staged index slice
+        unsigned long long mk = 0;
+        for (int i = lane; i < la.x; i += 32) {
+          const int u = st.idx[j][irem + i] - t0;
+          if (u >= 0 && u < KVQ_TILE) mk |= 1ull << u;
         }
-        pbase += LM.ngrp;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mk |= __shfl_xor_sync(0xffffffffu, mk, off);
+        bits = int((mk >> (16 * w)) & 0xFFFFull);
+        rb = __popcll(mk & ((1ull << (16 * w)) - 1ull));
+        cnt = __popc(bits);
       }
+      if (lane == 0) Gs.slice[w][j] = SliceInfo{rb, cnt, bits, 0};
+      if (cnt == 0) continue;
+      // K groups of the slice's rows, relative to the tile's first group
+      const int ga = ((c0 + rb) >> 6) - g0;
+      const int gb = ((c0 + rb + cnt - 1) >> 6) - g0;
+      const bool split = gb != ga;
+      // A: staged rows rb + g and rb + g + 8, the 16 bytes of chunk q
+      const uint4 wa = *reinterpret_cast<const uint4*>(&st.kc[j][(rb + g) * kRowBytes + 16 * q]);
+      const uint4 wb = *reinterpret_cast<const uint4*>(&st.kc[j][(rb + g + 8) * kRowBytes + 16 * q]);
+      float e[4];
+      qk_pass(st, j, ga, qp, wa, wb, q, e);
+      if (split) {  // rows of the second K group: a second pass with that group's Q'
+        float f[4];
+        qk_pass(st, j, gb, qp, wa, wb, q, f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int row = k < 2 ? g : g + 8;  // staged row rb + row
+          if (((c0 + rb + row) >> 6) - g0 != ga) e[k] = f[k];
+        }
+      }
+      // rows -> the warp's tokens: identity for a dense loop; a sparse loop's row r
+      // holds the r-th present token, fetched by shuffles
+      uint32_t pi = 0;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int tok = g + 8 * half;
+        const bool present = (bits >> tok) & 1;
+        int row = tok;
+        float x0 = e[2 * half], x1 = e[2 * half + 1];
+        if (sparse) {  // warp-uniform: fetch row `row` from its owner (every lane sends both halves)
+          row = __popc(bits & ((1 << tok) - 1));
+          const int src = ((row & 7) << 2) | q;
+          const float lo0 = __shfl_sync(0xffffffffu, e[0], src), lo1 = __shfl_sync(0xffffffffu, e[1], src);
+          const float hi0 = __shfl_sync(0xffffffffu, e[2], src), hi1 = __shfl_sync(0xffffffffu, e[3], src);
+          x0 = row < 8 ? lo0 : hi0;
+          x1 = row < 8 ? lo1 : hi1;
+        }
+        if (present) {
+          sv[2 * half] += x0;
+          sv[2 * half + 1] += x1;
+          const int G = ((c0 + rb + row) >> 6) - g0;
+          pi |= (1u | (uint32_t(G) << 1)) << (2 * half);
+        }
+      }
+      (void)ngrp;
+      pinfo |= pi << (4 * j);
     }
-    consumer_sync();
+    group_sync(grp);  // K-min terms and slice info visible
 
-    // ---- softmax over the tile (online, log2 units) and P' = p * sV
+    // ---- logits in log2 units, tile max per head across the group
     {
-      // logits of this thread's tokens tt = tid/8 and tid/8 + 32 for head hme,
-      // scaled into log2 units
-      const float lsc = a.scale * kLog2e;
-      float sv[2];
-      int rows[2][kLoops];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int tt = (tid >> 3) + 32 * u;
-        float acc = -INFINITY;
-        if (tt < M.nvalid && hme < gq) {
-          acc = 0.f;
-          for (int j = 0; j < depth; ++j) {
-            const LoopMeta& LM = M.loop[j];
-            int row = tt;
-            if (LM.sparse) {
-              const unsigned long long mk = S.mask[j];
-              row = ((mk >> tt) & 1ull) ? popc64(mk & ((1ull << tt) - 1ull)) : -1;
-            }
-            rows[u][j] = row;
-            if (row >= 0) acc += S.s[j][row][hme];
-          }
-          acc *= lsc;
-        } else {
-          for (int j = 0; j < depth; ++j) rows[u][j] = -1;
-        }
-        sv[u] = acc;
-      }
-      float mloc = fmaxf(sv[0], sv[1]);
-      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
-      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
-      if (lane < 8) S.red[warp][lane] = mloc;
-      consumer_sync();
-      float mt = S.red[0][hme];
+      for (int j = 0; j < DEPTH; ++j) {
+        const int pbase = st.meta[16 + 8 * j + 7];
 #pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) mt = fmaxf(mt, S.red[w][hme]);
-      const float mnew = fmaxf(U.m, mt);
-      const float alpha = (U.m == -INFINITY) ? 0.f : exp2f(U.m - mnew);
-      U.m = mnew;
-      if (tid < 8) S.alpha[tid] = alpha;
-      U.l *= alpha;
-      U.vb[0] *= alpha;
-      U.vb[1] *= alpha;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int tt = (tid >> 3) + 32 * u;
-        const float p = (sv[u] == -INFINITY) ? 0.f : exp2f(sv[u] - mnew);
-        U.l += p;
-        const __half2 p2 = __floats2half2_rn(p, p);
-        for (int j = 0; j < depth; ++j) {
-          const LoopMeta& LM = M.loop[j];
-          const int row = LM.sparse ? rows[u][j] : tt;
-          if (row < 0 || hme >= gq) continue;
-          if (LM.sparse && row >= LM.nrows) continue;
-          const int vi = LM.vrem + 2 * row;
-          const __half2 sc2 = *reinterpret_cast<const __half2*>(&st.vsc[j][vi]);
-          const __half2 pv = (p != 0.f) ? __hmul2(p2, sc2) : __float2half2_rn(0.f);
-          const int ks = row >> 4, rr = row & 15;
-          const int pos = 4 * (rr & 3) + (rr >> 2);
-          S.pp[j][0][ks][hme][pos] = __low2half(pv);
-          S.pp[j][1][ks][hme][pos] = __high2half(pv);
-          if (p != 0.f) {
-            const float2 mv = __half22float2(*reinterpret_cast<const __half2*>(&st.vmin[j][vi]));
-            U.vb[0] = fmaf(p, mv.x, U.vb[0]);
-            U.vb[1] = fmaf(p, mv.y, U.vb[1]);
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t f = (pinfo >> (4 * j + 2 * half)) & 3u;
+          if (f & 1u) {
+            const float2 kb = *reinterpret_cast<const float2*>(&Gs.kbias[pbase + int(f >> 1)][2 * q]);
+            sv[2 * half] += kb.x;
+            sv[2 * half + 1] += kb.y;
           }
         }
       }
-      // sparse loops: zero P' of the compact rows past nrows inside the last k-step
-      for (int j = 0; j < depth; ++j) {
-        const LoopMeta& LM = M.loop[j];
-        if (!LM.sparse) continue;
-        const int pad_end = (LM.nrows + 15) & ~15;
-        for (int i = tid; i < (pad_end - LM.nrows) * 8; i += kConsumers) {
-          const int row = LM.nrows + i / 8, hh = i % 8;
-          const int ks = row >> 4, rr = row & 15;
-          const int pos = 4 * (rr & 3) + (rr >> 2);
-          S.pp[j][0][ks][hh][pos] = __float2half_rn(0.f);
-          S.pp[j][1][ks][hh][pos] = __float2half_rn(0.f);
-        }
+      const bool h0ok = 2 * q < gq, h1ok = 2 * q + 1 < gq;
+      const bool t0ok = 16 * w + g < nvalid, t1ok = 16 * w + g + 8 < nvalid;
+      sv[0] = (t0ok && h0ok) ? sv[0] * lsc : -INFINITY;
+      sv[1] = (t0ok && h1ok) ? sv[1] * lsc : -INFINITY;
+      sv[2] = (t1ok && h0ok) ? sv[2] * lsc : -INFINITY;
+      sv[3] = (t1ok && h1ok) ? sv[3] * lsc : -INFINITY;
+      float m0v = fmaxf(sv[0], sv[2]), m1v = fmaxf(sv[1], sv[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        m0v = fmaxf(m0v, __shfl_xor_sync(0xffffffffu, m0v, off));
+        m1v = fmaxf(m1v, __shfl_xor_sync(0xffffffffu, m1v, off));
+      }
+      if (g == 0) {
+        Gs.red[w][2 * q] = m0v;
+        Gs.red[w][2 * q + 1] = m1v;
       }
     }
-    consumer_sync();
+    group_sync(grp);
 
-    // ---- PV: warp = (V group, row quarter); item = (loop, 16-row k-step)
+    // ---- online softmax in registers, then PV over every loop
     {
-      const int grp = warp >> 2, rq = warp & 3;
-      const float al0 = S.alpha[2 * q], al1 = S.alpha[2 * q + 1];
+      float mt0 = Gs.red[0][2 * q], mt1 = Gs.red[0][2 * q + 1];
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int ww = 1; ww < kGroupWarps; ++ww) {
+        mt0 = fmaxf(mt0, Gs.red[ww][2 * q]);
+        mt1 = fmaxf(mt1, Gs.red[ww][2 * q + 1]);
+      }
+      const float mn0 = fmaxf(U.m[0], mt0), mn1 = fmaxf(U.m[1], mt1);
+      const float al0 = (U.m[0] == -INFINITY) ? 0.f : exp2f(U.m[0] - mn0);
+      const float al1 = (U.m[1] == -INFINITY) ? 0.f : exp2f(U.m[1] - mn1);
+      U.m[0] = mn0;
+      U.m[1] = mn1;
+      float p[4];
+      p[0] = sv[0] == -INFINITY ? 0.f : exp2f(sv[0] - mn0);
+      p[1] = sv[1] == -INFINITY ? 0.f : exp2f(sv[1] - mn1);
+      p[2] = sv[2] == -INFINITY ? 0.f : exp2f(sv[2] - mn0);
+      p[3] = sv[3] == -INFINITY ? 0.f : exp2f(sv[3] - mn1);
+      U.l[0] = U.l[0] * al0 + (p[0] + p[2]);
+      U.l[1] = U.l[1] * al1 + (p[1] + p[3]);
+#pragma unroll
+      for (int vg = 0; vg < 2; ++vg) {
+        U.vb[vg][0] *= al0;
+        U.vb[vg][1] *= al1;
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
         U.acc[mt][0] *= al0;
         U.acc[mt][1] *= al1;
         U.acc[mt][2] *= al0;
         U.acc[mt][3] *= al1;
       }
-      int item = 0;
-      for (int j = 0; j < depth; ++j) {
-        const int nks = (M.loop[j].nrows + 15) >> 4;
-        for (int ks = 0; ks < nks; ++ks, ++item) {
-          if ((item & 3) != rq) continue;
-          const uint8_t* base = &st.vc[j][(16 * ks) * kRowBytes + 4 * (8 * grp + g)];
-          const uint32_t wa = *reinterpret_cast<const uint32_t*>(base + (q)*kRowBytes);
-          const uint32_t wb = *reinterpret_cast<const uint32_t*>(base + (q + 4) * kRowBytes);
-          const uint32_t wc = *reinterpret_cast<const uint32_t*>(base + (q + 8) * kRowBytes);
-          const uint32_t wd = *reinterpret_cast<const uint32_t*>(base + (q + 12) * kRowBytes);
-          const uint2 bp = *reinterpret_cast<const uint2*>(&S.pp[j][grp][ks][g][4 * q]);
-          const uint32_t xab[2] = {__byte_perm(wa, wb, 0x5410), __byte_perm(wa, wb, 0x7632)};
-          const uint32_t xcd[2] = {__byte_perm(wc, wd, 0x5410), __byte_perm(wc, wd, 0x7632)};
+      for (int j = 0; j < DEPTH; ++j) {
+        const SliceInfo si = Gs.slice[w][j];
+        if (si.cnt == 0) continue;
+        const int vrem = st.meta[16 + 8 * j + 4];
+        const int sparse = st.meta[16 + 8 * j + 6];
+        // p of the slice's stored rows g and g + 8 (zero past cnt)
+        float pr[4];
 #pragma unroll
-          for (int hbyte = 0; hbyte < 2; ++hbyte) {
-#pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-              const int mt = 2 * hbyte + sub;
-              const uint32_t x1 = sub ? (xab[hbyte] >> 8) : xab[hbyte];
-              const uint32_t x2 = sub ? (xcd[hbyte] >> 8) : xcd[hbyte];
-              uint32_t A[4];
-              A[0] = h2_sub1024(lop3_and_or(x1, 0x000F000Fu, 0x64006400u));
-              A[1] = h2_hi_nibble(lop3_and_or(x1, 0x00F000F0u, 0x64006400u));
-              A[2] = h2_sub1024(lop3_and_or(x2, 0x000F000Fu, 0x64006400u));
-              A[3] = h2_hi_nibble(lop3_and_or(x2, 0x00F000F0u, 0x64006400u));
-              mma16816(U.acc[mt], A, bp.x, bp.y);
+        for (int half = 0; half < 2; ++half) {
+          const int row = g + 8 * half;
+          if (!sparse) {
+            pr[2 * half] = p[2 * half];
+            pr[2 * half + 1] = p[2 * half + 1];
+          } else {
+            // token of the row-th present bit
+            int tok = 0;
+            {
+              uint32_t bb = uint32_t(si.bits);
+              for (int r = 0; r < row && bb; ++r) bb &= bb - 1;
+              tok = bb ? __ffs(bb) - 1 : 0;
             }
+            const int src = ((tok & 7) << 2) | q;
+            const float a0 = __shfl_sync(0xffffffffu, p[0], src), a1 = __shfl_sync(0xffffffffu, p[1], src);
+            const float a2 = __shfl_sync(0xffffffffu, p[2], src), a3 = __shfl_sync(0xffffffffu, p[3], src);
+            const float y0 = tok < 8 ? a0 : a2;
+            const float y1 = tok < 8 ? a1 : a3;
+            const bool ok = row < si.cnt;
+            pr[2 * half] = ok ? y0 : 0.f;
+            pr[2 * half + 1] = ok ? y1 : 0.f;
+          }
+        }
+        // P' = p * sV per V group, and the V-min terms
+        uint32_t r[2][2];  // [V group][row half] = {P'(row, 2q), P'(row, 2q+1)}
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int row = g + 8 * half;
+          const bool ok = row < si.cnt;
+          const int vi = vrem + 2 * (si.rb + row);
+          const uint32_t sraw = ok ? *reinterpret_cast<const uint32_t*>(&st.vsc[j][vi]) : 0u;
+          const uint32_t mraw = ok ? *reinterpret_cast<const uint32_t*>(&st.vmin[j][vi]) : 0u;
+          const __half2 pp = __floats2half2_rn(pr[2 * half], pr[2 * half + 1]);
+          const __half2 sv2 = u2h(sraw);
+          const float2 mv = __half22float2(u2h(mraw));
+#pragma unroll
+          for (int vg = 0; vg < 2; ++vg) {
+            const __half2 sg = vg == 0 ? __low2half2(sv2) : __high2half2(sv2);
+            const __half2 pv = __hmul2(pp, sg);
+            r[vg][half] = h2u(pv);
+            const float2 pf = __half22float2(pv);
+            const float mg = vg == 0 ? mv.x : mv.y;
+            U.vb[vg][0] = fmaf(pr[2 * half], mg, fmaf(-64.f, pf.x, U.vb[vg][0]));
+            U.vb[vg][1] = fmaf(pr[2 * half + 1], mg, fmaf(-64.f, pf.y, U.vb[vg][1]));
+          }
+        }
+        // B operands (k = rows, n = heads) by 8x8 transposes of the (row, head) blocks
+        const uint32_t B00 = transpose8x8(r[0][0]), B01 = transpose8x8(r[0][1]);
+        const uint32_t B10 = transpose8x8(r[1][0]), B11 = transpose8x8(r[1][1]);
+        // A: V codes of staged rows rb + {2q, 2q+1, 2q+8, 2q+9}; thread g takes word
+        // 8*vg + g of each row (channels 64vg + 8g .. +7)
+        const uint8_t* base = &st.vc[j][si.rb * kRowBytes];
+        uint32_t wv[2][4];
+#pragma unroll
+        for (int vg = 0; vg < 2; ++vg) {
+          wv[vg][0] = *reinterpret_cast<const uint32_t*>(base + (2 * q) * kRowBytes + 4 * (8 * vg + g));
+          wv[vg][1] = *reinterpret_cast<const uint32_t*>(base + (2 * q + 1) * kRowBytes + 4 * (8 * vg + g));
+          wv[vg][2] = *reinterpret_cast<const uint32_t*>(base + (2 * q + 8) * kRowBytes + 4 * (8 * vg + g));
+          wv[vg][3] = *reinterpret_cast<const uint32_t*>(base + (2 * q + 9) * kRowBytes + 4 * (8 * vg + g));
+        }
+#pragma unroll
+        for (int vg = 0; vg < 2; ++vg) {
+          const uint32_t b0 = vg == 0 ? B00 : B10, b1 = vg == 0 ? B01 : B11;
+          const uint32_t x[2] = {__byte_perm(wv[vg][0], wv[vg][1], 0x5410), __byte_perm(wv[vg][0], wv[vg][1], 0x7632)};
+          const uint32_t y[2] = {__byte_perm(wv[vg][2], wv[vg][3], 0x5410), __byte_perm(wv[vg][2], wv[vg][3], 0x7632)};
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const uint32_t A0[4] = {nib(x[hb] << 4), nib(x[hb]), nib(y[hb] << 4), nib(y[hb])};
+            const uint32_t A1[4] = {nib(x[hb] >> 4), nib(x[hb] >> 8), nib(y[hb] >> 4), nib(y[hb] >> 8)};
+            mma16816(U.acc[4 * vg + 2 * hb], A0, b0, b1);
+            mma16816(U.acc[4 * vg + 2 * hb + 1], A1, b0, b1);
           }
         }
       }
     }
-    // release the stage: every consumer warp is done reading it
+    // release the stage: every warp of the group is done reading it
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[s]);
   }
-  if (cur_unit >= 0) finish_unit(a, S, U, Mprev, warp, lane);
+  if (cur_unit >= 0) finish_unit(a, Gs, U, Mprev, grp, vcta, w, lane);
 }
 
+template <int DEPTH>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
-  const int C = a.n_ctas;
+  const int C = a.n_ctas;  // virtual CTAs: two per block
   const long long W = a.prefix[a.n_requests];
-  const long long s0 = cta_start(blockIdx.x, W, C), e0 = cta_start(blockIdx.x + 1, W, C);
-  if (s0 >= e0) return;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&S.full[i], 1);
-      mbar_init(&S.empty[i], kConsumerWarps);
+      mbar_init(&S.empty[i], kGroupWarps);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // P' rows of heads past the group size stay zero for the whole kernel
-  for (int i = threadIdx.x; i < int(sizeof(S.pp) / 4); i += blockDim.x) reinterpret_cast<uint32_t*>(S.pp)[i] = 0u;
   __syncthreads();
-  if (threadIdx.x >= kConsumers) {
-    if (threadIdx.x == kConsumers) producer(a, S, s0, e0);
+  int grp;
+  bool producer_warp;
+  if (threadIdx.x < kConsumers) {
+    grp = threadIdx.x / kGroupThreads;
+    producer_warp = false;
+  } else {
+    grp = (threadIdx.x - kConsumers) >> 5;
+    producer_warp = true;
+  }
+  const int vcta = kGroups * blockIdx.x + grp;
+  const long long s0 = cta_start(vcta, W, C), e0 = cta_start(vcta + 1, W, C);
+  if (s0 >= e0) return;
+  if (producer_warp) {
+    if ((threadIdx.x & 31) == 0) producer<DEPTH>(a, S, grp, s0, e0);
     return;
   }
-  consumer(a, S, s0, e0);
+  consumer<DEPTH>(a, S, grp, vcta, s0, e0);
+}
+
+template <int DEPTH>
+cudaError_t launch_depth(const AttnArgs& a, cudaStream_t stream) {
+  const int smem = int(sizeof(Smem));
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<DEPTH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  attn_mma_kernel<DEPTH><<<a.n_ctas / kGroups, kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace mma_attn
 
+int mma_virtual_ctas_per_block() { return mma_attn::kGroups; }
+
 cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {
   using namespace mma_attn;
-  const int smem = int(sizeof(Smem));
-  static int configured = 0;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = 1;
+  cudaError_t e;
+  switch (a.depth) {
+    case 1: e = launch_depth<1>(a, stream); break;
+    case 2: e = launch_depth<2>(a, stream); break;
+    case 3: e = launch_depth<3>(a, stream); break;
+    case 4: e = launch_depth<4>(a, stream); break;
+    default: return cudaErrorInvalidValue;
   }
-  attn_mma_kernel<<<a.n_ctas, kThreads, smem, stream>>>(a);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace kvq
