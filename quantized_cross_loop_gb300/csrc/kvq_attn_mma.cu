@@ -33,8 +33,9 @@
 //                   channels as M. A sparse loop contributes over its compact
 //                   rows only; rows and tokens are matched through a 64-bit
 //                   presence mask of the tile and warp shuffles.
-// Per tile and group: two named barriers (K-min terms ready; max exchange).
-// Softmax is online over tiles in the log2 domain, FP32 throughout.
+// Each warp keeps its own online softmax (max, sum, PV accumulators) over its
+// tokens; the group merges the four at the end of a unit. Per tile and group:
+// one named barrier (K-min terms ready). Log2 domain, FP32 throughout.
 #include <cuda_fp16.h>
 
 #include "kvq_attn_common.cuh"
@@ -80,8 +81,10 @@ struct SliceInfo {
 
 struct GroupSmem {
   __half q16[8][kD];                     // query of the current unit (BF16 values, exact in FP16)
-  float kbias[kMaxPairs][8];             // sum_d q*mK - 64 sum_d q*sK per (pair, head)
-  float red[kGroupWarps][8];             // per-warp max per head
+  // sum_d q*mK - 64 sum_d q*sK per (pair, head), double-buffered by tile parity:
+  // warp 0 writes the next tile's terms while other warps may still read these
+  float kbias[2][kMaxPairs][8];
+  float red[kGroupWarps][8];             // per-warp running max per head (unit-end merge)
   float lsum[kGroupWarps][8];
   float vbs[kGroupWarps][2][8];
   SliceInfo slice[kGroupWarps][kLoops];
@@ -311,7 +314,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
 // ---------------------------------------------------------------- consumers
 
 struct UnitState {
-  float m[2];       // running max of heads 2q, 2q+1 (log2 units)
+  float m[2];       // this warp's running max of heads 2q, 2q+1 (log2 units)
   float l[2];       // partial sums of exp2 of this thread's tokens for heads 2q, 2q+1
   float vb[2][2];   // partial V-min terms (with the -64 offset correction): [V group][head 2q / 2q+1]
   float acc[8][4];  // PV accumulators: 8 channel m-tiles x (2 rows x 2 heads)
@@ -331,12 +334,26 @@ __device__ void load_unit_query(const AttnArgs& a, GroupSmem& G, int b, int h, i
 }
 
 // Writes the unit's result: output rows (whole unit) or the group's partial slot.
+// The four warps' online-softmax states are merged: each warp rescales its sums
+// by exp2(m_warp - m_group) before they are added.
 __device__ void finish_unit(const AttnArgs& a, GroupSmem& G, UnitState& U, const UnitInfo& M, int grp, int vcta,
                             int w, int lane) {
   const int gt = w * 32 + lane;
   const int g = lane >> 2, q = lane & 3;
-  float l0 = U.l[0], l1 = U.l[1];
-  float v00 = U.vb[0][0], v01 = U.vb[0][1], v10 = U.vb[1][0], v11 = U.vb[1][1];
+  if (g == 0) {
+    G.red[w][2 * q] = U.m[0];
+    G.red[w][2 * q + 1] = U.m[1];
+  }
+  group_sync(grp);
+  float mg[2], sc[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int hh = 2 * q + e;
+    mg[e] = fmaxf(fmaxf(G.red[0][hh], G.red[1][hh]), fmaxf(G.red[2][hh], G.red[3][hh]));
+    sc[e] = (mg[e] == -INFINITY || U.m[e] == -INFINITY) ? 0.f : exp2f(U.m[e] - mg[e]);
+  }
+  float l0 = U.l[0] * sc[0], l1 = U.l[1] * sc[1];
+  float v00 = U.vb[0][0] * sc[0], v01 = U.vb[0][1] * sc[1], v10 = U.vb[1][0] * sc[0], v11 = U.vb[1][1] * sc[1];
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -360,27 +377,26 @@ __device__ void finish_unit(const AttnArgs& a, GroupSmem& G, UnitState& U, const
     for (int mt = 0; mt < 4; ++mt) {
       const int ch = 64 * vg + 8 * g + 2 * mt;
       const float* c = U.acc[4 * vg + mt];
-      *reinterpret_cast<float2*>(&G.fin[w][ch][2 * q]) = make_float2(c[0], c[1]);
-      *reinterpret_cast<float2*>(&G.fin[w][ch + 1][2 * q]) = make_float2(c[2], c[3]);
+      *reinterpret_cast<float2*>(&G.fin[w][ch][2 * q]) = make_float2(c[0] * sc[0], c[1] * sc[1]);
+      *reinterpret_cast<float2*>(&G.fin[w][ch + 1][2 * q]) = make_float2(c[2] * sc[0], c[3] * sc[1]);
     }
   group_sync(grp);
   const int gq = a.g;
   float* slot = a.partials + (size_t)(vcta + M.unit) * kSlotFloats;
   for (int i = gt; i < gq * kD; i += kGroupThreads) {
-    const int hh = i / kD, d = i % kD;
+    const int hh = i / kD, d = i % kD, vg = d >> 6;
     const float lt = G.lsum[0][hh] + G.lsum[1][hh] + G.lsum[2][hh] + G.lsum[3][hh];
-    const float vb = G.vbs[0][d >> 6][hh] + G.vbs[1][d >> 6][hh] + G.vbs[2][d >> 6][hh] + G.vbs[3][d >> 6][hh];
+    const float vb = G.vbs[0][vg][hh] + G.vbs[1][vg][hh] + G.vbs[2][vg][hh] + G.vbs[3][vg][hh];
     const float o = (G.fin[0][d][hh] + G.fin[1][d][hh]) + (G.fin[2][d][hh] + G.fin[3][d][hh]) + vb;
     if (M.whole) {
       a.out[((long long)M.b * a.Hq + (long long)M.h * gq + hh) * kD + d] = o / lt;
     } else {
       slot[2 * kMaxG + hh * kD + d] = o;
-      if (d == 0) slot[kMaxG + hh] = lt;
+      if (d == 0) {
+        slot[kMaxG + hh] = lt;
+        slot[hh] = fmaxf(fmaxf(G.red[0][hh], G.red[1][hh]), fmaxf(G.red[2][hh], G.red[3][hh]));
+      }
     }
-  }
-  if (!M.whole && w == 0 && g == 0) {  // the running max is the same in every thread
-    if (2 * q < gq) slot[2 * q] = U.m[0];
-    if (2 * q + 1 < gq) slot[2 * q + 1] = U.m[1];
   }
   group_sync(grp);
 }
@@ -493,7 +509,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&Gs.q16[g][16 * kk + 2 * q + 8]);
         mma16816(c, av, b0, b1);
       }
-      if (live) *reinterpret_cast<float2*>(&Gs.kbias[g][2 * q]) = make_float2(c[0] + c[2], c[1] + c[3]);
+      if (live) *reinterpret_cast<float2*>(&Gs.kbias[it & 1][g][2 * q]) = make_float2(c[0] + c[2], c[1] + c[3]);
     }
 
     // ---- QK^T of the warp's 16 tokens [16w, 16w + 16) over every loop
@@ -504,7 +520,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
     for (int j = 0; j < DEPTH; ++j) {
       const int4 la = *reinterpret_cast<const int4*>(&st.meta[16 + 8 * j]);
       const int4 lb = *reinterpret_cast<const int4*>(&st.meta[20 + 8 * j]);
-      const int c0 = la.y, g0 = la.z, ngrp = la.w, irem = lb.y, sparse = lb.z, pbase = lb.w;
+      const int c0 = la.y, g0 = la.z, ngrp = la.w, irem = lb.y, sparse = lb.z;
       int rb, cnt, bits;
       if (!sparse) {
         rb = 16 * w;
@@ -572,7 +588,8 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
     }
     group_sync(grp);  // K-min terms and slice info visible
 
-    // ---- logits in log2 units, tile max per head across the group
+    // ---- logits in log2 units and this warp's max per head
+    float mt0, mt1;
     {
 #pragma unroll
       for (int j = 0; j < DEPTH; ++j) {
@@ -581,7 +598,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         for (int half = 0; half < 2; ++half) {
           const uint32_t f = (pinfo >> (4 * j + 2 * half)) & 3u;
           if (f & 1u) {
-            const float2 kb = *reinterpret_cast<const float2*>(&Gs.kbias[pbase + int(f >> 1)][2 * q]);
+            const float2 kb = *reinterpret_cast<const float2*>(&Gs.kbias[it & 1][pbase + int(f >> 1)][2 * q]);
             sv[2 * half] += kb.x;
             sv[2 * half + 1] += kb.y;
           }
@@ -593,27 +610,17 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       sv[1] = (t0ok && h1ok) ? sv[1] * lsc : -INFINITY;
       sv[2] = (t1ok && h0ok) ? sv[2] * lsc : -INFINITY;
       sv[3] = (t1ok && h1ok) ? sv[3] * lsc : -INFINITY;
-      float m0v = fmaxf(sv[0], sv[2]), m1v = fmaxf(sv[1], sv[3]);
+      mt0 = fmaxf(sv[0], sv[2]);
+      mt1 = fmaxf(sv[1], sv[3]);
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        m0v = fmaxf(m0v, __shfl_xor_sync(0xffffffffu, m0v, off));
-        m1v = fmaxf(m1v, __shfl_xor_sync(0xffffffffu, m1v, off));
-      }
-      if (g == 0) {
-        Gs.red[w][2 * q] = m0v;
-        Gs.red[w][2 * q + 1] = m1v;
+      for (int off = 4; off < 32; off <<= 1) {  // this warp's 16 tokens
+        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, off));
+        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, off));
       }
     }
-    group_sync(grp);
 
-    // ---- online softmax in registers, then PV over every loop
+    // ---- online softmax of the warp in registers, then PV over every loop
     {
-      float mt0 = Gs.red[0][2 * q], mt1 = Gs.red[0][2 * q + 1];
-#pragma unroll
-      for (int ww = 1; ww < kGroupWarps; ++ww) {
-        mt0 = fmaxf(mt0, Gs.red[ww][2 * q]);
-        mt1 = fmaxf(mt1, Gs.red[ww][2 * q + 1]);
-      }
       const float mn0 = fmaxf(U.m[0], mt0), mn1 = fmaxf(U.m[1], mt1);
       const float al0 = (U.m[0] == -INFINITY) ? 0.f : exp2f(U.m[0] - mn0);
       const float al1 = (U.m[1] == -INFINITY) ? 0.f : exp2f(U.m[1] - mn1);
