@@ -48,6 +48,10 @@ __device__ __forceinline__ int items_of(const CodecArgs& a, const kvq_request& R
       if (a.loop >= R.n_loops || R.loop[a.loop].active_idx == nullptr) return 0;
       return (R.n_tokens + KVQ_TILE - 1) / KVQ_TILE + 1;
     }
+    case kModeReconK: {  // one item per (64-token tile, head)
+      if (a.loop > R.n_loops) return 0;
+      return ((R.n_tokens + KVQ_TILE - 1) / KVQ_TILE) * a.H;
+    }
     default: {  // kModeRecon
       if (a.loop > R.n_loops) return 0;
       return (R.n_tokens + KVQ_TILE - 1) / KVQ_TILE;
@@ -145,9 +149,14 @@ __device__ __forceinline__ const uint16_t* source_of(const CodecArgs& a, int b) 
   return a.reqs ? a.x[b] : a.one_x;
 }
 
-// ---------------------------------------------------------------- encode K
+// ---------------------------------------------------------------- generic kernels (any depth)
+//
+// One element (or four) at a time with the scalar helpers of kvq_internal.cuh;
+// used for chains deeper than the fast kernels below are instantiated for.
 
-__global__ void __launch_bounds__(kD) encode_k_kernel(const __grid_constant__ CodecArgs a, const int32_t* prefix_ws) {
+// ---------------------------------------------------------------- encode K (generic)
+
+__global__ void __launch_bounds__(kD) encode_k_generic_kernel(const __grid_constant__ CodecArgs a, const int32_t* prefix_ws) {
   const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
   const int d = threadIdx.x;
   const int H = a.H;
@@ -230,7 +239,7 @@ __global__ void __launch_bounds__(kD) encode_k_kernel(const __grid_constant__ Co
 
 constexpr int kEncVThreads = 256;
 
-__global__ void __launch_bounds__(kEncVThreads) encode_v_kernel(const __grid_constant__ CodecArgs a,
+__global__ void __launch_bounds__(kEncVThreads) encode_v_generic_kernel(const __grid_constant__ CodecArgs a,
                                                                 const int32_t* prefix_ws) {
   const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -343,7 +352,7 @@ __global__ void __launch_bounds__(256) tile_dir_kernel(const __grid_constant__ C
 
 constexpr int kReconThreads = 256;
 
-__global__ void __launch_bounds__(kReconThreads) reconstruct_kernel(const __grid_constant__ CodecArgs a,
+__global__ void __launch_bounds__(kReconThreads) reconstruct_generic_kernel(const __grid_constant__ CodecArgs a,
                                                                     const int32_t* prefix_ws) {
   const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -404,6 +413,565 @@ __global__ void __launch_bounds__(kReconThreads) reconstruct_kernel(const __grid
   }
 }
 
+// ---------------------------------------------------------------- fast kernels (chains of up to 4 loops)
+
+constexpr int kFastMaxDepth = 4;  // deepest chain the fast kernels are instantiated for
+//
+// The same arithmetic as the generic kernels, two channels at a time:
+//  - decode RN_bf16(min + scale * c) takes one FP32 FMA per channel: scale * c
+//    is exact (an FP16 significand times a 4-bit code), so the FMA rounds once
+//    exactly where the generic code rounds the sum; the pair is then converted
+//    to BF16 in one instruction;
+//  - the chain add and the residual subtraction run on BF16 pairs with a single
+//    rounding (add.rn.bf16x2 / sub.rn.bf16x2). For BF16 operands that equals
+//    rounding the FP32 result to BF16: the exact sum of two BF16 values fits in
+//    FP32 unless their exponents differ by more than 15, and then both
+//    roundings return the larger operand;
+//  - a code is rint(d * RN32(1 / scale)) instead of rint(RN32(d / scale)). The
+//    two quotients differ by less than 1.5 ulp of 16 (2.9e-6), so their
+//    rounding to an integer agrees unless the product lies within 4e-6 of a
+//    half-integer; such elements, and non-finite products, take the IEEE
+//    division of the generic path;
+//  - min and max come from BF16 pair min/max; when a group's min or max is
+//    zero its sign is re-taken from the first zero in scan order, which is the
+//    one the in-order scan keeps.
+namespace fast {
+
+constexpr float kMagic23 = 8388608.0f;         // 2^23: x + 2^23 rounds x in [0, 2^23) to an integer
+constexpr float kTieWindow = 0.5f - 4.0e-6f;  // |y - rint(y)| above this: exact division
+
+__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf2_min(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// {RN_bf16(v.x), RN_bf16(v.y)} with v.x in the low half
+__device__ __forceinline__ uint32_t f2_to_bf2(float2 v) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(v.y), "f"(v.x));
+  return d;
+}
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t v) { return make_float2(bf_lo(v), bf_hi(v)); }
+__device__ __forceinline__ float2 f16x2_to_f2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+__device__ __forceinline__ uint32_t f16_pair(float lo, float hi) {
+  return uint32_t(f32_to_f16_bits(lo)) | (uint32_t(f32_to_f16_bits(hi)) << 16);
+}
+
+// One codes byte (low nibble = even channel) -> the BF16 pair of decodes,
+// with the FP32 min m and scale s of each channel.
+__device__ __forceinline__ uint32_t dequant_byte(uint32_t byte, float2 m, float2 s) {
+  const float2 c = __fadd2_rn(make_float2(__uint_as_float((byte & 0xFu) | 0x4B000000u),
+                                          __uint_as_float((byte >> 4) | 0x4B000000u)),
+                              make_float2(-kMagic23, -kMagic23));
+  return f2_to_bf2(__ffma2_rn(s, c, m));
+}
+
+// One codes word (byte k = channels 2k, 2k+1) -> four BF16 pairs, one min and
+// scale for all eight channels.
+__device__ __forceinline__ void dequant_word(uint32_t w, float2 m, float2 s, uint32_t* out) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 c = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440 + k)),
+                                            __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440 + k))),
+                                make_float2(-kMagic23, -kMagic23));
+    out[k] = f2_to_bf2(__ffma2_rn(s, c, m));
+  }
+}
+
+// Codes of a BF16 pair against the FP32 min, scale and RN32(1 / scale) of each
+// channel (reciprocal 0 for a constant group): code(lo) | code(hi) << 4.
+__device__ __forceinline__ uint32_t quant_pair(uint32_t v, float2 mn, float2 rc, float2 s32) {
+  const float2 x = bf2_to_f2(v);
+  const float2 y = __fmul2_rn(__fadd2_rn(x, make_float2(-mn.x, -mn.y)), rc);
+  const float2 z = __fadd2_rn(y, make_float2(kMagic23, kMagic23));
+  const float2 e = __ffma2_rn(__fadd2_rn(z, make_float2(-kMagic23, -kMagic23)), make_float2(-1.0f, -1.0f), y);
+  uint32_t code = (__float_as_uint(z.x) & 0xFu) | ((__float_as_uint(z.y) & 0xFu) << 4);
+  if (!(fabsf(e.x) <= kTieWindow && fabsf(e.y) <= kTieWindow))
+    code = uint32_t(quantize(x.x, mn.x, s32.x)) | (uint32_t(quantize(x.y, mn.y, s32.y)) << 4);
+  return code;
+}
+
+__device__ __forceinline__ float scale_of(float mn, float mx) {
+  return (mx != mn) ? __fdiv_rn(__fsub_rn(mx, mn), 15.0f) : 0.0f;
+}
+__device__ __forceinline__ float recip_of(float s32) { return s32 != 0.0f ? __frcp_rn(s32) : 0.0f; }
+
+}  // namespace fast
+
+// ---------------------------------------------------------------- encode K (fast)
+//
+// item = (64-row compact group, head); thread p = channel pair 2p, 2p+1. The
+// thread keeps the group's 64 residual pairs in registers, so min/max is an
+// in-order scan over rows and the codes of row i are one byte of a 64-byte row
+// (a warp stores 32 consecutive bytes). The K parameters of a predecessor
+// loop are reloaded only when the stored row crosses into another group.
+
+template <int R>
+__global__ void __launch_bounds__(kG) encode_k_fast_kernel(const __grid_constant__ CodecArgs a,
+                                                           const int32_t* prefix_ws) {
+  using namespace fast;
+  constexpr int RA = R > 0 ? R : 1;
+  const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
+  const int p = threadIdx.x;
+  const int H = a.H;
+  __shared__ Chain C;  // C.loop[0..R-1]: predecessor chain; C.loop[R]: output planes
+  __shared__ int s_tok[kG];
+  __shared__ int s_row[RA][kG];
+  __shared__ int s_b;
+
+  const ItemRange ir = cta_items(prefix, a.n_requests);
+  int cur_b = -1;
+  for (long long it = ir.begin; it < ir.end; ++it) {
+    if (p == 0) s_b = owner_of(prefix, a.n_requests, it);
+    __syncthreads();
+    const int b = s_b;
+    if (b != cur_b) {
+      if (p == 0) fill_chain(req_at(a, b), KVQ_K, R + 1, H, C);
+      cur_b = b;
+    }
+    __syncthreads();
+    const int local = int(it - prefix[b]);
+    const int g = local / H, h = local % H;
+    const LoopPlanes& O = C.loop[R];
+    const int n = O.n_rows;
+    const int r0 = g * kG;
+    const int len = min(kG, n - r0);
+    const uint16_t* x = source_of(a, b);
+    if (p < len) {
+      const int t = O.sparse ? __ldg(O.active + r0 + p) : r0 + p;
+      s_tok[p] = t;
+#pragma unroll
+      for (int j = 0; j < R; ++j) s_row[j][p] = row_of(C.loop[j], t);
+    }
+    __syncthreads();
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) {  // batch source not 16-byte aligned: skip
+      if (p == 0 && a.err) atomicOr(a.err, 16);
+      continue;
+    }
+    const uint32_t* xw = reinterpret_cast<const uint32_t*>(x);
+
+    float2 pm[RA], ps[RA];
+    int pg[RA];
+#pragma unroll
+    for (int j = 0; j < RA; ++j) {
+      pg[j] = -1;
+      pm[j] = ps[j] = make_float2(0.0f, 0.0f);
+    }
+    uint32_t v[kG];
+    uint32_t mn2 = 0, mx2 = 0;
+#pragma unroll
+    for (int i = 0; i < kG; ++i) {
+      v[i] = 0;
+      if (i < len) {
+        const int t = s_tok[i];
+        const uint32_t xv = __ldg(xw + ((long long)t * H + h) * (kD / 2) + p);
+        uint32_t d = xv;
+        if (R > 0) {
+          uint32_t acc = 0;
+#pragma unroll
+          for (int j = 0; j < R; ++j) {
+            const int row = s_row[j][i];
+            if (row < 0) continue;  // absent: inherit the predecessor
+            const LoopPlanes& L = C.loop[j];
+            if ((row >> 6) != pg[j]) {
+              pg[j] = row >> 6;
+              const long long pi = ((long long)h * ((L.n_rows + kG - 1) / kG) + pg[j]) * kD + 2 * p;
+              pm[j] = f16x2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(L.mins + pi)));
+              ps[j] = f16x2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(L.scales + pi)));
+            }
+            const uint32_t byte = __ldg(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + p);
+            const uint32_t dq = dequant_byte(byte, pm[j], ps[j]);
+            acc = (j == 0) ? dq : bf2_add(acc, dq);
+          }
+          d = bf2_sub(xv, acc);
+        }
+        v[i] = d;
+        mn2 = (i == 0) ? d : bf2_min(mn2, d);
+        mx2 = (i == 0) ? d : bf2_max(mx2, d);
+      }
+    }
+    float mn[2] = {bf_lo(mn2), bf_hi(mn2)}, mx[2] = {bf_lo(mx2), bf_hi(mx2)};
+    if (mn[0] == 0.0f || mn[1] == 0.0f || mx[0] == 0.0f || mx[1] == 0.0f) {
+      bool done[4] = {mn[0] != 0.0f, mn[1] != 0.0f, mx[0] != 0.0f, mx[1] != 0.0f};
+#pragma unroll 1
+      for (int i = 0; i < len; ++i) {
+        uint32_t vi = 0;
+#pragma unroll
+        for (int k = 0; k < kG; ++k)
+          if (k == i) vi = v[k];
+        const float lo = bf_lo(vi), hi = bf_hi(vi);
+        if (!done[0] && lo == 0.0f) { mn[0] = lo; done[0] = true; }
+        if (!done[2] && lo == 0.0f) { mx[0] = lo; done[2] = true; }
+        if (!done[1] && hi == 0.0f) { mn[1] = hi; done[1] = true; }
+        if (!done[3] && hi == 0.0f) { mx[1] = hi; done[3] = true; }
+      }
+    }
+    const float s0 = scale_of(mn[0], mx[0]), s1 = scale_of(mn[1], mx[1]);
+    const float2 mnv = make_float2(mn[0], mn[1]), sv = make_float2(s0, s1);
+    const float2 rc = make_float2(recip_of(s0), recip_of(s1));
+    uint8_t* dst = const_cast<uint8_t*>(O.codes) + ((long long)h * n + r0) * kRowBytes + p;
+#pragma unroll
+    for (int i = 0; i < kG; ++i)
+      if (i < len) dst[(long long)i * kRowBytes] = uint8_t(quant_pair(v[i], mnv, rc, sv));
+    const long long pi = ((long long)h * ((n + kG - 1) / kG) + g) * kD + 2 * p;
+    *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.mins) + pi) = f16_pair(mn[0], mn[1]);
+    *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.scales) + pi) = f16_pair(s0, s1);
+  }
+}
+
+// ---------------------------------------------------------------- encode V (fast)
+//
+// item = 64 stored rows (all heads). Eight lanes cover one (row, head): lane
+// `sub` holds channels 16 sub .. 16 sub + 15, four lanes one V group; a warp
+// takes four consecutive rows of one head, so the codes (4 x 64 B), the
+// parameters (4 x 4 B) and each source row (256 B) are contiguous. Every load
+// of a (row, head) is issued before its arithmetic.
+
+constexpr int kEncVFastThreads = 256;
+
+template <int R>
+__global__ void __launch_bounds__(kEncVFastThreads) encode_v_fast_kernel(const __grid_constant__ CodecArgs a,
+                                                                         const int32_t* prefix_ws) {
+  using namespace fast;
+  constexpr int RA = R > 0 ? R : 1;
+  constexpr int kWarps = kEncVFastThreads / 32;
+  const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane & 7, lg = lane >> 3;
+  const int H = a.H;
+  __shared__ Chain C;
+  __shared__ int s_tok[kG];
+  __shared__ int s_row[RA][kG];
+  __shared__ int s_b;
+
+  const ItemRange ir = cta_items(prefix, a.n_requests);
+  int cur_b = -1;
+  for (long long it = ir.begin; it < ir.end; ++it) {
+    if (threadIdx.x == 0) s_b = owner_of(prefix, a.n_requests, it);
+    __syncthreads();
+    const int b = s_b;
+    if (b != cur_b) {
+      if (threadIdx.x == 0) fill_chain(req_at(a, b), KVQ_V, R + 1, H, C);
+      cur_b = b;
+    }
+    __syncthreads();
+    const LoopPlanes& O = C.loop[R];
+    const int n = O.n_rows;
+    const int r0 = int(it - prefix[b]) * kG;
+    const int len = min(kG, n - r0);
+    const uint16_t* x = source_of(a, b);
+    if (threadIdx.x < len) {
+      const int t = O.sparse ? __ldg(O.active + r0 + threadIdx.x) : r0 + threadIdx.x;
+      s_tok[threadIdx.x] = t;
+#pragma unroll
+      for (int j = 0; j < R; ++j) s_row[j][threadIdx.x] = row_of(C.loop[j], t);
+    }
+    __syncthreads();
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) {
+      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 16);
+      continue;
+    }
+    const int nquads = H * (kG / 4);
+    for (int qd = warp; qd < nquads; qd += kWarps) {
+      const int h = qd / (kG / 4);
+      const int i = (qd % (kG / 4)) * 4 + lg;
+      const bool live = i < len;
+      uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+      uint2 cw[RA];
+      uint32_t m16[RA], s16[RA];
+      bool have[RA];
+#pragma unroll
+      for (int j = 0; j < RA; ++j) {
+        cw[j] = make_uint2(0, 0);
+        m16[j] = s16[j] = 0;
+        have[j] = false;
+      }
+      if (live) {
+        const int t = s_tok[i];
+        const uint4* src = reinterpret_cast<const uint4*>(x + ((long long)t * H + h) * kD + 16 * sub);
+        xa = __ldg(src);
+        xb = __ldg(src + 1);
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int row = s_row[j][i];
+          if (row >= 0) {
+            const LoopPlanes& L = C.loop[j];
+            const long long rr = (long long)h * L.n_rows + row;
+            cw[j] = __ldg(reinterpret_cast<const uint2*>(L.codes + rr * kRowBytes + 8 * sub));
+            m16[j] = __ldg(L.mins + rr * (kD / kG) + (sub >> 2));
+            s16[j] = __ldg(L.scales + rr * (kD / kG) + (sub >> 2));
+            have[j] = true;
+          }
+        }
+      }
+      uint32_t d[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      if (R > 0) {
+        uint32_t acc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = 0;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          if (!have[j]) continue;
+          const float mf = f16_bits_to_f32(uint16_t(m16[j])), sf = f16_bits_to_f32(uint16_t(s16[j]));
+          uint32_t dq[8];
+          dequant_word(cw[j].x, make_float2(mf, mf), make_float2(sf, sf), dq);
+          dequant_word(cw[j].y, make_float2(mf, mf), make_float2(sf, sf), dq + 4);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc[k] = (j == 0) ? dq[k] : bf2_add(acc[k], dq[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) d[k] = bf2_sub(d[k], acc[k]);
+      }
+      const uint32_t m2 = bf2_min(bf2_min(bf2_min(d[0], d[1]), bf2_min(d[2], d[3])),
+                                  bf2_min(bf2_min(d[4], d[5]), bf2_min(d[6], d[7])));
+      const uint32_t M2 = bf2_max(bf2_max(bf2_max(d[0], d[1]), bf2_max(d[2], d[3])),
+                                  bf2_max(bf2_max(d[4], d[5]), bf2_max(d[6], d[7])));
+      float mn = fminf(bf_lo(m2), bf_hi(m2)), mx = fmaxf(bf_lo(M2), bf_hi(M2));
+#pragma unroll
+      for (int off = 1; off <= 2; off <<= 1) {  // the four lanes of this V group
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      }
+      if (__any_sync(0xffffffffu, live && (mn == 0.0f || mx == 0.0f))) {
+        // the first zero of the group in channel order carries the sign the scan keeps
+        bool has = false;
+        float fz = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float lo = bf_lo(d[k]), hi = bf_hi(d[k]);
+          if (!has && lo == 0.0f) { has = true; fz = lo; }
+          if (!has && hi == 0.0f) { has = true; fz = hi; }
+        }
+        const unsigned ball = __ballot_sync(0xffffffffu, has);
+        const unsigned grp = ball & (0xFu << (lane & ~3));
+        const float first = __shfl_sync(0xffffffffu, fz, grp ? __ffs(grp) - 1 : lane);
+        if (mn == 0.0f) mn = first;
+        if (mx == 0.0f) mx = first;
+      }
+      const float s32 = scale_of(mn, mx);
+      const float2 mnv = make_float2(mn, mn), sv = make_float2(s32, s32);
+      const float rcs = recip_of(s32);
+      const float2 rc = make_float2(rcs, rcs);
+      uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w0 |= quant_pair(d[k], mnv, rc, sv) << (8 * k);
+        w1 |= quant_pair(d[4 + k], mnv, rc, sv) << (8 * k);
+      }
+      const uint32_t mp = f32_to_f16_bits(mn), sp = f32_to_f16_bits(s32);
+      const uint32_t mp1 = __shfl_down_sync(0xffffffffu, mp, 4), sp1 = __shfl_down_sync(0xffffffffu, sp, 4);
+      if (live) {
+        const long long rr = (long long)h * n + r0 + i;
+        *reinterpret_cast<uint2*>(const_cast<uint8_t*>(O.codes) + rr * kRowBytes + 8 * sub) = make_uint2(w0, w1);
+        if (sub == 0) {
+          *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.mins) + rr * (kD / kG)) = mp | (mp1 << 16);
+          *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.scales) + rr * (kD / kG)) = sp | (sp1 << 16);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- reconstruct (fast)
+//
+// Both kinds build, per 64-token tile, the stored row of every token in every
+// loop (-1: absent, inherit) from the tile directory.
+
+// Fills s_map[j][tt] for loops 0..depth-1 of tile k; returns false (and sets the
+// error bit) if a sparse loop's directory entry is inconsistent.
+__device__ __forceinline__ void build_tile_map(const CodecArgs& a, const Chain& C, int depth, int k, int nvalid,
+                                               int (*s_map)[KVQ_TILE]) {
+  const int t0 = k * KVQ_TILE;
+  for (int idx = threadIdx.x; idx < depth * KVQ_TILE; idx += blockDim.x) {
+    const int j = idx / KVQ_TILE, tt = idx % KVQ_TILE;
+    s_map[j][tt] = (C.loop[j].sparse || tt >= nvalid) ? -1 : t0 + tt;
+  }
+  __syncthreads();
+  for (int j = 1; j < depth; ++j) {
+    const LoopPlanes& L = C.loop[j];
+    if (!L.sparse) continue;
+    const int c0 = __ldg(L.tile_dir + k), c1 = __ldg(L.tile_dir + k + 1);
+    if (c0 < 0 || c1 > L.n_rows || c0 > c1 || c1 - c0 > KVQ_TILE) {
+      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 4);
+      continue;
+    }
+    for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
+      const int tt = __ldg(L.active + c) - t0;
+      if (tt >= 0 && tt < KVQ_TILE) s_map[j][tt] = c;
+      else if (a.err) atomicOr(a.err, 4);
+    }
+  }
+}
+
+// K: item = (64-token tile, head); thread p = channel pair. Parameters are
+// reloaded only when a loop's stored row crosses into another group.
+template <int DEPTH>
+__global__ void __launch_bounds__(kG) reconstruct_k_fast_kernel(const __grid_constant__ CodecArgs a,
+                                                                const int32_t* prefix_ws) {
+  using namespace fast;
+  const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
+  const int p = threadIdx.x;
+  const int H = a.H;
+  __shared__ Chain C;
+  __shared__ int s_map[DEPTH][KVQ_TILE];
+  __shared__ int s_b;
+
+  const ItemRange ir = cta_items(prefix, a.n_requests);
+  int cur_b = -1;
+  for (long long it = ir.begin; it < ir.end; ++it) {
+    if (p == 0) s_b = owner_of(prefix, a.n_requests, it);
+    __syncthreads();
+    const int b = s_b;
+    if (b != cur_b) {
+      if (p == 0) fill_chain(req_at(a, b), KVQ_K, DEPTH, H, C);
+      cur_b = b;
+    }
+    __syncthreads();
+    const int local = int(it - prefix[b]);
+    const int k = local / H, h = local % H;
+    const int t0 = k * KVQ_TILE;
+    const int nvalid = min(KVQ_TILE, C.n_tokens - t0);
+    build_tile_map(a, C, DEPTH, k, nvalid, s_map);
+    __syncthreads();
+    uint16_t* out = a.reqs ? a.out[b] : a.one_out;
+    if ((reinterpret_cast<uintptr_t>(out) & 15u) != 0) {
+      if (p == 0 && a.err) atomicOr(a.err, 16);
+      continue;
+    }
+    uint32_t* ow = reinterpret_cast<uint32_t*>(out) + ((long long)t0 * H + h) * (kD / 2) + p;
+    float2 pm[DEPTH], ps[DEPTH];
+    int pg[DEPTH];
+#pragma unroll
+    for (int j = 0; j < DEPTH; ++j) {
+      pg[j] = -1;
+      pm[j] = ps[j] = make_float2(0.0f, 0.0f);
+    }
+#pragma unroll 4
+    for (int tt = 0; tt < nvalid; ++tt) {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int j = 0; j < DEPTH; ++j) {
+        const int row = s_map[j][tt];
+        if (row < 0) continue;
+        const LoopPlanes& L = C.loop[j];
+        if ((row >> 6) != pg[j]) {
+          pg[j] = row >> 6;
+          const long long pi = ((long long)h * ((L.n_rows + kG - 1) / kG) + pg[j]) * kD + 2 * p;
+          pm[j] = f16x2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(L.mins + pi)));
+          ps[j] = f16x2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(L.scales + pi)));
+        }
+        const uint32_t byte = __ldg(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + p);
+        const uint32_t dq = dequant_byte(byte, pm[j], ps[j]);
+        acc = (j == 0) ? dq : bf2_add(acc, dq);
+      }
+      ow[(long long)tt * H * (kD / 2)] = acc;
+    }
+  }
+}
+
+// V: item = 64-token tile (all heads); eight lanes per (token, head), lane
+// `sub` = channels 16 sub .. +15; a warp takes four consecutive (token, head)
+// pairs, i.e. 1 KB of contiguous output.
+constexpr int kReconVFastThreads = 256;
+
+template <int DEPTH>
+__global__ void __launch_bounds__(kReconVFastThreads) reconstruct_v_fast_kernel(const __grid_constant__ CodecArgs a,
+                                                                                const int32_t* prefix_ws) {
+  using namespace fast;
+  constexpr int kWarps = kReconVFastThreads / 32;
+  const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane & 7, lg = lane >> 3;
+  const int H = a.H;
+  __shared__ Chain C;
+  __shared__ int s_map[DEPTH][KVQ_TILE];
+  __shared__ int s_b;
+
+  const ItemRange ir = cta_items(prefix, a.n_requests);
+  int cur_b = -1;
+  for (long long it = ir.begin; it < ir.end; ++it) {
+    if (threadIdx.x == 0) s_b = owner_of(prefix, a.n_requests, it);
+    __syncthreads();
+    const int b = s_b;
+    if (b != cur_b) {
+      if (threadIdx.x == 0) fill_chain(req_at(a, b), KVQ_V, DEPTH, H, C);
+      cur_b = b;
+    }
+    __syncthreads();
+    const int k = int(it - prefix[b]);
+    const int t0 = k * KVQ_TILE;
+    const int nvalid = min(KVQ_TILE, C.n_tokens - t0);
+    build_tile_map(a, C, DEPTH, k, nvalid, s_map);
+    __syncthreads();
+    uint16_t* out = a.reqs ? a.out[b] : a.one_out;
+    if ((reinterpret_cast<uintptr_t>(out) & 15u) != 0) {
+      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 16);
+      continue;
+    }
+    const int npairs = nvalid * H;
+    for (int q4 = warp; q4 * 4 < npairs; q4 += kWarps) {
+      const int pr = q4 * 4 + lg;
+      const bool live = pr < npairs;
+      const int tt = live ? pr / H : 0, h = live ? pr % H : 0;
+      uint2 cw[DEPTH];
+      uint32_t m16[DEPTH], s16[DEPTH];
+      bool have[DEPTH];
+#pragma unroll
+      for (int j = 0; j < DEPTH; ++j) {
+        const int row = live ? s_map[j][tt] : -1;
+        have[j] = row >= 0;
+        cw[j] = make_uint2(0, 0);
+        m16[j] = s16[j] = 0;
+        if (have[j]) {
+          const LoopPlanes& L = C.loop[j];
+          const long long rr = (long long)h * L.n_rows + row;
+          cw[j] = __ldg(reinterpret_cast<const uint2*>(L.codes + rr * kRowBytes + 8 * sub));
+          m16[j] = __ldg(L.mins + rr * (kD / kG) + (sub >> 2));
+          s16[j] = __ldg(L.scales + rr * (kD / kG) + (sub >> 2));
+        }
+      }
+      uint32_t acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0;
+#pragma unroll
+      for (int j = 0; j < DEPTH; ++j) {
+        if (!have[j]) continue;
+        const float mf = f16_bits_to_f32(uint16_t(m16[j])), sf = f16_bits_to_f32(uint16_t(s16[j]));
+        uint32_t dq[8];
+        dequant_word(cw[j].x, make_float2(mf, mf), make_float2(sf, sf), dq);
+        dequant_word(cw[j].y, make_float2(mf, mf), make_float2(sf, sf), dq + 4);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = (j == 0) ? dq[e] : bf2_add(acc[e], dq[e]);
+      }
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(out + ((long long)(t0 + tt) * H + h) * kD + 16 * sub);
+        dst[0] = make_uint4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_uint4(acc[4], acc[5], acc[6], acc[7]);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- launchers
 
 static int single_items(const CodecArgs& a, int mode) {
@@ -413,12 +981,15 @@ static int single_items(const CodecArgs& a, int mode) {
     case kModeEncK: return n > 0 ? a.H * ((n + kG - 1) / kG) : 0;
     case kModeEncV: return (n + kG - 1) / kG;
     case kModeTileDir: return R.loop[a.loop].active_idx ? (R.n_tokens + KVQ_TILE - 1) / KVQ_TILE + 1 : 0;
+    case kModeReconK: return ((R.n_tokens + KVQ_TILE - 1) / KVQ_TILE) * a.H;
     default: return (R.n_tokens + KVQ_TILE - 1) / KVQ_TILE;
   }
 }
 
 cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, int sms, cudaStream_t stream) {
   CodecArgs a = a_in;
+  // K reconstruction of chains up to 4 loops runs one item per (tile, head)
+  if (mode == kModeRecon && a.kind == KVQ_K && a.loop >= 1 && a.loop <= kFastMaxDepth) mode = kModeReconK;
   const int32_t* prefix = nullptr;  // nullptr: kernels read a.one_prefix
   long long items = -1;             // -1: known only on the device
   if (a.reqs == nullptr) {
@@ -435,21 +1006,63 @@ cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, in
     if (e != cudaSuccess) return e;
     prefix = prefix_ws;
   }
-  // a fixed grid of a few CTAs per SM, fewer when a single request has fewer items
+  // a fixed grid of as many CTAs as fit on the GPU, fewer when a single
+  // request has fewer items
   auto grid_for = [&](int per_sm) {
     long long cap = (long long)per_sm * sms;
     return int(items >= 0 && items < cap ? items : cap);
   };
+  auto run = [&](auto kern, int threads) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    kern<<<grid_for(per_sm), threads, 0, stream>>>(a, prefix);
+  };
   switch (mode) {
-    case kModeEncK: encode_k_kernel<<<grid_for(8), kD, 0, stream>>>(a, prefix); break;
-    case kModeEncV: encode_v_kernel<<<grid_for(4), kEncVThreads, 0, stream>>>(a, prefix); break;
+    case kModeEncK:
+      switch (a.loop) {
+        case 0: run(encode_k_fast_kernel<0>, kG); break;
+        case 1: run(encode_k_fast_kernel<1>, kG); break;
+        case 2: run(encode_k_fast_kernel<2>, kG); break;
+        case 3: run(encode_k_fast_kernel<3>, kG); break;
+        default: encode_k_generic_kernel<<<grid_for(8), kD, 0, stream>>>(a, prefix); break;
+      }
+      break;
+    case kModeEncV:
+      switch (a.loop) {
+        case 0: run(encode_v_fast_kernel<0>, kEncVFastThreads); break;
+        case 1: run(encode_v_fast_kernel<1>, kEncVFastThreads); break;
+        case 2: run(encode_v_fast_kernel<2>, kEncVFastThreads); break;
+        case 3: run(encode_v_fast_kernel<3>, kEncVFastThreads); break;
+        default: encode_v_generic_kernel<<<grid_for(4), kEncVThreads, 0, stream>>>(a, prefix); break;
+      }
+      break;
     case kModeTileDir: {
       long long blocks = items >= 0 ? (items + 255) / 256 : 2LL * sms;
       if (blocks > 2LL * sms) blocks = 2LL * sms;
       tile_dir_kernel<<<int(blocks), 256, 0, stream>>>(a, prefix);
       break;
     }
-    default: reconstruct_kernel<<<grid_for(4), kReconThreads, 0, stream>>>(a, prefix); break;
+    case kModeReconK:
+      switch (a.loop) {
+        case 1: run(reconstruct_k_fast_kernel<1>, kG); break;
+        case 2: run(reconstruct_k_fast_kernel<2>, kG); break;
+        case 3: run(reconstruct_k_fast_kernel<3>, kG); break;
+        default: run(reconstruct_k_fast_kernel<4>, kG); break;
+      }
+      break;
+    default:
+      if (a.kind == KVQ_V && a.loop >= 1 && a.loop <= kFastMaxDepth) {
+        switch (a.loop) {
+          case 1: run(reconstruct_v_fast_kernel<1>, kReconVFastThreads); break;
+          case 2: run(reconstruct_v_fast_kernel<2>, kReconVFastThreads); break;
+          case 3: run(reconstruct_v_fast_kernel<3>, kReconVFastThreads); break;
+          default: run(reconstruct_v_fast_kernel<4>, kReconVFastThreads); break;
+        }
+      } else {
+        reconstruct_generic_kernel<<<grid_for(4), kReconThreads, 0, stream>>>(a, prefix);
+      }
+      break;
   }
   count_launch();
   return cudaGetLastError();

@@ -150,7 +150,7 @@ __device__ __forceinline__ float chain1(const Chain& C, int depth, const int* ro
 // Number of kernels this library has launched in the process (host counter).
 void count_launch();
 
-enum { kModeEncK = 0, kModeEncV = 1, kModeTileDir = 2, kModeRecon = 3 };
+enum { kModeEncK = 0, kModeEncV = 1, kModeTileDir = 2, kModeRecon = 3, kModeReconK = 4 };
 
 // Arguments of the codec kernels: either a batch described by a device table of
 // requests, or one request carried by value in the kernel parameters.
