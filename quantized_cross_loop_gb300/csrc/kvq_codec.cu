@@ -498,6 +498,18 @@ __device__ __forceinline__ void dequant_word(uint32_t w, float2 m, float2 s, uin
   }
 }
 
+// One codes word -> four BF16 pairs with the min and scale of each pair.
+__device__ __forceinline__ void dequant_word_pp(uint32_t w, const float2* m, const float2* s, uint32_t* out) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 c = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440 + k)),
+                                            __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440 + k))),
+                                make_float2(-kMagic23, -kMagic23));
+    out[k] = f2_to_bf2(__ffma2_rn(s[k], c, m[k]));
+  }
+}
+
 // Codes of a BF16 pair against the FP32 min, scale and RN32(1 / scale) of each
 // channel (reciprocal 0 for a constant group): code(lo) | code(hi) << 4.
 __device__ __forceinline__ uint32_t quant_pair(uint32_t v, float2 mn, float2 rc, float2 s32) {
@@ -518,108 +530,226 @@ __device__ __forceinline__ float recip_of(float s32) { return s32 != 0.0f ? __fr
 
 }  // namespace fast
 
+// ---------------------------------------------------------------- K parameters in shared memory
+
+// A K group's parameters staged as FP32 (min lo, min hi, scale lo, scale hi)
+// per channel pair. Pair P is stored in slot kpar_slot(P): the eight lanes of a
+// row, each reading pair 8 sub + k in the same instruction, hit eight different
+// 16-byte bank groups.
+constexpr int kKParGroups = 6;  // groups of one predecessor loop staged per item
+__device__ __forceinline__ int kpar_slot(int pair) { return (pair & ~7) | (((pair & 7) + (pair >> 3)) & 7); }
+
+// Stages groups g0 .. g0 + ng - 1 of head h of loop L (K) into par[0 .. ng-1][64].
+__device__ __forceinline__ void stage_kpar(const LoopPlanes& L, int h, int g0, int ng, float4 (*par)[kD / 2]) {
+  const long long G = (L.n_rows + kG - 1) / kG;
+  for (int idx = threadIdx.x; idx < ng * (kD / 2); idx += blockDim.x) {
+    const int gi = idx / (kD / 2), pair = idx % (kD / 2);
+    const long long pi = ((long long)h * G + g0 + gi) * kD + 2 * pair;
+    const float2 m = fast::f16x2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(L.mins + pi)));
+    const float2 s = fast::f16x2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(L.scales + pi)));
+    par[gi][kpar_slot(pair)] = make_float4(m.x, m.y, s.x, s.y);
+  }
+}
+
+// Decodes the 16 channels 16 sub .. 16 sub + 15 of stored row `row` of head h
+// of K loop L (codes cw) into 8 BF16 pairs; parameters from the staged groups
+// when the row's group is among them, else from the planes.
+__device__ __forceinline__ void dequant16_k(const LoopPlanes& L, int h, int row, uint2 cw, int sub,
+                                            const float4 (*par)[kD / 2], int g0, int ng, uint32_t* out) {
+  const int gi = (row >> 6) - g0;
+  float2 m[8], s[8];
+  if (gi >= 0 && gi < ng) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float4 q = par[gi][8 * sub + ((k + sub) & 7)];
+      m[k] = make_float2(q.x, q.y);
+      s[k] = make_float2(q.z, q.w);
+    }
+  } else {
+    const long long pi = ((long long)h * ((L.n_rows + kG - 1) / kG) + (row >> 6)) * kD + 16 * sub;
+    const uint4* mp = reinterpret_cast<const uint4*>(L.mins + pi);
+    const uint4* sp = reinterpret_cast<const uint4*>(L.scales + pi);
+    const uint4 m0 = __ldg(mp), m1 = __ldg(mp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
+    const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      m[k] = fast::f16x2_to_f2(mw[k]);
+      s[k] = fast::f16x2_to_f2(sw[k]);
+    }
+  }
+  fast::dequant_word_pp(cw.x, m, s, out);
+  fast::dequant_word_pp(cw.y, m + 4, s + 4, out + 4);
+}
+
 // ---------------------------------------------------------------- encode K (fast)
 //
-// item = (64-row compact group, head); thread p = channel pair 2p, 2p+1. The
-// thread keeps the group's 64 residual pairs in registers, so min/max is an
-// in-order scan over rows and the codes of row i are one byte of a 64-byte row
-// (a warp stores 32 consecutive bytes). The K parameters of a predecessor
-// loop are reloaded only when the stored row crosses into another group.
+// item = (64-row compact group, head), 256 threads, two phases.
+//  1. Residuals: eight lanes per row (lane `sub` = channels 16 sub .. +15), a
+//     warp four rows; every load of a row is issued before its arithmetic and
+//     the BF16 residual pairs go to a shared [row][pair] tile.
+//  2. Columns: thread (pair p, quarter q) scans rows 16 q .. 16 q + 15 of pair
+//     p; the four partial min/max are merged in row order, then each thread
+//     quantises its rows into a shared code tile that leaves in 16-byte stores.
+
+constexpr int kEncKThreads = 256;
 
 template <int R>
-__global__ void __launch_bounds__(kG) encode_k_fast_kernel(const __grid_constant__ CodecArgs a,
-                                                           const int32_t* prefix_ws) {
+struct EncKSmem {
+  uint32_t delta[kG][kD / 2];                  // residual BF16 pairs
+  uint8_t codes[kG][kRowBytes];                // output codes
+  float4 par[R > 0 ? R : 1][kKParGroups][kD / 2];  // staged predecessor parameters
+  uint32_t pmn[4][kD / 2], pmx[4][kD / 2];     // partial min/max per row quarter
+  Chain C;
+  int tok[kG];
+  int row[R > 0 ? R : 1][kG];
+  int glo[R > 0 ? R : 1], ghi[R > 0 ? R : 1];
+  int b;
+};
+
+template <int R>
+__global__ void __launch_bounds__(kEncKThreads) encode_k_fast_kernel(const __grid_constant__ CodecArgs a,
+                                                                     const int32_t* prefix_ws) {
   using namespace fast;
-  constexpr int RA = R > 0 ? R : 1;
+  constexpr int kWarps = kEncKThreads / 32;
   const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
-  const int p = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sub = lane & 7, lg = lane >> 3;
   const int H = a.H;
-  __shared__ Chain C;  // C.loop[0..R-1]: predecessor chain; C.loop[R]: output planes
-  __shared__ int s_tok[kG];
-  __shared__ int s_row[RA][kG];
-  __shared__ int s_b;
+  __shared__ EncKSmem<R> S;
 
   const ItemRange ir = cta_items(prefix, a.n_requests);
   int cur_b = -1;
   for (long long it = ir.begin; it < ir.end; ++it) {
-    if (p == 0) s_b = owner_of(prefix, a.n_requests, it);
+    if (tid == 0) S.b = owner_of(prefix, a.n_requests, it);
     __syncthreads();
-    const int b = s_b;
+    const int b = S.b;
     if (b != cur_b) {
-      if (p == 0) fill_chain(req_at(a, b), KVQ_K, R + 1, H, C);
+      if (tid == 0) fill_chain(req_at(a, b), KVQ_K, R + 1, H, S.C);
       cur_b = b;
+    }
+    if (tid < R) {
+      S.glo[tid] = 0x7FFFFFFF;
+      S.ghi[tid] = -1;
     }
     __syncthreads();
     const int local = int(it - prefix[b]);
     const int g = local / H, h = local % H;
-    const LoopPlanes& O = C.loop[R];
+    const LoopPlanes& O = S.C.loop[R];
     const int n = O.n_rows;
     const int r0 = g * kG;
     const int len = min(kG, n - r0);
     const uint16_t* x = source_of(a, b);
-    if (p < len) {
-      const int t = O.sparse ? __ldg(O.active + r0 + p) : r0 + p;
-      s_tok[p] = t;
+    if (tid < len) {
+      const int t = O.sparse ? __ldg(O.active + r0 + tid) : r0 + tid;
+      S.tok[tid] = t;
 #pragma unroll
-      for (int j = 0; j < R; ++j) s_row[j][p] = row_of(C.loop[j], t);
+      for (int j = 0; j < R; ++j) {
+        const int row = row_of(S.C.loop[j], t);
+        S.row[j][tid] = row;
+        if (row >= 0) {
+          atomicMin(&S.glo[j], row >> 6);
+          atomicMax(&S.ghi[j], row >> 6);
+        }
+      }
     }
     __syncthreads();
     if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) {  // batch source not 16-byte aligned: skip
-      if (p == 0 && a.err) atomicOr(a.err, 16);
+      if (tid == 0 && a.err) atomicOr(a.err, 16);
       continue;
     }
-    const uint32_t* xw = reinterpret_cast<const uint32_t*>(x);
-
-    float2 pm[RA], ps[RA];
-    int pg[RA];
+    int g0[R > 0 ? R : 1], ng[R > 0 ? R : 1];
 #pragma unroll
-    for (int j = 0; j < RA; ++j) {
-      pg[j] = -1;
-      pm[j] = ps[j] = make_float2(0.0f, 0.0f);
+    for (int j = 0; j < R; ++j) {
+      g0[j] = S.glo[j];
+      ng[j] = S.ghi[j] >= g0[j] ? S.ghi[j] - g0[j] + 1 : 0;
+      if (ng[j] > kKParGroups) ng[j] = 0;  // too spread: read the planes instead
+      stage_kpar(S.C.loop[j], h, g0[j], ng[j], S.par[j]);
     }
-    uint32_t v[kG];
-    uint32_t mn2 = 0, mx2 = 0;
+    __syncthreads();
+
+    // ---- phase 1: residual rows
+#pragma unroll 1
+    for (int i0 = 0; i0 < kG; i0 += 4 * kWarps) {
+      const int i = i0 + 4 * warp + lg;
+      const bool live = i < len;
+      uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+      uint2 cw[R > 0 ? R : 1];
+      int rows[R > 0 ? R : 1];
 #pragma unroll
-    for (int i = 0; i < kG; ++i) {
-      v[i] = 0;
-      if (i < len) {
-        const int t = s_tok[i];
-        const uint32_t xv = __ldg(xw + ((long long)t * H + h) * (kD / 2) + p);
-        uint32_t d = xv;
-        if (R > 0) {
-          uint32_t acc = 0;
-#pragma unroll
-          for (int j = 0; j < R; ++j) {
-            const int row = s_row[j][i];
-            if (row < 0) continue;  // absent: inherit the predecessor
-            const LoopPlanes& L = C.loop[j];
-            if ((row >> 6) != pg[j]) {
-              pg[j] = row >> 6;
-              const long long pi = ((long long)h * ((L.n_rows + kG - 1) / kG) + pg[j]) * kD + 2 * p;
-              pm[j] = f16x2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(L.mins + pi)));
-              ps[j] = f16x2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(L.scales + pi)));
-            }
-            const uint32_t byte = __ldg(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + p);
-            const uint32_t dq = dequant_byte(byte, pm[j], ps[j]);
-            acc = (j == 0) ? dq : bf2_add(acc, dq);
-          }
-          d = bf2_sub(xv, acc);
-        }
-        v[i] = d;
-        mn2 = (i == 0) ? d : bf2_min(mn2, d);
-        mx2 = (i == 0) ? d : bf2_max(mx2, d);
+      for (int j = 0; j < R; ++j) {
+        cw[j] = make_uint2(0, 0);
+        rows[j] = -1;
       }
+      if (live) {
+        const int t = S.tok[i];
+        const uint4* src = reinterpret_cast<const uint4*>(x + ((long long)t * H + h) * kD + 16 * sub);
+        xa = __ldg(src);
+        xb = __ldg(src + 1);
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          rows[j] = S.row[j][i];
+          if (rows[j] >= 0) {
+            const LoopPlanes& L = S.C.loop[j];
+            cw[j] = __ldg(reinterpret_cast<const uint2*>(L.codes + ((long long)h * L.n_rows + rows[j]) * kRowBytes +
+                                                         8 * sub));
+          }
+        }
+      }
+      uint32_t d[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      if (R > 0) {
+        uint32_t acc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = 0;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          if (rows[j] < 0) continue;
+          uint32_t dq[8];
+          dequant16_k(S.C.loop[j], h, rows[j], cw[j], sub, S.par[j], g0[j], ng[j], dq);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc[k] = (j == 0) ? dq[k] : bf2_add(acc[k], dq[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) d[k] = bf2_sub(d[k], acc[k]);
+      }
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(&S.delta[i][8 * sub]);
+        dst[0] = make_uint4(d[0], d[1], d[2], d[3]);
+        dst[1] = make_uint4(d[4], d[5], d[6], d[7]);
+      }
+    }
+    __syncthreads();
+
+    // ---- phase 2: per channel pair p, rows of quarter q
+    const int p = tid & (kD / 2 - 1), q = tid >> 6;
+    const int ia = 16 * q, ib = min(16 * q + 16, len);
+    uint32_t mn2 = 0, mx2 = 0;
+    bool any = false;
+    for (int i = ia; i < ib; ++i) {
+      const uint32_t v = S.delta[i][p];
+      mn2 = any ? bf2_min(mn2, v) : v;
+      mx2 = any ? bf2_max(mx2, v) : v;
+      any = true;
+    }
+    if (any) {
+      S.pmn[q][p] = mn2;
+      S.pmx[q][p] = mx2;
+    }
+    __syncthreads();
+    const int nq = (len + 15) / 16;
+    mn2 = S.pmn[0][p];
+    mx2 = S.pmx[0][p];
+    for (int qq = 1; qq < nq; ++qq) {
+      mn2 = bf2_min(mn2, S.pmn[qq][p]);
+      mx2 = bf2_max(mx2, S.pmx[qq][p]);
     }
     float mn[2] = {bf_lo(mn2), bf_hi(mn2)}, mx[2] = {bf_lo(mx2), bf_hi(mx2)};
     if (mn[0] == 0.0f || mn[1] == 0.0f || mx[0] == 0.0f || mx[1] == 0.0f) {
+      // the in-order scan keeps the first zero it meets: take its sign
       bool done[4] = {mn[0] != 0.0f, mn[1] != 0.0f, mx[0] != 0.0f, mx[1] != 0.0f};
-#pragma unroll 1
       for (int i = 0; i < len; ++i) {
-        uint32_t vi = 0;
-#pragma unroll
-        for (int k = 0; k < kG; ++k)
-          if (k == i) vi = v[k];
-        const float lo = bf_lo(vi), hi = bf_hi(vi);
+        const uint32_t v = S.delta[i][p];
+        const float lo = bf_lo(v), hi = bf_hi(v);
         if (!done[0] && lo == 0.0f) { mn[0] = lo; done[0] = true; }
         if (!done[2] && lo == 0.0f) { mx[0] = lo; done[2] = true; }
         if (!done[1] && hi == 0.0f) { mn[1] = hi; done[1] = true; }
@@ -629,13 +759,18 @@ __global__ void __launch_bounds__(kG) encode_k_fast_kernel(const __grid_constant
     const float s0 = scale_of(mn[0], mx[0]), s1 = scale_of(mn[1], mx[1]);
     const float2 mnv = make_float2(mn[0], mn[1]), sv = make_float2(s0, s1);
     const float2 rc = make_float2(recip_of(s0), recip_of(s1));
-    uint8_t* dst = const_cast<uint8_t*>(O.codes) + ((long long)h * n + r0) * kRowBytes + p;
-#pragma unroll
-    for (int i = 0; i < kG; ++i)
-      if (i < len) dst[(long long)i * kRowBytes] = uint8_t(quant_pair(v[i], mnv, rc, sv));
-    const long long pi = ((long long)h * ((n + kG - 1) / kG) + g) * kD + 2 * p;
-    *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.mins) + pi) = f16_pair(mn[0], mn[1]);
-    *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.scales) + pi) = f16_pair(s0, s1);
+    for (int i = ia; i < ib; ++i) S.codes[i][p] = uint8_t(quant_pair(S.delta[i][p], mnv, rc, sv));
+    if (q == 0) {
+      const long long pi = ((long long)h * ((n + kG - 1) / kG) + g) * kD + 2 * p;
+      *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.mins) + pi) = f16_pair(mn[0], mn[1]);
+      *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.scales) + pi) = f16_pair(s0, s1);
+    }
+    __syncthreads();
+    // len rows x 64 bytes, contiguous in the head-major plane
+    if (tid < len * (kRowBytes / 16)) {
+      uint4* dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(O.codes) + ((long long)h * n + r0) * kRowBytes);
+      dst[tid] = reinterpret_cast<const uint4*>(&S.codes[0][0])[tid];
+    }
   }
 }
 
@@ -823,68 +958,101 @@ __device__ __forceinline__ void build_tile_map(const CodecArgs& a, const Chain& 
   }
 }
 
-// K: item = (64-token tile, head); thread p = channel pair. Parameters are
-// reloaded only when a loop's stored row crosses into another group.
+// K: item = (64-token tile, head), 256 threads; eight lanes per token (lane
+// `sub` = channels 16 sub .. +15), a warp four tokens, so each token's output
+// row (256 B) leaves in 16-byte stores. The K parameters of the tile's groups
+// (one per dense loop, at most two per sparse loop: its rows in the tile are
+// one compact range of at most 64) are staged as FP32 first.
+constexpr int kReconKThreads = 256;
+
 template <int DEPTH>
-__global__ void __launch_bounds__(kG) reconstruct_k_fast_kernel(const __grid_constant__ CodecArgs a,
-                                                                const int32_t* prefix_ws) {
+struct ReconKSmem {
+  float4 par[DEPTH][2][kD / 2];
+  Chain C;
+  int map[DEPTH][KVQ_TILE];
+  int b;
+};
+
+template <int DEPTH>
+__global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(const __grid_constant__ CodecArgs a,
+                                                                            const int32_t* prefix_ws) {
   using namespace fast;
+  constexpr int kWarps = kReconKThreads / 32;
   const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
-  const int p = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sub = lane & 7, lg = lane >> 3;
   const int H = a.H;
-  __shared__ Chain C;
-  __shared__ int s_map[DEPTH][KVQ_TILE];
-  __shared__ int s_b;
+  __shared__ ReconKSmem<DEPTH> S;
 
   const ItemRange ir = cta_items(prefix, a.n_requests);
   int cur_b = -1;
   for (long long it = ir.begin; it < ir.end; ++it) {
-    if (p == 0) s_b = owner_of(prefix, a.n_requests, it);
+    if (tid == 0) S.b = owner_of(prefix, a.n_requests, it);
     __syncthreads();
-    const int b = s_b;
+    const int b = S.b;
     if (b != cur_b) {
-      if (p == 0) fill_chain(req_at(a, b), KVQ_K, DEPTH, H, C);
+      if (tid == 0) fill_chain(req_at(a, b), KVQ_K, DEPTH, H, S.C);
       cur_b = b;
     }
     __syncthreads();
     const int local = int(it - prefix[b]);
     const int k = local / H, h = local % H;
     const int t0 = k * KVQ_TILE;
-    const int nvalid = min(KVQ_TILE, C.n_tokens - t0);
-    build_tile_map(a, C, DEPTH, k, nvalid, s_map);
+    const int nvalid = min(KVQ_TILE, S.C.n_tokens - t0);
+    build_tile_map(a, S.C, DEPTH, k, nvalid, S.map);
+    int g0[DEPTH], ng[DEPTH];
+#pragma unroll
+    for (int j = 0; j < DEPTH; ++j) {
+      const LoopPlanes& L = S.C.loop[j];
+      if (!L.sparse) {
+        g0[j] = k;  // dense: rows t0 .. t0 + nvalid - 1, one group
+        ng[j] = 1;
+      } else {
+        const int c0 = __ldg(L.tile_dir + k), c1 = __ldg(L.tile_dir + k + 1);
+        const bool ok = c0 >= 0 && c1 <= L.n_rows && c0 < c1 && c1 - c0 <= KVQ_TILE;
+        g0[j] = ok ? c0 >> 6 : 0;
+        ng[j] = ok ? ((c1 - 1) >> 6) - (c0 >> 6) + 1 : 0;
+      }
+      stage_kpar(L, h, g0[j], ng[j], S.par[j]);
+    }
     __syncthreads();
     uint16_t* out = a.reqs ? a.out[b] : a.one_out;
     if ((reinterpret_cast<uintptr_t>(out) & 15u) != 0) {
-      if (p == 0 && a.err) atomicOr(a.err, 16);
+      if (tid == 0 && a.err) atomicOr(a.err, 16);
       continue;
     }
-    uint32_t* ow = reinterpret_cast<uint32_t*>(out) + ((long long)t0 * H + h) * (kD / 2) + p;
-    float2 pm[DEPTH], ps[DEPTH];
-    int pg[DEPTH];
-#pragma unroll
-    for (int j = 0; j < DEPTH; ++j) {
-      pg[j] = -1;
-      pm[j] = ps[j] = make_float2(0.0f, 0.0f);
-    }
-#pragma unroll 4
-    for (int tt = 0; tt < nvalid; ++tt) {
-      uint32_t acc = 0;
+#pragma unroll 1
+    for (int i0 = 0; i0 < nvalid; i0 += 4 * kWarps) {
+      const int tt = i0 + 4 * warp + lg;
+      const bool live = tt < nvalid;
+      uint2 cw[DEPTH];
+      int rows[DEPTH];
 #pragma unroll
       for (int j = 0; j < DEPTH; ++j) {
-        const int row = s_map[j][tt];
-        if (row < 0) continue;
-        const LoopPlanes& L = C.loop[j];
-        if ((row >> 6) != pg[j]) {
-          pg[j] = row >> 6;
-          const long long pi = ((long long)h * ((L.n_rows + kG - 1) / kG) + pg[j]) * kD + 2 * p;
-          pm[j] = f16x2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(L.mins + pi)));
-          ps[j] = f16x2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(L.scales + pi)));
+        rows[j] = live ? S.map[j][tt] : -1;
+        cw[j] = make_uint2(0, 0);
+        if (rows[j] >= 0) {
+          const LoopPlanes& L = S.C.loop[j];
+          cw[j] = __ldg(reinterpret_cast<const uint2*>(L.codes + ((long long)h * L.n_rows + rows[j]) * kRowBytes +
+                                                       8 * sub));
         }
-        const uint32_t byte = __ldg(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + p);
-        const uint32_t dq = dequant_byte(byte, pm[j], ps[j]);
-        acc = (j == 0) ? dq : bf2_add(acc, dq);
       }
-      ow[(long long)tt * H * (kD / 2)] = acc;
+      uint32_t acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0;
+#pragma unroll
+      for (int j = 0; j < DEPTH; ++j) {
+        if (rows[j] < 0) continue;
+        uint32_t dq[8];
+        dequant16_k(S.C.loop[j], h, rows[j], cw[j], sub, S.par[j], g0[j], ng[j], dq);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = (j == 0) ? dq[e] : bf2_add(acc[e], dq[e]);
+      }
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(out + ((long long)(t0 + tt) * H + h) * kD + 16 * sub);
+        dst[0] = make_uint4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_uint4(acc[4], acc[5], acc[6], acc[7]);
+      }
     }
   }
 }
@@ -1021,10 +1189,10 @@ cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, in
   switch (mode) {
     case kModeEncK:
       switch (a.loop) {
-        case 0: run(encode_k_fast_kernel<0>, kG); break;
-        case 1: run(encode_k_fast_kernel<1>, kG); break;
-        case 2: run(encode_k_fast_kernel<2>, kG); break;
-        case 3: run(encode_k_fast_kernel<3>, kG); break;
+        case 0: run(encode_k_fast_kernel<0>, kEncKThreads); break;
+        case 1: run(encode_k_fast_kernel<1>, kEncKThreads); break;
+        case 2: run(encode_k_fast_kernel<2>, kEncKThreads); break;
+        case 3: run(encode_k_fast_kernel<3>, kEncKThreads); break;
         default: encode_k_generic_kernel<<<grid_for(8), kD, 0, stream>>>(a, prefix); break;
       }
       break;
@@ -1045,10 +1213,10 @@ cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, in
     }
     case kModeReconK:
       switch (a.loop) {
-        case 1: run(reconstruct_k_fast_kernel<1>, kG); break;
-        case 2: run(reconstruct_k_fast_kernel<2>, kG); break;
-        case 3: run(reconstruct_k_fast_kernel<3>, kG); break;
-        default: run(reconstruct_k_fast_kernel<4>, kG); break;
+        case 1: run(reconstruct_k_fast_kernel<1>, kReconKThreads); break;
+        case 2: run(reconstruct_k_fast_kernel<2>, kReconKThreads); break;
+        case 3: run(reconstruct_k_fast_kernel<3>, kReconKThreads); break;
+        default: run(reconstruct_k_fast_kernel<4>, kReconKThreads); break;
       }
       break;
     default:
