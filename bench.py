@@ -47,7 +47,7 @@ WORKLOADS = {
 }
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
@@ -58,7 +58,11 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target wall time of the CPU-oracle sample")
-    return ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def parse_args_list(argv):
+    return parse_args(list(argv))
 
 
 # ------------------------------------------------------------------ algorithmic bytes
@@ -175,6 +179,35 @@ def kernel_traffic(kernel_key: str):
     return d
 
 
+# ------------------------------------------------------------------ multi-rank helpers
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank time over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, step_bytes: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own batch of step_bytes
+    per step (weak scaling); the step time is the slowest rank's."""
+    return world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+
+def rank_workload(cfg_idx: int, rank: int, replicate: int, device):
+    """The independent batch of one rank: same shapes on every rank, drawn from
+    a rank-specific seed (the rank plays the role of the layer index)."""
+    from quantized_cross_loop_gb300 import workloads as W
+
+    return W.make_workload(cfg_idx, device=device, layer=rank, replicate=replicate)
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 
@@ -224,7 +257,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     # ---- workload, resident in HBM (each rank its own independent batch)
-    wl = W.make_workload(cfg_idx, device=dev, layer=rank, replicate=replicate)
+    wl = rank_workload(cfg_idx, rank, replicate, dev)
     reqs = wl.requests
     B, H, D, Hq, depth = wl.n_requests, wl.H, wl.D, wl.Hq, wl.depth
     lengths = [r.T for r in reqs]
@@ -302,15 +335,12 @@ def main():
     enc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     rec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     att_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
 
     ab = algorithmic_bytes(reqs, H, D, Hq, depth, lambda k, n, s: kvq.payload_bytes(k, n, H, D, s))
     step_bytes = ab["encode"] + ab["reconstruct"] + ab["attention"]
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, step_bytes, ms_per_step)
     peak, peak_kind = measured_peak()
     phase_ms = {"encode": enc_ms, "reconstruct": rec_ms, "attention": att_ms}
     phase_gbs = {k: ab[k] / (phase_ms[k] * 1e-3) / 1e9 for k in phase_ms}
@@ -400,12 +430,8 @@ def run_e2e(args, torch, kvq, reqs, q, out, step, stream, world, dev, step_bytes
         e2e_step()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / n
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": world * step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+    ms = max_over_ranks(a.elapsed_time(b) / n, dev)
+    return {"value": whole_job_gbs(world, step_bytes, ms), "unit": "GB/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
 
 

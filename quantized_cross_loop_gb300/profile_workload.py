@@ -1,0 +1,80 @@
+"""Runs one stage of the packed-KV path on a seeded synthetic workload, for
+profilers (ncu captures of a single kernel). It reports no timing.
+
+  python -m quantized_cross_loop_gb300.profile_workload --workload cfg3 --stage attention --reps 2
+  python -m quantized_cross_loop_gb300.profile_workload --workload cfg2x128 --stage encode
+
+Workloads: cfg1..cfg4 (the synthetic configurations), cfg2xN (N independent
+requests of configuration 2). Stages:
+  encode       batched encode of every loop of K and V (the sources are freed
+               before the other stages run);
+  reconstruct  batched reconstruction of K and V at full depth, `reps` times;
+  attention    packed decode attention at full depth, `reps` times, with a
+               256 MiB buffer written between calls so that every call starts
+               with a cold L2.
+Every stage first encodes the workload (the launches a capture should skip:
+2 + 4 (loops - 1) per kind, plus one per reconstruct or attention call before
+the one captured).
+"""
+
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from quantized_cross_loop_gb300 import kvq
+from quantized_cross_loop_gb300 import workloads as W
+
+
+def parse_workload(name: str):
+    if name.startswith("cfg2x"):
+        return 2, int(name[5:])
+    return int(name[3:]), 1
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="cfg3")
+    ap.add_argument("--stage", choices=["encode", "reconstruct", "attention"], default="attention")
+    ap.add_argument("--algo", choices=["auto", "simt", "mma"], default="auto")
+    ap.add_argument("--reps", type=int, default=2)
+    args = ap.parse_args()
+    cfg, rep = parse_workload(args.workload)
+    dev = torch.device("cuda")
+    wl = W.make_workload(cfg, device=dev, replicate=rep)
+    reqs = wl.requests
+    pool = kvq.PackedPool([r.T for r in reqs], [r.active for r in reqs], wl.H, wl.D, wl.depth, dev)
+    for j in range(wl.depth):
+        kvq.kvq_encode_batch(pool, kvq.KVQ_K, j, kvq.pointer_array([r.xk[j] for r in reqs], dev))
+        kvq.kvq_encode_batch(pool, kvq.KVQ_V, j, kvq.pointer_array([r.xv[j] for r in reqs], dev))
+    lengths = [r.T for r in reqs]
+    del reqs, wl.requests[:]
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if args.stage == "reconstruct":
+        outs = [[torch.empty((t, wl.H, wl.D), dtype=torch.bfloat16, device=dev) for t in lengths] for _ in range(2)]
+        ptrs = [kvq.pointer_array(o, dev) for o in outs]
+        for _ in range(args.reps):
+            for kind in (kvq.KVQ_K, kvq.KVQ_V):
+                kvq.kvq_reconstruct_batch(pool, kind, wl.depth, ptrs[kind])
+    elif args.stage == "attention":
+        algo = {"auto": kvq.ATTN_AUTO, "simt": kvq.ATTN_SIMT, "mma": kvq.ATTN_MMA}[args.algo]
+        q = wl.q
+        out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        ws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(q.shape[0], wl.H, wl.Hq, wl.D), dtype=torch.uint8,
+                         device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for _ in range(args.reps):
+            flush.zero_()
+            kvq.kvq_decode_attn_packed(pool.table, q, wl.depth, wl.H, algo=algo, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    err = kvq.attn_error_word(pool.workspace)
+    if args.stage == "attention":
+        err |= kvq.attn_error_word(ws)
+    print("ok" if err == 0 else f"error word {err}")
+    return 0 if err == 0 else 1
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
