@@ -126,6 +126,20 @@ __device__ __forceinline__ int owner_of(const int32_t* prefix, int n_requests, l
   return lo;
 }
 
+// Owner of item x for a CTA whose previous item belonged to request `cur` (-1:
+// none yet). A CTA's items ascend, so the search starts at `cur` and is
+// usually a single comparison. Every thread computes the same value.
+__device__ __forceinline__ int owner_next(const int32_t* prefix, int n_requests, long long x, int cur) {
+  if (cur >= 0 && x < prefix[cur + 1]) return cur;
+  int lo = cur >= 0 ? cur + 1 : 0, hi = n_requests - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
 // One thread fills the chain of loops 0..n-1 of request R for `kind`.
 __device__ void fill_chain(const kvq_request& R, int kind, int n, int H, Chain& C) {
   C.depth = n;
@@ -551,13 +565,12 @@ __device__ __forceinline__ void stage_kpar(const LoopPlanes& L, int h, int g0, i
   }
 }
 
-// Decodes the 16 channels 16 sub .. 16 sub + 15 of stored row `row` of head h
-// of K loop L (codes cw) into 8 BF16 pairs; parameters from the staged groups
-// when the row's group is among them, else from the planes.
-__device__ __forceinline__ void dequant16_k(const LoopPlanes& L, int h, int row, uint2 cw, int sub,
-                                            const float4 (*par)[kD / 2], int g0, int ng, uint32_t* out) {
+// Parameters of the 16 channels 16 sub .. 16 sub + 15 for stored row `row` of
+// head h of K loop L: from the staged groups when the row's group is among
+// them, else from the planes.
+__device__ __forceinline__ void load_kpar16(const LoopPlanes& L, int h, int row, int sub,
+                                            const float4 (*par)[kD / 2], int g0, int ng, float2* m, float2* s) {
   const int gi = (row >> 6) - g0;
-  float2 m[8], s[8];
   if (gi >= 0 && gi < ng) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -578,6 +591,14 @@ __device__ __forceinline__ void dequant16_k(const LoopPlanes& L, int h, int row,
       s[k] = fast::f16x2_to_f2(sw[k]);
     }
   }
+}
+
+// Decodes the 16 channels 16 sub .. 16 sub + 15 of one stored K row (codes cw)
+// into 8 BF16 pairs.
+__device__ __forceinline__ void dequant16_k(const LoopPlanes& L, int h, int row, uint2 cw, int sub,
+                                            const float4 (*par)[kD / 2], int g0, int ng, uint32_t* out) {
+  float2 m[8], s[8];
+  load_kpar16(L, h, row, sub, par, g0, ng, m, s);
   fast::dequant_word_pp(cw.x, m, s, out);
   fast::dequant_word_pp(cw.y, m + 4, s + 4, out + 4);
 }
@@ -604,7 +625,6 @@ struct EncKSmem {
   int tok[kG];
   int row[R > 0 ? R : 1][kG];
   int glo[R > 0 ? R : 1], ghi[R > 0 ? R : 1];
-  int b;
 };
 
 template <int R>
@@ -621,10 +641,9 @@ __global__ void __launch_bounds__(kEncKThreads) encode_k_fast_kernel(const __gri
   const ItemRange ir = cta_items(prefix, a.n_requests);
   int cur_b = -1;
   for (long long it = ir.begin; it < ir.end; ++it) {
-    if (tid == 0) S.b = owner_of(prefix, a.n_requests, it);
-    __syncthreads();
-    const int b = S.b;
+    const int b = owner_next(prefix, a.n_requests, it, cur_b);
     if (b != cur_b) {
+      __syncthreads();  // every thread is done with the previous request's chain
       if (tid == 0) fill_chain(req_at(a, b), KVQ_K, R + 1, H, S.C);
       cur_b = b;
     }
@@ -797,15 +816,13 @@ __global__ void __launch_bounds__(kEncVFastThreads) encode_v_fast_kernel(const _
   __shared__ Chain C;
   __shared__ int s_tok[kG];
   __shared__ int s_row[RA][kG];
-  __shared__ int s_b;
 
   const ItemRange ir = cta_items(prefix, a.n_requests);
   int cur_b = -1;
   for (long long it = ir.begin; it < ir.end; ++it) {
-    if (threadIdx.x == 0) s_b = owner_of(prefix, a.n_requests, it);
-    __syncthreads();
-    const int b = s_b;
+    const int b = owner_next(prefix, a.n_requests, it, cur_b);
     if (b != cur_b) {
+      __syncthreads();  // every thread is done with the previous request's chain
       if (threadIdx.x == 0) fill_chain(req_at(a, b), KVQ_V, R + 1, H, C);
       cur_b = b;
     }
@@ -958,26 +975,27 @@ __device__ __forceinline__ void build_tile_map(const CodecArgs& a, const Chain& 
   }
 }
 
-// K: item = (64-token tile, head), 256 threads; eight lanes per token (lane
-// `sub` = channels 16 sub .. +15), a warp four tokens, so each token's output
-// row (256 B) leaves in 16-byte stores. The K parameters of the tile's groups
-// (one per dense loop, at most two per sparse loop: its rows in the tile are
-// one compact range of at most 64) are staged as FP32 first.
-constexpr int kReconKThreads = 256;
+// K: item = (64-token tile, head), 128 threads; eight lanes per token (lane
+// `sub` = channels 16 sub .. +15) and four tokens per lane (16 w + 4 u + lg), so
+// a lane loads each loop's parameters once for its four tokens (twice when a
+// sparse loop's rows cross a group), and each token's output row (256 B)
+// leaves in 16-byte stores. The K parameters of the tile's groups (one per
+// dense loop, at most two per sparse loop: its rows in the tile are one compact
+// range of at most 64) are staged as FP32 first.
+constexpr int kReconKThreads = 128;
+constexpr int kReconKTok = 4;
 
 template <int DEPTH>
 struct ReconKSmem {
   float4 par[DEPTH][2][kD / 2];
   Chain C;
   int map[DEPTH][KVQ_TILE];
-  int b;
 };
 
 template <int DEPTH>
 __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(const __grid_constant__ CodecArgs a,
                                                                             const int32_t* prefix_ws) {
   using namespace fast;
-  constexpr int kWarps = kReconKThreads / 32;
   const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sub = lane & 7, lg = lane >> 3;
@@ -987,10 +1005,9 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
   const ItemRange ir = cta_items(prefix, a.n_requests);
   int cur_b = -1;
   for (long long it = ir.begin; it < ir.end; ++it) {
-    if (tid == 0) S.b = owner_of(prefix, a.n_requests, it);
-    __syncthreads();
-    const int b = S.b;
+    const int b = owner_next(prefix, a.n_requests, it, cur_b);
     if (b != cur_b) {
+      __syncthreads();  // every thread is done with the previous request's chain
       if (tid == 0) fill_chain(req_at(a, b), KVQ_K, DEPTH, H, S.C);
       cur_b = b;
     }
@@ -1021,37 +1038,54 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
       if (tid == 0 && a.err) atomicOr(a.err, 16);
       continue;
     }
-#pragma unroll 1
-    for (int i0 = 0; i0 < nvalid; i0 += 4 * kWarps) {
-      const int tt = i0 + 4 * warp + lg;
-      const bool live = tt < nvalid;
-      uint2 cw[DEPTH];
-      int rows[DEPTH];
+    int rows[kReconKTok][DEPTH];
+    uint2 cw[kReconKTok][DEPTH];
+#pragma unroll
+    for (int u = 0; u < kReconKTok; ++u) {
+      const int tt = 16 * warp + 4 * u + lg;
 #pragma unroll
       for (int j = 0; j < DEPTH; ++j) {
-        rows[j] = live ? S.map[j][tt] : -1;
-        cw[j] = make_uint2(0, 0);
-        if (rows[j] >= 0) {
+        rows[u][j] = tt < nvalid ? S.map[j][tt] : -1;
+        cw[u][j] = make_uint2(0, 0);
+        if (rows[u][j] >= 0) {
           const LoopPlanes& L = S.C.loop[j];
-          cw[j] = __ldg(reinterpret_cast<const uint2*>(L.codes + ((long long)h * L.n_rows + rows[j]) * kRowBytes +
-                                                       8 * sub));
+          cw[u][j] = __ldg(reinterpret_cast<const uint2*>(L.codes + ((long long)h * L.n_rows + rows[u][j]) * kRowBytes +
+                                                          8 * sub));
         }
       }
-      uint32_t acc[8];
+    }
+    uint32_t acc[kReconKTok][8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0;
+    for (int u = 0; u < kReconKTok; ++u)
 #pragma unroll
-      for (int j = 0; j < DEPTH; ++j) {
-        if (rows[j] < 0) continue;
+      for (int e = 0; e < 8; ++e) acc[u][e] = 0;
+#pragma unroll
+    for (int j = 0; j < DEPTH; ++j) {
+      const LoopPlanes& L = S.C.loop[j];
+      float2 m[8], s[8];
+      int cached = -0x7FFFFFFF;
+#pragma unroll
+      for (int u = 0; u < kReconKTok; ++u) {
+        const int row = rows[u][j];
+        if (row < 0) continue;
+        if ((row >> 6) != cached) {
+          cached = row >> 6;
+          load_kpar16(L, h, row, sub, S.par[j], g0[j], ng[j], m, s);
+        }
         uint32_t dq[8];
-        dequant16_k(S.C.loop[j], h, rows[j], cw[j], sub, S.par[j], g0[j], ng[j], dq);
+        dequant_word_pp(cw[u][j].x, m, s, dq);
+        dequant_word_pp(cw[u][j].y, m + 4, s + 4, dq + 4);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = (j == 0) ? dq[e] : bf2_add(acc[e], dq[e]);
+        for (int e = 0; e < 8; ++e) acc[u][e] = (j == 0) ? dq[e] : bf2_add(acc[u][e], dq[e]);
       }
-      if (live) {
+    }
+#pragma unroll
+    for (int u = 0; u < kReconKTok; ++u) {
+      const int tt = 16 * warp + 4 * u + lg;
+      if (tt < nvalid) {
         uint4* dst = reinterpret_cast<uint4*>(out + ((long long)(t0 + tt) * H + h) * kD + 16 * sub);
-        dst[0] = make_uint4(acc[0], acc[1], acc[2], acc[3]);
-        dst[1] = make_uint4(acc[4], acc[5], acc[6], acc[7]);
+        dst[0] = make_uint4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+        dst[1] = make_uint4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
       }
     }
   }
@@ -1073,15 +1107,13 @@ __global__ void __launch_bounds__(kReconVFastThreads) reconstruct_v_fast_kernel(
   const int H = a.H;
   __shared__ Chain C;
   __shared__ int s_map[DEPTH][KVQ_TILE];
-  __shared__ int s_b;
 
   const ItemRange ir = cta_items(prefix, a.n_requests);
   int cur_b = -1;
   for (long long it = ir.begin; it < ir.end; ++it) {
-    if (threadIdx.x == 0) s_b = owner_of(prefix, a.n_requests, it);
-    __syncthreads();
-    const int b = s_b;
+    const int b = owner_next(prefix, a.n_requests, it, cur_b);
     if (b != cur_b) {
+      __syncthreads();  // every thread is done with the previous request's chain
       if (threadIdx.x == 0) fill_chain(req_at(a, b), KVQ_V, DEPTH, H, C);
       cur_b = b;
     }
