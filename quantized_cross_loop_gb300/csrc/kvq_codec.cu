@@ -621,6 +621,8 @@ struct EncKSmem {
   uint8_t codes[kG][kRowBytes];                // output codes
   float4 par[R > 0 ? R : 1][kKParGroups][kD / 2];  // staged predecessor parameters
   uint32_t pmn[4][kD / 2], pmx[4][kD / 2];     // partial min/max per row quarter
+  float4 qp[kD / 2];                           // per pair: min lo, min hi, 1/scale lo, 1/scale hi
+  float2 qs[kD / 2];                           // per pair: scales
   Chain C;
   int tok[kG];
   int row[R > 0 ? R : 1][kG];
@@ -628,7 +630,7 @@ struct EncKSmem {
 };
 
 template <int R>
-__global__ void __launch_bounds__(kEncKThreads) encode_k_fast_kernel(const __grid_constant__ CodecArgs a,
+__global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __grid_constant__ CodecArgs a,
                                                                      const int32_t* prefix_ws) {
   using namespace fast;
   constexpr int kWarps = kEncKThreads / 32;
@@ -739,50 +741,57 @@ __global__ void __launch_bounds__(kEncKThreads) encode_k_fast_kernel(const __gri
     }
     __syncthreads();
 
-    // ---- phase 2: per channel pair p, rows of quarter q
+    // ---- phase 2: per channel pair p, rows of quarter q (held in registers)
     const int p = tid & (kD / 2 - 1), q = tid >> 6;
-    const int ia = 16 * q, ib = min(16 * q + 16, len);
-    uint32_t mn2 = 0, mx2 = 0;
-    bool any = false;
-    for (int i = ia; i < ib; ++i) {
-      const uint32_t v = S.delta[i][p];
-      mn2 = any ? bf2_min(mn2, v) : v;
-      mx2 = any ? bf2_max(mx2, v) : v;
-      any = true;
-    }
-    if (any) {
+    const int nr = min(16, len - 16 * q);  // rows of this quarter (<= 0: none)
+    if (nr > 0) {
+      uint32_t v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = S.delta[16 * q + min(k, nr - 1)][p];  // repeats leave min/max unchanged
+      uint32_t mn2 = v[0], mx2 = v[0];
+#pragma unroll
+      for (int k = 1; k < 16; ++k) {
+        mn2 = bf2_min(mn2, v[k]);
+        mx2 = bf2_max(mx2, v[k]);
+      }
       S.pmn[q][p] = mn2;
       S.pmx[q][p] = mx2;
     }
     __syncthreads();
-    const int nq = (len + 15) / 16;
-    mn2 = S.pmn[0][p];
-    mx2 = S.pmx[0][p];
-    for (int qq = 1; qq < nq; ++qq) {
-      mn2 = bf2_min(mn2, S.pmn[qq][p]);
-      mx2 = bf2_max(mx2, S.pmx[qq][p]);
-    }
-    float mn[2] = {bf_lo(mn2), bf_hi(mn2)}, mx[2] = {bf_lo(mx2), bf_hi(mx2)};
-    if (mn[0] == 0.0f || mn[1] == 0.0f || mx[0] == 0.0f || mx[1] == 0.0f) {
-      // the in-order scan keeps the first zero it meets: take its sign
-      bool done[4] = {mn[0] != 0.0f, mn[1] != 0.0f, mx[0] != 0.0f, mx[1] != 0.0f};
-      for (int i = 0; i < len; ++i) {
-        const uint32_t v = S.delta[i][p];
-        const float lo = bf_lo(v), hi = bf_hi(v);
-        if (!done[0] && lo == 0.0f) { mn[0] = lo; done[0] = true; }
-        if (!done[2] && lo == 0.0f) { mx[0] = lo; done[2] = true; }
-        if (!done[1] && hi == 0.0f) { mn[1] = hi; done[1] = true; }
-        if (!done[3] && hi == 0.0f) { mx[1] = hi; done[3] = true; }
+    if (q == 0) {  // the pair's parameters, once
+      const int nq = (len + 15) / 16;
+      uint32_t mn2 = S.pmn[0][p], mx2 = S.pmx[0][p];
+      for (int qq = 1; qq < nq; ++qq) {
+        mn2 = bf2_min(mn2, S.pmn[qq][p]);
+        mx2 = bf2_max(mx2, S.pmx[qq][p]);
       }
-    }
-    const float s0 = scale_of(mn[0], mx[0]), s1 = scale_of(mn[1], mx[1]);
-    const float2 mnv = make_float2(mn[0], mn[1]), sv = make_float2(s0, s1);
-    const float2 rc = make_float2(recip_of(s0), recip_of(s1));
-    for (int i = ia; i < ib; ++i) S.codes[i][p] = uint8_t(quant_pair(S.delta[i][p], mnv, rc, sv));
-    if (q == 0) {
+      float mn[2] = {bf_lo(mn2), bf_hi(mn2)}, mx[2] = {bf_lo(mx2), bf_hi(mx2)};
+      if (mn[0] == 0.0f || mn[1] == 0.0f || mx[0] == 0.0f || mx[1] == 0.0f) {
+        // the in-order scan keeps the first zero it meets: take its sign
+        bool done[4] = {mn[0] != 0.0f, mn[1] != 0.0f, mx[0] != 0.0f, mx[1] != 0.0f};
+        for (int i = 0; i < len; ++i) {
+          const uint32_t w = S.delta[i][p];
+          const float lo = bf_lo(w), hi = bf_hi(w);
+          if (!done[0] && lo == 0.0f) { mn[0] = lo; done[0] = true; }
+          if (!done[2] && lo == 0.0f) { mx[0] = lo; done[2] = true; }
+          if (!done[1] && hi == 0.0f) { mn[1] = hi; done[1] = true; }
+          if (!done[3] && hi == 0.0f) { mx[1] = hi; done[3] = true; }
+        }
+      }
+      const float s0 = scale_of(mn[0], mx[0]), s1 = scale_of(mn[1], mx[1]);
+      S.qp[p] = make_float4(mn[0], mn[1], recip_of(s0), recip_of(s1));
+      S.qs[p] = make_float2(s0, s1);
       const long long pi = ((long long)h * ((n + kG - 1) / kG) + g) * kD + 2 * p;
       *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.mins) + pi) = f16_pair(mn[0], mn[1]);
       *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.scales) + pi) = f16_pair(s0, s1);
+    }
+    __syncthreads();
+    if (nr > 0) {
+      const float4 qp = S.qp[p];
+      const float2 mnv = make_float2(qp.x, qp.y), rc = make_float2(qp.z, qp.w), sv = S.qs[p];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (k < nr) S.codes[16 * q + k][p] = uint8_t(quant_pair(S.delta[16 * q + k][p], mnv, rc, sv));
     }
     __syncthreads();
     // len rows x 64 bytes, contiguous in the head-major plane
