@@ -30,9 +30,11 @@
 //                   tokens as M and the 8 query heads of a KV head as N; the
 //                   softmax stays in the accumulator registers; p * sV becomes
 //                   the PV B operand through movmatrix.trans; PV runs with
-//                   channels as M. A sparse loop contributes over its compact
-//                   rows only; rows and tokens are matched through a 64-bit
-//                   presence mask of the tile and warp shuffles.
+//                   channels as M. Both contractions run in token order: each
+//                   thread addresses the stored row of its tokens (the rank of
+//                   the token in the tile's 64-bit presence mask of a sparse
+//                   loop), and a token without a row in a loop contributes
+//                   neither logit nor value there.
 // Each warp keeps its own online softmax (max, sum, PV accumulators) over its
 // tokens; the group merges the four at the end of a unit. Per tile and group:
 // one named barrier (K-min terms ready). Log2 domain, FP32 throughout.
@@ -528,13 +530,18 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         bits = cnt >= 16 ? 0xFFFF : ((1 << cnt) - 1);
       } else {
         // presence of the tile's tokens in this loop, from its staged index slice
-        unsigned long long mk = 0;
-        for (int i = lane; i < la.x; i += 32) {
-          const int u = st.idx[j][irem + i] - t0;
-          if (u >= 0 && u < KVQ_TILE) mk |= 1ull << u;
-        }
+        // (at most 64 entries: two per lane, OR-reduced over the warp)
+        uint32_t lo = 0, hi = 0;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mk |= __shfl_xor_sync(0xffffffffu, mk, off);
+        for (int i0 = 0; i0 < KVQ_TILE; i0 += 32) {
+          const int i = i0 + lane;
+          const int u = i < la.x ? st.idx[j][irem + i] - t0 : -1;
+          if (u >= 0 && u < 32) lo |= 1u << u;
+          if (u >= 32 && u < KVQ_TILE) hi |= 1u << (u - 32);
+        }
+        lo = __reduce_or_sync(0xffffffffu, lo);
+        hi = __reduce_or_sync(0xffffffffu, hi);
+        const unsigned long long mk = (unsigned long long)hi << 32 | lo;
         bits = int((mk >> (16 * w)) & 0xFFFFull);
         rb = __popcll(mk & ((1ull << (16 * w)) - 1ull));
         cnt = __popc(bits);
@@ -545,43 +552,32 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       const int ga = ((c0 + rb) >> 6) - g0;
       const int gb = ((c0 + rb + cnt - 1) >> 6) - g0;
       const bool split = gb != ga;
-      // A: staged rows rb + g and rb + g + 8, the 16 bytes of chunk q
-      const uint4 wa = *reinterpret_cast<const uint4*>(&st.kc[j][(rb + g) * kRowBytes + 16 * q]);
-      const uint4 wb = *reinterpret_cast<const uint4*>(&st.kc[j][(rb + g + 8) * kRowBytes + 16 * q]);
+      // A: the stored rows of the warp's tokens g and g + 8 (a sparse loop's r-th
+      // present token sits in row rb + r; an absent token reads a valid row whose
+      // logit is then dropped), the 16 bytes of chunk q
+      const int ra = rb + min(__popc(bits & ((1 << g) - 1)), cnt - 1);
+      const int rc = rb + min(__popc(bits & ((1 << (g + 8)) - 1)), cnt - 1);
+      const uint4 wa = *reinterpret_cast<const uint4*>(&st.kc[j][ra * kRowBytes + 16 * q]);
+      const uint4 wb = *reinterpret_cast<const uint4*>(&st.kc[j][rc * kRowBytes + 16 * q]);
       float e[4];
       qk_pass(st, j, ga, qp, wa, wb, q, e);
+      const int Ga = ((c0 + ra) >> 6) - g0, Gc = ((c0 + rc) >> 6) - g0;
       if (split) {  // rows of the second K group: a second pass with that group's Q'
         float f[4];
         qk_pass(st, j, gb, qp, wa, wb, q, f);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int row = k < 2 ? g : g + 8;  // staged row rb + row
-          if (((c0 + rb + row) >> 6) - g0 != ga) e[k] = f[k];
-        }
+        if (Ga != ga) e[0] = f[0], e[1] = f[1];
+        if (Gc != ga) e[2] = f[2], e[3] = f[3];
       }
-      // rows -> the warp's tokens: identity for a dense loop; a sparse loop's row r
-      // holds the r-th present token, fetched by shuffles
       uint32_t pi = 0;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int tok = g + 8 * half;
-        const bool present = (bits >> tok) & 1;
-        int row = tok;
-        float x0 = e[2 * half], x1 = e[2 * half + 1];
-        if (sparse) {  // warp-uniform: fetch row `row` from its owner (every lane sends both halves)
-          row = __popc(bits & ((1 << tok) - 1));
-          const int src = ((row & 7) << 2) | q;
-          const float lo0 = __shfl_sync(0xffffffffu, e[0], src), lo1 = __shfl_sync(0xffffffffu, e[1], src);
-          const float hi0 = __shfl_sync(0xffffffffu, e[2], src), hi1 = __shfl_sync(0xffffffffu, e[3], src);
-          x0 = row < 8 ? lo0 : hi0;
-          x1 = row < 8 ? lo1 : hi1;
-        }
-        if (present) {
-          sv[2 * half] += x0;
-          sv[2 * half + 1] += x1;
-          const int G = ((c0 + rb + row) >> 6) - g0;
-          pi |= (1u | (uint32_t(G) << 1)) << (2 * half);
-        }
+      if ((bits >> g) & 1) {
+        sv[0] += e[0];
+        sv[1] += e[1];
+        pi |= 1u | (uint32_t(Ga) << 1);
+      }
+      if ((bits >> (g + 8)) & 1) {
+        sv[2] += e[2];
+        sv[3] += e[3];
+        pi |= (1u | (uint32_t(Gc) << 1)) << 2;
       }
       (void)ngrp;
       pinfo |= pi << (4 * j);
@@ -649,43 +645,19 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         const SliceInfo si = Gs.slice[w][j];
         if (si.cnt == 0) continue;
         const int vrem = st.meta[16 + 8 * j + 4];
-        const int sparse = st.meta[16 + 8 * j + 6];
-        // p of the slice's stored rows g and g + 8 (zero past cnt)
-        float pr[4];
+        const int bits = si.bits, rb = si.rb, cnt = si.cnt;
+        // P' = p * sV per V group for the warp's tokens g and g + 8 (zero for a token
+        // with no row in this loop), and the V-min terms
+        uint32_t r[2][2];  // [V group][token half] = {P'(token, 2q), P'(token, 2q+1)}
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          const int row = g + 8 * half;
-          if (!sparse) {
-            pr[2 * half] = p[2 * half];
-            pr[2 * half + 1] = p[2 * half + 1];
-          } else {
-            // token of the row-th present bit
-            int tok = 0;
-            {
-              uint32_t bb = uint32_t(si.bits);
-              for (int r = 0; r < row && bb; ++r) bb &= bb - 1;
-              tok = bb ? __ffs(bb) - 1 : 0;
-            }
-            const int src = ((tok & 7) << 2) | q;
-            const float a0 = __shfl_sync(0xffffffffu, p[0], src), a1 = __shfl_sync(0xffffffffu, p[1], src);
-            const float a2 = __shfl_sync(0xffffffffu, p[2], src), a3 = __shfl_sync(0xffffffffu, p[3], src);
-            const float y0 = tok < 8 ? a0 : a2;
-            const float y1 = tok < 8 ? a1 : a3;
-            const bool ok = row < si.cnt;
-            pr[2 * half] = ok ? y0 : 0.f;
-            pr[2 * half + 1] = ok ? y1 : 0.f;
-          }
-        }
-        // P' = p * sV per V group, and the V-min terms
-        uint32_t r[2][2];  // [V group][row half] = {P'(row, 2q), P'(row, 2q+1)}
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int row = g + 8 * half;
-          const bool ok = row < si.cnt;
-          const int vi = vrem + 2 * (si.rb + row);
+          const int tok = g + 8 * half;
+          const bool ok = (bits >> tok) & 1;
+          const int vi = vrem + 2 * (rb + min(__popc(bits & ((1 << tok) - 1)), cnt - 1));
           const uint32_t sraw = ok ? *reinterpret_cast<const uint32_t*>(&st.vsc[j][vi]) : 0u;
           const uint32_t mraw = ok ? *reinterpret_cast<const uint32_t*>(&st.vmin[j][vi]) : 0u;
-          const __half2 pp = __floats2half2_rn(pr[2 * half], pr[2 * half + 1]);
+          const float p0 = ok ? p[2 * half] : 0.f, p1 = ok ? p[2 * half + 1] : 0.f;
+          const __half2 pp = __floats2half2_rn(p0, p1);
           const __half2 sv2 = u2h(sraw);
           const float2 mv = __half22float2(u2h(mraw));
 #pragma unroll
@@ -695,23 +667,28 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
             r[vg][half] = h2u(pv);
             const float2 pf = __half22float2(pv);
             const float mg = vg == 0 ? mv.x : mv.y;
-            U.vb[vg][0] = fmaf(pr[2 * half], mg, fmaf(-64.f, pf.x, U.vb[vg][0]));
-            U.vb[vg][1] = fmaf(pr[2 * half + 1], mg, fmaf(-64.f, pf.y, U.vb[vg][1]));
+            U.vb[vg][0] = fmaf(p0, mg, fmaf(-64.f, pf.x, U.vb[vg][0]));
+            U.vb[vg][1] = fmaf(p1, mg, fmaf(-64.f, pf.y, U.vb[vg][1]));
           }
         }
-        // B operands (k = rows, n = heads) by 8x8 transposes of the (row, head) blocks
+        // B operands (k = tokens, n = heads) by 8x8 transposes of the (token, head) blocks
         const uint32_t B00 = transpose8x8(r[0][0]), B01 = transpose8x8(r[0][1]);
         const uint32_t B10 = transpose8x8(r[1][0]), B11 = transpose8x8(r[1][1]);
-        // A: V codes of staged rows rb + {2q, 2q+1, 2q+8, 2q+9}; thread g takes word
-        // 8*vg + g of each row (channels 64vg + 8g .. +7)
-        const uint8_t* base = &st.vc[j][si.rb * kRowBytes];
+        // A: V codes of the stored rows of tokens 2q, 2q+1, 2q+8, 2q+9 (an absent
+        // token reads a valid row against a zero P'); thread g takes word 8*vg + g of
+        // each row (channels 64vg + 8g .. +7)
+        const uint8_t* base = &st.vc[j][0];
+        const int o0 = (rb + min(__popc(bits & ((1 << (2 * q)) - 1)), cnt - 1)) * kRowBytes;
+        const int o1 = (rb + min(__popc(bits & ((2 << (2 * q)) - 1)), cnt - 1)) * kRowBytes;
+        const int o2 = (rb + min(__popc(bits & ((1 << (2 * q + 8)) - 1)), cnt - 1)) * kRowBytes;
+        const int o3 = (rb + min(__popc(bits & ((2 << (2 * q + 8)) - 1)), cnt - 1)) * kRowBytes;
         uint32_t wv[2][4];
 #pragma unroll
         for (int vg = 0; vg < 2; ++vg) {
-          wv[vg][0] = *reinterpret_cast<const uint32_t*>(base + (2 * q) * kRowBytes + 4 * (8 * vg + g));
-          wv[vg][1] = *reinterpret_cast<const uint32_t*>(base + (2 * q + 1) * kRowBytes + 4 * (8 * vg + g));
-          wv[vg][2] = *reinterpret_cast<const uint32_t*>(base + (2 * q + 8) * kRowBytes + 4 * (8 * vg + g));
-          wv[vg][3] = *reinterpret_cast<const uint32_t*>(base + (2 * q + 9) * kRowBytes + 4 * (8 * vg + g));
+          wv[vg][0] = *reinterpret_cast<const uint32_t*>(base + o0 + 4 * (8 * vg + g));
+          wv[vg][1] = *reinterpret_cast<const uint32_t*>(base + o1 + 4 * (8 * vg + g));
+          wv[vg][2] = *reinterpret_cast<const uint32_t*>(base + o2 + 4 * (8 * vg + g));
+          wv[vg][3] = *reinterpret_cast<const uint32_t*>(base + o3 + 4 * (8 * vg + g));
         }
 #pragma unroll
         for (int vg = 0; vg < 2; ++vg) {
