@@ -955,51 +955,80 @@ __global__ void __launch_bounds__(kEncVFastThreads) encode_v_fast_kernel(const _
 
 // ---------------------------------------------------------------- reconstruct (fast)
 //
-// Both kinds build, per 64-token tile, the stored row of every token in every
-// loop (-1: absent, inherit) from the tile directory.
+// Every warp finds the stored rows of its tile's tokens by itself: a dense
+// loop stores token t at row t; a sparse loop stores the tile's present tokens
+// in the compact rows tile_dir[k] .. tile_dir[k+1]-1, in token order, so the
+// row of a present token is tile_dir[k] plus its rank in the tile's 64-bit
+// presence mask (two warp OR-reductions over the tile's index slice). No
+// block-wide barrier separates the items.
 
-// Fills s_map[j][tt] for loops 0..depth-1 of tile k; returns false (and sets the
-// error bit) if a sparse loop's directory entry is inconsistent.
-__device__ __forceinline__ void build_tile_map(const CodecArgs& a, const Chain& C, int depth, int k, int nvalid,
-                                               int (*s_map)[KVQ_TILE]) {
-  const int t0 = k * KVQ_TILE;
-  for (int idx = threadIdx.x; idx < depth * KVQ_TILE; idx += blockDim.x) {
-    const int j = idx / KVQ_TILE, tt = idx % KVQ_TILE;
-    s_map[j][tt] = (C.loop[j].sparse || tt >= nvalid) ? -1 : t0 + tt;
+struct TileRows {
+  unsigned long long mask;  // presence of tokens t0 .. t0 + 63 in the loop
+  int c0;                   // stored row of the first present token
+};
+
+// Rows of tile k (tokens t0 = 64 k ..) in loop L, computed by a whole warp;
+// an inconsistent directory entry yields an empty mask and sets bit 4.
+__device__ __forceinline__ TileRows tile_rows(const CodecArgs& a, const LoopPlanes& L, int k, int nvalid, int lane) {
+  TileRows r;
+  if (!L.sparse) {
+    r.mask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+    r.c0 = k * KVQ_TILE;
+    return r;
   }
-  __syncthreads();
-  for (int j = 1; j < depth; ++j) {
-    const LoopPlanes& L = C.loop[j];
-    if (!L.sparse) continue;
-    const int c0 = __ldg(L.tile_dir + k), c1 = __ldg(L.tile_dir + k + 1);
-    if (c0 < 0 || c1 > L.n_rows || c0 > c1 || c1 - c0 > KVQ_TILE) {
-      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 4);
-      continue;
-    }
-    for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
-      const int tt = __ldg(L.active + c) - t0;
-      if (tt >= 0 && tt < KVQ_TILE) s_map[j][tt] = c;
+  const int c0 = __ldg(L.tile_dir + k), c1 = __ldg(L.tile_dir + k + 1);
+  r.mask = 0;
+  r.c0 = c0;
+  if (c0 < 0 || c1 > L.n_rows || c0 > c1 || c1 - c0 > KVQ_TILE) {
+    if (lane == 0 && a.err) atomicOr(a.err, 4);
+    return r;
+  }
+  const int t0 = k * KVQ_TILE;
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i0 = 0; i0 < KVQ_TILE; i0 += 32) {
+    const int c = c0 + i0 + lane;
+    if (c < c1) {
+      const int u = __ldg(L.active + c) - t0;
+      if (u >= 0 && u < 32) lo |= 1u << u;
+      else if (u >= 32 && u < KVQ_TILE) hi |= 1u << (u - 32);
       else if (a.err) atomicOr(a.err, 4);
     }
+  }
+  lo = __reduce_or_sync(0xffffffffu, lo);
+  hi = __reduce_or_sync(0xffffffffu, hi);
+  r.mask = (unsigned long long)hi << 32 | lo;
+  return r;
+}
+
+// Stored row of token tt of the tile, or -1 if the loop holds no row for it.
+__device__ __forceinline__ int row_in(const TileRows& r, int tt) {
+  if (!((r.mask >> tt) & 1ull)) return -1;
+  return r.c0 + __popcll(r.mask & ((1ull << tt) - 1ull));
+}
+
+// K parameters of the 16 channels 16 sub .. +15 of group `grp` of head h, loop L.
+__device__ __forceinline__ void load_kpar16_global(const LoopPlanes& L, int h, int grp, int sub, float2* m, float2* s) {
+  const long long pi = ((long long)h * ((L.n_rows + kG - 1) / kG) + grp) * kD + 16 * sub;
+  const uint4* mp = reinterpret_cast<const uint4*>(L.mins + pi);
+  const uint4* sp = reinterpret_cast<const uint4*>(L.scales + pi);
+  const uint4 m0 = __ldg(mp), m1 = __ldg(mp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
+  const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+  const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    m[k] = fast::f16x2_to_f2(mw[k]);
+    s[k] = fast::f16x2_to_f2(sw[k]);
   }
 }
 
 // K: item = (64-token tile, head), 128 threads; eight lanes per token (lane
 // `sub` = channels 16 sub .. +15) and four tokens per lane (16 w + 4 u + lg), so
 // a lane loads each loop's parameters once for its four tokens (twice when a
-// sparse loop's rows cross a group), and each token's output row (256 B)
-// leaves in 16-byte stores. The K parameters of the tile's groups (one per
-// dense loop, at most two per sparse loop: its rows in the tile are one compact
-// range of at most 64) are staged as FP32 first.
+// sparse loop's rows cross a group), and each token's output row (256 B) leaves
+// in 16-byte stores.
 constexpr int kReconKThreads = 128;
 constexpr int kReconKTok = 4;
-
-template <int DEPTH>
-struct ReconKSmem {
-  float4 par[DEPTH][2][kD / 2];
-  Chain C;
-  int map[DEPTH][KVQ_TILE];
-};
 
 template <int DEPTH>
 __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(const __grid_constant__ CodecArgs a,
@@ -1009,7 +1038,7 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sub = lane & 7, lg = lane >> 3;
   const int H = a.H;
-  __shared__ ReconKSmem<DEPTH> S;
+  __shared__ Chain C;
 
   const ItemRange ir = cta_items(prefix, a.n_requests);
   int cur_b = -1;
@@ -1017,31 +1046,14 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
     const int b = owner_next(prefix, a.n_requests, it, cur_b);
     if (b != cur_b) {
       __syncthreads();  // every thread is done with the previous request's chain
-      if (tid == 0) fill_chain(req_at(a, b), KVQ_K, DEPTH, H, S.C);
+      if (tid == 0) fill_chain(req_at(a, b), KVQ_K, DEPTH, H, C);
+      __syncthreads();
       cur_b = b;
     }
-    __syncthreads();
     const int local = int(it - prefix[b]);
     const int k = local / H, h = local % H;
     const int t0 = k * KVQ_TILE;
-    const int nvalid = min(KVQ_TILE, S.C.n_tokens - t0);
-    build_tile_map(a, S.C, DEPTH, k, nvalid, S.map);
-    int g0[DEPTH], ng[DEPTH];
-#pragma unroll
-    for (int j = 0; j < DEPTH; ++j) {
-      const LoopPlanes& L = S.C.loop[j];
-      if (!L.sparse) {
-        g0[j] = k;  // dense: rows t0 .. t0 + nvalid - 1, one group
-        ng[j] = 1;
-      } else {
-        const int c0 = __ldg(L.tile_dir + k), c1 = __ldg(L.tile_dir + k + 1);
-        const bool ok = c0 >= 0 && c1 <= L.n_rows && c0 < c1 && c1 - c0 <= KVQ_TILE;
-        g0[j] = ok ? c0 >> 6 : 0;
-        ng[j] = ok ? ((c1 - 1) >> 6) - (c0 >> 6) + 1 : 0;
-      }
-      stage_kpar(L, h, g0[j], ng[j], S.par[j]);
-    }
-    __syncthreads();
+    const int nvalid = min(KVQ_TILE, C.n_tokens - t0);
     uint16_t* out = a.reqs ? a.out[b] : a.one_out;
     if ((reinterpret_cast<uintptr_t>(out) & 15u) != 0) {
       if (tid == 0 && a.err) atomicOr(a.err, 16);
@@ -1050,17 +1062,17 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
     int rows[kReconKTok][DEPTH];
     uint2 cw[kReconKTok][DEPTH];
 #pragma unroll
-    for (int u = 0; u < kReconKTok; ++u) {
-      const int tt = 16 * warp + 4 * u + lg;
+    for (int j = 0; j < DEPTH; ++j) {
+      const LoopPlanes& L = C.loop[j];
+      const TileRows tr = tile_rows(a, L, k, nvalid, lane);
 #pragma unroll
-      for (int j = 0; j < DEPTH; ++j) {
-        rows[u][j] = tt < nvalid ? S.map[j][tt] : -1;
+      for (int u = 0; u < kReconKTok; ++u) {
+        const int tt = 16 * warp + 4 * u + lg;
+        rows[u][j] = tt < nvalid ? row_in(tr, tt) : -1;
         cw[u][j] = make_uint2(0, 0);
-        if (rows[u][j] >= 0) {
-          const LoopPlanes& L = S.C.loop[j];
+        if (rows[u][j] >= 0)
           cw[u][j] = __ldg(reinterpret_cast<const uint2*>(L.codes + ((long long)h * L.n_rows + rows[u][j]) * kRowBytes +
                                                           8 * sub));
-        }
       }
     }
     uint32_t acc[kReconKTok][8];
@@ -1070,16 +1082,16 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
       for (int e = 0; e < 8; ++e) acc[u][e] = 0;
 #pragma unroll
     for (int j = 0; j < DEPTH; ++j) {
-      const LoopPlanes& L = S.C.loop[j];
+      const LoopPlanes& L = C.loop[j];
       float2 m[8], s[8];
-      int cached = -0x7FFFFFFF;
+      int cached = -1;
 #pragma unroll
       for (int u = 0; u < kReconKTok; ++u) {
         const int row = rows[u][j];
         if (row < 0) continue;
         if ((row >> 6) != cached) {
           cached = row >> 6;
-          load_kpar16(L, h, row, sub, S.par[j], g0[j], ng[j], m, s);
+          load_kpar16_global(L, h, cached, sub, m, s);
         }
         uint32_t dq[8];
         dequant_word_pp(cw[u][j].x, m, s, dq);
@@ -1102,7 +1114,7 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
 
 // V: item = 64-token tile (all heads); eight lanes per (token, head), lane
 // `sub` = channels 16 sub .. +15; a warp takes four consecutive (token, head)
-// pairs, i.e. 1 KB of contiguous output.
+// pairs, i.e. 1 KB of contiguous output, and finds the tile's rows itself.
 constexpr int kReconVFastThreads = 256;
 
 template <int DEPTH>
@@ -1111,11 +1123,10 @@ __global__ void __launch_bounds__(kReconVFastThreads) reconstruct_v_fast_kernel(
   using namespace fast;
   constexpr int kWarps = kReconVFastThreads / 32;
   const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sub = lane & 7, lg = lane >> 3;
   const int H = a.H;
   __shared__ Chain C;
-  __shared__ int s_map[DEPTH][KVQ_TILE];
 
   const ItemRange ir = cta_items(prefix, a.n_requests);
   int cur_b = -1;
@@ -1123,20 +1134,21 @@ __global__ void __launch_bounds__(kReconVFastThreads) reconstruct_v_fast_kernel(
     const int b = owner_next(prefix, a.n_requests, it, cur_b);
     if (b != cur_b) {
       __syncthreads();  // every thread is done with the previous request's chain
-      if (threadIdx.x == 0) fill_chain(req_at(a, b), KVQ_V, DEPTH, H, C);
+      if (tid == 0) fill_chain(req_at(a, b), KVQ_V, DEPTH, H, C);
+      __syncthreads();
       cur_b = b;
     }
-    __syncthreads();
     const int k = int(it - prefix[b]);
     const int t0 = k * KVQ_TILE;
     const int nvalid = min(KVQ_TILE, C.n_tokens - t0);
-    build_tile_map(a, C, DEPTH, k, nvalid, s_map);
-    __syncthreads();
     uint16_t* out = a.reqs ? a.out[b] : a.one_out;
     if ((reinterpret_cast<uintptr_t>(out) & 15u) != 0) {
-      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 16);
+      if (tid == 0 && a.err) atomicOr(a.err, 16);
       continue;
     }
+    TileRows tr[DEPTH];
+#pragma unroll
+    for (int j = 0; j < DEPTH; ++j) tr[j] = tile_rows(a, C.loop[j], k, nvalid, lane);
     const int npairs = nvalid * H;
     for (int q4 = warp; q4 * 4 < npairs; q4 += kWarps) {
       const int pr = q4 * 4 + lg;
@@ -1147,7 +1159,7 @@ __global__ void __launch_bounds__(kReconVFastThreads) reconstruct_v_fast_kernel(
       bool have[DEPTH];
 #pragma unroll
       for (int j = 0; j < DEPTH; ++j) {
-        const int row = live ? s_map[j][tt] : -1;
+        const int row = live ? row_in(tr[j], tt) : -1;
         have[j] = row >= 0;
         cw[j] = make_uint2(0, 0);
         m16[j] = s16[j] = 0;
