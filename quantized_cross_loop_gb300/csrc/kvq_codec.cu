@@ -1233,11 +1233,13 @@ cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, in
     long long cap = (long long)per_sm * sms;
     return int(items >= 0 && items < cap ? items : cap);
   };
+  // Fast kernels: four waves of resident blocks, so that blocks finishing early
+  // take the remaining items and kernels on other streams can interleave.
   auto run = [&](auto kern, int threads) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess || per_sm < 1)
       per_sm = 1;
-    kern<<<grid_for(per_sm), threads, 0, stream>>>(a, prefix);
+    kern<<<grid_for(4 * per_sm), threads, 0, stream>>>(a, prefix);
   };
   switch (mode) {
     case kModeEncK:

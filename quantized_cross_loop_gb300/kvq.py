@@ -388,18 +388,23 @@ def pointer_array(tensors: list, device) -> torch.Tensor:
     return torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=device)
 
 
-def kvq_encode_batch(pool: PackedPool, kind: int, loop: int, x_ptrs: torch.Tensor, stream=None):
+def kvq_encode_batch(pool: PackedPool, kind: int, loop: int, x_ptrs: torch.Tensor, stream=None,
+                     workspace: torch.Tensor | None = None):
     """Encode loop `loop` (0 = base) of `kind` for every request of the pool;
-    x_ptrs: device int64 array of BF16 [T_b, H, D] source pointers."""
+    x_ptrs: device int64 array of BF16 [T_b, H, D] source pointers. Calls that
+    may run concurrently (on different streams) need their own `workspace`
+    (kvq_batch_workspace_bytes(n_requests) bytes); the default is the pool's."""
+    ws = pool.workspace if workspace is None else workspace
     _check(lib().kvq_encode_batch(_dptr(pool.table.table), pool.n_requests, pool.n_heads, pool.head_dim, kind, loop,
-                                  _dptr(x_ptrs), _dptr(pool.workspace), pool.workspace.numel(),
-                                  _stream_handle(stream)), "kvq_encode_batch")
+                                  _dptr(x_ptrs), _dptr(ws), ws.numel(), _stream_handle(stream)), "kvq_encode_batch")
 
 
-def kvq_reconstruct_batch(pool: PackedPool, kind: int, depth: int, out_ptrs: torch.Tensor, stream=None):
+def kvq_reconstruct_batch(pool: PackedPool, kind: int, depth: int, out_ptrs: torch.Tensor, stream=None,
+                          workspace: torch.Tensor | None = None):
+    ws = pool.workspace if workspace is None else workspace
     _check(lib().kvq_reconstruct_batch(_dptr(pool.table.table), pool.n_requests, pool.n_heads, pool.head_dim, kind,
-                                       depth, _dptr(out_ptrs), _dptr(pool.workspace), pool.workspace.numel(),
-                                       _stream_handle(stream)), "kvq_reconstruct_batch")
+                                       depth, _dptr(out_ptrs), _dptr(ws), ws.numel(), _stream_handle(stream)),
+           "kvq_reconstruct_batch")
 
 
 def launch_count() -> int:
