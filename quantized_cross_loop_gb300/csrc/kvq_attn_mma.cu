@@ -64,14 +64,21 @@ constexpr uint32_t kMagic = 0x54005400u;     // FP16 64.0 in both halves
 //   loop j (8 words from 16 + 8j): nrows c0 g0 ngrp vrem irem sparse pbase
 constexpr int kMetaWords = 16 + 8 * kLoops;
 
+// One loop's staged planes of a tile (every field a multiple of 16 bytes, so
+// that each starts on a 16-byte boundary for the bulk copies).
+struct LoopStage {
+  uint8_t kc[KVQ_TILE * kRowBytes];
+  uint8_t vc[KVQ_TILE * kRowBytes];
+  uint16_t kmin[2 * kD];
+  uint16_t ksc[2 * kD];
+  uint16_t vmin[144];  // 64 rows x 2 groups + 16 B rounding slack
+  uint16_t vsc[144];
+  int32_t idx[80];     // 64 indices + rounding slack
+};
+static_assert(sizeof(LoopStage) % 16 == 0, "loop stages keep 16-byte alignment");
+
 struct __align__(128) Stage {
-  uint8_t kc[kLoops][KVQ_TILE * kRowBytes];
-  uint8_t vc[kLoops][KVQ_TILE * kRowBytes];
-  uint16_t kmin[kLoops][2 * kD];
-  uint16_t ksc[kLoops][2 * kD];
-  uint16_t vmin[kLoops][144];  // 64 rows x 2 groups + 16 B rounding slack
-  uint16_t vsc[kLoops][144];
-  int32_t idx[kLoops][80];     // 64 indices + rounding slack
+  LoopStage l[kLoops];
   int32_t meta[kMetaWords];
 };
 
@@ -285,24 +292,24 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       for (int G = 0; G < ngrp; ++G) M[8 + np++] = (j << 1) | G;
       if (n == 0) continue;
       const long long hr = (long long)h * nr[j] + c0;  // first stored row of this head
-      bulk_copy(st.kc[j], kc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
-      bulk_copy(st.vc[j], vc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
+      bulk_copy(st.l[j].kc, kc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
+      bulk_copy(st.l[j].vc, vc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
       const long long gb = ((long long)h * ((nr[j] + kG - 1) / kG) + g0) * kD;
-      bulk_copy(st.kmin[j], kmn[j] + gb, ngrp * kD * 2, &S.full[s]);
-      bulk_copy(st.ksc[j], ksc[j] + gb, ngrp * kD * 2, &S.full[s]);
+      bulk_copy(st.l[j].kmin, kmn[j] + gb, ngrp * kD * 2, &S.full[s]);
+      bulk_copy(st.l[j].ksc, ksc[j] + gb, ngrp * kD * 2, &S.full[s]);
       {  // V params: 4 B per row and plane, moved in whole 16-byte units
         const long long off = hr * 4;
         const long long lo = off & ~15LL;
         const uint32_t nb = uint32_t(((off + (long long)n * 4 + 15) & ~15LL) - lo);
-        bulk_copy(st.vmin[j], reinterpret_cast<const uint8_t*>(vmn[j]) + lo, nb, &S.full[s]);
-        bulk_copy(st.vsc[j], reinterpret_cast<const uint8_t*>(vsc[j]) + lo, nb, &S.full[s]);
+        bulk_copy(st.l[j].vmin, reinterpret_cast<const uint8_t*>(vmn[j]) + lo, nb, &S.full[s]);
+        bulk_copy(st.l[j].vsc, reinterpret_cast<const uint8_t*>(vsc[j]) + lo, nb, &S.full[s]);
         LM[4] = int((off - lo) / 2);
       }
       if (act[j] != nullptr) {
         const long long off = (long long)c0 * 4;
         const long long lo = off & ~15LL;
         const uint32_t nb = uint32_t(((off + (long long)n * 4 + 15) & ~15LL) - lo);
-        bulk_copy(st.idx[j], reinterpret_cast<const uint8_t*>(act[j]) + lo, nb, &S.full[s]);
+        bulk_copy(st.l[j].idx, reinterpret_cast<const uint8_t*>(act[j]) + lo, nb, &S.full[s]);
         LM[5] = int((off - lo) / 4);
       }
     }
@@ -412,7 +419,7 @@ __device__ __forceinline__ void qk_pass(const Stage& st, int j, int G, const uin
   float c[4][4] = {};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint4 sv4 = *reinterpret_cast<const uint4*>(&st.ksc[j][G * kD + 32 * q + 8 * i]);
+    const uint4 sv4 = *reinterpret_cast<const uint4*>(&st.l[j].ksc[G * kD + 32 * q + 8 * i]);
     const uint32_t sp[4] = {__byte_perm(sv4.x, sv4.z, 0x5410), __byte_perm(sv4.x, sv4.z, 0x7632),
                             __byte_perm(sv4.y, sv4.w, 0x5410), __byte_perm(sv4.y, sv4.w, 0x7632)};
     uint32_t bh[4], bl[4];
@@ -495,8 +502,8 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       const bool live = g < npairs;
       const int pj = live ? st.meta[8 + g] : 0;
-      const uint16_t* mrow = &st.kmin[pj >> 1][(pj & 1) * kD];
-      const uint16_t* srow = &st.ksc[pj >> 1][(pj & 1) * kD];
+      const uint16_t* mrow = &st.l[pj >> 1].kmin[(pj & 1) * kD];
+      const uint16_t* srow = &st.l[pj >> 1].ksc[(pj & 1) * kD];
       const __half2 m64 = __float2half2_rn(-64.f);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
@@ -535,7 +542,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
 #pragma unroll
         for (int i0 = 0; i0 < KVQ_TILE; i0 += 32) {
           const int i = i0 + lane;
-          const int u = i < la.x ? st.idx[j][irem + i] - t0 : -1;
+          const int u = i < la.x ? st.l[j].idx[irem + i] - t0 : -1;
           if (u >= 0 && u < 32) lo |= 1u << u;
           if (u >= 32 && u < KVQ_TILE) hi |= 1u << (u - 32);
         }
@@ -557,8 +564,8 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       // logit is then dropped), the 16 bytes of chunk q
       const int ra = rb + min(__popc(bits & ((1 << g) - 1)), cnt - 1);
       const int rc = rb + min(__popc(bits & ((1 << (g + 8)) - 1)), cnt - 1);
-      const uint4 wa = *reinterpret_cast<const uint4*>(&st.kc[j][ra * kRowBytes + 16 * q]);
-      const uint4 wb = *reinterpret_cast<const uint4*>(&st.kc[j][rc * kRowBytes + 16 * q]);
+      const uint4 wa = *reinterpret_cast<const uint4*>(&st.l[j].kc[ra * kRowBytes + 16 * q]);
+      const uint4 wb = *reinterpret_cast<const uint4*>(&st.l[j].kc[rc * kRowBytes + 16 * q]);
       float e[4];
       qk_pass(st, j, ga, qp, wa, wb, q, e);
       const int Ga = ((c0 + ra) >> 6) - g0, Gc = ((c0 + rc) >> 6) - g0;
@@ -654,8 +661,8 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
           const int tok = g + 8 * half;
           const bool ok = (bits >> tok) & 1;
           const int vi = vrem + 2 * (rb + min(__popc(bits & ((1 << tok) - 1)), cnt - 1));
-          const uint32_t sraw = ok ? *reinterpret_cast<const uint32_t*>(&st.vsc[j][vi]) : 0u;
-          const uint32_t mraw = ok ? *reinterpret_cast<const uint32_t*>(&st.vmin[j][vi]) : 0u;
+          const uint32_t sraw = ok ? *reinterpret_cast<const uint32_t*>(&st.l[j].vsc[vi]) : 0u;
+          const uint32_t mraw = ok ? *reinterpret_cast<const uint32_t*>(&st.l[j].vmin[vi]) : 0u;
           const float p0 = ok ? p[2 * half] : 0.f, p1 = ok ? p[2 * half + 1] : 0.f;
           const __half2 pp = __floats2half2_rn(p0, p1);
           const __half2 sv2 = u2h(sraw);
@@ -677,7 +684,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         // A: V codes of the stored rows of tokens 2q, 2q+1, 2q+8, 2q+9 (an absent
         // token reads a valid row against a zero P'); thread g takes word 8*vg + g of
         // each row (channels 64vg + 8g .. +7)
-        const uint8_t* base = &st.vc[j][0];
+        const uint8_t* base = &st.l[j].vc[0];
         const int o0 = (rb + min(__popc(bits & ((1 << (2 * q)) - 1)), cnt - 1)) * kRowBytes;
         const int o1 = (rb + min(__popc(bits & ((2 << (2 * q)) - 1)), cnt - 1)) * kRowBytes;
         const int o2 = (rb + min(__popc(bits & ((1 << (2 * q + 8)) - 1)), cnt - 1)) * kRowBytes;
