@@ -169,10 +169,32 @@ typedef struct kvq_loop_ref {
   uint16_t* v_scales;
 } kvq_loop_ref;
 
+/*
+ * BF16 segments read by the decode attention next to the packed chain (RFC
+ * §3.3: a rolling BF16 tail of the newest tokens, flushed into the packed form
+ * in whole 64-token groups, so 64..127 tokens remain; INT4 codec PR review:
+ * the first tokens and a recent window kept in BF16).
+ *   sink: the first n_sink tokens (n_sink <= n_tokens) are read from sink_k /
+ *         sink_v (BF16 [n_sink][H][D]) instead of the packed chain;
+ *   tail: n_tail further tokens (positions n_tokens .. n_tokens + n_tail - 1)
+ *         from tail_k / tail_v (BF16 [n_tail][H][D]).
+ * Zero counts (the default of kvq_request_fill) read the packed chain alone.
+ * Pointers must be 16-byte aligned when their count is nonzero; a request
+ * whose segment fields are inconsistent gets a NaN output and sets the error
+ * word, like any inconsistent table entry.
+ */
+#define KVQ_MAX_SEGMENT 1024 /* largest n_sink + n_tail per request */
+
 typedef struct kvq_request {
   int32_t n_tokens; /* T of this request (>= 0) */
   int32_t n_loops;  /* loops stored (>= the requested depth) */
   kvq_loop_ref loop[KVQ_MAX_LOOPS];
+  int32_t n_sink;   /* BF16 sink tokens (0: none) */
+  int32_t n_tail;   /* BF16 tail tokens (0: none) */
+  const uint16_t* sink_k;
+  const uint16_t* sink_v;
+  const uint16_t* tail_k;
+  const uint16_t* tail_v;
 } kvq_request;
 
 /* Host helper: fill one kvq_request from the K and V stream descriptors of a

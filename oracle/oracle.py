@@ -238,6 +238,28 @@ def attention_f32(q: np.ndarray, kf: np.ndarray, vf: np.ndarray, scale: float) -
     return out
 
 
+def attention_with_segments(q: np.ndarray, kf: np.ndarray, vf: np.ndarray, scale: float,
+                            sink_k: np.ndarray | None = None, sink_v: np.ndarray | None = None,
+                            tail_k: np.ndarray | None = None, tail_v: np.ndarray | None = None) -> np.ndarray:
+    """FP32 decode attention over the FP32-decoded chain kf, vf [T, H, D] with the
+    BF16 segments of a request (FlashLoop RFC §3.3 rolling BF16 tail; INT4 codec
+    PR review, BF16 sink tokens): the first n_sink tokens take their BF16 values
+    from sink_k / sink_v [n_sink, H, D] instead of the chain, and the tail tokens
+    tail_k / tail_v [n_tail, H, D] follow the T chain tokens. BF16 as uint16 bits."""
+    kf = np.array(kf, dtype=np.float32, copy=True)
+    vf = np.array(vf, dtype=np.float32, copy=True)
+    if sink_k is not None and len(sink_k):
+        n = len(sink_k)
+        kf[:n] = bf16_bits_to_f32(sink_k)
+        vf[:n] = bf16_bits_to_f32(sink_v)
+    if tail_k is not None and len(tail_k):
+        kf = np.concatenate([kf, bf16_bits_to_f32(tail_k)], axis=0)
+        vf = np.concatenate([vf, bf16_bits_to_f32(tail_v)], axis=0)
+    if kf.shape[0] == 0:  # nothing to attend: zero output
+        return np.zeros(np.asarray(q).shape, dtype=np.float32)
+    return attention_f32(q, kf, vf, scale)
+
+
 def request_path(xk: list[np.ndarray], xv: list[np.ndarray], actives: list[np.ndarray | None], q: np.ndarray,
                  depth: int, scale: float):
     """The whole path for one request: encode both chains, reconstruct to

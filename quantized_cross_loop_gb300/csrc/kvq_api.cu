@@ -420,13 +420,12 @@ kvq_status kvq_request_fill(const kvq_stream* k_loops, const kvq_stream* v_loops
 }
 
 size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim) {
-  (void)n_q_heads;
   (void)head_dim;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   int sms = sm_count(dev);
-  if (n_requests < 0 || n_heads < 1 || sms <= 0) return 0;
-  return ws_bytes(n_requests, n_heads, sms * kMaxCtasPerSm);
+  if (n_requests < 0 || n_heads < 1 || n_q_heads < 1 || sms <= 0) return 0;
+  return ws_bytes(n_requests, n_heads, n_q_heads, sms * kMaxCtasPerSm);
 }
 
 kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads,
@@ -452,7 +451,7 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
   const int sms = sm_count(dev);
   if (sms <= 0) return fail(KVQ_ERR_CUDA, "cannot read the SM count of device %d", dev);
-  const size_t need = ws_bytes(n_requests, n_heads, sms * kMaxCtasPerSm);
+  const size_t need = ws_bytes(n_requests, n_heads, n_q_heads, sms * kMaxCtasPerSm);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
     return fail(KVQ_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", need);
   if (algo == KVQ_ATTN_AUTO) algo = depth <= kMmaMaxDepth ? KVQ_ATTN_MMA : KVQ_ATTN_SIMT;
@@ -475,6 +474,7 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   a.err = reinterpret_cast<int32_t*>(ws);
   a.prefix = reinterpret_cast<int32_t*>(ws + ws_prefix_offset());
   a.partials = reinterpret_cast<float*>(ws + ws_partials_offset(n_requests));
+  a.stats = reinterpret_cast<float2*>(ws + ws_stats_offset(n_requests, n_heads, sms * kMaxCtasPerSm));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   e = cudaMemsetAsync(a.err, 0, 16, s);
   if (e != cudaSuccess) return cuda_status(e, "clear error word");
@@ -484,6 +484,8 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   if (e != cudaSuccess) return cuda_status(e, "attention launch");
   e = launch_combine(a, s);
   if (e != cudaSuccess) return cuda_status(e, "combine launch");
+  e = launch_segments(a, s);
+  if (e != cudaSuccess) return cuda_status(e, "segment launch");
   return ok();
 }
 

@@ -33,16 +33,22 @@ struct AttnArgs {
   int32_t* err;       // error word
   int32_t* prefix;    // [B+1] tile prefix
   float* partials;    // slots
+  float2* stats;      // [B][Hq] (max in log2 units, sum of exponentials) of the packed part
 };
 
 // Workspace layout: [0,16) error word; then int32 prefix[B+1] (rounded to 16 B);
-// then (n_ctas + B*H) partial slots of kSlotFloats floats.
+// then (n_ctas + B*H) partial slots of kSlotFloats floats; then float2
+// stats[B*Hq] (the packed part's softmax max and sum, merged with the BF16
+// segments afterwards).
 __host__ __device__ inline size_t ws_prefix_offset() { return 16; }
 __host__ __device__ inline size_t ws_partials_offset(int B) {
   return 16 + ((size_t(B) + 1) * 4 + 15) / 16 * 16;
 }
-__host__ __device__ inline size_t ws_bytes(int B, int H, int n_ctas) {
+__host__ __device__ inline size_t ws_stats_offset(int B, int H, int n_ctas) {
   return ws_partials_offset(B) + (size_t(n_ctas) + size_t(B) * H) * kSlotFloats * 4;
+}
+__host__ __device__ inline size_t ws_bytes(int B, int H, int Hq, int n_ctas) {
+  return ws_stats_offset(B, H, n_ctas) + (size_t(B) * Hq * 8 + 15) / 16 * 16;
 }
 
 __device__ __forceinline__ long long cta_start(int c, long long W, int C) { return (long long)c * W / C; }
@@ -68,9 +74,20 @@ __device__ __forceinline__ int request_of(const int32_t* prefix, int B, long lon
 
 __device__ __forceinline__ int n_tiles_of(int T) { return (T + KVQ_TILE - 1) / KVQ_TILE; }
 
+// BF16 segment fields of a request entry (sink within the packed tokens, at
+// most KVQ_MAX_SEGMENT tokens in all, aligned buffers for nonzero counts).
+__device__ __forceinline__ bool segments_ok(const kvq_request& r) {
+  if (r.n_sink < 0 || r.n_tail < 0 || r.n_sink > r.n_tokens || r.n_sink + r.n_tail > KVQ_MAX_SEGMENT) return false;
+  auto aligned = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (r.n_sink > 0 && !(aligned(r.sink_k) && aligned(r.sink_v))) return false;
+  if (r.n_tail > 0 && !(aligned(r.tail_k) && aligned(r.tail_v))) return false;
+  return true;
+}
+
 // A request entry the kernels can read without going out of bounds.
 __device__ __forceinline__ bool request_ok(const kvq_request& r, int depth) {
   if (r.n_tokens < 0 || r.n_loops < depth || r.n_loops > KVQ_MAX_LOOPS) return false;
+  if (!segments_ok(r)) return false;
   if (r.n_tokens == 0) return true;
   if (r.loop[0].active_idx != nullptr || r.loop[0].n_rows != r.n_tokens) return false;
   for (int j = 0; j < depth; ++j) {
@@ -87,6 +104,7 @@ __device__ __forceinline__ bool request_ok(const kvq_request& r, int depth) {
 
 cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_segments(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
 int attn_ctas(int algo, int device);

@@ -59,7 +59,9 @@ constexpr long long kWaitNs = 2000000000LL;  // bounded waits: 2 s, then flag an
 constexpr uint32_t kMagic = 0x54005400u;     // FP16 64.0 in both halves
 
 // Per-tile metadata written by the producer (int32 words).
-//   [0] unit  [1] b  [2] h  [3] t0  [4] nvalid  [5] whole  [6] npairs  [7] -
+//   [0] unit  [1] b  [2] h  [3] t0  [4] nvalid  [5] whole  [6] npairs
+//   [7] first token of the tile read from the packed chain (later ones; earlier
+//       tokens belong to the request's BF16 sink)
 //   pair p (8 words from 8): loop index << 1 | group
 //   loop j (8 words from 16 + 8j): nrows c0 g0 ngrp vrem irem sparse pbase
 constexpr int kMetaWords = 16 + 8 * kLoops;
@@ -206,7 +208,7 @@ template <int DEPTH>
 __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long long e0) {
   int b = request_of(a.prefix, a.n_requests, s0);
   long long us = 0, ue = -1;  // current unit's tile range
-  int h = 0, T = 0, unit = -1;
+  int h = 0, T = 0, unit = -1, nsink = 0;
   int nr[DEPTH];
   const int32_t* act[DEPTH];
   const int32_t* dir[DEPTH];
@@ -222,6 +224,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       while (a.prefix[b + 1] <= x) ++b;
       const kvq_request& R = a.reqs[b];
       T = R.n_tokens;
+      nsink = R.n_sink;
       const int nt = n_tiles_of(T);
       const long long rb = a.prefix[b];
       h = int((x - rb) / nt);
@@ -269,6 +272,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
     M[3] = k * KVQ_TILE;
     M[4] = min(KVQ_TILE, T - k * KVQ_TILE);
     M[5] = (us >= s0 && ue <= e0) ? 1 : 0;
+    M[7] = max(0, min(KVQ_TILE, nsink - k * KVQ_TILE));
     int np = 0;
 #pragma unroll
     for (int j = 0; j < DEPTH; ++j) {
@@ -399,6 +403,9 @@ __device__ void finish_unit(const AttnArgs& a, GroupSmem& G, UnitState& U, const
     const float o = (G.fin[0][d][hh] + G.fin[1][d][hh]) + (G.fin[2][d][hh] + G.fin[3][d][hh]) + vb;
     if (M.whole) {
       a.out[((long long)M.b * a.Hq + (long long)M.h * gq + hh) * kD + d] = o / lt;
+      if (d == 0)
+        a.stats[(long long)M.b * a.Hq + (long long)M.h * gq + hh] =
+            make_float2(fmaxf(fmaxf(G.red[0][hh], G.red[1][hh]), fmaxf(G.red[2][hh], G.red[3][hh])), lt);
     } else {
       slot[2 * kMaxG + hh * kD + d] = o;
       if (d == 0) {
@@ -468,7 +475,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
     const Stage& st = S.st[s];
     const int4 m0 = *reinterpret_cast<const int4*>(&st.meta[0]);
     const int4 m1 = *reinterpret_cast<const int4*>(&st.meta[4]);
-    const int unit = m0.x, t0 = m0.w, nvalid = m1.x, npairs = m1.z;
+    const int unit = m0.x, t0 = m0.w, nvalid = m1.x, npairs = m1.z, tfirst = m1.w;
     if (unit != cur_unit) {
       if (cur_unit >= 0) finish_unit(a, Gs, U, Mprev, grp, vcta, w, lane);
       cur_unit = unit;
@@ -608,7 +615,8 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         }
       }
       const bool h0ok = 2 * q < gq, h1ok = 2 * q + 1 < gq;
-      const bool t0ok = 16 * w + g < nvalid, t1ok = 16 * w + g + 8 < nvalid;
+      const bool t0ok = 16 * w + g < nvalid && 16 * w + g >= tfirst;
+      const bool t1ok = 16 * w + g + 8 < nvalid && 16 * w + g + 8 >= tfirst;
       sv[0] = (t0ok && h0ok) ? sv[0] * lsc : -INFINITY;
       sv[1] = (t0ok && h1ok) ? sv[1] * lsc : -INFINITY;
       sv[2] = (t1ok && h0ok) ? sv[2] * lsc : -INFINITY;

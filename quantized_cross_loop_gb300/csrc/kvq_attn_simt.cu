@@ -81,13 +81,15 @@ __global__ void __launch_bounds__(kD) combine_kernel(AttnArgs a) {
   const int g = a.g;
   const kvq_request& r = a.reqs[b];
   float* outp = a.out + ((long long)b * a.Hq + (long long)h * g) * kD;
+  float2* stats = a.stats + (long long)b * a.Hq + (long long)h * g;
   if (!request_ok(r, a.depth)) {
     for (int i = 0; i < g; ++i) outp[i * kD + d] = __int_as_float(0x7fc00000);
     return;
   }
   const int nt = n_tiles_of(r.n_tokens);
-  if (nt == 0) {
+  if (nt == 0) {  // no packed tokens: zero output and an empty softmax state
     for (int i = 0; i < g; ++i) outp[i * kD + d] = 0.0f;
+    if (d < g) stats[d] = make_float2(-INFINITY, 0.0f);
     return;
   }
   const long long W = a.prefix[a.n_requests];
@@ -113,12 +115,108 @@ __global__ void __launch_bounds__(kD) combine_kernel(AttnArgs a) {
       acc += slot[2 * kMaxG + i * kD + d] * w;
     }
     outp[i * kD + d] = acc / L;
+    if (d == 0) stats[i] = make_float2(M, L);
   }
 }
 
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
   combine_kernel<<<a.n_requests * a.H, kD, 0, stream>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- BF16 segments
+//
+// One block per (request, KV head): the request's BF16 sink and tail tokens are
+// attended in FP32 (log2 domain, online over chunks of 32 tokens), then merged
+// by log-sum-exp with the packed part's result and its (max, sum) state.
+
+constexpr int kSegChunk = 32;
+constexpr float kSegLog2e = 1.4426950408889634f;
+
+__global__ void __launch_bounds__(kD) segment_kernel(AttnArgs a) {
+  const int u = blockIdx.x;
+  const int b = u / a.H, h = u % a.H;
+  const int tid = threadIdx.x;  // channel
+  const int g = a.g;
+  const kvq_request& r = a.reqs[b];
+  if (!request_ok(r, a.depth)) return;  // the output is already NaN
+  const int ns = r.n_sink, n = r.n_sink + r.n_tail;
+  if (n == 0) return;
+  __shared__ float qs[kMaxG][kD + 1];
+  __shared__ float kt[kSegChunk][kD + 1];
+  __shared__ float vt[kSegChunk][kD];
+  __shared__ float lg[kSegChunk][kMaxG];
+  __shared__ float sm[kMaxG], sl[kMaxG], alpha[kMaxG];
+  const float qscale = a.scale * kSegLog2e;
+  for (int i = 0; i < g; ++i)
+    qs[i][tid] = bf16_bits_to_f32(a.q[((long long)b * a.Hq + (long long)h * g + i) * kD + tid]) * qscale;
+  if (tid < kMaxG) {
+    sm[tid] = -INFINITY;
+    sl[tid] = 0.0f;
+  }
+  float acc[kMaxG];
+#pragma unroll
+  for (int i = 0; i < kMaxG; ++i) acc[i] = 0.0f;
+  __syncthreads();
+  for (int c0 = 0; c0 < n; c0 += kSegChunk) {
+    const int cn = min(kSegChunk, n - c0);
+    for (int t = 0; t < cn; ++t) {
+      const int tok = c0 + t;
+      const long long row = tok < ns ? ((long long)tok * a.H + h) * kD : ((long long)(tok - ns) * a.H + h) * kD;
+      const uint16_t* kr = tok < ns ? r.sink_k : r.tail_k;
+      const uint16_t* vr = tok < ns ? r.sink_v : r.tail_v;
+      kt[t][tid] = bf16_bits_to_f32(kr[row + tid]);
+      vt[t][tid] = bf16_bits_to_f32(vr[row + tid]);
+    }
+    __syncthreads();
+    for (int idx = tid; idx < cn * g; idx += blockDim.x) {  // logits: one (token, head) pair per thread
+      const int t = idx / g, i = idx % g;
+      float sacc = 0.0f;
+      for (int d = 0; d < kD; ++d) sacc = fmaf(qs[i][d], kt[t][d], sacc);
+      lg[t][i] = sacc;
+    }
+    __syncthreads();
+    if (tid < g) {
+      float mt = -INFINITY;
+      for (int t = 0; t < cn; ++t) mt = fmaxf(mt, lg[t][tid]);
+      const float mn = fmaxf(sm[tid], mt);
+      const float al = (sm[tid] == -INFINITY) ? 0.0f : exp2f(sm[tid] - mn);
+      float sum = 0.0f;
+      for (int t = 0; t < cn; ++t) {
+        const float p = exp2f(lg[t][tid] - mn);
+        lg[t][tid] = p;
+        sum += p;
+      }
+      alpha[tid] = al;
+      sl[tid] = sl[tid] * al + sum;
+      sm[tid] = mn;
+    }
+    __syncthreads();
+    for (int i = 0; i < g; ++i) {
+      float sacc = acc[i] * alpha[i];
+      for (int t = 0; t < cn; ++t) sacc = fmaf(lg[t][i], vt[t][tid], sacc);
+      acc[i] = sacc;
+    }
+    __syncthreads();
+  }
+  for (int i = 0; i < g; ++i) {
+    const long long oi = (long long)b * a.Hq + (long long)h * g + i;
+    const float2 st = a.stats[oi];  // the packed part: max (log2 units), sum
+    const bool packed = st.y > 0.0f && st.x != -INFINITY;
+    const float M = packed ? fmaxf(st.x, sm[i]) : sm[i];
+    const float w0 = packed ? exp2f(st.x - M) : 0.0f;
+    const float w1 = exp2f(sm[i] - M);
+    const float num = (packed ? a.out[oi * kD + tid] * (st.y * w0) : 0.0f) + acc[i] * w1;
+    const float den = (packed ? st.y * w0 : 0.0f) + sl[i] * w1;
+    a.out[oi * kD + tid] = num / den;
+  }
+}
+
+cudaError_t launch_segments(const AttnArgs& a, cudaStream_t stream) {
+  if (a.n_requests == 0) return cudaSuccess;
+  segment_kernel<<<a.n_requests * a.H, kD, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }
@@ -182,6 +280,7 @@ __device__ void simt_finish_unit(const AttnArgs& a, SimtSmem& S, float* acc, int
       int i = k / kD, d = k % kD;
       a.out[((long long)b * a.Hq + (long long)h * g + i) * kD + d] = acc[n] / S.l[i];
     }
+    if (tid < g) a.stats[(long long)b * a.Hq + (long long)h * g + tid] = make_float2(S.m[tid], S.l[tid]);
   } else {
     float* slot = a.partials + (size_t)(blockIdx.x + u) * kSlotFloats;
     if (tid < g) {
@@ -273,7 +372,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
       for (int idx = tid; idx < KVQ_TILE * g; idx += blockDim.x) {
         int tt = idx / g, i = idx % g;
         float sacc = -INFINITY;
-        if (tt < nvalid) {
+        if (tt < nvalid && t0 + tt >= r.n_sink) {  // sink tokens are read from their BF16 copy instead
           sacc = 0.0f;
           for (int d = 0; d < kD; ++d) sacc = fmaf(S.q[i][d], S.khat[tt][d], sacc);
         }
@@ -287,7 +386,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
         float al = (S.m[tid] == -INFINITY) ? 0.0f : exp2f(S.m[tid] - mn);
         float sum = 0.0f;
         for (int tt = 0; tt < KVQ_TILE; ++tt) {
-          float p = tt < nvalid ? exp2f(S.p[tt][tid] - mn) : 0.0f;
+          float p = (tt < nvalid && S.p[tt][tid] != -INFINITY) ? exp2f(S.p[tt][tid] - mn) : 0.0f;
           S.p[tt][tid] = p;
           sum += p;
         }

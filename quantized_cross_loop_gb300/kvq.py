@@ -80,6 +80,12 @@ class kvq_request(ctypes.Structure):
         ("n_tokens", ctypes.c_int32),
         ("n_loops", ctypes.c_int32),
         ("loop", kvq_loop_ref * KVQ_MAX_LOOPS),
+        ("n_sink", ctypes.c_int32),
+        ("n_tail", ctypes.c_int32),
+        ("sink_k", ctypes.c_void_p),
+        ("sink_v", ctypes.c_void_p),
+        ("tail_k", ctypes.c_void_p),
+        ("tail_v", ctypes.c_void_p),
     ]
 
 
@@ -268,20 +274,34 @@ class RequestTable:
     """Device array of kvq_request for a batch of requests (each a pair of K and
     V stream lists). Holds references to the streams so their planes outlive it."""
 
-    def __init__(self, k_chains: list, v_chains: list, device=None):
+    def __init__(self, k_chains: list, v_chains: list, device=None, segments: list | None = None):
+        """segments[b]: None, or (sink_k, sink_v, tail_k, tail_v) — BF16 device
+        tensors [n, H, D] (or None) read by the attention next to the packed
+        chain: the sink replaces the first tokens, the tail follows the last."""
         n = len(k_chains)
         host = (kvq_request * max(n, 1))()
+        keep = []
         for b in range(n):
             ks, vs = k_chains[b], v_chains[b]
             ka = (kvq_stream * len(ks))(*[s.desc for s in ks])
             va = (kvq_stream * len(vs))(*[s.desc for s in vs])
             _check(lib().kvq_request_fill(ka, va, len(ks), ctypes.byref(host[b])), f"kvq_request_fill[{b}]")
+            seg = segments[b] if segments is not None else None
+            if seg is not None:
+                sk, sv, tk, tv = seg
+                for name, t in (("sink_k", sk), ("sink_v", sv), ("tail_k", tk), ("tail_v", tv)):
+                    if t is not None:
+                        _require_cuda(t, name, torch.bfloat16)
+                        setattr(host[b], name, t.data_ptr() if t.numel() else None)
+                        keep.append(t)
+                host[b].n_sink = 0 if sk is None else int(sk.shape[0])
+                host[b].n_tail = 0 if tk is None else int(tk.shape[0])
         raw = bytes(memoryview(host).cast("B"))
         if device is None:
             device = k_chains[0][0].codes.device if n else torch.device("cuda")
         self.table = torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(device)
         self.n_requests = n
-        self._keep = (k_chains, v_chains)
+        self._keep = (k_chains, v_chains, keep)
 
 
 def kvq_decode_attn_workspace_bytes(n_requests: int, n_heads: int, n_q_heads: int, head_dim: int) -> int:

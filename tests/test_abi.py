@@ -53,8 +53,9 @@ def test_struct_layouts_match_header():
 #include <stdio.h>
 #include <stddef.h>
 #include "kvq.h"
-int main(void){printf("%zu %zu %zu %zu %zu\n", sizeof(kvq_stream), offsetof(kvq_stream, codes),
-  offsetof(kvq_stream, tile_dir), sizeof(kvq_loop_ref), sizeof(kvq_request)); return 0;}
+int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_stream), offsetof(kvq_stream, codes),
+  offsetof(kvq_stream, tile_dir), sizeof(kvq_loop_ref), sizeof(kvq_request), offsetof(kvq_request, n_sink),
+  offsetof(kvq_request, tail_v)); return 0;}
 '''
     import subprocess
     import tempfile
@@ -66,7 +67,8 @@ int main(void){printf("%zu %zu %zu %zu %zu\n", sizeof(kvq_stream), offsetof(kvq_
         subprocess.run(["gcc", "-I" + os.path.join(ROOT, "include"), c, "-o", exe], check=True)
         got = [int(v) for v in subprocess.run([exe], capture_output=True, text=True).stdout.split()]
     assert got == [ctypes.sizeof(kvq.kvq_stream), kvq.kvq_stream.codes.offset, kvq.kvq_stream.tile_dir.offset,
-                   ctypes.sizeof(kvq.kvq_loop_ref), ctypes.sizeof(kvq.kvq_request)]
+                   ctypes.sizeof(kvq.kvq_loop_ref), ctypes.sizeof(kvq.kvq_request), kvq.kvq_request.n_sink.offset,
+                   kvq.kvq_request.tail_v.offset]
 
 
 def test_plane_sizes_and_payload(L):

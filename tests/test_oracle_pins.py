@@ -508,3 +508,60 @@ def test_attention_f32_matches_float64_sdpa_on_decoded_chain():
     vt = torch.from_numpy(vf.astype(np.float64)).permute(1, 0, 2).repeat_interleave(g, 0).unsqueeze(0)
     ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=1 / math.sqrt(D)).reshape(Hq, D)
     assert np.max(np.abs(out - ref.numpy())) < 2e-5
+
+
+# ---------------------------------------------------------------- BF16 sink and tail segments
+
+
+def _sdpa64_rows(q, krows, vrows, scale, Hq):
+    """float64 SDPA over explicit K/V rows [N, H, D] (float64 arrays)."""
+    N, H, D = krows.shape
+    g = Hq // H
+    qt = torch.from_numpy(f32(q).astype(np.float64)).reshape(1, Hq, 1, D)
+    kt = torch.from_numpy(krows).permute(1, 0, 2).repeat_interleave(g, 0).unsqueeze(0)
+    vt = torch.from_numpy(vrows).permute(1, 0, 2).repeat_interleave(g, 0).unsqueeze(0)
+    return torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale).reshape(Hq, D).numpy()
+
+
+def test_segments_absent_is_the_chain_attention():
+    rng = np.random.default_rng(31)
+    T, H, Hq, D = 90, 2, 8, 128
+    kf = rng.standard_normal((T, H, D)).astype(np.float32)
+    vf = rng.standard_normal((T, H, D)).astype(np.float32)
+    q = bf16(rng.standard_normal((Hq, D)))
+    empty = np.zeros((0, H, D), dtype=np.uint16)
+    a = O.attention_f32(q, kf, vf, 0.088)
+    assert np.array_equal(O.attention_with_segments(q, kf, vf, 0.088), a)
+    assert np.array_equal(O.attention_with_segments(q, kf, vf, 0.088, empty, empty, empty, empty), a)
+
+
+@pytest.mark.parametrize("T,ns,nt", [(90, 4, 64), (64, 64, 127), (0, 0, 100), (130, 0, 1), (70, 3, 0)])
+def test_segments_replace_the_sink_and_append_the_tail(T, ns, nt):
+    """FlashLoop RFC §3.3 rolling BF16 tail and the BF16 sink of the codec PR
+    review: against float64 attention over the rows assembled independently
+    (sink values for the first tokens, chain values after them, tail last)."""
+    rng = np.random.default_rng(T + 7 * ns + nt)
+    H, Hq, D = 2, 8, 128
+    kf = rng.standard_normal((T, H, D)).astype(np.float32)
+    vf = rng.standard_normal((T, H, D)).astype(np.float32)
+    sk, sv = bf16(rng.standard_normal((ns, H, D))), bf16(rng.standard_normal((ns, H, D)))
+    tk, tv = bf16(rng.standard_normal((nt, H, D))), bf16(rng.standard_normal((nt, H, D)))
+    q = bf16(rng.standard_normal((Hq, D)))
+    out = O.attention_with_segments(q, kf, vf, 0.088, sk, sv, tk, tv)
+    krows = np.concatenate([f32(sk).astype(np.float64), kf[ns:].astype(np.float64), f32(tk).astype(np.float64)])
+    vrows = np.concatenate([f32(sv).astype(np.float64), vf[ns:].astype(np.float64), f32(tv).astype(np.float64)])
+    assert krows.shape[0] == T + nt
+    ref = _sdpa64_rows(q, krows, vrows, 0.088, Hq)
+    assert np.max(np.abs(out - ref)) < 2e-5
+    # the sink replaces tokens: the original chain values of those tokens are not read
+    if ns:
+        kf2, vf2 = kf.copy(), vf.copy()
+        kf2[:ns] += 100.0
+        vf2[:ns] -= 50.0
+        assert np.array_equal(O.attention_with_segments(q, kf2, vf2, 0.088, sk, sv, tk, tv), out)
+
+
+def test_segments_nothing_to_attend_is_zero():
+    q = bf16(np.ones((8, 128)))
+    z = np.zeros((0, 2, 128), dtype=np.float32)
+    assert np.array_equal(O.attention_with_segments(q, z, z, 0.1), np.zeros((8, 128), dtype=np.float32))
