@@ -274,7 +274,7 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
  * loads it until the process exits.
  *   - Sizes whose kvq_decode_attn_workspace_bytes() exceed 32 MiB are rejected
  *     with KVQ_ERR_WORKSPACE before any launch (on a 152-SM GB300 that is about
- *     6850 request x KV-head pairs per call).
+ *     6800 request x KV-head pairs per call).
  *   - The first call on a device looks up the array's device address with that
  *     device current; make that first call before any stream capture.
  *   - Every call shares the array and leaves its contents behind; calls that
