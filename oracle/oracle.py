@@ -273,3 +273,68 @@ def request_path(xk: list[np.ndarray], xv: list[np.ndarray], actives: list[np.nd
     vhat = reconstruct(vs, depth)
     out = attention_f32(q, decode_f32(ks, depth), decode_f32(vs, depth), scale)
     return ks, vs, khat, vhat, out
+
+
+# --------------------------------------------------------------------------- sparse decode attention
+
+
+def sparse_reference(q: np.ndarray, kf: np.ndarray, vf: np.ndarray, scale: float, n_select: int):
+    """Reference-loop state of sparse decode attention (FlashLoop RFC §3.2),
+    in float64 from q [Hq, D] (BF16 bits) and the FP32 decode kf, vf [T, H, D]
+    of the chain at the reference depth. Per query head h (KV head h // g):
+      p      = softmax(q_h . k_t * scale) over all T keys
+      S      = the n_select keys of largest p (equal p: lower position first),
+               returned in ascending position order
+      m      = sum of p over S
+      O_ref  = sum_t p_t v_t        (the full attention output)
+      C_ref  = sum over S of p_t v_t
+    Returns (S [Hq, K] int32, m [Hq], O_ref [Hq, D], C_ref [Hq, D]), K = min(n_select, T)."""
+    q64 = bf16_bits_to_f32(q).astype(np.float64)
+    k64 = np.asarray(kf, dtype=np.float64)
+    v64 = np.asarray(vf, dtype=np.float64)
+    T, H, D = k64.shape
+    Hq = q64.shape[0]
+    g = Hq // H
+    K = min(int(n_select), T)
+    S = np.zeros((Hq, K), dtype=np.int32)
+    m = np.zeros(Hq)
+    o_ref = np.zeros((Hq, D))
+    c_ref = np.zeros((Hq, D))
+    for hq in range(Hq):
+        h = hq // g
+        s = k64[:, h, :] @ q64[hq] * scale
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        order = np.lexsort((np.arange(T), -p))  # largest p first, then lower position
+        sel = np.sort(order[:K])
+        S[hq] = sel
+        m[hq] = p[sel].sum()
+        o_ref[hq] = p @ v64[:, h, :]
+        c_ref[hq] = p[sel] @ v64[sel, h, :]
+    return S, m, o_ref, c_ref
+
+
+def sparse_decode(q: np.ndarray, kf: np.ndarray, vf: np.ndarray, scale: float, S: np.ndarray, m: np.ndarray,
+                  o_ref: np.ndarray, c_ref: np.ndarray) -> np.ndarray:
+    """A later loop of sparse decode attention (FlashLoop RFC §3.2), float64:
+      p_local = softmax(q_h . k_t * scale) over t in S (keys at this loop's depth)
+      C_new   = m * sum over S of p_local_t v_t
+      O       = O_ref - C_ref + C_new"""
+    q64 = bf16_bits_to_f32(q).astype(np.float64)
+    k64 = np.asarray(kf, dtype=np.float64)
+    v64 = np.asarray(vf, dtype=np.float64)
+    T, H, D = k64.shape
+    Hq = q64.shape[0]
+    g = Hq // H
+    out = np.zeros((Hq, D))
+    for hq in range(Hq):
+        h = hq // g
+        sel = np.asarray(S[hq], dtype=np.int64)
+        if sel.size == 0:
+            out[hq] = o_ref[hq] - c_ref[hq]
+            continue
+        s = k64[sel, h, :] @ q64[hq] * scale
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        out[hq] = o_ref[hq] - c_ref[hq] + m[hq] * (p @ v64[sel, h, :])
+    return out

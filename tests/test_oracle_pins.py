@@ -565,3 +565,57 @@ def test_segments_nothing_to_attend_is_zero():
     q = bf16(np.ones((8, 128)))
     z = np.zeros((0, 2, 128), dtype=np.float32)
     assert np.array_equal(O.attention_with_segments(q, z, z, 0.1), np.zeros((8, 128), dtype=np.float32))
+
+
+# ---------------------------------------------------------------- sparse decode attention
+
+
+def test_sparse_scalar_example():
+    """The RFC §3.2 worked example, with one channel and logits log(p)."""
+    gold = json.load(open(os.path.join(GOLD, "sparse_scalar_example.json")))
+    one = bf16(np.ones((1, 1)))
+    kr = np.log(np.array(gold["ref_probs"]))[:, None, None]
+    vr = np.array(gold["ref_values"])[:, None, None]
+    S, m, o_ref, c_ref = O.sparse_reference(one, kr, vr, 1.0, gold["n_select"])
+    assert S[0].tolist() == gold["selected"]
+    assert abs(m[0] - gold["mass"]) < 1e-12
+    assert abs(o_ref[0, 0] - gold["o_ref"]) < 1e-12
+    assert abs(c_ref[0, 0] - gold["c_ref"]) < 1e-12
+    k_new = np.zeros((3, 1, 1))
+    v_new = np.zeros((3, 1, 1))
+    k_new[S[0], 0, 0] = np.log(np.array(gold["later_probs_on_selected"]))
+    v_new[S[0], 0, 0] = gold["later_values_on_selected"]
+    k_new[0, 0, 0] = 50.0  # an unselected key: not read at the later loop
+    out = O.sparse_decode(one, k_new, v_new, 1.0, S, m, o_ref, c_ref)
+    assert abs(out[0, 0] - gold["o_new"]) < 1e-12
+
+
+def test_sparse_all_keys_is_dense_attention():
+    """With every key retained, m = 1 and C_ref = O_ref, so the later loop is
+    plain dense attention over its own keys (RFC §3.2)."""
+    rng = np.random.default_rng(12)
+    T, H, Hq, D = 50, 2, 8, 128
+    q = bf16(rng.standard_normal((Hq, D)))
+    k0, v0 = rng.standard_normal((T, H, D)), rng.standard_normal((T, H, D))
+    k1, v1 = rng.standard_normal((T, H, D)), rng.standard_normal((T, H, D))
+    S, m, o_ref, c_ref = O.sparse_reference(q, k0, v0, 0.09, T)
+    assert np.allclose(m, 1.0) and np.allclose(c_ref, o_ref)
+    out = O.sparse_decode(q, k1, v1, 0.09, S, m, o_ref, c_ref)
+    assert np.max(np.abs(out - _sdpa64_rows(q, k1, v1, 0.09, Hq))) < 1e-9
+
+
+def test_sparse_selection_is_top_k_with_position_ties():
+    rng = np.random.default_rng(13)
+    T, H, Hq, D = 40, 1, 2, 128
+    q = bf16(rng.standard_normal((Hq, D)))
+    k = rng.standard_normal((T, H, D))
+    k[10] = k[30] = k[5]  # three equal logits
+    for K in (1, 7, 20, 40, 55):
+        S, m, _, _ = O.sparse_reference(q, k, k, 0.1, K)
+        assert S.shape == (Hq, min(K, T))
+        for hq in range(Hq):
+            s = k[:, 0, :] @ f32(q)[hq].astype(np.float64) * 0.1
+            brute = sorted(range(T), key=lambda t: (-s[t], t))[:min(K, T)]
+            assert S[hq].tolist() == sorted(brute)
+            p = np.exp(s - s.max())
+            assert abs(m[hq] - p[sorted(brute)].sum() / p.sum()) < 1e-12
