@@ -260,6 +260,43 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
                                      int head_dim, int depth, const uint16_t* q, float softmax_scale, float* out,
                                      void* workspace, size_t workspace_bytes, int algo, kvq_cuda_stream stream);
 
+/*
+ * Sparse decode attention over the packed chains (RFC §3.2). At the reference
+ * loop the full attention is computed and, per query head, the n_select keys
+ * of largest probability are kept (equal probabilities: lower position
+ * first) with their probability mass m, the full output O_ref and their
+ * contribution C_ref = sum over S of p_t v_t; a later loop r reads only the
+ * keys of S at its own depth and returns
+ *     O = O_ref - C_ref + m * softmax(q_r K_r[S]^T * scale) V_r[S].
+ * K = min(n_select, n_tokens) keys per (request, query head). All of it is
+ * FP32 on the FP32 decode of the packed chain. Requests with BF16 segments
+ * (n_sink or n_tail nonzero) and requests longer than max_tokens are refused
+ * on the device: their outputs are NaN and bit 1 of the error word is set.
+ */
+size_t kvq_sparse_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim, int max_tokens);
+
+/* Reference loop at ref_depth (usually 2).
+ *   q_ref     BF16 [n_requests][n_q_heads][head_dim].
+ *   sel_idx   int32 [n_requests][n_q_heads][n_select]: the selected positions in
+ *             ascending order, -1 past the request's K.
+ *   mass      FP32 [n_requests][n_q_heads]; o_ref, c_ref FP32 [..][..][head_dim]
+ *             (16-byte aligned).
+ *   workspace >= kvq_sparse_workspace_bytes(...) bytes, 16-byte aligned; int32 at
+ *             offset 0 is the error word (bits: 1 inconsistent request, ...). */
+kvq_status kvq_sparse_ref_state(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
+                                int ref_depth, const uint16_t* q_ref, float softmax_scale, int n_select,
+                                int max_tokens, int32_t* sel_idx, float* mass, float* o_ref, float* c_ref,
+                                void* workspace, size_t workspace_bytes, kvq_cuda_stream stream);
+
+/* A later loop at `depth` with the state of kvq_sparse_ref_state (same n_select
+ * and max_tokens); out FP32 [n_requests][n_q_heads][head_dim]. workspace: at
+ * least 16 bytes, 16-byte aligned, for the error word (bit 32: a selected
+ * position outside its request). */
+kvq_status kvq_sparse_decode_attn(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
+                                  int depth, const uint16_t* q, float softmax_scale, int n_select, int max_tokens,
+                                  const int32_t* sel_idx, const float* mass, const float* o_ref, const float* c_ref,
+                                  float* out, void* workspace, size_t workspace_bytes, kvq_cuda_stream stream);
+
 /* Bytes of the static device scratch used by kvq_decode_attn_packed_noalloc. */
 #define KVQ_NOALLOC_SCRATCH_BYTES (32u << 20)
 

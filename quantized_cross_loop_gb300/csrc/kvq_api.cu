@@ -7,6 +7,7 @@
 #include <cstring>
 
 #include "kvq_attn_common.cuh"
+#include "kvq_sparse.cuh"
 
 using namespace kvq;
 
@@ -494,6 +495,108 @@ kvq_status kvq_decode_attn_packed(const kvq_request* reqs, int n_requests, int n
                                   void* workspace, size_t workspace_bytes, kvq_cuda_stream stream) {
   return kvq_decode_attn_packed_ex(reqs, n_requests, n_heads, n_q_heads, head_dim, depth, q, softmax_scale, out,
                                    workspace, workspace_bytes, KVQ_ATTN_AUTO, stream);
+}
+
+// ---------------------------------------------------------------- sparse decode attention
+
+static size_t sparse_attn_part(int n_requests, int n_heads, int n_q_heads) {
+  return (kvq_decode_attn_workspace_bytes(n_requests, n_heads, n_q_heads, kD) + 255) / 256 * 256;
+}
+
+size_t kvq_sparse_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim, int max_tokens) {
+  (void)head_dim;
+  if (n_requests < 0 || n_heads < 1 || n_q_heads < 1 || max_tokens < 0) return 0;
+  return sparse_attn_part(n_requests, n_heads, n_q_heads) + size_t(n_requests) * n_q_heads * size_t(max_tokens) * 4;
+}
+
+static kvq_status check_sparse(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
+                               int depth, const uint16_t* q, float softmax_scale, int n_select, int max_tokens) {
+  if (n_requests < 0) return fail(KVQ_ERR_BAD_ARG, "n_requests %d", n_requests);
+  if (n_heads < 1 || n_heads > 1024) return fail(KVQ_ERR_BAD_ARG, "n_heads %d", n_heads);
+  if (n_q_heads < n_heads || n_q_heads % n_heads != 0)
+    return fail(KVQ_ERR_BAD_ARG, "n_q_heads %d is not a multiple of n_heads %d", n_q_heads, n_heads);
+  if (n_q_heads / n_heads > kMaxG) return fail(KVQ_ERR_UNSUPPORTED, "more than %d query heads per KV head", kMaxG);
+  if (head_dim != kD) return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d (kernels support 128)", head_dim);
+  if (depth < 1 || depth > KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "depth %d", depth);
+  if (!(softmax_scale > 0.0f) || softmax_scale > 1e30f) return fail(KVQ_ERR_BAD_ARG, "softmax_scale");
+  if (n_select < 0) return fail(KVQ_ERR_BAD_ARG, "n_select %d", n_select);
+  if (max_tokens < 0 || max_tokens > (1 << 24)) return fail(KVQ_ERR_BAD_ARG, "max_tokens %d", max_tokens);
+  if (n_requests > 0 && (!reqs || !q)) return fail(KVQ_ERR_BAD_ARG, "NULL reqs or q");
+  if (n_requests > 0 && (!aligned16(reqs) || !aligned16(q))) return fail(KVQ_ERR_MISALIGNED, "reqs and q must be 16-byte aligned");
+  return KVQ_OK;
+}
+
+kvq_status kvq_sparse_ref_state(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
+                                int ref_depth, const uint16_t* q_ref, float softmax_scale, int n_select,
+                                int max_tokens, int32_t* sel_idx, float* mass, float* o_ref, float* c_ref,
+                                void* workspace, size_t workspace_bytes, kvq_cuda_stream stream) {
+  kvq_status st = check_sparse(reqs, n_requests, n_heads, n_q_heads, head_dim, ref_depth, q_ref, softmax_scale,
+                               n_select, max_tokens);
+  if (st != KVQ_OK) return st;
+  if (n_requests == 0) return ok();
+  if ((n_select > 0 && !sel_idx) || !mass || !o_ref || !c_ref) return fail(KVQ_ERR_BAD_ARG, "NULL output");
+  if (!aligned16(o_ref) || !aligned16(c_ref)) return fail(KVQ_ERR_MISALIGNED, "o_ref and c_ref must be 16-byte aligned");
+  const size_t need = kvq_sparse_workspace_bytes(n_requests, n_heads, n_q_heads, head_dim, max_tokens);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return fail(KVQ_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", need);
+  // the full attention at the reference depth: O_ref (and a cleared error word)
+  const size_t apart = sparse_attn_part(n_requests, n_heads, n_q_heads);
+  st = kvq_decode_attn_packed_ex(reqs, n_requests, n_heads, n_q_heads, head_dim, ref_depth, q_ref, softmax_scale,
+                                 o_ref, workspace, apart, KVQ_ATTN_AUTO, stream);
+  if (st != KVQ_OK) return st;
+  SparseArgs a;
+  memset(&a, 0, sizeof a);
+  a.reqs = reqs;
+  a.n_requests = n_requests;
+  a.H = n_heads;
+  a.Hq = n_q_heads;
+  a.g = n_q_heads / n_heads;
+  a.depth = ref_depth;
+  a.max_tokens = max_tokens;
+  a.n_select = n_select;
+  a.q = q_ref;
+  a.scale = softmax_scale;
+  a.logits = reinterpret_cast<float*>(static_cast<char*>(workspace) + apart);
+  a.sel_idx = sel_idx;
+  a.mass = mass;
+  a.c_ref = c_ref;
+  a.err = static_cast<int32_t*>(workspace);
+  return cuda_status(launch_sparse_select_path(a, reinterpret_cast<cudaStream_t>(stream)), "sparse reference launch");
+}
+
+kvq_status kvq_sparse_decode_attn(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
+                                  int depth, const uint16_t* q, float softmax_scale, int n_select, int max_tokens,
+                                  const int32_t* sel_idx, const float* mass, const float* o_ref, const float* c_ref,
+                                  float* out, void* workspace, size_t workspace_bytes, kvq_cuda_stream stream) {
+  kvq_status st = check_sparse(reqs, n_requests, n_heads, n_q_heads, head_dim, depth, q, softmax_scale, n_select,
+                               max_tokens);
+  if (st != KVQ_OK) return st;
+  if (n_requests == 0) return ok();
+  if ((n_select > 0 && !sel_idx) || !mass || !o_ref || !c_ref || !out) return fail(KVQ_ERR_BAD_ARG, "NULL argument");
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < 16)
+    return fail(KVQ_ERR_WORKSPACE, "workspace needs 16 bytes, 16-byte aligned");
+  SparseArgs a;
+  memset(&a, 0, sizeof a);
+  a.reqs = reqs;
+  a.n_requests = n_requests;
+  a.H = n_heads;
+  a.Hq = n_q_heads;
+  a.g = n_q_heads / n_heads;
+  a.depth = depth;
+  a.max_tokens = max_tokens;
+  a.n_select = n_select;
+  a.q = q;
+  a.scale = softmax_scale;
+  a.sel_idx = const_cast<int32_t*>(sel_idx);
+  a.mass = const_cast<float*>(mass);
+  a.c_ref = const_cast<float*>(c_ref);
+  a.o_ref = o_ref;
+  a.out = out;
+  a.err = static_cast<int32_t*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(a.err, 0, 16, s);
+  if (e != cudaSuccess) return cuda_status(e, "clear error word");
+  return cuda_status(launch_sparse_attn(a, s), "sparse attention launch");
 }
 
 }  // extern "C"

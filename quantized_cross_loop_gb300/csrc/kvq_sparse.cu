@@ -1,0 +1,356 @@
+// kvq_sparse.cu — sparse decode attention over packed K/V (FlashLoop RFC,
+// vllm-rlt issue #156, §3.2).
+//
+// At the reference loop the full attention is computed and, per query head,
+// the keys S of largest probability are kept with their mass m, the full
+// output O_ref and their contribution C_ref = sum_{t in S} p_t v_t; a later
+// loop r attends over S only, at its own depth, and returns
+//   O = O_ref - C_ref + m * softmax(q_r . K_r[S] / sqrt(d)) V_r[S].
+// Historical K/V are read from the packed chain (decoded in FP32, as the
+// dense reader does); the keys of S are gathered row by row.
+//
+// Kernels (ours):
+//   sparse_logits_kernel  block = (request, KV head, 64-token tile): the FP32
+//                         logits (log2 units) of every key for the g query heads
+//   sparse_select_kernel  block = (request, query head): softmax max and sum,
+//                         exact top-k by a 4-pass radix select on
+//                         order-preserving keys (ties: lower position), the
+//                         selected indices in ascending order, m and C_ref
+//   sparse_attn_kernel    block = (request, query head): the later loop
+#include "kvq_attn_common.cuh"
+#include "kvq_sparse.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr float kL2e = 1.4426950408889634f;
+
+// The K or V chain of a request as the decode helpers read it.
+__device__ void chain_of(const kvq_request& r, int kind, int depth, int H, Chain& C) {
+  C.depth = depth;
+  C.kind = kind;
+  C.n_tokens = r.n_tokens;
+  C.n_heads = H;
+  for (int j = 0; j < depth; ++j) {
+    const kvq_loop_ref& L = r.loop[j];
+    LoopPlanes& P = C.loop[j];
+    P.n_rows = L.n_rows;
+    P.sparse = L.active_idx != nullptr;
+    P.active = L.active_idx;
+    P.tile_dir = L.tile_dir;
+    P.codes = kind == KVQ_K ? L.k_codes : L.v_codes;
+    P.mins = kind == KVQ_K ? L.k_mins : L.v_mins;
+    P.scales = kind == KVQ_K ? L.k_scales : L.v_scales;
+  }
+}
+
+// A request the sparse kernels accept: a consistent packed chain, no BF16
+// segments, at most max_tokens keys.
+__device__ __forceinline__ bool sparse_request_ok(const kvq_request& r, int depth, int max_tokens) {
+  return request_ok(r, depth) && r.n_sink == 0 && r.n_tail == 0 && r.n_tokens <= max_tokens;
+}
+
+// Stored rows of token t in loops 0..depth-1 (-1: absent, inherit).
+__device__ __forceinline__ void rows_of(const Chain& C, int depth, int t, int* rows) {
+  for (int j = 0; j < depth; ++j) rows[j] = row_of(C.loop[j], t);
+}
+
+// Order-preserving unsigned key of a float (larger float, larger key).
+__device__ __forceinline__ uint32_t okey(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- logits
+
+__global__ void __launch_bounds__(128) sparse_logits_kernel(SparseArgs a) {
+  const int u = blockIdx.x, k = blockIdx.y;
+  const int b = u / a.H, h = u % a.H;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const kvq_request& r = a.reqs[b];
+  if (!sparse_request_ok(r, a.depth, a.max_tokens)) return;
+  const int T = r.n_tokens;
+  const int t0 = k * KVQ_TILE;
+  if (t0 >= T) return;
+  const int g = a.g;
+  __shared__ Chain C;
+  __shared__ float qs[kMaxG][kD];
+  if (threadIdx.x == 0) chain_of(r, KVQ_K, a.depth, a.H, C);
+  for (int i = 0; i < g; ++i)
+    qs[i][threadIdx.x] =
+        bf16_bits_to_f32(a.q[((long long)b * a.Hq + (long long)h * g + i) * kD + threadIdx.x]) * (a.scale * kL2e);
+  __syncthreads();
+  const int nvalid = min(KVQ_TILE, T - t0);
+  for (int tt = warp; tt < nvalid; tt += 4) {
+    const int t = t0 + tt;
+    int rows[KVQ_MAX_LOOPS];
+    rows_of(C, a.depth, t, rows);
+    float kv[4];
+    chain4_f32(C, a.depth, rows, h, 4 * lane, kv);
+    for (int i = 0; i < g; ++i) {
+      float s = qs[i][4 * lane] * kv[0] + qs[i][4 * lane + 1] * kv[1] + qs[i][4 * lane + 2] * kv[2] +
+                qs[i][4 * lane + 3] * kv[3];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (lane == 0) a.logits[((long long)b * a.Hq + (long long)h * g + i) * a.max_tokens + t] = s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- selection, m and C_ref
+
+constexpr int kSelThreads = 256;
+
+// Block-wide exclusive scan of one flag per thread; returns the prefix and
+// writes the total to *total (every thread).
+__device__ __forceinline__ int block_scan(int flag, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned ball = __ballot_sync(0xffffffffu, flag);
+  const int within = __popc(ball & ((1u << lane) - 1u));
+  if (lane == 0) s_warp[warp] = __popc(ball);
+  __syncthreads();
+  int before = 0, sum = 0;
+  for (int w = 0; w < kSelThreads / 32; ++w) {
+    const int c = s_warp[w];
+    if (w < warp) before += c;
+    sum += c;
+  }
+  __syncthreads();
+  *total = sum;
+  return before + within;
+}
+
+__global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseArgs a) {
+  const int bq = blockIdx.x;
+  const int b = bq / a.Hq, hq = bq % a.Hq;
+  const int h = hq / a.g;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const kvq_request& r = a.reqs[b];
+  int32_t* sel = a.sel_idx + (long long)bq * a.n_select;
+  float* cref = a.c_ref + (long long)bq * kD;
+  const bool ok = sparse_request_ok(r, a.depth, a.max_tokens);
+  const int T = ok ? r.n_tokens : 0;
+  const int K = min(a.n_select, T);
+  for (int i = K + tid; i < a.n_select; i += kSelThreads) sel[i] = -1;
+  if (!ok) {
+    if (tid == 0) {
+      atomicOr(a.err, 1);
+      a.mass[bq] = __int_as_float(0x7fc00000);
+    }
+    if (tid < kD) cref[tid] = __int_as_float(0x7fc00000);
+    return;
+  }
+  if (K == 0) {
+    if (tid == 0) a.mass[bq] = 0.0f;
+    if (tid < kD) cref[tid] = 0.0f;
+    return;
+  }
+  const float* s = a.logits + (long long)bq * a.max_tokens;
+  __shared__ float s_red[kSelThreads / 32];
+  __shared__ int s_warp[kSelThreads / 32];
+  __shared__ unsigned s_hist[256];
+  __shared__ unsigned s_prefix, s_need;
+  __shared__ Chain C;
+  __shared__ float s_acc[kSelThreads / 32][kD];
+
+  // softmax max and sum (log2 units)
+  float mx = -INFINITY;
+  for (int t = tid; t < T; t += kSelThreads) mx = fmaxf(mx, s[t]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) s_red[warp] = mx;
+  __syncthreads();
+  float M = s_red[0];
+  for (int w = 1; w < kSelThreads / 32; ++w) M = fmaxf(M, s_red[w]);
+  __syncthreads();
+  float sum = 0.0f;
+  for (int t = tid; t < T; t += kSelThreads) sum += exp2f(s[t] - M);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane == 0) s_red[warp] = sum;
+  __syncthreads();
+  float L = 0.0f;
+  for (int w = 0; w < kSelThreads / 32; ++w) L += s_red[w];
+  __syncthreads();
+
+  // the K-th largest key: four passes over the key bytes, most significant first
+  if (tid == 0) {
+    s_prefix = 0;
+    s_need = unsigned(K);  // keys still to take at and below the current prefix
+  }
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += kSelThreads) s_hist[i] = 0;
+    __syncthreads();
+    const unsigned prefix = s_prefix;
+    const unsigned hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
+    for (int t = tid; t < T; t += kSelThreads) {
+      const uint32_t key = okey(s[t]);
+      if ((key & hmask) == (prefix & hmask)) atomicAdd(&s_hist[(key >> shift) & 0xFFu], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned need = s_need, acc = 0;
+      int bin = 255;
+      for (; bin > 0; --bin) {
+        if (acc + s_hist[bin] >= need) break;
+        acc += s_hist[bin];
+      }
+      s_prefix = prefix | (unsigned(bin) << shift);
+      s_need = need - acc;  // keys to take equal to the prefix so far
+    }
+    __syncthreads();
+  }
+  const uint32_t tau = s_prefix;    // the K-th largest key
+  const unsigned take_eq = s_need;  // keys equal to tau to take, lowest positions first
+
+  // compaction in position order; m from the selected probabilities
+  int written = 0, eq_seen = 0;
+  float msum = 0.0f;
+  for (int base = 0; base < T; base += kSelThreads) {
+    const int t = base + tid;
+    const uint32_t key = t < T ? okey(s[t]) : 0u;
+    const int is_eq = (t < T && key == tau) ? 1 : 0;
+    int eq_total = 0;
+    const int eq_before = eq_seen + block_scan(is_eq, s_warp, &eq_total);
+    const int take = (t < T) && (key > tau || (is_eq && unsigned(eq_before) < take_eq));
+    int n_take = 0;
+    const int pos = written + block_scan(take, s_warp, &n_take);
+    if (take) {
+      sel[pos] = t;
+      msum += exp2f(s[t] - M);
+    }
+    written += n_take;
+    eq_seen += eq_total;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) msum += __shfl_xor_sync(0xffffffffu, msum, off);
+  if (lane == 0) s_red[warp] = msum;
+  if (tid == 0) chain_of(r, KVQ_V, a.depth, a.H, C);
+  __syncthreads();
+  if (tid == 0) {
+    float ms = 0.0f;
+    for (int w = 0; w < kSelThreads / 32; ++w) ms += s_red[w];
+    a.mass[bq] = ms / L;
+  }
+
+  // C_ref: the selected rows of V at the reference depth, weighted by p
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int i = warp; i < K; i += kSelThreads / 32) {
+    const int t = sel[i];
+    int rows[KVQ_MAX_LOOPS];
+    rows_of(C, a.depth, t, rows);
+    float vv[4];
+    chain4_f32(C, a.depth, rows, h, 4 * lane, vv);
+    const float p = exp2f(s[t] - M) / L;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = fmaf(p, vv[e], acc[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) s_acc[warp][4 * lane + e] = acc[e];
+  __syncthreads();
+  if (tid < kD) {
+    float c = 0.0f;
+    for (int w = 0; w < kSelThreads / 32; ++w) c += s_acc[w][tid];
+    cref[tid] = c;
+  }
+}
+
+// ---------------------------------------------------------------- later loop
+
+constexpr int kAttnWarps = 4;
+
+__global__ void __launch_bounds__(32 * kAttnWarps) sparse_attn_kernel(SparseArgs a) {
+  const int bq = blockIdx.x;
+  const int b = bq / a.Hq, hq = bq % a.Hq;
+  const int h = hq / a.g;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const kvq_request& r = a.reqs[b];
+  float* out = a.out + (long long)bq * kD;
+  const bool ok = sparse_request_ok(r, a.depth, a.max_tokens);
+  if (!ok) {
+    if (tid == 0) atomicOr(a.err, 1);
+    out[tid] = __int_as_float(0x7fc00000);
+    return;
+  }
+  const int K = min(a.n_select, r.n_tokens);
+  const int32_t* sel = a.sel_idx + (long long)bq * a.n_select;
+  __shared__ Chain CK, CV;
+  __shared__ float qs[kD];
+  __shared__ float s_m[kAttnWarps], s_l[kAttnWarps];
+  __shared__ float s_acc[kAttnWarps][kD];
+  if (tid == 0) {
+    chain_of(r, KVQ_K, a.depth, a.H, CK);
+    chain_of(r, KVQ_V, a.depth, a.H, CV);
+  }
+  qs[tid] = bf16_bits_to_f32(a.q[(long long)bq * kD + tid]) * (a.scale * kL2e);
+  __syncthreads();
+  float m = -INFINITY, l = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  bool bad = false;
+  for (int i = warp; i < K; i += kAttnWarps) {
+    const int t = sel[i];
+    if (t < 0 || t >= r.n_tokens) {  // not a selection of this request
+      bad = true;
+      continue;
+    }
+    int rows[KVQ_MAX_LOOPS];
+    rows_of(CK, a.depth, t, rows);
+    float kv[4], vv[4];
+    chain4_f32(CK, a.depth, rows, h, 4 * lane, kv);
+    chain4_f32(CV, a.depth, rows, h, 4 * lane, vv);
+    float s = qs[4 * lane] * kv[0] + qs[4 * lane + 1] * kv[1] + qs[4 * lane + 2] * kv[2] + qs[4 * lane + 3] * kv[3];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    const float mn = fmaxf(m, s);
+    const float al = m == -INFINITY ? 0.0f : exp2f(m - mn);
+    const float p = exp2f(s - mn);
+    l = l * al + p;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = fmaf(p, vv[e], acc[e] * al);
+    m = mn;
+  }
+  if (bad && lane == 0) atomicOr(a.err, 32);
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_l[warp] = l;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) s_acc[warp][4 * lane + e] = acc[e];
+  __syncthreads();
+  float M = -INFINITY;
+  for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w]);
+  float Lt = 0.0f, c = 0.0f;
+  for (int w = 0; w < kAttnWarps; ++w) {
+    const float wgt = s_m[w] == -INFINITY ? 0.0f : exp2f(s_m[w] - M);
+    Lt += s_l[w] * wgt;
+    c += s_acc[w][tid] * wgt;
+  }
+  const float cnew = Lt > 0.0f ? c / Lt : 0.0f;
+  out[tid] = a.o_ref[(long long)bq * kD + tid] - a.c_ref[(long long)bq * kD + tid] + a.mass[bq] * cnew;
+}
+
+cudaError_t launch_sparse_select_path(const SparseArgs& a, cudaStream_t stream) {
+  if (a.n_requests == 0) return cudaSuccess;
+  const int tiles = (a.max_tokens + KVQ_TILE - 1) / KVQ_TILE;
+  if (tiles > 0) {
+    sparse_logits_kernel<<<dim3(a.n_requests * a.H, tiles), 128, 0, stream>>>(a);
+    count_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  sparse_select_kernel<<<a.n_requests * a.Hq, kSelThreads, 0, stream>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_attn(const SparseArgs& a, cudaStream_t stream) {
+  if (a.n_requests == 0) return cudaSuccess;
+  sparse_attn_kernel<<<a.n_requests * a.Hq, 32 * kAttnWarps, 0, stream>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

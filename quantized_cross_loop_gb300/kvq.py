@@ -32,7 +32,8 @@ EXPORTED = (
     "kvq_build_tile_dir", "kvq_reconstruct", "kvq_request_fill", "kvq_decode_attn_workspace_bytes",
     "kvq_decode_attn_packed", "kvq_decode_attn_packed_ex", "kvq_status_string", "kvq_last_error", "kvq_version",
     "kvq_batch_workspace_bytes", "kvq_encode_batch", "kvq_reconstruct_batch", "kvq_launch_count",
-    "kvq_decode_attn_packed_noalloc",
+    "kvq_decode_attn_packed_noalloc", "kvq_sparse_workspace_bytes", "kvq_sparse_ref_state",
+    "kvq_sparse_decode_attn",
 )
 
 
@@ -118,6 +119,12 @@ def lib():
             L.kvq_decode_attn_packed.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_float, vp, vp, sz, vp]
             L.kvq_decode_attn_packed_ex.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_float, vp, vp, sz,
                                                     i32, vp]
+            L.kvq_sparse_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            L.kvq_sparse_workspace_bytes.restype = sz
+            L.kvq_sparse_ref_state.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_float, i32, i32, vp, vp, vp,
+                                               vp, vp, sz, vp]
+            L.kvq_sparse_decode_attn.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_float, i32, i32, vp, vp, vp,
+                                                 vp, vp, vp, sz, vp]
             L.kvq_status_string.argtypes = [i32]
             L.kvq_status_string.restype = ctypes.c_char_p
             L.kvq_last_error.restype = ctypes.c_char_p
@@ -455,3 +462,61 @@ def kvq_decode_attn_packed_noalloc(table: RequestTable, q: torch.Tensor, depth: 
 def attn_error_word(workspace: torch.Tensor) -> int:
     """The error word the attention kernels set in the workspace (reads the device)."""
     return int(workspace[:4].view(torch.int32).item())
+
+
+# --------------------------------------------------------------------------- sparse decode attention
+
+
+def kvq_sparse_workspace_bytes(n_requests: int, n_heads: int, n_q_heads: int, head_dim: int, max_tokens: int) -> int:
+    return int(lib().kvq_sparse_workspace_bytes(n_requests, n_heads, n_q_heads, head_dim, max_tokens))
+
+
+class SparseState:
+    """Reference-loop state of sparse decode attention: selected positions
+    [B, Hq, n_select] (-1 padded), mass [B, Hq], O_ref and C_ref [B, Hq, D]."""
+
+    def __init__(self, sel_idx, mass, o_ref, c_ref, n_select, max_tokens, workspace):
+        self.sel_idx, self.mass, self.o_ref, self.c_ref = sel_idx, mass, o_ref, c_ref
+        self.n_select, self.max_tokens, self.workspace = n_select, max_tokens, workspace
+
+
+def kvq_sparse_ref_state(table: RequestTable, q_ref: torch.Tensor, ref_depth: int, n_heads: int, n_select: int,
+                         max_tokens: int, softmax_scale: float | None = None, workspace: torch.Tensor | None = None,
+                         stream=None) -> SparseState:
+    _require_cuda(q_ref, "q_ref", torch.bfloat16)
+    B, Hq, D = q_ref.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    dev = q_ref.device
+    sel = torch.empty((B, Hq, max(n_select, 1)), dtype=torch.int32, device=dev)
+    mass = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    o_ref = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    c_ref = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    need = kvq_sparse_workspace_bytes(B, n_heads, Hq, D, max_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(lib().kvq_sparse_ref_state(_dptr(table.table), B, n_heads, Hq, D, ref_depth, _dptr(q_ref),
+                                      ctypes.c_float(softmax_scale), n_select, max_tokens, _dptr(sel), _dptr(mass),
+                                      _dptr(o_ref), _dptr(c_ref), _dptr(workspace), workspace.numel(),
+                                      _stream_handle(stream)), "kvq_sparse_ref_state")
+    return SparseState(sel[:, :, :n_select], mass, o_ref, c_ref, n_select, max_tokens, workspace)
+
+
+def kvq_sparse_decode_attn(table: RequestTable, q: torch.Tensor, depth: int, n_heads: int, state: SparseState,
+                           softmax_scale: float | None = None, out: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _require_cuda(q, "q", torch.bfloat16)
+    B, Hq, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(16, dtype=torch.uint8, device=q.device)
+    sel = state.sel_idx.contiguous()
+    _check(lib().kvq_sparse_decode_attn(_dptr(table.table), B, n_heads, Hq, D, depth, _dptr(q),
+                                        ctypes.c_float(softmax_scale), state.n_select, state.max_tokens, _dptr(sel),
+                                        _dptr(state.mass), _dptr(state.o_ref), _dptr(state.c_ref), _dptr(out),
+                                        _dptr(workspace), workspace.numel(), _stream_handle(stream)),
+           "kvq_sparse_decode_attn")
+    return out

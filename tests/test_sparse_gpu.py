@@ -1,0 +1,138 @@
+"""Sparse decode attention over the packed chains (FlashLoop RFC, vllm-rlt
+issue #156, §3.2), through the C ABI, against the oracle on the same packed
+data: the reference state at loop 2 (selection, mass, full output, selected
+contribution) and the corrected output of loops 3 and 4.
+
+The selection is decided in floating point on both sides (FP32 on the GPU,
+float64 in the oracle), so keys whose probabilities tie with the k-th one to
+within rounding may differ; the test checks the GPU selection against the
+oracle's probabilities (every selected key at least, every other key at most,
+the k-th probability up to 1e-5 relative) and then compares mass, C_ref and
+the later-loop output computed from that selection."""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from quantized_cross_loop_gb300 import kvq
+from quantized_cross_loop_gb300 import workloads as W
+from quantized_cross_loop_gb300.workloads import bf16_bits
+
+from tests import pathrun as P
+
+pytestmark = pytest.mark.gpu
+
+H, D = 8, 128
+
+
+def _setup(Ts, sparse, Hq=32, seed=0):
+    reqs, kc, vc, oks, ovs = [], [], [], [], []
+    for b, T in enumerate(Ts):
+        spec = W.ConfigSpec("sp", seed + b, 1, max(T, 1), H, D, Hq, 4, 0.1,
+                            (1.0, 1.0, 0.5, 0.25) if sparse else (1.0, 1.0, 1.0, 1.0))
+        r = W.make_request(spec, 0, 0, "cpu", T=T, sparse=sparse)
+        k, v = P.gpu_chains(r)
+        kc.append(k)
+        vc.append(v)
+        act = [None if a is None else a.numpy().astype(np.int32) for a in r.active]
+        oks.append(O.encode_chain(O.KIND_K, [bf16_bits(x) for x in r.xk], act))
+        ovs.append(O.encode_chain(O.KIND_V, [bf16_bits(x) for x in r.xv], act))
+        reqs.append(r)
+    table = kvq.RequestTable(kc, vc, torch.device("cuda"))
+    g = torch.Generator().manual_seed(seed + 100)
+    qs = [torch.randn((len(Ts), Hq, D), generator=g).to(torch.bfloat16) for _ in range(3)]  # loops 2, 3, 4
+    return table, reqs, oks, ovs, qs
+
+
+def _logits64(q_bits, kf, hq, g, scale):
+    return np.asarray(kf, np.float64)[:, hq // g, :] @ O.bf16_bits_to_f32(q_bits[hq]).astype(np.float64) * scale
+
+
+def _check_selection(sel, q_bits, kf, Hq, g, K, scale):
+    T = kf.shape[0]
+    for hq in range(Hq):
+        s = _logits64(q_bits, kf, hq, g, scale)
+        S = sel[hq][:K]
+        assert len(S) == K and np.all(np.diff(S) > 0) and (K == 0 or (S[0] >= 0 and S[-1] < T))
+        if K == 0 or K == T:
+            assert K == 0 or np.array_equal(S, np.arange(T))
+            continue
+        kth = np.sort(s)[::-1][K - 1]
+        tol = 1e-5 * max(1.0, abs(kth))
+        mask = np.zeros(T, bool)
+        mask[S] = True
+        assert np.all(s[mask] >= kth - tol), f"head {hq}: a selected key below the k-th"
+        assert np.all(s[~mask] <= kth + tol), f"head {hq}: an unselected key above the k-th"
+
+
+@pytest.mark.parametrize("Ts,sparse,n_select,Hq", [
+    ([300, 1000], True, 64, 32),
+    ([4096], False, 1024, 32),
+    ([777, 64, 1], True, 100, 64),
+    ([200], False, 500, 32),  # more than T: every key
+])
+def test_sparse_reference_and_later_loops(Ts, sparse, n_select, Hq):
+    table, reqs, oks, ovs, qs = _setup(Ts, sparse, Hq, seed=sum(Ts) + n_select)
+    g = Hq // H
+    scale = 1.0 / math.sqrt(D)
+    max_tokens = max(Ts)
+    st = kvq.kvq_sparse_ref_state(table, qs[0].cuda(), 2, H, n_select, max_tokens)
+    torch.cuda.synchronize()
+    assert kvq.attn_error_word(st.workspace) == 0
+    sel, mass, o_ref, c_ref = (t.cpu().numpy() for t in (st.sel_idx, st.mass, st.o_ref, st.c_ref))
+    outs = {}
+    for depth, q in ((3, qs[1]), (4, qs[2])):
+        ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+        outs[depth] = kvq.kvq_sparse_decode_attn(table, q.cuda(), depth, H, st, workspace=ws).cpu().numpy()
+        assert kvq.attn_error_word(ws) == 0
+    for b, T in enumerate(Ts):
+        K = min(n_select, T)
+        assert np.all(sel[b][:, K:] == -1)
+        kf2, vf2 = O.decode_f32(oks[b], 2), O.decode_f32(ovs[b], 2)
+        qb = bf16_bits(qs[0][b])
+        _check_selection(sel[b], qb, kf2, Hq, g, K, scale)
+        # the oracle's state on the GPU's selection
+        S = sel[b][:, :K]
+        m_o, c_o, o_o = np.zeros(Hq), np.zeros((Hq, D)), np.zeros((Hq, D))
+        for hq in range(Hq):
+            s = _logits64(qb, kf2, hq, g, scale)
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            m_o[hq] = p[S[hq]].sum()
+            c_o[hq] = p[S[hq]] @ np.asarray(vf2, np.float64)[S[hq], hq // g, :]
+            o_o[hq] = p @ np.asarray(vf2, np.float64)[:, hq // g, :]
+        assert np.max(np.abs(mass[b] - m_o)) < 1e-4
+        P.assert_attention_close(c_ref[b], c_o, f"C_ref req {b}")
+        P.assert_attention_close(o_ref[b], o_o, f"O_ref req {b}")
+        # later loops from the GPU state
+        for depth, q in ((3, qs[1]), (4, qs[2])):
+            kf, vf = O.decode_f32(oks[b], depth), O.decode_f32(ovs[b], depth)
+            ref = O.sparse_decode(bf16_bits(q[b]), kf, vf, scale, S, mass[b].astype(np.float64),
+                                  o_ref[b].astype(np.float64), c_ref[b].astype(np.float64))
+            P.assert_attention_close(outs[depth][b], ref, f"req {b} depth {depth}")
+            if K == T:  # every key kept: plain dense attention at this depth
+                dense = O.attention_f32(bf16_bits(q[b]), kf, vf, scale)
+                P.assert_attention_close(outs[depth][b], dense, f"dense req {b} depth {depth}")
+
+
+def test_sparse_refuses_segments_and_bad_selections():
+    table, reqs, oks, ovs, qs = _setup([100, 100], False, 32, seed=9)
+    seg = tuple(torch.randn((n, H, D)).to(torch.bfloat16).cuda() for n in (2, 2, 0, 0))
+    table2 = kvq.RequestTable([table._keep[0][0], table._keep[0][1]], [table._keep[1][0], table._keep[1][1]],
+                              torch.device("cuda"), segments=[seg, None])
+    st = kvq.kvq_sparse_ref_state(table2, qs[0].cuda(), 2, H, 16, 100)
+    torch.cuda.synchronize()
+    assert kvq.attn_error_word(st.workspace) != 0
+    assert np.all(np.isnan(st.mass.cpu().numpy()[0])) and not np.any(np.isnan(st.mass.cpu().numpy()[1]))
+    # a corrupted selection (position past the request) is flagged, not read
+    st = kvq.kvq_sparse_ref_state(table, qs[0].cuda(), 2, H, 16, 100)
+    st.sel_idx[1, 0, 3] = 5000
+    ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    kvq.kvq_sparse_decode_attn(table, qs[1].cuda(), 3, H, st, workspace=ws)
+    torch.cuda.synchronize()
+    assert kvq.attn_error_word(ws) & 32
