@@ -57,6 +57,7 @@ def parse_args(argv=None):
     ap.add_argument("--algo", choices=["auto", "simt", "mma"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the sparse-decode and BF16-tail timings")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target wall time of the CPU-oracle sample")
     return ap.parse_args(argv)
 
@@ -383,6 +384,10 @@ def main():
             "algorithmic_bytes_per_launch": ab["attention"], "avg_launch_ms": att_ms,
             "dominant_phase_of_step": dominant}
 
+    extras = None
+    if not args.no_extras:
+        extras = run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq)
@@ -408,6 +413,7 @@ def main():
                        "attended_tokens_per_s": ab["tokens"] / (att_ms * 1e-3),
                        "encoded_tokens_per_s": ab["tokens"] / (enc_ms * 1e-3)},
             "roofline": roof,
+            "extras": extras,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clk,
@@ -433,6 +439,52 @@ def pack_sources(reqs, torch, dev):
                 off += x.numel()
     torch.cuda.synchronize()
     return flat
+
+
+def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, reps=10):
+    """Timings of the two reader variants next to the dense step, on the same
+    packed pool (CUDA events, after one warm-up call each):
+      sparse decode attention (RFC §3.2): reference state at loop 2 keeping a
+      quarter of each request's keys per query head, then one later loop at
+      the full depth reading only those keys;
+      dense attention with a 100-token BF16 tail per request (RFC §3.3)."""
+    B = len(reqs)
+    max_t = max(r.T for r in reqs)
+    n_select = max(1, max_t // 4)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    q2 = torch.randn(q.shape, generator=g, device=dev).to(torch.bfloat16)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            r = fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps, r
+
+    ref_ms, st = timed(lambda: kvq.kvq_sparse_ref_state(pool.table, q2, 2, H, n_select, max_t))
+    dec_ws = torch.zeros(16, dtype=torch.uint8, device=dev)
+    dec_ms, _ = timed(lambda: kvq.kvq_sparse_decode_attn(pool.table, q, depth, H, st, workspace=dec_ws))
+    err = kvq.attn_error_word(st.workspace) | kvq.attn_error_word(dec_ws)
+    selected = sum(min(n_select, r.T) for r in reqs) * Hq
+    empty = torch.zeros((0, H, D), dtype=torch.bfloat16, device=dev)
+    tail = [(empty, empty, torch.randn((100, H, D), generator=g, device=dev).to(torch.bfloat16),
+             torch.randn((100, H, D), generator=g, device=dev).to(torch.bfloat16)) for _ in reqs]
+    ks = [pool.k_streams[b] for b in range(B)]
+    vs = [pool.v_streams[b] for b in range(B)]
+    ttable = kvq.RequestTable(ks, vs, dev, segments=tail)
+    tws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(B, H, Hq, D), dtype=torch.uint8, device=dev)
+    tail_ms, _ = timed(lambda: kvq.kvq_decode_attn_packed(ttable, q, depth, H, workspace=tws))
+    err |= kvq.attn_error_word(tws)
+    return {"sparse_decode": {"budget_keys_per_query_head": n_select, "ref_depth": 2, "depth": depth,
+                              "ref_state_ms": ref_ms, "later_loop_ms": dec_ms,
+                              "selected_keys_per_s": selected / (dec_ms * 1e-3)},
+            "bf16_tail": {"tail_tokens_per_request": 100, "attention_ms": tail_ms},
+            "error_word": err}
 
 
 def run_e2e(args, torch, kvq, src_all, q, out, step, stream, world, dev, step_bytes, dist):
