@@ -129,94 +129,100 @@ cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
 // ---------------------------------------------------------------- BF16 segments
 //
 // One block per (request, KV head): the request's BF16 sink and tail tokens are
-// attended in FP32 (log2 domain, online over chunks of 32 tokens), then merged
-// by log-sum-exp with the packed part's result and its (max, sum) state.
+// attended in FP32 (log2 domain) — each warp takes every fourth token, a lane
+// four channels, and keeps its own online softmax over its tokens; the four
+// are merged, then combined by log-sum-exp with the packed part's result and
+// its (max, sum) state.
 
-constexpr int kSegChunk = 32;
+constexpr int kSegWarps = 4;
 constexpr float kSegLog2e = 1.4426950408889634f;
 
-__global__ void __launch_bounds__(kD) segment_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(32 * kSegWarps) segment_kernel(AttnArgs a) {
   const int u = blockIdx.x;
   const int b = u / a.H, h = u % a.H;
-  const int tid = threadIdx.x;  // channel
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = a.g;
   const kvq_request& r = a.reqs[b];
   if (!request_ok(r, a.depth)) return;  // the output is already NaN
   const int ns = r.n_sink, n = r.n_sink + r.n_tail;
   if (n == 0) return;
-  __shared__ float qs[kMaxG][kD + 1];
-  __shared__ float kt[kSegChunk][kD + 1];
-  __shared__ float vt[kSegChunk][kD];
-  __shared__ float lg[kSegChunk][kMaxG];
-  __shared__ float sm[kMaxG], sl[kMaxG], alpha[kMaxG];
+  __shared__ float s_m[kSegWarps][kMaxG], s_l[kSegWarps][kMaxG];
+  __shared__ float s_acc[kSegWarps][kMaxG][kD];
   const float qscale = a.scale * kSegLog2e;
-  for (int i = 0; i < g; ++i)
-    qs[i][tid] = bf16_bits_to_f32(a.q[((long long)b * a.Hq + (long long)h * g + i) * kD + tid]) * qscale;
-  if (tid < kMaxG) {
-    sm[tid] = -INFINITY;
-    sl[tid] = 0.0f;
-  }
-  float acc[kMaxG];
+  float qv[kMaxG][4];
 #pragma unroll
-  for (int i = 0; i < kMaxG; ++i) acc[i] = 0.0f;
-  __syncthreads();
-  for (int c0 = 0; c0 < n; c0 += kSegChunk) {
-    const int cn = min(kSegChunk, n - c0);
-    for (int t = 0; t < cn; ++t) {
-      const int tok = c0 + t;
-      const long long row = tok < ns ? ((long long)tok * a.H + h) * kD : ((long long)(tok - ns) * a.H + h) * kD;
-      const uint16_t* kr = tok < ns ? r.sink_k : r.tail_k;
-      const uint16_t* vr = tok < ns ? r.sink_v : r.tail_v;
-      kt[t][tid] = bf16_bits_to_f32(kr[row + tid]);
-      vt[t][tid] = bf16_bits_to_f32(vr[row + tid]);
-    }
-    __syncthreads();
-    for (int idx = tid; idx < cn * g; idx += blockDim.x) {  // logits: one (token, head) pair per thread
-      const int t = idx / g, i = idx % g;
-      float sacc = 0.0f;
-      for (int d = 0; d < kD; ++d) sacc = fmaf(qs[i][d], kt[t][d], sacc);
-      lg[t][i] = sacc;
-    }
-    __syncthreads();
-    if (tid < g) {
-      float mt = -INFINITY;
-      for (int t = 0; t < cn; ++t) mt = fmaxf(mt, lg[t][tid]);
-      const float mn = fmaxf(sm[tid], mt);
-      const float al = (sm[tid] == -INFINITY) ? 0.0f : exp2f(sm[tid] - mn);
-      float sum = 0.0f;
-      for (int t = 0; t < cn; ++t) {
-        const float p = exp2f(lg[t][tid] - mn);
-        lg[t][tid] = p;
-        sum += p;
-      }
-      alpha[tid] = al;
-      sl[tid] = sl[tid] * al + sum;
-      sm[tid] = mn;
-    }
-    __syncthreads();
-    for (int i = 0; i < g; ++i) {
-      float sacc = acc[i] * alpha[i];
-      for (int t = 0; t < cn; ++t) sacc = fmaf(lg[t][i], vt[t][tid], sacc);
-      acc[i] = sacc;
-    }
-    __syncthreads();
+  for (int i = 0; i < kMaxG; ++i) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      qv[i][e] = i < g ? bf16_bits_to_f32(a.q[((long long)b * a.Hq + (long long)h * g + i) * kD + 4 * lane + e]) * qscale
+                       : 0.0f;
   }
-  for (int i = 0; i < g; ++i) {
+  float m[kMaxG], l[kMaxG], acc[kMaxG][4];
+#pragma unroll
+  for (int i = 0; i < kMaxG; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[i][e] = 0.0f;
+  }
+  for (int tok = warp; tok < n; tok += kSegWarps) {
+    const bool sink = tok < ns;
+    const long long row = ((long long)(sink ? tok : tok - ns) * a.H + h) * kD + 4 * lane;
+    const uint2 kw = *reinterpret_cast<const uint2*>((sink ? r.sink_k : r.tail_k) + row);
+    const uint2 vw = *reinterpret_cast<const uint2*>((sink ? r.sink_v : r.tail_v) + row);
+    const float kf[4] = {__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
+                         __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u)};
+    const float vf[4] = {__uint_as_float(vw.x << 16), __uint_as_float(vw.x & 0xFFFF0000u),
+                         __uint_as_float(vw.y << 16), __uint_as_float(vw.y & 0xFFFF0000u)};
+#pragma unroll
+    for (int i = 0; i < kMaxG; ++i) {
+      if (i >= g) break;
+      float s = qv[i][0] * kf[0] + qv[i][1] * kf[1] + qv[i][2] * kf[2] + qv[i][3] * kf[3];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      const float mn = fmaxf(m[i], s);
+      const float al = m[i] == -INFINITY ? 0.0f : exp2f(m[i] - mn);
+      const float p = exp2f(s - mn);
+      l[i] = l[i] * al + p;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[i][e] = fmaf(p, vf[e], acc[i][e] * al);
+      m[i] = mn;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxG; ++i) {
+    if (lane == 0) {
+      s_m[warp][i] = m[i];
+      s_l[warp][i] = l[i];
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s_acc[warp][i][4 * lane + e] = acc[i][e];
+  }
+  __syncthreads();
+  for (int i = 0; i < g; ++i) {  // thread = channel
+    float ms = -INFINITY;
+    for (int w = 0; w < kSegWarps; ++w) ms = fmaxf(ms, s_m[w][i]);
+    float ls = 0.0f, cs = 0.0f;
+    for (int w = 0; w < kSegWarps; ++w) {
+      const float wt = s_m[w][i] == -INFINITY ? 0.0f : exp2f(s_m[w][i] - ms);
+      ls += s_l[w][i] * wt;
+      cs += s_acc[w][i][tid] * wt;
+    }
     const long long oi = (long long)b * a.Hq + (long long)h * g + i;
     const float2 st = a.stats[oi];  // the packed part: max (log2 units), sum
     const bool packed = st.y > 0.0f && st.x != -INFINITY;
-    const float M = packed ? fmaxf(st.x, sm[i]) : sm[i];
+    const float M = packed ? fmaxf(st.x, ms) : ms;
     const float w0 = packed ? exp2f(st.x - M) : 0.0f;
-    const float w1 = exp2f(sm[i] - M);
-    const float num = (packed ? a.out[oi * kD + tid] * (st.y * w0) : 0.0f) + acc[i] * w1;
-    const float den = (packed ? st.y * w0 : 0.0f) + sl[i] * w1;
+    const float w1 = exp2f(ms - M);
+    const float num = (packed ? a.out[oi * kD + tid] * (st.y * w0) : 0.0f) + cs * w1;
+    const float den = (packed ? st.y * w0 : 0.0f) + ls * w1;
     a.out[oi * kD + tid] = num / den;
   }
 }
 
 cudaError_t launch_segments(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
-  segment_kernel<<<a.n_requests * a.H, kD, 0, stream>>>(a);
+  segment_kernel<<<a.n_requests * a.H, 32 * kSegWarps, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }

@@ -290,27 +290,36 @@ __global__ void __launch_bounds__(32 * kAttnWarps) sparse_attn_kernel(SparseArgs
   __syncthreads();
   float m = -INFINITY, l = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   bool bad = false;
-  for (int i = warp; i < K; i += kAttnWarps) {
-    const int t = sel[i];
-    if (t < 0 || t >= r.n_tokens) {  // not a selection of this request
-      bad = true;
-      continue;
+  // a warp takes 32 consecutive selected keys at a time: lane i resolves the
+  // stored rows of key i (the searches run side by side), then the warp walks
+  // the 32 keys with the rows passed by shuffles
+  for (int base = 32 * warp; base < K; base += 32 * kAttnWarps) {
+    const int nk = min(32, K - base);
+    int my_t = lane < nk ? sel[base + lane] : -1;
+    const bool my_bad = lane < nk && (my_t < 0 || my_t >= r.n_tokens);  // not a selection of this request
+    if (my_bad) my_t = -1;
+    bad |= __any_sync(0xffffffffu, my_bad);
+    int my_rows[KVQ_MAX_LOOPS];
+    for (int j = 0; j < a.depth; ++j) my_rows[j] = my_t >= 0 ? row_of(CK.loop[j], my_t) : -1;
+    for (int kk = 0; kk < nk; ++kk) {
+      const int t = __shfl_sync(0xffffffffu, my_t, kk);
+      int rows[KVQ_MAX_LOOPS];
+      for (int j = 0; j < a.depth; ++j) rows[j] = __shfl_sync(0xffffffffu, my_rows[j], kk);
+      if (t < 0) continue;
+      float kv[4], vv[4];
+      chain4_f32(CK, a.depth, rows, h, 4 * lane, kv);
+      chain4_f32(CV, a.depth, rows, h, 4 * lane, vv);
+      float s = qs[4 * lane] * kv[0] + qs[4 * lane + 1] * kv[1] + qs[4 * lane + 2] * kv[2] + qs[4 * lane + 3] * kv[3];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      const float mn = fmaxf(m, s);
+      const float al = m == -INFINITY ? 0.0f : exp2f(m - mn);
+      const float p = exp2f(s - mn);
+      l = l * al + p;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = fmaf(p, vv[e], acc[e] * al);
+      m = mn;
     }
-    int rows[KVQ_MAX_LOOPS];
-    rows_of(CK, a.depth, t, rows);
-    float kv[4], vv[4];
-    chain4_f32(CK, a.depth, rows, h, 4 * lane, kv);
-    chain4_f32(CV, a.depth, rows, h, 4 * lane, vv);
-    float s = qs[4 * lane] * kv[0] + qs[4 * lane + 1] * kv[1] + qs[4 * lane + 2] * kv[2] + qs[4 * lane + 3] * kv[3];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    const float mn = fmaxf(m, s);
-    const float al = m == -INFINITY ? 0.0f : exp2f(m - mn);
-    const float p = exp2f(s - mn);
-    l = l * al + p;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] = fmaf(p, vv[e], acc[e] * al);
-    m = mn;
   }
   if (bad && lane == 0) atomicOr(a.err, 32);
   if (lane == 0) {
