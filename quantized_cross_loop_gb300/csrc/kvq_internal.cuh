@@ -106,6 +106,8 @@ __device__ __forceinline__ void chain4(const Chain& C, int depth, const int* row
 
 // The same chain in FP32: decode = RN32(min16 + RN32(scale16 * c)), loops
 // summed with FP32 rounding only (the values a direct packed reader uses).
+// The four channels share one V group, and their K parameters are adjacent,
+// so each loop's parameters come in one load per plane.
 __device__ __forceinline__ void chain4_f32(const Chain& C, int depth, const int* rows, int h, int c0, float out[4]) {
 #pragma unroll
   for (int e = 0; e < 4; ++e) out[e] = 0.0f;
@@ -114,11 +116,30 @@ __device__ __forceinline__ void chain4_f32(const Chain& C, int depth, const int*
     if (row < 0) continue;
     const LoopPlanes& L = C.loop[j];
     uint16_t two = *reinterpret_cast<const uint16_t*>(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + c0 / 2);
+    float mn[4], sc[4];
+    if (C.kind == KVQ_K) {
+      const long long pi = param_index(KVQ_K, L.n_rows, h, row, c0);
+      const uint2 m4 = __ldg(reinterpret_cast<const uint2*>(L.mins + pi));
+      const uint2 s4 = __ldg(reinterpret_cast<const uint2*>(L.scales + pi));
+      const uint32_t mw[2] = {m4.x, m4.y}, sw[2] = {s4.x, s4.y};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        mn[e] = f16_bits_to_f32(uint16_t(mw[e >> 1] >> (16 * (e & 1))));
+        sc[e] = f16_bits_to_f32(uint16_t(sw[e >> 1] >> (16 * (e & 1))));
+      }
+    } else {
+      const long long pi = param_index(KVQ_V, L.n_rows, h, row, c0);
+      const float m1 = f16_bits_to_f32(__ldg(L.mins + pi)), s1 = f16_bits_to_f32(__ldg(L.scales + pi));
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        mn[e] = m1;
+        sc[e] = s1;
+      }
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       int c = (two >> (4 * e)) & 0xF;
-      long long pi = param_index(C.kind, L.n_rows, h, row, c0 + e);
-      float dq = __fadd_rn(f16_bits_to_f32(__ldg(L.mins + pi)), __fmul_rn(f16_bits_to_f32(__ldg(L.scales + pi)), float(c)));
+      float dq = __fadd_rn(mn[e], __fmul_rn(sc[e], float(c)));
       out[e] = (j == 0) ? dq : __fadd_rn(out[e], dq);
     }
   }
