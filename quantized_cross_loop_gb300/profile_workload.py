@@ -11,7 +11,12 @@ requests of configuration 2). Stages:
   reconstruct  batched reconstruction of K and V at full depth, `reps` times;
   attention    packed decode attention at full depth, `reps` times, with a
                256 MiB buffer written between calls so that every call starts
-               with a cold L2.
+               with a cold L2;
+  sparse       sparse decode attention: the reference state at loop 2 keeping a
+               quarter of the keys per query head, then the full-depth loop,
+               `reps` times each;
+  tail         packed decode attention with a 100-token BF16 tail per request,
+               `reps` times.
 Every stage first encodes the workload (the launches a capture should skip:
 2 + 4 (loops - 1) per kind, plus one per reconstruct or attention call before
 the one captured).
@@ -36,7 +41,7 @@ def parse_workload(name: str):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="cfg3")
-    ap.add_argument("--stage", choices=["encode", "reconstruct", "attention"], default="attention")
+    ap.add_argument("--stage", choices=["encode", "reconstruct", "attention", "sparse", "tail"], default="attention")
     ap.add_argument("--algo", choices=["auto", "simt", "mma"], default="auto")
     ap.add_argument("--reps", type=int, default=2)
     args = ap.parse_args()
@@ -68,10 +73,31 @@ def main():
         for _ in range(args.reps):
             flush.zero_()
             kvq.kvq_decode_attn_packed(pool.table, q, wl.depth, wl.H, algo=algo, out=out, workspace=ws)
+    elif args.stage == "sparse":
+        max_t = max(lengths)
+        n_select = max(1, max_t // 4)
+        for _ in range(args.reps):
+            st = kvq.kvq_sparse_ref_state(pool.table, wl.q, 2, wl.H, n_select, max_t)
+        ws = torch.zeros(16, dtype=torch.uint8, device=dev)
+        for _ in range(args.reps):
+            kvq.kvq_sparse_decode_attn(pool.table, wl.q, wl.depth, wl.H, st, workspace=ws)
+    elif args.stage == "tail":
+        empty = torch.zeros((0, wl.H, wl.D), dtype=torch.bfloat16, device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+        tail = [(empty, empty, torch.randn((100, wl.H, wl.D), generator=g, device=dev).to(torch.bfloat16),
+                 torch.randn((100, wl.H, wl.D), generator=g, device=dev).to(torch.bfloat16)) for _ in lengths]
+        table = kvq.RequestTable(pool.k_streams, pool.v_streams, dev, segments=tail)
+        ws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(len(lengths), wl.H, wl.Hq, wl.D), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(args.reps):
+            kvq.kvq_decode_attn_packed(table, wl.q, wl.depth, wl.H, workspace=ws)
     torch.cuda.synchronize()
     err = kvq.attn_error_word(pool.workspace)
-    if args.stage == "attention":
+    if args.stage in ("attention", "tail"):
         err |= kvq.attn_error_word(ws)
+    elif args.stage == "sparse":
+        err |= kvq.attn_error_word(st.workspace) | kvq.attn_error_word(ws)
     print("ok" if err == 0 else f"error word {err}")
     return 0 if err == 0 else 1
 
