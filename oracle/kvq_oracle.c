@@ -28,6 +28,9 @@
  *     residual = inherit (not code 0); loop-4 read example:  RFC §3.3 (fourth paragraph)
  *   - decode attention at the requested depth, scale 1/sqrt(head_dim):
  *                                                           RFC §3.2
+ *   - K groups that never mix rows of different logical groups, so a page's
+ *     metadata stays local (the alternative to compact-row groups):
+ *                                                           PR, review by 0z5a (group ownership)
  *
  * Readings taken where the pages are silent (each also listed in the design doc):
  *   - code rounding: round half to even, then clamp to [0, 15];
@@ -44,7 +47,13 @@
  *     chain sums rounded to FP32 only) before FP32 attention: the direct
  *     packed reader's values; the BF16 reconstruction is a separate output;
  *   - plane layout (head-major): codes u8[H][n][D/2]; K params f16[H][⌈n/G⌉][D];
- *     V params f16[H][n][⌈D/G⌉]; sparse index int32[n] ascending.
+ *     V params f16[H][n][⌈D/G⌉]; sparse index int32[n] ascending;
+ *   - tile-local K grouping (ORC_KGROUP_TILE): a K group of a sparse loop holds
+ *     the stored rows whose logical positions lie in one logical tile
+ *     [G·k, G·k + G); its params sit in slot k of f16[H][⌈T/G⌉][D]; a tile with
+ *     no stored row keeps +0 min and +0 scale (an empty stream stores no params).
+ *     Dense loops group the same rows either way, so their bytes do not depend
+ *     on the grouping.
  */
 #include <math.h>
 #include <stdint.h>
@@ -53,6 +62,9 @@
 
 #define ORC_KIND_K 0
 #define ORC_KIND_V 1
+
+#define ORC_KGROUP_COMPACT 0 /* K groups: G consecutive stored rows */
+#define ORC_KGROUP_TILE 1    /* K groups: the stored rows of one logical tile of G tokens */
 
 #define ORC_OK 0
 #define ORC_EINVAL (-1)
@@ -201,21 +213,37 @@ static float dequant(uint16_t min16, uint16_t scale16, int c) {
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-/* Byte-exact sizes of the planes of one stream with n stored rows. */
+/* K groups per head of a stream: by stored rows, or one per logical tile of a
+ * tile-grouped sparse stream. */
+static int64_t k_groups(int n, int T, int G, int kgroup, int sparse) {
+  if (n <= 0) return 0; /* an empty stream stores no params */
+  return (kgroup == ORC_KGROUP_TILE && sparse) ? ceil_div(T, G) : ceil_div(n, G);
+}
+
+/* Byte-exact sizes of the planes of one stream with n stored rows of T tokens. */
 int64_t orc_codes_bytes(int n, int H, int D) { return (int64_t)H * n * (D / 2); }
-int64_t orc_param_count(int kind, int n, int H, int D, int G) {
-  if (kind == ORC_KIND_K) return (int64_t)H * ceil_div(n, G) * D;
+int64_t orc_param_count_ex(int kind, int n, int T, int H, int D, int G, int kgroup, int sparse) {
+  if (kind == ORC_KIND_K) return (int64_t)H * k_groups(n, T, G, kgroup, sparse) * D;
   return (int64_t)H * n * ceil_div(D, G);
 }
+int64_t orc_param_count(int kind, int n, int H, int D, int G) {
+  return orc_param_count_ex(kind, n, n, H, D, G, ORC_KGROUP_COMPACT, 0);
+}
+int64_t orc_stream_bytes_ex(int kind, int n, int T, int H, int D, int G, int kgroup, int sparse) {
+  return orc_codes_bytes(n, H, D) + 2 * 2 * orc_param_count_ex(kind, n, T, H, D, G, kgroup, sparse) +
+         (sparse ? 4 * (int64_t)n : 0);
+}
 int64_t orc_stream_bytes(int kind, int n, int H, int D, int G, int sparse) {
-  return orc_codes_bytes(n, H, D) + 2 * 2 * orc_param_count(kind, n, H, D, G) + (sparse ? 4 * (int64_t)n : 0);
+  return orc_stream_bytes_ex(kind, n, n, H, D, G, ORC_KGROUP_COMPACT, sparse);
 }
 
 static int64_t code_byte_index(int n, int D, int h, int row, int d) {
   return ((int64_t)h * n + row) * (D / 2) + d / 2;
 }
-static int64_t param_index(int kind, int n, int D, int G, int h, int row, int d) {
-  if (kind == ORC_KIND_K) return ((int64_t)h * ceil_div(n, G) + row / G) * D + d;
+/* Params of (head h, stored row, channel d). K: group kg of ngk groups per head
+ * (the caller maps the row to its group); V: the row's channel group. */
+static int64_t k_param_index(int64_t ngk, int D, int h, int64_t kg, int d) { return ((int64_t)h * ngk + kg) * D + d; }
+static int64_t v_param_index(int n, int D, int G, int h, int row, int d) {
   return ((int64_t)h * n + row) * ceil_div(D, G) + d / G;
 }
 
@@ -241,12 +269,14 @@ static int check_active(const int32_t* a, int n, int T) {
  * x    : BF16 bits [T][H][D], the loop-r source in logical token order.
  * pred : BF16 bits [T][H][D], X̂_{r-1} in logical order; NULL encodes the base (loop 1).
  * active, n : sorted logical rows to store (NULL: dense, n must equal T).
+ * kgroup : ORC_KGROUP_COMPACT or ORC_KGROUP_TILE (K only; V ignores it).
  * Outputs use the head-major planes described at the top of the file.
  */
-int orc_encode(int kind, int T, int H, int D, int G, const uint16_t* x, const uint16_t* pred, const int32_t* active,
-               int n, uint8_t* codes, uint16_t* mins, uint16_t* scales) {
+int orc_encode_ex(int kind, int T, int H, int D, int G, int kgroup, const uint16_t* x, const uint16_t* pred,
+                  const int32_t* active, int n, uint8_t* codes, uint16_t* mins, uint16_t* scales) {
   if (T < 0 || H <= 0 || D <= 0 || (D & 1) || G <= 0) return ORC_EINVAL;
   if (kind != ORC_KIND_K && kind != ORC_KIND_V) return ORC_EINVAL;
+  if (kgroup != ORC_KGROUP_COMPACT && kgroup != ORC_KGROUP_TILE) return ORC_EINVAL;
   if (active == NULL) {
     if (n != T) return ORC_EINVAL;
   } else if (n < 0 || n > T || !check_active(active, n, T)) {
@@ -281,24 +311,48 @@ int orc_encode(int kind, int T, int H, int D, int G, const uint16_t* x, const ui
   }
 
   if (kind == ORC_KIND_K) {
-    /* K: per (head, channel), groups of G consecutive stored rows. */
-    int ng = (int)ceil_div(n, G);
+    /* K: per (head, channel), groups of stored rows. Compact grouping: G
+     * consecutive stored rows. Tile grouping of a sparse loop: the stored rows
+     * of logical tile k (consecutive too, the index being ascending), group k. */
+    int tiled = (kgroup == ORC_KGROUP_TILE && active != NULL);
+    int64_t ng = k_groups(n, T, G, kgroup, active != NULL);
+    int32_t* first = (int32_t*)malloc(sizeof(int32_t) * (size_t)(ng + 1));
+    if (!first) {
+      free(v);
+      free(c);
+      return ORC_ENOMEM;
+    }
+    for (int64_t g = 0; g <= ng; ++g) {
+      if (!tiled) {
+        first[g] = (int32_t)(g * G < n ? g * G : n);
+      } else { /* first stored row at or after logical token G·g */
+        int r = 0;
+        while (r < n && active[r] < g * G) ++r;
+        first[g] = r;
+      }
+    }
     uint8_t gc[4096];
     for (int h = 0; h < H; ++h) {
       for (int d = 0; d < D; ++d) {
-        for (int g = 0; g < ng; ++g) {
-          int r0 = g * G;
-          int len = (r0 + G <= n) ? G : n - r0;
+        for (int64_t g = 0; g < ng; ++g) {
+          int r0 = first[g];
+          int len = first[g + 1] - r0;
+          int64_t pi = k_param_index(ng, D, h, g, d);
+          if (len == 0) { /* a tile with no stored row */
+            mins[pi] = 0;
+            scales[pi] = 0;
+            continue;
+          }
           const float* base = v + ((int64_t)r0 * H + h) * D + d;
           uint16_t m16, s16;
           quantize_group(base, len, H * D, gc, &m16, &s16);
           for (int i = 0; i < len; ++i) c[((int64_t)(r0 + i) * H + h) * D + d] = gc[i];
-          int64_t pi = param_index(kind, n, D, G, h, r0, d);
           mins[pi] = m16;
           scales[pi] = s16;
         }
       }
     }
+    free(first);
   } else {
     /* V: per (stored row, head), groups of G consecutive channels. */
     int ngc = (int)ceil_div(D, G);
@@ -312,7 +366,7 @@ int orc_encode(int kind, int T, int H, int D, int G, const uint16_t* x, const ui
           uint16_t m16, s16;
           quantize_group(base, len, 1, gc, &m16, &s16);
           for (int i = 0; i < len; ++i) c[((int64_t)row * H + h) * D + d0 + i] = gc[i];
-          int64_t pi = param_index(kind, n, D, G, h, row, d0);
+          int64_t pi = v_param_index(n, D, G, h, row, d0);
           mins[pi] = m16;
           scales[pi] = s16;
         }
@@ -335,18 +389,32 @@ int orc_encode(int kind, int T, int H, int D, int G, const uint16_t* x, const ui
   return ORC_OK;
 }
 
+int orc_encode(int kind, int T, int H, int D, int G, const uint16_t* x, const uint16_t* pred, const int32_t* active,
+               int n, uint8_t* codes, uint16_t* mins, uint16_t* scales) {
+  return orc_encode_ex(kind, T, H, D, G, ORC_KGROUP_COMPACT, x, pred, active, n, codes, mins, scales);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Reconstruct the chain to a requested depth (RFC §3.3).                     */
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
   int32_t n;              /* stored rows */
-  int32_t _pad;
+  int32_t kgroup;         /* ORC_KGROUP_COMPACT or ORC_KGROUP_TILE */
   const int32_t* active;  /* NULL: dense (n == T) */
   const uint8_t* codes;
   const uint16_t* mins;
   const uint16_t* scales;
 } orc_stream;
+
+/* Index of the params of (head h, stored row, channel d) of stream s. */
+static int64_t stream_param_index(int kind, const orc_stream* s, int T, int D, int G, int h, int row, int d) {
+  if (kind != ORC_KIND_K) return v_param_index(s->n, D, G, h, row, d);
+  int sparse = s->active != NULL;
+  int64_t ng = k_groups(s->n, T, G, s->kgroup, sparse);
+  int64_t kg = (s->kgroup == ORC_KGROUP_TILE && sparse) ? s->active[row] / G : row / G;
+  return k_param_index(ng, D, h, kg, d);
+}
 
 /*
  * loops[0] is the base, loops[j-1] the residual of loop j. out: BF16 bits
@@ -371,7 +439,7 @@ int orc_reconstruct(int kind, int T, int H, int D, int G, int depth, const orc_s
   for (int t = 0; t < T; ++t)
     for (int h = 0; h < H; ++h)
       for (int d = 0; d < D; ++d) {
-        int64_t pi = param_index(kind, T, D, G, h, t, d);
+        int64_t pi = stream_param_index(kind, b, T, D, G, h, t, d);
         float val = dequant(b->mins[pi], b->scales[pi], get_code(b->codes, T, D, h, t, d));
         out[((int64_t)t * H + h) * D + d] = orc_f32_to_bf16(val);
       }
@@ -386,7 +454,7 @@ int orc_reconstruct(int kind, int T, int H, int D, int G, int depth, const orc_s
       if (row < 0) continue; /* absent: inherit */
       for (int h = 0; h < H; ++h)
         for (int d = 0; d < D; ++d) {
-          int64_t pi = param_index(kind, s->n, D, G, h, row, d);
+          int64_t pi = stream_param_index(kind, s, T, D, G, h, row, d);
           float dq = dequant(s->mins[pi], s->scales[pi], get_code(s->codes, s->n, D, h, row, d));
           int64_t li = ((int64_t)t * H + h) * D + d;
           float sum = orc_bf16_to_f32(out[li]) + dq; /* RN32 */
@@ -432,7 +500,7 @@ int orc_decode_f32(int kind, int T, int H, int D, int G, int depth, const orc_st
       if (row < 0) continue;
       for (int h = 0; h < H; ++h)
         for (int d = 0; d < D; ++d) {
-          int64_t pi = param_index(kind, s->n, D, G, h, row, d);
+          int64_t pi = stream_param_index(kind, s, T, D, G, h, row, d);
           float m = orc_f16_to_f32(s->mins[pi]);
           float sc = orc_f16_to_f32(s->scales[pi]);
           float prod = sc * (float)get_code(s->codes, s->n, D, h, row, d);

@@ -31,6 +31,8 @@ _lib = None
 KIND_K = 0
 KIND_V = 1
 GROUP = 64
+KGROUP_COMPACT = 0  # K groups: 64 consecutive stored rows (the codec PR's grouping)
+KGROUP_TILE = 1     # K groups: the stored rows of one 64-token logical tile (page-local metadata)
 
 
 def build(force: bool = False) -> str:
@@ -49,7 +51,7 @@ def build(force: bool = False) -> str:
 class _Stream(ctypes.Structure):
     _fields_ = [
         ("n", ctypes.c_int32),
-        ("_pad", ctypes.c_int32),
+        ("kgroup", ctypes.c_int32),
         ("active", ctypes.c_void_p),
         ("codes", ctypes.c_void_p),
         ("mins", ctypes.c_void_p),
@@ -66,6 +68,8 @@ def lib():
             vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
             L.orc_encode.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp, vp]
             L.orc_encode.restype = i32
+            L.orc_encode_ex.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp, vp]
+            L.orc_encode_ex.restype = i32
             L.orc_reconstruct.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(_Stream), vp]
             L.orc_reconstruct.restype = i32
             L.orc_attention.argtypes = [i32, i32, i32, i32, vp, vp, vp, ctypes.c_float, vp]
@@ -76,6 +80,8 @@ def lib():
             L.orc_decode_f32.restype = i32
             L.orc_stream_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
             L.orc_stream_bytes.restype = i64
+            L.orc_stream_bytes_ex.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+            L.orc_stream_bytes_ex.restype = i64
             for name in ("orc_f32_to_f16_n", "orc_f32_to_bf16_n", "orc_f16_to_f32_n"):
                 getattr(L, name).argtypes = [vp, vp, i64]
                 getattr(L, name).restype = None
@@ -130,12 +136,14 @@ class Stream:
     n: int
     active: np.ndarray | None  # int32 [n] ascending, or None (dense)
     codes: np.ndarray  # uint8 [H, n, D/2]
-    mins: np.ndarray  # uint16 (f16 bits): K [H, ceil(n/G), D]; V [H, n, ceil(D/G)]
+    mins: np.ndarray  # uint16 (f16 bits): K [H, groups, D] (see param_shape); V [H, n, ceil(D/G)]
     scales: np.ndarray
+    kgroup: int = KGROUP_COMPACT
 
     def c_struct(self) -> _Stream:
         s = _Stream()
         s.n = self.n
+        s.kgroup = self.kgroup
         s.active = None if self.active is None else self.active.ctypes.data
         s.codes = self.codes.ctypes.data
         s.mins = self.mins.ctypes.data
@@ -143,15 +151,22 @@ class Stream:
         return s
 
 
-def param_shape(kind: int, n: int, H: int, D: int, G: int = GROUP):
+def param_shape(kind: int, n: int, H: int, D: int, G: int = GROUP, T: int | None = None,
+                kgroup: int = KGROUP_COMPACT, sparse: bool = False):
+    """Param plane shape. K: one group per G stored rows, or, for a tile-grouped
+    sparse stream, one per logical tile of G tokens (ceil(T/G)); V: per stored
+    row and channel group."""
     if kind == KIND_K:
+        if kgroup == KGROUP_TILE and sparse and n > 0:
+            return (H, -(-T // G), D)
         return (H, -(-n // G), D)
     return (H, n, -(-D // G))
 
 
 def encode(kind: int, x: np.ndarray, pred: np.ndarray | None = None, active: np.ndarray | None = None,
-           G: int = GROUP) -> Stream:
-    """Encode one stream. x, pred: uint16 BF16 bits [T, H, D] (logical order)."""
+           G: int = GROUP, kgroup: int = KGROUP_COMPACT) -> Stream:
+    """Encode one stream. x, pred: uint16 BF16 bits [T, H, D] (logical order).
+    kgroup selects the K grouping of a sparse stream (V ignores it)."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
     T, H, D = x.shape
     if pred is not None:
@@ -163,13 +178,13 @@ def encode(kind: int, x: np.ndarray, pred: np.ndarray | None = None, active: np.
     else:
         n = T
     codes = np.zeros((H, n, D // 2), dtype=np.uint8)
-    mins = np.zeros(param_shape(kind, n, H, D, G), dtype=np.uint16)
+    mins = np.zeros(param_shape(kind, n, H, D, G, T, kgroup, active is not None), dtype=np.uint16)
     scales = np.zeros_like(mins)
-    rc = lib().orc_encode(kind, T, H, D, G, _ptr(x), _ptr(pred), _ptr(active), n, _ptr(codes), _ptr(mins),
-                          _ptr(scales))
+    rc = lib().orc_encode_ex(kind, T, H, D, G, kgroup, _ptr(x), _ptr(pred), _ptr(active), n, _ptr(codes),
+                             _ptr(mins), _ptr(scales))
     if rc != 0:
         raise ValueError(f"orc_encode failed with status {rc}")
-    return Stream(kind, T, H, D, n, active, codes, mins, scales)
+    return Stream(kind, T, H, D, n, active, codes, mins, scales, kgroup)
 
 
 def reconstruct(streams: list[Stream], depth: int, G: int = GROUP) -> np.ndarray:
@@ -183,12 +198,13 @@ def reconstruct(streams: list[Stream], depth: int, G: int = GROUP) -> np.ndarray
     return out
 
 
-def encode_chain(kind: int, xs: list[np.ndarray], actives: list[np.ndarray | None], G: int = GROUP) -> list[Stream]:
+def encode_chain(kind: int, xs: list[np.ndarray], actives: list[np.ndarray | None], G: int = GROUP,
+                 kgroup: int = KGROUP_COMPACT) -> list[Stream]:
     """Loop 1 encodes X1; loop r encodes X_r minus reconstruct(r-1) at its rows."""
-    streams = [encode(kind, xs[0], None, None, G)]
+    streams = [encode(kind, xs[0], None, None, G, kgroup)]
     for r in range(1, len(xs)):
         pred = reconstruct(streams, r, G)
-        streams.append(encode(kind, xs[r], pred, actives[r], G))
+        streams.append(encode(kind, xs[r], pred, actives[r], G, kgroup))
     return streams
 
 
@@ -207,8 +223,12 @@ def attention(q: np.ndarray, khat: np.ndarray, vhat: np.ndarray, scale: float) -
     return out
 
 
-def stream_bytes(kind: int, n: int, H: int, D: int, G: int = GROUP, sparse: bool = False) -> int:
-    return int(lib().orc_stream_bytes(kind, n, H, D, G, int(sparse)))
+def stream_bytes(kind: int, n: int, H: int, D: int, G: int = GROUP, sparse: bool = False,
+                 T: int | None = None, kgroup: int = KGROUP_COMPACT) -> int:
+    """Byte-exact payload of one stream (codes, FP16 params, the sparse index)."""
+    if T is None and kgroup == KGROUP_COMPACT:
+        return int(lib().orc_stream_bytes(kind, n, H, D, G, int(sparse)))
+    return int(lib().orc_stream_bytes_ex(kind, n, n if T is None else T, H, D, G, kgroup, int(sparse)))
 
 
 def decode_f32(streams: list[Stream], depth: int, G: int = GROUP) -> np.ndarray:

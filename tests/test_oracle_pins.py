@@ -376,6 +376,114 @@ def test_sparse_k_groups_follow_compact_rows():
         assert np.array_equal(s.mins[:, g, :], delta[rows].min(axis=0).astype(np.float16).view(np.uint16))
 
 
+def _tile_chain(T, H, D, seed, drop_tile=2):
+    """A sparse loop-3 chain whose active set misses one whole 64-token tile."""
+    xs = _offset_chain(T, H, D, seed)
+    rng = np.random.default_rng(seed + 1)
+    a = np.sort(rng.choice(T, T // 2, replace=False)).astype(np.int32)
+    a = a[(a // 64) != drop_tile]
+    return xs, a
+
+
+def test_tile_k_groups_hold_one_logical_tile():
+    """Codec PR review by 0z5a (group ownership vs pages): under tile grouping a
+    sparse K group holds exactly the stored rows of one 64-token logical tile;
+    its FP16 min and scale are those of that group's residuals (numpy min/max,
+    FP32 division by 15, then the FP16 cast), and a tile with no stored row keeps
+    +0 min and +0 scale."""
+    T, H, D = 300, 2, 128
+    xs, a = _tile_chain(T, H, D, 21)
+    ks = O.encode_chain(O.KIND_K, xs[:3], [None, None, a], kgroup=O.KGROUP_TILE)
+    s = ks[2]
+    assert s.mins.shape == (H, 5, D)  # ceil(300/64) logical tiles, whatever |a| is
+    pred = f32(O.reconstruct(ks, 2))
+    delta = f32(bf16(f32(xs[2])[a] - pred[a]))  # [n, H, D] in compact order
+    codes = unpack(s.codes)
+    for k in range(5):
+        rows = np.nonzero(a // 64 == k)[0]
+        if rows.size == 0:
+            assert k == 2 and not s.mins[:, k].any() and not s.scales[:, k].any()
+            continue
+        assert np.array_equal(rows, np.arange(rows[0], rows[-1] + 1))  # consecutive compact rows
+        mn, mx = delta[rows].min(axis=0), delta[rows].max(axis=0)
+        scale = ((mx - mn) / np.float32(15)).astype(np.float32)
+        assert np.array_equal(s.mins[:, k, :], mn.astype(np.float16).view(np.uint16))
+        assert np.array_equal(s.scales[:, k, :], scale.astype(np.float16).view(np.uint16))
+        # every code is the nearest of the group's 16 FP32 levels
+        lv = mn[None] + scale[None] * codes[rows]
+        err = np.abs(delta[rows] - lv)
+        assert np.all(err <= scale[None] / 2 * (1 + 1e-6) + 1e-30)
+
+
+def test_tile_grouping_is_local_to_a_tile():
+    """The point of tile grouping: changing the residual rows of one logical
+    tile changes that tile's codes and K params only. Compact grouping offers
+    no such bound (its groups straddle tiles)."""
+    T, H, D = 300, 2, 128
+    xs, a = _tile_chain(T, H, D, 22)
+    x3 = f32(xs[2]).copy()
+    hit = a[(a // 64) == 3]
+    x3[hit] += 0.75
+    xs_b = xs[:2] + [bf16(x3)]
+    for kgroup in (O.KGROUP_TILE, O.KGROUP_COMPACT):
+        s0 = O.encode_chain(O.KIND_K, xs[:3], [None, None, a], kgroup=kgroup)[2]
+        s1 = O.encode_chain(O.KIND_K, xs_b, [None, None, a], kgroup=kgroup)[2]
+        inside = (a // 64) == 3
+        rows_changed = np.any(s0.codes != s1.codes, axis=(0, 2))
+        groups_changed = np.any(s0.mins != s1.mins, axis=(0, 2)) | np.any(s0.scales != s1.scales, axis=(0, 2))
+        if kgroup == O.KGROUP_TILE:
+            assert not rows_changed[~inside].any()
+            assert np.array_equal(np.nonzero(groups_changed)[0], [3])
+        else:  # some row outside tile 3 shares a group with tile 3's rows and is re-coded
+            assert rows_changed[~inside].any()
+
+
+def test_tile_grouping_dense_bytes_and_chain_decode():
+    """Dense loops group the same rows under both groupings (identical bytes);
+    the sparse loop decodes through its tile's params: the FP32 chain step of a
+    stored token t equals min16[t // 64] + scale16[t // 64] * code."""
+    T, H, D = 200, 2, 128
+    xs, a = _tile_chain(T, H, D, 23, drop_tile=1)
+    acts = [None, None, a, a[::2].copy()]
+    kt = O.encode_chain(O.KIND_K, xs, acts, kgroup=O.KGROUP_TILE)
+    kc = O.encode_chain(O.KIND_K, xs, acts)
+    for j in (0, 1):
+        assert np.array_equal(kt[j].codes, kc[j].codes) and np.array_equal(kt[j].mins, kc[j].mins)
+        assert np.array_equal(kt[j].scales, kc[j].scales)
+    f2, f3 = O.decode_f32(kt, 2), O.decode_f32(kt, 3)
+    s = kt[2]
+    codes = unpack(s.codes)
+    for i, t in enumerate(a):
+        m = f16_to_f32(s.mins[:, t // 64, :])
+        sc = f16_to_f32(s.scales[:, t // 64, :])
+        step = (m + (sc * codes[i]).astype(np.float32)).astype(np.float32)
+        assert np.array_equal(f3[t], (f2[t] + step).astype(np.float32))
+    absent = np.setdiff1d(np.arange(T), a)
+    assert np.array_equal(f3[absent], f2[absent])
+    # the BF16 reconstruction agrees with the FP32 decode within its rounding
+    rec = f32(O.reconstruct(kt, 4))
+    assert np.max(np.abs(rec - O.decode_f32(kt, 4))) < 0.05
+
+
+def test_tile_grouping_storage():
+    """Tile grouping stores ceil(T/64) K groups per (head, channel) for a
+    sparse loop, whatever its number of stored rows (an empty stream stores
+    none); V and dense streams are unchanged."""
+    H, D = 8, 128
+    for n, T in ((130, 300), (1, 1000), (64, 64)):
+        assert O.stream_bytes(O.KIND_K, n, H, D, sparse=True, T=T, kgroup=O.KGROUP_TILE) == \
+            n * H * 64 + 2 * 2 * (-(-T // 64)) * H * D + 4 * n
+        assert O.stream_bytes(O.KIND_V, n, H, D, sparse=True, T=T, kgroup=O.KGROUP_TILE) == \
+            O.stream_bytes(O.KIND_V, n, H, D, sparse=True)
+    assert O.stream_bytes(O.KIND_K, 0, H, D, sparse=True, T=300, kgroup=O.KGROUP_TILE) == 0
+    assert O.stream_bytes(O.KIND_K, 300, H, D, sparse=False, T=300, kgroup=O.KGROUP_TILE) == \
+        O.stream_bytes(O.KIND_K, 300, H, D)
+    xs, a = _tile_chain(300, H, D, 24)
+    s = O.encode_chain(O.KIND_K, xs[:3], [None, None, a], kgroup=O.KGROUP_TILE)[2]
+    assert s.codes.nbytes + s.mins.nbytes + s.scales.nbytes + 4 * a.size == \
+        O.stream_bytes(O.KIND_K, a.size, H, D, sparse=True, T=300, kgroup=O.KGROUP_TILE)
+
+
 def test_rejects_unsorted_or_out_of_range_active():
     x = bf16(np.zeros((8, 1, 2), dtype=np.float32))
     for bad in ([3, 1], [1, 1], [-1, 2], [2, 8]):
