@@ -57,7 +57,7 @@ def parse_args(argv=None):
     ap.add_argument("--algo", choices=["auto", "simt", "mma"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extras", action="store_true", help="skip the sparse-decode and BF16-tail timings")
+    ap.add_argument("--no-extras", action="store_true", help="skip the extra timings (sparse decode, BF16 tail, tile-local K grouping)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target wall time of the CPU-oracle sample")
     return ap.parse_args(argv)
 
@@ -386,7 +386,8 @@ def main():
 
     extras = None
     if not args.no_extras:
-        extras = run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream)
+        extras = run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream,
+                            (xk_ptrs, xv_ptrs, rk_ptrs))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -441,13 +442,17 @@ def pack_sources(reqs, torch, dev):
     return flat
 
 
-def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, reps=10):
-    """Timings of the two reader variants next to the dense step, on the same
-    packed pool (CUDA events, after one warm-up call each):
+def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, reps=10):
+    """Timings of the variants next to the step, on the same workload (CUDA
+    events, after one warm-up call each):
       sparse decode attention (RFC §3.2): reference state at loop 2 keeping a
       quarter of each request's keys per query head, then one later loop at
       the full depth reading only those keys;
-      dense attention with a 100-token BF16 tail per request (RFC §3.3)."""
+      dense attention with a 100-token BF16 tail per request (RFC §3.3);
+      tile-local K grouping (codec PR review, group ownership vs pages): the
+      K encode, K reconstruction and attention of a second pool whose sparse
+      K groups stay inside one 64-token tile, beside the K phases of the
+      compact-grouped pool."""
     B = len(reqs)
     max_t = max(r.T for r in reqs)
     n_select = max(1, max_t // 4)
@@ -480,7 +485,29 @@ def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, reps=10)
     tws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(B, H, Hq, D), dtype=torch.uint8, device=dev)
     tail_ms, _ = timed(lambda: kvq.kvq_decode_attn_packed(ttable, q, depth, H, workspace=tws))
     err |= kvq.attn_error_word(tws)
-    return {"sparse_decode": {"budget_keys_per_query_head": n_select, "ref_depth": 2, "depth": depth,
+
+    xk_ptrs, xv_ptrs, rk_ptrs = ptrs
+    tpool = kvq.PackedPool([r.T for r in reqs], [r.active for r in reqs], H, D, depth, dev, kgroup=kvq.KVQ_KGROUP_TILE)
+
+    def enc_k(pl):
+        for j in range(depth):
+            kvq.kvq_encode_batch(pl, kvq.KVQ_K, j, xk_ptrs[j], stream=stream)
+
+    for j in range(depth):
+        kvq.kvq_encode_batch(tpool, kvq.KVQ_V, j, xv_ptrs[j], stream=stream)
+    ek_t, _ = timed(lambda: enc_k(tpool))
+    ek_c, _ = timed(lambda: enc_k(pool))
+    rk_t, _ = timed(lambda: kvq.kvq_reconstruct_batch(tpool, kvq.KVQ_K, depth, rk_ptrs, stream=stream))
+    rk_c, _ = timed(lambda: kvq.kvq_reconstruct_batch(pool, kvq.KVQ_K, depth, rk_ptrs, stream=stream))
+    kws = torch.empty_like(tws)
+    at_t, _ = timed(lambda: kvq.kvq_decode_attn_packed(tpool.table, q, depth, H, workspace=kws))
+    err |= kvq.attn_error_word(kws) | kvq.attn_error_word(tpool.workspace)
+    kgroup_tile = {"payload_bytes": tpool.payload_bytes, "payload_bytes_compact": pool.payload_bytes,
+                   "encode_k_ms": ek_t, "encode_k_ms_compact": ek_c,
+                   "reconstruct_k_ms": rk_t, "reconstruct_k_ms_compact": rk_c, "attention_ms": at_t}
+    del tpool
+    return {"kgroup_tile": kgroup_tile,
+            "sparse_decode": {"budget_keys_per_query_head": n_select, "ref_depth": 2, "depth": depth,
                               "ref_state_ms": ref_ms, "later_loop_ms": dec_ms,
                               "selected_keys_per_s": selected / (dec_ms * 1e-3)},
             "bf16_tail": {"tail_tokens_per_request": 100, "attention_ms": tail_ms},

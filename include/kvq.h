@@ -27,6 +27,11 @@
  *   codes   uint8  [H][n_rows][D/2]   byte (h,i,k) = code(i,h,2k) | code(i,h,2k+1) << 4
  *   K mins, scales  FP16 [H][ceil(n_rows/64)][D]   one group = 64 consecutive stored
  *                                                  rows of one (head, channel)
+ *                   (KVQ_KGROUP_TILE, sparse stream)
+ *                   FP16 [H][ceil(n_tokens/64)][D] group k = the stored rows whose
+ *                                                  logical token lies in [64k, 64k+64);
+ *                                                  a tile with no stored row keeps
+ *                                                  min +0 and scale +0
  *   V mins, scales  FP16 [H][n_rows][ceil(D/64)]   one group = 64 channels of one
  *                                                  (stored row, head)
  *   active_idx int32 [n_rows]  ascending logical rows of a compact sparse
@@ -40,6 +45,13 @@
  * delta = RN_bf16(X_r - X̂_{r-1}) at the stored rows; X̂_r = RN_bf16(X̂_{r-1} +
  * decode(delta)) where a token is stored, and X̂_{r-1} (inherited) where it is
  * absent (RFC §3.3: an absent residual is not an INT4 code 0).
+ *
+ * K grouping (codec PR review by 0z5a, group ownership vs pages): the codec
+ * PR groups a sparse K residual over consecutive compact rows, so one group can
+ * mix distant positions. KVQ_KGROUP_TILE keeps every K group inside one
+ * 64-token logical tile instead, so a tile's rows and metadata can be freed,
+ * moved or shared without re-encoding any other tile. Dense streams group the
+ * same rows either way (identical bytes).
  *
  * Alignment: every plane pointer (codes, mins, scales, active_idx) must be
  * 16-byte aligned and its allocation at least kvq_plane_bytes() long (sizes
@@ -61,6 +73,8 @@ extern "C" {
 #define KVQ_TILE 64
 #define KVQ_MAX_LOOPS 8
 #define KVQ_NIBBLE_LO_FIRST 0
+#define KVQ_KGROUP_COMPACT 0 /* K groups: 64 consecutive stored rows (default) */
+#define KVQ_KGROUP_TILE 1    /* K groups: the stored rows of one 64-token logical tile */
 
 typedef int32_t kvq_status;
 #define KVQ_OK 0
@@ -85,7 +99,8 @@ typedef struct kvq_stream {
   uint8_t kind;              /* KVQ_K (groups over rows) or KVQ_V (groups over channels) */
   uint16_t group;            /* 64 */
   uint8_t nibble_order;      /* KVQ_NIBBLE_LO_FIRST */
-  uint8_t reserved[3];
+  uint8_t kgroup;            /* KVQ_KGROUP_COMPACT or KVQ_KGROUP_TILE (K streams; V ignores it) */
+  uint8_t reserved[2];
   int32_t n_rows;            /* stored rows: n_tokens if dense, |active set| if sparse */
   int32_t n_tokens;          /* logical tokens T of the request */
   int32_t n_heads;           /* KV heads H */
@@ -110,6 +125,10 @@ size_t kvq_plane_bytes(const kvq_stream* s, int plane);
  * derived tile directory. 4.5 bits per element on full groups (codec PR review
  * by 0z5a); partial groups pay their padding (RFC §7.4). */
 int64_t kvq_stream_payload_bytes(int kind, int n_rows, int n_heads, int head_dim, int sparse);
+/* The same for any K grouping: a tile-grouped sparse K stream stores
+ * ceil(n_tokens/64) groups per (head, channel) whatever n_rows is. */
+int64_t kvq_stream_payload_bytes_ex(int kind, int n_rows, int n_tokens, int n_heads, int head_dim, int sparse,
+                                    int kgroup);
 
 /*
  * Encode the loop-1 base of K or V (RFC §3.3: X̂[1] = deq(q(X[1]))).
@@ -156,9 +175,11 @@ kvq_status kvq_reconstruct(const kvq_stream* loops, int depth, uint16_t* out, kv
  * memory (an array of kvq_request, one per request). The batched encode
  * writes the planes (and, for a sparse loop, the tile_dir) of the loop it
  * encodes; every other call only reads through these pointers. */
+#define KVQ_LOOP_K_TILE 1 /* kvq_loop_ref.flags: the K planes use KVQ_KGROUP_TILE */
+
 typedef struct kvq_loop_ref {
   int32_t n_rows;
-  int32_t reserved;
+  int32_t flags;             /* KVQ_LOOP_K_TILE or 0 */
   const int32_t* active_idx; /* NULL: dense */
   int32_t* tile_dir;         /* required for sparse loops */
   uint8_t* k_codes;

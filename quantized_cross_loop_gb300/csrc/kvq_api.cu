@@ -46,6 +46,8 @@ kvq_status check_format(const kvq_stream* s, const char* name) {
     return fail(KVQ_ERR_UNSUPPORTED, "%s: bits %d group %d nibble order %d", name, s->bits, s->group,
                 s->nibble_order);
   if (s->kind != KVQ_K && s->kind != KVQ_V) return fail(KVQ_ERR_BAD_ARG, "%s: kind %d", name, s->kind);
+  if (s->kgroup != KVQ_KGROUP_COMPACT && s->kgroup != KVQ_KGROUP_TILE)
+    return fail(KVQ_ERR_UNSUPPORTED, "%s: K grouping %d", name, s->kgroup);
   if (s->n_tokens < 0 || s->n_rows < 0 || s->n_rows > s->n_tokens)
     return fail(KVQ_ERR_BAD_ARG, "%s: n_rows %d n_tokens %d", name, s->n_rows, s->n_tokens);
   if (s->n_heads < 1 || s->n_heads > 1024) return fail(KVQ_ERR_BAD_ARG, "%s: n_heads %d", name, s->n_heads);
@@ -68,9 +70,13 @@ kvq_status check_planes(const kvq_stream* s, const char* name, bool need_dir) {
   return KVQ_OK;
 }
 
+bool k_tile(const kvq_stream* s) { return s->kind == KVQ_K && s->kgroup == KVQ_KGROUP_TILE; }
+
 void to_planes(const kvq_stream* s, LoopPlanes* p) {
   p->n_rows = s->n_rows;
   p->sparse = s->active_idx != nullptr;
+  p->ktile = k_tile(s);
+  p->kgroups = k_groups_of(k_tile(s), s->n_rows, s->n_tokens);
   p->active = s->active_idx;
   p->tile_dir = s->tile_dir;
   p->codes = s->codes;
@@ -177,7 +183,7 @@ size_t kvq_plane_bytes(const kvq_stream* s, int plane) {
     case KVQ_PLANE_CODES: return round16(size_t(H * n * (D / 2)));
     case KVQ_PLANE_MINS:
     case KVQ_PLANE_SCALES:
-      if (s->kind == KVQ_K) return round16(size_t(2 * H * cdiv(n, KVQ_GROUP) * D));
+      if (s->kind == KVQ_K) return round16(size_t(2 * H * k_groups_of(k_tile(s), s->n_rows, s->n_tokens) * D));
       return round16(size_t(2 * H * n * cdiv(D, KVQ_GROUP)));
     case KVQ_PLANE_INDEX: return n > 0 ? round16(size_t(4 * n)) : 16;  // never NULL: NULL means dense
     case KVQ_PLANE_TILE_DIR: return round16(size_t(4 * (cdiv(s->n_tokens, KVQ_TILE) + 1)));
@@ -185,15 +191,22 @@ size_t kvq_plane_bytes(const kvq_stream* s, int plane) {
   }
 }
 
-int64_t kvq_stream_payload_bytes(int kind, int n_rows, int n_heads, int head_dim, int sparse) {
+int64_t kvq_stream_payload_bytes_ex(int kind, int n_rows, int n_tokens, int n_heads, int head_dim, int sparse,
+                                    int kgroup) {
   const int64_t n = n_rows, H = n_heads, D = head_dim;
-  int64_t params = (kind == KVQ_K) ? H * cdiv(n, KVQ_GROUP) * D : H * n * cdiv(D, KVQ_GROUP);
+  const bool tile = kgroup == KVQ_KGROUP_TILE && sparse;
+  int64_t params = (kind == KVQ_K) ? H * k_groups_of(tile, n_rows, n_tokens) * D : H * n * cdiv(D, KVQ_GROUP);
   return H * n * (D / 2) + 2 * 2 * params + (sparse ? 4 * n : 0);
+}
+
+int64_t kvq_stream_payload_bytes(int kind, int n_rows, int n_heads, int head_dim, int sparse) {
+  return kvq_stream_payload_bytes_ex(kind, n_rows, n_rows, n_heads, head_dim, sparse, KVQ_KGROUP_COMPACT);
 }
 
 // Planes of a stream descriptor as one loop entry of a request.
 static void to_loop_ref(const kvq_stream* s, kvq_loop_ref* L) {
   L->n_rows = s->n_rows;
+  if (k_tile(s)) L->flags |= KVQ_LOOP_K_TILE;
   L->active_idx = s->active_idx;
   L->tile_dir = s->tile_dir;
   if (s->kind == KVQ_K) {
@@ -406,6 +419,7 @@ kvq_status kvq_request_fill(const kvq_stream* k_loops, const kvq_stream* v_loops
     if (j == 0 && k->active_idx != nullptr) return fail(KVQ_ERR_BAD_ARG, "loop 1 must be dense");
     kvq_loop_ref& L = out->loop[j];
     L.n_rows = k->n_rows;
+    L.flags = k_tile(k) ? KVQ_LOOP_K_TILE : 0;
     L.active_idx = k->active_idx;
     L.tile_dir = k->tile_dir ? k->tile_dir : v->tile_dir;
     L.k_codes = k->codes;

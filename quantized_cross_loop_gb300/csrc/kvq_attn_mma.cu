@@ -64,6 +64,7 @@ constexpr uint32_t kMagic = 0x54005400u;     // FP16 64.0 in both halves
 //       tokens belong to the request's BF16 sink)
 //   pair p (8 words from 8): loop index << 1 | group
 //   loop j (8 words from 16 + 8j): nrows c0 g0 ngrp vrem irem sparse pbase
+//       (c0: first stored row of the tile; under tile grouping of K, 64 x tile)
 constexpr int kMetaWords = 16 + 8 * kLoops;
 
 // One loop's staged planes of a tile (every field a multiple of 16 bytes, so
@@ -209,7 +210,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
   int b = request_of(a.prefix, a.n_requests, s0);
   long long us = 0, ue = -1;  // current unit's tile range
   int h = 0, T = 0, unit = -1, nsink = 0;
-  int nr[DEPTH];
+  int nr[DEPTH], kgr[DEPTH];  // stored rows; K groups per head (0: compact grouping, else tile grouping)
   const int32_t* act[DEPTH];
   const int32_t* dir[DEPTH];
   const uint8_t* kc[DEPTH];
@@ -235,6 +236,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       for (int j = 0; j < DEPTH; ++j) {
         const kvq_loop_ref& L = R.loop[j];
         nr[j] = L.n_rows;
+        kgr[j] = (L.flags & KVQ_LOOP_K_TILE) ? k_groups_of(true, L.n_rows, T) : 0;
         act[j] = L.active_idx;
         dir[j] = L.tile_dir;
         kc[j] = L.k_codes;
@@ -283,10 +285,13 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
         c0 = c1 = 0;
       }
       const int n = c1 - c0;
-      const int g0 = c0 / kG;
-      const int ngrp = n > 0 ? (c1 - 1) / kG - g0 + 1 : 0;
+      // K groups of the tile's rows: under tile grouping the tile's own group k,
+      // and word 1 is set so that a consumer's ((word1 + row) >> 6) - g0 is 0
+      const bool kt = kgr[j] > 0;
+      const int g0 = kt ? k : c0 / kG;
+      const int ngrp = n > 0 ? (kt ? 1 : (c1 - 1) / kG - g0 + 1) : 0;
       LM[0] = n;
-      LM[1] = c0;
+      LM[1] = kt ? k * kG : c0;
       LM[2] = g0;
       LM[3] = ngrp;
       LM[4] = 0;
@@ -298,7 +303,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       const long long hr = (long long)h * nr[j] + c0;  // first stored row of this head
       bulk_copy(st.l[j].kc, kc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
       bulk_copy(st.l[j].vc, vc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
-      const long long gb = ((long long)h * ((nr[j] + kG - 1) / kG) + g0) * kD;
+      const long long gb = ((long long)h * (kt ? kgr[j] : (nr[j] + kG - 1) / kG) + g0) * kD;
       bulk_copy(st.l[j].kmin, kmn[j] + gb, ngrp * kD * 2, &S.full[s]);
       bulk_copy(st.l[j].ksc, ksc[j] + gb, ngrp * kD * 2, &S.full[s]);
       {  // V params: 4 B per row and plane, moved in whole 16-byte units

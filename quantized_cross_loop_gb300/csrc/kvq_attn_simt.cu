@@ -264,16 +264,7 @@ __device__ void simt_load_unit(const AttnArgs& a, SimtSmem& S, int b, int h) {
       C.kind = kind;
       C.n_tokens = r.n_tokens;
       C.n_heads = a.H;
-      for (int j = 0; j < a.depth; ++j) {
-        const kvq_loop_ref& L = r.loop[j];
-        C.loop[j].n_rows = L.n_rows;
-        C.loop[j].sparse = L.active_idx != nullptr;
-        C.loop[j].active = L.active_idx;
-        C.loop[j].tile_dir = L.tile_dir;
-        C.loop[j].codes = kind == 0 ? L.k_codes : L.v_codes;
-        C.loop[j].mins = kind == 0 ? L.k_mins : L.v_mins;
-        C.loop[j].scales = kind == 0 ? L.k_scales : L.v_scales;
-      }
+      for (int j = 0; j < a.depth; ++j) planes_of(r, j, kind, C.loop[j]);
     }
   }
 }
@@ -364,8 +355,8 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
           int rows[KVQ_MAX_LOOPS];
           for (int j = 0; j < a.depth; ++j) rows[j] = S.map[j][tt];
           float kv[4], vv[4];
-          chain4_f32(S.ck, a.depth, rows, h, c0, kv);
-          chain4_f32(S.cv, a.depth, rows, h, c0, vv);
+          chain4_f32(S.ck, a.depth, rows, t0 + tt, h, c0, kv);
+          chain4_f32(S.cv, a.depth, rows, t0 + tt, h, c0, vv);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             S.khat[tt][c0 + e] = kv[e];

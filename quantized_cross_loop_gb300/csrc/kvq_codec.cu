@@ -34,10 +34,10 @@ __device__ __forceinline__ const kvq_request& req_at(const CodecArgs& a, int b) 
 __device__ __forceinline__ int items_of(const CodecArgs& a, const kvq_request& R, int mode) {
   if (R.n_tokens < 0 || R.n_loops > KVQ_MAX_LOOPS) return 0;
   switch (mode) {
-    case kModeEncK: {
+    case kModeEncK: {  // one item per (K group, head)
       if (a.loop >= R.n_loops) return 0;
-      int n = R.loop[a.loop].n_rows;
-      return n > 0 ? a.H * ((n + kG - 1) / kG) : 0;
+      const kvq_loop_ref& L = R.loop[a.loop];
+      return a.H * k_groups_of((L.flags & KVQ_LOOP_K_TILE) != 0, L.n_rows, R.n_tokens);
     }
     case kModeEncV: {
       if (a.loop >= R.n_loops) return 0;
@@ -146,17 +146,7 @@ __device__ void fill_chain(const kvq_request& R, int kind, int n, int H, Chain& 
   C.kind = kind;
   C.n_tokens = R.n_tokens;
   C.n_heads = H;
-  for (int j = 0; j < n; ++j) {
-    const kvq_loop_ref& L = R.loop[j];
-    LoopPlanes& P = C.loop[j];
-    P.n_rows = L.n_rows;
-    P.sparse = L.active_idx != nullptr;
-    P.active = L.active_idx;
-    P.tile_dir = L.tile_dir;
-    P.codes = kind == KVQ_K ? L.k_codes : L.v_codes;
-    P.mins = kind == KVQ_K ? L.k_mins : L.v_mins;
-    P.scales = kind == KVQ_K ? L.k_scales : L.v_scales;
-  }
+  for (int j = 0; j < n; ++j) planes_of(R, j, kind, C.loop[j]);
 }
 
 __device__ __forceinline__ const uint16_t* source_of(const CodecArgs& a, int b) {
@@ -196,8 +186,18 @@ __global__ void __launch_bounds__(kD) encode_k_generic_kernel(const __grid_const
     const int g = local / H, h = local % H;
     const LoopPlanes& O = C.loop[r];
     const int n = O.n_rows;
-    const int r0 = g * kG;
-    const int len = min(kG, n - r0);
+    // rows of group g: 64 consecutive stored rows, or those of logical tile g
+    int r0 = g * kG, len = min(kG, n - r0);
+    if (O.ktile && O.sparse) {
+      r0 = __ldg(O.tile_dir + g);
+      const int r1 = __ldg(O.tile_dir + g + 1);
+      len = r1 - r0;
+      if (r0 < 0 || r1 > n || len < 0 || len > kG) {  // inconsistent tile map: leave the group
+        if (d == 0 && a.err) atomicOr(a.err, 4);
+        r0 = 0;
+        len = 0;
+      }
+    }
     const uint16_t* x = source_of(a, b);
 
     if (d < len) {
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kD) encode_k_generic_kernel(const __grid_const
         if (r > 0) {
           int rows[KVQ_MAX_LOOPS];
           for (int j = 0; j < r; ++j) rows[j] = s_row[j][i];
-          val = round_bf16(__fsub_rn(xv, chain1(C, r, rows, h, d)));
+          val = round_bf16(__fsub_rn(xv, chain1(C, r, rows, t, h, d)));
         }
         v[i] = val;
         if (i == 0) {
@@ -238,7 +238,8 @@ __global__ void __launch_bounds__(kD) encode_k_generic_kernel(const __grid_const
       int hi = __shfl_down_sync(0xffffffffu, c, 1);
       if ((d & 1) == 0 && i < len) s_codes[i][d >> 1] = uint8_t(c | (hi << 4));
     }
-    long long pi = ((long long)h * ((n + kG - 1) / kG) + g) * kD + d;
+    // (a tile with no stored row keeps +0 min and +0 scale)
+    long long pi = ((long long)h * O.kgroups + g) * kD + d;
     const_cast<uint16_t*>(O.mins)[pi] = f32_to_f16_bits(mn);
     const_cast<uint16_t*>(O.scales)[pi] = f32_to_f16_bits(s32);
     __syncthreads();
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__(kEncVThreads) encode_v_generic_kernel(const __
         int rows[KVQ_MAX_LOOPS];
         for (int j = 0; j < r; ++j) rows[j] = s_row[j][i];
         float xh[4];
-        chain4(C, r, rows, h, c0, xh);
+        chain4(C, r, rows, t, h, c0, xh);
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[e] = round_bf16(__fsub_rn(xv[e], xh[e]));
       }
@@ -417,7 +418,7 @@ __global__ void __launch_bounds__(kReconThreads) reconstruct_generic_kernel(cons
       int rows[KVQ_MAX_LOOPS];
       for (int j = 0; j < depth; ++j) rows[j] = s_map[j][tt];
       float v[4];
-      chain4(C, depth, rows, h, lane * 4, v);
+      chain4(C, depth, rows, t0 + tt, h, lane * 4, v);
       uint2 o;
       o.x = uint32_t(f32_to_bf16_bits(v[0])) | (uint32_t(f32_to_bf16_bits(v[1])) << 16);
       o.y = uint32_t(f32_to_bf16_bits(v[2])) | (uint32_t(f32_to_bf16_bits(v[3])) << 16);
@@ -555,7 +556,7 @@ __device__ __forceinline__ int kpar_slot(int pair) { return (pair & ~7) | (((pai
 
 // Stages groups g0 .. g0 + ng - 1 of head h of loop L (K) into par[0 .. ng-1][64].
 __device__ __forceinline__ void stage_kpar(const LoopPlanes& L, int h, int g0, int ng, float4 (*par)[kD / 2]) {
-  const long long G = (L.n_rows + kG - 1) / kG;
+  const long long G = L.kgroups;
   for (int idx = threadIdx.x; idx < ng * (kD / 2); idx += blockDim.x) {
     const int gi = idx / (kD / 2), pair = idx % (kD / 2);
     const long long pi = ((long long)h * G + g0 + gi) * kD + 2 * pair;
@@ -565,12 +566,12 @@ __device__ __forceinline__ void stage_kpar(const LoopPlanes& L, int h, int g0, i
   }
 }
 
-// Parameters of the 16 channels 16 sub .. 16 sub + 15 for stored row `row` of
-// head h of K loop L: from the staged groups when the row's group is among
-// them, else from the planes.
-__device__ __forceinline__ void load_kpar16(const LoopPlanes& L, int h, int row, int sub,
+// Parameters of the 16 channels 16 sub .. 16 sub + 15 of K group `grp` of
+// head h of K loop L: from the staged groups when the group is among them,
+// else from the planes.
+__device__ __forceinline__ void load_kpar16(const LoopPlanes& L, int h, int grp, int sub,
                                             const float4 (*par)[kD / 2], int g0, int ng, float2* m, float2* s) {
-  const int gi = (row >> 6) - g0;
+  const int gi = grp - g0;
   if (gi >= 0 && gi < ng) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -579,7 +580,7 @@ __device__ __forceinline__ void load_kpar16(const LoopPlanes& L, int h, int row,
       s[k] = make_float2(q.z, q.w);
     }
   } else {
-    const long long pi = ((long long)h * ((L.n_rows + kG - 1) / kG) + (row >> 6)) * kD + 16 * sub;
+    const long long pi = ((long long)h * L.kgroups + grp) * kD + 16 * sub;
     const uint4* mp = reinterpret_cast<const uint4*>(L.mins + pi);
     const uint4* sp = reinterpret_cast<const uint4*>(L.scales + pi);
     const uint4 m0 = __ldg(mp), m1 = __ldg(mp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
@@ -593,19 +594,21 @@ __device__ __forceinline__ void load_kpar16(const LoopPlanes& L, int h, int row,
   }
 }
 
-// Decodes the 16 channels 16 sub .. 16 sub + 15 of one stored K row (codes cw)
-// into 8 BF16 pairs.
-__device__ __forceinline__ void dequant16_k(const LoopPlanes& L, int h, int row, uint2 cw, int sub,
+// Decodes the 16 channels 16 sub .. 16 sub + 15 of one stored K row (codes cw,
+// K group grp) into 8 BF16 pairs.
+__device__ __forceinline__ void dequant16_k(const LoopPlanes& L, int h, int grp, uint2 cw, int sub,
                                             const float4 (*par)[kD / 2], int g0, int ng, uint32_t* out) {
   float2 m[8], s[8];
-  load_kpar16(L, h, row, sub, par, g0, ng, m, s);
+  load_kpar16(L, h, grp, sub, par, g0, ng, m, s);
   fast::dequant_word_pp(cw.x, m, s, out);
   fast::dequant_word_pp(cw.y, m + 4, s + 4, out + 4);
 }
 
 // ---------------------------------------------------------------- encode K (fast)
 //
-// item = (64-row compact group, head), 256 threads, two phases.
+// item = (K group, head), 256 threads, two phases. A K group is 64 consecutive
+// stored rows, or (tile grouping of a sparse loop) the stored rows of one
+// 64-token logical tile, found through the tile directory.
 //  1. Residuals: eight lanes per row (lane `sub` = channels 16 sub .. +15), a
 //     warp four rows; every load of a row is issued before its arithmetic and
 //     the BF16 residual pairs go to a shared [row][pair] tile.
@@ -658,8 +661,24 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
     const int g = local / H, h = local % H;
     const LoopPlanes& O = S.C.loop[R];
     const int n = O.n_rows;
-    const int r0 = g * kG;
-    const int len = min(kG, n - r0);
+    int r0 = g * kG, len = min(kG, n - r0);
+    if (O.ktile && O.sparse) {
+      r0 = __ldg(O.tile_dir + g);
+      const int r1 = __ldg(O.tile_dir + g + 1);
+      len = r1 - r0;
+      if (r0 < 0 || r1 > n || len < 0 || len > kG) {  // inconsistent tile map: leave the group
+        if (tid == 0 && a.err) atomicOr(a.err, 4);
+        continue;
+      }
+    }
+    const long long opi = ((long long)h * O.kgroups + g) * kD;  // this group's params
+    if (len == 0) {  // a logical tile with no stored row: +0 min and +0 scale
+      if (tid < kD / 2) {
+        *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.mins) + opi + 2 * tid) = 0u;
+        *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.scales) + opi + 2 * tid) = 0u;
+      }
+      continue;
+    }
     const uint16_t* x = source_of(a, b);
     if (tid < len) {
       const int t = O.sparse ? __ldg(O.active + r0 + tid) : r0 + tid;
@@ -669,8 +688,9 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
         const int row = row_of(S.C.loop[j], t);
         S.row[j][tid] = row;
         if (row >= 0) {
-          atomicMin(&S.glo[j], row >> 6);
-          atomicMax(&S.ghi[j], row >> 6);
+          const int kg = k_group(S.C.loop[j], t, row);
+          atomicMin(&S.glo[j], kg);
+          atomicMax(&S.ghi[j], kg);
         }
       }
     }
@@ -726,7 +746,8 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
         for (int j = 0; j < R; ++j) {
           if (rows[j] < 0) continue;
           uint32_t dq[8];
-          dequant16_k(S.C.loop[j], h, rows[j], cw[j], sub, S.par[j], g0[j], ng[j], dq);
+          dequant16_k(S.C.loop[j], h, k_group(S.C.loop[j], S.tok[i], rows[j]), cw[j], sub, S.par[j], g0[j], ng[j],
+                      dq);
 #pragma unroll
           for (int k = 0; k < 8; ++k) acc[k] = (j == 0) ? dq[k] : bf2_add(acc[k], dq[k]);
         }
@@ -781,7 +802,7 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
       const float s0 = scale_of(mn[0], mx[0]), s1 = scale_of(mn[1], mx[1]);
       S.qp[p] = make_float4(mn[0], mn[1], recip_of(s0), recip_of(s1));
       S.qs[p] = make_float2(s0, s1);
-      const long long pi = ((long long)h * ((n + kG - 1) / kG) + g) * kD + 2 * p;
+      const long long pi = opi + 2 * p;
       *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.mins) + pi) = f16_pair(mn[0], mn[1]);
       *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.scales) + pi) = f16_pair(s0, s1);
     }
@@ -1009,7 +1030,7 @@ __device__ __forceinline__ int row_in(const TileRows& r, int tt) {
 
 // K parameters of the 16 channels 16 sub .. +15 of group `grp` of head h, loop L.
 __device__ __forceinline__ void load_kpar16_global(const LoopPlanes& L, int h, int grp, int sub, float2* m, float2* s) {
-  const long long pi = ((long long)h * ((L.n_rows + kG - 1) / kG) + grp) * kD + 16 * sub;
+  const long long pi = ((long long)h * L.kgroups + grp) * kD + 16 * sub;
   const uint4* mp = reinterpret_cast<const uint4*>(L.mins + pi);
   const uint4* sp = reinterpret_cast<const uint4*>(L.scales + pi);
   const uint4 m0 = __ldg(mp), m1 = __ldg(mp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
@@ -1089,8 +1110,9 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
       for (int u = 0; u < kReconKTok; ++u) {
         const int row = rows[u][j];
         if (row < 0) continue;
-        if ((row >> 6) != cached) {
-          cached = row >> 6;
+        const int grp = L.ktile ? k : (row >> 6);  // tile grouping: the tile's own group
+        if (grp != cached) {
+          cached = grp;
           load_kpar16_global(L, h, cached, sub, m, s);
         }
         uint32_t dq[8];
@@ -1199,7 +1221,10 @@ static int single_items(const CodecArgs& a, int mode) {
   const kvq_request& R = a.one;
   const int n = R.loop[a.loop < KVQ_MAX_LOOPS ? a.loop : 0].n_rows;
   switch (mode) {
-    case kModeEncK: return n > 0 ? a.H * ((n + kG - 1) / kG) : 0;
+    case kModeEncK: {
+      const kvq_loop_ref& L = R.loop[a.loop < KVQ_MAX_LOOPS ? a.loop : 0];
+      return a.H * k_groups_of((L.flags & KVQ_LOOP_K_TILE) != 0, n, R.n_tokens);
+    }
     case kModeEncV: return (n + kG - 1) / kG;
     case kModeTileDir: return R.loop[a.loop].active_idx ? (R.n_tokens + KVQ_TILE - 1) / KVQ_TILE + 1 : 0;
     case kModeReconK: return ((R.n_tokens + KVQ_TILE - 1) / KVQ_TILE) * a.H;

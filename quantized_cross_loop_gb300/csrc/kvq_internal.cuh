@@ -24,6 +24,8 @@ constexpr int kRowBytes = kD / 2;  // packed bytes per (row, head)
 struct LoopPlanes {
   int32_t n_rows;
   int32_t sparse;
+  int32_t ktile;    // K groups by 64-token logical tile (KVQ_KGROUP_TILE) instead of 64 stored rows
+  int32_t kgroups;  // K groups per head: ceil(n_tokens/64) if ktile, else ceil(n_rows/64)
   const int32_t* active;
   const int32_t* tile_dir;
   const uint8_t* codes;
@@ -71,14 +73,40 @@ __device__ __forceinline__ int sparse_rank(const LoopPlanes& L, int t) {
 
 __device__ __forceinline__ int row_of(const LoopPlanes& L, int t) { return L.sparse ? sparse_rank(L, t) : t; }
 
-__device__ __forceinline__ long long param_index(int kind, int n_rows, int h, int row, int d) {
-  if (kind == KVQ_K) return ((long long)h * ((n_rows + kG - 1) / kG) + row / kG) * kD + d;
-  return ((long long)h * n_rows + row) * (kD / kG) + d / kG;
+// K groups per head of a loop with n_rows stored rows of n_tokens tokens.
+__host__ __device__ __forceinline__ int k_groups_of(bool ktile, int n_rows, int n_tokens) {
+  if (n_rows <= 0) return 0;
+  return ktile ? (n_tokens + kG - 1) / kG : (n_rows + kG - 1) / kG;
+}
+
+// K group of the stored row `row` of logical token t: its 64-token logical tile
+// under tile grouping, else its block of 64 stored rows (the same for a dense loop).
+__device__ __forceinline__ int k_group(const LoopPlanes& L, int t, int row) { return L.ktile ? (t >> 6) : (row >> 6); }
+
+// Index of the params of (head h, logical token t stored at `row`, channel d).
+__device__ __forceinline__ long long param_index(int kind, const LoopPlanes& L, int h, int t, int row, int d) {
+  if (kind == KVQ_K) return ((long long)h * L.kgroups + k_group(L, t, row)) * kD + d;
+  return ((long long)h * L.n_rows + row) * (kD / kG) + d / kG;
+}
+
+// Loop j of request R as the K (kind 0) or V planes the kernels read.
+__device__ __forceinline__ void planes_of(const kvq_request& R, int j, int kind, LoopPlanes& P) {
+  const kvq_loop_ref& L = R.loop[j];
+  P.n_rows = L.n_rows;
+  P.sparse = L.active_idx != nullptr;
+  P.ktile = kind == KVQ_K && (L.flags & KVQ_LOOP_K_TILE) != 0;
+  P.kgroups = k_groups_of(P.ktile != 0, L.n_rows, R.n_tokens);
+  P.active = L.active_idx;
+  P.tile_dir = L.tile_dir;
+  P.codes = kind == KVQ_K ? L.k_codes : L.v_codes;
+  P.mins = kind == KVQ_K ? L.k_mins : L.v_mins;
+  P.scales = kind == KVQ_K ? L.k_scales : L.v_scales;
 }
 
 // Reconstruct 4 consecutive channels c0..c0+3 (c0 % 4 == 0) of token t, head h,
 // through loops 0..depth-1, given each loop's stored row (rows[j] < 0: absent).
-__device__ __forceinline__ void chain4(const Chain& C, int depth, const int* rows, int h, int c0, float out[4]) {
+__device__ __forceinline__ void chain4(const Chain& C, int depth, const int* rows, int t, int h, int c0,
+                                       float out[4]) {
   {
     const LoopPlanes& B = C.loop[0];
     int row = rows[0];
@@ -86,7 +114,7 @@ __device__ __forceinline__ void chain4(const Chain& C, int depth, const int* row
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       int c = (two >> (4 * e)) & 0xF;
-      long long pi = param_index(C.kind, B.n_rows, h, row, c0 + e);
+      long long pi = param_index(C.kind, B, h, t, row, c0 + e);
       out[e] = dequant(__ldg(B.mins + pi), __ldg(B.scales + pi), c);
     }
   }
@@ -98,7 +126,7 @@ __device__ __forceinline__ void chain4(const Chain& C, int depth, const int* row
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       int c = (two >> (4 * e)) & 0xF;
-      long long pi = param_index(C.kind, L.n_rows, h, row, c0 + e);
+      long long pi = param_index(C.kind, L, h, t, row, c0 + e);
       out[e] = round_bf16(__fadd_rn(out[e], dequant(__ldg(L.mins + pi), __ldg(L.scales + pi), c)));
     }
   }
@@ -108,7 +136,8 @@ __device__ __forceinline__ void chain4(const Chain& C, int depth, const int* row
 // summed with FP32 rounding only (the values a direct packed reader uses).
 // The four channels share one V group, and their K parameters are adjacent,
 // so each loop's parameters come in one load per plane.
-__device__ __forceinline__ void chain4_f32(const Chain& C, int depth, const int* rows, int h, int c0, float out[4]) {
+__device__ __forceinline__ void chain4_f32(const Chain& C, int depth, const int* rows, int t, int h, int c0,
+                                           float out[4]) {
 #pragma unroll
   for (int e = 0; e < 4; ++e) out[e] = 0.0f;
   for (int j = 0; j < depth; ++j) {
@@ -118,7 +147,7 @@ __device__ __forceinline__ void chain4_f32(const Chain& C, int depth, const int*
     uint16_t two = *reinterpret_cast<const uint16_t*>(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + c0 / 2);
     float mn[4], sc[4];
     if (C.kind == KVQ_K) {
-      const long long pi = param_index(KVQ_K, L.n_rows, h, row, c0);
+      const long long pi = param_index(KVQ_K, L, h, t, row, c0);
       const uint2 m4 = __ldg(reinterpret_cast<const uint2*>(L.mins + pi));
       const uint2 s4 = __ldg(reinterpret_cast<const uint2*>(L.scales + pi));
       const uint32_t mw[2] = {m4.x, m4.y}, sw[2] = {s4.x, s4.y};
@@ -128,7 +157,7 @@ __device__ __forceinline__ void chain4_f32(const Chain& C, int depth, const int*
         sc[e] = f16_bits_to_f32(uint16_t(sw[e >> 1] >> (16 * (e & 1))));
       }
     } else {
-      const long long pi = param_index(KVQ_V, L.n_rows, h, row, c0);
+      const long long pi = param_index(KVQ_V, L, h, t, row, c0);
       const float m1 = f16_bits_to_f32(__ldg(L.mins + pi)), s1 = f16_bits_to_f32(__ldg(L.scales + pi));
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -146,14 +175,14 @@ __device__ __forceinline__ void chain4_f32(const Chain& C, int depth, const int*
 }
 
 // Same for one channel d.
-__device__ __forceinline__ float chain1(const Chain& C, int depth, const int* rows, int h, int d) {
+__device__ __forceinline__ float chain1(const Chain& C, int depth, const int* rows, int t, int h, int d) {
   float v;
   {
     const LoopPlanes& B = C.loop[0];
     int row = rows[0];
     uint8_t byte = __ldg(B.codes + ((long long)h * B.n_rows + row) * kRowBytes + d / 2);
     int c = (d & 1) ? (byte >> 4) : (byte & 0xF);
-    long long pi = param_index(C.kind, B.n_rows, h, row, d);
+    long long pi = param_index(C.kind, B, h, t, row, d);
     v = dequant(__ldg(B.mins + pi), __ldg(B.scales + pi), c);
   }
   for (int j = 1; j < depth; ++j) {
@@ -162,7 +191,7 @@ __device__ __forceinline__ float chain1(const Chain& C, int depth, const int* ro
     const LoopPlanes& L = C.loop[j];
     uint8_t byte = __ldg(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + d / 2);
     int c = (d & 1) ? (byte >> 4) : (byte & 0xF);
-    long long pi = param_index(C.kind, L.n_rows, h, row, d);
+    long long pi = param_index(C.kind, L, h, t, row, d);
     v = round_bf16(__fadd_rn(v, dequant(__ldg(L.mins + pi), __ldg(L.scales + pi), c)));
   }
   return v;

@@ -32,17 +32,7 @@ __device__ void chain_of(const kvq_request& r, int kind, int depth, int H, Chain
   C.kind = kind;
   C.n_tokens = r.n_tokens;
   C.n_heads = H;
-  for (int j = 0; j < depth; ++j) {
-    const kvq_loop_ref& L = r.loop[j];
-    LoopPlanes& P = C.loop[j];
-    P.n_rows = L.n_rows;
-    P.sparse = L.active_idx != nullptr;
-    P.active = L.active_idx;
-    P.tile_dir = L.tile_dir;
-    P.codes = kind == KVQ_K ? L.k_codes : L.v_codes;
-    P.mins = kind == KVQ_K ? L.k_mins : L.v_mins;
-    P.scales = kind == KVQ_K ? L.k_scales : L.v_scales;
-  }
+  for (int j = 0; j < depth; ++j) planes_of(r, j, kind, C.loop[j]);
 }
 
 // A request the sparse kernels accept: a consistent packed chain, no BF16
@@ -89,7 +79,7 @@ __global__ void __launch_bounds__(128) sparse_logits_kernel(SparseArgs a) {
     int rows[KVQ_MAX_LOOPS];
     rows_of(C, a.depth, t, rows);
     float kv[4];
-    chain4_f32(C, a.depth, rows, h, 4 * lane, kv);
+    chain4_f32(C, a.depth, rows, t, h, 4 * lane, kv);
     for (int i = 0; i < g; ++i) {
       float s = qs[i][4 * lane] * kv[0] + qs[i][4 * lane + 1] * kv[1] + qs[i][4 * lane + 2] * kv[2] +
                 qs[i][4 * lane + 3] * kv[3];
@@ -244,7 +234,7 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseArgs a
     int rows[KVQ_MAX_LOOPS];
     rows_of(C, a.depth, t, rows);
     float vv[4];
-    chain4_f32(C, a.depth, rows, h, 4 * lane, vv);
+    chain4_f32(C, a.depth, rows, t, h, 4 * lane, vv);
     const float p = exp2f(s[t] - M) / L;
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] = fmaf(p, vv[e], acc[e]);
@@ -307,8 +297,8 @@ __global__ void __launch_bounds__(32 * kAttnWarps) sparse_attn_kernel(SparseArgs
       for (int j = 0; j < a.depth; ++j) rows[j] = __shfl_sync(0xffffffffu, my_rows[j], kk);
       if (t < 0) continue;
       float kv[4], vv[4];
-      chain4_f32(CK, a.depth, rows, h, 4 * lane, kv);
-      chain4_f32(CV, a.depth, rows, h, 4 * lane, vv);
+      chain4_f32(CK, a.depth, rows, t, h, 4 * lane, kv);
+      chain4_f32(CV, a.depth, rows, t, h, 4 * lane, vv);
       float s = qs[4 * lane] * kv[0] + qs[4 * lane + 1] * kv[1] + qs[4 * lane + 2] * kv[2] + qs[4 * lane + 3] * kv[3];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);

@@ -26,6 +26,8 @@ KVQ_MAX_LOOPS = 8
 KVQ_FORMAT_VERSION = 1
 PLANE_CODES, PLANE_MINS, PLANE_SCALES, PLANE_INDEX, PLANE_TILE_DIR = range(5)
 ATTN_AUTO, ATTN_SIMT, ATTN_MMA = 0, 1, 2
+KVQ_KGROUP_COMPACT, KVQ_KGROUP_TILE = 0, 1  # K groups: 64 stored rows / the stored rows of one 64-token tile
+KVQ_LOOP_K_TILE = 1
 
 EXPORTED = (
     "kvq_stream_init", "kvq_plane_bytes", "kvq_stream_payload_bytes", "kvq_encode_base", "kvq_encode_residual",
@@ -33,7 +35,7 @@ EXPORTED = (
     "kvq_decode_attn_packed", "kvq_decode_attn_packed_ex", "kvq_status_string", "kvq_last_error", "kvq_version",
     "kvq_batch_workspace_bytes", "kvq_encode_batch", "kvq_reconstruct_batch", "kvq_launch_count",
     "kvq_decode_attn_packed_noalloc", "kvq_sparse_workspace_bytes", "kvq_sparse_ref_state",
-    "kvq_sparse_decode_attn",
+    "kvq_sparse_decode_attn", "kvq_stream_payload_bytes_ex",
 )
 
 
@@ -48,7 +50,8 @@ class kvq_stream(ctypes.Structure):
         ("kind", ctypes.c_uint8),
         ("group", ctypes.c_uint16),
         ("nibble_order", ctypes.c_uint8),
-        ("reserved", ctypes.c_uint8 * 3),
+        ("kgroup", ctypes.c_uint8),
+        ("reserved", ctypes.c_uint8 * 2),
         ("n_rows", ctypes.c_int32),
         ("n_tokens", ctypes.c_int32),
         ("n_heads", ctypes.c_int32),
@@ -64,7 +67,7 @@ class kvq_stream(ctypes.Structure):
 class kvq_loop_ref(ctypes.Structure):
     _fields_ = [
         ("n_rows", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
         ("active_idx", ctypes.c_void_p),
         ("tile_dir", ctypes.c_void_p),
         ("k_codes", ctypes.c_void_p),
@@ -109,6 +112,8 @@ def lib():
             L.kvq_plane_bytes.restype = sz
             L.kvq_stream_payload_bytes.argtypes = [i32, i32, i32, i32, i32]
             L.kvq_stream_payload_bytes.restype = ctypes.c_int64
+            L.kvq_stream_payload_bytes_ex.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.kvq_stream_payload_bytes_ex.restype = ctypes.c_int64
             L.kvq_encode_base.argtypes = [vp, P(kvq_stream), vp]
             L.kvq_encode_residual.argtypes = [vp, P(kvq_stream), i32, P(kvq_stream), vp]
             L.kvq_build_tile_dir.argtypes = [vp, i32, i32, vp, vp]
@@ -171,11 +176,13 @@ class Stream:
     the C descriptor pointing at them."""
 
     def __init__(self, kind: int, n_rows: int, n_tokens: int, n_heads: int, head_dim: int, device,
-                 active: torch.Tensor | None = None, alloc=None, shared_index=None):
+                 active: torch.Tensor | None = None, alloc=None, shared_index=None, kgroup: int = KVQ_KGROUP_COMPACT):
         self.desc = kvq_stream()
         _check(lib().kvq_stream_init(ctypes.byref(self.desc), kind, n_rows, n_tokens, n_heads, head_dim),
                "kvq_stream_init")
+        self.desc.kgroup = kgroup
         self.kind, self.n_rows, self.n_tokens, self.n_heads, self.head_dim = kind, n_rows, n_tokens, n_heads, head_dim
+        self.kgroup = kgroup
 
         def plane(p):
             nbytes = int(lib().kvq_plane_bytes(ctypes.byref(self.desc), p))
@@ -212,7 +219,10 @@ class Stream:
 
     def param_shape(self):
         if self.kind == KVQ_K:
-            return (self.n_heads, -(-self.n_rows // KVQ_GROUP), self.head_dim)
+            groups = -(-self.n_rows // KVQ_GROUP)
+            if self.kgroup == KVQ_KGROUP_TILE and self.n_rows > 0:
+                groups = -(-self.n_tokens // KVQ_GROUP)
+            return (self.n_heads, groups, self.head_dim)
         return (self.n_heads, self.n_rows, -(-self.head_dim // KVQ_GROUP))
 
     def mins_view(self):
@@ -232,27 +242,34 @@ class Stream:
         return self.tile_dir.view(torch.int32)[: -(-self.n_tokens // KVQ_TILE) + 1]
 
 
-def payload_bytes(kind: int, n_rows: int, n_heads: int, head_dim: int, sparse: bool) -> int:
-    return int(lib().kvq_stream_payload_bytes(kind, n_rows, n_heads, head_dim, int(sparse)))
+def payload_bytes(kind: int, n_rows: int, n_heads: int, head_dim: int, sparse: bool, n_tokens: int | None = None,
+                  kgroup: int = KVQ_KGROUP_COMPACT) -> int:
+    if n_tokens is None and kgroup == KVQ_KGROUP_COMPACT:
+        return int(lib().kvq_stream_payload_bytes(kind, n_rows, n_heads, head_dim, int(sparse)))
+    T = n_rows if n_tokens is None else n_tokens
+    return int(lib().kvq_stream_payload_bytes_ex(kind, n_rows, T, n_heads, head_dim, int(sparse), kgroup))
 
 
-def kvq_encode_base(x: torch.Tensor, kind: int, stream=None) -> Stream:
-    """Encode the loop-1 base of K (kind=KVQ_K) or V from BF16 x [T, H, D]."""
+def kvq_encode_base(x: torch.Tensor, kind: int, stream=None, kgroup: int = KVQ_KGROUP_COMPACT) -> Stream:
+    """Encode the loop-1 base of K (kind=KVQ_K) or V from BF16 x [T, H, D]. The
+    base is dense, so `kgroup` changes no byte; it is recorded with the stream."""
     _require_cuda(x, "x", torch.bfloat16)
     T, H, D = x.shape
-    out = Stream(kind, T, T, H, D, x.device)
+    out = Stream(kind, T, T, H, D, x.device, kgroup=kgroup)
     _check(lib().kvq_encode_base(_dptr(x), ctypes.byref(out.desc), _stream_handle(stream)), "kvq_encode_base")
     return out
 
 
-def kvq_encode_residual(x_r: torch.Tensor, prev: list, active: torch.Tensor | None = None, stream=None) -> Stream:
+def kvq_encode_residual(x_r: torch.Tensor, prev: list, active: torch.Tensor | None = None, stream=None,
+                        kgroup: int | None = None) -> Stream:
     """Encode loop len(prev)+1 of the chain `prev` from BF16 x_r [T, H, D];
-    `active` (sorted int32 logical rows) makes it a compact sparse residual."""
+    `active` (sorted int32 logical rows) makes it a compact sparse residual.
+    `kgroup` (K only): KVQ_KGROUP_COMPACT or KVQ_KGROUP_TILE; default: the base's."""
     _require_cuda(x_r, "x_r", torch.bfloat16)
     T, H, D = x_r.shape
     kind = prev[0].kind
     n = T if active is None else int(active.numel())
-    out = Stream(kind, n, T, H, D, x_r.device, active)
+    out = Stream(kind, n, T, H, D, x_r.device, active, kgroup=prev[0].kgroup if kgroup is None else kgroup)
     arr = (kvq_stream * len(prev))(*[p.desc for p in prev])
     _check(lib().kvq_encode_residual(_dptr(x_r), arr, len(prev), ctypes.byref(out.desc), _stream_handle(stream)),
            "kvq_encode_residual")
@@ -338,9 +355,11 @@ def kvq_decode_attn_packed(table: RequestTable, q: torch.Tensor, depth: int, n_h
     return out
 
 
-def plane_bytes(kind: int, n_rows: int, n_tokens: int, n_heads: int, head_dim: int) -> list:
+def plane_bytes(kind: int, n_rows: int, n_tokens: int, n_heads: int, head_dim: int,
+                kgroup: int = KVQ_KGROUP_COMPACT) -> list:
     d = kvq_stream()
     _check(lib().kvq_stream_init(ctypes.byref(d), kind, n_rows, n_tokens, n_heads, head_dim), "kvq_stream_init")
+    d.kgroup = kgroup
     return [int(lib().kvq_plane_bytes(ctypes.byref(d), p)) for p in range(5)]
 
 
@@ -350,12 +369,15 @@ class PackedPool:
     through the device request table (kvq_request per request).
 
     active_sets[b][r] is the sorted int32 active set of loop r of request b, or
-    None for a dense loop (loop 0 must be dense)."""
+    None for a dense loop (loop 0 must be dense). kgroup: the K grouping of
+    every K stream (KVQ_KGROUP_COMPACT or KVQ_KGROUP_TILE)."""
 
     ALIGN = 256
 
-    def __init__(self, lengths: list, active_sets: list, n_heads: int, head_dim: int, n_loops: int, device):
+    def __init__(self, lengths: list, active_sets: list, n_heads: int, head_dim: int, n_loops: int, device,
+                 kgroup: int = KVQ_KGROUP_COMPACT):
         device = torch.device(device)
+        self.kgroup = kgroup
         self.lengths = list(lengths)
         self.n_heads, self.head_dim, self.n_loops = n_heads, head_dim, n_loops
         # pass 1: sizes
@@ -366,7 +388,7 @@ class PackedPool:
             for r in range(n_loops):
                 act = active_sets[b][r]
                 n = T if act is None else int(act.numel())
-                k = plane_bytes(KVQ_K, n, T, n_heads, head_dim)
+                k = plane_bytes(KVQ_K, n, T, n_heads, head_dim, kgroup)
                 v = plane_bytes(KVQ_V, n, T, n_heads, head_dim)
                 per.append((n, k, v, act is not None))
                 total += sum(self._up(x) for x in k[:3]) + sum(self._up(x) for x in v[:3])
@@ -387,9 +409,10 @@ class PackedPool:
                     idx = self._take(kb[PLANE_INDEX])
                     idx.view(torch.int32)[:n].copy_(active_sets[b][r].to(device=device, dtype=torch.int32))
                     shared = (idx, self._take(kb[PLANE_TILE_DIR]))
-                ks.append(Stream(KVQ_K, n, T, n_heads, head_dim, device, alloc=self._take, shared_index=shared))
+                ks.append(Stream(KVQ_K, n, T, n_heads, head_dim, device, alloc=self._take, shared_index=shared,
+                                 kgroup=kgroup))
                 vs.append(Stream(KVQ_V, n, T, n_heads, head_dim, device, alloc=self._take, shared_index=shared))
-                self.payload_bytes += payload_bytes(KVQ_K, n, n_heads, head_dim, sparse)
+                self.payload_bytes += payload_bytes(KVQ_K, n, n_heads, head_dim, sparse, T, kgroup)
                 self.payload_bytes += payload_bytes(KVQ_V, n, n_heads, head_dim, False)
             self.k_streams.append(ks)
             self.v_streams.append(vs)

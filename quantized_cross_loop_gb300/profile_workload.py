@@ -17,6 +17,8 @@ requests of configuration 2). Stages:
                `reps` times each;
   tail         packed decode attention with a 100-token BF16 tail per request,
                `reps` times.
+--kgroup tile builds the K chains with tile-local K groups (the stored rows of
+one 64-token logical tile per group) instead of 64 consecutive stored rows.
 Every stage first encodes the workload (the launches a capture should skip:
 2 + 4 (loops - 1) per kind, plus one per reconstruct or attention call before
 the one captured).
@@ -44,12 +46,14 @@ def main():
     ap.add_argument("--stage", choices=["encode", "reconstruct", "attention", "sparse", "tail"], default="attention")
     ap.add_argument("--algo", choices=["auto", "simt", "mma"], default="auto")
     ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--kgroup", choices=["compact", "tile"], default="compact")
     args = ap.parse_args()
     cfg, rep = parse_workload(args.workload)
     dev = torch.device("cuda")
     wl = W.make_workload(cfg, device=dev, replicate=rep)
     reqs = wl.requests
-    pool = kvq.PackedPool([r.T for r in reqs], [r.active for r in reqs], wl.H, wl.D, wl.depth, dev)
+    kgroup = kvq.KVQ_KGROUP_TILE if args.kgroup == "tile" else kvq.KVQ_KGROUP_COMPACT
+    pool = kvq.PackedPool([r.T for r in reqs], [r.active for r in reqs], wl.H, wl.D, wl.depth, dev, kgroup=kgroup)
     for j in range(wl.depth):
         kvq.kvq_encode_batch(pool, kvq.KVQ_K, j, kvq.pointer_array([r.xk[j] for r in reqs], dev))
         kvq.kvq_encode_batch(pool, kvq.KVQ_V, j, kvq.pointer_array([r.xv[j] for r in reqs], dev))

@@ -53,9 +53,9 @@ def test_struct_layouts_match_header():
 #include <stdio.h>
 #include <stddef.h>
 #include "kvq.h"
-int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_stream), offsetof(kvq_stream, codes),
+int main(void){printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_stream), offsetof(kvq_stream, codes),
   offsetof(kvq_stream, tile_dir), sizeof(kvq_loop_ref), sizeof(kvq_request), offsetof(kvq_request, n_sink),
-  offsetof(kvq_request, tail_v)); return 0;}
+  offsetof(kvq_request, tail_v), offsetof(kvq_stream, kgroup), offsetof(kvq_loop_ref, flags)); return 0;}
 '''
     import subprocess
     import tempfile
@@ -68,7 +68,7 @@ int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_stream), offse
         got = [int(v) for v in subprocess.run([exe], capture_output=True, text=True).stdout.split()]
     assert got == [ctypes.sizeof(kvq.kvq_stream), kvq.kvq_stream.codes.offset, kvq.kvq_stream.tile_dir.offset,
                    ctypes.sizeof(kvq.kvq_loop_ref), ctypes.sizeof(kvq.kvq_request), kvq.kvq_request.n_sink.offset,
-                   kvq.kvq_request.tail_v.offset]
+                   kvq.kvq_request.tail_v.offset, kvq.kvq_stream.kgroup.offset, kvq.kvq_loop_ref.flags.offset]
 
 
 def test_plane_sizes_and_payload(L):
@@ -86,6 +86,13 @@ def test_plane_sizes_and_payload(L):
                 # byte-exact storage agrees with the oracle's own accounting
                 assert L.kvq_stream_payload_bytes(kind, n, 8, 128, sparse) == O.stream_bytes(kind, n, 8, 128,
                                                                                                sparse=bool(sparse))
+                # and under tile grouping of K (ceil(T/64) groups of a sparse stream)
+                assert L.kvq_stream_payload_bytes_ex(kind, n, T, 8, 128, sparse, kvq.KVQ_KGROUP_TILE) == \
+                    O.stream_bytes(kind, n, 8, 128, sparse=bool(sparse), T=T, kgroup=O.KGROUP_TILE)
+            s.kgroup = kvq.KVQ_KGROUP_TILE
+            groups = (-(-T // 64) if n > 0 else 0) if kind == kvq.KVQ_K else None
+            if groups is not None:
+                assert L.kvq_plane_bytes(ctypes.byref(s), 1) == -(-(2 * 8 * groups * 128) // 16) * 16
 
 
 def _stream(L, kind=0, n=64, T=64, H=8, D=128):
