@@ -48,6 +48,10 @@
  *     packed reader's values; the BF16 reconstruction is a separate output;
  *   - plane layout (head-major): codes u8[H][n][D/2]; K params f16[H][⌈n/G⌉][D];
  *     V params f16[H][n][⌈D/G⌉]; sparse index int32[n] ascending;
+ *   - NVFP4 residual (orc_encode_nvfp4): two-level scaling in the order given
+ *     there (tensor amax/2688, E4M3 block scale of amax_b/(6·s_t), E2M1 codes
+ *     of δ/(s_b·s_t)); blocks of 16 channels of one (row, head) for K and V;
+ *     the base stays INT4;
  *   - tile-local K grouping (ORC_KGROUP_TILE): a K group of a sparse loop holds
  *     the stored rows whose logical positions lie in one logical tile
  *     [G·k, G·k + G); its params sit in slot k of f16[H][⌈T/G⌉][D]; a tile with
@@ -65,6 +69,9 @@
 
 #define ORC_KGROUP_COMPACT 0 /* K groups: G consecutive stored rows */
 #define ORC_KGROUP_TILE 1    /* K groups: the stored rows of one logical tile of G tokens */
+
+#define ORC_FMT_INT4 0  /* affine INT4 groups of G (FP16 min and scale) */
+#define ORC_FMT_NVFP4 1 /* E2M1 + E4M3 per 16 channels + FP32 per stream */
 
 #define ORC_OK 0
 #define ORC_EINVAL (-1)
@@ -165,6 +172,74 @@ static float round_half_even(float v) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* FP8 E4M3 and FP4 E2M1 (the NVFP4 element and block-scale types; codec PR  */
+/* review by 0z5a: "E2M1 round-to-nearest-even, E4M3 scale rounding").       */
+/* ------------------------------------------------------------------------ */
+
+/* E4M3, finite variant: 1 sign, 4 exponent (bias 7), 3 mantissa bits; no
+ * infinities; largest finite 448 = 1.75·2^8; subnormals m·2^-9. Round to
+ * nearest, ties to even; anything above 448 saturates to 448. */
+uint8_t orc_f32_to_e4m3(float f) {
+  uint8_t sign = (f32_bits(f) >> 31) ? 0x80 : 0x00;
+  float v = fabsf(f);
+  if (v != v) return 0x7F; /* NaN */
+  if (v >= 448.0f) return (uint8_t)(sign | (15 << 3) | 6);
+  if (v < 0.015625f) { /* below 2^-6: subnormal, in units of 2^-9 */
+    float m = round_half_even(v * 512.0f);
+    if (m >= 8.0f) return (uint8_t)(sign | (1 << 3)); /* rounds up to 2^-6 */
+    return (uint8_t)(sign | (int)m);
+  }
+  int ex;
+  float fr = frexpf(v, &ex); /* v = fr·2^ex, fr in [0.5, 1) */
+  int E = ex - 1;            /* v = (2 fr)·2^E, 2 fr in [1, 2) */
+  float M = round_half_even((2.0f * fr - 1.0f) * 8.0f);
+  if (M >= 8.0f) {
+    M = 0.0f;
+    E += 1;
+  }
+  if (E > 8 || (E == 8 && M > 6.0f)) return (uint8_t)(sign | (15 << 3) | 6);
+  return (uint8_t)(sign | ((E + 7) << 3) | (int)M);
+}
+
+float orc_e4m3_to_f32(uint8_t b) {
+  int E = (b >> 3) & 15, M = b & 7;
+  float v = (E == 0) ? ldexpf((float)M, -9) : ldexpf(1.0f + (float)M / 8.0f, E - 7);
+  return (b & 0x80) ? -v : v;
+}
+
+/* E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa bit; the eight magnitudes
+ * below, code = index. The nearest magnitude wins; a tie goes to the even
+ * code (even mantissa); anything above 6 saturates to 6. The sign is kept,
+ * zero included. */
+static const float kE2M1[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+
+uint8_t orc_f32_to_e2m1(float f) {
+  uint8_t sign = (f32_bits(f) >> 31) ? 0x8 : 0x0;
+  float v = fabsf(f);
+  int best = 7;
+  if (v <= 6.0f) {
+    best = 0;
+    for (int k = 1; k < 8; ++k) {
+      float dk = fabsf(v - kE2M1[k]), db = fabsf(v - kE2M1[best]);
+      if (dk < db || (dk == db && (k % 2) == 0)) best = k;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+float orc_e2m1_to_f32(uint8_t n) {
+  float v = kE2M1[n & 7];
+  return (n & 8) ? -v : v;
+}
+
+void orc_f32_to_e4m3_n(const float* x, uint8_t* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = orc_f32_to_e4m3(x[i]);
+}
+void orc_f32_to_e2m1_n(const float* x, uint8_t* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = orc_f32_to_e2m1(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Affine INT4 group quantiser (RFC §3.3; FP32 codes before FP16 rounding,    */
 /* PR review by 0z5a).                                                        */
 /* ------------------------------------------------------------------------ */
@@ -235,6 +310,11 @@ int64_t orc_stream_bytes_ex(int kind, int n, int T, int H, int D, int G, int kgr
 }
 int64_t orc_stream_bytes(int kind, int n, int H, int D, int G, int sparse) {
   return orc_stream_bytes_ex(kind, n, n, H, D, G, ORC_KGROUP_COMPACT, sparse);
+}
+/* NVFP4 stream: E2M1 codes, one E4M3 byte per 16 channels, the FP32 tensor scale. */
+int64_t orc_stream_bytes_nvfp4(int n, int H, int D, int sparse) {
+  if (n <= 0) return 0;
+  return orc_codes_bytes(n, H, D) + (int64_t)H * n * (D / 16) + 4 + (sparse ? 4 * (int64_t)n : 0);
 }
 
 static int64_t code_byte_index(int n, int D, int h, int row, int d) {
@@ -395,6 +475,85 @@ int orc_encode(int kind, int T, int H, int D, int G, const uint16_t* x, const ui
 }
 
 /* ------------------------------------------------------------------------ */
+/* NVFP4 residual (codec PR review by 0z5a: E2M1 elements, one E4M3 scale per */
+/* 16 elements, one FP32 scale per tensor; symmetric, no zero point; blocks   */
+/* along channels for K and V alike, so K metadata is page-local).           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Encode the residual of loop r as NVFP4 (a residual only: the base stays INT4).
+ * Same residual rows as orc_encode: δ = RN_bf16(RN32(X_r − X̂_{r−1})) at the
+ * stored rows. Two-level scaling, in this order:
+ *   a_t  = max |δ| over the whole stream (all stored rows, heads, channels);
+ *   s_t  = RN32(a_t / 2688)                     FP32 tensor scale (2688 = 6·448)
+ *   per block of 16 channels of one (row, head), a_b = max |δ| in the block:
+ *   s_b  = E4M3(RN32(a_b / RN32(6·s_t)))        block scale (a_t's block: 448)
+ *   e_b  = RN32(f32(s_b)·s_t)                   the block's quantisation step
+ *   code = E2M1(RN32(δ / e_b)) (IEEE division; e_b = 0: code +0)
+ * a_t = 0 gives s_t = 0 and every scale and code 0.
+ * Decode: RN32(RN32(e2m1·s_b)·s_t) (e2m1·s_b is exact); the BF16 chain rounds it
+ * to BF16 before the add, as for INT4.
+ * Planes: codes u8[H][n][D/2] (nibble = code, even channel low);
+ * bscale u8[H][n][D/16] (E4M3 bits); *tscale = s_t.
+ */
+int orc_encode_nvfp4(int kind, int T, int H, int D, const uint16_t* x, const uint16_t* pred, const int32_t* active,
+                     int n, uint8_t* codes, uint8_t* bscale, float* tscale) {
+  if (T < 0 || H <= 0 || D <= 0 || (D % 16) != 0 || pred == NULL) return ORC_EINVAL;
+  if (kind != ORC_KIND_K && kind != ORC_KIND_V) return ORC_EINVAL;
+  if (active == NULL) {
+    if (n != T) return ORC_EINVAL;
+  } else if (n < 0 || n > T || !check_active(active, n, T)) {
+    return ORC_EINVAL;
+  }
+  *tscale = 0.0f;
+  if (n == 0) return ORC_OK;
+  float* v = (float*)malloc(sizeof(float) * (size_t)n * H * D);
+  if (!v) return ORC_ENOMEM;
+  float amax = 0.0f;
+  for (int row = 0; row < n; ++row) {
+    int t = active ? active[row] : row;
+    for (int h = 0; h < H; ++h)
+      for (int d = 0; d < D; ++d) {
+        int64_t li = ((int64_t)t * H + h) * D + d;
+        float diff = orc_bf16_to_f32(x[li]) - orc_bf16_to_f32(pred[li]); /* RN32 */
+        float val = orc_bf16_to_f32(orc_f32_to_bf16(diff));
+        v[((int64_t)row * H + h) * D + d] = val;
+        if (fabsf(val) > amax) amax = fabsf(val);
+      }
+  }
+  float st = amax / 2688.0f; /* RN32 */
+  *tscale = st;
+  float six_st = 6.0f * st;  /* RN32 */
+  for (int row = 0; row < n; ++row)
+    for (int h = 0; h < H; ++h) {
+      const float* r = v + ((int64_t)row * H + h) * D;
+      uint8_t* crow = codes + ((int64_t)h * n + row) * (D / 2);
+      for (int b = 0; b < D / 16; ++b) {
+        float ab = 0.0f;
+        for (int i = 0; i < 16; ++i)
+          if (fabsf(r[16 * b + i]) > ab) ab = fabsf(r[16 * b + i]);
+        uint8_t sb = (amax == 0.0f) ? 0 : orc_f32_to_e4m3(ab / six_st);
+        bscale[((int64_t)h * n + row) * (D / 16) + b] = sb;
+        float eb = orc_e4m3_to_f32(sb) * st; /* RN32 */
+        for (int i = 0; i < 16; i += 2) {
+          uint8_t c[2];
+          for (int k = 0; k < 2; ++k)
+            c[k] = (eb == 0.0f) ? 0 : orc_f32_to_e2m1(r[16 * b + i + k] / eb); /* IEEE division, RN32 */
+          crow[(16 * b + i) / 2] = (uint8_t)(c[0] | (c[1] << 4));
+        }
+      }
+    }
+  free(v);
+  return ORC_OK;
+}
+
+/* Decode one NVFP4 element in FP32: RN32(RN32(e2m1 · s_b) · s_t). */
+static float nvfp4_dequant(uint8_t code, uint8_t sb, float st) {
+  float p = orc_e2m1_to_f32(code) * orc_e4m3_to_f32(sb); /* exact */
+  return p * st;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Reconstruct the chain to a requested depth (RFC §3.3).                     */
 /* ------------------------------------------------------------------------ */
 
@@ -403,8 +562,12 @@ typedef struct {
   int32_t kgroup;         /* ORC_KGROUP_COMPACT or ORC_KGROUP_TILE */
   const int32_t* active;  /* NULL: dense (n == T) */
   const uint8_t* codes;
-  const uint16_t* mins;
-  const uint16_t* scales;
+  const uint16_t* mins;   /* INT4 */
+  const uint16_t* scales; /* INT4 */
+  int32_t fmt;            /* ORC_FMT_INT4 or ORC_FMT_NVFP4 (residual loops only) */
+  int32_t _pad;
+  const uint8_t* bscale;  /* NVFP4: E4M3 [H][n][D/16] */
+  const float* tscale;    /* NVFP4: the FP32 tensor scale */
 } orc_stream;
 
 /* Index of the params of (head h, stored row, channel d) of stream s. */
@@ -416,6 +579,20 @@ static int64_t stream_param_index(int kind, const orc_stream* s, int T, int D, i
   return k_param_index(ng, D, h, kg, d);
 }
 
+/* Decoded value (FP32, before any BF16 rounding) of (head h, stored row, channel d)
+ * of stream s: INT4 RN32(min16 + RN32(scale16·c)), or the NVFP4 decode. */
+static float stream_dequant32(int kind, const orc_stream* s, int T, int D, int G, int h, int row, int d) {
+  int c = get_code(s->codes, s->n, D, h, row, d);
+  if (s->fmt == ORC_FMT_NVFP4)
+    return nvfp4_dequant((uint8_t)c, s->bscale[((int64_t)h * s->n + row) * (D / 16) + d / 16], s->tscale[0]);
+  int64_t pi = stream_param_index(kind, s, T, D, G, h, row, d);
+  float m = orc_f16_to_f32(s->mins[pi]);
+  float sc = orc_f16_to_f32(s->scales[pi]);
+  float prod = sc * (float)c;
+  return m + prod;
+}
+
+
 /*
  * loops[0] is the base, loops[j-1] the residual of loop j. out: BF16 bits
  * [T][H][D] in logical order. A token absent from loop j keeps its value
@@ -423,7 +600,7 @@ static int64_t stream_param_index(int kind, const orc_stream* s, int T, int D, i
  */
 int orc_reconstruct(int kind, int T, int H, int D, int G, int depth, const orc_stream* loops, uint16_t* out) {
   if (T < 0 || H <= 0 || D <= 0 || (D & 1) || G <= 0 || depth < 1) return ORC_EINVAL;
-  if (loops[0].active != NULL || loops[0].n != T) return ORC_EINVAL;
+  if (loops[0].active != NULL || loops[0].n != T || loops[0].fmt != ORC_FMT_INT4) return ORC_EINVAL;
   for (int j = 1; j < depth; ++j) {
     if (loops[j].active == NULL) {
       if (loops[j].n != T) return ORC_EINVAL;
@@ -454,8 +631,8 @@ int orc_reconstruct(int kind, int T, int H, int D, int G, int depth, const orc_s
       if (row < 0) continue; /* absent: inherit */
       for (int h = 0; h < H; ++h)
         for (int d = 0; d < D; ++d) {
-          int64_t pi = stream_param_index(kind, s, T, D, G, h, row, d);
-          float dq = dequant(s->mins[pi], s->scales[pi], get_code(s->codes, s->n, D, h, row, d));
+          /* the decoded residual in the BF16 compute dtype (INT4: RN_bf16(min16 + scale16·c)) */
+          float dq = orc_bf16_to_f32(orc_f32_to_bf16(stream_dequant32(kind, s, T, D, G, h, row, d)));
           int64_t li = ((int64_t)t * H + h) * D + d;
           float sum = orc_bf16_to_f32(out[li]) + dq; /* RN32 */
           out[li] = orc_f32_to_bf16(sum);
@@ -481,7 +658,7 @@ int orc_reconstruct(int kind, int T, int H, int D, int G, int depth, const orc_s
  */
 int orc_decode_f32(int kind, int T, int H, int D, int G, int depth, const orc_stream* loops, float* out) {
   if (T < 0 || H <= 0 || D <= 0 || (D & 1) || G <= 0 || depth < 1) return ORC_EINVAL;
-  if (loops[0].active != NULL || loops[0].n != T) return ORC_EINVAL;
+  if (loops[0].active != NULL || loops[0].n != T || loops[0].fmt != ORC_FMT_INT4) return ORC_EINVAL;
   for (int j = 1; j < depth; ++j) {
     if (loops[j].active == NULL) {
       if (loops[j].n != T) return ORC_EINVAL;
@@ -500,11 +677,7 @@ int orc_decode_f32(int kind, int T, int H, int D, int G, int depth, const orc_st
       if (row < 0) continue;
       for (int h = 0; h < H; ++h)
         for (int d = 0; d < D; ++d) {
-          int64_t pi = stream_param_index(kind, s, T, D, G, h, row, d);
-          float m = orc_f16_to_f32(s->mins[pi]);
-          float sc = orc_f16_to_f32(s->scales[pi]);
-          float prod = sc * (float)get_code(s->codes, s->n, D, h, row, d);
-          float dq = m + prod;
+          float dq = stream_dequant32(kind, s, T, D, G, h, row, d);
           int64_t li = ((int64_t)t * H + h) * D + d;
           out[li] = (j == 0) ? dq : out[li] + dq;
         }

@@ -33,6 +33,8 @@ KIND_V = 1
 GROUP = 64
 KGROUP_COMPACT = 0  # K groups: 64 consecutive stored rows (the codec PR's grouping)
 KGROUP_TILE = 1     # K groups: the stored rows of one 64-token logical tile (page-local metadata)
+FMT_INT4 = 0        # affine INT4 groups of 64, FP16 min and scale
+FMT_NVFP4 = 1       # E2M1 elements, E4M3 scale per 16 channels, FP32 scale per stream (residuals only)
 
 
 def build(force: bool = False) -> str:
@@ -56,6 +58,10 @@ class _Stream(ctypes.Structure):
         ("codes", ctypes.c_void_p),
         ("mins", ctypes.c_void_p),
         ("scales", ctypes.c_void_p),
+        ("fmt", ctypes.c_int32),
+        ("_pad", ctypes.c_int32),
+        ("bscale", ctypes.c_void_p),
+        ("tscale", ctypes.c_void_p),
     ]
 
 
@@ -82,6 +88,17 @@ def lib():
             L.orc_stream_bytes.restype = i64
             L.orc_stream_bytes_ex.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
             L.orc_stream_bytes_ex.restype = i64
+            L.orc_stream_bytes_nvfp4.argtypes = [i32, i32, i32, i32]
+            L.orc_stream_bytes_nvfp4.restype = i64
+            L.orc_encode_nvfp4.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp, vp, vp]
+            L.orc_encode_nvfp4.restype = i32
+            for name in ("orc_f32_to_e4m3_n", "orc_f32_to_e2m1_n"):
+                getattr(L, name).argtypes = [vp, vp, i64]
+                getattr(L, name).restype = None
+            L.orc_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+            L.orc_e4m3_to_f32.restype = ctypes.c_float
+            L.orc_e2m1_to_f32.argtypes = [ctypes.c_uint8]
+            L.orc_e2m1_to_f32.restype = ctypes.c_float
             for name in ("orc_f32_to_f16_n", "orc_f32_to_bf16_n", "orc_f16_to_f32_n"):
                 getattr(L, name).argtypes = [vp, vp, i64]
                 getattr(L, name).restype = None
@@ -117,6 +134,32 @@ def f16_bits_to_f32(x) -> np.ndarray:
     return y
 
 
+def f32_to_e4m3_bits(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint8)
+    lib().orc_f32_to_e4m3_n(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def f32_to_e2m1_bits(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint8)
+    lib().orc_f32_to_e2m1_n(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def e4m3_bits_to_f32(b) -> np.ndarray:
+    b = np.asarray(b, dtype=np.uint8)
+    table = np.array([lib().orc_e4m3_to_f32(i) for i in range(256)], dtype=np.float32)
+    return table[b]
+
+
+def e2m1_bits_to_f32(b) -> np.ndarray:
+    b = np.asarray(b, dtype=np.uint8)
+    table = np.array([lib().orc_e2m1_to_f32(i) for i in range(16)], dtype=np.float32)
+    return table[b & 15]
+
+
 def bf16_bits_to_f32(x) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.uint16)
     return (x.astype(np.uint32) << 16).view(np.float32)
@@ -139,11 +182,17 @@ class Stream:
     mins: np.ndarray  # uint16 (f16 bits): K [H, groups, D] (see param_shape); V [H, n, ceil(D/G)]
     scales: np.ndarray
     kgroup: int = KGROUP_COMPACT
+    fmt: int = FMT_INT4
+    bscale: np.ndarray | None = None  # NVFP4: uint8 E4M3 bits [H, n, D/16]
+    tscale: np.ndarray | None = None  # NVFP4: float32 [1], the tensor scale
 
     def c_struct(self) -> _Stream:
         s = _Stream()
         s.n = self.n
         s.kgroup = self.kgroup
+        s.fmt = self.fmt
+        s.bscale = None if self.bscale is None else self.bscale.ctypes.data
+        s.tscale = None if self.tscale is None else self.tscale.ctypes.data
         s.active = None if self.active is None else self.active.ctypes.data
         s.codes = self.codes.ctypes.data
         s.mins = self.mins.ctypes.data
@@ -187,6 +236,35 @@ def encode(kind: int, x: np.ndarray, pred: np.ndarray | None = None, active: np.
     return Stream(kind, T, H, D, n, active, codes, mins, scales, kgroup)
 
 
+def encode_nvfp4(kind: int, x: np.ndarray, pred: np.ndarray, active: np.ndarray | None = None) -> Stream:
+    """Encode a residual stream as NVFP4 (see orc_encode_nvfp4). x, pred: uint16
+    BF16 bits [T, H, D] (logical order); pred is the reconstruction X̂_{r-1}."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    pred = np.ascontiguousarray(pred, dtype=np.uint16)
+    T, H, D = x.shape
+    assert pred.shape == x.shape
+    if active is not None:
+        active = np.ascontiguousarray(active, dtype=np.int32)
+        n = int(active.size)
+    else:
+        n = T
+    codes = np.zeros((H, n, D // 2), dtype=np.uint8)
+    bscale = np.zeros((H, n, D // 16), dtype=np.uint8)
+    tscale = np.zeros(1, dtype=np.float32)
+    rc = lib().orc_encode_nvfp4(kind, T, H, D, _ptr(x), _ptr(pred), _ptr(active), n, _ptr(codes), _ptr(bscale),
+                                _ptr(tscale))
+    if rc != 0:
+        raise ValueError(f"orc_encode_nvfp4 failed with status {rc}")
+    empty = np.zeros(0, dtype=np.uint16)
+    return Stream(kind, T, H, D, n, active, codes, empty, empty, KGROUP_COMPACT, FMT_NVFP4, bscale, tscale)
+
+
+def stream_bytes_nvfp4(n: int, H: int, D: int, sparse: bool = False) -> int:
+    """Byte-exact payload of an NVFP4 stream: codes, E4M3 block scales, the FP32
+    tensor scale (and the sparse index)."""
+    return int(lib().orc_stream_bytes_nvfp4(n, H, D, int(sparse)))
+
+
 def reconstruct(streams: list[Stream], depth: int, G: int = GROUP) -> np.ndarray:
     """BF16 bits [T, H, D] of the chain summed to `depth` (1 = base only)."""
     s0 = streams[0]
@@ -199,12 +277,16 @@ def reconstruct(streams: list[Stream], depth: int, G: int = GROUP) -> np.ndarray
 
 
 def encode_chain(kind: int, xs: list[np.ndarray], actives: list[np.ndarray | None], G: int = GROUP,
-                 kgroup: int = KGROUP_COMPACT) -> list[Stream]:
-    """Loop 1 encodes X1; loop r encodes X_r minus reconstruct(r-1) at its rows."""
+                 kgroup: int = KGROUP_COMPACT, formats: list[int] | None = None) -> list[Stream]:
+    """Loop 1 encodes X1 (INT4); loop r encodes X_r minus reconstruct(r-1) at its
+    rows, in formats[r] (FMT_INT4 default, or FMT_NVFP4)."""
     streams = [encode(kind, xs[0], None, None, G, kgroup)]
     for r in range(1, len(xs)):
         pred = reconstruct(streams, r, G)
-        streams.append(encode(kind, xs[r], pred, actives[r], G, kgroup))
+        if formats is not None and formats[r] == FMT_NVFP4:
+            streams.append(encode_nvfp4(kind, xs[r], pred, actives[r]))
+        else:
+            streams.append(encode(kind, xs[r], pred, actives[r], G, kgroup))
     return streams
 
 

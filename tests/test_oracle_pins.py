@@ -727,3 +727,149 @@ def test_sparse_selection_is_top_k_with_position_ties():
             assert S[hq].tolist() == sorted(brute)
             p = np.exp(s - s.max())
             assert abs(m[hq] - p[sorted(brute)].sum() / p.sum()) < 1e-12
+
+
+# ---------------------------------------------------------------- NVFP4 residual (codec PR review by 0z5a)
+
+
+def test_e4m3_matches_torch_float8_cast():
+    """E4M3 rounding (round to nearest even) agrees with torch's float8_e4m3fn cast
+    (a library routine) below its overflow point; above 448 the oracle saturates."""
+    rng = np.random.default_rng(5)
+    x = np.concatenate([
+        rng.uniform(0, 464, 200_000), np.exp(rng.uniform(np.log(1e-6), np.log(464), 200_000)),
+        np.arange(0, 4096) / 4096 * 2 ** -6,                # subnormal range and its ties
+        (np.arange(1, 2048) / 8.0 + 0.0625) * 2.0 ** rng.integers(-6, 8, 2047),  # mantissa ties
+    ]).astype(np.float32)
+    x = x[x < 464]
+    for sign in (1, -1):
+        got = O.f32_to_e4m3_bits(sign * x)
+        ref = torch.from_numpy(sign * x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(got, ref)
+    assert np.all(O.f32_to_e4m3_bits(np.array([464.0, 500.0, 1e30], np.float32)) == 0x7E)
+    # decoding every finite pattern agrees with torch's float8 view
+    bits = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], dtype=np.uint8)
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    assert np.array_equal(O.e4m3_bits_to_f32(bits), ref)
+
+
+def test_e2m1_is_nearest_with_ties_to_even():
+    """E2M1 codes: the nearest of the eight magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6
+    (exact rational distances), ties to the even code, above 6 saturating; the
+    sign bit follows the input's sign."""
+    mags = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3), Fraction(4),
+            Fraction(6)]
+    assert list(O.e2m1_bits_to_f32(np.arange(8))) == [float(m) for m in mags]
+    assert list(O.e2m1_bits_to_f32(np.arange(8, 16))) == [-float(m) for m in mags]
+    vals = np.concatenate([np.arange(0, 8.5, 1 / 64), np.random.default_rng(6).uniform(0, 7, 5000)]).astype(np.float32)
+    for sign in (1.0, -1.0):
+        codes = O.f32_to_e2m1_bits(sign * vals)
+        for v, c in zip(vals, codes):
+            fv = Fraction(float(v))
+            if fv > 6:
+                assert c & 7 == 7
+            else:
+                d = [abs(fv - m) for m in mags]
+                best = min(d)
+                cands = [k for k in range(8) if d[k] == best]
+                want = cands[0] if len(cands) == 1 else [k for k in cands if k % 2 == 0][0]
+                assert c & 7 == want, (float(v), c)
+            assert (c >> 3) == (1 if sign < 0 else 0)
+
+
+def _nvfp4_case(T, H, D, seed, sparse):
+    xs = _offset_chain(T, H, D, seed)
+    act = None
+    if sparse:
+        act = np.sort(np.random.default_rng(seed).choice(T, T // 2, replace=False)).astype(np.int32)
+    base = O.encode(O.KIND_K, xs[0])
+    pred = O.reconstruct([base], 1)
+    s = O.encode_nvfp4(O.KIND_K, xs[1], pred, act)
+    rows = act if act is not None else np.arange(T)
+    delta = f32(bf16(f32(xs[1])[rows] - f32(pred)[rows]))  # [n, H, D] compact order
+    return s, delta
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+def test_nvfp4_scales_follow_the_two_level_recipe(sparse):
+    """Codec PR review by 0z5a (NVFP4: E2M1 elements, one E4M3 scale per 16
+    elements, one FP32 scale per tensor): s_t = amax/(6·448) in FP32; each
+    block of 16 channels of one (row, head) stores E4M3(a_b / (6 s_t)) (torch's
+    float8 cast), and the block holding the tensor's largest |δ| gets 448."""
+    T, H, D = 130, 4, 128
+    s, delta = _nvfp4_case(T, H, D, 31, sparse)
+    amax = np.float32(np.abs(delta).max())
+    st = np.float32(amax / np.float32(2688))
+    assert s.tscale[0] == st
+    blk = np.abs(delta).reshape(delta.shape[0], H, D // 16, 16).max(axis=3)  # [n, H, D/16]
+    want = torch.from_numpy((blk / np.float32(np.float32(6) * st)).astype(np.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(np.transpose(s.bscale, (1, 0, 2)), want)
+    where = np.unravel_index(np.argmax(np.abs(delta)), delta.shape)
+    assert O.e4m3_bits_to_f32(s.bscale[where[1], where[0], where[2] // 16]) == 448.0
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+def test_nvfp4_codes_are_nearest_levels(sparse):
+    """Each code is the E2M1 value nearest to δ / (s_b · s_t) with the sign of δ;
+    the decode error is at most one quantisation step e_b = s_b · s_t."""
+    T, H, D = 70, 2, 128
+    s, delta = _nvfp4_case(T, H, D, 32, sparse)
+    n = delta.shape[0]
+    codes = unpack(s.codes)  # [n, H, D]
+    sb = O.e4m3_bits_to_f32(np.transpose(s.bscale, (1, 0, 2)))  # [n, H, D/16]
+    eb = (np.repeat(sb, 16, axis=2) * s.tscale[0]).astype(np.float32)
+    vals = O.e2m1_bits_to_f32(codes)
+    y = (delta / eb).astype(np.float32)  # IEEE FP32 division, like the quantiser
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    dist = np.abs(np.abs(y)[..., None] - mags)
+    best = dist.min(axis=-1)
+    assert np.all(np.abs(np.abs(y) - np.abs(vals)) == best)  # a nearest magnitude (ties checked below)
+    neg = np.signbit(y)
+    assert np.array_equal(codes >= 8, neg)
+    tie = (dist == best[..., None]).sum(axis=-1) > 1
+    assert np.all((codes[tie] & 7) % 2 == 0)
+    dq = (vals * np.repeat(sb, 16, axis=2)).astype(np.float32) * s.tscale[0]
+    assert np.all(np.abs(delta - dq) <= eb * 1.0001)
+    assert n == (T // 2 if sparse else T)
+
+
+def test_nvfp4_zero_stream_and_chain_decode():
+    """A residual that vanishes stores s_t = 0 and zero codes; the chain decodes
+    an NVFP4 loop as e2m1 · s_b · s_t at its stored rows (absent rows inherit),
+    and the BF16 reconstruction rounds that step to BF16 before the add."""
+    T, H, D = 100, 2, 128
+    xs = _offset_chain(T, H, D, 33)
+    base = O.encode(O.KIND_V, xs[0])
+    pred = O.reconstruct([base], 1)
+    z = O.encode_nvfp4(O.KIND_V, pred, pred)  # X_2 = X̂_1: δ = 0 everywhere
+    assert z.tscale[0] == 0 and not z.codes.any() and not z.bscale.any()
+    assert np.array_equal(O.reconstruct([base, z], 2), pred)
+    act = np.sort(np.random.default_rng(3).choice(T, 37, replace=False)).astype(np.int32)
+    ch = O.encode_chain(O.KIND_K, xs, [None, None, act, act[::3].copy()],
+                        formats=[O.FMT_INT4, O.FMT_NVFP4, O.FMT_NVFP4, O.FMT_NVFP4])
+    f2, f3 = O.decode_f32(ch, 2), O.decode_f32(ch, 3)
+    s = ch[2]
+    codes = unpack(s.codes)
+    sb = O.e4m3_bits_to_f32(np.transpose(s.bscale, (1, 0, 2)))
+    step = (O.e2m1_bits_to_f32(codes) * np.repeat(sb, 16, axis=2)).astype(np.float32) * s.tscale[0]
+    assert np.array_equal(f3[act], (f2[act] + step).astype(np.float32))
+    absent = np.setdiff1d(np.arange(T), act)
+    assert np.array_equal(f3[absent], f2[absent])
+    r2, r3 = f32(O.reconstruct(ch, 2)), f32(O.reconstruct(ch, 3))
+    assert np.array_equal(r3[act], f32(bf16(r2[act] + f32(bf16(step)))))
+    assert np.max(np.abs(f32(O.reconstruct(ch, 4)) - O.decode_f32(ch, 4))) < 0.05
+
+
+def test_nvfp4_storage():
+    """4 bits of code and one E4M3 byte per 16 elements: 4.5 bits per element,
+    plus the 4-byte tensor scale (codec PR review by 0z5a: NVFP4 ties INT4's
+    4.5 bits)."""
+    H, D = 8, 128
+    for n in (64, 1000, 4096):
+        bits = O.stream_bytes_nvfp4(n, H, D) * 8 / (n * H * D)
+        assert abs(bits - (4.5 + 32 / (n * H * D))) < 1e-12
+        assert O.stream_bytes_nvfp4(n, H, D, sparse=True) == O.stream_bytes_nvfp4(n, H, D) + 4 * n
+    assert O.stream_bytes_nvfp4(0, H, D) == 0
+    s, _ = _nvfp4_case(130, H, D, 34, False)
+    assert s.codes.nbytes + s.bscale.nbytes + s.tscale.nbytes == O.stream_bytes_nvfp4(130, H, D)
