@@ -46,6 +46,22 @@
  * decode(delta)) where a token is stored, and X̂_{r-1} (inherited) where it is
  * absent (RFC §3.3: an absent residual is not an INT4 code 0).
  *
+ * NVFP4 residual format (codec PR review by 0z5a: "INT4 base plus NVFP4
+ * residuals is a legitimate option"; E2M1 elements, one E4M3 scale per 16
+ * elements, one FP32 scale per tensor). A residual stream (never the base) may
+ * use format KVQ_FMT_NVFP4 (group 16) instead of KVQ_FMT_INT4 (group 64):
+ *   codes   uint8 [H][n_rows][D/2]    byte = e2m1(2k) | e2m1(2k+1) << 4 (sign bit 3)
+ *   mins    read as uint8 [H][n_rows][D/16]   E4M3 scale of each 16-channel block
+ *                                             of one (stored row, head), K and V alike
+ *   scales  read as float [4]         [0] the FP32 tensor scale s_t, [1] scratch of
+ *                                     the encoder (the stream's max |delta|)
+ * Encode of loop r, delta as above: s_t = RN32(max|delta| / 2688); block scale
+ * s_b = E4M3(RN32(a_b / RN32(6 s_t))) (a_b = max |delta| of the block; E4M3
+ * round to nearest even, saturating at 448); code = E2M1(RN32(delta /
+ * RN32(s_b s_t))) (nearest of 0, .5, 1, 1.5, 2, 3, 4, 6, ties to even,
+ * saturating at 6, sign kept; a zero step gives code 0). Decode:
+ * RN32(RN32(e2m1 s_b) s_t), rounded to BF16 before the chain add like INT4.
+ *
  * K grouping (codec PR review by 0z5a, group ownership vs pages): the codec
  * PR groups a sparse K residual over consecutive compact rows, so one group can
  * mix distant positions. KVQ_KGROUP_TILE keeps every K group inside one
@@ -75,6 +91,8 @@ extern "C" {
 #define KVQ_NIBBLE_LO_FIRST 0
 #define KVQ_KGROUP_COMPACT 0 /* K groups: 64 consecutive stored rows (default) */
 #define KVQ_KGROUP_TILE 1    /* K groups: the stored rows of one 64-token logical tile */
+#define KVQ_FMT_INT4 0       /* affine INT4 groups of 64 with FP16 min and scale */
+#define KVQ_FMT_NVFP4 1      /* E2M1 + E4M3 per 16 channels + FP32 per stream (residual loops) */
 
 typedef int32_t kvq_status;
 #define KVQ_OK 0
@@ -100,7 +118,8 @@ typedef struct kvq_stream {
   uint16_t group;            /* 64 */
   uint8_t nibble_order;      /* KVQ_NIBBLE_LO_FIRST */
   uint8_t kgroup;            /* KVQ_KGROUP_COMPACT or KVQ_KGROUP_TILE (K streams; V ignores it) */
-  uint8_t reserved[2];
+  uint8_t format;            /* KVQ_FMT_INT4 (group 64) or KVQ_FMT_NVFP4 (group 16) */
+  uint8_t reserved;
   int32_t n_rows;            /* stored rows: n_tokens if dense, |active set| if sparse */
   int32_t n_tokens;          /* logical tokens T of the request */
   int32_t n_heads;           /* KV heads H */
@@ -115,6 +134,10 @@ typedef struct kvq_stream {
 /* Fill the format fields of `s` and clear its pointers. */
 kvq_status kvq_stream_init(kvq_stream* s, int kind, int n_rows, int n_tokens, int n_heads, int head_dim);
 
+/* Set the element format of `s` (KVQ_FMT_INT4 or KVQ_FMT_NVFP4) and its group
+ * size (64 or 16). Call before kvq_plane_bytes. */
+kvq_status kvq_stream_set_format(kvq_stream* s, int format);
+
 /* Bytes to allocate for one plane of `s` (KVQ_PLANE_*), rounded up to 16. The
  * index plane is at least 16 bytes, so that an empty sparse set still has a
  * non-NULL active_idx (NULL marks a dense stream). */
@@ -125,10 +148,12 @@ size_t kvq_plane_bytes(const kvq_stream* s, int plane);
  * derived tile directory. 4.5 bits per element on full groups (codec PR review
  * by 0z5a); partial groups pay their padding (RFC §7.4). */
 int64_t kvq_stream_payload_bytes(int kind, int n_rows, int n_heads, int head_dim, int sparse);
-/* The same for any K grouping: a tile-grouped sparse K stream stores
- * ceil(n_tokens/64) groups per (head, channel) whatever n_rows is. */
+/* The same for any K grouping and format: a tile-grouped sparse K stream
+ * stores ceil(n_tokens/64) groups per (head, channel) whatever n_rows is; an
+ * NVFP4 stream stores its codes, one E4M3 byte per 16 channels of a stored row
+ * and head, and the 4-byte FP32 tensor scale (4.5 bits per element + 4 bytes). */
 int64_t kvq_stream_payload_bytes_ex(int kind, int n_rows, int n_tokens, int n_heads, int head_dim, int sparse,
-                                    int kgroup);
+                                    int kgroup, int format);
 
 /*
  * Encode the loop-1 base of K or V (RFC §3.3: X̂[1] = deq(q(X[1]))).
@@ -175,11 +200,13 @@ kvq_status kvq_reconstruct(const kvq_stream* loops, int depth, uint16_t* out, kv
  * memory (an array of kvq_request, one per request). The batched encode
  * writes the planes (and, for a sparse loop, the tile_dir) of the loop it
  * encodes; every other call only reads through these pointers. */
-#define KVQ_LOOP_K_TILE 1 /* kvq_loop_ref.flags: the K planes use KVQ_KGROUP_TILE */
+#define KVQ_LOOP_K_TILE 1  /* kvq_loop_ref.flags: the K planes use KVQ_KGROUP_TILE */
+#define KVQ_LOOP_K_NVFP4 2 /* kvq_loop_ref.flags: the K planes are NVFP4 */
+#define KVQ_LOOP_V_NVFP4 4 /* kvq_loop_ref.flags: the V planes are NVFP4 */
 
 typedef struct kvq_loop_ref {
   int32_t n_rows;
-  int32_t flags;             /* KVQ_LOOP_K_TILE or 0 */
+  int32_t flags;             /* KVQ_LOOP_* bits */
   const int32_t* active_idx; /* NULL: dense */
   int32_t* tile_dir;         /* required for sparse loops */
   uint8_t* k_codes;
@@ -238,11 +265,19 @@ size_t kvq_batch_workspace_bytes(int n_requests);
  *   workspace  >= kvq_batch_workspace_bytes(n_requests) bytes, 16-byte aligned.
  * Table contents are preconditions (as for the single-request calls); an
  * inconsistent sparse tile map sets bit 4 of the int32 error word at offset 0
- * of the workspace.
+ * of the workspace. Every loop of the chain must be INT4 (see the _ex form).
  */
 kvq_status kvq_encode_batch(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind, int loop,
                             const uint16_t* const* x, void* workspace, size_t workspace_bytes,
                             kvq_cuda_stream stream);
+
+/* kvq_encode_batch for chains with NVFP4 residual loops: bit j of nvfp4_loops
+ * says that loop j of `kind` is NVFP4 in every request of the table (bit 0,
+ * the base, must be clear). A request whose loop flags disagree with the mask
+ * is skipped and sets bit 64 of the error word. */
+kvq_status kvq_encode_batch_ex(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind,
+                               int loop, const uint16_t* const* x, uint32_t nvfp4_loops, void* workspace,
+                               size_t workspace_bytes, kvq_cuda_stream stream);
 
 /* Batched reconstruction at `depth` of K or V for n_requests requests into
  * out[b] (DEVICE array of device pointers to BF16 [T_b][H][D]). */
@@ -250,12 +285,22 @@ kvq_status kvq_reconstruct_batch(const kvq_request* reqs, int n_requests, int n_
                                  int depth, uint16_t* const* out, void* workspace, size_t workspace_bytes,
                                  kvq_cuda_stream stream);
 
+/* kvq_reconstruct_batch for chains with NVFP4 residual loops (nvfp4_loops as
+ * in kvq_encode_batch_ex). */
+kvq_status kvq_reconstruct_batch_ex(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind,
+                                    int depth, uint16_t* const* out, uint32_t nvfp4_loops, void* workspace,
+                                    size_t workspace_bytes, kvq_cuda_stream stream);
+
 /* Workspace bytes kvq_decode_attn_packed needs on the current device. */
 size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim);
 
 #define KVQ_ATTN_AUTO 0 /* tensor-core kernel for depth <= 4, CUDA-core kernel beyond */
 #define KVQ_ATTN_SIMT 1 /* CUDA-core kernel: exact BF16 chain per element, FP32 dot products */
 #define KVQ_ATTN_MMA 2  /* tensor-core kernel (depth <= 4): unpack + folded dequant into m16n8k16 MMAs */
+#define KVQ_ATTN_NVFP4 8 /* OR-ed into algo: the table may hold NVFP4 residual loops. Without it the
+                           tensor-core kernel refuses such a request (NaN output, error bit 64); the
+                           CUDA-core kernel reads either format. kvq_decode_attn_packed and the
+                           no-alloc entry run without it (INT4 tables). */
 
 /*
  * Packed-KV GQA decode attention at `depth` (RFC §3.2: historical K/V are read

@@ -42,9 +42,11 @@ size_t round16(size_t x) { return (x + 15) / 16 * 16; }
 kvq_status check_format(const kvq_stream* s, const char* name) {
   if (s == nullptr) return fail(KVQ_ERR_BAD_ARG, "%s is NULL", name);
   if (s->version != KVQ_FORMAT_VERSION) return fail(KVQ_ERR_UNSUPPORTED, "%s: format version %u", name, s->version);
-  if (s->bits != KVQ_BITS || s->group != KVQ_GROUP || s->nibble_order != KVQ_NIBBLE_LO_FIRST)
-    return fail(KVQ_ERR_UNSUPPORTED, "%s: bits %d group %d nibble order %d", name, s->bits, s->group,
-                s->nibble_order);
+  const bool fmt_ok = (s->format == KVQ_FMT_INT4 && s->group == KVQ_GROUP) ||
+                      (s->format == KVQ_FMT_NVFP4 && s->group == 16);
+  if (s->bits != KVQ_BITS || !fmt_ok || s->nibble_order != KVQ_NIBBLE_LO_FIRST)
+    return fail(KVQ_ERR_UNSUPPORTED, "%s: bits %d format %d group %d nibble order %d", name, s->bits, s->format,
+                s->group, s->nibble_order);
   if (s->kind != KVQ_K && s->kind != KVQ_V) return fail(KVQ_ERR_BAD_ARG, "%s: kind %d", name, s->kind);
   if (s->kgroup != KVQ_KGROUP_COMPACT && s->kgroup != KVQ_KGROUP_TILE)
     return fail(KVQ_ERR_UNSUPPORTED, "%s: K grouping %d", name, s->kgroup);
@@ -71,12 +73,29 @@ kvq_status check_planes(const kvq_stream* s, const char* name, bool need_dir) {
 }
 
 bool k_tile(const kvq_stream* s) { return s->kind == KVQ_K && s->kgroup == KVQ_KGROUP_TILE; }
+bool nvfp4(const kvq_stream* s) { return s->format == KVQ_FMT_NVFP4; }
+
+// Loop-ref flag bits of a stream (K or V planes).
+int32_t loop_flags(const kvq_stream* s) {
+  int32_t f = k_tile(s) ? KVQ_LOOP_K_TILE : 0;
+  if (nvfp4(s)) f |= s->kind == KVQ_K ? KVQ_LOOP_K_NVFP4 : KVQ_LOOP_V_NVFP4;
+  return f;
+}
+
+// Bit j: loop j of the streams is NVFP4.
+uint32_t nvfp4_mask(const kvq_stream* loops, int n) {
+  uint32_t m = 0;
+  for (int j = 0; j < n; ++j)
+    if (nvfp4(&loops[j])) m |= 1u << j;
+  return m;
+}
 
 void to_planes(const kvq_stream* s, LoopPlanes* p) {
   p->n_rows = s->n_rows;
   p->sparse = s->active_idx != nullptr;
   p->ktile = k_tile(s);
   p->kgroups = k_groups_of(k_tile(s), s->n_rows, s->n_tokens);
+  p->fmt = s->format;
   p->active = s->active_idx;
   p->tile_dir = s->tile_dir;
   p->codes = s->codes;
@@ -97,6 +116,7 @@ kvq_status build_chain(const kvq_stream* loops, int depth, Chain* C, const char*
       return fail(KVQ_ERR_BAD_ARG, "%s: loops disagree on kind, n_tokens or n_heads", name);
   }
   if (loops[0].active_idx != nullptr) return fail(KVQ_ERR_BAD_ARG, "%s[0]: the base must be dense", name);
+  if (nvfp4(&loops[0])) return fail(KVQ_ERR_UNSUPPORTED, "%s[0]: the base must be INT4", name);
   memset(C, 0, sizeof *C);
   C->depth = depth;
   C->kind = loops[0].kind;
@@ -169,6 +189,7 @@ kvq_status kvq_stream_init(kvq_stream* s, int kind, int n_rows, int n_tokens, in
   s->n_tokens = n_tokens;
   s->n_heads = n_heads;
   s->head_dim = head_dim;
+  s->format = KVQ_FMT_INT4;
   if (kind != KVQ_K && kind != KVQ_V) return fail(KVQ_ERR_BAD_ARG, "kind %d", kind);
   if (n_tokens < 0 || n_rows < 0 || n_rows > n_tokens || n_heads < 1 || head_dim < 2 || (head_dim & 1))
     return fail(KVQ_ERR_BAD_ARG, "sizes n_rows %d n_tokens %d n_heads %d head_dim %d", n_rows, n_tokens, n_heads,
@@ -176,9 +197,26 @@ kvq_status kvq_stream_init(kvq_stream* s, int kind, int n_rows, int n_tokens, in
   return ok();
 }
 
+kvq_status kvq_stream_set_format(kvq_stream* s, int format) {
+  if (s == nullptr) return fail(KVQ_ERR_BAD_ARG, "stream is NULL");
+  if (format == KVQ_FMT_INT4) {
+    s->format = KVQ_FMT_INT4;
+    s->group = KVQ_GROUP;
+  } else if (format == KVQ_FMT_NVFP4) {
+    if (s->head_dim % 16 != 0) return fail(KVQ_ERR_UNSUPPORTED, "NVFP4 needs head_dim %% 16 == 0");
+    s->format = KVQ_FMT_NVFP4;
+    s->group = 16;
+  } else {
+    return fail(KVQ_ERR_BAD_ARG, "format %d", format);
+  }
+  return ok();
+}
+
 size_t kvq_plane_bytes(const kvq_stream* s, int plane) {
   if (s == nullptr) return 0;
   const int64_t n = s->n_rows, H = s->n_heads, D = s->head_dim;
+  if (nvfp4(s) && plane == KVQ_PLANE_MINS) return round16(size_t(H * n * (D / 16)));  // E4M3 block scales
+  if (nvfp4(s) && plane == KVQ_PLANE_SCALES) return 16;                              // FP32 tensor-scale record
   switch (plane) {
     case KVQ_PLANE_CODES: return round16(size_t(H * n * (D / 2)));
     case KVQ_PLANE_MINS:
@@ -192,21 +230,23 @@ size_t kvq_plane_bytes(const kvq_stream* s, int plane) {
 }
 
 int64_t kvq_stream_payload_bytes_ex(int kind, int n_rows, int n_tokens, int n_heads, int head_dim, int sparse,
-                                    int kgroup) {
+                                    int kgroup, int format) {
   const int64_t n = n_rows, H = n_heads, D = head_dim;
+  if (format == KVQ_FMT_NVFP4) return n > 0 ? H * n * (D / 2) + H * n * (D / 16) + 4 + (sparse ? 4 * n : 0) : 0;
   const bool tile = kgroup == KVQ_KGROUP_TILE && sparse;
   int64_t params = (kind == KVQ_K) ? H * k_groups_of(tile, n_rows, n_tokens) * D : H * n * cdiv(D, KVQ_GROUP);
   return H * n * (D / 2) + 2 * 2 * params + (sparse ? 4 * n : 0);
 }
 
 int64_t kvq_stream_payload_bytes(int kind, int n_rows, int n_heads, int head_dim, int sparse) {
-  return kvq_stream_payload_bytes_ex(kind, n_rows, n_rows, n_heads, head_dim, sparse, KVQ_KGROUP_COMPACT);
+  return kvq_stream_payload_bytes_ex(kind, n_rows, n_rows, n_heads, head_dim, sparse, KVQ_KGROUP_COMPACT,
+                                     KVQ_FMT_INT4);
 }
 
 // Planes of a stream descriptor as one loop entry of a request.
 static void to_loop_ref(const kvq_stream* s, kvq_loop_ref* L) {
   L->n_rows = s->n_rows;
-  if (k_tile(s)) L->flags |= KVQ_LOOP_K_TILE;
+  L->flags |= loop_flags(s);
   L->active_idx = s->active_idx;
   L->tile_dir = s->tile_dir;
   if (s->kind == KVQ_K) {
@@ -240,6 +280,7 @@ kvq_status kvq_encode_base(const uint16_t* x, const kvq_stream* out, kvq_cuda_st
   kvq_status st = check_planes(out, "out", false);
   if (st != KVQ_OK) return st;
   if (out->active_idx != nullptr) return fail(KVQ_ERR_BAD_ARG, "out: the base stream must be dense");
+  if (nvfp4(out)) return fail(KVQ_ERR_UNSUPPORTED, "out: the base must be INT4 (NVFP4 is a residual format)");
   if (out->n_rows == 0) return ok();
   if (x == nullptr) return fail(KVQ_ERR_BAD_ARG, "x is NULL");
   if (!aligned16(x)) return fail(KVQ_ERR_MISALIGNED, "x must be 16-byte aligned");
@@ -297,7 +338,13 @@ kvq_status kvq_encode_residual(const uint16_t* x_r, const kvq_stream* prev, int 
   for (int j = 0; j < n_prev; ++j) to_loop_ref(&prev[j], &a.one.loop[j]);
   to_loop_ref(out, &a.one.loop[n_prev]);
   a.one_x = x_r;
+  a.nvfp4 = nvfp4_mask(prev, n_prev) | (nvfp4(out) ? 1u << n_prev : 0u);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (nvfp4(out)) {  // the tensor-scale record: s_t and the encoder's running max |delta| start at 0
+    if (out->scales == nullptr || !aligned16(out->scales)) return fail(KVQ_ERR_BAD_ARG, "out: NVFP4 scale record");
+    cudaError_t e = cudaMemsetAsync(out->scales, 0, 16, s);
+    if (e != cudaSuccess) return cuda_status(e, "clear tensor scale");
+  }
   if (out->active_idx != nullptr) {
     st = run_single(a, kModeTileDir, s, "tile_dir launch");
     if (st != KVQ_OK) return st;
@@ -321,6 +368,7 @@ kvq_status kvq_reconstruct(const kvq_stream* loops, int depth, uint16_t* out, kv
   a.one.n_loops = depth;
   for (int j = 0; j < depth; ++j) to_loop_ref(&loops[j], &a.one.loop[j]);
   a.one_out = out;
+  a.nvfp4 = nvfp4_mask(loops, depth);
   return run_single(a, kModeRecon, reinterpret_cast<cudaStream_t>(stream), "reconstruct launch");
 }
 
@@ -346,9 +394,19 @@ static kvq_status check_batch(const kvq_request* reqs, int n_requests, int n_hea
 kvq_status kvq_encode_batch(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind, int loop,
                             const uint16_t* const* x, void* workspace, size_t workspace_bytes,
                             kvq_cuda_stream stream) {
+  return kvq_encode_batch_ex(reqs, n_requests, n_heads, head_dim, kind, loop, x, 0u, workspace, workspace_bytes,
+                             stream);
+}
+
+kvq_status kvq_encode_batch_ex(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind,
+                               int loop, const uint16_t* const* x, uint32_t nvfp4_loops, void* workspace,
+                               size_t workspace_bytes, kvq_cuda_stream stream) {
   kvq_status st = check_batch(reqs, n_requests, n_heads, head_dim, kind, x, workspace, workspace_bytes);
   if (st != KVQ_OK) return st;
   if (loop < 0 || loop >= KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "loop %d", loop);
+  if ((nvfp4_loops & 1u) || (nvfp4_loops >> KVQ_MAX_LOOPS))
+    return fail(KVQ_ERR_BAD_ARG, "nvfp4_loops 0x%x: the base is INT4 and at most %d loops", nvfp4_loops,
+                KVQ_MAX_LOOPS);
   if (n_requests == 0) return ok();
   int sms = 0;
   st = current_sms(&sms);
@@ -361,6 +419,7 @@ kvq_status kvq_encode_batch(const kvq_request* reqs, int n_requests, int n_heads
   a.H = n_heads;
   a.kind = kind;
   a.loop = loop;
+  a.nvfp4 = nvfp4_loops & ((2u << loop) - 1u);  // loops 0 .. loop
   char* ws = static_cast<char*>(workspace);
   a.err = reinterpret_cast<int32_t*>(ws);
   int32_t* prefix = reinterpret_cast<int32_t*>(ws + 16);
@@ -377,9 +436,19 @@ kvq_status kvq_encode_batch(const kvq_request* reqs, int n_requests, int n_heads
 kvq_status kvq_reconstruct_batch(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind,
                                  int depth, uint16_t* const* out, void* workspace, size_t workspace_bytes,
                                  kvq_cuda_stream stream) {
+  return kvq_reconstruct_batch_ex(reqs, n_requests, n_heads, head_dim, kind, depth, out, 0u, workspace,
+                                  workspace_bytes, stream);
+}
+
+kvq_status kvq_reconstruct_batch_ex(const kvq_request* reqs, int n_requests, int n_heads, int head_dim, int kind,
+                                    int depth, uint16_t* const* out, uint32_t nvfp4_loops, void* workspace,
+                                    size_t workspace_bytes, kvq_cuda_stream stream) {
   kvq_status st = check_batch(reqs, n_requests, n_heads, head_dim, kind, out, workspace, workspace_bytes);
   if (st != KVQ_OK) return st;
   if (depth < 1 || depth > KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "depth %d", depth);
+  if ((nvfp4_loops & 1u) || (nvfp4_loops >> KVQ_MAX_LOOPS))
+    return fail(KVQ_ERR_BAD_ARG, "nvfp4_loops 0x%x: the base is INT4 and at most %d loops", nvfp4_loops,
+                KVQ_MAX_LOOPS);
   if (n_requests == 0) return ok();
   int sms = 0;
   st = current_sms(&sms);
@@ -392,6 +461,7 @@ kvq_status kvq_reconstruct_batch(const kvq_request* reqs, int n_requests, int n_
   a.H = n_heads;
   a.kind = kind;
   a.loop = depth;
+  a.nvfp4 = nvfp4_loops & ((1u << depth) - 1u);  // loops 0 .. depth-1
   char* ws = static_cast<char*>(workspace);
   a.err = reinterpret_cast<int32_t*>(ws);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -419,7 +489,7 @@ kvq_status kvq_request_fill(const kvq_stream* k_loops, const kvq_stream* v_loops
     if (j == 0 && k->active_idx != nullptr) return fail(KVQ_ERR_BAD_ARG, "loop 1 must be dense");
     kvq_loop_ref& L = out->loop[j];
     L.n_rows = k->n_rows;
-    L.flags = k_tile(k) ? KVQ_LOOP_K_TILE : 0;
+    L.flags = loop_flags(k) | loop_flags(v);
     L.active_idx = k->active_idx;
     L.tile_dir = k->tile_dir ? k->tile_dir : v->tile_dir;
     L.k_codes = k->codes;
@@ -456,6 +526,8 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   if (head_dim != kD) return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d (kernels support 128)", head_dim);
   if (depth < 1 || depth > KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "depth %d", depth);
   if (!(softmax_scale > 0.0f) || softmax_scale > 1e30f) return fail(KVQ_ERR_BAD_ARG, "softmax_scale");
+  const bool nvfp4_hint = (algo & KVQ_ATTN_NVFP4) != 0;
+  algo &= ~KVQ_ATTN_NVFP4;
   if (algo < KVQ_ATTN_AUTO || algo > KVQ_ATTN_MMA) return fail(KVQ_ERR_BAD_ARG, "algo %d", algo);
   if (n_requests == 0) return ok();
   if (!reqs || !q || !out) return fail(KVQ_ERR_BAD_ARG, "NULL reqs, q or out");
@@ -481,6 +553,8 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   a.Hq = n_q_heads;
   a.g = g;
   a.depth = depth;
+  a.nvfp4 = nvfp4_hint ? 1 : 0;
+  a.refuse_nvfp4 = (algo == KVQ_ATTN_MMA && !nvfp4_hint) ? 1 : 0;
   a.n_ctas = attn_ctas(algo, dev);
   a.q = q;
   a.scale = softmax_scale;
@@ -556,7 +630,7 @@ kvq_status kvq_sparse_ref_state(const kvq_request* reqs, int n_requests, int n_h
   // the full attention at the reference depth: O_ref (and a cleared error word)
   const size_t apart = sparse_attn_part(n_requests, n_heads, n_q_heads);
   st = kvq_decode_attn_packed_ex(reqs, n_requests, n_heads, n_q_heads, head_dim, ref_depth, q_ref, softmax_scale,
-                                 o_ref, workspace, apart, KVQ_ATTN_AUTO, stream);
+                                 o_ref, workspace, apart, KVQ_ATTN_AUTO | KVQ_ATTN_NVFP4, stream);
   if (st != KVQ_OK) return st;
   SparseArgs a;
   memset(&a, 0, sizeof a);

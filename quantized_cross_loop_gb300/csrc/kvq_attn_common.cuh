@@ -34,6 +34,8 @@ struct AttnArgs {
   int32_t* prefix;    // [B+1] tile prefix
   float* partials;    // slots
   float2* stats;      // [B][Hq] (max in log2 units, sum of exponentials) of the packed part
+  int32_t nvfp4;      // the table may hold NVFP4 loops (the tensor-core kernel's NVFP4-reading form)
+  int32_t refuse_nvfp4;  // the kernel of this call reads no NVFP4 loop: such requests are refused
 };
 
 // Workspace layout: [0,16) error word; then int32 prefix[B+1] (rounded to 16 B);
@@ -100,6 +102,18 @@ __device__ __forceinline__ bool request_ok(const kvq_request& r, int depth) {
       return false;
   }
   return true;
+}
+
+// A request this call can attend: a consistent entry, and no NVFP4 loop when
+// the call's kernel does not read them.
+__device__ __forceinline__ bool nvfp4_refused(const AttnArgs& a, const kvq_request& r) {
+  if (!a.refuse_nvfp4) return false;
+  for (int j = 0; j < a.depth && j < KVQ_MAX_LOOPS; ++j)
+    if (r.loop[j].flags & (KVQ_LOOP_K_NVFP4 | KVQ_LOOP_V_NVFP4)) return true;
+  return false;
+}
+__device__ __forceinline__ bool attn_request_ok(const AttnArgs& a, const kvq_request& r) {
+  return request_ok(r, a.depth) && !nvfp4_refused(a, r);
 }
 
 cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream);

@@ -38,6 +38,18 @@
 // Each warp keeps its own online softmax (max, sum, PV accumulators) over its
 // tokens; the group merges the four at the end of a unit. Per tile and group:
 // one named barrier (K-min terms ready). Log2 domain, FP32 throughout.
+//
+// NVFP4 residual loops (INT4 codec PR review: E2M1 codes, an E4M3 scale per 16
+// channels of a (row, head), an FP32 scale per stream), in the kNv
+// instantiation. The scales vary along the contraction, so they scale the A
+// operand instead of folding into Q or P:
+//   QK^T: A = e2m1 * s_b (hardware E2M1 / E4M3 to FP16 conversions; the product
+//         has at most six significant bits and lies in [2^-10, 2688], so it is
+//         exact in FP16), B = q; the loop's logits are then scaled by s_t in FP32.
+//   PV:   A = (e2m1 * 2^-14) * s_b, built from the nibble by bit placement
+//         (FP16 bits (c & 7) << 9 | (c & 8) << 12 encode e2m1 * 2^-14 exactly,
+//         and the product stays an exact FP16 multiple of 2^-24), B = RN16(p *
+//         s_t * 2^14); NVFP4 has no zero point, so no min terms.
 #include <cuda_fp16.h>
 
 #include "kvq_attn_common.cuh"
@@ -65,10 +77,16 @@ constexpr uint32_t kMagic = 0x54005400u;     // FP16 64.0 in both halves
 //   pair p (8 words from 8): loop index << 1 | group
 //   loop j (8 words from 16 + 8j): nrows c0 g0 ngrp vrem irem sparse pbase
 //       (c0: first stored row of the tile; under tile grouping of K, 64 x tile)
-constexpr int kMetaWords = 16 + 8 * kLoops;
+//   loop j formats (4 words from 16 + 8 kLoops + 4j): NVFP4 flags (1: K, 2: V),
+//       K tensor scale, V tensor scale (float bits), byte offsets of the first
+//       staged K | V block-scale row (low | high 16 bits)
+constexpr int kMetaFmt = 16 + 8 * kLoops;
+constexpr int kMetaWords = kMetaFmt + 4 * kLoops;
 
 // One loop's staged planes of a tile (every field a multiple of 16 bytes, so
 // that each starts on a 16-byte boundary for the bulk copies).
+// An NVFP4 loop stages its E4M3 block scales (8 bytes per row, up to 528 bytes
+// with the 16-byte rounding) over kmin..ksc (K) and vmin..vsc (V).
 struct LoopStage {
   uint8_t kc[KVQ_TILE * kRowBytes];
   uint8_t vc[KVQ_TILE * kRowBytes];
@@ -203,14 +221,40 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
 __device__ __forceinline__ uint32_t h2u(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
 __device__ __forceinline__ __half2 u2h(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
 
+// Two E2M1 codes (the low byte of x: low nibble, high nibble) as an exact FP16
+// pair {low, high}, by the hardware conversion.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(x));
+  return r;
+}
+
+// Two E4M3 values (the low 16 bits of x) as an exact FP16 pair {low byte, high byte}.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(r) : "r"(x));
+  return r;
+}
+
+// Nibble c (0..3) of each 16-bit half of x as FP16 e2m1 * 2^-14: the nibble is
+// moved to bits 12..15, then its magnitude bits to 9..11 under its sign at 15.
+template <int C>
+__device__ __forceinline__ uint32_t nv_pair(uint32_t x) {
+  const uint32_t a = (C < 3 ? (x << (12 - 4 * C)) : x) & 0xF000F000u;
+  return (a | (a >> 3)) & 0x8E008E00u;
+}
+
 // ---------------------------------------------------------------- producer
 
-template <int DEPTH>
+template <int DEPTH, bool kNv>
 __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long long e0) {
   int b = request_of(a.prefix, a.n_requests, s0);
   long long us = 0, ue = -1;  // current unit's tile range
   int h = 0, T = 0, unit = -1, nsink = 0;
   int nr[DEPTH], kgr[DEPTH];  // stored rows; K groups per head (0: compact grouping, else tile grouping)
+  bool refused = false;       // a loop in a format this kernel does not read: the unit reads no rows
+  int fl[DEPTH];              // NVFP4 flags per loop (1: K, 2: V)
+  float kst[DEPTH], vst[DEPTH];  // their tensor scales
   const int32_t* act[DEPTH];
   const int32_t* dir[DEPTH];
   const uint8_t* kc[DEPTH];
@@ -232,11 +276,16 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       us = rb + (long long)h * nt;
       ue = us + nt;
       unit = b * a.H + h;
+      refused = false;
 #pragma unroll
       for (int j = 0; j < DEPTH; ++j) {
         const kvq_loop_ref& L = R.loop[j];
         nr[j] = L.n_rows;
         kgr[j] = (L.flags & KVQ_LOOP_K_TILE) ? k_groups_of(true, L.n_rows, T) : 0;
+        fl[j] = ((L.flags & KVQ_LOOP_K_NVFP4) ? 1 : 0) | ((L.flags & KVQ_LOOP_V_NVFP4) ? 2 : 0);
+        if (fl[j] && !kNv) refused = true;
+        kst[j] = (kNv && (fl[j] & 1) && L.n_rows > 0) ? __ldg(reinterpret_cast<const float*>(L.k_scales)) : 0.0f;
+        vst[j] = (kNv && (fl[j] & 2) && L.n_rows > 0) ? __ldg(reinterpret_cast<const float*>(L.v_scales)) : 0.0f;
         act[j] = L.active_idx;
         dir[j] = L.tile_dir;
         kc[j] = L.k_codes;
@@ -284,12 +333,22 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
         atomicOr(a.err, 4);
         c0 = c1 = 0;
       }
+      if (refused) {
+        if (k == 0 && j == 0) atomicOr(a.err, 64);
+        c0 = c1 = 0;
+      }
       const int n = c1 - c0;
       // K groups of the tile's rows: under tile grouping the tile's own group k,
       // and word 1 is set so that a consumer's ((word1 + row) >> 6) - g0 is 0
       const bool kt = kgr[j] > 0;
+      const bool nk = kNv && (fl[j] & 1), nv = kNv && (fl[j] & 2);
       const int g0 = kt ? k : c0 / kG;
-      const int ngrp = n > 0 ? (kt ? 1 : (c1 - 1) / kG - g0 + 1) : 0;
+      const int ngrp = (n > 0 && !nk) ? (kt ? 1 : (c1 - 1) / kG - g0 + 1) : 0;  // INT4 K groups (NVFP4: none)
+      int32_t* LF = M + kMetaFmt + 4 * j;
+      LF[0] = kNv ? fl[j] : 0;
+      LF[1] = __float_as_int(kst[j]);
+      LF[2] = __float_as_int(vst[j]);
+      LF[3] = 0;
       LM[0] = n;
       LM[1] = kt ? k * kG : c0;
       LM[2] = g0;
@@ -303,10 +362,25 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       const long long hr = (long long)h * nr[j] + c0;  // first stored row of this head
       bulk_copy(st.l[j].kc, kc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
       bulk_copy(st.l[j].vc, vc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
-      const long long gb = ((long long)h * (kt ? kgr[j] : (nr[j] + kG - 1) / kG) + g0) * kD;
-      bulk_copy(st.l[j].kmin, kmn[j] + gb, ngrp * kD * 2, &S.full[s]);
-      bulk_copy(st.l[j].ksc, ksc[j] + gb, ngrp * kD * 2, &S.full[s]);
-      {  // V params: 4 B per row and plane, moved in whole 16-byte units
+      int krem = 0, vrem = 0;
+      if (nk) {  // E4M3 block scales: 8 B per row, in whole 16-byte units
+        const long long off = hr * 8;
+        const long long lo = off & ~15LL;
+        const uint32_t nb = uint32_t(((off + (long long)n * 8 + 15) & ~15LL) - lo);
+        bulk_copy(st.l[j].kmin, reinterpret_cast<const uint8_t*>(kmn[j]) + lo, nb, &S.full[s]);
+        krem = int(off - lo);
+      } else {
+        const long long gb = ((long long)h * (kt ? kgr[j] : (nr[j] + kG - 1) / kG) + g0) * kD;
+        bulk_copy(st.l[j].kmin, kmn[j] + gb, ngrp * kD * 2, &S.full[s]);
+        bulk_copy(st.l[j].ksc, ksc[j] + gb, ngrp * kD * 2, &S.full[s]);
+      }
+      if (nv) {
+        const long long off = hr * 8;
+        const long long lo = off & ~15LL;
+        const uint32_t nb = uint32_t(((off + (long long)n * 8 + 15) & ~15LL) - lo);
+        bulk_copy(st.l[j].vmin, reinterpret_cast<const uint8_t*>(vmn[j]) + lo, nb, &S.full[s]);
+        vrem = int(off - lo);
+      } else {  // V params: 4 B per row and plane, moved in whole 16-byte units
         const long long off = hr * 4;
         const long long lo = off & ~15LL;
         const uint32_t nb = uint32_t(((off + (long long)n * 4 + 15) & ~15LL) - lo);
@@ -314,6 +388,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
         bulk_copy(st.l[j].vsc, reinterpret_cast<const uint8_t*>(vsc[j]) + lo, nb, &S.full[s]);
         LM[4] = int((off - lo) / 2);
       }
+      LF[3] = krem | (vrem << 16);
       if (act[j] != nullptr) {
         const long long off = (long long)c0 * 4;
         const long long lo = off & ~15LL;
@@ -456,7 +531,38 @@ __device__ __forceinline__ void qk_pass(const Stage& st, int j, int G, const uin
   for (int k = 0; k < 4; ++k) e[k] = (c[0][k] + c[1][k]) + (c[2][k] + c[3][k]);
 }
 
-template <int DEPTH>
+// Logits of rows ra (token g) and rc (token g + 8) of an NVFP4 K loop j: A =
+// e2m1 * s_b (FP16, exact), B = q, two MMA chains; the sum is scaled by the
+// stream's tensor scale st. krem: byte offset of the staged block-scale rows.
+__device__ __forceinline__ void qk_pass_nv(const Stage& st, int j, const __half* qrow, int krem, int ra, int rc,
+                                           const uint4 wa, const uint4 wb, int q, float tscale, float e[4]) {
+  const uint8_t* ks = reinterpret_cast<const uint8_t*>(st.l[j].kmin) + krem;  // row r: 8 bytes at 8 r
+  // blocks 2q and 2q + 1 of each row: channels 32q .. 32q + 31, this thread's
+  const uint32_t sa2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + 8 * ra + 2 * q));
+  const uint32_t sc2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ks + 8 * rc + 2 * q));
+  const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w}, wB[4] = {wb.x, wb.y, wb.z, wb.w};
+  float c[2][4] = {};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 sa = i < 2 ? __low2half2(u2h(sa2)) : __high2half2(u2h(sa2));
+    const __half2 sc = i < 2 ? __low2half2(u2h(sc2)) : __high2half2(u2h(sc2));
+    uint32_t ua[4], ub[4];  // channel pairs (2k, 2k + 1) of word i, scaled
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      ua[k] = h2u(__hmul2(u2h(e2m1x2_to_f16x2(wA[i] >> (8 * k))), sa));
+      ub[k] = h2u(__hmul2(u2h(e2m1x2_to_f16x2(wB[i] >> (8 * k))), sc));
+    }
+    const uint4 qv = *reinterpret_cast<const uint4*>(qrow + 32 * q + 8 * i);  // q of channels 32q + 8i .. + 7
+    const uint32_t A0[4] = {ua[0], ub[0], ua[1], ub[1]};
+    const uint32_t A1[4] = {ua[2], ub[2], ua[3], ub[3]};
+    mma16816(c[0], A0, qv.x, qv.y);
+    mma16816(c[1], A1, qv.z, qv.w);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) e[k] = (c[0][k] + c[1][k]) * tscale;
+}
+
+template <int DEPTH, bool kNv>
 __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long long s0, long long e0) {
   const int gt = threadIdx.x - grp * kGroupThreads;  // thread within the group
   const int w = gt >> 5, lane = gt & 31;
@@ -567,10 +673,6 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       }
       if (lane == 0) Gs.slice[w][j] = SliceInfo{rb, cnt, bits, 0};
       if (cnt == 0) continue;
-      // K groups of the slice's rows, relative to the tile's first group
-      const int ga = ((c0 + rb) >> 6) - g0;
-      const int gb = ((c0 + rb + cnt - 1) >> 6) - g0;
-      const bool split = gb != ga;
       // A: the stored rows of the warp's tokens g and g + 8 (a sparse loop's r-th
       // present token sits in row rb + r; an absent token reads a valid row whose
       // logit is then dropped), the 16 bytes of chunk q
@@ -579,6 +681,23 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       const uint4 wa = *reinterpret_cast<const uint4*>(&st.l[j].kc[ra * kRowBytes + 16 * q]);
       const uint4 wb = *reinterpret_cast<const uint4*>(&st.l[j].kc[rc * kRowBytes + 16 * q]);
       float e[4];
+      if (kNv && (st.meta[kMetaFmt + 4 * j] & 1)) {  // NVFP4 K: no groups, no min terms
+        const int4 lf = *reinterpret_cast<const int4*>(&st.meta[kMetaFmt + 4 * j]);
+        qk_pass_nv(st, j, &Gs.q16[g][0], lf.w & 0xFFFF, ra, rc, wa, wb, q, __int_as_float(lf.y), e);
+        if ((bits >> g) & 1) {
+          sv[0] += e[0];
+          sv[1] += e[1];
+        }
+        if ((bits >> (g + 8)) & 1) {
+          sv[2] += e[2];
+          sv[3] += e[3];
+        }
+        continue;
+      }
+      // K groups of the slice's rows, relative to the tile's first group
+      const int ga = ((c0 + rb) >> 6) - g0;
+      const int gb = ((c0 + rb + cnt - 1) >> 6) - g0;
+      const bool split = gb != ga;
       qk_pass(st, j, ga, qp, wa, wb, q, e);
       const int Ga = ((c0 + ra) >> 6) - g0, Gc = ((c0 + rc) >> 6) - g0;
       if (split) {  // rows of the second K group: a second pass with that group's Q'
@@ -666,6 +785,47 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         if (si.cnt == 0) continue;
         const int vrem = st.meta[16 + 8 * j + 4];
         const int bits = si.bits, rb = si.rb, cnt = si.cnt;
+        // stored rows of the tokens 2q, 2q+1, 2q+8, 2q+9 (an absent token reads a
+        // valid row against a zero P')
+        const int r0 = rb + min(__popc(bits & ((1 << (2 * q)) - 1)), cnt - 1);
+        const int r1 = rb + min(__popc(bits & ((2 << (2 * q)) - 1)), cnt - 1);
+        const int r2 = rb + min(__popc(bits & ((1 << (2 * q + 8)) - 1)), cnt - 1);
+        const int r3 = rb + min(__popc(bits & ((2 << (2 * q + 8)) - 1)), cnt - 1);
+        if (kNv && (st.meta[kMetaFmt + 4 * j] & 2)) {  // NVFP4 V
+          const int4 lf = *reinterpret_cast<const int4*>(&st.meta[kMetaFmt + 4 * j]);
+          const float st14 = __int_as_float(lf.z) * 16384.0f;  // s_t * 2^14 (the codes carry 2^-14)
+          const uint8_t* vs = reinterpret_cast<const uint8_t*>(st.l[j].vmin) + (lf.w >> 16);
+          uint32_t rr[2];  // [token half] = {P'(token, 2q), P'(token, 2q+1)}
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const bool ok = (bits >> (g + 8 * half)) & 1;
+            rr[half] = h2u(__floats2half2_rn(ok ? p[2 * half] * st14 : 0.f, ok ? p[2 * half + 1] * st14 : 0.f));
+          }
+          const uint32_t B0 = transpose8x8(rr[0]), B1 = transpose8x8(rr[1]);
+          const uint8_t* base = &st.l[j].vc[0];
+#pragma unroll
+          for (int vg = 0; vg < 2; ++vg) {
+            const int blk = 4 * vg + (g >> 1);  // the 16-channel block of channels 64 vg + 8 g .. + 7
+            const __half2 S01 = u2h(e4m3x2_to_f16x2(uint32_t(vs[8 * r0 + blk]) | (uint32_t(vs[8 * r1 + blk]) << 8)));
+            const __half2 S89 = u2h(e4m3x2_to_f16x2(uint32_t(vs[8 * r2 + blk]) | (uint32_t(vs[8 * r3 + blk]) << 8)));
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(base + r0 * kRowBytes + 4 * (8 * vg + g));
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(base + r1 * kRowBytes + 4 * (8 * vg + g));
+            const uint32_t w2 = *reinterpret_cast<const uint32_t*>(base + r2 * kRowBytes + 4 * (8 * vg + g));
+            const uint32_t w3 = *reinterpret_cast<const uint32_t*>(base + r3 * kRowBytes + 4 * (8 * vg + g));
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              const uint32_t x = __byte_perm(w0, w1, hb ? 0x7632 : 0x5410);
+              const uint32_t y = __byte_perm(w2, w3, hb ? 0x7632 : 0x5410);
+              const uint32_t A0[4] = {h2u(__hmul2(u2h(nv_pair<0>(x)), S01)), h2u(__hmul2(u2h(nv_pair<1>(x)), S01)),
+                                      h2u(__hmul2(u2h(nv_pair<0>(y)), S89)), h2u(__hmul2(u2h(nv_pair<1>(y)), S89))};
+              const uint32_t A1[4] = {h2u(__hmul2(u2h(nv_pair<2>(x)), S01)), h2u(__hmul2(u2h(nv_pair<3>(x)), S01)),
+                                      h2u(__hmul2(u2h(nv_pair<2>(y)), S89)), h2u(__hmul2(u2h(nv_pair<3>(y)), S89))};
+              mma16816(U.acc[4 * vg + 2 * hb], A0, B0, B1);
+              mma16816(U.acc[4 * vg + 2 * hb + 1], A1, B0, B1);
+            }
+          }
+          continue;
+        }
         // P' = p * sV per V group for the warp's tokens g and g + 8 (zero for a token
         // with no row in this loop), and the V-min terms
         uint32_t r[2][2];  // [V group][token half] = {P'(token, 2q), P'(token, 2q+1)}
@@ -698,10 +858,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         // token reads a valid row against a zero P'); thread g takes word 8*vg + g of
         // each row (channels 64vg + 8g .. +7)
         const uint8_t* base = &st.l[j].vc[0];
-        const int o0 = (rb + min(__popc(bits & ((1 << (2 * q)) - 1)), cnt - 1)) * kRowBytes;
-        const int o1 = (rb + min(__popc(bits & ((2 << (2 * q)) - 1)), cnt - 1)) * kRowBytes;
-        const int o2 = (rb + min(__popc(bits & ((1 << (2 * q + 8)) - 1)), cnt - 1)) * kRowBytes;
-        const int o3 = (rb + min(__popc(bits & ((2 << (2 * q + 8)) - 1)), cnt - 1)) * kRowBytes;
+        const int o0 = r0 * kRowBytes, o1 = r1 * kRowBytes, o2 = r2 * kRowBytes, o3 = r3 * kRowBytes;
         uint32_t wv[2][4];
 #pragma unroll
         for (int vg = 0; vg < 2; ++vg) {
@@ -732,7 +889,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
   if (cur_unit >= 0) finish_unit(a, Gs, U, Mprev, grp, vcta, w, lane);
 }
 
-template <int DEPTH>
+template <int DEPTH, bool kNv>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -759,22 +916,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a) {
   const long long s0 = cta_start(vcta, W, C), e0 = cta_start(vcta + 1, W, C);
   if (s0 >= e0) return;
   if (producer_warp) {
-    if ((threadIdx.x & 31) == 0) producer<DEPTH>(a, S, grp, s0, e0);
+    if ((threadIdx.x & 31) == 0) producer<DEPTH, kNv>(a, S, grp, s0, e0);
     return;
   }
-  consumer<DEPTH>(a, S, grp, vcta, s0, e0);
+  consumer<DEPTH, kNv>(a, S, grp, vcta, s0, e0);
 }
 
-template <int DEPTH>
+template <int DEPTH, bool kNv>
 cudaError_t launch_depth(const AttnArgs& a, cudaStream_t stream) {
   const int smem = int(sizeof(Smem));
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<DEPTH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_mma_kernel<DEPTH, kNv>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attn_mma_kernel<DEPTH><<<a.n_ctas / kGroups, kThreads, smem, stream>>>(a);
+  attn_mma_kernel<DEPTH, kNv><<<a.n_ctas / kGroups, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -785,11 +943,17 @@ int mma_virtual_ctas_per_block() { return mma_attn::kGroups; }
 cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {
   using namespace mma_attn;
   cudaError_t e;
-  switch (a.depth) {
-    case 1: e = launch_depth<1>(a, stream); break;
-    case 2: e = launch_depth<2>(a, stream); break;
-    case 3: e = launch_depth<3>(a, stream); break;
-    case 4: e = launch_depth<4>(a, stream); break;
+  // the NVFP4-reading instantiation only when the caller says the table may
+  // hold NVFP4 loops (the INT4 one refuses them: error bit 64, NaN output)
+  switch (a.depth * 2 + (a.nvfp4 ? 1 : 0)) {
+    case 2: e = launch_depth<1, false>(a, stream); break;
+    case 3: e = launch_depth<1, true>(a, stream); break;
+    case 4: e = launch_depth<2, false>(a, stream); break;
+    case 5: e = launch_depth<2, true>(a, stream); break;
+    case 6: e = launch_depth<3, false>(a, stream); break;
+    case 7: e = launch_depth<3, true>(a, stream); break;
+    case 8: e = launch_depth<4, false>(a, stream); break;
+    case 9: e = launch_depth<4, true>(a, stream); break;
     default: return cudaErrorInvalidValue;
   }
   count_launch();

@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a) {
       const kvq_request& r = a.reqs[b];
       if (!request_ok(r, a.depth)) {
         atomicOr(a.err, 1);
+      } else if (nvfp4_refused(a, r)) {
+        atomicOr(a.err, 64);
       } else {
         v = a.H * n_tiles_of(r.n_tokens);
       }
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(kD) combine_kernel(AttnArgs a) {
   const kvq_request& r = a.reqs[b];
   float* outp = a.out + ((long long)b * a.Hq + (long long)h * g) * kD;
   float2* stats = a.stats + (long long)b * a.Hq + (long long)h * g;
-  if (!request_ok(r, a.depth)) {
+  if (!attn_request_ok(a, r)) {
     for (int i = 0; i < g; ++i) outp[i * kD + d] = __int_as_float(0x7fc00000);
     return;
   }
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(32 * kSegWarps) segment_kernel(AttnArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = a.g;
   const kvq_request& r = a.reqs[b];
-  if (!request_ok(r, a.depth)) return;  // the output is already NaN
+  if (!attn_request_ok(a, r)) return;  // the output is already NaN
   const int ns = r.n_sink, n = r.n_sink + r.n_tail;
   if (n == 0) return;
   __shared__ float s_m[kSegWarps][kMaxG], s_l[kSegWarps][kMaxG];

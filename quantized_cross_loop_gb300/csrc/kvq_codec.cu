@@ -39,7 +39,9 @@ __device__ __forceinline__ int items_of(const CodecArgs& a, const kvq_request& R
       const kvq_loop_ref& L = R.loop[a.loop];
       return a.H * k_groups_of((L.flags & KVQ_LOOP_K_TILE) != 0, L.n_rows, R.n_tokens);
     }
-    case kModeEncV: {
+    case kModeEncV:
+    case kModeNvAmax:
+    case kModeNvEnc: {  // one item per 64 stored rows (all heads)
       if (a.loop >= R.n_loops) return 0;
       int n = R.loop[a.loop].n_rows;
       return (n + kG - 1) / kG;
@@ -73,6 +75,12 @@ __global__ void __launch_bounds__(1024) items_plan_kernel(const __grid_constant_
   for (int base = 0; base < a.n_requests; base += blockDim.x) {
     int b = base + threadIdx.x;
     int v = b < a.n_requests ? items_of(a, req_at(a, b), mode) : 0;
+    if (mode == kModeNvAmax && v > 0) {  // the NVFP4 encoder's running max |delta| of this stream starts at 0
+      const kvq_loop_ref& L = req_at(a, b).loop[a.loop];
+      const bool nv = (L.flags & (a.kind == KVQ_K ? KVQ_LOOP_K_NVFP4 : KVQ_LOOP_V_NVFP4)) != 0;
+      float* rec = reinterpret_cast<float*>(a.kind == KVQ_K ? L.k_scales : L.v_scales);
+      if (nv && rec != nullptr) rec[1] = 0.0f;  // (an INT4 plane here is left alone; the encoder refuses it)
+    }
     int x = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -146,7 +154,11 @@ __device__ void fill_chain(const kvq_request& R, int kind, int n, int H, Chain& 
   C.kind = kind;
   C.n_tokens = R.n_tokens;
   C.n_heads = H;
-  for (int j = 0; j < n; ++j) planes_of(R, j, kind, C.loop[j]);
+  C.any_nvfp4 = 0;
+  for (int j = 0; j < n; ++j) {
+    planes_of(R, j, kind, C.loop[j]);
+    C.any_nvfp4 |= C.loop[j].fmt == KVQ_FMT_NVFP4;
+  }
 }
 
 __device__ __forceinline__ const uint16_t* source_of(const CodecArgs& a, int b) {
@@ -182,6 +194,10 @@ __global__ void __launch_bounds__(kD) encode_k_generic_kernel(const __grid_const
       cur_b = b;
     }
     __syncthreads();
+    if (C.loop[r].fmt != KVQ_FMT_INT4) {  // an NVFP4 output loop: not this kernel's format
+      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 64);
+      continue;
+    }
     const int local = int(it - prefix[b]);
     const int g = local / H, h = local % H;
     const LoopPlanes& O = C.loop[r];
@@ -277,6 +293,10 @@ __global__ void __launch_bounds__(kEncVThreads) encode_v_generic_kernel(const __
       cur_b = b;
     }
     __syncthreads();
+    if (C.loop[r].fmt != KVQ_FMT_INT4) {  // an NVFP4 output loop: not this kernel's format
+      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 64);
+      continue;
+    }
     const LoopPlanes& O = C.loop[r];
     const int n = O.n_rows;
     const int r0 = int(it - prefix[b]) * kG;
@@ -338,6 +358,109 @@ __global__ void __launch_bounds__(kEncVThreads) encode_v_generic_kernel(const __
         const_cast<uint16_t*>(O.mins)[pi] = f32_to_f16_bits(mn);
         const_cast<uint16_t*>(O.scales)[pi] = f32_to_f16_bits(s32);
       }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- NVFP4 residual encode (any depth)
+//
+// A residual loop in NVFP4 (INT4 codec PR review by 0z5a: E2M1 elements, one
+// E4M3 scale per 16 channels of a (row, head), one FP32 scale per stream). Two
+// passes over the stream's residual rows, both with item = 64 stored rows and a
+// warp per (row, head), lane = channels 4 lane .. 4 lane + 3 (four lanes form a
+// block): pass 1 (kAmax) takes max |delta| of the stream into word 1 of its
+// tensor-scale record (zeroed beforehand); pass 2 derives s_t from it, then each
+// block's E4M3 scale and the E2M1 codes. The residual is recomputed in pass 2
+// rather than stored. IEEE divisions, as the format's definition states them.
+
+template <bool kAmax>
+__global__ void __launch_bounds__(kEncVThreads) nvfp4_encode_kernel(const __grid_constant__ CodecArgs a,
+                                                                   const int32_t* prefix_ws) {
+  const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kWarps = kEncVThreads / 32;
+  const int H = a.H;
+  const int r = a.loop;
+  __shared__ Chain C;
+  __shared__ int s_tok[kG];
+  __shared__ int s_row[KVQ_MAX_LOOPS][kG];
+  __shared__ int s_b;
+
+  const ItemRange ir = cta_items(prefix, a.n_requests);
+  int cur_b = -1;
+  for (long long it = ir.begin; it < ir.end; ++it) {
+    if (threadIdx.x == 0) s_b = owner_of(prefix, a.n_requests, it);
+    __syncthreads();
+    const int b = s_b;
+    if (b != cur_b) {
+      if (threadIdx.x == 0) fill_chain(req_at(a, b), a.kind, r + 1, H, C);
+      cur_b = b;
+    }
+    __syncthreads();
+    const LoopPlanes& O = C.loop[r];
+    if (r < 1 || O.fmt != KVQ_FMT_NVFP4) {  // the table does not hold an NVFP4 residual here
+      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 64);
+      continue;
+    }
+    const int n = O.n_rows;
+    const int r0 = int(it - prefix[b]) * kG;
+    const int len = min(kG, n - r0);
+    const uint16_t* x = source_of(a, b);
+    if (threadIdx.x < len) {
+      int t = O.sparse ? __ldg(O.active + r0 + threadIdx.x) : r0 + threadIdx.x;
+      s_tok[threadIdx.x] = t;
+      for (int j = 0; j < r; ++j) s_row[j][threadIdx.x] = row_of(C.loop[j], t);
+    }
+    __syncthreads();
+    float* rec = reinterpret_cast<float*>(const_cast<uint16_t*>(O.scales));
+    float st = 0.0f, six_st = 0.0f;
+    bool all_zero = true;
+    if (!kAmax) {
+      const float amax = rec[1];
+      all_zero = !(amax > 0.0f);
+      st = __fdiv_rn(amax, 2688.0f);  // 6 * 448: the largest block scale times the largest E2M1 value
+      six_st = __fmul_rn(6.0f, st);
+    }
+    float tmax = 0.0f;
+    for (int p = warp; p < len * H; p += kWarps) {
+      const int i = p / H, h = p % H;
+      const int t = s_tok[i];
+      const int c0 = lane * 4;
+      const uint2 raw = *reinterpret_cast<const uint2*>(x + ((long long)t * H + h) * kD + c0);
+      const float xv[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                           __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+      int rows[KVQ_MAX_LOOPS];
+      for (int j = 0; j < r; ++j) rows[j] = s_row[j][i];
+      float xh[4], v[4];
+      chain4(C, r, rows, t, h, c0, xh);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = round_bf16(__fsub_rn(xv[e], xh[e]));
+      float ab = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+      if (kAmax) {
+        tmax = fmaxf(tmax, ab);
+        continue;
+      }
+      ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 1));  // the block's four lanes
+      ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 2));
+      const uint32_t sb = all_zero ? 0u : f32_to_e4m3(__fdiv_rn(ab, six_st));
+      const float eb = __fmul_rn(e4m3_to_f32(sb), st);
+      uint32_t packed = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) packed |= (eb == 0.0f ? 0u : f32_to_e2m1(__fdiv_rn(v[e], eb))) << (4 * e);
+      const long long row = r0 + i;
+      *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(O.codes) + ((long long)h * n + row) * kRowBytes + lane * 2) =
+          uint16_t(packed);
+      if ((lane & 3) == 0)
+        reinterpret_cast<uint8_t*>(const_cast<uint16_t*>(O.mins))[((long long)h * n + row) * (kD / 16) + (lane >> 2)] =
+            uint8_t(sb);
+    }
+    if (kAmax) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+      if (lane == 0 && tmax > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(rec + 1), __float_as_uint(tmax));
+    } else if (r0 == 0 && threadIdx.x == 0) {
+      rec[0] = st;  // the stream's tensor scale, once
     }
     __syncthreads();
   }
@@ -657,6 +780,10 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
       S.ghi[tid] = -1;
     }
     __syncthreads();
+    if (S.C.any_nvfp4) {  // NVFP4 loops: the INT4-only fast path refuses the request
+      if (tid == 0 && a.err) atomicOr(a.err, 64);
+      continue;
+    }
     const int local = int(it - prefix[b]);
     const int g = local / H, h = local % H;
     const LoopPlanes& O = S.C.loop[R];
@@ -857,6 +984,10 @@ __global__ void __launch_bounds__(kEncVFastThreads) encode_v_fast_kernel(const _
       cur_b = b;
     }
     __syncthreads();
+    if (C.any_nvfp4) {  // NVFP4 loops: the INT4-only fast path refuses the request
+      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 64);
+      continue;
+    }
     const LoopPlanes& O = C.loop[R];
     const int n = O.n_rows;
     const int r0 = int(it - prefix[b]) * kG;
@@ -1071,6 +1202,10 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
       __syncthreads();
       cur_b = b;
     }
+    if (C.any_nvfp4) {  // NVFP4 loops: the INT4-only fast path refuses the request
+      if (tid == 0 && a.err) atomicOr(a.err, 64);
+      continue;
+    }
     const int local = int(it - prefix[b]);
     const int k = local / H, h = local % H;
     const int t0 = k * KVQ_TILE;
@@ -1160,6 +1295,10 @@ __global__ void __launch_bounds__(kReconVFastThreads) reconstruct_v_fast_kernel(
       __syncthreads();
       cur_b = b;
     }
+    if (C.any_nvfp4) {  // NVFP4 loops: the INT4-only fast path refuses the request
+      if (tid == 0 && a.err) atomicOr(a.err, 64);
+      continue;
+    }
     const int k = int(it - prefix[b]);
     const int t0 = k * KVQ_TILE;
     const int nvalid = min(KVQ_TILE, C.n_tokens - t0);
@@ -1221,6 +1360,8 @@ static int single_items(const CodecArgs& a, int mode) {
   const kvq_request& R = a.one;
   const int n = R.loop[a.loop < KVQ_MAX_LOOPS ? a.loop : 0].n_rows;
   switch (mode) {
+    case kModeNvAmax:
+    case kModeNvEnc: return (n + kG - 1) / kG;
     case kModeEncK: {
       const kvq_loop_ref& L = R.loop[a.loop < KVQ_MAX_LOOPS ? a.loop : 0];
       return a.H * k_groups_of((L.flags & KVQ_LOOP_K_TILE) != 0, n, R.n_tokens);
@@ -1234,8 +1375,16 @@ static int single_items(const CodecArgs& a, int mode) {
 
 cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, int sms, cudaStream_t stream) {
   CodecArgs a = a_in;
-  // K reconstruction of chains up to 4 loops runs one item per (tile, head)
-  if (mode == kModeRecon && a.kind == KVQ_K && a.loop >= 1 && a.loop <= kFastMaxDepth) mode = kModeReconK;
+  // NVFP4 loops (bit j of a.nvfp4: loop j): an NVFP4 output loop takes the two
+  // NVFP4 passes; an INT4 output loop or a reconstruction whose chain holds an
+  // NVFP4 loop takes the any-depth kernels, which decode either format.
+  const uint32_t below = a.loop >= 32 ? 0xFFFFFFFFu : ((1u << a.loop) - 1u);  // loops 0 .. loop-1
+  const bool nv_out = (mode == kModeEncK || mode == kModeEncV) && a.loop < 32 && ((a.nvfp4 >> a.loop) & 1u);
+  const bool nv_chain = (a.nvfp4 & below) != 0;
+  if (nv_out) mode = kModeNvAmax;
+  // K reconstruction of INT4 chains up to 4 loops runs one item per (tile, head)
+  if (mode == kModeRecon && a.kind == KVQ_K && a.loop >= 1 && a.loop <= kFastMaxDepth && !nv_chain)
+    mode = kModeReconK;
   const int32_t* prefix = nullptr;  // nullptr: kernels read a.one_prefix
   long long items = -1;             // -1: known only on the device
   if (a.reqs == nullptr) {
@@ -1267,8 +1416,13 @@ cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, in
     kern<<<grid_for(4 * per_sm), threads, 0, stream>>>(a, prefix);
   };
   switch (mode) {
+    case kModeNvAmax:
+      nvfp4_encode_kernel<true><<<grid_for(4), kEncVThreads, 0, stream>>>(a, prefix);
+      count_launch();
+      nvfp4_encode_kernel<false><<<grid_for(4), kEncVThreads, 0, stream>>>(a, prefix);
+      break;
     case kModeEncK:
-      switch (a.loop) {
+      switch (nv_chain ? -1 : a.loop) {
         case 0: run(encode_k_fast_kernel<0>, kEncKThreads); break;
         case 1: run(encode_k_fast_kernel<1>, kEncKThreads); break;
         case 2: run(encode_k_fast_kernel<2>, kEncKThreads); break;
@@ -1277,7 +1431,7 @@ cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, in
       }
       break;
     case kModeEncV:
-      switch (a.loop) {
+      switch (nv_chain ? -1 : a.loop) {
         case 0: run(encode_v_fast_kernel<0>, kEncVFastThreads); break;
         case 1: run(encode_v_fast_kernel<1>, kEncVFastThreads); break;
         case 2: run(encode_v_fast_kernel<2>, kEncVFastThreads); break;
@@ -1300,7 +1454,7 @@ cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, in
       }
       break;
     default:
-      if (a.kind == KVQ_V && a.loop >= 1 && a.loop <= kFastMaxDepth) {
+      if (a.kind == KVQ_V && a.loop >= 1 && a.loop <= kFastMaxDepth && !nv_chain) {
         switch (a.loop) {
           case 1: run(reconstruct_v_fast_kernel<1>, kReconVFastThreads); break;
           case 2: run(reconstruct_v_fast_kernel<2>, kReconVFastThreads); break;

@@ -26,11 +26,13 @@ struct LoopPlanes {
   int32_t sparse;
   int32_t ktile;    // K groups by 64-token logical tile (KVQ_KGROUP_TILE) instead of 64 stored rows
   int32_t kgroups;  // K groups per head: ceil(n_tokens/64) if ktile, else ceil(n_rows/64)
+  int32_t fmt;      // KVQ_FMT_INT4 or KVQ_FMT_NVFP4
+  int32_t pad;
   const int32_t* active;
   const int32_t* tile_dir;
   const uint8_t* codes;
-  const uint16_t* mins;
-  const uint16_t* scales;
+  const uint16_t* mins;    // INT4 (NVFP4: the E4M3 block scales, as bytes)
+  const uint16_t* scales;  // INT4 (NVFP4: the tensor-scale record, as floats)
 };
 
 struct Chain {
@@ -38,8 +40,63 @@ struct Chain {
   int32_t kind;
   int32_t n_tokens;
   int32_t n_heads;
+  int32_t any_nvfp4;  // some loop of the chain is NVFP4 (the INT4-only kernels refuse it)
+  int32_t pad[3];
   LoopPlanes loop[KVQ_MAX_LOOPS];
 };
+
+// ---- NVFP4 element and scale types, written from the format definitions
+// (codec PR review by 0z5a: E2M1 round-to-nearest-even, E4M3 scale rounding).
+
+// E4M3 (finite variant: bias 7, subnormals m * 2^-9, largest 448) to FP32.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  const uint32_t E = (b >> 3) & 15u, M = b & 7u;
+  const float mag = E ? __uint_as_float(((E + 120u) << 23) | (M << 20)) : float(M) * 0.001953125f;
+  return (b & 0x80u) ? -mag : mag;
+}
+
+// E4M3 byte of v >= 0: round to nearest even (three mantissa bits), saturating at 448.
+__device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
+  if (!(v < 448.0f)) return 0x7Eu;
+  if (v < 0.015625f) {  // below 2^-6: a multiple of 2^-9 (v * 512 < 8 is exact; adding 2^23 rounds it)
+    const float m = __fsub_rn(__fadd_rn(__fmul_rn(v, 512.0f), 8388608.0f), 8388608.0f);
+    return m >= 8.0f ? 0x08u : uint32_t(m);
+  }
+  uint32_t u = __float_as_uint(v);
+  u += 0x7FFFFu + ((u >> 20) & 1u);  // ties to even at the third mantissa bit; a carry bumps the exponent
+  u &= 0xFFF00000u;
+  return (((u >> 23) - 120u) << 3) | ((u >> 20) & 7u);
+}
+
+// E2M1 nibble (sign in bit 3; magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6) to FP32.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t n) {
+  const uint32_t c = n & 7u;
+  const float mag = c >= 2u ? __uint_as_float((((c >> 1) + 126u) << 23) | ((c & 1u) << 22)) : 0.5f * float(c);
+  return (n & 8u) ? -mag : mag;
+}
+
+// E2M1 nibble of y: the nearest magnitude (ties to the even code, i.e. to the
+// even mantissa), saturating at 6, with the sign bit of y.
+__device__ __forceinline__ uint32_t f32_to_e2m1(float y) {
+  const float a = fabsf(y);
+  const uint32_t c = uint32_t(a > 0.25f) + uint32_t(a >= 0.75f) + uint32_t(a > 1.25f) + uint32_t(a >= 1.75f) +
+                     uint32_t(a > 2.5f) + uint32_t(a >= 3.5f) + uint32_t(a > 5.0f);
+  return c | ((__float_as_uint(y) >> 28) & 8u);
+}
+
+// One NVFP4 element in FP32: RN32(RN32(e2m1 * s_b) * s_t), the inner product exact.
+__device__ __forceinline__ float nvfp4_dequant(uint32_t nib, float sb, float st) {
+  return __fmul_rn(__fmul_rn(e2m1_to_f32(nib), sb), st);
+}
+
+// NVFP4 planes of a loop: E4M3 block scale of (head h, stored row, block of 16
+// channels) and the tensor scale.
+__device__ __forceinline__ float nvfp4_block_scale(const LoopPlanes& L, int h, int row, int blk) {
+  return e4m3_to_f32(__ldg(reinterpret_cast<const uint8_t*>(L.mins) + ((long long)h * L.n_rows + row) * (kD / 16) + blk));
+}
+__device__ __forceinline__ float nvfp4_tensor_scale(const LoopPlanes& L) {
+  return __ldg(reinterpret_cast<const float*>(L.scales));
+}
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
@@ -96,6 +153,7 @@ __device__ __forceinline__ void planes_of(const kvq_request& R, int j, int kind,
   P.sparse = L.active_idx != nullptr;
   P.ktile = kind == KVQ_K && (L.flags & KVQ_LOOP_K_TILE) != 0;
   P.kgroups = k_groups_of(P.ktile != 0, L.n_rows, R.n_tokens);
+  P.fmt = (L.flags & (kind == KVQ_K ? KVQ_LOOP_K_NVFP4 : KVQ_LOOP_V_NVFP4)) ? KVQ_FMT_NVFP4 : KVQ_FMT_INT4;
   P.active = L.active_idx;
   P.tile_dir = L.tile_dir;
   P.codes = kind == KVQ_K ? L.k_codes : L.v_codes;
@@ -123,6 +181,13 @@ __device__ __forceinline__ void chain4(const Chain& C, int depth, const int* row
     if (row < 0) continue;  // absent: inherit the predecessor
     const LoopPlanes& L = C.loop[j];
     uint16_t two = *reinterpret_cast<const uint16_t*>(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + c0 / 2);
+    if (L.fmt == KVQ_FMT_NVFP4) {  // the four channels share one 16-channel block
+      const float sb = nvfp4_block_scale(L, h, row, c0 / 16), st = nvfp4_tensor_scale(L);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        out[e] = round_bf16(__fadd_rn(out[e], round_bf16(nvfp4_dequant((two >> (4 * e)) & 0xF, sb, st))));
+      continue;
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       int c = (two >> (4 * e)) & 0xF;
@@ -145,6 +210,15 @@ __device__ __forceinline__ void chain4_f32(const Chain& C, int depth, const int*
     if (row < 0) continue;
     const LoopPlanes& L = C.loop[j];
     uint16_t two = *reinterpret_cast<const uint16_t*>(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + c0 / 2);
+    if (L.fmt == KVQ_FMT_NVFP4) {
+      const float sb = nvfp4_block_scale(L, h, row, c0 / 16), st = nvfp4_tensor_scale(L);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float dq = nvfp4_dequant((two >> (4 * e)) & 0xF, sb, st);
+        out[e] = (j == 0) ? dq : __fadd_rn(out[e], dq);
+      }
+      continue;
+    }
     float mn[4], sc[4];
     if (C.kind == KVQ_K) {
       const long long pi = param_index(KVQ_K, L, h, t, row, c0);
@@ -191,6 +265,11 @@ __device__ __forceinline__ float chain1(const Chain& C, int depth, const int* ro
     const LoopPlanes& L = C.loop[j];
     uint8_t byte = __ldg(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + d / 2);
     int c = (d & 1) ? (byte >> 4) : (byte & 0xF);
+    if (L.fmt == KVQ_FMT_NVFP4) {
+      v = round_bf16(__fadd_rn(v, round_bf16(nvfp4_dequant(c, nvfp4_block_scale(L, h, row, d / 16),
+                                                           nvfp4_tensor_scale(L)))));
+      continue;
+    }
     long long pi = param_index(C.kind, L, h, t, row, d);
     v = round_bf16(__fadd_rn(v, dequant(__ldg(L.mins + pi), __ldg(L.scales + pi), c)));
   }
@@ -200,7 +279,8 @@ __device__ __forceinline__ float chain1(const Chain& C, int depth, const int* ro
 // Number of kernels this library has launched in the process (host counter).
 void count_launch();
 
-enum { kModeEncK = 0, kModeEncV = 1, kModeTileDir = 2, kModeRecon = 3, kModeReconK = 4 };
+enum { kModeEncK = 0, kModeEncV = 1, kModeTileDir = 2, kModeRecon = 3, kModeReconK = 4, kModeNvAmax = 5,
+       kModeNvEnc = 6 };
 
 // Arguments of the codec kernels: either a batch described by a device table of
 // requests, or one request carried by value in the kernel parameters.
@@ -213,6 +293,7 @@ struct CodecArgs {
   int32_t H;
   int32_t kind;
   int32_t loop;              // encode and tile directory: loop written; reconstruct: depth
+  uint32_t nvfp4;            // bit j: loop j of `kind` is NVFP4 in every request
   kvq_request one;
   const uint16_t* one_x;
   uint16_t* one_out;

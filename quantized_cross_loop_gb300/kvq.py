@@ -26,8 +26,10 @@ KVQ_MAX_LOOPS = 8
 KVQ_FORMAT_VERSION = 1
 PLANE_CODES, PLANE_MINS, PLANE_SCALES, PLANE_INDEX, PLANE_TILE_DIR = range(5)
 ATTN_AUTO, ATTN_SIMT, ATTN_MMA = 0, 1, 2
+ATTN_NVFP4 = 8  # OR-ed into algo: the table may hold NVFP4 residual loops
 KVQ_KGROUP_COMPACT, KVQ_KGROUP_TILE = 0, 1  # K groups: 64 stored rows / the stored rows of one 64-token tile
-KVQ_LOOP_K_TILE = 1
+KVQ_LOOP_K_TILE, KVQ_LOOP_K_NVFP4, KVQ_LOOP_V_NVFP4 = 1, 2, 4
+KVQ_FMT_INT4, KVQ_FMT_NVFP4 = 0, 1  # residual formats: affine INT4 / E2M1 + E4M3 per 16 + FP32 per stream
 
 EXPORTED = (
     "kvq_stream_init", "kvq_plane_bytes", "kvq_stream_payload_bytes", "kvq_encode_base", "kvq_encode_residual",
@@ -35,7 +37,8 @@ EXPORTED = (
     "kvq_decode_attn_packed", "kvq_decode_attn_packed_ex", "kvq_status_string", "kvq_last_error", "kvq_version",
     "kvq_batch_workspace_bytes", "kvq_encode_batch", "kvq_reconstruct_batch", "kvq_launch_count",
     "kvq_decode_attn_packed_noalloc", "kvq_sparse_workspace_bytes", "kvq_sparse_ref_state",
-    "kvq_sparse_decode_attn", "kvq_stream_payload_bytes_ex",
+    "kvq_sparse_decode_attn", "kvq_stream_payload_bytes_ex", "kvq_stream_set_format", "kvq_encode_batch_ex",
+    "kvq_reconstruct_batch_ex",
 )
 
 
@@ -51,7 +54,8 @@ class kvq_stream(ctypes.Structure):
         ("group", ctypes.c_uint16),
         ("nibble_order", ctypes.c_uint8),
         ("kgroup", ctypes.c_uint8),
-        ("reserved", ctypes.c_uint8 * 2),
+        ("format", ctypes.c_uint8),
+        ("reserved", ctypes.c_uint8),
         ("n_rows", ctypes.c_int32),
         ("n_tokens", ctypes.c_int32),
         ("n_heads", ctypes.c_int32),
@@ -112,7 +116,8 @@ def lib():
             L.kvq_plane_bytes.restype = sz
             L.kvq_stream_payload_bytes.argtypes = [i32, i32, i32, i32, i32]
             L.kvq_stream_payload_bytes.restype = ctypes.c_int64
-            L.kvq_stream_payload_bytes_ex.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.kvq_stream_payload_bytes_ex.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+            L.kvq_stream_set_format.argtypes = [P(kvq_stream), i32]
             L.kvq_stream_payload_bytes_ex.restype = ctypes.c_int64
             L.kvq_encode_base.argtypes = [vp, P(kvq_stream), vp]
             L.kvq_encode_residual.argtypes = [vp, P(kvq_stream), i32, P(kvq_stream), vp]
@@ -139,9 +144,12 @@ def lib():
             L.kvq_batch_workspace_bytes.restype = sz
             L.kvq_encode_batch.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, sz, vp]
             L.kvq_reconstruct_batch.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, sz, vp]
+            L.kvq_encode_batch_ex.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_uint32, vp, sz, vp]
+            L.kvq_reconstruct_batch_ex.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_uint32, vp, sz, vp]
             for name in ("kvq_stream_init", "kvq_encode_base", "kvq_encode_residual", "kvq_build_tile_dir",
                          "kvq_reconstruct", "kvq_request_fill", "kvq_decode_attn_packed",
-                         "kvq_decode_attn_packed_ex", "kvq_encode_batch", "kvq_reconstruct_batch"):
+                         "kvq_decode_attn_packed_ex", "kvq_encode_batch", "kvq_reconstruct_batch",
+                         "kvq_stream_set_format", "kvq_encode_batch_ex", "kvq_reconstruct_batch_ex"):
                 getattr(L, name).restype = ctypes.c_int32
             _lib = L
     return _lib
@@ -176,13 +184,15 @@ class Stream:
     the C descriptor pointing at them."""
 
     def __init__(self, kind: int, n_rows: int, n_tokens: int, n_heads: int, head_dim: int, device,
-                 active: torch.Tensor | None = None, alloc=None, shared_index=None, kgroup: int = KVQ_KGROUP_COMPACT):
+                 active: torch.Tensor | None = None, alloc=None, shared_index=None, kgroup: int = KVQ_KGROUP_COMPACT,
+                 fmt: int = KVQ_FMT_INT4):
         self.desc = kvq_stream()
         _check(lib().kvq_stream_init(ctypes.byref(self.desc), kind, n_rows, n_tokens, n_heads, head_dim),
                "kvq_stream_init")
         self.desc.kgroup = kgroup
+        _check(lib().kvq_stream_set_format(ctypes.byref(self.desc), fmt), "kvq_stream_set_format")
         self.kind, self.n_rows, self.n_tokens, self.n_heads, self.head_dim = kind, n_rows, n_tokens, n_heads, head_dim
-        self.kgroup = kgroup
+        self.kgroup, self.fmt = kgroup, fmt
 
         def plane(p):
             nbytes = int(lib().kvq_plane_bytes(ctypes.byref(self.desc), p))
@@ -218,6 +228,8 @@ class Stream:
                                                                                   self.head_dim // 2)
 
     def param_shape(self):
+        if self.fmt == KVQ_FMT_NVFP4:  # E4M3 block scales (bytes)
+            return (self.n_heads, self.n_rows, self.head_dim // 16)
         if self.kind == KVQ_K:
             groups = -(-self.n_rows // KVQ_GROUP)
             if self.kgroup == KVQ_KGROUP_TILE and self.n_rows > 0:
@@ -226,10 +238,16 @@ class Stream:
         return (self.n_heads, self.n_rows, -(-self.head_dim // KVQ_GROUP))
 
     def mins_view(self):
+        """INT4: FP16 mins (int16 bits); NVFP4: the E4M3 block scales (uint8 bits)."""
         shp = self.param_shape()
+        if self.fmt == KVQ_FMT_NVFP4:
+            return self.mins[: math.prod(shp)].view(shp)
         return self.mins.view(torch.int16)[: math.prod(shp)].view(shp)
 
     def scales_view(self):
+        """INT4: FP16 scales (int16 bits); NVFP4: the tensor scale (float32 [1])."""
+        if self.fmt == KVQ_FMT_NVFP4:
+            return self.scales.view(torch.float32)[:1]
         shp = self.param_shape()
         return self.scales.view(torch.int16)[: math.prod(shp)].view(shp)
 
@@ -243,11 +261,11 @@ class Stream:
 
 
 def payload_bytes(kind: int, n_rows: int, n_heads: int, head_dim: int, sparse: bool, n_tokens: int | None = None,
-                  kgroup: int = KVQ_KGROUP_COMPACT) -> int:
-    if n_tokens is None and kgroup == KVQ_KGROUP_COMPACT:
+                  kgroup: int = KVQ_KGROUP_COMPACT, fmt: int = KVQ_FMT_INT4) -> int:
+    if n_tokens is None and kgroup == KVQ_KGROUP_COMPACT and fmt == KVQ_FMT_INT4:
         return int(lib().kvq_stream_payload_bytes(kind, n_rows, n_heads, head_dim, int(sparse)))
     T = n_rows if n_tokens is None else n_tokens
-    return int(lib().kvq_stream_payload_bytes_ex(kind, n_rows, T, n_heads, head_dim, int(sparse), kgroup))
+    return int(lib().kvq_stream_payload_bytes_ex(kind, n_rows, T, n_heads, head_dim, int(sparse), kgroup, fmt))
 
 
 def kvq_encode_base(x: torch.Tensor, kind: int, stream=None, kgroup: int = KVQ_KGROUP_COMPACT) -> Stream:
@@ -261,15 +279,16 @@ def kvq_encode_base(x: torch.Tensor, kind: int, stream=None, kgroup: int = KVQ_K
 
 
 def kvq_encode_residual(x_r: torch.Tensor, prev: list, active: torch.Tensor | None = None, stream=None,
-                        kgroup: int | None = None) -> Stream:
+                        kgroup: int | None = None, fmt: int = KVQ_FMT_INT4) -> Stream:
     """Encode loop len(prev)+1 of the chain `prev` from BF16 x_r [T, H, D];
     `active` (sorted int32 logical rows) makes it a compact sparse residual.
-    `kgroup` (K only): KVQ_KGROUP_COMPACT or KVQ_KGROUP_TILE; default: the base's."""
+    `kgroup` (K only): KVQ_KGROUP_COMPACT or KVQ_KGROUP_TILE; default: the base's.
+    `fmt`: KVQ_FMT_INT4 or KVQ_FMT_NVFP4 for this residual."""
     _require_cuda(x_r, "x_r", torch.bfloat16)
     T, H, D = x_r.shape
     kind = prev[0].kind
     n = T if active is None else int(active.numel())
-    out = Stream(kind, n, T, H, D, x_r.device, active, kgroup=prev[0].kgroup if kgroup is None else kgroup)
+    out = Stream(kind, n, T, H, D, x_r.device, active, kgroup=prev[0].kgroup if kgroup is None else kgroup, fmt=fmt)
     arr = (kvq_stream * len(prev))(*[p.desc for p in prev])
     _check(lib().kvq_encode_residual(_dptr(x_r), arr, len(prev), ctypes.byref(out.desc), _stream_handle(stream)),
            "kvq_encode_residual")
@@ -325,6 +344,8 @@ class RequestTable:
             device = k_chains[0][0].codes.device if n else torch.device("cuda")
         self.table = torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(device)
         self.n_requests = n
+        self.has_nvfp4 = any(getattr(st, "fmt", KVQ_FMT_INT4) == KVQ_FMT_NVFP4
+                             for chains in (k_chains, v_chains) for ch in chains for st in ch)
         self._keep = (k_chains, v_chains, keep)
 
 
@@ -348,6 +369,8 @@ def kvq_decode_attn_packed(table: RequestTable, q: torch.Tensor, depth: int, n_h
     need = kvq_decode_attn_workspace_bytes(B, n_heads, Hq, D)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if table.has_nvfp4:
+        algo |= ATTN_NVFP4
     _check(lib().kvq_decode_attn_packed_ex(_dptr(table.table), B, n_heads, Hq, D, depth, _dptr(q),
                                            ctypes.c_float(softmax_scale), _dptr(out), _dptr(workspace),
                                            workspace.numel(), algo, _stream_handle(stream)),
@@ -356,10 +379,11 @@ def kvq_decode_attn_packed(table: RequestTable, q: torch.Tensor, depth: int, n_h
 
 
 def plane_bytes(kind: int, n_rows: int, n_tokens: int, n_heads: int, head_dim: int,
-                kgroup: int = KVQ_KGROUP_COMPACT) -> list:
+                kgroup: int = KVQ_KGROUP_COMPACT, fmt: int = KVQ_FMT_INT4) -> list:
     d = kvq_stream()
     _check(lib().kvq_stream_init(ctypes.byref(d), kind, n_rows, n_tokens, n_heads, head_dim), "kvq_stream_init")
     d.kgroup = kgroup
+    _check(lib().kvq_stream_set_format(ctypes.byref(d), fmt), "kvq_stream_set_format")
     return [int(lib().kvq_plane_bytes(ctypes.byref(d), p)) for p in range(5)]
 
 
@@ -370,14 +394,20 @@ class PackedPool:
 
     active_sets[b][r] is the sorted int32 active set of loop r of request b, or
     None for a dense loop (loop 0 must be dense). kgroup: the K grouping of
-    every K stream (KVQ_KGROUP_COMPACT or KVQ_KGROUP_TILE)."""
+    every K stream (KVQ_KGROUP_COMPACT or KVQ_KGROUP_TILE). formats[r]: the
+    format of loop r of K and V in every request (KVQ_FMT_INT4 default;
+    KVQ_FMT_NVFP4 for residual loops r >= 1)."""
 
     ALIGN = 256
 
     def __init__(self, lengths: list, active_sets: list, n_heads: int, head_dim: int, n_loops: int, device,
-                 kgroup: int = KVQ_KGROUP_COMPACT):
+                 kgroup: int = KVQ_KGROUP_COMPACT, formats: list | None = None):
         device = torch.device(device)
         self.kgroup = kgroup
+        self.formats = [KVQ_FMT_INT4] * n_loops if formats is None else list(formats)
+        if self.formats[0] != KVQ_FMT_INT4:
+            raise KvqError("the base loop is INT4")
+        self.nvfp4_mask = sum(1 << r for r, f in enumerate(self.formats) if f == KVQ_FMT_NVFP4)
         self.lengths = list(lengths)
         self.n_heads, self.head_dim, self.n_loops = n_heads, head_dim, n_loops
         # pass 1: sizes
@@ -388,8 +418,9 @@ class PackedPool:
             for r in range(n_loops):
                 act = active_sets[b][r]
                 n = T if act is None else int(act.numel())
-                k = plane_bytes(KVQ_K, n, T, n_heads, head_dim, kgroup)
-                v = plane_bytes(KVQ_V, n, T, n_heads, head_dim)
+                fm = self.formats[r]
+                k = plane_bytes(KVQ_K, n, T, n_heads, head_dim, kgroup, fm)
+                v = plane_bytes(KVQ_V, n, T, n_heads, head_dim, KVQ_KGROUP_COMPACT, fm)
                 per.append((n, k, v, act is not None))
                 total += sum(self._up(x) for x in k[:3]) + sum(self._up(x) for x in v[:3])
                 if act is not None:
@@ -409,11 +440,13 @@ class PackedPool:
                     idx = self._take(kb[PLANE_INDEX])
                     idx.view(torch.int32)[:n].copy_(active_sets[b][r].to(device=device, dtype=torch.int32))
                     shared = (idx, self._take(kb[PLANE_TILE_DIR]))
+                fm = self.formats[r]
                 ks.append(Stream(KVQ_K, n, T, n_heads, head_dim, device, alloc=self._take, shared_index=shared,
-                                 kgroup=kgroup))
-                vs.append(Stream(KVQ_V, n, T, n_heads, head_dim, device, alloc=self._take, shared_index=shared))
-                self.payload_bytes += payload_bytes(KVQ_K, n, n_heads, head_dim, sparse, T, kgroup)
-                self.payload_bytes += payload_bytes(KVQ_V, n, n_heads, head_dim, False)
+                                 kgroup=kgroup, fmt=fm))
+                vs.append(Stream(KVQ_V, n, T, n_heads, head_dim, device, alloc=self._take, shared_index=shared,
+                                 fmt=fm))
+                self.payload_bytes += payload_bytes(KVQ_K, n, n_heads, head_dim, sparse, T, kgroup, fm)
+                self.payload_bytes += payload_bytes(KVQ_V, n, n_heads, head_dim, False, T, KVQ_KGROUP_COMPACT, fm)
             self.k_streams.append(ks)
             self.v_streams.append(vs)
         self.table = RequestTable(self.k_streams, self.v_streams, device)
@@ -445,16 +478,17 @@ def kvq_encode_batch(pool: PackedPool, kind: int, loop: int, x_ptrs: torch.Tenso
     may run concurrently (on different streams) need their own `workspace`
     (kvq_batch_workspace_bytes(n_requests) bytes); the default is the pool's."""
     ws = pool.workspace if workspace is None else workspace
-    _check(lib().kvq_encode_batch(_dptr(pool.table.table), pool.n_requests, pool.n_heads, pool.head_dim, kind, loop,
-                                  _dptr(x_ptrs), _dptr(ws), ws.numel(), _stream_handle(stream)), "kvq_encode_batch")
+    _check(lib().kvq_encode_batch_ex(_dptr(pool.table.table), pool.n_requests, pool.n_heads, pool.head_dim, kind,
+                                     loop, _dptr(x_ptrs), pool.nvfp4_mask, _dptr(ws), ws.numel(),
+                                     _stream_handle(stream)), "kvq_encode_batch")
 
 
 def kvq_reconstruct_batch(pool: PackedPool, kind: int, depth: int, out_ptrs: torch.Tensor, stream=None,
                           workspace: torch.Tensor | None = None):
     ws = pool.workspace if workspace is None else workspace
-    _check(lib().kvq_reconstruct_batch(_dptr(pool.table.table), pool.n_requests, pool.n_heads, pool.head_dim, kind,
-                                       depth, _dptr(out_ptrs), _dptr(ws), ws.numel(), _stream_handle(stream)),
-           "kvq_reconstruct_batch")
+    _check(lib().kvq_reconstruct_batch_ex(_dptr(pool.table.table), pool.n_requests, pool.n_heads, pool.head_dim,
+                                          kind, depth, _dptr(out_ptrs), pool.nvfp4_mask, _dptr(ws), ws.numel(),
+                                          _stream_handle(stream)), "kvq_reconstruct_batch")
 
 
 def launch_count() -> int:

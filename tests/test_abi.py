@@ -87,8 +87,18 @@ def test_plane_sizes_and_payload(L):
                 assert L.kvq_stream_payload_bytes(kind, n, 8, 128, sparse) == O.stream_bytes(kind, n, 8, 128,
                                                                                                sparse=bool(sparse))
                 # and under tile grouping of K (ceil(T/64) groups of a sparse stream)
-                assert L.kvq_stream_payload_bytes_ex(kind, n, T, 8, 128, sparse, kvq.KVQ_KGROUP_TILE) == \
+                assert L.kvq_stream_payload_bytes_ex(kind, n, T, 8, 128, sparse, kvq.KVQ_KGROUP_TILE,
+                                                     kvq.KVQ_FMT_INT4) == \
                     O.stream_bytes(kind, n, 8, 128, sparse=bool(sparse), T=T, kgroup=O.KGROUP_TILE)
+                # and for an NVFP4 residual stream
+                assert L.kvq_stream_payload_bytes_ex(kind, n, T, 8, 128, sparse, kvq.KVQ_KGROUP_COMPACT,
+                                                     kvq.KVQ_FMT_NVFP4) == O.stream_bytes_nvfp4(n, 8, 128, bool(sparse))
+            nv = kvq.kvq_stream()
+            assert L.kvq_stream_init(ctypes.byref(nv), kind, n, T, 8, 128) == 0
+            assert L.kvq_stream_set_format(ctypes.byref(nv), kvq.KVQ_FMT_NVFP4) == 0 and nv.group == 16
+            assert L.kvq_plane_bytes(ctypes.byref(nv), 1) == -(-(8 * n * 8) // 16) * 16  # E4M3 per 16 channels
+            assert L.kvq_plane_bytes(ctypes.byref(nv), 2) == 16                          # tensor-scale record
+            assert L.kvq_stream_set_format(ctypes.byref(nv), 7) == -1
             s.kgroup = kvq.KVQ_KGROUP_TILE
             groups = (-(-T // 64) if n > 0 else 0) if kind == kvq.KVQ_K else None
             if groups is not None:
@@ -134,6 +144,22 @@ def test_host_validation_rejects_bad_arguments(L):
     prev[0].active_idx, prev[0].n_rows, prev[0].tile_dir = None, 64, None
     out.active_idx, out.n_rows = 64, 32
     assert L.kvq_encode_residual(ctypes.c_void_p(64), prev, 1, ctypes.byref(out), None) == BAD
+    # NVFP4 is a residual format: the base refuses it, and so does a chain whose base carries it
+    out.active_idx, out.n_rows = None, 64
+    nv = _stream(L)
+    nv.codes, nv.mins, nv.scales = 16, 32, 48
+    assert L.kvq_stream_set_format(ctypes.byref(nv), kvq.KVQ_FMT_NVFP4) == 0
+    assert L.kvq_encode_base(ctypes.c_void_p(64), ctypes.byref(nv), None) == UNSUP
+    nvprev = (kvq.kvq_stream * 1)(nv)
+    assert L.kvq_encode_residual(ctypes.c_void_p(64), nvprev, 1, ctypes.byref(out), None) == UNSUP
+    nv.group = 64  # NVFP4 with the INT4 group size: not a format the kernels read
+    assert L.kvq_encode_residual(ctypes.c_void_p(64), prev, 1, ctypes.byref(nv), None) == UNSUP
+    # batched calls: the base bit of the NVFP4 loop mask must be clear
+    ws = ctypes.create_string_buffer(64)
+    assert L.kvq_encode_batch_ex(ctypes.c_void_p(64), 1, 8, 128, 0, 1, ctypes.c_void_p(64), 1, ws, 64, None) == BAD
+    assert b"nvfp4_loops" in L.kvq_last_error()
+    assert L.kvq_reconstruct_batch_ex(ctypes.c_void_p(64), 1, 8, 128, 0, 2, ctypes.c_void_p(64), 1, ws, 64,
+                                      None) == BAD
     # attention: shape checks come first
     f = L.kvq_decode_attn_packed_ex
     assert f(None, 1, 8, 30, 128, 4, None, ctypes.c_float(0.1), None, None, 0, 0, None) == BAD  # 30 % 8
