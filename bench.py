@@ -387,7 +387,7 @@ def main():
     extras = None
     if not args.no_extras:
         extras = run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream,
-                            (xk_ptrs, xv_ptrs, rk_ptrs))
+                            (xk_ptrs, xv_ptrs, rk_ptrs, rv_ptrs, rk, rv, offs))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -452,7 +452,14 @@ def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, re
       tile-local K grouping (codec PR review, group ownership vs pages): the
       K encode, K reconstruction and attention of a second pool whose sparse
       K groups stay inside one 64-token tile, beside the K phases of the
-      compact-grouped pool."""
+      compact-grouped pool;
+      NVFP4 residual loops (codec PR review: INT4 base + NVFP4 residuals,
+      compared on fused-attention speed and accuracy): encode, reconstruction
+      and attention of a pool whose loops 2.. are NVFP4, beside the INT4 pool
+      on one stream, and the accuracy of both on a sample of requests against
+      the unquantised chain (each token's BF16 source from the deepest loop
+      that stores it, which is what the chain reconstructs): reconstruction
+      RMS error, and the attention error against FP32 attention over it."""
     B = len(reqs)
     max_t = max(r.T for r in reqs)
     n_select = max(1, max_t // 4)
@@ -486,7 +493,7 @@ def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, re
     tail_ms, _ = timed(lambda: kvq.kvq_decode_attn_packed(ttable, q, depth, H, workspace=tws))
     err |= kvq.attn_error_word(tws)
 
-    xk_ptrs, xv_ptrs, rk_ptrs = ptrs
+    xk_ptrs, xv_ptrs, rk_ptrs, rv_ptrs, rk, rv, offs = ptrs
     tpool = kvq.PackedPool([r.T for r in reqs], [r.active for r in reqs], H, D, depth, dev, kgroup=kvq.KVQ_KGROUP_TILE)
 
     def enc_k(pl):
@@ -506,12 +513,90 @@ def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, re
                    "encode_k_ms": ek_t, "encode_k_ms_compact": ek_c,
                    "reconstruct_k_ms": rk_t, "reconstruct_k_ms_compact": rk_c, "attention_ms": at_t}
     del tpool
-    return {"kgroup_tile": kgroup_tile,
+    nvfp4 = run_nvfp4_extra(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, timed, ptrs)
+    err |= nvfp4.pop("error_word")
+    return {"kgroup_tile": kgroup_tile, "nvfp4_residuals": nvfp4,
             "sparse_decode": {"budget_keys_per_query_head": n_select, "ref_depth": 2, "depth": depth,
                               "ref_state_ms": ref_ms, "later_loop_ms": dec_ms,
                               "selected_keys_per_s": selected / (dec_ms * 1e-3)},
             "bf16_tail": {"tail_tokens_per_request": 100, "attention_ms": tail_ms},
             "error_word": err}
+
+
+def run_nvfp4_extra(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, timed, ptrs, n_sample=16):
+    """INT4-base + NVFP4-residual chains against the INT4 chains of `pool` (see run_extras)."""
+    xk_ptrs, xv_ptrs, rk_ptrs, rv_ptrs, rk, rv, offs = ptrs
+    formats = [kvq.KVQ_FMT_INT4] + [kvq.KVQ_FMT_NVFP4] * (depth - 1)
+    npool = kvq.PackedPool([r.T for r in reqs], [r.active for r in reqs], H, D, depth, dev, formats=formats)
+
+    def enc(pl):
+        for j in range(depth):
+            kvq.kvq_encode_batch(pl, kvq.KVQ_K, j, xk_ptrs[j], stream=stream)
+            kvq.kvq_encode_batch(pl, kvq.KVQ_V, j, xv_ptrs[j], stream=stream)
+
+    def rec(pl):
+        kvq.kvq_reconstruct_batch(pl, kvq.KVQ_K, depth, rk_ptrs, stream=stream)
+        kvq.kvq_reconstruct_batch(pl, kvq.KVQ_V, depth, rv_ptrs, stream=stream)
+
+    B = len(reqs)
+    ws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(B, H, Hq, D), dtype=torch.uint8, device=dev)
+    out_n = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    out_i = torch.empty_like(out_n)
+    enc_n, _ = timed(lambda: enc(npool))
+    enc_i, _ = timed(lambda: enc(pool))
+    rec_i, _ = timed(lambda: rec(pool))
+    sample = list(range(min(n_sample, B)))
+    rmse = {}
+
+    def target(xs, act):  # the unquantised chain: a token keeps the source of the deepest loop storing it
+        t = xs[0].clone()
+        for j in range(1, depth):
+            if act[j] is None:
+                t = xs[j].clone()
+            else:
+                t[act[j].long()] = xs[j][act[j].long()]
+        return t
+
+    tk = {b: target(reqs[b].xk, reqs[b].active) for b in sample}
+    tv = {b: target(reqs[b].xv, reqs[b].active) for b in sample}
+
+    def recon_rmse(tag):
+        for kind, buf, src in (("k", rk, tk), ("v", rv, tv)):
+            num = den = 0.0
+            for b in sample:
+                d = buf[offs[b]:offs[b + 1]].float() - src[b].float()
+                num += float((d * d).sum())
+                den += d.numel()
+            rmse[f"{kind}_{tag}"] = (num / max(den, 1)) ** 0.5
+
+    recon_rmse("int4")
+    rec_n, _ = timed(lambda: rec(npool))
+    recon_rmse("nvfp4")
+    att_n, _ = timed(lambda: kvq.kvq_decode_attn_packed(npool.table, q, depth, H, out=out_n, workspace=ws))
+    att_i, _ = timed(lambda: kvq.kvq_decode_attn_packed(pool.table, q, depth, H, out=out_i, workspace=ws))
+    # the NVFP4-reading form of the tensor-core kernel on the INT4 pool: the cost of carrying both formats
+    att_in, _ = timed(lambda: kvq.kvq_decode_attn_packed(pool.table, q, depth, H, algo=kvq.ATTN_AUTO | kvq.ATTN_NVFP4,
+                                                         out=out_i, workspace=ws))
+    err = kvq.attn_error_word(ws) | kvq.attn_error_word(npool.workspace)
+    # attention error against FP32 attention over the unquantised chain
+    g = Hq // H
+    scale = 1.0 / math.sqrt(D)
+    worst = {"int4": 0.0, "nvfp4": 0.0}
+    for b in sample:
+        kx, vx = tk[b].float(), tv[b].float()  # [T, H, D]
+        qb = q[b].float().view(H, g, D)
+        s_ = torch.einsum("hgd,thd->hgt", qb, kx) * scale
+        ref = torch.einsum("hgt,thd->hgd", torch.softmax(s_, dim=-1), vx).reshape(Hq, D)
+        worst["int4"] = max(worst["int4"], float((out_i[b] - ref).abs().max()))
+        worst["nvfp4"] = max(worst["nvfp4"], float((out_n[b] - ref).abs().max()))
+    res = {"formats": "INT4 base, NVFP4 loops 2..%d" % depth, "payload_bytes": npool.payload_bytes,
+           "payload_bytes_int4": pool.payload_bytes, "encode_ms": enc_n, "encode_ms_int4": enc_i,
+           "reconstruct_ms": rec_n, "reconstruct_ms_int4": rec_i, "attention_ms": att_n, "attention_ms_int4": att_i,
+           "attention_ms_int4_in_nvfp4_form": att_in, "sample_requests": len(sample),
+           "recon_rmse_vs_unquantised_chain": rmse, "attn_max_abs_err_vs_unquantised_chain": worst,
+           "error_word": err}
+    del npool
+    return res
 
 
 def run_e2e(args, torch, kvq, src_all, q, out, step, stream, world, dev, step_bytes, dist):

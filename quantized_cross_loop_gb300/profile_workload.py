@@ -18,7 +18,8 @@ requests of configuration 2). Stages:
   tail         packed decode attention with a 100-token BF16 tail per request,
                `reps` times.
 --kgroup tile builds the K chains with tile-local K groups (the stored rows of
-one 64-token logical tile per group) instead of 64 consecutive stored rows.
+one 64-token logical tile per group) instead of 64 consecutive stored rows;
+--residual nvfp4 encodes loops 2.. of K and V as NVFP4 (INT4 base).
 Every stage first encodes the workload (the launches a capture should skip:
 2 + 4 (loops - 1) per kind, plus one per reconstruct or attention call before
 the one captured).
@@ -47,13 +48,18 @@ def main():
     ap.add_argument("--algo", choices=["auto", "simt", "mma"], default="auto")
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--kgroup", choices=["compact", "tile"], default="compact")
+    ap.add_argument("--residual", choices=["int4", "nvfp4"], default="int4")
     args = ap.parse_args()
     cfg, rep = parse_workload(args.workload)
     dev = torch.device("cuda")
     wl = W.make_workload(cfg, device=dev, replicate=rep)
     reqs = wl.requests
     kgroup = kvq.KVQ_KGROUP_TILE if args.kgroup == "tile" else kvq.KVQ_KGROUP_COMPACT
-    pool = kvq.PackedPool([r.T for r in reqs], [r.active for r in reqs], wl.H, wl.D, wl.depth, dev, kgroup=kgroup)
+    formats = None
+    if args.residual == "nvfp4":
+        formats = [kvq.KVQ_FMT_INT4] + [kvq.KVQ_FMT_NVFP4] * (wl.depth - 1)
+    pool = kvq.PackedPool([r.T for r in reqs], [r.active for r in reqs], wl.H, wl.D, wl.depth, dev, kgroup=kgroup,
+                          formats=formats)
     for j in range(wl.depth):
         kvq.kvq_encode_batch(pool, kvq.KVQ_K, j, kvq.pointer_array([r.xk[j] for r in reqs], dev))
         kvq.kvq_encode_batch(pool, kvq.KVQ_V, j, kvq.pointer_array([r.xv[j] for r in reqs], dev))
