@@ -129,6 +129,8 @@ typedef struct kvq_stream {
   uint16_t* scales;
   const int32_t* active_idx; /* NULL: dense */
   int32_t* tile_dir;         /* sparse streams: written by kvq_encode_residual, read by attention/reconstruct */
+  int32_t row_cap;           /* rows per head the planes hold (>= n_rows; 0: n_rows) */
+  int32_t token_cap;         /* tokens the K groups, index and tile directory hold (>= n_tokens; 0: n_tokens) */
 } kvq_stream;
 
 /* Fill the format fields of `s` and clear its pointers. */
@@ -137,6 +139,14 @@ kvq_status kvq_stream_init(kvq_stream* s, int kind, int n_rows, int n_tokens, in
 /* Set the element format of `s` (KVQ_FMT_INT4 or KVQ_FMT_NVFP4) and its group
  * size (64 or 16). Call before kvq_plane_bytes. */
 kvq_status kvq_stream_set_format(kvq_stream* s, int format);
+
+/* Give the planes of `s` room to grow (kvq_append_tile): row_cap rows per head
+ * and token_cap tokens. Every plane is then laid out with the capacities in
+ * place of the counts (codes [H][row_cap][D/2], V params [H][row_cap][..], K
+ * params [H][groups of the capacity][D], index [row_cap], tile directory
+ * [ceil(token_cap/64)+1]); readers index by the capacities and read the first
+ * n_rows / n_tokens. Call before kvq_plane_bytes. */
+kvq_status kvq_stream_set_capacity(kvq_stream* s, int row_cap, int token_cap);
 
 /* Bytes to allocate for one plane of `s` (KVQ_PLANE_*), rounded up to 16. The
  * index plane is at least 16 bytes, so that an empty sparse set still has a
@@ -189,6 +199,34 @@ kvq_status kvq_build_tile_dir(const int32_t* active_idx, int n_rows, int n_token
                               kvq_cuda_stream stream);
 
 /*
+ * Append one 64-token tile to a K or V chain in place: the flush of the rolling
+ * BF16 tail into the packed form in whole 64-token groups (RFC §3.3).
+ *   loops[0..n_loops-1]  the chain; host descriptors, updated on success
+ *          (n_tokens += 64; n_rows += the tile's stored rows of each loop).
+ *          Requirements: every loop INT4; n_tokens a multiple of 64; room for
+ *          the tile in the capacities (kvq_stream_set_capacity); a sparse K
+ *          loop in tile grouping (KVQ_KGROUP_TILE: its new rows form a group of
+ *          their own, where compact grouping would merge them into an old one).
+ *   x_tile       host array [n_loops] of device pointers: BF16 [64][H][D], the
+ *                tile's source of each loop.
+ *   tile_active  host array [n_loops] of device pointers: a sparse loop's
+ *                ascending positions (0..63) of the tile's tokens it stores,
+ *                nested in the previous sparse loop's; NULL for a dense loop.
+ *   n_tile_active host array [n_loops]: their counts (a dense loop: 64).
+ *   workspace    >= kvq_append_workspace_bytes(n_loops) bytes of device memory,
+ *                16-byte aligned.
+ * The sparse loops' index and tile directory planes are extended too (K and V
+ * of a request share them; appending both kinds writes the same values twice).
+ * The planes then hold exactly the bytes an encode of the whole extended chain
+ * would write. NVFP4 loops are refused (UNSUPPORTED): their tensor scale spans
+ * the whole stream.
+ */
+size_t kvq_append_workspace_bytes(int n_loops);
+kvq_status kvq_append_tile(kvq_stream* loops, int n_loops, const uint16_t* const* x_tile,
+                           const int32_t* const* tile_active, const int* n_tile_active, void* workspace,
+                           size_t workspace_bytes, kvq_cuda_stream stream);
+
+/*
  * Reconstruct X̂ at `depth` (1 = base only) into BF16 [n_tokens][n_heads][head_dim]
  * (RFC §3.3: unpack, dequantise and sum the chain in BF16; absent tokens
  * inherit). loops[0..depth-1] describe loops 1..depth of one K or V chain.
@@ -215,6 +253,8 @@ typedef struct kvq_loop_ref {
   uint8_t* v_codes;
   uint16_t* v_mins;
   uint16_t* v_scales;
+  int32_t row_cap;           /* rows per head of the planes (0: n_rows) */
+  int32_t kgroup_cap;        /* K groups per head of the K param planes (0: those of n_rows) */
 } kvq_loop_ref;
 
 /*

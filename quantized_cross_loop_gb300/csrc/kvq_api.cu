@@ -56,8 +56,16 @@ kvq_status check_format(const kvq_stream* s, const char* name) {
   if (s->head_dim != kD) return fail(KVQ_ERR_UNSUPPORTED, "%s: head_dim %d (kernels support 128)", name, s->head_dim);
   if (s->active_idx == nullptr && s->n_rows != s->n_tokens)
     return fail(KVQ_ERR_BAD_ARG, "%s: dense stream with n_rows %d != n_tokens %d", name, s->n_rows, s->n_tokens);
+  if (s->row_cap < 0 || (s->row_cap > 0 && s->row_cap < s->n_rows) || s->token_cap < 0 ||
+      (s->token_cap > 0 && s->token_cap < s->n_tokens) || (s->row_cap > 0) != (s->token_cap > 0))
+    return fail(KVQ_ERR_BAD_ARG, "%s: capacities row %d token %d for n_rows %d n_tokens %d", name, s->row_cap,
+                s->token_cap, s->n_rows, s->n_tokens);
   return KVQ_OK;
 }
+
+// Rows per head and tokens the planes of s are laid out for.
+int row_capacity(const kvq_stream* s) { return s->row_cap > 0 ? s->row_cap : s->n_rows; }
+int token_capacity(const kvq_stream* s) { return s->token_cap > 0 ? s->token_cap : s->n_tokens; }
 
 // Checks pointers of a stream that is read (need_dir: sparse streams must carry tile_dir).
 kvq_status check_planes(const kvq_stream* s, const char* name, bool need_dir) {
@@ -94,7 +102,8 @@ void to_planes(const kvq_stream* s, LoopPlanes* p) {
   p->n_rows = s->n_rows;
   p->sparse = s->active_idx != nullptr;
   p->ktile = k_tile(s);
-  p->kgroups = k_groups_of(k_tile(s), s->n_rows, s->n_tokens);
+  p->kgroups = k_groups_of(k_tile(s), row_capacity(s), token_capacity(s));
+  p->stride = row_capacity(s);
   p->fmt = s->format;
   p->active = s->active_idx;
   p->tile_dir = s->tile_dir;
@@ -197,6 +206,16 @@ kvq_status kvq_stream_init(kvq_stream* s, int kind, int n_rows, int n_tokens, in
   return ok();
 }
 
+kvq_status kvq_stream_set_capacity(kvq_stream* s, int row_cap, int token_cap) {
+  if (s == nullptr) return fail(KVQ_ERR_BAD_ARG, "stream is NULL");
+  if (row_cap < s->n_rows || token_cap < s->n_tokens || row_cap > token_cap)
+    return fail(KVQ_ERR_BAD_ARG, "capacities row %d token %d below n_rows %d n_tokens %d (or rows above tokens)",
+                row_cap, token_cap, s->n_rows, s->n_tokens);
+  s->row_cap = row_cap;
+  s->token_cap = token_cap;
+  return ok();
+}
+
 kvq_status kvq_stream_set_format(kvq_stream* s, int format) {
   if (s == nullptr) return fail(KVQ_ERR_BAD_ARG, "stream is NULL");
   if (format == KVQ_FMT_INT4) {
@@ -215,16 +234,17 @@ kvq_status kvq_stream_set_format(kvq_stream* s, int format) {
 size_t kvq_plane_bytes(const kvq_stream* s, int plane) {
   if (s == nullptr) return 0;
   const int64_t n = s->n_rows, H = s->n_heads, D = s->head_dim;
-  if (nvfp4(s) && plane == KVQ_PLANE_MINS) return round16(size_t(H * n * (D / 16)));  // E4M3 block scales
+  const int64_t nc = row_capacity(s), tc = token_capacity(s);
+  if (nvfp4(s) && plane == KVQ_PLANE_MINS) return round16(size_t(H * nc * (D / 16)));  // E4M3 block scales
   if (nvfp4(s) && plane == KVQ_PLANE_SCALES) return 16;                              // FP32 tensor-scale record
   switch (plane) {
-    case KVQ_PLANE_CODES: return round16(size_t(H * n * (D / 2)));
+    case KVQ_PLANE_CODES: return round16(size_t(H * nc * (D / 2)));
     case KVQ_PLANE_MINS:
     case KVQ_PLANE_SCALES:
-      if (s->kind == KVQ_K) return round16(size_t(2 * H * k_groups_of(k_tile(s), s->n_rows, s->n_tokens) * D));
-      return round16(size_t(2 * H * n * cdiv(D, KVQ_GROUP)));
-    case KVQ_PLANE_INDEX: return n > 0 ? round16(size_t(4 * n)) : 16;  // never NULL: NULL means dense
-    case KVQ_PLANE_TILE_DIR: return round16(size_t(4 * (cdiv(s->n_tokens, KVQ_TILE) + 1)));
+      if (s->kind == KVQ_K) return round16(size_t(2 * H * k_groups_of(k_tile(s), int(nc), int(tc)) * D));
+      return round16(size_t(2 * H * nc * cdiv(D, KVQ_GROUP)));
+    case KVQ_PLANE_INDEX: return nc > 0 ? round16(size_t(4 * nc)) : 16;  // never NULL: NULL means dense
+    case KVQ_PLANE_TILE_DIR: return round16(size_t(4 * (cdiv(tc, KVQ_TILE) + 1)));
     default: return 0;
   }
 }
@@ -247,6 +267,10 @@ int64_t kvq_stream_payload_bytes(int kind, int n_rows, int n_heads, int head_dim
 static void to_loop_ref(const kvq_stream* s, kvq_loop_ref* L) {
   L->n_rows = s->n_rows;
   L->flags |= loop_flags(s);
+  if (s->row_cap > 0) {
+    L->row_cap = s->row_cap;
+    if (s->kind == KVQ_K) L->kgroup_cap = k_groups_of(k_tile(s), s->row_cap, s->token_cap);
+  }
   L->active_idx = s->active_idx;
   L->tile_dir = s->tile_dir;
   if (s->kind == KVQ_K) {
@@ -350,6 +374,130 @@ kvq_status kvq_encode_residual(const uint16_t* x_r, const kvq_stream* prev, int 
     if (st != KVQ_OK) return st;
   }
   return run_single(a, out->kind == KVQ_K ? kModeEncK : kModeEncV, s, "encode_residual launch");
+}
+
+constexpr size_t kAppendLoopBytes = 320;  // per loop: 64 checked positions, a 2-entry directory, padding
+
+size_t kvq_append_workspace_bytes(int n_loops) {
+  if (n_loops < 1 || n_loops > KVQ_MAX_LOOPS) return 0;
+  return 16 + size_t(n_loops) * kAppendLoopBytes;
+}
+
+kvq_status kvq_append_tile(kvq_stream* loops, int n_loops, const uint16_t* const* x_tile,
+                           const int32_t* const* tile_active, const int* n_tile_active, void* workspace,
+                           size_t workspace_bytes, kvq_cuda_stream stream) {
+  if (n_loops < 1 || n_loops > KVQ_MAX_LOOPS) return fail(KVQ_ERR_BAD_ARG, "n_loops %d", n_loops);
+  if (!loops || !x_tile || !tile_active || !n_tile_active) return fail(KVQ_ERR_BAD_ARG, "NULL argument");
+  Chain C;
+  kvq_status st = build_chain(loops, n_loops, &C, "loops");
+  if (st != KVQ_OK) return st;
+  const size_t need = kvq_append_workspace_bytes(n_loops);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return fail(KVQ_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", need);
+  const int T = loops[0].n_tokens, H = loops[0].n_heads, kind = loops[0].kind;
+  if (T % KVQ_TILE != 0) return fail(KVQ_ERR_BAD_ARG, "n_tokens %d is not a multiple of %d", T, KVQ_TILE);
+  for (int r = 0; r < n_loops; ++r) {
+    const kvq_stream& L = loops[r];
+    const int m = n_tile_active[r];
+    if (nvfp4(&L)) return fail(KVQ_ERR_UNSUPPORTED, "loop %d: NVFP4 streams cannot grow (per-stream tensor scale)", r);
+    if (L.row_cap <= 0 || L.token_cap < T + KVQ_TILE || L.n_rows + m > L.row_cap)
+      return fail(KVQ_ERR_BAD_ARG, "loop %d: capacities row %d token %d cannot take the tile", r, L.row_cap,
+                  L.token_cap);
+    if (L.active_idx == nullptr) {
+      if (tile_active[r] != nullptr || m != KVQ_TILE)
+        return fail(KVQ_ERR_BAD_ARG, "loop %d: a dense loop stores all %d tokens of the tile", r, KVQ_TILE);
+    } else {
+      if (tile_active[r] == nullptr || m < 0 || m > KVQ_TILE)
+        return fail(KVQ_ERR_BAD_ARG, "loop %d: sparse loop needs 0..%d tile positions", r, KVQ_TILE);
+      if (L.kind == KVQ_K && L.kgroup != KVQ_KGROUP_TILE)
+        return fail(KVQ_ERR_UNSUPPORTED, "loop %d: a sparse K loop grows only under tile grouping", r);
+    }
+    if (x_tile[r] == nullptr || !aligned16(x_tile[r])) return fail(KVQ_ERR_MISALIGNED, "x_tile[%d]", r);
+    if (!L.codes || !L.mins || !L.scales || (L.active_idx && !L.tile_dir))
+      return fail(KVQ_ERR_BAD_ARG, "loop %d: planes missing", r);
+    if (!aligned16(L.codes) || !aligned16(L.mins) || !aligned16(L.scales))
+      return fail(KVQ_ERR_MISALIGNED, "loop %d: planes must be 16-byte aligned", r);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int32_t* err = reinterpret_cast<int32_t*>(ws);
+  cudaError_t e = cudaMemsetAsync(err, 0, 16, s);
+  if (e != cudaSuccess) return cuda_status(e, "clear error word");
+  AppendIndexArgs ia;
+  memset(&ia, 0, sizeof ia);
+  ia.n_loops = n_loops;
+  ia.T = T;
+  ia.err = err;
+  for (int r = 0; r < n_loops; ++r) {
+    int32_t* base = reinterpret_cast<int32_t*>(ws + 16 + size_t(r) * kAppendLoopBytes);
+    ia.loop[r].rel = loops[r].active_idx ? tile_active[r] : nullptr;
+    ia.loop[r].rel_ws = base;
+    ia.loop[r].dir_ws = base + 64;
+    ia.loop[r].active = const_cast<int32_t*>(loops[r].active_idx);
+    ia.loop[r].tile_dir = loops[r].tile_dir;
+    ia.loop[r].n_old = loops[r].n_rows;
+    ia.loop[r].n_new = n_tile_active[r];
+  }
+  e = launch_append_index(ia, s);
+  if (e != cudaSuccess) return cuda_status(e, "append index launch");
+  // tile-grouped sparse K: the groups of tiles without stored rows hold +0 min and scale
+  for (int r = 0; r < n_loops && kind == KVQ_K; ++r) {
+    const kvq_stream& L = loops[r];
+    if (L.active_idx == nullptr) continue;
+    const int m = n_tile_active[r], k = T / KVQ_TILE;
+    int g0 = 0, g1 = 0;  // groups to clear
+    if (m == 0 && L.n_rows > 0) g0 = k, g1 = k + 1;
+    if (m > 0 && L.n_rows == 0) g0 = 0, g1 = k;  // the stream's first rows: the earlier tiles are empty
+    if (g1 <= g0) continue;
+    const size_t pitch = size_t(k_groups_of(true, L.row_cap, L.token_cap)) * kD * 2;
+    for (uint16_t* plane : {L.mins, L.scales}) {
+      e = cudaMemset2DAsync(reinterpret_cast<char*>(plane) + size_t(g0) * kD * 2, pitch, 0, size_t(g1 - g0) * kD * 2,
+                            H, s);
+      if (e != cudaSuccess) return cuda_status(e, "clear empty tile groups");
+    }
+  }
+  // encode loop by loop through views of the tile's rows (tokens 0..63 of x_tile)
+  for (int r = 0; r < n_loops; ++r) {
+    CodecArgs a;
+    memset(&a, 0, sizeof a);
+    a.H = H;
+    a.kind = kind;
+    a.loop = r;
+    a.err = err;
+    a.one.n_tokens = KVQ_TILE;
+    a.one.n_loops = r + 1;
+    for (int j = 0; j <= r; ++j) {
+      const kvq_stream& L = loops[j];
+      kvq_loop_ref& V = a.one.loop[j];
+      const int32_t* base = reinterpret_cast<const int32_t*>(ws + 16 + size_t(j) * kAppendLoopBytes);
+      V.n_rows = n_tile_active[j];
+      V.flags = loop_flags(&L);
+      V.row_cap = L.row_cap;
+      V.kgroup_cap = kind == KVQ_K ? k_groups_of(k_tile(&L), L.row_cap, L.token_cap) : 0;
+      V.active_idx = L.active_idx ? base : nullptr;
+      V.tile_dir = L.active_idx ? const_cast<int32_t*>(base + 64) : nullptr;
+      uint8_t* codes = L.codes + size_t(L.n_rows) * kRowBytes;  // row n_rows of head 0; heads at row_cap
+      // K: the tile's group (index T/64 under either grouping of a growable loop); V: row n_rows
+      const size_t poff = kind == KVQ_K ? size_t(T / KVQ_TILE) * kD : size_t(L.n_rows) * (kD / kG);
+      if (kind == KVQ_K) {
+        V.k_codes = codes;
+        V.k_mins = L.mins + poff;
+        V.k_scales = L.scales + poff;
+      } else {
+        V.v_codes = codes;
+        V.v_mins = L.mins + poff;
+        V.v_scales = L.scales + poff;
+      }
+    }
+    a.one_x = x_tile[r];
+    st = run_single(a, kind == KVQ_K ? kModeEncK : kModeEncV, s, "append encode launch");
+    if (st != KVQ_OK) return st;
+  }
+  for (int r = 0; r < n_loops; ++r) {
+    loops[r].n_rows += n_tile_active[r];
+    loops[r].n_tokens += KVQ_TILE;
+  }
+  return ok();
 }
 
 kvq_status kvq_reconstruct(const kvq_stream* loops, int depth, uint16_t* out, kvq_cuda_stream stream) {
@@ -490,6 +638,9 @@ kvq_status kvq_request_fill(const kvq_stream* k_loops, const kvq_stream* v_loops
     kvq_loop_ref& L = out->loop[j];
     L.n_rows = k->n_rows;
     L.flags = loop_flags(k) | loop_flags(v);
+    if (row_capacity(k) != row_capacity(v)) return fail(KVQ_ERR_BAD_ARG, "loop %d: K and V row capacities differ", j);
+    L.row_cap = k->row_cap;
+    L.kgroup_cap = k->row_cap > 0 ? k_groups_of(k_tile(k), k->row_cap, k->token_cap) : 0;
     L.active_idx = k->active_idx;
     L.tile_dir = k->tile_dir ? k->tile_dir : v->tile_dir;
     L.k_codes = k->codes;

@@ -252,6 +252,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
   long long us = 0, ue = -1;  // current unit's tile range
   int h = 0, T = 0, unit = -1, nsink = 0;
   int nr[DEPTH], kgr[DEPTH];  // stored rows; K groups per head (0: compact grouping, else tile grouping)
+  int rs[DEPTH], gs[DEPTH];   // plane strides: rows per head, K groups per head
   bool refused = false;       // a loop in a format this kernel does not read: the unit reads no rows
   int fl[DEPTH];              // NVFP4 flags per loop (1: K, 2: V)
   float kst[DEPTH], vst[DEPTH];  // their tensor scales
@@ -282,6 +283,8 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
         const kvq_loop_ref& L = R.loop[j];
         nr[j] = L.n_rows;
         kgr[j] = (L.flags & KVQ_LOOP_K_TILE) ? k_groups_of(true, L.n_rows, T) : 0;
+        rs[j] = L.row_cap > 0 ? L.row_cap : L.n_rows;
+        gs[j] = L.kgroup_cap > 0 ? L.kgroup_cap : (kgr[j] > 0 ? kgr[j] : (L.n_rows + kG - 1) / kG);
         fl[j] = ((L.flags & KVQ_LOOP_K_NVFP4) ? 1 : 0) | ((L.flags & KVQ_LOOP_V_NVFP4) ? 2 : 0);
         if (fl[j] && !kNv) refused = true;
         kst[j] = (kNv && (fl[j] & 1) && L.n_rows > 0) ? __ldg(reinterpret_cast<const float*>(L.k_scales)) : 0.0f;
@@ -359,7 +362,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       LM[7] = np;
       for (int G = 0; G < ngrp; ++G) M[8 + np++] = (j << 1) | G;
       if (n == 0) continue;
-      const long long hr = (long long)h * nr[j] + c0;  // first stored row of this head
+      const long long hr = (long long)h * rs[j] + c0;  // first stored row of this head
       bulk_copy(st.l[j].kc, kc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
       bulk_copy(st.l[j].vc, vc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
       int krem = 0, vrem = 0;
@@ -370,7 +373,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
         bulk_copy(st.l[j].kmin, reinterpret_cast<const uint8_t*>(kmn[j]) + lo, nb, &S.full[s]);
         krem = int(off - lo);
       } else {
-        const long long gb = ((long long)h * (kt ? kgr[j] : (nr[j] + kG - 1) / kG) + g0) * kD;
+        const long long gb = ((long long)h * gs[j] + g0) * kD;
         bulk_copy(st.l[j].kmin, kmn[j] + gb, ngrp * kD * 2, &S.full[s]);
         bulk_copy(st.l[j].ksc, ksc[j] + gb, ngrp * kD * 2, &S.full[s]);
       }

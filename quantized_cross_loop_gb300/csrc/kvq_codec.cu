@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kD) encode_k_generic_kernel(const __grid_const
     const_cast<uint16_t*>(O.scales)[pi] = f32_to_f16_bits(s32);
     __syncthreads();
     // len rows x 64 bytes, contiguous in the head-major plane: 16-byte stores.
-    uint4* dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(O.codes) + ((long long)h * n + r0) * kRowBytes);
+    uint4* dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(O.codes) + ((long long)h * O.stride + r0) * kRowBytes);
     const uint4* src = reinterpret_cast<const uint4*>(&s_codes[0][0]);
     for (int k = d; k < len * (kRowBytes / 16); k += blockDim.x) dst[k] = src[k];
   }
@@ -351,10 +351,10 @@ __global__ void __launch_bounds__(kEncVThreads) encode_v_generic_kernel(const __
       for (int e = 0; e < 4; ++e) c[e] = quantize(v[e], mn, s32);
       uint16_t packed = uint16_t(c[0] | (c[1] << 4) | (c[2] << 8) | (c[3] << 12));
       const long long row = r0 + i;
-      *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(O.codes) + ((long long)h * n + row) * kRowBytes + lane * 2) =
-          packed;
+      *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(O.codes) + ((long long)h * O.stride + row) * kRowBytes +
+                                   lane * 2) = packed;
       if ((lane & 15) == 0) {
-        long long pi = ((long long)h * n + row) * (kD / kG) + (lane >> 4);
+        long long pi = ((long long)h * O.stride + row) * (kD / kG) + (lane >> 4);
         const_cast<uint16_t*>(O.mins)[pi] = f32_to_f16_bits(mn);
         const_cast<uint16_t*>(O.scales)[pi] = f32_to_f16_bits(s32);
       }
@@ -449,10 +449,10 @@ __global__ void __launch_bounds__(kEncVThreads) nvfp4_encode_kernel(const __grid
 #pragma unroll
       for (int e = 0; e < 4; ++e) packed |= (eb == 0.0f ? 0u : f32_to_e2m1(__fdiv_rn(v[e], eb))) << (4 * e);
       const long long row = r0 + i;
-      *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(O.codes) + ((long long)h * n + row) * kRowBytes + lane * 2) =
-          uint16_t(packed);
+      *reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(O.codes) + ((long long)h * O.stride + row) * kRowBytes +
+                                   lane * 2) = uint16_t(packed);
       if ((lane & 3) == 0)
-        reinterpret_cast<uint8_t*>(const_cast<uint16_t*>(O.mins))[((long long)h * n + row) * (kD / 16) + (lane >> 2)] =
+        reinterpret_cast<uint8_t*>(const_cast<uint16_t*>(O.mins))[((long long)h * O.stride + row) * (kD / 16) + (lane >> 2)] =
             uint8_t(sb);
     }
     if (kAmax) {
@@ -859,7 +859,7 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
           rows[j] = S.row[j][i];
           if (rows[j] >= 0) {
             const LoopPlanes& L = S.C.loop[j];
-            cw[j] = __ldg(reinterpret_cast<const uint2*>(L.codes + ((long long)h * L.n_rows + rows[j]) * kRowBytes +
+            cw[j] = __ldg(reinterpret_cast<const uint2*>(L.codes + ((long long)h * L.stride + rows[j]) * kRowBytes +
                                                          8 * sub));
           }
         }
@@ -944,7 +944,7 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
     __syncthreads();
     // len rows x 64 bytes, contiguous in the head-major plane
     if (tid < len * (kRowBytes / 16)) {
-      uint4* dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(O.codes) + ((long long)h * n + r0) * kRowBytes);
+      uint4* dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(O.codes) + ((long long)h * O.stride + r0) * kRowBytes);
       dst[tid] = reinterpret_cast<const uint4*>(&S.codes[0][0])[tid];
     }
   }
@@ -1029,7 +1029,7 @@ __global__ void __launch_bounds__(kEncVFastThreads) encode_v_fast_kernel(const _
           const int row = s_row[j][i];
           if (row >= 0) {
             const LoopPlanes& L = C.loop[j];
-            const long long rr = (long long)h * L.n_rows + row;
+            const long long rr = (long long)h * L.stride + row;
             cw[j] = __ldg(reinterpret_cast<const uint2*>(L.codes + rr * kRowBytes + 8 * sub));
             m16[j] = __ldg(L.mins + rr * (kD / kG) + (sub >> 2));
             s16[j] = __ldg(L.scales + rr * (kD / kG) + (sub >> 2));
@@ -1094,7 +1094,7 @@ __global__ void __launch_bounds__(kEncVFastThreads) encode_v_fast_kernel(const _
       const uint32_t mp = f32_to_f16_bits(mn), sp = f32_to_f16_bits(s32);
       const uint32_t mp1 = __shfl_down_sync(0xffffffffu, mp, 4), sp1 = __shfl_down_sync(0xffffffffu, sp, 4);
       if (live) {
-        const long long rr = (long long)h * n + r0 + i;
+        const long long rr = (long long)h * O.stride + r0 + i;
         *reinterpret_cast<uint2*>(const_cast<uint8_t*>(O.codes) + rr * kRowBytes + 8 * sub) = make_uint2(w0, w1);
         if (sub == 0) {
           *reinterpret_cast<uint32_t*>(const_cast<uint16_t*>(O.mins) + rr * (kD / kG)) = mp | (mp1 << 16);
@@ -1227,7 +1227,7 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
         rows[u][j] = tt < nvalid ? row_in(tr, tt) : -1;
         cw[u][j] = make_uint2(0, 0);
         if (rows[u][j] >= 0)
-          cw[u][j] = __ldg(reinterpret_cast<const uint2*>(L.codes + ((long long)h * L.n_rows + rows[u][j]) * kRowBytes +
+          cw[u][j] = __ldg(reinterpret_cast<const uint2*>(L.codes + ((long long)h * L.stride + rows[u][j]) * kRowBytes +
                                                           8 * sub));
       }
     }
@@ -1326,7 +1326,7 @@ __global__ void __launch_bounds__(kReconVFastThreads) reconstruct_v_fast_kernel(
         m16[j] = s16[j] = 0;
         if (have[j]) {
           const LoopPlanes& L = C.loop[j];
-          const long long rr = (long long)h * L.n_rows + row;
+          const long long rr = (long long)h * L.stride + row;
           cw[j] = __ldg(reinterpret_cast<const uint2*>(L.codes + rr * kRowBytes + 8 * sub));
           m16[j] = __ldg(L.mins + rr * (kD / kG) + (sub >> 2));
           s16[j] = __ldg(L.scales + rr * (kD / kG) + (sub >> 2));
@@ -1352,6 +1352,47 @@ __global__ void __launch_bounds__(kReconVFastThreads) reconstruct_v_fast_kernel(
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- tile append: index planes
+
+// One block per loop. A position outside [0, 64), or not ascending, sets bit 4
+// and is replaced by a valid ascending list, so the encode that follows stays
+// inside the tile.
+__global__ void __launch_bounds__(64) append_index_kernel(const __grid_constant__ AppendIndexArgs a) {
+  const AppendIndexArgs::Loop& L = a.loop[blockIdx.x];
+  if (L.rel == nullptr) return;  // dense loop: no index
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  const int i = threadIdx.x;
+  int v = 0;
+  if (i < L.n_new) {
+    v = __ldg(L.rel + i);
+    const int prev = i > 0 ? __ldg(L.rel + i - 1) : -1;
+    if (v < 0 || v >= KVQ_TILE || v <= prev) s_bad = 1;
+  }
+  __syncthreads();
+  if (s_bad) {
+    v = i;  // 0 .. n_new - 1
+    if (i == 0 && a.err) atomicOr(a.err, 4);
+  }
+  if (i < L.n_new) {
+    L.rel_ws[i] = v;
+    L.active[L.n_old + i] = a.T + v;
+  }
+  if (i == 0) {
+    L.dir_ws[0] = 0;
+    L.dir_ws[1] = L.n_new;
+    L.tile_dir[a.T / KVQ_TILE] = L.n_old;
+    L.tile_dir[a.T / KVQ_TILE + 1] = L.n_old + L.n_new;
+  }
+}
+
+cudaError_t launch_append_index(const AppendIndexArgs& a, cudaStream_t stream) {
+  append_index_kernel<<<a.n_loops, 64, 0, stream>>>(a);
+  count_launch();
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- launchers

@@ -25,9 +25,10 @@ struct LoopPlanes {
   int32_t n_rows;
   int32_t sparse;
   int32_t ktile;    // K groups by 64-token logical tile (KVQ_KGROUP_TILE) instead of 64 stored rows
-  int32_t kgroups;  // K groups per head: ceil(n_tokens/64) if ktile, else ceil(n_rows/64)
+  int32_t kgroups;  // K groups per head of the param planes: ceil(n_tokens/64) if ktile, else ceil(n_rows/64),
+                    // or the capacity's
   int32_t fmt;      // KVQ_FMT_INT4 or KVQ_FMT_NVFP4
-  int32_t pad;
+  int32_t stride;   // rows per head of the planes (the row capacity; n_rows unless the stream can grow)
   const int32_t* active;
   const int32_t* tile_dir;
   const uint8_t* codes;
@@ -92,7 +93,7 @@ __device__ __forceinline__ float nvfp4_dequant(uint32_t nib, float sb, float st)
 // NVFP4 planes of a loop: E4M3 block scale of (head h, stored row, block of 16
 // channels) and the tensor scale.
 __device__ __forceinline__ float nvfp4_block_scale(const LoopPlanes& L, int h, int row, int blk) {
-  return e4m3_to_f32(__ldg(reinterpret_cast<const uint8_t*>(L.mins) + ((long long)h * L.n_rows + row) * (kD / 16) + blk));
+  return e4m3_to_f32(__ldg(reinterpret_cast<const uint8_t*>(L.mins) + ((long long)h * L.stride + row) * (kD / 16) + blk));
 }
 __device__ __forceinline__ float nvfp4_tensor_scale(const LoopPlanes& L) {
   return __ldg(reinterpret_cast<const float*>(L.scales));
@@ -143,7 +144,7 @@ __device__ __forceinline__ int k_group(const LoopPlanes& L, int t, int row) { re
 // Index of the params of (head h, logical token t stored at `row`, channel d).
 __device__ __forceinline__ long long param_index(int kind, const LoopPlanes& L, int h, int t, int row, int d) {
   if (kind == KVQ_K) return ((long long)h * L.kgroups + k_group(L, t, row)) * kD + d;
-  return ((long long)h * L.n_rows + row) * (kD / kG) + d / kG;
+  return ((long long)h * L.stride + row) * (kD / kG) + d / kG;
 }
 
 // Loop j of request R as the K (kind 0) or V planes the kernels read.
@@ -152,7 +153,8 @@ __device__ __forceinline__ void planes_of(const kvq_request& R, int j, int kind,
   P.n_rows = L.n_rows;
   P.sparse = L.active_idx != nullptr;
   P.ktile = kind == KVQ_K && (L.flags & KVQ_LOOP_K_TILE) != 0;
-  P.kgroups = k_groups_of(P.ktile != 0, L.n_rows, R.n_tokens);
+  P.kgroups = L.kgroup_cap > 0 ? L.kgroup_cap : k_groups_of(P.ktile != 0, L.n_rows, R.n_tokens);
+  P.stride = L.row_cap > 0 ? L.row_cap : L.n_rows;
   P.fmt = (L.flags & (kind == KVQ_K ? KVQ_LOOP_K_NVFP4 : KVQ_LOOP_V_NVFP4)) ? KVQ_FMT_NVFP4 : KVQ_FMT_INT4;
   P.active = L.active_idx;
   P.tile_dir = L.tile_dir;
@@ -168,7 +170,7 @@ __device__ __forceinline__ void chain4(const Chain& C, int depth, const int* row
   {
     const LoopPlanes& B = C.loop[0];
     int row = rows[0];
-    uint16_t two = *reinterpret_cast<const uint16_t*>(B.codes + ((long long)h * B.n_rows + row) * kRowBytes + c0 / 2);
+    uint16_t two = *reinterpret_cast<const uint16_t*>(B.codes + ((long long)h * B.stride + row) * kRowBytes + c0 / 2);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       int c = (two >> (4 * e)) & 0xF;
@@ -180,7 +182,7 @@ __device__ __forceinline__ void chain4(const Chain& C, int depth, const int* row
     int row = rows[j];
     if (row < 0) continue;  // absent: inherit the predecessor
     const LoopPlanes& L = C.loop[j];
-    uint16_t two = *reinterpret_cast<const uint16_t*>(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + c0 / 2);
+    uint16_t two = *reinterpret_cast<const uint16_t*>(L.codes + ((long long)h * L.stride + row) * kRowBytes + c0 / 2);
     if (L.fmt == KVQ_FMT_NVFP4) {  // the four channels share one 16-channel block
       const float sb = nvfp4_block_scale(L, h, row, c0 / 16), st = nvfp4_tensor_scale(L);
 #pragma unroll
@@ -209,7 +211,7 @@ __device__ __forceinline__ void chain4_f32(const Chain& C, int depth, const int*
     int row = rows[j];
     if (row < 0) continue;
     const LoopPlanes& L = C.loop[j];
-    uint16_t two = *reinterpret_cast<const uint16_t*>(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + c0 / 2);
+    uint16_t two = *reinterpret_cast<const uint16_t*>(L.codes + ((long long)h * L.stride + row) * kRowBytes + c0 / 2);
     if (L.fmt == KVQ_FMT_NVFP4) {
       const float sb = nvfp4_block_scale(L, h, row, c0 / 16), st = nvfp4_tensor_scale(L);
 #pragma unroll
@@ -254,7 +256,7 @@ __device__ __forceinline__ float chain1(const Chain& C, int depth, const int* ro
   {
     const LoopPlanes& B = C.loop[0];
     int row = rows[0];
-    uint8_t byte = __ldg(B.codes + ((long long)h * B.n_rows + row) * kRowBytes + d / 2);
+    uint8_t byte = __ldg(B.codes + ((long long)h * B.stride + row) * kRowBytes + d / 2);
     int c = (d & 1) ? (byte >> 4) : (byte & 0xF);
     long long pi = param_index(C.kind, B, h, t, row, d);
     v = dequant(__ldg(B.mins + pi), __ldg(B.scales + pi), c);
@@ -263,7 +265,7 @@ __device__ __forceinline__ float chain1(const Chain& C, int depth, const int* ro
     int row = rows[j];
     if (row < 0) continue;
     const LoopPlanes& L = C.loop[j];
-    uint8_t byte = __ldg(L.codes + ((long long)h * L.n_rows + row) * kRowBytes + d / 2);
+    uint8_t byte = __ldg(L.codes + ((long long)h * L.stride + row) * kRowBytes + d / 2);
     int c = (d & 1) ? (byte >> 4) : (byte & 0xF);
     if (L.fmt == KVQ_FMT_NVFP4) {
       v = round_bf16(__fadd_rn(v, round_bf16(nvfp4_dequant(c, nvfp4_block_scale(L, h, row, d / 16),
@@ -299,6 +301,25 @@ struct CodecArgs {
   uint16_t* one_out;
   int32_t one_prefix[2];
 };
+
+// Index extension of a tile append (kvq_append_tile): per sparse loop, the
+// tile's relative positions (checked into `rel_ws`), their absolute indices
+// after the n_old stored rows, the tile directory entries of the new tile, and
+// a two-entry directory of the tile alone for the encode of its rows.
+struct AppendIndexArgs {
+  int32_t n_loops;
+  int32_t T;        // tokens before the tile (a multiple of 64)
+  int32_t* err;
+  struct Loop {
+    const int32_t* rel;  // caller's positions 0..63 (NULL: dense loop)
+    int32_t* rel_ws;     // [64] checked copy
+    int32_t* dir_ws;     // [2] = {0, n_new}
+    int32_t* active;     // the stream's index plane
+    int32_t* tile_dir;   // the stream's tile directory
+    int32_t n_old, n_new;
+  } loop[KVQ_MAX_LOOPS];
+};
+cudaError_t launch_append_index(const AppendIndexArgs& a, cudaStream_t stream);
 
 // Launches one codec stage (kMode*) for a batch or a single request; a batch
 // first plans its items into prefix_ws ([n_requests + 1] int32, device).

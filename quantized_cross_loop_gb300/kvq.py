@@ -38,7 +38,7 @@ EXPORTED = (
     "kvq_batch_workspace_bytes", "kvq_encode_batch", "kvq_reconstruct_batch", "kvq_launch_count",
     "kvq_decode_attn_packed_noalloc", "kvq_sparse_workspace_bytes", "kvq_sparse_ref_state",
     "kvq_sparse_decode_attn", "kvq_stream_payload_bytes_ex", "kvq_stream_set_format", "kvq_encode_batch_ex",
-    "kvq_reconstruct_batch_ex",
+    "kvq_reconstruct_batch_ex", "kvq_stream_set_capacity", "kvq_append_workspace_bytes", "kvq_append_tile",
 )
 
 
@@ -65,6 +65,8 @@ class kvq_stream(ctypes.Structure):
         ("scales", ctypes.c_void_p),
         ("active_idx", ctypes.c_void_p),
         ("tile_dir", ctypes.c_void_p),
+        ("row_cap", ctypes.c_int32),
+        ("token_cap", ctypes.c_int32),
     ]
 
 
@@ -80,6 +82,8 @@ class kvq_loop_ref(ctypes.Structure):
         ("v_codes", ctypes.c_void_p),
         ("v_mins", ctypes.c_void_p),
         ("v_scales", ctypes.c_void_p),
+        ("row_cap", ctypes.c_int32),
+        ("kgroup_cap", ctypes.c_int32),
     ]
 
 
@@ -118,6 +122,10 @@ def lib():
             L.kvq_stream_payload_bytes.restype = ctypes.c_int64
             L.kvq_stream_payload_bytes_ex.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
             L.kvq_stream_set_format.argtypes = [P(kvq_stream), i32]
+            L.kvq_stream_set_capacity.argtypes = [P(kvq_stream), i32, i32]
+            L.kvq_append_workspace_bytes.argtypes = [i32]
+            L.kvq_append_workspace_bytes.restype = sz
+            L.kvq_append_tile.argtypes = [P(kvq_stream), i32, vp, vp, vp, vp, sz, vp]
             L.kvq_stream_payload_bytes_ex.restype = ctypes.c_int64
             L.kvq_encode_base.argtypes = [vp, P(kvq_stream), vp]
             L.kvq_encode_residual.argtypes = [vp, P(kvq_stream), i32, P(kvq_stream), vp]
@@ -149,7 +157,8 @@ def lib():
             for name in ("kvq_stream_init", "kvq_encode_base", "kvq_encode_residual", "kvq_build_tile_dir",
                          "kvq_reconstruct", "kvq_request_fill", "kvq_decode_attn_packed",
                          "kvq_decode_attn_packed_ex", "kvq_encode_batch", "kvq_reconstruct_batch",
-                         "kvq_stream_set_format", "kvq_encode_batch_ex", "kvq_reconstruct_batch_ex"):
+                         "kvq_stream_set_format", "kvq_encode_batch_ex", "kvq_reconstruct_batch_ex",
+                         "kvq_stream_set_capacity", "kvq_append_tile"):
                 getattr(L, name).restype = ctypes.c_int32
             _lib = L
     return _lib
@@ -185,14 +194,19 @@ class Stream:
 
     def __init__(self, kind: int, n_rows: int, n_tokens: int, n_heads: int, head_dim: int, device,
                  active: torch.Tensor | None = None, alloc=None, shared_index=None, kgroup: int = KVQ_KGROUP_COMPACT,
-                 fmt: int = KVQ_FMT_INT4):
+                 fmt: int = KVQ_FMT_INT4, row_cap: int = 0, token_cap: int = 0):
+        """row_cap, token_cap: room to grow (kvq_append_tile); 0 = exactly n_rows / n_tokens."""
         self.desc = kvq_stream()
         _check(lib().kvq_stream_init(ctypes.byref(self.desc), kind, n_rows, n_tokens, n_heads, head_dim),
                "kvq_stream_init")
         self.desc.kgroup = kgroup
         _check(lib().kvq_stream_set_format(ctypes.byref(self.desc), fmt), "kvq_stream_set_format")
+        if row_cap or token_cap:
+            _check(lib().kvq_stream_set_capacity(ctypes.byref(self.desc), row_cap, token_cap),
+                   "kvq_stream_set_capacity")
         self.kind, self.n_rows, self.n_tokens, self.n_heads, self.head_dim = kind, n_rows, n_tokens, n_heads, head_dim
         self.kgroup, self.fmt = kgroup, fmt
+        self.row_cap, self.token_cap = (row_cap or n_rows), (token_cap or n_tokens)
 
         def plane(p):
             nbytes = int(lib().kvq_plane_bytes(ctypes.byref(self.desc), p))
@@ -209,7 +223,7 @@ class Stream:
             self.active, self.tile_dir = shared_index
         elif active is not None:
             buf = plane(PLANE_INDEX)
-            buf.view(torch.int32)[:n_rows].copy_(active.to(device=device, dtype=torch.int32))
+            buf.view(torch.int32)[:n_rows].copy_(active.to(device=device, dtype=torch.int32).reshape(-1))
             self.active = buf
             self.tile_dir = plane(PLANE_TILE_DIR)
         self.desc.codes = self.codes.data_ptr()
@@ -224,32 +238,40 @@ class Stream:
 
     # views with the logical plane shapes
     def codes_view(self):
-        return self.codes[: self.n_heads * self.n_rows * self.head_dim // 2].view(self.n_heads, self.n_rows,
-                                                                                  self.head_dim // 2)
+        """uint8 [H, n_rows, D/2] (the live rows of the [H, row_cap, D/2] plane)."""
+        full = self.codes[: self.n_heads * self.row_cap * self.head_dim // 2].view(self.n_heads, self.row_cap,
+                                                                                   self.head_dim // 2)
+        return full[:, : self.n_rows]
 
-    def param_shape(self):
+    def _groups(self, rows: int, tokens: int) -> int:
+        if rows <= 0:
+            return 0
+        if self.kgroup == KVQ_KGROUP_TILE:
+            return -(-tokens // KVQ_GROUP)
+        return -(-rows // KVQ_GROUP)
+
+    def param_shape(self, capacity: bool = False):
+        rows = self.row_cap if capacity else self.n_rows
         if self.fmt == KVQ_FMT_NVFP4:  # E4M3 block scales (bytes)
-            return (self.n_heads, self.n_rows, self.head_dim // 16)
+            return (self.n_heads, rows, self.head_dim // 16)
         if self.kind == KVQ_K:
-            groups = -(-self.n_rows // KVQ_GROUP)
-            if self.kgroup == KVQ_KGROUP_TILE and self.n_rows > 0:
-                groups = -(-self.n_tokens // KVQ_GROUP)
-            return (self.n_heads, groups, self.head_dim)
-        return (self.n_heads, self.n_rows, -(-self.head_dim // KVQ_GROUP))
+            return (self.n_heads, self._groups(rows, self.token_cap if capacity else self.n_tokens), self.head_dim)
+        return (self.n_heads, rows, -(-self.head_dim // KVQ_GROUP))
+
+    def _param_view(self, buf, dtype):
+        full = self.param_shape(capacity=True)
+        live = self.param_shape()
+        return buf.view(dtype)[: math.prod(full)].view(full)[:, : live[1]]
 
     def mins_view(self):
         """INT4: FP16 mins (int16 bits); NVFP4: the E4M3 block scales (uint8 bits)."""
-        shp = self.param_shape()
-        if self.fmt == KVQ_FMT_NVFP4:
-            return self.mins[: math.prod(shp)].view(shp)
-        return self.mins.view(torch.int16)[: math.prod(shp)].view(shp)
+        return self._param_view(self.mins, torch.uint8 if self.fmt == KVQ_FMT_NVFP4 else torch.int16)
 
     def scales_view(self):
         """INT4: FP16 scales (int16 bits); NVFP4: the tensor scale (float32 [1])."""
         if self.fmt == KVQ_FMT_NVFP4:
             return self.scales.view(torch.float32)[:1]
-        shp = self.param_shape()
-        return self.scales.view(torch.int16)[: math.prod(shp)].view(shp)
+        return self._param_view(self.scales, torch.int16)
 
     def active_view(self):
         return None if self.active is None else self.active.view(torch.int32)[: self.n_rows]
@@ -268,18 +290,21 @@ def payload_bytes(kind: int, n_rows: int, n_heads: int, head_dim: int, sparse: b
     return int(lib().kvq_stream_payload_bytes_ex(kind, n_rows, T, n_heads, head_dim, int(sparse), kgroup, fmt))
 
 
-def kvq_encode_base(x: torch.Tensor, kind: int, stream=None, kgroup: int = KVQ_KGROUP_COMPACT) -> Stream:
+def kvq_encode_base(x: torch.Tensor, kind: int, stream=None, kgroup: int = KVQ_KGROUP_COMPACT,
+                    token_cap: int = 0) -> Stream:
     """Encode the loop-1 base of K (kind=KVQ_K) or V from BF16 x [T, H, D]. The
-    base is dense, so `kgroup` changes no byte; it is recorded with the stream."""
+    base is dense, so `kgroup` changes no byte; it is recorded with the stream.
+    token_cap > T leaves room to append tiles (kvq_append_tile)."""
     _require_cuda(x, "x", torch.bfloat16)
     T, H, D = x.shape
-    out = Stream(kind, T, T, H, D, x.device, kgroup=kgroup)
+    out = Stream(kind, T, T, H, D, x.device, kgroup=kgroup, row_cap=token_cap, token_cap=token_cap)
     _check(lib().kvq_encode_base(_dptr(x), ctypes.byref(out.desc), _stream_handle(stream)), "kvq_encode_base")
     return out
 
 
 def kvq_encode_residual(x_r: torch.Tensor, prev: list, active: torch.Tensor | None = None, stream=None,
-                        kgroup: int | None = None, fmt: int = KVQ_FMT_INT4) -> Stream:
+                        kgroup: int | None = None, fmt: int = KVQ_FMT_INT4, row_cap: int = 0,
+                        token_cap: int = 0) -> Stream:
     """Encode loop len(prev)+1 of the chain `prev` from BF16 x_r [T, H, D];
     `active` (sorted int32 logical rows) makes it a compact sparse residual.
     `kgroup` (K only): KVQ_KGROUP_COMPACT or KVQ_KGROUP_TILE; default: the base's.
@@ -288,12 +313,49 @@ def kvq_encode_residual(x_r: torch.Tensor, prev: list, active: torch.Tensor | No
     T, H, D = x_r.shape
     kind = prev[0].kind
     n = T if active is None else int(active.numel())
-    out = Stream(kind, n, T, H, D, x_r.device, active, kgroup=prev[0].kgroup if kgroup is None else kgroup, fmt=fmt)
+    out = Stream(kind, n, T, H, D, x_r.device, active, kgroup=prev[0].kgroup if kgroup is None else kgroup, fmt=fmt,
+                 row_cap=row_cap, token_cap=token_cap)
     arr = (kvq_stream * len(prev))(*[p.desc for p in prev])
     _check(lib().kvq_encode_residual(_dptr(x_r), arr, len(prev), ctypes.byref(out.desc), _stream_handle(stream)),
            "kvq_encode_residual")
     out._keep = list(prev)  # noqa: the chain must outlive the launch
     return out
+
+
+def kvq_append_tile(streams: list, x_tile: list, tile_active: list, workspace: torch.Tensor | None = None,
+                    stream=None):
+    """Append one 64-token tile to the chain `streams` (one kind) in place: the
+    flush of the BF16 tail into the packed form. x_tile[r]: BF16 [64, H, D] of
+    loop r; tile_active[r]: int32 ascending positions 0..63 a sparse loop
+    stores (None for a dense loop). Updates the streams' row and token counts."""
+    n = len(streams)
+    dev = streams[0].codes.device
+    arr = (kvq_stream * n)(*[st.desc for st in streams])
+    keep = []
+    xs = (ctypes.c_void_p * n)()
+    acts = (ctypes.c_void_p * n)()
+    counts = (ctypes.c_int * n)()
+    for r in range(n):
+        _require_cuda(x_tile[r], f"x_tile[{r}]", torch.bfloat16)
+        xs[r] = x_tile[r].data_ptr()
+        a = tile_active[r]
+        if a is None:
+            acts[r] = None
+            counts[r] = KVQ_TILE
+        else:
+            a = a.to(device=dev, dtype=torch.int32).contiguous()
+            keep.append(a)
+            acts[r] = a.data_ptr()
+            counts[r] = int(a.numel())
+    if workspace is None:
+        workspace = torch.empty(int(lib().kvq_append_workspace_bytes(n)), dtype=torch.uint8, device=dev)
+    _check(lib().kvq_append_tile(arr, n, xs, acts, counts, _dptr(workspace), workspace.numel(), _stream_handle(stream)),
+           "kvq_append_tile")
+    for r, st in enumerate(streams):
+        st.desc = arr[r]
+        st.n_rows, st.n_tokens = arr[r].n_rows, arr[r].n_tokens
+    streams[0]._append_keep = (keep, workspace)  # noqa: the launch reads them
+    return workspace
 
 
 def kvq_build_tile_dir(active: torch.Tensor, n_tokens: int, stream=None) -> torch.Tensor:
