@@ -515,12 +515,44 @@ def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, re
     del tpool
     nvfp4 = run_nvfp4_extra(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, timed, ptrs)
     err |= nvfp4.pop("error_word")
-    return {"kgroup_tile": kgroup_tile, "nvfp4_residuals": nvfp4,
+    append = run_append_extra(torch, kvq, reqs, H, D, depth, dev, stream)
+    return {"kgroup_tile": kgroup_tile, "nvfp4_residuals": nvfp4, "append_tile": append,
             "sparse_decode": {"budget_keys_per_query_head": n_select, "ref_depth": 2, "depth": depth,
                               "ref_state_ms": ref_ms, "later_loop_ms": dec_ms,
                               "selected_keys_per_s": selected / (dec_ms * 1e-3)},
             "bf16_tail": {"tail_tokens_per_request": 100, "attention_ms": tail_ms},
             "error_word": err}
+
+
+def run_append_extra(torch, kvq, reqs, H, D, depth, dev, stream, n_req=8):
+    """Latency of the tail flush (RFC §3.3): one 64-token tile appended to the K
+    and V chains of a request (tile-local K grouping), averaged over n_req
+    requests; the chains hold the request's tokens up to the last whole tile."""
+    from quantized_cross_loop_gb300.kvq import KVQ_KGROUP_TILE
+    chains, tiles = [], []
+    for r in reqs[:n_req]:
+        T0 = (r.T // 64 - 1) * 64  # leave the last whole tile to append
+        cap = T0 + 64
+        for kind, xs in ((kvq.KVQ_K, r.xk), (kvq.KVQ_V, r.xv)):
+            gs = [kvq.kvq_encode_base(xs[0][:T0], kind, kgroup=KVQ_KGROUP_TILE, token_cap=cap)]
+            for j in range(1, depth):
+                a = r.active[j]
+                a0 = None if a is None else a[a < T0].contiguous()
+                gs.append(kvq.kvq_encode_residual(xs[j][:T0], gs, a0, row_cap=cap, token_cap=cap))
+            rel = [None if a is None else (a[(a >= T0) & (a < T0 + 64)] - T0).to(torch.int32) for a in r.active]
+            chains.append(gs)
+            tiles.append(([x[T0:T0 + 64].contiguous() for x in xs], rel))
+    ws = torch.empty(int(kvq.lib().kvq_append_workspace_bytes(depth)), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for gs, (xt, rel) in zip(chains, tiles):
+        kvq.kvq_append_tile(gs, xt, rel, workspace=ws)
+    b.record(stream)
+    torch.cuda.synchronize()
+    err = kvq.attn_error_word(ws)
+    return {"requests": len(chains) // 2, "us_per_request_k_and_v": a.elapsed_time(b) * 1e3 / max(len(chains) // 2, 1),
+            "launches_per_kind": 1 + depth, "error_word": err}
 
 
 def run_nvfp4_extra(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, timed, ptrs, n_sample=16):

@@ -253,8 +253,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
   int h = 0, T = 0, unit = -1, nsink = 0;
   int nr[DEPTH], kgr[DEPTH];  // stored rows; K groups per head (0: compact grouping, else tile grouping)
   int rs[DEPTH], gs[DEPTH];   // plane strides: rows per head, K groups per head
-  bool refused = false;       // a loop in a format this kernel does not read: the unit reads no rows
-  int fl[DEPTH];              // NVFP4 flags per loop (1: K, 2: V)
+  int fl[DEPTH];              // NVFP4 flags per loop (1: K, 2: V); the INT4 form never sees them (plan)
   float kst[DEPTH], vst[DEPTH];  // their tensor scales
   const int32_t* act[DEPTH];
   const int32_t* dir[DEPTH];
@@ -277,7 +276,6 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       us = rb + (long long)h * nt;
       ue = us + nt;
       unit = b * a.H + h;
-      refused = false;
 #pragma unroll
       for (int j = 0; j < DEPTH; ++j) {
         const kvq_loop_ref& L = R.loop[j];
@@ -285,8 +283,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
         kgr[j] = (L.flags & KVQ_LOOP_K_TILE) ? k_groups_of(true, L.n_rows, T) : 0;
         rs[j] = L.row_cap > 0 ? L.row_cap : L.n_rows;
         gs[j] = L.kgroup_cap > 0 ? L.kgroup_cap : (kgr[j] > 0 ? kgr[j] : (L.n_rows + kG - 1) / kG);
-        fl[j] = ((L.flags & KVQ_LOOP_K_NVFP4) ? 1 : 0) | ((L.flags & KVQ_LOOP_V_NVFP4) ? 2 : 0);
-        if (fl[j] && !kNv) refused = true;
+        fl[j] = kNv ? (((L.flags & KVQ_LOOP_K_NVFP4) ? 1 : 0) | ((L.flags & KVQ_LOOP_V_NVFP4) ? 2 : 0)) : 0;
         kst[j] = (kNv && (fl[j] & 1) && L.n_rows > 0) ? __ldg(reinterpret_cast<const float*>(L.k_scales)) : 0.0f;
         vst[j] = (kNv && (fl[j] & 2) && L.n_rows > 0) ? __ldg(reinterpret_cast<const float*>(L.v_scales)) : 0.0f;
         act[j] = L.active_idx;
@@ -336,10 +333,6 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
         atomicOr(a.err, 4);
         c0 = c1 = 0;
       }
-      if (refused) {
-        if (k == 0 && j == 0) atomicOr(a.err, 64);
-        c0 = c1 = 0;
-      }
       const int n = c1 - c0;
       // K groups of the tile's rows: under tile grouping the tile's own group k,
       // and word 1 is set so that a consumer's ((word1 + row) >> 6) - g0 is 0
@@ -347,11 +340,13 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       const bool nk = kNv && (fl[j] & 1), nv = kNv && (fl[j] & 2);
       const int g0 = kt ? k : c0 / kG;
       const int ngrp = (n > 0 && !nk) ? (kt ? 1 : (c1 - 1) / kG - g0 + 1) : 0;  // INT4 K groups (NVFP4: none)
-      int32_t* LF = M + kMetaFmt + 4 * j;
-      LF[0] = kNv ? fl[j] : 0;
-      LF[1] = __float_as_int(kst[j]);
-      LF[2] = __float_as_int(vst[j]);
-      LF[3] = 0;
+      int32_t* LF = M + kMetaFmt + 4 * j;  // read by the NVFP4 form only
+      if (kNv) {
+        LF[0] = fl[j];
+        LF[1] = __float_as_int(kst[j]);
+        LF[2] = __float_as_int(vst[j]);
+        LF[3] = 0;
+      }
       LM[0] = n;
       LM[1] = kt ? k * kG : c0;
       LM[2] = g0;
@@ -391,7 +386,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
         bulk_copy(st.l[j].vsc, reinterpret_cast<const uint8_t*>(vsc[j]) + lo, nb, &S.full[s]);
         LM[4] = int((off - lo) / 2);
       }
-      LF[3] = krem | (vrem << 16);
+      if (kNv) LF[3] = krem | (vrem << 16);
       if (act[j] != nullptr) {
         const long long off = (long long)c0 * 4;
         const long long lo = off & ~15LL;
@@ -676,15 +671,12 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       }
       if (lane == 0) Gs.slice[w][j] = SliceInfo{rb, cnt, bits, 0};
       if (cnt == 0) continue;
-      // A: the stored rows of the warp's tokens g and g + 8 (a sparse loop's r-th
-      // present token sits in row rb + r; an absent token reads a valid row whose
-      // logit is then dropped), the 16 bytes of chunk q
-      const int ra = rb + min(__popc(bits & ((1 << g) - 1)), cnt - 1);
-      const int rc = rb + min(__popc(bits & ((1 << (g + 8)) - 1)), cnt - 1);
-      const uint4 wa = *reinterpret_cast<const uint4*>(&st.l[j].kc[ra * kRowBytes + 16 * q]);
-      const uint4 wb = *reinterpret_cast<const uint4*>(&st.l[j].kc[rc * kRowBytes + 16 * q]);
       float e[4];
       if (kNv && (st.meta[kMetaFmt + 4 * j] & 1)) {  // NVFP4 K: no groups, no min terms
+        const int ra = rb + min(__popc(bits & ((1 << g) - 1)), cnt - 1);
+        const int rc = rb + min(__popc(bits & ((1 << (g + 8)) - 1)), cnt - 1);
+        const uint4 wa = *reinterpret_cast<const uint4*>(&st.l[j].kc[ra * kRowBytes + 16 * q]);
+        const uint4 wb = *reinterpret_cast<const uint4*>(&st.l[j].kc[rc * kRowBytes + 16 * q]);
         const int4 lf = *reinterpret_cast<const int4*>(&st.meta[kMetaFmt + 4 * j]);
         qk_pass_nv(st, j, &Gs.q16[g][0], lf.w & 0xFFFF, ra, rc, wa, wb, q, __int_as_float(lf.y), e);
         if ((bits >> g) & 1) {
@@ -701,6 +693,13 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       const int ga = ((c0 + rb) >> 6) - g0;
       const int gb = ((c0 + rb + cnt - 1) >> 6) - g0;
       const bool split = gb != ga;
+      // A: the stored rows of the warp's tokens g and g + 8 (a sparse loop's r-th
+      // present token sits in row rb + r; an absent token reads a valid row whose
+      // logit is then dropped), the 16 bytes of chunk q
+      const int ra = rb + min(__popc(bits & ((1 << g) - 1)), cnt - 1);
+      const int rc = rb + min(__popc(bits & ((1 << (g + 8)) - 1)), cnt - 1);
+      const uint4 wa = *reinterpret_cast<const uint4*>(&st.l[j].kc[ra * kRowBytes + 16 * q]);
+      const uint4 wb = *reinterpret_cast<const uint4*>(&st.l[j].kc[rc * kRowBytes + 16 * q]);
       qk_pass(st, j, ga, qp, wa, wb, q, e);
       const int Ga = ((c0 + ra) >> 6) - g0, Gc = ((c0 + rc) >> 6) - g0;
       if (split) {  // rows of the second K group: a second pass with that group's Q'
@@ -788,13 +787,13 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         if (si.cnt == 0) continue;
         const int vrem = st.meta[16 + 8 * j + 4];
         const int bits = si.bits, rb = si.rb, cnt = si.cnt;
-        // stored rows of the tokens 2q, 2q+1, 2q+8, 2q+9 (an absent token reads a
-        // valid row against a zero P')
-        const int r0 = rb + min(__popc(bits & ((1 << (2 * q)) - 1)), cnt - 1);
-        const int r1 = rb + min(__popc(bits & ((2 << (2 * q)) - 1)), cnt - 1);
-        const int r2 = rb + min(__popc(bits & ((1 << (2 * q + 8)) - 1)), cnt - 1);
-        const int r3 = rb + min(__popc(bits & ((2 << (2 * q + 8)) - 1)), cnt - 1);
         if (kNv && (st.meta[kMetaFmt + 4 * j] & 2)) {  // NVFP4 V
+          // stored rows of the tokens 2q, 2q+1, 2q+8, 2q+9 (an absent token reads a
+          // valid row against a zero P')
+          const int r0 = rb + min(__popc(bits & ((1 << (2 * q)) - 1)), cnt - 1);
+          const int r1 = rb + min(__popc(bits & ((2 << (2 * q)) - 1)), cnt - 1);
+          const int r2 = rb + min(__popc(bits & ((1 << (2 * q + 8)) - 1)), cnt - 1);
+          const int r3 = rb + min(__popc(bits & ((2 << (2 * q + 8)) - 1)), cnt - 1);
           const int4 lf = *reinterpret_cast<const int4*>(&st.meta[kMetaFmt + 4 * j]);
           const float st14 = __int_as_float(lf.z) * 16384.0f;  // s_t * 2^14 (the codes carry 2^-14)
           const uint8_t* vs = reinterpret_cast<const uint8_t*>(st.l[j].vmin) + (lf.w >> 16);
@@ -861,7 +860,10 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         // token reads a valid row against a zero P'); thread g takes word 8*vg + g of
         // each row (channels 64vg + 8g .. +7)
         const uint8_t* base = &st.l[j].vc[0];
-        const int o0 = r0 * kRowBytes, o1 = r1 * kRowBytes, o2 = r2 * kRowBytes, o3 = r3 * kRowBytes;
+        const int o0 = (rb + min(__popc(bits & ((1 << (2 * q)) - 1)), cnt - 1)) * kRowBytes;
+        const int o1 = (rb + min(__popc(bits & ((2 << (2 * q)) - 1)), cnt - 1)) * kRowBytes;
+        const int o2 = (rb + min(__popc(bits & ((1 << (2 * q + 8)) - 1)), cnt - 1)) * kRowBytes;
+        const int o3 = (rb + min(__popc(bits & ((2 << (2 * q + 8)) - 1)), cnt - 1)) * kRowBytes;
         uint32_t wv[2][4];
 #pragma unroll
         for (int vg = 0; vg < 2; ++vg) {
