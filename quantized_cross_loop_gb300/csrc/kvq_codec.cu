@@ -661,6 +661,22 @@ __device__ __forceinline__ uint32_t quant_pair(uint32_t v, float2 mn, float2 rc,
   return code;
 }
 
+// quant_pair without the division: the product codes, and in *near bit 0 / 1
+// the channels whose product lies too close to a half-integer (or is not
+// finite) to decide; the caller gives those quantize() later. Exact ties are
+// common on BF16 data (up to ~2% of residual pairs), so a warp that ran the
+// IEEE division for every pair one of its lanes flags would take it on a large
+// share of its pairs; collecting the flags first lets the lanes that need it
+// run it together.
+__device__ __forceinline__ uint32_t quant_pair_fast(uint32_t v, float2 mn, float2 rc, uint32_t* near) {
+  const float2 x = bf2_to_f2(v);
+  const float2 y = __fmul2_rn(__fadd2_rn(x, make_float2(-mn.x, -mn.y)), rc);
+  const float2 z = __fadd2_rn(y, make_float2(kMagic23, kMagic23));
+  const float2 e = __ffma2_rn(__fadd2_rn(z, make_float2(-kMagic23, -kMagic23)), make_float2(-1.0f, -1.0f), y);
+  *near = uint32_t(!(fabsf(e.x) <= kTieWindow)) | (uint32_t(!(fabsf(e.y) <= kTieWindow)) << 1);
+  return (__float_as_uint(z.x) & 0xFu) | ((__float_as_uint(z.y) & 0xFu) << 4);
+}
+
 __device__ __forceinline__ float scale_of(float mn, float mx) {
   return (mx != mn) ? __fdiv_rn(__fsub_rn(mx, mn), 15.0f) : 0.0f;
 }
@@ -937,9 +953,23 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
     if (nr > 0) {
       const float4 qp = S.qp[p];
       const float2 mnv = make_float2(qp.x, qp.y), rc = make_float2(qp.z, qp.w), sv = S.qs[p];
+      uint32_t pend = 0;  // bit 2k + c: channel c of row k needs the division
 #pragma unroll
       for (int k = 0; k < 16; ++k)
-        if (k < nr) S.codes[16 * q + k][p] = uint8_t(quant_pair(S.delta[16 * q + k][p], mnv, rc, sv));
+        if (k < nr) {
+          uint32_t nb;
+          S.codes[16 * q + k][p] = uint8_t(quant_pair_fast(S.delta[16 * q + k][p], mnv, rc, &nb));
+          pend |= nb << (2 * k);
+        }
+      while (pend) {  // the flagged channels (this thread's rows only: no warp-wide work needed)
+        const int bit = __ffs(pend) - 1;
+        pend &= pend - 1;
+        const int k = bit >> 1, c = bit & 1;
+        const uint32_t w = S.delta[16 * q + k][p];
+        const uint32_t code = uint32_t(c ? quantize(bf_hi(w), mnv.y, sv.y) : quantize(bf_lo(w), mnv.x, sv.x));
+        uint8_t& byte = S.codes[16 * q + k][p];
+        byte = uint8_t((byte & ~(0xFu << (4 * c))) | (code << (4 * c)));
+      }
     }
     __syncthreads();
     // len rows x 64 bytes, contiguous in the head-major plane
@@ -1085,11 +1115,36 @@ __global__ void __launch_bounds__(kEncVFastThreads) encode_v_fast_kernel(const _
       const float2 mnv = make_float2(mn, mn), sv = make_float2(s32, s32);
       const float rcs = recip_of(s32);
       const float2 rc = make_float2(rcs, rcs);
-      uint32_t w0 = 0, w1 = 0;
+      uint32_t w0 = 0, w1 = 0, pend = 0;  // pend bit 2k + c: channel c of pair k needs the division
+      if (R == 0) {  // base data: ties are rare (~0.2% of elements), the per-pair fallback is cheaper
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        w0 |= quant_pair(d[k], mnv, rc, sv) << (8 * k);
-        w1 |= quant_pair(d[4 + k], mnv, rc, sv) << (8 * k);
+        for (int k = 0; k < 4; ++k) {
+          w0 |= quant_pair(d[k], mnv, rc, sv) << (8 * k);
+          w1 |= quant_pair(d[4 + k], mnv, rc, sv) << (8 * k);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t n0, n1;
+          w0 |= quant_pair_fast(d[k], mnv, rc, &n0) << (8 * k);
+          w1 |= quant_pair_fast(d[4 + k], mnv, rc, &n1) << (8 * k);
+          pend |= (n0 << (2 * k)) | (n1 << (2 * (4 + k)));
+        }
+      }
+      while (R > 0 && __any_sync(0xffffffffu, pend != 0)) {  // the flagged channels, one per lane per round
+        if (pend) {
+          const int bit = __ffs(pend) - 1;
+          pend &= pend - 1;
+          const int k = bit >> 1, c = bit & 1;
+          uint32_t dv = d[0];
+#pragma unroll
+          for (int kk = 1; kk < 8; ++kk)
+            if (k == kk) dv = d[kk];
+          const uint32_t code = uint32_t(quantize(c ? bf_hi(dv) : bf_lo(dv), mn, s32));
+          const int sh = 8 * (k & 3) + 4 * c;
+          if (k < 4) w0 = (w0 & ~(0xFu << sh)) | (code << sh);
+          else w1 = (w1 & ~(0xFu << sh)) | (code << sh);
+        }
       }
       const uint32_t mp = f32_to_f16_bits(mn), sp = f32_to_f16_bits(s32);
       const uint32_t mp1 = __shfl_down_sync(0xffffffffu, mp, 4), sp1 = __shfl_down_sync(0xffffffffu, sp, 4);
