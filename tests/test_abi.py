@@ -53,9 +53,10 @@ def test_struct_layouts_match_header():
 #include <stdio.h>
 #include <stddef.h>
 #include "kvq.h"
-int main(void){printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_stream), offsetof(kvq_stream, codes),
+int main(void){printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_stream), offsetof(kvq_stream, codes),
   offsetof(kvq_stream, tile_dir), sizeof(kvq_loop_ref), sizeof(kvq_request), offsetof(kvq_request, n_sink),
-  offsetof(kvq_request, tail_v), offsetof(kvq_stream, kgroup), offsetof(kvq_loop_ref, flags)); return 0;}
+  offsetof(kvq_request, tail_v), offsetof(kvq_stream, kgroup), offsetof(kvq_loop_ref, flags),
+  offsetof(kvq_stream, format), offsetof(kvq_stream, token_cap), offsetof(kvq_loop_ref, kgroup_cap)); return 0;}
 '''
     import subprocess
     import tempfile
@@ -68,7 +69,8 @@ int main(void){printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_stream
         got = [int(v) for v in subprocess.run([exe], capture_output=True, text=True).stdout.split()]
     assert got == [ctypes.sizeof(kvq.kvq_stream), kvq.kvq_stream.codes.offset, kvq.kvq_stream.tile_dir.offset,
                    ctypes.sizeof(kvq.kvq_loop_ref), ctypes.sizeof(kvq.kvq_request), kvq.kvq_request.n_sink.offset,
-                   kvq.kvq_request.tail_v.offset, kvq.kvq_stream.kgroup.offset, kvq.kvq_loop_ref.flags.offset]
+                   kvq.kvq_request.tail_v.offset, kvq.kvq_stream.kgroup.offset, kvq.kvq_loop_ref.flags.offset,
+                   kvq.kvq_stream.format.offset, kvq.kvq_stream.token_cap.offset, kvq.kvq_loop_ref.kgroup_cap.offset]
 
 
 def test_plane_sizes_and_payload(L):
