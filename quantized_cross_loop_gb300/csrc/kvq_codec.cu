@@ -1234,11 +1234,12 @@ __device__ __forceinline__ void load_kpar16_global(const LoopPlanes& L, int h, i
 // a lane loads each loop's parameters once for its four tokens (twice when a
 // sparse loop's rows cross a group), and each token's output row (256 B) leaves
 // in 16-byte stores.
-constexpr int kReconKThreads = 128;
-constexpr int kReconKTok = 4;
+constexpr int kReconKTok = 4;                             // tokens per lane
+// (four 128-thread blocks per SM at 128 registers: faster than three at 159 despite a few spilled words)
+constexpr int kReconKThreads = KVQ_TILE * 8 / kReconKTok;  // eight lanes per token, one tile per item
 
 template <int DEPTH>
-__global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(const __grid_constant__ CodecArgs a,
+__global__ void __launch_bounds__(kReconKThreads, 4) reconstruct_k_fast_kernel(const __grid_constant__ CodecArgs a,
                                                                             const int32_t* prefix_ws) {
   using namespace fast;
   const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
@@ -1278,7 +1279,7 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
       const TileRows tr = tile_rows(a, L, k, nvalid, lane);
 #pragma unroll
       for (int u = 0; u < kReconKTok; ++u) {
-        const int tt = 16 * warp + 4 * u + lg;
+        const int tt = 4 * kReconKTok * warp + 4 * u + lg;
         rows[u][j] = tt < nvalid ? row_in(tr, tt) : -1;
         cw[u][j] = make_uint2(0, 0);
         if (rows[u][j] >= 0)
@@ -1314,7 +1315,7 @@ __global__ void __launch_bounds__(kReconKThreads) reconstruct_k_fast_kernel(cons
     }
 #pragma unroll
     for (int u = 0; u < kReconKTok; ++u) {
-      const int tt = 16 * warp + 4 * u + lg;
+      const int tt = 4 * kReconKTok * warp + 4 * u + lg;
       if (tt < nvalid) {
         uint4* dst = reinterpret_cast<uint4*>(out + ((long long)(t0 + tt) * H + h) * kD + 16 * sub);
         dst[0] = make_uint4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
