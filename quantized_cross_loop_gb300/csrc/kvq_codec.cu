@@ -991,7 +991,7 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
 constexpr int kEncVFastThreads = 256;
 
 template <int R>
-__global__ void __launch_bounds__(kEncVFastThreads) encode_v_fast_kernel(const __grid_constant__ CodecArgs a,
+__global__ void __launch_bounds__(kEncVFastThreads, 5) encode_v_fast_kernel(const __grid_constant__ CodecArgs a,
                                                                          const int32_t* prefix_ws) {
   using namespace fast;
   constexpr int RA = R > 0 ? R : 1;
@@ -1331,7 +1331,7 @@ __global__ void __launch_bounds__(kReconKThreads, 4) reconstruct_k_fast_kernel(c
 constexpr int kReconVFastThreads = 256;
 
 template <int DEPTH>
-__global__ void __launch_bounds__(kReconVFastThreads) reconstruct_v_fast_kernel(const __grid_constant__ CodecArgs a,
+__global__ void __launch_bounds__(kReconVFastThreads, 5) reconstruct_v_fast_kernel(const __grid_constant__ CodecArgs a,
                                                                                 const int32_t* prefix_ws) {
   using namespace fast;
   constexpr int kWarps = kReconVFastThreads / 32;
