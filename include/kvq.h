@@ -289,6 +289,30 @@ typedef struct kvq_request {
  * request (n_loops of each). Checks that K and V agree on rows and sets. */
 kvq_status kvq_request_fill(const kvq_stream* k_loops, const kvq_stream* v_loops, int n_loops, kvq_request* out);
 
+/*
+ * Batched tail flush: one 64-token tile appended to the K and V chains of every
+ * request of a DEVICE table, all loops in one call (same bytes as
+ * kvq_append_tile per request).
+ *   reqs    DEVICE table (kvq_request_fill entries of growable streams); updated in
+ *           place: n_tokens += 64 and each loop's n_rows += its tile rows. Each
+ *           request: n_loops loops (1..4), whole tiles so far, INT4 loops with
+ *           room for the tile (row_cap, kgroup_cap), sparse loops in tile grouping.
+ *           A request that does not qualify is left unchanged and sets bit 1 of the
+ *           error word.
+ *   xk_tile, xv_tile  DEVICE arrays [n_loops * n_requests] (loop-major) of device
+ *           pointers to the tile's BF16 [64][H][D] sources.
+ *   tile_active  DEVICE array [n_loops * n_requests] of device pointers to a sparse
+ *           loop's ascending positions 0..63 (NULL for a dense loop);
+ *           n_tile_active DEVICE int32 [n_loops * n_requests], their counts (64 dense).
+ *   workspace  >= kvq_append_batch_workspace_bytes(n_requests), 16-byte aligned;
+ *           int32 error word at offset 0 (bit 1 refused request, bit 4 bad positions).
+ */
+size_t kvq_append_batch_workspace_bytes(int n_requests);
+kvq_status kvq_append_tile_batch(kvq_request* reqs, int n_requests, int n_heads, int head_dim, int n_loops,
+                                 const uint16_t* const* xk_tile, const uint16_t* const* xv_tile,
+                                 const int32_t* const* tile_active, const int32_t* n_tile_active, void* workspace,
+                                 size_t workspace_bytes, kvq_cuda_stream stream);
+
 /* Workspace bytes the batched codec calls need for n_requests requests. */
 size_t kvq_batch_workspace_bytes(int n_requests);
 

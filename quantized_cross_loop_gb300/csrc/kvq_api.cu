@@ -500,6 +500,70 @@ kvq_status kvq_append_tile(kvq_stream* loops, int n_loops, const uint16_t* const
   return ok();
 }
 
+size_t kvq_append_batch_workspace_bytes(int n_requests) {
+  if (n_requests < 0) return 0;
+  return 16 + round16(size_t(n_requests + 1) * 4) + round16(size_t(n_requests) * 4);
+}
+
+kvq_status kvq_append_tile_batch(kvq_request* reqs, int n_requests, int n_heads, int head_dim, int n_loops,
+                                 const uint16_t* const* xk_tile, const uint16_t* const* xv_tile,
+                                 const int32_t* const* tile_active, const int32_t* n_tile_active, void* workspace,
+                                 size_t workspace_bytes, kvq_cuda_stream stream) {
+  if (n_requests < 0) return fail(KVQ_ERR_BAD_ARG, "n_requests %d", n_requests);
+  if (n_loops < 1 || n_loops > 4)
+    return fail(KVQ_ERR_UNSUPPORTED, "n_loops %d (the batched append takes chains of 1..4 loops)", n_loops);
+  if (n_heads < 1 || n_heads > 1024) return fail(KVQ_ERR_BAD_ARG, "n_heads %d", n_heads);
+  if (head_dim != kD) return fail(KVQ_ERR_UNSUPPORTED, "head_dim %d (kernels support 128)", head_dim);
+  const size_t need = kvq_append_batch_workspace_bytes(n_requests);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return fail(KVQ_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", need);
+  if (n_requests == 0) return ok();
+  if (!reqs || !xk_tile || !xv_tile || !tile_active || !n_tile_active)
+    return fail(KVQ_ERR_BAD_ARG, "NULL argument");
+  if (!aligned16(reqs)) return fail(KVQ_ERR_MISALIGNED, "reqs must be 16-byte aligned");
+  int sms = 0;
+  kvq_status st = current_sms(&sms);
+  if (st != KVQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int32_t* err = reinterpret_cast<int32_t*>(ws);
+  int32_t* prefix = reinterpret_cast<int32_t*>(ws + 16);
+  int32_t* skip = reinterpret_cast<int32_t*>(ws + 16 + round16(size_t(n_requests + 1) * 4));
+  cudaError_t e = cudaMemsetAsync(err, 0, 16, s);
+  if (e != cudaSuccess) return cuda_status(e, "clear error word");
+  AppendBatchArgs pa;
+  memset(&pa, 0, sizeof pa);
+  pa.reqs = reqs;
+  pa.n_requests = n_requests;
+  pa.n_loops = n_loops;
+  pa.H = n_heads;
+  pa.tile_active = tile_active;
+  pa.n_tile_active = n_tile_active;
+  pa.skip = skip;
+  pa.err = err;
+  e = launch_append_batch_prep(pa, s);
+  if (e != cudaSuccess) return cuda_status(e, "append preparation launch");
+  // the table now counts the tile: encode the last tile of every loop, K and V
+  for (int r = 0; r < n_loops; ++r) {
+    for (int kind = KVQ_K; kind <= KVQ_V; ++kind) {
+      CodecArgs a;
+      memset(&a, 0, sizeof a);
+      a.reqs = reqs;
+      a.x = (kind == KVQ_K ? xk_tile : xv_tile) + size_t(r) * n_requests;
+      a.n_requests = n_requests;
+      a.H = n_heads;
+      a.kind = kind;
+      a.loop = r;
+      a.append = 1;
+      a.skip = skip;
+      a.err = err;
+      e = launch_codec(a, kind == KVQ_K ? kModeEncK : kModeEncV, prefix, sms, s);
+      if (e != cudaSuccess) return cuda_status(e, "append encode launch");
+    }
+  }
+  return ok();
+}
+
 kvq_status kvq_reconstruct(const kvq_stream* loops, int depth, uint16_t* out, kvq_cuda_stream stream) {
   Chain C;
   kvq_status st = build_chain(loops, depth, &C, "loops");

@@ -31,8 +31,27 @@ __device__ __forceinline__ const kvq_request& req_at(const CodecArgs& a, int b) 
   return a.reqs ? a.reqs[b] : a.one;
 }
 
+// Stored rows of the last 64-token tile of loop L (append mode): [*r0, *r0 + return).
+__device__ __forceinline__ int last_tile_rows(const kvq_request& R, const kvq_loop_ref& L, int* r0) {
+  const int k = R.n_tokens / KVQ_TILE - 1;
+  if (L.active_idx == nullptr) {
+    *r0 = k * KVQ_TILE;
+    return KVQ_TILE;
+  }
+  *r0 = L.tile_dir[k];
+  return L.tile_dir[k + 1] - L.tile_dir[k];
+}
+
 __device__ __forceinline__ int items_of(const CodecArgs& a, const kvq_request& R, int mode) {
   if (R.n_tokens < 0 || R.n_loops > KVQ_MAX_LOOPS) return 0;
+  if (a.append) {  // the last tile: one K group per head, or one block of at most 64 stored rows
+    if (a.loop >= R.n_loops || R.n_tokens < KVQ_TILE || R.n_tokens % KVQ_TILE) return 0;
+    const kvq_loop_ref& L = R.loop[a.loop];
+    int r0;
+    const int m = last_tile_rows(R, L, &r0);
+    if (m <= 0) return 0;
+    return mode == kModeEncK ? a.H : (mode == kModeEncV ? 1 : 0);
+  }
   switch (mode) {
     case kModeEncK: {  // one item per (K group, head)
       if (a.loop >= R.n_loops) return 0;
@@ -74,7 +93,7 @@ __global__ void __launch_bounds__(1024) items_plan_kernel(const __grid_constant_
   __syncthreads();
   for (int base = 0; base < a.n_requests; base += blockDim.x) {
     int b = base + threadIdx.x;
-    int v = b < a.n_requests ? items_of(a, req_at(a, b), mode) : 0;
+    int v = (b < a.n_requests && !(a.skip && a.skip[b])) ? items_of(a, req_at(a, b), mode) : 0;
     if (mode == kModeNvAmax && v > 0) {  // the NVFP4 encoder's running max |delta| of this stream starts at 0
       const kvq_loop_ref& L = req_at(a, b).loop[a.loop];
       const bool nv = (L.flags & (a.kind == KVQ_K ? KVQ_LOOP_K_NVFP4 : KVQ_LOOP_V_NVFP4)) != 0;
@@ -801,7 +820,8 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
       continue;
     }
     const int local = int(it - prefix[b]);
-    const int g = local / H, h = local % H;
+    // append mode: the item is the last tile's group (the table already counts the tile)
+    const int g = a.append ? S.C.n_tokens / kG - 1 : local / H, h = local % H;
     const LoopPlanes& O = S.C.loop[R];
     const int n = O.n_rows;
     int r0 = g * kG, len = min(kG, n - r0);
@@ -823,6 +843,7 @@ __global__ void __launch_bounds__(kEncKThreads, 3) encode_k_fast_kernel(const __
       continue;
     }
     const uint16_t* x = source_of(a, b);
+    if (a.append) x -= (long long)(S.C.n_tokens - KVQ_TILE) * H * kD;  // the tile's source holds its 64 tokens
     if (tid < len) {
       const int t = O.sparse ? __ldg(O.active + r0 + tid) : r0 + tid;
       S.tok[tid] = t;
@@ -1020,9 +1041,15 @@ __global__ void __launch_bounds__(kEncVFastThreads, 5) encode_v_fast_kernel(cons
     }
     const LoopPlanes& O = C.loop[R];
     const int n = O.n_rows;
-    const int r0 = int(it - prefix[b]) * kG;
-    const int len = min(kG, n - r0);
+    int r0 = int(it - prefix[b]) * kG, len = min(kG, n - r0);
     const uint16_t* x = source_of(a, b);
+    if (a.append) {  // the stored rows of the last tile (the table already counts it)
+      const int k = C.n_tokens / KVQ_TILE - 1;
+      r0 = O.sparse ? __ldg(O.tile_dir + k) : k * KVQ_TILE;
+      len = O.sparse ? __ldg(O.tile_dir + k + 1) - r0 : KVQ_TILE;
+      if (r0 < 0 || len < 0 || len > kG || r0 + len > n) len = 0;
+      x -= (long long)(C.n_tokens - KVQ_TILE) * H * kD;  // the tile's source holds its 64 tokens
+    }
     if (threadIdx.x < len) {
       const int t = O.sparse ? __ldg(O.active + r0 + threadIdx.x) : r0 + threadIdx.x;
       s_tok[threadIdx.x] = t;
@@ -1447,6 +1474,97 @@ __global__ void __launch_bounds__(64) append_index_kernel(const __grid_constant_
 
 cudaError_t launch_append_index(const AppendIndexArgs& a, cudaStream_t stream) {
   append_index_kernel<<<a.n_loops, 64, 0, stream>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- batched tile append: checks, index, table
+
+// One thread per request: the request can take the tile (whole tiles so far,
+// every loop INT4 with room for the tile, a dense base, sparse loops under
+// tile grouping with 0..64 positions, dense loops with all 64).
+__global__ void __launch_bounds__(256) append_check_kernel(const __grid_constant__ AppendBatchArgs a) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= a.n_requests) return;
+  const kvq_request& R = a.reqs[b];
+  bool ok = R.n_tokens >= 0 && R.n_tokens % KVQ_TILE == 0 && R.n_loops == a.n_loops;
+  for (int j = 0; ok && j < a.n_loops; ++j) {
+    const kvq_loop_ref& L = R.loop[j];
+    const int m = a.n_tile_active[j * a.n_requests + b];
+    const int32_t* rel = a.tile_active[j * a.n_requests + b];
+    ok = !(L.flags & (KVQ_LOOP_K_NVFP4 | KVQ_LOOP_V_NVFP4)) && L.row_cap > 0 && L.n_rows + m <= L.row_cap &&
+         R.n_tokens / KVQ_TILE < L.kgroup_cap && L.k_codes && L.k_mins && L.k_scales && L.v_codes && L.v_mins &&
+         L.v_scales;
+    if (L.active_idx == nullptr)
+      ok = ok && rel == nullptr && m == KVQ_TILE && L.n_rows == R.n_tokens;
+    else
+      ok = ok && j > 0 && rel != nullptr && m >= 0 && m <= KVQ_TILE && (L.flags & KVQ_LOOP_K_TILE) && L.tile_dir;
+  }
+  a.skip[b] = ok ? 0 : 1;
+  if (!ok) atomicOr(a.err, 1);
+}
+
+// Block (request, loop), 64 threads: a sparse loop's positions (checked: a bad
+// list sets bit 4 and is replaced by 0 .. m-1) become absolute indices after the
+// stored rows, the tile directory gains the tile, and K groups of tiles without
+// stored rows get +0 parameters.
+__global__ void __launch_bounds__(64) append_index_batch_kernel(const __grid_constant__ AppendBatchArgs a) {
+  const int b = blockIdx.x, j = blockIdx.y;
+  if (a.skip[b]) return;
+  const kvq_request& R = a.reqs[b];
+  const kvq_loop_ref& L = R.loop[j];
+  if (L.active_idx == nullptr) return;
+  const int T = R.n_tokens, k = T / KVQ_TILE, n_old = L.n_rows;
+  const int m = a.n_tile_active[j * a.n_requests + b];
+  const int32_t* rel = a.tile_active[j * a.n_requests + b];
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  const int i = threadIdx.x;
+  int v = 0;
+  if (i < m) {
+    v = rel[i];
+    const int prev = i > 0 ? rel[i - 1] : -1;
+    if (v < 0 || v >= KVQ_TILE || v <= prev) s_bad = 1;
+  }
+  __syncthreads();
+  if (s_bad) {
+    v = i;
+    if (i == 0) atomicOr(a.err, 4);
+  }
+  if (i < m) const_cast<int32_t*>(L.active_idx)[n_old + i] = T + v;
+  if (i == 0) {
+    L.tile_dir[k] = n_old;
+    L.tile_dir[k + 1] = n_old + m;
+  }
+  int g0 = 0, g1 = 0;  // K groups to clear (tile grouping: a tile without stored rows)
+  if (m == 0 && n_old > 0) g0 = k, g1 = k + 1;
+  if (m > 0 && n_old == 0) g0 = 0, g1 = k;
+  const int per = (g1 - g0) * kD;
+  for (int x = i; x < a.H * per; x += blockDim.x) {
+    const int h = x / per, r = x % per;
+    const long long pi = ((long long)h * L.kgroup_cap + g0) * kD + r;
+    L.k_mins[pi] = 0;
+    L.k_scales[pi] = 0;
+  }
+}
+
+// One thread per request: the table counts the tile.
+__global__ void __launch_bounds__(256) append_table_kernel(const __grid_constant__ AppendBatchArgs a) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= a.n_requests || a.skip[b]) return;
+  kvq_request& R = a.reqs[b];
+  for (int j = 0; j < a.n_loops; ++j) R.loop[j].n_rows += a.n_tile_active[j * a.n_requests + b];
+  R.n_tokens += KVQ_TILE;
+}
+
+cudaError_t launch_append_batch_prep(const AppendBatchArgs& a, cudaStream_t stream) {
+  const int blocks = (a.n_requests + 255) / 256;
+  append_check_kernel<<<blocks, 256, 0, stream>>>(a);
+  count_launch();
+  append_index_batch_kernel<<<dim3(a.n_requests, a.n_loops), 64, 0, stream>>>(a);
+  count_launch();
+  append_table_kernel<<<blocks, 256, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }

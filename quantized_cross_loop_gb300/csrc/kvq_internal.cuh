@@ -296,6 +296,8 @@ struct CodecArgs {
   int32_t kind;
   int32_t loop;              // encode and tile directory: loop written; reconstruct: depth
   uint32_t nvfp4;            // bit j: loop j of `kind` is NVFP4 in every request
+  int32_t append;            // batch encode of the last 64-token tile only (the table already counts it)
+  const int32_t* skip;       // append: requests to leave alone (device [n_requests]), or nullptr
   kvq_request one;
   const uint16_t* one_x;
   uint16_t* one_out;
@@ -320,6 +322,20 @@ struct AppendIndexArgs {
   } loop[KVQ_MAX_LOOPS];
 };
 cudaError_t launch_append_index(const AppendIndexArgs& a, cudaStream_t stream);
+
+// Batched tile append (kvq_append_tile_batch): checks, index extension and the
+// table update for every request of a device table, before the encodes.
+struct AppendBatchArgs {
+  kvq_request* reqs;
+  int32_t n_requests;
+  int32_t n_loops;
+  int32_t H;
+  const int32_t* const* tile_active;  // [n_loops * n_requests], loop-major; NULL entries: dense loops
+  const int32_t* n_tile_active;       // [n_loops * n_requests]
+  int32_t* skip;                      // [n_requests]: 1 = request refused (error bit 1)
+  int32_t* err;
+};
+cudaError_t launch_append_batch_prep(const AppendBatchArgs& a, cudaStream_t stream);
 
 // Launches one codec stage (kMode*) for a batch or a single request; a batch
 // first plans its items into prefix_ws ([n_requests + 1] int32, device).

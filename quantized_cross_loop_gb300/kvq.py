@@ -39,6 +39,7 @@ EXPORTED = (
     "kvq_decode_attn_packed_noalloc", "kvq_sparse_workspace_bytes", "kvq_sparse_ref_state",
     "kvq_sparse_decode_attn", "kvq_stream_payload_bytes_ex", "kvq_stream_set_format", "kvq_encode_batch_ex",
     "kvq_reconstruct_batch_ex", "kvq_stream_set_capacity", "kvq_append_workspace_bytes", "kvq_append_tile",
+    "kvq_append_batch_workspace_bytes", "kvq_append_tile_batch",
 )
 
 
@@ -126,6 +127,9 @@ def lib():
             L.kvq_append_workspace_bytes.argtypes = [i32]
             L.kvq_append_workspace_bytes.restype = sz
             L.kvq_append_tile.argtypes = [P(kvq_stream), i32, vp, vp, vp, vp, sz, vp]
+            L.kvq_append_batch_workspace_bytes.argtypes = [i32]
+            L.kvq_append_batch_workspace_bytes.restype = sz
+            L.kvq_append_tile_batch.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
             L.kvq_stream_payload_bytes_ex.restype = ctypes.c_int64
             L.kvq_encode_base.argtypes = [vp, P(kvq_stream), vp]
             L.kvq_encode_residual.argtypes = [vp, P(kvq_stream), i32, P(kvq_stream), vp]
@@ -158,7 +162,7 @@ def lib():
                          "kvq_reconstruct", "kvq_request_fill", "kvq_decode_attn_packed",
                          "kvq_decode_attn_packed_ex", "kvq_encode_batch", "kvq_reconstruct_batch",
                          "kvq_stream_set_format", "kvq_encode_batch_ex", "kvq_reconstruct_batch_ex",
-                         "kvq_stream_set_capacity", "kvq_append_tile"):
+                         "kvq_stream_set_capacity", "kvq_append_tile", "kvq_append_tile_batch"):
                 getattr(L, name).restype = ctypes.c_int32
             _lib = L
     return _lib
@@ -344,9 +348,11 @@ def kvq_append_tile(streams: list, x_tile: list, tile_active: list, workspace: t
             counts[r] = KVQ_TILE
         else:
             a = a.to(device=dev, dtype=torch.int32).contiguous()
+            counts[r] = int(a.numel())
+            if a.numel() == 0:  # an empty sparse tile still passes a valid pointer (NULL means dense)
+                a = torch.zeros(1, dtype=torch.int32, device=dev)
             keep.append(a)
             acts[r] = a.data_ptr()
-            counts[r] = int(a.numel())
     if workspace is None:
         workspace = torch.empty(int(lib().kvq_append_workspace_bytes(n)), dtype=torch.uint8, device=dev)
     _check(lib().kvq_append_tile(arr, n, xs, acts, counts, _dptr(workspace), workspace.numel(), _stream_handle(stream)),
@@ -441,11 +447,13 @@ def kvq_decode_attn_packed(table: RequestTable, q: torch.Tensor, depth: int, n_h
 
 
 def plane_bytes(kind: int, n_rows: int, n_tokens: int, n_heads: int, head_dim: int,
-                kgroup: int = KVQ_KGROUP_COMPACT, fmt: int = KVQ_FMT_INT4) -> list:
+                kgroup: int = KVQ_KGROUP_COMPACT, fmt: int = KVQ_FMT_INT4, row_cap: int = 0, token_cap: int = 0) -> list:
     d = kvq_stream()
     _check(lib().kvq_stream_init(ctypes.byref(d), kind, n_rows, n_tokens, n_heads, head_dim), "kvq_stream_init")
     d.kgroup = kgroup
     _check(lib().kvq_stream_set_format(ctypes.byref(d), fmt), "kvq_stream_set_format")
+    if row_cap or token_cap:
+        _check(lib().kvq_stream_set_capacity(ctypes.byref(d), row_cap, token_cap), "kvq_stream_set_capacity")
     return [int(lib().kvq_plane_bytes(ctypes.byref(d), p)) for p in range(5)]
 
 
@@ -463,9 +471,12 @@ class PackedPool:
     ALIGN = 256
 
     def __init__(self, lengths: list, active_sets: list, n_heads: int, head_dim: int, n_loops: int, device,
-                 kgroup: int = KVQ_KGROUP_COMPACT, formats: list | None = None):
+                 kgroup: int = KVQ_KGROUP_COMPACT, formats: list | None = None, token_caps: list | None = None):
+        """token_caps[b]: tokens request b may grow to by appended tiles (kvq_append_tile_batch);
+        None: no room to grow."""
         device = torch.device(device)
         self.kgroup = kgroup
+        self.token_caps = None if token_caps is None else [int(c) for c in token_caps]
         self.formats = [KVQ_FMT_INT4] * n_loops if formats is None else list(formats)
         if self.formats[0] != KVQ_FMT_INT4:
             raise KvqError("the base loop is INT4")
@@ -481,8 +492,9 @@ class PackedPool:
                 act = active_sets[b][r]
                 n = T if act is None else int(act.numel())
                 fm = self.formats[r]
-                k = plane_bytes(KVQ_K, n, T, n_heads, head_dim, kgroup, fm)
-                v = plane_bytes(KVQ_V, n, T, n_heads, head_dim, KVQ_KGROUP_COMPACT, fm)
+                cap = 0 if self.token_caps is None else self.token_caps[b]
+                k = plane_bytes(KVQ_K, n, T, n_heads, head_dim, kgroup, fm, cap, cap)
+                v = plane_bytes(KVQ_V, n, T, n_heads, head_dim, KVQ_KGROUP_COMPACT, fm, cap, cap)
                 per.append((n, k, v, act is not None))
                 total += sum(self._up(x) for x in k[:3]) + sum(self._up(x) for x in v[:3])
                 if act is not None:
@@ -503,10 +515,11 @@ class PackedPool:
                     idx.view(torch.int32)[:n].copy_(active_sets[b][r].to(device=device, dtype=torch.int32))
                     shared = (idx, self._take(kb[PLANE_TILE_DIR]))
                 fm = self.formats[r]
+                cap = 0 if self.token_caps is None else self.token_caps[b]
                 ks.append(Stream(KVQ_K, n, T, n_heads, head_dim, device, alloc=self._take, shared_index=shared,
-                                 kgroup=kgroup, fmt=fm))
+                                 kgroup=kgroup, fmt=fm, row_cap=cap, token_cap=cap))
                 vs.append(Stream(KVQ_V, n, T, n_heads, head_dim, device, alloc=self._take, shared_index=shared,
-                                 fmt=fm))
+                                 fmt=fm, row_cap=cap, token_cap=cap))
                 self.payload_bytes += payload_bytes(KVQ_K, n, n_heads, head_dim, sparse, T, kgroup, fm)
                 self.payload_bytes += payload_bytes(KVQ_V, n, n_heads, head_dim, False, T, KVQ_KGROUP_COMPACT, fm)
             self.k_streams.append(ks)
@@ -526,6 +539,54 @@ class PackedPool:
     @property
     def n_requests(self):
         return len(self.lengths)
+
+    def append_tile(self, xk_tiles: list, xv_tiles: list, tile_active: list, workspace: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+        """Append one 64-token tile to every request (kvq_append_tile_batch): xk_tiles[r][b],
+        xv_tiles[r][b] are BF16 [64, H, D] device tensors of loop r and request b; tile_active[r][b]
+        an int32 tensor of positions 0..63 (sparse loop) or None (dense loop). The device table is
+        updated in place; sync_counts() brings the new counts to the host objects. Returns the
+        workspace (error word at offset 0)."""
+        dev = self.storage.device
+        nb, nl = self.n_requests, self.n_loops
+        keep = []
+        acts, counts = [], []
+        for r in range(nl):
+            for b in range(nb):
+                a = tile_active[r][b]
+                if a is None:
+                    acts.append(0)
+                    counts.append(KVQ_TILE)
+                else:
+                    a = a.to(device=dev, dtype=torch.int32).contiguous()
+                    counts.append(int(a.numel()))
+                    if a.numel() == 0:  # an empty sparse tile still passes a valid pointer (NULL means dense)
+                        a = torch.zeros(1, dtype=torch.int32, device=dev)
+                    keep.append(a)
+                    acts.append(a.data_ptr())
+        xk = pointer_array([xk_tiles[r][b] for r in range(nl) for b in range(nb)], dev)
+        xv = pointer_array([xv_tiles[r][b] for r in range(nl) for b in range(nb)], dev)
+        act = torch.tensor(acts, dtype=torch.int64, device=dev)
+        cnt = torch.tensor(counts, dtype=torch.int32, device=dev)
+        if workspace is None:
+            workspace = torch.empty(int(lib().kvq_append_batch_workspace_bytes(nb)), dtype=torch.uint8, device=dev)
+        _check(lib().kvq_append_tile_batch(_dptr(self.table.table), nb, self.n_heads, self.head_dim, nl, _dptr(xk),
+                                           _dptr(xv), _dptr(act), _dptr(cnt), _dptr(workspace), workspace.numel(),
+                                           _stream_handle(stream)), "kvq_append_tile_batch")
+        self._append_keep = (keep, xk, xv, act, cnt, xk_tiles, xv_tiles)
+        return workspace
+
+    def sync_counts(self):
+        """Read the device table back and update the host stream objects' row and token counts
+        (a device-to-host read: for tests and tools, not for the serving path)."""
+        raw = self.table.table.cpu().numpy().tobytes()
+        host = (kvq_request * self.n_requests).from_buffer_copy(raw[: ctypes.sizeof(kvq_request) * self.n_requests])
+        for b in range(self.n_requests):
+            self.lengths[b] = host[b].n_tokens
+            for r in range(self.n_loops):
+                for st in (self.k_streams[b][r], self.v_streams[b][r]):
+                    st.n_rows, st.n_tokens = host[b].loop[r].n_rows, host[b].n_tokens
+                    st.desc.n_rows, st.desc.n_tokens = st.n_rows, st.n_tokens
 
 
 def pointer_array(tensors: list, device) -> torch.Tensor:

@@ -123,3 +123,78 @@ def test_append_refusals():
         kvq.kvq_append_tile(chain(TILE, fmt=kvq.KVQ_FMT_NVFP4), x_tile, rel)
     with pytest.raises(kvq.KvqError, match="multiple"):
         kvq.kvq_append_tile(chain(TILE, T=T0 - 8, cap=T0 + 64), x_tile, rel)
+
+
+def test_batched_append_equals_full_encode():
+    """kvq_append_tile_batch: tiles appended to every request of a pool in one call
+    per tile give the bytes of the oracle's encode of each whole chain (K and V),
+    update the device table, and the attention reads the grown chains."""
+    H, D_, loops = 8, 128, 4
+    dev = torch.device("cuda")
+    lengths0 = [256, 0, 128, 320, 64]
+    n_tiles = 2
+    caps = [T + 64 * n_tiles for T in lengths0]
+    xs_all, act_all = [], []
+    for b, Ttot in enumerate(caps):
+        xs_all.append({kind: drift(Ttot, H, loops, 1100 + 2 * b + kind) for kind in (0, 1)})
+        act_all.append(nested(Ttot, (1.0, 1.0, 0.5, 0.1), 1110 + b))
+    act0 = [[None if a is None else a[a < lengths0[b]].contiguous().to(dev) for a in act_all[b]]
+            for b in range(len(caps))]
+    pool = kvq.PackedPool(lengths0, act0, H, D_, loops, dev, kgroup=TILE, token_caps=caps)
+    for j in range(loops):
+        for kind in (kvq.KVQ_K, kvq.KVQ_V):
+            kvq.kvq_encode_batch(pool, kind, j, kvq.pointer_array(
+                [xs_all[b][kind][j][:lengths0[b]].contiguous().to(dev) for b in range(len(caps))], dev))
+    for k in range(n_tiles):
+        xk = [[None] * len(caps) for _ in range(loops)]
+        xv = [[None] * len(caps) for _ in range(loops)]
+        rel = [[None] * len(caps) for _ in range(loops)]
+        for b in range(len(caps)):
+            t0 = lengths0[b] + 64 * k
+            for j in range(loops):
+                xk[j][b] = xs_all[b][0][j][t0:t0 + 64].contiguous().to(dev)
+                xv[j][b] = xs_all[b][1][j][t0:t0 + 64].contiguous().to(dev)
+                a = act_all[b][j]
+                rel[j][b] = None if a is None else (a[(a >= t0) & (a < t0 + 64)] - t0).to(torch.int32)
+        ws = pool.append_tile(xk, xv, rel)
+        torch.cuda.synchronize()
+        assert kvq.attn_error_word(ws) == 0
+    pool.sync_counts()
+    for b, Ttot in enumerate(caps):
+        assert pool.lengths[b] == Ttot
+        for kind, streams in ((kvq.KVQ_K, pool.k_streams[b]), (kvq.KVQ_V, pool.v_streams[b])):
+            os_ = oracle_chain(kind, xs_all[b][kind], act_all[b])
+            for r in range(loops):
+                P.assert_stream_equal(streams[r], os_[r], f"req {b} kind {kind} loop {r + 1}")
+                P.assert_tile_dir(streams[r])
+    # the device table already describes the grown chains
+    Hq = 32
+    q = torch.randn((len(caps), Hq, D_), generator=torch.Generator().manual_seed(1120)).to(torch.bfloat16)
+    out = kvq.kvq_decode_attn_packed(pool.table, q.cuda(), 4, H, algo=kvq.ATTN_MMA).cpu().numpy()
+    scale = 1.0 / math.sqrt(D_)
+    for b in range(len(caps)):
+        ok_ = oracle_chain(kvq.KVQ_K, xs_all[b][0], act_all[b])
+        ov_ = oracle_chain(kvq.KVQ_V, xs_all[b][1], act_all[b])
+        ref = O.attention_f32(bf16_bits(q[b]), O.decode_f32(ok_, 4), O.decode_f32(ov_, 4), scale)
+        P.assert_attention_close(out[b], ref, f"req {b}")
+
+
+def test_batched_append_refuses_per_request():
+    """A request without room for the tile is left unchanged (error bit 1); the
+    others grow."""
+    H, D_, loops = 8, 128, 2
+    dev = torch.device("cuda")
+    lengths0 = [128, 64]
+    caps = [192, 64]  # request 1 has no room
+    xs = [drift(c if c > L else L + 64, H, loops, 1200 + b) for b, (L, c) in enumerate(zip(lengths0, caps))]
+    pool = kvq.PackedPool(lengths0, [[None, None]] * 2, H, D_, loops, dev, kgroup=TILE, token_caps=caps)
+    for j in range(loops):
+        ptr = kvq.pointer_array([xs[b][j][:lengths0[b]].contiguous().to(dev) for b in range(2)], dev)
+        kvq.kvq_encode_batch(pool, kvq.KVQ_K, j, ptr)
+        kvq.kvq_encode_batch(pool, kvq.KVQ_V, j, ptr)
+    tiles = [[xs[b][j][lengths0[b]:lengths0[b] + 64].contiguous().to(dev) for b in range(2)] for j in range(loops)]
+    ws = pool.append_tile(tiles, tiles, [[None, None]] * loops)
+    torch.cuda.synchronize()
+    assert kvq.attn_error_word(ws) & 1
+    pool.sync_counts()
+    assert pool.lengths == [192, 64]
