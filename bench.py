@@ -524,35 +524,49 @@ def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, re
             "error_word": err}
 
 
-def run_append_extra(torch, kvq, reqs, H, D, depth, dev, stream, n_req=8):
-    """Latency of the tail flush (RFC §3.3): one 64-token tile appended to the K
-    and V chains of a request (tile-local K grouping), averaged over n_req
-    requests; the chains hold the request's tokens up to the last whole tile."""
+def run_append_extra(torch, kvq, reqs, H, D, depth, dev, stream, reps=5):
+    """Cost of the tail flush (RFC §3.3): one 64-token tile appended to the K and V
+    chains of every request in one batched call (kvq_append_tile_batch), on a pool
+    of growable chains (tile-local K grouping) holding each request's tokens up to
+    its last whole tile but one; `reps` fresh pools are timed and averaged."""
     from quantized_cross_loop_gb300.kvq import KVQ_KGROUP_TILE
-    chains, tiles = [], []
-    for r in reqs[:n_req]:
-        T0 = (r.T // 64 - 1) * 64  # leave the last whole tile to append
-        cap = T0 + 64
-        for kind, xs in ((kvq.KVQ_K, r.xk), (kvq.KVQ_V, r.xv)):
-            gs = [kvq.kvq_encode_base(xs[0][:T0], kind, kgroup=KVQ_KGROUP_TILE, token_cap=cap)]
-            for j in range(1, depth):
-                a = r.active[j]
-                a0 = None if a is None else a[a < T0].contiguous()
-                gs.append(kvq.kvq_encode_residual(xs[j][:T0], gs, a0, row_cap=cap, token_cap=cap))
-            rel = [None if a is None else (a[(a >= T0) & (a < T0 + 64)] - T0).to(torch.int32) for a in r.active]
-            chains.append(gs)
-            tiles.append(([x[T0:T0 + 64].contiguous() for x in xs], rel))
-    ws = torch.empty(int(kvq.lib().kvq_append_workspace_bytes(depth)), dtype=torch.uint8, device=dev)
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for gs, (xt, rel) in zip(chains, tiles):
-        kvq.kvq_append_tile(gs, xt, rel, workspace=ws)
-    b.record(stream)
-    torch.cuda.synchronize()
-    err = kvq.attn_error_word(ws)
-    return {"requests": len(chains) // 2, "us_per_request_k_and_v": a.elapsed_time(b) * 1e3 / max(len(chains) // 2, 1),
-            "launches_per_kind": 1 + depth, "error_word": err}
+    B = len(reqs)
+    T0 = [(r.T // 64 - 1) * 64 for r in reqs]
+    act0 = [[None if a is None else a[a < T0[b]].contiguous() for a in reqs[b].active] for b in range(B)]
+    xk = [[reqs[b].xk[j][T0[b]:T0[b] + 64].contiguous() for b in range(B)] for j in range(depth)]
+    xv = [[reqs[b].xv[j][T0[b]:T0[b] + 64].contiguous() for b in range(B)] for j in range(depth)]
+    rel = [[None if reqs[b].active[j] is None else
+            (reqs[b].active[j][(reqs[b].active[j] >= T0[b]) & (reqs[b].active[j] < T0[b] + 64)] - T0[b]).to(torch.int32)
+            for b in range(B)] for j in range(depth)]
+    src = [[kvq.pointer_array([reqs[b].xk[j] for b in range(B)], dev) for j in range(depth)],
+           [kvq.pointer_array([reqs[b].xv[j] for b in range(B)], dev) for j in range(depth)]]
+    total, err = 0.0, 0
+    for _ in range(reps):
+        pool = kvq.PackedPool(T0, act0, H, D, depth, dev, kgroup=KVQ_KGROUP_TILE, token_caps=[t + 64 for t in T0])
+        for j in range(depth):
+            kvq.kvq_encode_batch(pool, kvq.KVQ_K, j, src[0][j], stream=stream)
+            kvq.kvq_encode_batch(pool, kvq.KVQ_V, j, src[1][j], stream=stream)
+        ws = torch.empty(int(kvq.lib().kvq_append_batch_workspace_bytes(B)), dtype=torch.uint8, device=dev)
+        pool.append_tile(xk, xv, rel, workspace=ws, stream=stream)  # warm-up call
+        torch.cuda.synchronize()
+        err |= kvq.attn_error_word(ws)
+        pool2 = kvq.PackedPool(T0, act0, H, D, depth, dev, kgroup=KVQ_KGROUP_TILE, token_caps=[t + 64 for t in T0])
+        for j in range(depth):
+            kvq.kvq_encode_batch(pool2, kvq.KVQ_K, j, src[0][j], stream=stream)
+            kvq.kvq_encode_batch(pool2, kvq.KVQ_V, j, src[1][j], stream=stream)
+        prep = pool2.prepare_append(xk, xv, rel)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pool2.append_tile(workspace=ws, stream=stream, prepared=prep)
+        b.record(stream)
+        torch.cuda.synchronize()
+        total += a.elapsed_time(b)
+        err |= kvq.attn_error_word(ws)
+        del pool, pool2
+    ms = total / reps
+    return {"requests": B, "tokens_per_request": 64, "ms_per_call": ms, "us_per_request_k_and_v": ms * 1e3 / B,
+            "launches": 3 + 4 * depth, "error_word": err}
 
 
 def run_nvfp4_extra(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, timed, ptrs, n_sample=16):

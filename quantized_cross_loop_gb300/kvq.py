@@ -540,40 +540,48 @@ class PackedPool:
     def n_requests(self):
         return len(self.lengths)
 
-    def append_tile(self, xk_tiles: list, xv_tiles: list, tile_active: list, workspace: torch.Tensor | None = None,
-                    stream=None) -> torch.Tensor:
-        """Append one 64-token tile to every request (kvq_append_tile_batch): xk_tiles[r][b],
-        xv_tiles[r][b] are BF16 [64, H, D] device tensors of loop r and request b; tile_active[r][b]
-        an int32 tensor of positions 0..63 (sparse loop) or None (dense loop). The device table is
-        updated in place; sync_counts() brings the new counts to the host objects. Returns the
-        workspace (error word at offset 0)."""
+    def prepare_append(self, xk_tiles: list, xv_tiles: list, tile_active: list):
+        """Device argument arrays of one append_tile call: xk_tiles[r][b], xv_tiles[r][b] are
+        BF16 [64, H, D] device tensors of loop r and request b; tile_active[r][b] an int32
+        tensor of positions 0..63 (sparse loop) or None (dense loop)."""
         dev = self.storage.device
         nb, nl = self.n_requests, self.n_loops
-        keep = []
-        acts, counts = [], []
+        keep, acts, counts = [], [], []
         for r in range(nl):
             for b in range(nb):
                 a = tile_active[r][b]
                 if a is None:
                     acts.append(0)
                     counts.append(KVQ_TILE)
-                else:
-                    a = a.to(device=dev, dtype=torch.int32).contiguous()
-                    counts.append(int(a.numel()))
-                    if a.numel() == 0:  # an empty sparse tile still passes a valid pointer (NULL means dense)
-                        a = torch.zeros(1, dtype=torch.int32, device=dev)
-                    keep.append(a)
-                    acts.append(a.data_ptr())
+                    continue
+                a = a.to(device=dev, dtype=torch.int32).contiguous()
+                counts.append(int(a.numel()))
+                if a.numel() == 0:  # an empty sparse tile still passes a valid pointer (NULL means dense)
+                    a = torch.zeros(1, dtype=torch.int32, device=dev)
+                keep.append(a)
+                acts.append(a.data_ptr())
         xk = pointer_array([xk_tiles[r][b] for r in range(nl) for b in range(nb)], dev)
         xv = pointer_array([xv_tiles[r][b] for r in range(nl) for b in range(nb)], dev)
         act = torch.tensor(acts, dtype=torch.int64, device=dev)
         cnt = torch.tensor(counts, dtype=torch.int32, device=dev)
+        return (xk, xv, act, cnt, keep, xk_tiles, xv_tiles)
+
+    def append_tile(self, xk_tiles: list = None, xv_tiles: list = None, tile_active: list = None,
+                    workspace: torch.Tensor | None = None, stream=None, prepared=None) -> torch.Tensor:
+        """Append one 64-token tile to every request (kvq_append_tile_batch), from the tiles
+        (see prepare_append) or from a prepare_append result. The device table is updated
+        in place; sync_counts() brings the new counts to the host objects. Returns the
+        workspace (error word at offset 0)."""
+        dev = self.storage.device
+        args = prepared if prepared is not None else self.prepare_append(xk_tiles, xv_tiles, tile_active)
+        xk, xv, act, cnt = args[:4]
+        nb = self.n_requests
         if workspace is None:
             workspace = torch.empty(int(lib().kvq_append_batch_workspace_bytes(nb)), dtype=torch.uint8, device=dev)
-        _check(lib().kvq_append_tile_batch(_dptr(self.table.table), nb, self.n_heads, self.head_dim, nl, _dptr(xk),
-                                           _dptr(xv), _dptr(act), _dptr(cnt), _dptr(workspace), workspace.numel(),
-                                           _stream_handle(stream)), "kvq_append_tile_batch")
-        self._append_keep = (keep, xk, xv, act, cnt, xk_tiles, xv_tiles)
+        _check(lib().kvq_append_tile_batch(_dptr(self.table.table), nb, self.n_heads, self.head_dim, self.n_loops,
+                                           _dptr(xk), _dptr(xv), _dptr(act), _dptr(cnt), _dptr(workspace),
+                                           workspace.numel(), _stream_handle(stream)), "kvq_append_tile_batch")
+        self._append_keep = args
         return workspace
 
     def sync_counts(self):
