@@ -1437,6 +1437,189 @@ __global__ void __launch_bounds__(kReconVFastThreads, 5) reconstruct_v_fast_kern
   }
 }
 
+// ---------------------------------------------------------------- NVFP4 residual encode (fast, chains up to 4 loops)
+//
+// The two NVFP4 passes of a residual loop r <= 3 in the layout of the fast V
+// encoder: item = 64 stored rows (all heads), eight lanes per (row, head), lane
+// `sub` = channels 16 sub .. 16 sub + 15 = exactly one NVFP4 block, so a block's
+// max |delta| is lane-local. The predecessor chain is decoded per loop in its own
+// format (INT4 K, INT4 V, or NVFP4). Codes come from the product delta * RN32(1 /
+// e_b); an element whose product lies within 2^-20 (relative) of an E2M1
+// decision boundary takes the IEEE quotient, the definition's, instead.
+
+namespace fast {
+
+// 16 channels of one stored row of an NVFP4 loop (codes cw, block scale sb, tensor
+// scale st) as 8 BF16 pairs: RN_bf16(RN32(RN32(e2m1 * sb) * st)).
+__device__ __forceinline__ void dequant_nv16(uint2 cw, float sb, float st, uint32_t* out) {
+  const uint32_t w[2] = {cw.x, cw.y};
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t byte = (w[h] >> (8 * k)) & 0xFFu;
+      const float lo = __fmul_rn(__fmul_rn(e2m1_to_f32(byte & 0xFu), sb), st);
+      const float hi = __fmul_rn(__fmul_rn(e2m1_to_f32(byte >> 4), sb), st);
+      out[4 * h + k] = f2_to_bf2(make_float2(lo, hi));
+    }
+}
+
+// E2M1 code of the quotient y (sign of y kept); *near: |y| lies within 2^-20
+// (relative) of a decision boundary, where a product and the IEEE quotient may
+// fall on different sides.
+__device__ __forceinline__ uint32_t e2m1_code_near(float y, bool* near) {
+  const float a = fabsf(y);
+  const uint32_t c = f32_to_e2m1(y);
+  // boundaries between magnitudes: 0.25, 0.75, 1.25, 1.75 (steps of 0.5), then 2.5, 3.5, 5
+  const int m = int(c & 7u);
+  const float up = m < 4 ? 0.25f + 0.5f * float(m) : (m == 4 ? 2.5f : (m == 5 ? 3.5f : (m == 6 ? 5.0f : 1e30f)));
+  const float lo = m == 0 ? -1.0f : (m <= 4 ? 0.5f * float(m) - 0.25f : (m == 5 ? 2.5f : (m == 6 ? 3.5f : 5.0f)));
+  const float tol = a * 9.5367431640625e-7f + 1e-38f;  // 2^-20 relative
+  *near = (up - a <= tol) || (a - lo <= tol);
+  return c;
+}
+
+}  // namespace fast
+
+template <int R, bool kAmax>
+__global__ void __launch_bounds__(kEncVFastThreads, 3) nvfp4_encode_fast_kernel(const __grid_constant__ CodecArgs a,
+                                                                             const int32_t* prefix_ws) {
+  using namespace fast;
+  constexpr int RA = R > 0 ? R : 1;
+  constexpr int kWarps = kEncVFastThreads / 32;
+  const int32_t* prefix = prefix_ws ? prefix_ws : a.one_prefix;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane & 7, lg = lane >> 3;
+  const int H = a.H;
+  __shared__ Chain C;
+  __shared__ int s_tok[kG];
+  __shared__ int s_row[RA][kG];
+
+  const ItemRange ir = cta_items(prefix, a.n_requests);
+  int cur_b = -1;
+  for (long long it = ir.begin; it < ir.end; ++it) {
+    const int b = owner_next(prefix, a.n_requests, it, cur_b);
+    if (b != cur_b) {
+      __syncthreads();  // every thread is done with the previous request's chain
+      if (threadIdx.x == 0) fill_chain(req_at(a, b), a.kind, R + 1, H, C);
+      cur_b = b;
+    }
+    __syncthreads();
+    const LoopPlanes& O = C.loop[R];
+    if (R < 1 || O.fmt != KVQ_FMT_NVFP4) {  // the table does not hold an NVFP4 residual here
+      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 64);
+      continue;
+    }
+    const int n = O.n_rows;
+    const int r0 = int(it - prefix[b]) * kG;
+    const int len = min(kG, n - r0);
+    const uint16_t* x = source_of(a, b);
+    if (threadIdx.x < len) {
+      const int t = O.sparse ? __ldg(O.active + r0 + threadIdx.x) : r0 + threadIdx.x;
+      s_tok[threadIdx.x] = t;
+#pragma unroll
+      for (int j = 0; j < R; ++j) s_row[j][threadIdx.x] = row_of(C.loop[j], t);
+    }
+    __syncthreads();
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) {
+      if (threadIdx.x == 0 && a.err) atomicOr(a.err, 16);
+      continue;
+    }
+    float* rec = reinterpret_cast<float*>(const_cast<uint16_t*>(O.scales));
+    float st = 0.0f, six_st = 0.0f;
+    bool all_zero = true;
+    if (!kAmax) {
+      const float amax = rec[1];
+      all_zero = !(amax > 0.0f);
+      st = __fdiv_rn(amax, 2688.0f);
+      six_st = __fmul_rn(6.0f, st);
+    }
+    float wmax = 0.0f;
+    const int nquads = H * (kG / 4);
+    for (int qd = warp; qd < nquads; qd += kWarps) {
+      const int h = qd / (kG / 4);
+      const int i = (qd % (kG / 4)) * 4 + lg;
+      const bool live = i < len;
+      uint32_t d[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (live) {
+        const int t = s_tok[i];
+        const uint4* src = reinterpret_cast<const uint4*>(x + ((long long)t * H + h) * kD + 16 * sub);
+        const uint4 xa = __ldg(src), xb = __ldg(src + 1);
+        const uint32_t xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+        uint32_t acc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = 0u;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int row = s_row[j][i];
+          if (row < 0) continue;  // absent: the predecessor inherits
+          const LoopPlanes& L = C.loop[j];
+          const long long rr = (long long)h * L.stride + row;
+          const uint2 cw = __ldg(reinterpret_cast<const uint2*>(L.codes + rr * kRowBytes + 8 * sub));
+          uint32_t dq[8];
+          if (L.fmt == KVQ_FMT_NVFP4) {
+            dequant_nv16(cw, nvfp4_block_scale(L, h, row, sub), nvfp4_tensor_scale(L), dq);
+          } else if (a.kind == KVQ_K) {
+            float2 m[8], s[8];
+            load_kpar16_global(L, h, k_group(L, t, row), sub, m, s);
+            dequant_word_pp(cw.x, m, s, dq);
+            dequant_word_pp(cw.y, m + 4, s + 4, dq + 4);
+          } else {
+            const float mf = f16_bits_to_f32(__ldg(L.mins + rr * (kD / kG) + (sub >> 2)));
+            const float sf = f16_bits_to_f32(__ldg(L.scales + rr * (kD / kG) + (sub >> 2)));
+            dequant_word(cw.x, make_float2(mf, mf), make_float2(sf, sf), dq);
+            dequant_word(cw.y, make_float2(mf, mf), make_float2(sf, sf), dq + 4);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc[k] = (j == 0) ? dq[k] : bf2_add(acc[k], dq[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) d[k] = bf2_sub(xv[k], acc[k]);
+      }
+      // the block's max |delta| (BF16 pairs with the sign bits cleared)
+      uint32_t am2 = 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) am2 = bf2_max(am2, d[k] & 0x7FFF7FFFu);
+      const float ab = fmaxf(bf_lo(am2), bf_hi(am2));
+      if (kAmax) {
+        wmax = fmaxf(wmax, ab);
+        continue;
+      }
+      const uint32_t sb = all_zero ? 0u : f32_to_e4m3(__fdiv_rn(ab, six_st));
+      const float eb = __fmul_rn(e4m3_to_f32(sb), st);
+      const float rc = eb != 0.0f ? __frcp_rn(eb) : 0.0f;
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const float v = hf ? bf_hi(d[k]) : bf_lo(d[k]);
+          uint32_t code = 0u;
+          if (eb != 0.0f) {
+            bool near;
+            code = e2m1_code_near(__fmul_rn(v, rc), &near);
+            if (near) code = f32_to_e2m1(__fdiv_rn(v, eb));
+          }
+          w[k >> 2] |= code << (8 * (k & 3) + 4 * hf);
+        }
+      }
+      if (live) {
+        const long long rr = (long long)h * O.stride + r0 + i;
+        *reinterpret_cast<uint2*>(const_cast<uint8_t*>(O.codes) + rr * kRowBytes + 8 * sub) = make_uint2(w[0], w[1]);
+        reinterpret_cast<uint8_t*>(const_cast<uint16_t*>(O.mins))[rr * (kD / 16) + sub] = uint8_t(sb);
+      }
+    }
+    if (kAmax) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
+      if (lane == 0 && wmax > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(rec + 1), __float_as_uint(wmax));
+      wmax = 0.0f;
+    } else if (r0 == 0 && threadIdx.x == 0) {
+      rec[0] = st;  // the stream's tensor scale, once
+    }
+  }
+}
+
 // ---------------------------------------------------------------- tile append: index planes
 
 // One block per loop. A position outside [0, 64), or not ascending, sets bit 4
@@ -1632,9 +1815,28 @@ cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, in
   };
   switch (mode) {
     case kModeNvAmax:
-      nvfp4_encode_kernel<true><<<grid_for(4), kEncVThreads, 0, stream>>>(a, prefix);
-      count_launch();
-      nvfp4_encode_kernel<false><<<grid_for(4), kEncVThreads, 0, stream>>>(a, prefix);
+      switch (a.loop) {  // residual loops of chains up to 4 loops: the fast passes
+        case 1:
+          run(nvfp4_encode_fast_kernel<1, true>, kEncVFastThreads);
+          count_launch();
+          run(nvfp4_encode_fast_kernel<1, false>, kEncVFastThreads);
+          break;
+        case 2:
+          run(nvfp4_encode_fast_kernel<2, true>, kEncVFastThreads);
+          count_launch();
+          run(nvfp4_encode_fast_kernel<2, false>, kEncVFastThreads);
+          break;
+        case 3:
+          run(nvfp4_encode_fast_kernel<3, true>, kEncVFastThreads);
+          count_launch();
+          run(nvfp4_encode_fast_kernel<3, false>, kEncVFastThreads);
+          break;
+        default:
+          nvfp4_encode_kernel<true><<<grid_for(4), kEncVThreads, 0, stream>>>(a, prefix);
+          count_launch();
+          nvfp4_encode_kernel<false><<<grid_for(4), kEncVThreads, 0, stream>>>(a, prefix);
+          break;
+      }
       break;
     case kModeEncK:
       switch (nv_chain ? -1 : a.loop) {
