@@ -221,21 +221,6 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
 __device__ __forceinline__ uint32_t h2u(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
 __device__ __forceinline__ __half2 u2h(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
 
-// Two E2M1 codes (the low byte of x: low nibble, high nibble) as an exact FP16
-// pair {low, high}, by the hardware conversion.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t x) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(x));
-  return r;
-}
-
-// Two E4M3 values (the low 16 bits of x) as an exact FP16 pair {low byte, high byte}.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(r) : "r"(x));
-  return r;
-}
-
 // Nibble c (0..3) of each 16-bit half of x as FP16 e2m1 * 2^-14: the nibble is
 // moved to bits 12..15, then its magnitude bits to 9..11 under its sign at 15.
 template <int C>

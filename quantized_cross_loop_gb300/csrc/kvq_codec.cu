@@ -1256,6 +1256,39 @@ __device__ __forceinline__ void load_kpar16_global(const LoopPlanes& L, int h, i
   }
 }
 
+namespace fast {
+
+// 16 channels of one stored row of an NVFP4 loop (codes cw, block scale sb, tensor
+// scale st) as 8 BF16 pairs: RN_bf16(RN32(RN32(e2m1 * sb) * st)). The product
+// e2m1 * sb carries at most 6 significant bits and lies in [2^-10, 2880] or is
+// zero, so the FP16 pair product of the hardware-converted codes is that exact
+// FP32 product.
+__device__ __forceinline__ void dequant_nv16(uint2 cw, float sb, float st, uint32_t* out) {
+  const __half2 sb2 = __float2half2_rn(sb);  // an E4M3 value: exact in FP16
+  const uint32_t w[2] = {cw.x, cw.y};
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t e2 = e2m1x2_to_f16x2(w[h] >> (8 * k));
+      const float2 p = __half22float2(__hmul2(*reinterpret_cast<const __half2*>(&e2), sb2));
+      out[4 * h + k] = f2_to_bf2(make_float2(__fmul_rn(p.x, st), __fmul_rn(p.y, st)));
+    }
+}
+
+// E2M1 codes of the pair (lo, hi) as one byte {lo in bits 0..3, hi in 4..7}, by
+// the hardware conversion: nearest value, ties to the even code (the even
+// mantissa), saturating at 6, the sign kept (zero included).
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\tcvt.u32.u8 %0, b;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+}  // namespace fast
+
 // K: item = (64-token tile, head), 128 threads; eight lanes per token (lane
 // `sub` = channels 16 sub .. +15) and four tokens per lane (16 w + 4 u + lg), so
 // a lane loads each loop's parameters once for its four tokens (twice when a
@@ -1265,7 +1298,7 @@ constexpr int kReconKTok = 4;                             // tokens per lane
 // (four 128-thread blocks per SM at 128 registers: faster than three at 159 despite a few spilled words)
 constexpr int kReconKThreads = KVQ_TILE * 8 / kReconKTok;  // eight lanes per token, one tile per item
 
-template <int DEPTH>
+template <int DEPTH, bool kNv>
 __global__ void __launch_bounds__(kReconKThreads, 4) reconstruct_k_fast_kernel(const __grid_constant__ CodecArgs a,
                                                                             const int32_t* prefix_ws) {
   using namespace fast;
@@ -1285,7 +1318,7 @@ __global__ void __launch_bounds__(kReconKThreads, 4) reconstruct_k_fast_kernel(c
       __syncthreads();
       cur_b = b;
     }
-    if (C.any_nvfp4) {  // NVFP4 loops: the INT4-only fast path refuses the request
+    if (!kNv && C.any_nvfp4) {  // NVFP4 loops: the INT4-only instantiation refuses the request
       if (tid == 0 && a.err) atomicOr(a.err, 64);
       continue;
     }
@@ -1322,6 +1355,19 @@ __global__ void __launch_bounds__(kReconKThreads, 4) reconstruct_k_fast_kernel(c
 #pragma unroll
     for (int j = 0; j < DEPTH; ++j) {
       const LoopPlanes& L = C.loop[j];
+      if (kNv && L.fmt == KVQ_FMT_NVFP4) {  // NVFP4 residual: the lane's 16 channels are one block
+        const float st = nvfp4_tensor_scale(L);
+#pragma unroll
+        for (int u = 0; u < kReconKTok; ++u) {
+          const int row = rows[u][j];
+          if (row < 0) continue;
+          uint32_t dq[8];
+          dequant_nv16(cw[u][j], nvfp4_block_scale(L, h, row, sub), st, dq);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[u][e] = bf2_add(acc[u][e], dq[e]);
+        }
+        continue;
+      }
       float2 m[8], s[8];
       int cached = -1;
 #pragma unroll
@@ -1357,7 +1403,7 @@ __global__ void __launch_bounds__(kReconKThreads, 4) reconstruct_k_fast_kernel(c
 // pairs, i.e. 1 KB of contiguous output, and finds the tile's rows itself.
 constexpr int kReconVFastThreads = 256;
 
-template <int DEPTH>
+template <int DEPTH, bool kNv>
 __global__ void __launch_bounds__(kReconVFastThreads, 5) reconstruct_v_fast_kernel(const __grid_constant__ CodecArgs a,
                                                                                 const int32_t* prefix_ws) {
   using namespace fast;
@@ -1378,7 +1424,7 @@ __global__ void __launch_bounds__(kReconVFastThreads, 5) reconstruct_v_fast_kern
       __syncthreads();
       cur_b = b;
     }
-    if (C.any_nvfp4) {  // NVFP4 loops: the INT4-only fast path refuses the request
+    if (!kNv && C.any_nvfp4) {  // NVFP4 loops: the INT4-only instantiation refuses the request
       if (tid == 0 && a.err) atomicOr(a.err, 64);
       continue;
     }
@@ -1411,8 +1457,13 @@ __global__ void __launch_bounds__(kReconVFastThreads, 5) reconstruct_v_fast_kern
           const LoopPlanes& L = C.loop[j];
           const long long rr = (long long)h * L.stride + row;
           cw[j] = __ldg(reinterpret_cast<const uint2*>(L.codes + rr * kRowBytes + 8 * sub));
-          m16[j] = __ldg(L.mins + rr * (kD / kG) + (sub >> 2));
-          s16[j] = __ldg(L.scales + rr * (kD / kG) + (sub >> 2));
+          if (kNv && L.fmt == KVQ_FMT_NVFP4) {  // E4M3 block scale of the lane's block; the tensor scale
+            m16[j] = __ldg(reinterpret_cast<const uint8_t*>(L.mins) + rr * (kD / 16) + sub);
+            s16[j] = __float_as_uint(nvfp4_tensor_scale(L));
+          } else {
+            m16[j] = __ldg(L.mins + rr * (kD / kG) + (sub >> 2));
+            s16[j] = __ldg(L.scales + rr * (kD / kG) + (sub >> 2));
+          }
         }
       }
       uint32_t acc[8];
@@ -1421,10 +1472,14 @@ __global__ void __launch_bounds__(kReconVFastThreads, 5) reconstruct_v_fast_kern
 #pragma unroll
       for (int j = 0; j < DEPTH; ++j) {
         if (!have[j]) continue;
-        const float mf = f16_bits_to_f32(uint16_t(m16[j])), sf = f16_bits_to_f32(uint16_t(s16[j]));
         uint32_t dq[8];
-        dequant_word(cw[j].x, make_float2(mf, mf), make_float2(sf, sf), dq);
-        dequant_word(cw[j].y, make_float2(mf, mf), make_float2(sf, sf), dq + 4);
+        if (kNv && C.loop[j].fmt == KVQ_FMT_NVFP4) {
+          dequant_nv16(cw[j], e4m3_to_f32(m16[j]), __uint_as_float(s16[j]), dq);
+        } else {
+          const float mf = f16_bits_to_f32(uint16_t(m16[j])), sf = f16_bits_to_f32(uint16_t(s16[j]));
+          dequant_word(cw[j].x, make_float2(mf, mf), make_float2(sf, sf), dq);
+          dequant_word(cw[j].y, make_float2(mf, mf), make_float2(sf, sf), dq + 4);
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = (j == 0) ? dq[e] : bf2_add(acc[e], dq[e]);
       }
@@ -1443,43 +1498,11 @@ __global__ void __launch_bounds__(kReconVFastThreads, 5) reconstruct_v_fast_kern
 // encoder: item = 64 stored rows (all heads), eight lanes per (row, head), lane
 // `sub` = channels 16 sub .. 16 sub + 15 = exactly one NVFP4 block, so a block's
 // max |delta| is lane-local. The predecessor chain is decoded per loop in its own
-// format (INT4 K, INT4 V, or NVFP4). Codes come from the product delta * RN32(1 /
-// e_b); an element whose product lies within 2^-20 (relative) of an E2M1
-// decision boundary takes the IEEE quotient, the definition's, instead.
+// format (INT4 K, INT4 V, or NVFP4). Codes come from the hardware E2M1
+// conversion of the product delta * RN32(1 / e_b); a pair whose product lies
+// within 2^-20 (relative) of an E2M1 decision boundary takes the IEEE quotients,
+// the definition's, instead.
 
-namespace fast {
-
-// 16 channels of one stored row of an NVFP4 loop (codes cw, block scale sb, tensor
-// scale st) as 8 BF16 pairs: RN_bf16(RN32(RN32(e2m1 * sb) * st)).
-__device__ __forceinline__ void dequant_nv16(uint2 cw, float sb, float st, uint32_t* out) {
-  const uint32_t w[2] = {cw.x, cw.y};
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t byte = (w[h] >> (8 * k)) & 0xFFu;
-      const float lo = __fmul_rn(__fmul_rn(e2m1_to_f32(byte & 0xFu), sb), st);
-      const float hi = __fmul_rn(__fmul_rn(e2m1_to_f32(byte >> 4), sb), st);
-      out[4 * h + k] = f2_to_bf2(make_float2(lo, hi));
-    }
-}
-
-// E2M1 code of the quotient y (sign of y kept); *near: |y| lies within 2^-20
-// (relative) of a decision boundary, where a product and the IEEE quotient may
-// fall on different sides.
-__device__ __forceinline__ uint32_t e2m1_code_near(float y, bool* near) {
-  const float a = fabsf(y);
-  const uint32_t c = f32_to_e2m1(y);
-  // boundaries between magnitudes: 0.25, 0.75, 1.25, 1.75 (steps of 0.5), then 2.5, 3.5, 5
-  const int m = int(c & 7u);
-  const float up = m < 4 ? 0.25f + 0.5f * float(m) : (m == 4 ? 2.5f : (m == 5 ? 3.5f : (m == 6 ? 5.0f : 1e30f)));
-  const float lo = m == 0 ? -1.0f : (m <= 4 ? 0.5f * float(m) - 0.25f : (m == 5 ? 2.5f : (m == 6 ? 3.5f : 5.0f)));
-  const float tol = a * 9.5367431640625e-7f + 1e-38f;  // 2^-20 relative
-  *near = (up - a <= tol) || (a - lo <= tol);
-  return c;
-}
-
-}  // namespace fast
 
 template <int R, bool kAmax>
 __global__ void __launch_bounds__(kEncVFastThreads, 3) nvfp4_encode_fast_kernel(const __grid_constant__ CodecArgs a,
@@ -1587,20 +1610,24 @@ __global__ void __launch_bounds__(kEncVFastThreads, 3) nvfp4_encode_fast_kernel(
       }
       const uint32_t sb = all_zero ? 0u : f32_to_e4m3(__fdiv_rn(ab, six_st));
       const float eb = __fmul_rn(e4m3_to_f32(sb), st);
+      // the product y = delta * RN32(1 / e_b) lies within 2^-22 (relative) of the
+      // quotient while 1 / e_b is a normal number; a pair whose codes change when y
+      // moves by 2^-20 (relative) lies near a decision boundary and takes the IEEE
+      // quotients instead
       const float rc = eb != 0.0f ? __frcp_rn(eb) : 0.0f;
+      const bool by_div = !(fabsf(rc) >= 1.17549435e-38f && fabsf(rc) <= 3.0e38f);
+      constexpr float kUp = 1.00000095367431640625f, kDn = 0.99999904632568359375f;  // 1 +- 2^-20
       uint32_t w[2] = {0u, 0u};
+      if (eb != 0.0f) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const float v = hf ? bf_hi(d[k]) : bf_lo(d[k]);
-          uint32_t code = 0u;
-          if (eb != 0.0f) {
-            bool near;
-            code = e2m1_code_near(__fmul_rn(v, rc), &near);
-            if (near) code = f32_to_e2m1(__fdiv_rn(v, eb));
-          }
-          w[k >> 2] |= code << (8 * (k & 3) + 4 * hf);
+        for (int k = 0; k < 8; ++k) {
+          const float v0 = bf_lo(d[k]), v1 = bf_hi(d[k]);
+          const float y0 = __fmul_rn(v0, rc), y1 = __fmul_rn(v1, rc);
+          uint32_t c = f32x2_to_e2m1x2(y0, y1);
+          const uint32_t cu = f32x2_to_e2m1x2(__fmul_rn(y0, kUp), __fmul_rn(y1, kUp));
+          const uint32_t cd = f32x2_to_e2m1x2(__fmul_rn(y0, kDn), __fmul_rn(y1, kDn));
+          if (by_div || c != cu || c != cd) c = f32x2_to_e2m1x2(__fdiv_rn(v0, eb), __fdiv_rn(v1, eb));
+          w[k >> 2] |= c << (8 * (k & 3));
         }
       }
       if (live) {
@@ -1781,8 +1808,7 @@ cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, in
   const bool nv_chain = (a.nvfp4 & below) != 0;
   if (nv_out) mode = kModeNvAmax;
   // K reconstruction of INT4 chains up to 4 loops runs one item per (tile, head)
-  if (mode == kModeRecon && a.kind == KVQ_K && a.loop >= 1 && a.loop <= kFastMaxDepth && !nv_chain)
-    mode = kModeReconK;
+  if (mode == kModeRecon && a.kind == KVQ_K && a.loop >= 1 && a.loop <= kFastMaxDepth) mode = kModeReconK;
   const int32_t* prefix = nullptr;  // nullptr: kernels read a.one_prefix
   long long items = -1;             // -1: known only on the device
   if (a.reqs == nullptr) {
@@ -1862,21 +1888,27 @@ cudaError_t launch_codec(const CodecArgs& a_in, int mode, int32_t* prefix_ws, in
       tile_dir_kernel<<<int(blocks), 256, 0, stream>>>(a, prefix);
       break;
     }
-    case kModeReconK:
-      switch (a.loop) {
-        case 1: run(reconstruct_k_fast_kernel<1>, kReconKThreads); break;
-        case 2: run(reconstruct_k_fast_kernel<2>, kReconKThreads); break;
-        case 3: run(reconstruct_k_fast_kernel<3>, kReconKThreads); break;
-        default: run(reconstruct_k_fast_kernel<4>, kReconKThreads); break;
+    case kModeReconK:  // (a loop-1 chain is the INT4 base alone)
+      switch (a.loop + (nv_chain && a.loop >= 2 ? 8 : 0)) {
+        case 1: run(reconstruct_k_fast_kernel<1, false>, kReconKThreads); break;
+        case 2: run(reconstruct_k_fast_kernel<2, false>, kReconKThreads); break;
+        case 3: run(reconstruct_k_fast_kernel<3, false>, kReconKThreads); break;
+        case 4: run(reconstruct_k_fast_kernel<4, false>, kReconKThreads); break;
+        case 8 + 2: run(reconstruct_k_fast_kernel<2, true>, kReconKThreads); break;
+        case 8 + 3: run(reconstruct_k_fast_kernel<3, true>, kReconKThreads); break;
+        default: run(reconstruct_k_fast_kernel<4, true>, kReconKThreads); break;
       }
       break;
     default:
-      if (a.kind == KVQ_V && a.loop >= 1 && a.loop <= kFastMaxDepth && !nv_chain) {
-        switch (a.loop) {
-          case 1: run(reconstruct_v_fast_kernel<1>, kReconVFastThreads); break;
-          case 2: run(reconstruct_v_fast_kernel<2>, kReconVFastThreads); break;
-          case 3: run(reconstruct_v_fast_kernel<3>, kReconVFastThreads); break;
-          default: run(reconstruct_v_fast_kernel<4>, kReconVFastThreads); break;
+      if (a.kind == KVQ_V && a.loop >= 1 && a.loop <= kFastMaxDepth) {
+        switch (a.loop + (nv_chain && a.loop >= 2 ? 8 : 0)) {
+          case 1: run(reconstruct_v_fast_kernel<1, false>, kReconVFastThreads); break;
+          case 2: run(reconstruct_v_fast_kernel<2, false>, kReconVFastThreads); break;
+          case 3: run(reconstruct_v_fast_kernel<3, false>, kReconVFastThreads); break;
+          case 4: run(reconstruct_v_fast_kernel<4, false>, kReconVFastThreads); break;
+          case 8 + 2: run(reconstruct_v_fast_kernel<2, true>, kReconVFastThreads); break;
+          case 8 + 3: run(reconstruct_v_fast_kernel<3, true>, kReconVFastThreads); break;
+          default: run(reconstruct_v_fast_kernel<4, true>, kReconVFastThreads); break;
         }
       } else {
         reconstruct_generic_kernel<<<grid_for(4), kReconThreads, 0, stream>>>(a, prefix);

@@ -90,6 +90,21 @@ __device__ __forceinline__ float nvfp4_dequant(uint32_t nib, float sb, float st)
   return __fmul_rn(__fmul_rn(e2m1_to_f32(nib), sb), st);
 }
 
+// Two E2M1 codes (the low byte of x: low nibble, high nibble) as an exact FP16
+// pair {low, high}, by the hardware conversion.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(x));
+  return r;
+}
+
+// Two E4M3 values (the low 16 bits of x) as an exact FP16 pair {low byte, high byte}.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(r) : "r"(x));
+  return r;
+}
+
 // NVFP4 planes of a loop: E4M3 block scale of (head h, stored row, block of 16
 // channels) and the tensor scale.
 __device__ __forceinline__ float nvfp4_block_scale(const LoopPlanes& L, int h, int row, int blk) {
