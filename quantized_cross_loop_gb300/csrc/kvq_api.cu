@@ -776,6 +776,7 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   a.out = out;
   char* ws = static_cast<char*>(workspace);
   a.err = reinterpret_cast<int32_t*>(ws);
+  a.flags = reinterpret_cast<int32_t*>(ws + 4);  // cleared with the error word
   a.prefix = reinterpret_cast<int32_t*>(ws + ws_prefix_offset());
   a.partials = reinterpret_cast<float*>(ws + ws_partials_offset(n_requests));
   a.stats = reinterpret_cast<float2*>(ws + ws_stats_offset(n_requests, n_heads, sms * kMaxCtasPerSm));

@@ -31,6 +31,7 @@ struct AttnArgs {
   float scale;        // softmax scale (natural-log units)
   float* out;         // FP32 [B][Hq][128]
   int32_t* err;       // error word
+  int32_t* flags;     // word after the error word: bit 0 = some request has BF16 segments (set by the plan)
   int32_t* prefix;    // [B+1] tile prefix
   float* partials;    // slots
   float2* stats;      // [B][Hq] (max in log2 units, sum of exponentials) of the packed part
@@ -38,7 +39,7 @@ struct AttnArgs {
   int32_t refuse_nvfp4;  // the kernel of this call reads no NVFP4 loop: such requests are refused
 };
 
-// Workspace layout: [0,16) error word; then int32 prefix[B+1] (rounded to 16 B);
+// Workspace layout: [0,16) error word (int32 0) and plan flags (int32 1); then int32 prefix[B+1] (rounded to 16 B);
 // then (n_ctas + B*H) partial slots of kSlotFloats floats; then float2
 // stats[B*Hq] (the packed part's softmax max and sum, merged with the BF16
 // segments afterwards).

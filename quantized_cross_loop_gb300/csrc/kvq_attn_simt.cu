@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a) {
         atomicOr(a.err, 64);
       } else {
         v = a.H * n_tiles_of(r.n_tokens);
+        if (r.n_sink + r.n_tail > 0) atomicOr(a.flags, 1);
       }
     }
     int x = v;
@@ -76,54 +77,65 @@ cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream) {
 
 // ---------------------------------------------------------------- combine
 
+// Grid-stride over the (request, KV head) units. Most units need nothing: their
+// tile range lies inside one CTA's, which wrote the output directly; that is
+// decided from the tile prefix alone. A request with no tiles is read only to
+// tell a refused entry (NaN output) from one without packed tokens (zero output
+// and an empty softmax state).
 __global__ void __launch_bounds__(kD) combine_kernel(AttnArgs a) {
-  const int u = blockIdx.x;
-  const int b = u / a.H, h = u % a.H;
   const int d = threadIdx.x;
   const int g = a.g;
-  const kvq_request& r = a.reqs[b];
-  float* outp = a.out + ((long long)b * a.Hq + (long long)h * g) * kD;
-  float2* stats = a.stats + (long long)b * a.Hq + (long long)h * g;
-  if (!attn_request_ok(a, r)) {
-    for (int i = 0; i < g; ++i) outp[i * kD + d] = __int_as_float(0x7fc00000);
-    return;
-  }
-  const int nt = n_tiles_of(r.n_tokens);
-  if (nt == 0) {  // no packed tokens: zero output and an empty softmax state
-    for (int i = 0; i < g; ++i) outp[i * kD + d] = 0.0f;
-    if (d < g) stats[d] = make_float2(-INFINITY, 0.0f);
-    return;
-  }
   const long long W = a.prefix[a.n_requests];
   const int C = a.n_ctas;
-  const long long s = (long long)a.prefix[b] + (long long)h * nt;
-  const long long e = s + nt;
-  const int c_lo = cta_of(s, W, C), c_hi = cta_of(e - 1, W, C);
-  if (c_lo == c_hi) return;  // written directly by its only CTA
-  for (int i = 0; i < g; ++i) {
-    float M = -INFINITY;
-    for (int c = c_lo; c <= c_hi; ++c) {
-      if (cta_start(c, W, C) == cta_start(c + 1, W, C)) continue;  // empty range
-      const float* slot = a.partials + (size_t)(c + u) * kSlotFloats;
-      M = fmaxf(M, slot[i]);
+  for (int u = blockIdx.x; u < a.n_requests * a.H; u += gridDim.x) {
+    const int b = u / a.H, h = u % a.H;
+    float* outp = a.out + ((long long)b * a.Hq + (long long)h * g) * kD;
+    float2* stats = a.stats + (long long)b * a.Hq + (long long)h * g;
+    const int p0 = a.prefix[b], p1 = a.prefix[b + 1];
+    if (p1 <= p0) {
+      const bool ok = attn_request_ok(a, a.reqs[b]);
+      for (int i = 0; i < g; ++i) outp[i * kD + d] = ok ? 0.0f : __int_as_float(0x7fc00000);
+      if (ok && d < g) stats[d] = make_float2(-INFINITY, 0.0f);  // no packed tokens: an empty softmax state
+      continue;
     }
-    float L = 0.0f, acc = 0.0f;
-    for (int c = c_lo; c <= c_hi; ++c) {
-      if (cta_start(c, W, C) == cta_start(c + 1, W, C)) continue;
-      const float* slot = a.partials + (size_t)(c + u) * kSlotFloats;
-      float m = slot[i];
-      float w = (m == -INFINITY) ? 0.0f : exp2f(m - M);
-      L += slot[kMaxG + i] * w;
-      acc += slot[2 * kMaxG + i * kD + d] * w;
+    const int nt = (p1 - p0) / a.H;
+    const long long s = (long long)p0 + (long long)h * nt;
+    const long long e = s + nt;
+    const int c_lo = cta_of(s, W, C), c_hi = cta_of(e - 1, W, C);
+    if (c_lo == c_hi) continue;  // written directly by its only CTA
+    for (int i = 0; i < g; ++i) {
+      float M = -INFINITY;
+      for (int c = c_lo; c <= c_hi; ++c) {
+        if (cta_start(c, W, C) == cta_start(c + 1, W, C)) continue;  // empty range
+        const float* slot = a.partials + (size_t)(c + u) * kSlotFloats;
+        M = fmaxf(M, slot[i]);
+      }
+      float L = 0.0f, acc = 0.0f;
+      for (int c = c_lo; c <= c_hi; ++c) {
+        if (cta_start(c, W, C) == cta_start(c + 1, W, C)) continue;
+        const float* slot = a.partials + (size_t)(c + u) * kSlotFloats;
+        float m = slot[i];
+        float w = (m == -INFINITY) ? 0.0f : exp2f(m - M);
+        L += slot[kMaxG + i] * w;
+        acc += slot[2 * kMaxG + i * kD + d] * w;
+      }
+      outp[i * kD + d] = acc / L;
+      if (d == 0) stats[i] = make_float2(M, L);
     }
-    outp[i * kD + d] = acc / L;
-    if (d == 0) stats[i] = make_float2(M, L);
   }
+}
+
+// Blocks of the grid-stride kernels below: the unit count, capped at two
+// blocks per attention CTA.
+static int unit_grid(const AttnArgs& a) {
+  const long long units = (long long)a.n_requests * a.H;
+  const long long cap = 2LL * (a.n_ctas > 0 ? a.n_ctas : 1);
+  return int(units < cap ? units : cap);
 }
 
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
-  combine_kernel<<<a.n_requests * a.H, kD, 0, stream>>>(a);
+  combine_kernel<<<unit_grid(a), kD, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }
@@ -139,17 +151,20 @@ cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
 constexpr int kSegWarps = 4;
 constexpr float kSegLog2e = 1.4426950408889634f;
 
+// Grid-stride over the (request, KV head) units; the whole grid leaves at once
+// when the plan saw no request with segments.
 __global__ void __launch_bounds__(32 * kSegWarps) segment_kernel(AttnArgs a) {
-  const int u = blockIdx.x;
-  const int b = u / a.H, h = u % a.H;
+  if (!(*a.flags & 1)) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = a.g;
-  const kvq_request& r = a.reqs[b];
-  if (!attn_request_ok(a, r)) return;  // the output is already NaN
-  const int ns = r.n_sink, n = r.n_sink + r.n_tail;
-  if (n == 0) return;
   __shared__ float s_m[kSegWarps][kMaxG], s_l[kSegWarps][kMaxG];
   __shared__ float s_acc[kSegWarps][kMaxG][kD];
+  for (int u = blockIdx.x; u < a.n_requests * a.H; u += gridDim.x) {
+  const int b = u / a.H, h = u % a.H;
+  const kvq_request& r = a.reqs[b];
+  if (!attn_request_ok(a, r)) continue;  // the output is already NaN
+  const int ns = r.n_sink, n = r.n_sink + r.n_tail;
+  if (n == 0) continue;
   const float qscale = a.scale * kSegLog2e;
   float qv[kMaxG][4];
 #pragma unroll
@@ -220,11 +235,13 @@ __global__ void __launch_bounds__(32 * kSegWarps) segment_kernel(AttnArgs a) {
     const float den = (packed ? st.y * w0 : 0.0f) + ls * w1;
     a.out[oi * kD + tid] = num / den;
   }
+  __syncthreads();  // the next unit reuses the shared arrays
+  }
 }
 
 cudaError_t launch_segments(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
-  segment_kernel<<<a.n_requests * a.H, 32 * kSegWarps, 0, stream>>>(a);
+  segment_kernel<<<unit_grid(a), 32 * kSegWarps, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }
