@@ -479,9 +479,13 @@ def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, re
         return a.elapsed_time(b) / reps, r
 
     ref_ms, st = timed(lambda: kvq.kvq_sparse_ref_state(pool.table, q2, 2, H, n_select, max_t))
-    dec_ws = torch.zeros(16, dtype=torch.uint8, device=dev)
-    dec_ms, _ = timed(lambda: kvq.kvq_sparse_decode_attn(pool.table, q, depth, H, st, workspace=dec_ws))
-    err = kvq.attn_error_word(st.workspace) | kvq.attn_error_word(dec_ws)
+    dec_ws = torch.zeros(kvq.kvq_sparse_decode_workspace_bytes(B, H, Hq, D, max_t), dtype=torch.uint8, device=dev)
+    dec_ms, _ = timed(lambda: kvq.kvq_sparse_decode_attn(pool.table, q, depth, H, st, workspace=dec_ws,
+                                                         algo=kvq.ATTN_MMA))
+    pk_ws = torch.zeros(16, dtype=torch.uint8, device=dev)  # the per-key gather kernel
+    pk_ms, _ = timed(lambda: kvq.kvq_sparse_decode_attn(pool.table, q, depth, H, st, workspace=pk_ws,
+                                                        algo=kvq.ATTN_SIMT))
+    err = kvq.attn_error_word(st.workspace) | kvq.attn_error_word(dec_ws) | kvq.attn_error_word(pk_ws)
     selected = sum(min(n_select, r.T) for r in reqs) * Hq
     empty = torch.zeros((0, H, D), dtype=torch.bfloat16, device=dev)
     tail = [(empty, empty, torch.randn((100, H, D), generator=g, device=dev).to(torch.bfloat16),
@@ -519,6 +523,8 @@ def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, re
     return {"kgroup_tile": kgroup_tile, "nvfp4_residuals": nvfp4, "append_tile": append,
             "sparse_decode": {"budget_keys_per_query_head": n_select, "ref_depth": 2, "depth": depth,
                               "ref_state_ms": ref_ms, "later_loop_ms": dec_ms,
+                              "later_loop_kernel": "key-masked tensor-core attention",
+                              "later_loop_ms_per_key_kernel": pk_ms,
                               "selected_keys_per_s": selected / (dec_ms * 1e-3)},
             "bf16_tail": {"tail_tokens_per_request": 100, "attention_ms": tail_ms},
             "error_word": err}

@@ -420,12 +420,40 @@ kvq_status kvq_sparse_ref_state(const kvq_request* reqs, int n_requests, int n_h
 
 /* A later loop at `depth` with the state of kvq_sparse_ref_state (same n_select
  * and max_tokens); out FP32 [n_requests][n_q_heads][head_dim]. workspace: at
- * least 16 bytes, 16-byte aligned, for the error word (bit 32: a selected
- * position outside its request). */
+ * least 16 bytes, 16-byte aligned; int32 at offset 0 is the error word (bit 32:
+ * a selected position outside its request, which is then left out).
+ * Two kernels compute the later loop:
+ *   - with a workspace of at least kvq_sparse_decode_workspace_bytes(...), a
+ *     depth <= 4, 1, 2, 4 or 8 query heads per KV head and a 16-byte aligned
+ *     out, the selections become a key mask per (request, query head) and the
+ *     packed tensor-core attention (kvq_decode_attn_packed) attends with the
+ *     unselected keys' logits dropped; a small kernel then applies the
+ *     correction;
+ *   - otherwise a kernel that gathers the selected keys one by one.
+ * kvq_sparse_decode_attn reads NVFP4 loops (it passes KVQ_ATTN_NVFP4). */
 kvq_status kvq_sparse_decode_attn(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
                                   int depth, const uint16_t* q, float softmax_scale, int n_select, int max_tokens,
                                   const int32_t* sel_idx, const float* mass, const float* o_ref, const float* c_ref,
                                   float* out, void* workspace, size_t workspace_bytes, kvq_cuda_stream stream);
+
+/* Workspace bytes with which kvq_sparse_decode_attn takes the tensor-core path:
+ * the packed attention's workspace (kvq_decode_attn_workspace_bytes, rounded up
+ * to 256 bytes) followed by the key masks, 2 * ceil(max_tokens / 64) uint32
+ * words per (request, query head). 0 for invalid sizes. */
+size_t kvq_sparse_decode_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim, int max_tokens);
+
+/* Same as kvq_sparse_decode_attn, choosing the kernel: algo KVQ_ATTN_AUTO (the
+ * tensor-core path when the conditions above hold), KVQ_ATTN_SIMT (the per-key
+ * kernel) or KVQ_ATTN_MMA (the tensor-core path, or KVQ_ERR_UNSUPPORTED /
+ * KVQ_ERR_WORKSPACE when it cannot run), ORed with KVQ_ATTN_NVFP4 when the table
+ * may hold NVFP4 loops. Without that flag the tensor-core path refuses requests
+ * with NVFP4 loops (NaN output, bit 64 of the error word), as
+ * kvq_decode_attn_packed_ex does. */
+kvq_status kvq_sparse_decode_attn_ex(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
+                                     int depth, const uint16_t* q, float softmax_scale, int n_select, int max_tokens,
+                                     const int32_t* sel_idx, const float* mass, const float* o_ref, const float* c_ref,
+                                     float* out, void* workspace, size_t workspace_bytes, int algo,
+                                     kvq_cuda_stream stream);
 
 /* Bytes of the static device scratch used by kvq_decode_attn_packed_noalloc. */
 #define KVQ_NOALLOC_SCRATCH_BYTES (32u << 20)

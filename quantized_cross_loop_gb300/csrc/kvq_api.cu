@@ -728,6 +728,47 @@ size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_head
   return ws_bytes(n_requests, n_heads, n_q_heads, sms * kMaxCtasPerSm);
 }
 
+// Arguments of one packed attention call with its workspace at `ws` (sized by
+// ws_bytes for sms * kMaxCtasPerSm CTAs); algo is SIMT or MMA.
+static void attention_args(AttnArgs& a, const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int depth,
+                           const uint16_t* q, float softmax_scale, float* out, char* ws, int algo, bool nvfp4_hint,
+                           int dev, int sms) {
+  memset(&a, 0, sizeof a);
+  a.reqs = reqs;
+  a.n_requests = n_requests;
+  a.H = n_heads;
+  a.Hq = n_q_heads;
+  a.g = n_q_heads / n_heads;
+  a.depth = depth;
+  a.nvfp4 = nvfp4_hint ? 1 : 0;
+  a.refuse_nvfp4 = (algo == KVQ_ATTN_MMA && !nvfp4_hint) ? 1 : 0;
+  a.n_ctas = attn_ctas(algo, dev);
+  a.q = q;
+  a.scale = softmax_scale;
+  a.out = out;
+  a.err = reinterpret_cast<int32_t*>(ws);
+  a.flags = reinterpret_cast<int32_t*>(ws + 4);  // cleared with the error word
+  a.prefix = reinterpret_cast<int32_t*>(ws + ws_prefix_offset());
+  a.partials = reinterpret_cast<float*>(ws + ws_partials_offset(n_requests));
+  a.stats = reinterpret_cast<float2*>(ws + ws_stats_offset(n_requests, n_heads, sms * kMaxCtasPerSm));
+}
+
+// Plan, attention, split-unit merge and (when asked) the BF16 segments, on a
+// cleared error word.
+static kvq_status attention_launches(const AttnArgs& a, int algo, bool segments, cudaStream_t s) {
+  cudaError_t e = launch_plan(a, s);
+  if (e != cudaSuccess) return cuda_status(e, "plan launch");
+  e = (algo == KVQ_ATTN_SIMT) ? launch_attn_simt(a, s) : launch_attn_mma(a, s);
+  if (e != cudaSuccess) return cuda_status(e, "attention launch");
+  e = launch_combine(a, s);
+  if (e != cudaSuccess) return cuda_status(e, "combine launch");
+  if (segments) {
+    e = launch_segments(a, s);
+    if (e != cudaSuccess) return cuda_status(e, "segment launch");
+  }
+  return ok();
+}
+
 kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads,
                                      int head_dim, int depth, const uint16_t* q, float softmax_scale, float* out,
                                      void* workspace, size_t workspace_bytes, int algo, kvq_cuda_stream stream) {
@@ -761,37 +802,12 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
     return fail(KVQ_ERR_UNSUPPORTED, "the tensor-core kernel reads depth <= %d (got %d)", kMmaMaxDepth, depth);
 
   AttnArgs a;
-  memset(&a, 0, sizeof a);
-  a.reqs = reqs;
-  a.n_requests = n_requests;
-  a.H = n_heads;
-  a.Hq = n_q_heads;
-  a.g = g;
-  a.depth = depth;
-  a.nvfp4 = nvfp4_hint ? 1 : 0;
-  a.refuse_nvfp4 = (algo == KVQ_ATTN_MMA && !nvfp4_hint) ? 1 : 0;
-  a.n_ctas = attn_ctas(algo, dev);
-  a.q = q;
-  a.scale = softmax_scale;
-  a.out = out;
-  char* ws = static_cast<char*>(workspace);
-  a.err = reinterpret_cast<int32_t*>(ws);
-  a.flags = reinterpret_cast<int32_t*>(ws + 4);  // cleared with the error word
-  a.prefix = reinterpret_cast<int32_t*>(ws + ws_prefix_offset());
-  a.partials = reinterpret_cast<float*>(ws + ws_partials_offset(n_requests));
-  a.stats = reinterpret_cast<float2*>(ws + ws_stats_offset(n_requests, n_heads, sms * kMaxCtasPerSm));
+  attention_args(a, reqs, n_requests, n_heads, n_q_heads, depth, q, softmax_scale, out, static_cast<char*>(workspace),
+                 algo, nvfp4_hint, dev, sms);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   e = cudaMemsetAsync(a.err, 0, 16, s);
   if (e != cudaSuccess) return cuda_status(e, "clear error word");
-  e = launch_plan(a, s);
-  if (e != cudaSuccess) return cuda_status(e, "plan launch");
-  e = (algo == KVQ_ATTN_SIMT) ? launch_attn_simt(a, s) : launch_attn_mma(a, s);
-  if (e != cudaSuccess) return cuda_status(e, "attention launch");
-  e = launch_combine(a, s);
-  if (e != cudaSuccess) return cuda_status(e, "combine launch");
-  e = launch_segments(a, s);
-  if (e != cudaSuccess) return cuda_status(e, "segment launch");
-  return ok();
+  return attention_launches(a, algo, true, s);
 }
 
 kvq_status kvq_decode_attn_packed(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads,
@@ -868,17 +884,40 @@ kvq_status kvq_sparse_ref_state(const kvq_request* reqs, int n_requests, int n_h
   return cuda_status(launch_sparse_select_path(a, reinterpret_cast<cudaStream_t>(stream)), "sparse reference launch");
 }
 
-kvq_status kvq_sparse_decode_attn(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
-                                  int depth, const uint16_t* q, float softmax_scale, int n_select, int max_tokens,
-                                  const int32_t* sel_idx, const float* mass, const float* o_ref, const float* c_ref,
-                                  float* out, void* workspace, size_t workspace_bytes, kvq_cuda_stream stream) {
+static size_t sparse_mask_words(int max_tokens) { return 2 * ((size_t(max_tokens) + 63) / 64); }
+
+size_t kvq_sparse_decode_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim, int max_tokens) {
+  (void)head_dim;
+  if (n_requests < 0 || n_heads < 1 || n_q_heads < 1 || max_tokens < 0) return 0;
+  return sparse_attn_part(n_requests, n_heads, n_q_heads) +
+         size_t(n_requests) * n_q_heads * sparse_mask_words(max_tokens) * 4;
+}
+
+kvq_status kvq_sparse_decode_attn_ex(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
+                                     int depth, const uint16_t* q, float softmax_scale, int n_select, int max_tokens,
+                                     const int32_t* sel_idx, const float* mass, const float* o_ref, const float* c_ref,
+                                     float* out, void* workspace, size_t workspace_bytes, int algo,
+                                     kvq_cuda_stream stream) {
   kvq_status st = check_sparse(reqs, n_requests, n_heads, n_q_heads, head_dim, depth, q, softmax_scale, n_select,
                                max_tokens);
   if (st != KVQ_OK) return st;
+  const bool nvfp4_hint = (algo & KVQ_ATTN_NVFP4) != 0;
+  algo &= ~KVQ_ATTN_NVFP4;
+  if (algo < KVQ_ATTN_AUTO || algo > KVQ_ATTN_MMA) return fail(KVQ_ERR_BAD_ARG, "algo %d", algo);
   if (n_requests == 0) return ok();
   if ((n_select > 0 && !sel_idx) || !mass || !o_ref || !c_ref || !out) return fail(KVQ_ERR_BAD_ARG, "NULL argument");
   if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < 16)
     return fail(KVQ_ERR_WORKSPACE, "workspace needs 16 bytes, 16-byte aligned");
+  const int g = n_q_heads / n_heads;
+  const bool tc_ok = depth <= kMmaMaxDepth && (g == 1 || g == 2 || g == 4 || g == 8) && aligned16(out);
+  const size_t need = kvq_sparse_decode_workspace_bytes(n_requests, n_heads, n_q_heads, head_dim, max_tokens);
+  if (algo == KVQ_ATTN_MMA && !tc_ok)
+    return fail(KVQ_ERR_UNSUPPORTED,
+                "the tensor-core path reads depth <= %d with 1, 2, 4 or 8 query heads per KV head and a 16-byte "
+                "aligned out", kMmaMaxDepth);
+  if (algo == KVQ_ATTN_MMA && workspace_bytes < need)
+    return fail(KVQ_ERR_WORKSPACE, "the tensor-core path needs %zu bytes of workspace", need);
+  const bool tc = algo != KVQ_ATTN_SIMT && tc_ok && workspace_bytes >= need;
   SparseArgs a;
   memset(&a, 0, sizeof a);
   a.reqs = reqs;
@@ -900,7 +939,40 @@ kvq_status kvq_sparse_decode_attn(const kvq_request* reqs, int n_requests, int n
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(a.err, 0, 16, s);
   if (e != cudaSuccess) return cuda_status(e, "clear error word");
-  return cuda_status(launch_sparse_attn(a, s), "sparse attention launch");
+  if (!tc) return cuda_status(launch_sparse_attn(a, s), "sparse attention launch");
+
+  // tensor-core path: key masks, the masked packed attention, the correction
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+  const int sms = sm_count(dev);
+  if (sms <= 0) return fail(KVQ_ERR_CUDA, "cannot read the SM count of device %d", dev);
+  char* ws = static_cast<char*>(workspace);
+  const size_t apart = sparse_attn_part(n_requests, n_heads, n_q_heads);
+  a.mask_words = int32_t(sparse_mask_words(max_tokens));
+  a.sel_mask = reinterpret_cast<uint32_t*>(ws + apart);
+  e = cudaMemsetAsync(a.sel_mask, 0, size_t(n_requests) * n_q_heads * a.mask_words * 4, s);
+  if (e != cudaSuccess) return cuda_status(e, "clear key masks");
+  e = launch_sparse_mask(a, s);
+  if (e != cudaSuccess) return cuda_status(e, "key mask launch");
+  AttnArgs at;
+  attention_args(at, reqs, n_requests, n_heads, n_q_heads, depth, q, softmax_scale, out, ws, KVQ_ATTN_MMA, nvfp4_hint,
+                 dev, sms);
+  at.sel_mask = a.sel_mask;
+  at.mask_words = a.mask_words;
+  a.stats = at.stats;
+  st = attention_launches(at, KVQ_ATTN_MMA, false, s);
+  if (st != KVQ_OK) return st;
+  return cuda_status(launch_sparse_epilogue(a, s), "sparse epilogue launch");
+}
+
+kvq_status kvq_sparse_decode_attn(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
+                                  int depth, const uint16_t* q, float softmax_scale, int n_select, int max_tokens,
+                                  const int32_t* sel_idx, const float* mass, const float* o_ref, const float* c_ref,
+                                  float* out, void* workspace, size_t workspace_bytes, kvq_cuda_stream stream) {
+  return kvq_sparse_decode_attn_ex(reqs, n_requests, n_heads, n_q_heads, head_dim, depth, q, softmax_scale, n_select,
+                                   max_tokens, sel_idx, mass, o_ref, c_ref, out, workspace, workspace_bytes,
+                                   KVQ_ATTN_AUTO | KVQ_ATTN_NVFP4, stream);
 }
 
 }  // extern "C"

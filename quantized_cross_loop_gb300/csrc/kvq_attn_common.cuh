@@ -37,6 +37,10 @@ struct AttnArgs {
   float2* stats;      // [B][Hq] (max in log2 units, sum of exponentials) of the packed part
   int32_t nvfp4;      // the table may hold NVFP4 loops (the tensor-core kernel's NVFP4-reading form)
   int32_t refuse_nvfp4;  // the kernel of this call reads no NVFP4 loop: such requests are refused
+  // sparse decode (tensor-core kernel only): bit t of word t / 32 of row (b, query head)
+  // says key t is selected; the logits of the other keys are dropped. NULL: every key.
+  const uint32_t* sel_mask;
+  int32_t mask_words;
 };
 
 // Workspace layout: [0,16) error word (int32 0) and plan flags (int32 1); then int32 prefix[B+1] (rounded to 16 B);

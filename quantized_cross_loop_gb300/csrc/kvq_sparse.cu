@@ -331,6 +331,61 @@ __global__ void __launch_bounds__(32 * kAttnWarps) sparse_attn_kernel(SparseArgs
   out[tid] = a.o_ref[(long long)bq * kD + tid] - a.c_ref[(long long)bq * kD + tid] + a.mass[bq] * cnew;
 }
 
+// ---------------------------------------------------------------- later loop on the tensor-core kernel
+//
+// The selections become key masks, one bit per position and (request, query
+// head), for the packed tensor-core attention, which drops the logits of the
+// unselected keys; its normalised output is softmax(q K[S]^T) V[S] and its
+// (max, sum) state tells an empty selection. The epilogue applies the
+// correction O_ref - C_ref + m * that output.
+
+// One thread per selection entry; the mask words were zeroed before.
+__global__ void __launch_bounds__(256) sparse_mask_kernel(SparseArgs a) {
+  const long long n = (long long)a.n_requests * a.Hq * a.n_select;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long bq = i / a.n_select;
+    const int k = int(i - bq * a.n_select);
+    const kvq_request& r = a.reqs[bq / a.Hq];
+    const int T = r.n_tokens;
+    if (T > a.max_tokens || k >= min(a.n_select, T)) continue;  // refused request, or past the count
+    const int t = a.sel_idx[i];
+    if (t < 0 || t >= T) {  // not a selection of this request
+      atomicOr(a.err, 32);
+      continue;
+    }
+    atomicOr(a.sel_mask + bq * a.mask_words + (t >> 5), 1u << (t & 31));
+  }
+}
+
+__global__ void __launch_bounds__(kD) sparse_epilogue_kernel(SparseArgs a) {
+  const int bq = blockIdx.x, d = threadIdx.x;
+  const kvq_request& r = a.reqs[bq / a.Hq];
+  float* out = a.out + (long long)bq * kD;
+  if (!sparse_request_ok(r, a.depth, a.max_tokens)) {
+    if (d == 0) atomicOr(a.err, 1);
+    out[d] = __int_as_float(0x7fc00000);
+    return;
+  }
+  const float cnew = a.stats[bq].y > 0.0f ? out[d] : 0.0f;  // an empty selection contributes nothing
+  out[d] = a.o_ref[(long long)bq * kD + d] - a.c_ref[(long long)bq * kD + d] + a.mass[bq] * cnew;
+}
+
+cudaError_t launch_sparse_mask(const SparseArgs& a, cudaStream_t stream) {
+  const long long n = (long long)a.n_requests * a.Hq * a.n_select;
+  if (n == 0) return cudaSuccess;
+  const long long blocks = (n + 255) / 256;
+  sparse_mask_kernel<<<int(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_epilogue(const SparseArgs& a, cudaStream_t stream) {
+  if (a.n_requests == 0) return cudaSuccess;
+  sparse_epilogue_kernel<<<a.n_requests * a.Hq, kD, 0, stream>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_sparse_select_path(const SparseArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
   const int tiles = (a.max_tokens + KVQ_TILE - 1) / KVQ_TILE;

@@ -24,11 +24,19 @@ struct SparseArgs {
   const float* o_ref;  // [B][Hq][128], later loop
   float* out;          // [B][Hq][128], later loop
   int32_t* err;        // error word
+  // later loop on the tensor-core attention kernel
+  uint32_t* sel_mask;   // [B][Hq][mask_words]: bit t set for each selected position t
+  int32_t mask_words;   // 2 * ceil(max_tokens / 64): whole 64-token tiles
+  const float2* stats;  // [B][Hq] softmax (max, sum) of the masked attention
 };
 
 // Reference pass after the full attention: logits, selection, m and C_ref.
 cudaError_t launch_sparse_select_path(const SparseArgs& a, cudaStream_t stream);
 // A later loop: the corrected output from the selected keys.
 cudaError_t launch_sparse_attn(const SparseArgs& a, cudaStream_t stream);
+// A later loop on the tensor-core kernel: the key masks of the selections
+// (before the masked attention), then the correction of its output.
+cudaError_t launch_sparse_mask(const SparseArgs& a, cudaStream_t stream);
+cudaError_t launch_sparse_epilogue(const SparseArgs& a, cudaStream_t stream);
 
 }  // namespace kvq

@@ -39,7 +39,8 @@ EXPORTED = (
     "kvq_decode_attn_packed_noalloc", "kvq_sparse_workspace_bytes", "kvq_sparse_ref_state",
     "kvq_sparse_decode_attn", "kvq_stream_payload_bytes_ex", "kvq_stream_set_format", "kvq_encode_batch_ex",
     "kvq_reconstruct_batch_ex", "kvq_stream_set_capacity", "kvq_append_workspace_bytes", "kvq_append_tile",
-    "kvq_append_batch_workspace_bytes", "kvq_append_tile_batch",
+    "kvq_append_batch_workspace_bytes", "kvq_append_tile_batch", "kvq_sparse_decode_workspace_bytes",
+    "kvq_sparse_decode_attn_ex",
 )
 
 
@@ -147,6 +148,10 @@ def lib():
                                                vp, vp, sz, vp]
             L.kvq_sparse_decode_attn.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_float, i32, i32, vp, vp, vp,
                                                  vp, vp, vp, sz, vp]
+            L.kvq_sparse_decode_attn_ex.argtypes = [vp, i32, i32, i32, i32, i32, vp, ctypes.c_float, i32, i32, vp, vp,
+                                                    vp, vp, vp, vp, sz, i32, vp]
+            L.kvq_sparse_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            L.kvq_sparse_decode_workspace_bytes.restype = sz
             L.kvq_status_string.argtypes = [i32]
             L.kvq_status_string.restype = ctypes.c_char_p
             L.kvq_last_error.restype = ctypes.c_char_p
@@ -690,9 +695,18 @@ def kvq_sparse_ref_state(table: RequestTable, q_ref: torch.Tensor, ref_depth: in
     return SparseState(sel[:, :, :n_select], mass, o_ref, c_ref, n_select, max_tokens, workspace)
 
 
+def kvq_sparse_decode_workspace_bytes(n_requests: int, n_heads: int, n_q_heads: int, head_dim: int,
+                                      max_tokens: int) -> int:
+    return int(lib().kvq_sparse_decode_workspace_bytes(n_requests, n_heads, n_q_heads, head_dim, max_tokens))
+
+
 def kvq_sparse_decode_attn(table: RequestTable, q: torch.Tensor, depth: int, n_heads: int, state: SparseState,
                            softmax_scale: float | None = None, out: torch.Tensor | None = None,
-                           workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                           workspace: torch.Tensor | None = None, algo: int = ATTN_AUTO, stream=None) -> torch.Tensor:
+    """A later loop of sparse decode attention. With no workspace given, one of
+    kvq_sparse_decode_workspace_bytes is allocated, so that AUTO takes the
+    tensor-core path where it can; a 16-byte workspace selects the per-key
+    kernel."""
     _require_cuda(q, "q", torch.bfloat16)
     B, Hq, D = q.shape
     if softmax_scale is None:
@@ -700,11 +714,15 @@ def kvq_sparse_decode_attn(table: RequestTable, q: torch.Tensor, depth: int, n_h
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     if workspace is None:
-        workspace = torch.empty(16, dtype=torch.uint8, device=q.device)
+        need = kvq_sparse_decode_workspace_bytes(B, n_heads, Hq, D, state.max_tokens)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if table.has_nvfp4:
+        algo |= ATTN_NVFP4
     sel = state.sel_idx.contiguous()
-    _check(lib().kvq_sparse_decode_attn(_dptr(table.table), B, n_heads, Hq, D, depth, _dptr(q),
-                                        ctypes.c_float(softmax_scale), state.n_select, state.max_tokens, _dptr(sel),
-                                        _dptr(state.mass), _dptr(state.o_ref), _dptr(state.c_ref), _dptr(out),
-                                        _dptr(workspace), workspace.numel(), _stream_handle(stream)),
+    _check(lib().kvq_sparse_decode_attn_ex(_dptr(table.table), B, n_heads, Hq, D, depth, _dptr(q),
+                                           ctypes.c_float(softmax_scale), state.n_select, state.max_tokens,
+                                           _dptr(sel), _dptr(state.mass), _dptr(state.o_ref), _dptr(state.c_ref),
+                                           _dptr(out), _dptr(workspace), workspace.numel(), algo,
+                                           _stream_handle(stream)),
            "kvq_sparse_decode_attn")
     return out

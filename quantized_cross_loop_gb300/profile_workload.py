@@ -88,9 +88,11 @@ def main():
         n_select = max(1, max_t // 4)
         for _ in range(args.reps):
             st = kvq.kvq_sparse_ref_state(pool.table, wl.q, 2, wl.H, n_select, max_t)
-        ws = torch.zeros(16, dtype=torch.uint8, device=dev)
+        ws = torch.zeros(16, dtype=torch.uint8, device=dev)  # the per-key kernel, then the tensor-core path
         for _ in range(args.reps):
             kvq.kvq_sparse_decode_attn(pool.table, wl.q, wl.depth, wl.H, st, workspace=ws)
+        for _ in range(args.reps):
+            kvq.kvq_sparse_decode_attn(pool.table, wl.q, wl.depth, wl.H, st)
     elif args.stage == "tail":
         empty = torch.zeros((0, wl.H, wl.D), dtype=torch.bfloat16, device=dev)
         g = torch.Generator(device=dev)

@@ -213,10 +213,13 @@ def test_nvfp4_sparse_decode():
     scale = 1.0 / math.sqrt(D)
     st = kvq.kvq_sparse_ref_state(table, q.cuda(), 2, H, 128, max(lengths))
     q4 = torch.randn((len(lengths), Hq, D), generator=torch.Generator().manual_seed(601)).to(torch.bfloat16)
-    ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(16, dtype=torch.uint8, device="cuda")  # the per-key kernel
     out = kvq.kvq_sparse_decode_attn(table, q4.cuda(), 4, H, st, workspace=ws).cpu().numpy()
+    wsb = torch.zeros(kvq.kvq_sparse_decode_workspace_bytes(len(lengths), H, Hq, D, max(lengths)), dtype=torch.uint8,
+                      device="cuda")  # the key-masked tensor-core attention
+    out_tc = kvq.kvq_sparse_decode_attn(table, q4.cuda(), 4, H, st, workspace=wsb, algo=kvq.ATTN_MMA).cpu().numpy()
     torch.cuda.synchronize()
-    assert kvq.attn_error_word(st.workspace) == 0 and kvq.attn_error_word(ws) == 0
+    assert kvq.attn_error_word(st.workspace) == 0 and kvq.attn_error_word(ws) == 0 and kvq.attn_error_word(wsb) == 0
     sel, mass, o_ref, c_ref = (t.cpu().numpy() for t in (st.sel_idx, st.mass, st.o_ref, st.c_ref))
     for b, T in enumerate(lengths):
         S = sel[b][:, :min(128, T)]
@@ -225,3 +228,4 @@ def test_nvfp4_sparse_decode():
         ref = O.sparse_decode(bf16_bits(q4[b]), O.decode_f32(oks[b], 4), O.decode_f32(ovs[b], 4), scale, S,
                               mass[b].astype(np.float64), o_ref[b].astype(np.float64), c_ref[b].astype(np.float64))
         P.assert_attention_close(out[b], ref, f"sparse req {b}")
+        P.assert_attention_close(out_tc[b], ref, f"sparse req {b}, tensor-core path")

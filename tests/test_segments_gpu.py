@@ -111,3 +111,22 @@ def test_segments_inconsistent_entry_is_flagged():
         assert err != 0
         assert np.all(np.isnan(out[0]))
         P.assert_attention_close(out[1], ref1, f"algo {algo}")
+
+
+def test_segments_many_units_grid_stride():
+    """More (request, KV head) units than the epilogue kernels' grid (two blocks
+    per attention CTA): requests with segments far apart in the table, empty
+    requests with and without a tail, short packed requests, all in one call."""
+    n = 90  # 720 units
+    reqs, segs = [], []
+    for b in range(n):
+        T = (0, 64, 1, 130)[b % 4]
+        reqs.append(_request(T, T > 64 and b % 3 == 0, 300 + b))
+        segs.append(_segments(min(2, T), 5, 900 + b) if b in (1, 42, 44, 83, 87, 89) else None)
+    q, outs = _run(reqs, segs)
+    none = tuple(torch.zeros((0, H, D), dtype=torch.bfloat16) for _ in range(4))
+    for b, r in enumerate(reqs):
+        ref = _oracle(r, bf16_bits(q[b]), segs[b] if segs[b] is not None else none)
+        for algo, (out, err) in outs.items():
+            assert err == 0
+            P.assert_attention_close(out[b], ref, f"req {b} algo {algo}")

@@ -8,7 +8,9 @@ float64 in the oracle), so keys whose probabilities tie with the k-th one to
 within rounding may differ; the test checks the GPU selection against the
 oracle's probabilities (every selected key at least, every other key at most,
 the k-th probability up to 1e-5 relative) and then compares mass, C_ref and
-the later-loop output computed from that selection."""
+the later-loop output computed from that selection. Each later loop runs on
+both kernels: the per-key gather (a 16-byte workspace) and the key-masked
+tensor-core attention."""
 
 from __future__ import annotations
 
@@ -28,6 +30,19 @@ from tests import pathrun as P
 pytestmark = pytest.mark.gpu
 
 H, D = 8, 128
+PATHS = ("per_key", "tensor_core")
+
+
+def _decode(table, q, depth, st, path, Hq):
+    """A later loop on one of the two kernels; returns (out, error word)."""
+    if path == "per_key":
+        ws, algo = torch.zeros(16, dtype=torch.uint8, device="cuda"), kvq.ATTN_SIMT
+    else:
+        n = kvq.kvq_sparse_decode_workspace_bytes(q.shape[0], H, Hq, D, st.max_tokens)
+        ws, algo = torch.zeros(n, dtype=torch.uint8, device="cuda"), kvq.ATTN_MMA
+    out = kvq.kvq_sparse_decode_attn(table, q.cuda(), depth, H, st, workspace=ws, algo=algo)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), kvq.attn_error_word(ws)
 
 
 def _setup(Ts, sparse, Hq=32, seed=0):
@@ -86,10 +101,10 @@ def test_sparse_reference_and_later_loops(Ts, sparse, n_select, Hq):
     assert kvq.attn_error_word(st.workspace) == 0
     sel, mass, o_ref, c_ref = (t.cpu().numpy() for t in (st.sel_idx, st.mass, st.o_ref, st.c_ref))
     outs = {}
-    for depth, q in ((3, qs[1]), (4, qs[2])):
-        ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
-        outs[depth] = kvq.kvq_sparse_decode_attn(table, q.cuda(), depth, H, st, workspace=ws).cpu().numpy()
-        assert kvq.attn_error_word(ws) == 0
+    for path in PATHS:
+        for depth, q in ((3, qs[1]), (4, qs[2])):
+            outs[path, depth], err = _decode(table, q, depth, st, path, Hq)
+            assert err == 0, path
     for b, T in enumerate(Ts):
         K = min(n_select, T)
         assert np.all(sel[b][:, K:] == -1)
@@ -114,10 +129,11 @@ def test_sparse_reference_and_later_loops(Ts, sparse, n_select, Hq):
             kf, vf = O.decode_f32(oks[b], depth), O.decode_f32(ovs[b], depth)
             ref = O.sparse_decode(bf16_bits(q[b]), kf, vf, scale, S, mass[b].astype(np.float64),
                                   o_ref[b].astype(np.float64), c_ref[b].astype(np.float64))
-            P.assert_attention_close(outs[depth][b], ref, f"req {b} depth {depth}")
-            if K == T:  # every key kept: plain dense attention at this depth
-                dense = O.attention_f32(bf16_bits(q[b]), kf, vf, scale)
-                P.assert_attention_close(outs[depth][b], dense, f"dense req {b} depth {depth}")
+            for path in PATHS:
+                P.assert_attention_close(outs[path, depth][b], ref, f"req {b} depth {depth} {path}")
+                if K == T:  # every key kept: plain dense attention at this depth
+                    dense = O.attention_f32(bf16_bits(q[b]), kf, vf, scale)
+                    P.assert_attention_close(outs[path, depth][b], dense, f"dense req {b} depth {depth} {path}")
 
 
 def test_sparse_refuses_segments_and_bad_selections():
@@ -129,10 +145,32 @@ def test_sparse_refuses_segments_and_bad_selections():
     torch.cuda.synchronize()
     assert kvq.attn_error_word(st.workspace) != 0
     assert np.all(np.isnan(st.mass.cpu().numpy()[0])) and not np.any(np.isnan(st.mass.cpu().numpy()[1]))
+    # a later loop refuses the request with segments on both kernels
+    for path in PATHS:
+        out, err = _decode(table2, qs[1], 3, st, path, 32)
+        assert err & 1 and np.all(np.isnan(out[0])) and not np.any(np.isnan(out[1])), path
     # a corrupted selection (position past the request) is flagged, not read
     st = kvq.kvq_sparse_ref_state(table, qs[0].cuda(), 2, H, 16, 100)
     st.sel_idx[1, 0, 3] = 5000
-    ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
-    kvq.kvq_sparse_decode_attn(table, qs[1].cuda(), 3, H, st, workspace=ws)
+    for path in PATHS:
+        out, err = _decode(table, qs[1], 3, st, path, 32)
+        assert err & 32 and not np.any(np.isnan(out)), path
+
+
+def test_sparse_empty_selection_and_path_choice():
+    """n_select = 0: the later loop returns O_ref - C_ref on both kernels. The
+    tensor-core path asked for explicitly with a small workspace is an error;
+    AUTO with a small workspace takes the per-key kernel."""
+    table, reqs, oks, ovs, qs = _setup([300, 65], True, 32, seed=21)
+    st = kvq.kvq_sparse_ref_state(table, qs[0].cuda(), 2, H, 0, 300)
     torch.cuda.synchronize()
-    assert kvq.attn_error_word(ws) & 32
+    expect = (st.o_ref - st.c_ref).cpu().numpy()
+    for path in PATHS:
+        out, err = _decode(table, qs[1], 4, st, path, 32)
+        assert err == 0 and np.array_equal(out, expect), path
+    small = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_sparse_decode_attn(table, qs[1].cuda(), 4, H, st, workspace=small, algo=kvq.ATTN_MMA)
+    kvq.kvq_sparse_decode_attn(table, qs[1].cuda(), 4, H, st, workspace=small)
+    torch.cuda.synchronize()
+    assert kvq.attn_error_word(small) == 0
