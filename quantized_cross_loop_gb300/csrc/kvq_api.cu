@@ -859,10 +859,31 @@ kvq_status kvq_sparse_ref_state(const kvq_request* reqs, int n_requests, int n_h
   const size_t need = kvq_sparse_workspace_bytes(n_requests, n_heads, n_q_heads, head_dim, max_tokens);
   if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
     return fail(KVQ_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", need);
-  // the full attention at the reference depth: O_ref (and a cleared error word)
   const size_t apart = sparse_attn_part(n_requests, n_heads, n_q_heads);
-  st = kvq_decode_attn_packed_ex(reqs, n_requests, n_heads, n_q_heads, head_dim, ref_depth, q_ref, softmax_scale,
-                                 o_ref, workspace, apart, KVQ_ATTN_AUTO | KVQ_ATTN_NVFP4, stream);
+  float* logits = reinterpret_cast<float*>(static_cast<char*>(workspace) + apart);
+  const int g = n_q_heads / n_heads;
+  // the tensor-core attention writes every logit as it goes; the CUDA-core one
+  // (depth > 4) does not, and a separate kernel recomputes them
+  const bool tc = ref_depth <= kMmaMaxDepth && (g == 1 || g == 2 || g == 4 || g == 8) && aligned16(o_ref);
+  if (tc) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+    const int sms = sm_count(dev);
+    if (sms <= 0) return fail(KVQ_ERR_CUDA, "cannot read the SM count of device %d", dev);
+    AttnArgs at;
+    attention_args(at, reqs, n_requests, n_heads, n_q_heads, ref_depth, q_ref, softmax_scale, o_ref,
+                   static_cast<char*>(workspace), KVQ_ATTN_MMA, true, dev, sms);
+    at.logits = logits;
+    at.logit_stride = max_tokens;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(at.err, 0, 16, s);
+    if (e != cudaSuccess) return cuda_status(e, "clear error word");
+    st = attention_launches(at, KVQ_ATTN_MMA, true, s);
+  } else {  // the full attention at the reference depth: O_ref (and a cleared error word)
+    st = kvq_decode_attn_packed_ex(reqs, n_requests, n_heads, n_q_heads, head_dim, ref_depth, q_ref, softmax_scale,
+                                   o_ref, workspace, apart, KVQ_ATTN_AUTO | KVQ_ATTN_NVFP4, stream);
+  }
   if (st != KVQ_OK) return st;
   SparseArgs a;
   memset(&a, 0, sizeof a);
@@ -876,12 +897,13 @@ kvq_status kvq_sparse_ref_state(const kvq_request* reqs, int n_requests, int n_h
   a.n_select = n_select;
   a.q = q_ref;
   a.scale = softmax_scale;
-  a.logits = reinterpret_cast<float*>(static_cast<char*>(workspace) + apart);
+  a.logits = logits;
   a.sel_idx = sel_idx;
   a.mass = mass;
   a.c_ref = c_ref;
   a.err = static_cast<int32_t*>(workspace);
-  return cuda_status(launch_sparse_select_path(a, reinterpret_cast<cudaStream_t>(stream)), "sparse reference launch");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(tc ? launch_sparse_select(a, s) : launch_sparse_select_path(a, s), "sparse reference launch");
 }
 
 static size_t sparse_mask_words(int max_tokens) { return 2 * ((size_t(max_tokens) + 63) / 64); }

@@ -41,6 +41,10 @@ struct AttnArgs {
   // says key t is selected; the logits of the other keys are dropped. NULL: every key.
   const uint32_t* sel_mask;
   int32_t mask_words;
+  // sparse decode reference pass (tensor-core kernel only): every logit (log2
+  // units) of key t < logit_stride to logits[(b * Hq + query head) * logit_stride + t]
+  float* logits;
+  int32_t logit_stride;
 };
 
 // Workspace layout: [0,16) error word (int32 0) and plan flags (int32 1); then int32 prefix[B+1] (rounded to 16 B);

@@ -545,7 +545,7 @@ __device__ __forceinline__ void qk_pass_nv(const Stage& st, int j, const __half*
   for (int k = 0; k < 4; ++k) e[k] = (c[0][k] + c[1][k]) * tscale;
 }
 
-template <int DEPTH, bool kNv>
+template <int DEPTH, bool kNv, bool kSp>
 __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long long s0, long long e0) {
   const int gt = threadIdx.x - grp * kGroupThreads;  // thread within the group
   const int w = gt >> 5, lane = gt & 31;
@@ -732,7 +732,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       sv[1] = (t0ok && h1ok) ? sv[1] * lsc : -INFINITY;
       sv[2] = (t1ok && h0ok) ? sv[2] * lsc : -INFINITY;
       sv[3] = (t1ok && h1ok) ? sv[3] * lsc : -INFINITY;
-      if (a.sel_mask != nullptr) {  // sparse decode: only the query head's selected keys
+      if (kSp && a.sel_mask != nullptr) {  // sparse decode: only the query head's selected keys
         const int tb = t0 + 16 * w;   // the warp's first token: its 16 tokens share one mask word
         const uint32_t* mw = a.sel_mask + ((long long)Mprev.b * a.Hq + (long long)Mprev.h * gq) * a.mask_words + (tb >> 5);
         const uint32_t w0 = h0ok ? __ldg(mw + (long long)(2 * q) * a.mask_words) >> (tb & 31) : 0u;
@@ -741,6 +741,14 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         if (!((w1 >> g) & 1u)) sv[1] = -INFINITY;
         if (!((w0 >> (g + 8)) & 1u)) sv[2] = -INFINITY;
         if (!((w1 >> (g + 8)) & 1u)) sv[3] = -INFINITY;
+      }
+      if (kSp && a.logits != nullptr) {  // sparse decode reference pass: every logit, for the selection
+        const int ta = t0 + 16 * w + g, tc = ta + 8;
+        float* lr = a.logits + ((long long)Mprev.b * a.Hq + (long long)Mprev.h * gq) * a.logit_stride;
+        if (t0ok && h0ok && ta < a.logit_stride) lr[(long long)(2 * q) * a.logit_stride + ta] = sv[0];
+        if (t0ok && h1ok && ta < a.logit_stride) lr[(long long)(2 * q + 1) * a.logit_stride + ta] = sv[1];
+        if (t1ok && h0ok && tc < a.logit_stride) lr[(long long)(2 * q) * a.logit_stride + tc] = sv[2];
+        if (t1ok && h1ok && tc < a.logit_stride) lr[(long long)(2 * q + 1) * a.logit_stride + tc] = sv[3];
       }
       mt0 = fmaxf(sv[0], sv[2]);
       mt1 = fmaxf(sv[1], sv[3]);
@@ -889,7 +897,9 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
   if (cur_unit >= 0) finish_unit(a, Gs, U, Mprev, grp, vcta, w, lane);
 }
 
-template <int DEPTH, bool kNv>
+// kSp: the instantiation that reads the sparse-decode key masks and writes the
+// reference pass's logits (the dense calls run the one without those branches)
+template <int DEPTH, bool kNv, bool kSp>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -919,21 +929,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a) {
     if ((threadIdx.x & 31) == 0) producer<DEPTH, kNv>(a, S, grp, s0, e0);
     return;
   }
-  consumer<DEPTH, kNv>(a, S, grp, vcta, s0, e0);
+  consumer<DEPTH, kNv, kSp>(a, S, grp, vcta, s0, e0);
 }
 
-template <int DEPTH, bool kNv>
+template <int DEPTH, bool kNv, bool kSp>
 cudaError_t launch_depth(const AttnArgs& a, cudaStream_t stream) {
   const int smem = int(sizeof(Smem));
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
-        cudaFuncSetAttribute(attn_mma_kernel<DEPTH, kNv>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(attn_mma_kernel<DEPTH, kNv, kSp>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attn_mma_kernel<DEPTH, kNv><<<a.n_ctas / kGroups, kThreads, smem, stream>>>(a);
+  attn_mma_kernel<DEPTH, kNv, kSp><<<a.n_ctas / kGroups, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
+}
+
+// the NVFP4-reading instantiation only when the caller says the table may
+// hold NVFP4 loops (the INT4 one refuses them: error bit 64, NaN output)
+template <bool kSp>
+cudaError_t launch_form(const AttnArgs& a, cudaStream_t stream) {
+  switch (a.depth * 2 + (a.nvfp4 ? 1 : 0)) {
+    case 2: return launch_depth<1, false, kSp>(a, stream);
+    case 3: return launch_depth<1, true, kSp>(a, stream);
+    case 4: return launch_depth<2, false, kSp>(a, stream);
+    case 5: return launch_depth<2, true, kSp>(a, stream);
+    case 6: return launch_depth<3, false, kSp>(a, stream);
+    case 7: return launch_depth<3, true, kSp>(a, stream);
+    case 8: return launch_depth<4, false, kSp>(a, stream);
+    case 9: return launch_depth<4, true, kSp>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace mma_attn
@@ -942,20 +969,9 @@ int mma_virtual_ctas_per_block() { return mma_attn::kGroups; }
 
 cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {
   using namespace mma_attn;
-  cudaError_t e;
-  // the NVFP4-reading instantiation only when the caller says the table may
-  // hold NVFP4 loops (the INT4 one refuses them: error bit 64, NaN output)
-  switch (a.depth * 2 + (a.nvfp4 ? 1 : 0)) {
-    case 2: e = launch_depth<1, false>(a, stream); break;
-    case 3: e = launch_depth<1, true>(a, stream); break;
-    case 4: e = launch_depth<2, false>(a, stream); break;
-    case 5: e = launch_depth<2, true>(a, stream); break;
-    case 6: e = launch_depth<3, false>(a, stream); break;
-    case 7: e = launch_depth<3, true>(a, stream); break;
-    case 8: e = launch_depth<4, false>(a, stream); break;
-    case 9: e = launch_depth<4, true>(a, stream); break;
-    default: return cudaErrorInvalidValue;
-  }
+  const cudaError_t e = (a.sel_mask != nullptr || a.logits != nullptr) ? launch_form<true>(a, stream)
+                                                                        : launch_form<false>(a, stream);
+  if (e == cudaErrorInvalidValue) return e;
   count_launch();
   return e;
 }

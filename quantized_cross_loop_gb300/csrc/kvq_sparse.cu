@@ -400,6 +400,13 @@ cudaError_t launch_sparse_select_path(const SparseArgs& a, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
+cudaError_t launch_sparse_select(const SparseArgs& a, cudaStream_t stream) {
+  if (a.n_requests == 0) return cudaSuccess;
+  sparse_select_kernel<<<a.n_requests * a.Hq, kSelThreads, 0, stream>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_sparse_attn(const SparseArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
   sparse_attn_kernel<<<a.n_requests * a.Hq, 32 * kAttnWarps, 0, stream>>>(a);

@@ -32,6 +32,8 @@ struct SparseArgs {
 
 // Reference pass after the full attention: logits, selection, m and C_ref.
 cudaError_t launch_sparse_select_path(const SparseArgs& a, cudaStream_t stream);
+// The selection alone, when the tensor-core attention wrote the logits.
+cudaError_t launch_sparse_select(const SparseArgs& a, cudaStream_t stream);
 // A later loop: the corrected output from the selected keys.
 cudaError_t launch_sparse_attn(const SparseArgs& a, cudaStream_t stream);
 // A later loop on the tensor-core kernel: the key masks of the selections
