@@ -260,7 +260,7 @@ def main():
     # ---- workload, resident in HBM (each rank its own independent batch)
     wl = rank_workload(cfg_idx, rank, replicate, dev)
     reqs = wl.requests
-    src_all = pack_sources(reqs, torch, dev)  # one buffer, so the end-to-end run copies it in one piece
+    src_all, src_chunks = pack_sources(reqs, torch, dev)  # one buffer in (loop, kind) chunks for the end-to-end run
     B, H, D, Hq, depth = wl.n_requests, wl.H, wl.D, wl.Hq, wl.depth
     lengths = [r.T for r in reqs]
     pool = kvq.PackedPool(lengths, [r.active for r in reqs], H, D, depth, dev)
@@ -295,9 +295,13 @@ def main():
         ev.record(side)
         stream.wait_event(ev)
 
-    def encode_all():
+    def encode_all(ready=None):
+        """ready[j] = (K event, V event): the sources of loop j have arrived (end-to-end run)."""
         fork()
         for j in range(depth):
+            if ready is not None:
+                stream.wait_event(ready[j][0])
+                side.wait_event(ready[j][1])
             kvq.kvq_encode_batch(pool, kvq.KVQ_K, j, xk_ptrs[j], stream=stream)
             kvq.kvq_encode_batch(pool, kvq.KVQ_V, j, xv_ptrs[j], stream=side, workspace=side_ws)
         join()
@@ -314,10 +318,12 @@ def main():
     n_ev = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
 
-    def step(e=None):
+    def step(e=None, ready=None, after_encode=None):
         if e:
             e[0].record(stream)
-        encode_all()
+        encode_all(ready)
+        if after_encode is not None:
+            after_encode.record(stream)
         if e:
             e[1].record(stream)
         reconstruct_all()
@@ -369,7 +375,7 @@ def main():
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, torch, kvq, src_all, q, out, step, stream, world, dev, step_bytes, dist)
+        e2e = run_e2e(args, torch, kvq, src_all, src_chunks, q, out, step, stream, world, dev, step_bytes, dist)
 
     # ---- roofline of the attention kernel call (plan + attention + combine)
     dominant = max(phase_ms, key=phase_ms.get)
@@ -427,19 +433,28 @@ def main():
 
 def pack_sources(reqs, torch, dev):
     """Moves every request's BF16 sources into one device buffer (the
-    requests' tensors become views of it) and returns the buffer."""
+    requests' tensors become views of it), ordered by loop, then K before V,
+    then request, so that the sources of one (loop, kind) are one contiguous
+    chunk. Returns the buffer and the chunks' element ranges [loop][kind]."""
     total = sum(x.numel() for r in reqs for xs in (r.xk, r.xv) for x in xs)
     flat = torch.empty(total, dtype=torch.bfloat16, device=dev)
+    depth = len(reqs[0].xk) if reqs else 0
     off = 0
-    for r in reqs:
-        for xs in (r.xk, r.xv):
-            for j, x in enumerate(xs):
-                v = flat[off:off + x.numel()].view(x.shape)
-                v.copy_(x)
+    chunks = []
+    for j in range(depth):
+        per_kind = []
+        for kind in (0, 1):
+            start = off
+            for r in reqs:
+                xs = r.xk if kind == 0 else r.xv
+                v = flat[off:off + xs[j].numel()].view(xs[j].shape)
+                v.copy_(xs[j])
                 xs[j] = v
-                off += x.numel()
+                off += v.numel()
+            per_kind.append((start, off))
+        chunks.append(per_kind)
     torch.cuda.synchronize()
-    return flat
+    return flat, chunks
 
 
 def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, reps=10):
@@ -651,19 +666,36 @@ def run_nvfp4_extra(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, tim
     return res
 
 
-def run_e2e(args, torch, kvq, src_all, q, out, step, stream, world, dev, step_bytes, dist):
+def run_e2e(args, torch, kvq, src_all, src_chunks, q, out, step, stream, world, dev, step_bytes, dist):
     """Same step through the public API with host inputs: H2D of every BF16
-    source (one pinned buffer) and of q, the step, D2H of the attention output."""
+    source (one pinned buffer) and of q, the step, D2H of the attention output.
+    The sources move in (loop, kind) chunks on a copy stream, and each loop's
+    encode waits only for its own chunk, so the copies of later loops overlap
+    the encode of earlier ones (and the next step's copies the reconstruction
+    and attention of this one, once this step's encode has read its sources)."""
     host_src = torch.empty(src_all.shape, dtype=src_all.dtype, pin_memory=True).copy_(src_all)
     host_q = torch.empty(q.shape, dtype=q.dtype, pin_memory=True).copy_(q)
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = host_src.numel() * host_src.element_size() + host_q.numel() * host_q.element_size()
     d2h = host_out.numel() * host_out.element_size()
+    copy_s = torch.cuda.Stream(device=dev)
+    sources_free = torch.cuda.Event()  # the previous step's encode has read the sources
+    sources_free.record(stream)
 
     def e2e_step():
-        src_all.copy_(host_src, non_blocking=True)
+        copy_s.wait_event(sources_free)
+        ready = []
+        for per_kind in src_chunks:
+            evs = []
+            for (lo, hi) in per_kind:
+                with torch.cuda.stream(copy_s):
+                    src_all[lo:hi].copy_(host_src[lo:hi], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_s)
+                evs.append(ev)
+            ready.append(tuple(evs))
         q.copy_(host_q, non_blocking=True)
-        step()
+        step(ready=ready, after_encode=sources_free)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(2):
@@ -675,6 +707,7 @@ def run_e2e(args, torch, kvq, src_all, q, out, step, stream, world, dev, step_by
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
+    sources_free.record(stream)  # the copies start inside the timed region
     for _ in range(n):
         e2e_step()
     b.record(stream)
