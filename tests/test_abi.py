@@ -173,6 +173,16 @@ def test_host_validation_rejects_bad_arguments(L):
     assert f(None, 1, 8, 32, 128, 4, None, ctypes.c_float(0.1), None, None, 0, 5, None) == BAD
     assert f(None, 1, 8, 32, 128, 4, None, ctypes.c_float(0.1), None, None, 0, 0, None) == BAD  # NULL pointers
     assert L.kvq_status_string(-4) == b"KVQ_ERR_WORKSPACE"
+    # sparse later loop: algo, then the workspace the chosen kernel needs (no device work before either)
+    sp = L.kvq_sparse_decode_attn_ex
+    p16, ws16 = ctypes.c_void_p(64), ctypes.create_string_buffer(32)
+    ws_al = ctypes.c_void_p((ctypes.addressof(ws16) + 15) // 16 * 16)
+    args = (p16, 1, 8, 32, 128, 4, p16, ctypes.c_float(0.1), 4, 64, p16, p16, p16, p16, p16)
+    assert sp(*args, ws_al, 16, 5, None) == BAD  # not an algo
+    assert sp(*args, ws_al, 8, 0, None) == -4  # below the 16 bytes of the error word
+    assert sp(*args, ws_al, 16, 2, None) in (-4, -5)  # the tensor-core path asked for with 16 bytes (or no GPU here)
+    assert L.kvq_sparse_decode_workspace_bytes(-1, 8, 32, 128, 64) == 0
+    assert L.kvq_sparse_decode_workspace_bytes(1, 0, 32, 128, 64) == 0
 
 
 def test_request_fill_checks_pairs(L):
