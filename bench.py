@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -726,11 +727,33 @@ def run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq):
     n = max(1, min(len(reqs), int(args.cpu_seconds * cores / max(t1, 1e-3))))
     sample = reqs[:n]
     secs = oracle_sample(sample, q[:n], depth, scale, cores)
-    ab = algorithmic_bytes(sample, H, D, Hq, depth, lambda k, nn, s: kvq.payload_bytes(k, nn, H, D, s))
-    tot = ab["encode"] + ab["reconstruct"] + ab["attention"]
-    return {"value": tot / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+    def bytes_of(rs):
+        ab = algorithmic_bytes(rs, H, D, Hq, depth, lambda k, nn, s: kvq.payload_bytes(k, nn, H, D, s))
+        return ab["encode"] + ab["reconstruct"] + ab["attention"]
+
+    return {"value": bytes_of(sample) / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "value_1_thread": bytes_of(reqs[:1]) / t1 / 1e9, "cpu_model": cpu_model(),
             "sample": f"{n} of {len(reqs)} requests of the same workload, whole path (encode K/V 4 loops, "
-                      f"reconstruct, FP32 attention), {secs:.1f} s on {cores} threads"}
+                      f"reconstruct, FP32 attention), {secs:.1f} s on {cores} threads; value_1_thread: one "
+                      f"request on one thread, {t1:.2f} s"}
+
+
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (model name, or implementer and part on Arm)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return platform.machine()
+    fields = {}
+    for line in info:
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return platform.machine()
 
 
 def run_reference(args, world, rank, cfg_idx, replicate, desc):
@@ -770,7 +793,8 @@ def run_reference(args, world, rank, cfg_idx, replicate, desc):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
         "config": {"workload": args.workload, "description": desc, "oracle_requests_per_step": n},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
