@@ -734,9 +734,11 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       sv[3] = (t1ok && h1ok) ? sv[3] * lsc : -INFINITY;
       if (kSp && a.sel_mask != nullptr) {  // sparse decode: only the query head's selected keys
         const int tb = t0 + 16 * w;   // the warp's first token: its 16 tokens share one mask word
+        // a request longer than the masks cover (the sparse path refuses it) selects nothing here
+        const bool in = (tb >> 5) < a.mask_words;
         const uint32_t* mw = a.sel_mask + ((long long)Mprev.b * a.Hq + (long long)Mprev.h * gq) * a.mask_words + (tb >> 5);
-        const uint32_t w0 = h0ok ? __ldg(mw + (long long)(2 * q) * a.mask_words) >> (tb & 31) : 0u;
-        const uint32_t w1 = h1ok ? __ldg(mw + (long long)(2 * q + 1) * a.mask_words) >> (tb & 31) : 0u;
+        const uint32_t w0 = (in && h0ok) ? __ldg(mw + (long long)(2 * q) * a.mask_words) >> (tb & 31) : 0u;
+        const uint32_t w1 = (in && h1ok) ? __ldg(mw + (long long)(2 * q + 1) * a.mask_words) >> (tb & 31) : 0u;
         if (!((w0 >> g) & 1u)) sv[0] = -INFINITY;
         if (!((w1 >> g) & 1u)) sv[1] = -INFINITY;
         if (!((w0 >> (g + 8)) & 1u)) sv[2] = -INFINITY;

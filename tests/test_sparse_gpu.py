@@ -157,6 +157,27 @@ def test_sparse_refuses_segments_and_bad_selections():
         assert err & 32 and not np.any(np.isnan(out)), path
 
 
+def test_sparse_refuses_requests_longer_than_max_tokens():
+    """max_tokens below one request's length: that request is refused (NaN, bit 1)
+    by the reference pass and by both later-loop kernels, which read no key mask
+    or logit row past its end; the other request is unaffected."""
+    table, reqs, oks, ovs, qs = _setup([100, 200], False, 32, seed=31)
+    st = kvq.kvq_sparse_ref_state(table, qs[0].cuda(), 2, H, 16, 150)
+    torch.cuda.synchronize()
+    assert kvq.attn_error_word(st.workspace) & 1
+    mass = st.mass.cpu().numpy()
+    assert np.all(np.isnan(mass[1])) and not np.any(np.isnan(mass[0]))
+    scale = 1.0 / math.sqrt(D)
+    S = st.sel_idx.cpu().numpy()[0][:, :16]
+    ref = O.sparse_decode(bf16_bits(qs[1][0]), O.decode_f32(oks[0], 3), O.decode_f32(ovs[0], 3), scale, S,
+                          mass[0].astype(np.float64), st.o_ref.cpu().numpy()[0].astype(np.float64),
+                          st.c_ref.cpu().numpy()[0].astype(np.float64))
+    for path in PATHS:
+        out, err = _decode(table, qs[1], 3, st, path, 32)
+        assert err & 1 and np.all(np.isnan(out[1])), path
+        P.assert_attention_close(out[0], ref, f"request 0 {path}")
+
+
 def test_sparse_empty_selection_and_path_choice():
     """n_select = 0: the later loop returns O_ref - C_ref on both kernels. The
     tensor-core path asked for explicitly with a small workspace is an error;
