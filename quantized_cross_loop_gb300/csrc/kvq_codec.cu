@@ -877,8 +877,10 @@ __global__ void __launch_bounds__(kEncKThreads, R == 0 ? 5 : 4)
     }
     __syncthreads();
 
-    // ---- phase 1: residual rows
-#pragma unroll 1
+    // ---- phase 1: residual rows (both halves unrolled, so that the second
+    // half's loads issue early, except with two predecessor loops, where the
+    // extra live registers spill and it measured slower)
+#pragma unroll(R == 2 ? 1 : 2)
     for (int i0 = 0; i0 < kG; i0 += 4 * kWarps) {
       const int i = i0 + 4 * warp + lg;
       const bool live = i < len;
