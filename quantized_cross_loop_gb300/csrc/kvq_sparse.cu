@@ -177,9 +177,15 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseArgs a
     __syncthreads();
     const unsigned prefix = s_prefix;
     const unsigned hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
-    for (int t = tid; t < T; t += kSelThreads) {
-      const uint32_t key = okey(s[t]);
-      if ((key & hmask) == (prefix & hmask)) atomicAdd(&s_hist[(key >> shift) & 0xFFu], 1u);
+    // warp-aggregated increments: logits of one request crowd a few bins (the top
+    // byte is the sign and most of the exponent), so one atomic per bin and warp
+    for (int base = 0; base < T; base += kSelThreads) {
+      const int t = base + tid;
+      const uint32_t key = t < T ? okey(s[t]) : 0u;
+      const bool in = t < T && (key & hmask) == (prefix & hmask);
+      const unsigned bin = (key >> shift) & 0xFFu;
+      const unsigned peers = __match_any_sync(0xffffffffu, in ? bin : 256u + unsigned(lane));
+      if (in && __ffs(peers) - 1 == lane) atomicAdd(&s_hist[bin], unsigned(__popc(peers)));
     }
     __syncthreads();
     if (tid == 0) {
