@@ -739,7 +739,15 @@ def run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq):
 
 
 def cpu_model():
-    """The host CPU as /proc/cpuinfo names it (model name, or implementer and part on Arm)."""
+    """The host CPU as lscpu names it, else as /proc/cpuinfo does (model name, or
+    implementer and part on Arm)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
     try:
         info = open("/proc/cpuinfo").read().splitlines()
     except OSError:
