@@ -983,6 +983,7 @@ kvq_status kvq_sparse_decode_attn_ex(const kvq_request* reqs, int n_requests, in
   at.sel_mask = a.sel_mask;
   at.mask_words = a.mask_words;
   a.stats = at.stats;
+  a.refuse_nvfp4 = at.refuse_nvfp4;
   st = attention_launches(at, KVQ_ATTN_MMA, false, s);
   if (st != KVQ_OK) return st;
   return cuda_status(launch_sparse_epilogue(a, s), "sparse epilogue launch");

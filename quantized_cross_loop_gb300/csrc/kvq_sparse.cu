@@ -372,6 +372,13 @@ __global__ void __launch_bounds__(kD) sparse_epilogue_kernel(SparseArgs a) {
     out[d] = __int_as_float(0x7fc00000);
     return;
   }
+  if (a.refuse_nvfp4) {  // refused by the attention's plan (bit 64): its softmax state was never written
+    for (int j = 0; j < a.depth; ++j)
+      if (r.loop[j].flags & (KVQ_LOOP_K_NVFP4 | KVQ_LOOP_V_NVFP4)) {
+        out[d] = __int_as_float(0x7fc00000);
+        return;
+      }
+  }
   const float cnew = a.stats[bq].y > 0.0f ? out[d] : 0.0f;  // an empty selection contributes nothing
   out[d] = a.o_ref[(long long)bq * kD + d] - a.c_ref[(long long)bq * kD + d] + a.mass[bq] * cnew;
 }

@@ -28,6 +28,7 @@ struct SparseArgs {
   uint32_t* sel_mask;   // [B][Hq][mask_words]: bit t set for each selected position t
   int32_t mask_words;   // 2 * ceil(max_tokens / 64): whole 64-token tiles
   const float2* stats;  // [B][Hq] softmax (max, sum) of the masked attention
+  int32_t refuse_nvfp4; // the masked attention read no NVFP4 loop: requests holding one were refused
 };
 
 // Reference pass after the full attention: logits, selection, m and C_ref.

@@ -204,6 +204,33 @@ def test_int4_tensor_core_kernel_refuses_nvfp4():
     P.assert_attention_close(o[1], ref, "INT4 request")
 
 
+def test_sparse_later_loop_without_the_nvfp4_flag_refuses_nvfp4():
+    """The tensor-core sparse later loop called without KVQ_ATTN_NVFP4: the request
+    holding NVFP4 loops is refused (NaN, bit 64), the INT4 request beside it matches
+    the same call with the flag."""
+    H, Hq = 8, 32
+    _, kc, vc, oks, ovs, q = _nvfp4_requests([300], Hq, 710)
+    _, kc4, vc4, oks4, ovs4, _ = _nvfp4_requests([200], Hq, 711, (I4, I4, I4, I4))
+    table = kvq.RequestTable(kc + kc4, vc + vc4, torch.device("cuda"))
+    q2 = torch.randn((2, Hq, D), generator=torch.Generator().manual_seed(712)).to(torch.bfloat16).cuda()
+    st = kvq.kvq_sparse_ref_state(table, q2, 2, H, 64, 300)
+    L = kvq.lib()
+    outs = []
+    for algo in (kvq.ATTN_MMA, kvq.ATTN_MMA | kvq.ATTN_NVFP4):
+        ws = torch.zeros(kvq.kvq_sparse_decode_workspace_bytes(2, H, Hq, D, 300), dtype=torch.uint8, device="cuda")
+        out = torch.empty((2, Hq, D), dtype=torch.float32, device="cuda")
+        sel = st.sel_idx.contiguous()
+        rc = L.kvq_sparse_decode_attn_ex(kvq._dptr(table.table), 2, H, Hq, D, 4, kvq._dptr(q2), ctypes.c_float(0.088),
+                                         64, 300, kvq._dptr(sel), kvq._dptr(st.mass), kvq._dptr(st.o_ref),
+                                         kvq._dptr(st.c_ref), kvq._dptr(out), kvq._dptr(ws), ws.numel(), algo, None)
+        torch.cuda.synchronize()
+        assert rc == 0
+        outs.append((out.cpu().numpy(), kvq.attn_error_word(ws)))
+    (o_no, e_no), (o_nv, e_nv) = outs
+    assert e_no & 64 and np.all(np.isnan(o_no[0])) and e_nv == 0 and not np.any(np.isnan(o_nv))
+    assert np.array_equal(o_no[1], o_nv[1])
+
+
 def test_nvfp4_sparse_decode():
     """Sparse decode attention (FlashLoop RFC §3.2) over NVFP4 residual loops."""
     lengths = [1000, 300]
