@@ -359,7 +359,7 @@ kvq_status kvq_reconstruct_batch_ex(const kvq_request* reqs, int n_requests, int
 size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim);
 
 #define KVQ_ATTN_AUTO 0 /* tensor-core kernel for depth <= 4, CUDA-core kernel beyond */
-#define KVQ_ATTN_SIMT 1 /* CUDA-core kernel: exact BF16 chain per element, FP32 dot products */
+#define KVQ_ATTN_SIMT 1 /* CUDA-core kernel: FP32 decode of the chain per element, FP32 dot products */
 #define KVQ_ATTN_MMA 2  /* tensor-core kernel (depth <= 4): unpack + folded dequant into m16n8k16 MMAs */
 #define KVQ_ATTN_NVFP4 8 /* OR-ed into algo: the table may hold NVFP4 residual loops. Without it the
                            tensor-core kernel refuses such a request (NaN output, error bit 64); the
@@ -463,15 +463,22 @@ kvq_status kvq_sparse_decode_attn_ex(const kvq_request* reqs, int n_requests, in
  * There is no counterpart on the pages: it serves callers that cannot
  * allocate device memory (code running under CUDA graph capture, plugins in a
  * serving process that owns all device allocations, hosts whose allocator the
- * library cannot reach). Arguments, results and errors are those of
- * kvq_decode_attn_packed; the scratch it needs lives in a file-scope device
- * array of KVQ_NOALLOC_SCRATCH_BYTES (32 MiB), reserved on every device that
- * loads it until the process exits.
+ * library cannot reach). Arguments and results are those of
+ * kvq_decode_attn_packed (an INT4 table: a request holding NVFP4 loops is
+ * refused, as kvq_decode_attn_packed_ex refuses it without KVQ_ATTN_NVFP4).
+ * Host-side checks return the same status codes. The device-side error word
+ * lives in the static scratch, which the caller cannot read: a request the
+ * kernels refuse (NVFP4 loops, an inconsistent table entry, a timed-out
+ * pipeline wait) is seen only as NaN in its output rows. The scratch it needs
+ * lives in a file-scope device array of KVQ_NOALLOC_SCRATCH_BYTES (32 MiB),
+ * reserved on every device that loads it until the process exits.
  *   - Sizes whose kvq_decode_attn_workspace_bytes() exceed 32 MiB are rejected
  *     with KVQ_ERR_WORKSPACE before any launch (on a 152-SM GB300 that is about
  *     6800 request x KV-head pairs per call).
  *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *     device current; make that first call before any stream capture. The
+ *     address is kept for the life of the process: do not reset the device
+ *     (cudaDeviceReset) once this entry point has been used.
  *   - Every call shares the array and leaves its contents behind; calls that
  *     overlap on the GPU race on it and must be serialised by the caller.
  */

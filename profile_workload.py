@@ -1,8 +1,8 @@
 """Runs one stage of the packed-KV path on a seeded synthetic workload, for
 profilers (ncu captures of a single kernel). It reports no timing.
 
-  python -m quantized_cross_loop_gb300.profile_workload --workload cfg3 --stage attention --reps 2
-  python -m quantized_cross_loop_gb300.profile_workload --workload cfg2x128 --stage encode
+  python profile_workload.py --workload cfg3 --stage attention --reps 2
+  python profile_workload.py --workload cfg2x128 --stage encode
 
 Workloads: cfg1..cfg4 (the synthetic configurations), cfg2xN (N independent
 requests of configuration 2). Stages:

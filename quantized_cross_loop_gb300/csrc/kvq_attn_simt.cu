@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnArgs a) {
         }
       }
       __syncthreads();
-      // exact BF16 chain for the tile's K̂ and V̂ rows
+      // FP32 decode of the chain (no BF16 rounding) for the tile's K and V rows
       for (int idx = tid; idx < KVQ_TILE * (kD / 4); idx += blockDim.x) {
         int tt = idx / (kD / 4), c0 = (idx % (kD / 4)) * 4;
         if (tt < nvalid) {

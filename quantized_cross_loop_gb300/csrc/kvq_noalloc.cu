@@ -12,7 +12,10 @@
 // The array is reserved on every device where this code's module is loaded and
 // stays there until the process exits. Its device address is looked up once
 // per device (cudaGetSymbolAddress, with that device current) on the first call
-// made on that device, so that first call must come before any stream capture.
+// made on that device, so that first call must come before any stream capture;
+// the address is kept for the life of the process, so the device must not be
+// reset once this entry point has been used. The kernels' error word lives in
+// the array too: a request they refuse shows only as NaN output rows.
 // All calls share the array and leave the last call's contents in it; calls
 // that overlap on the GPU (other streams or threads) race on it and must be
 // serialised by the caller.

@@ -19,6 +19,7 @@ import pytest
 import torch
 
 from oracle import oracle as O
+from tests import reader_bound as RB
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -616,6 +617,83 @@ def test_attention_f32_matches_float64_sdpa_on_decoded_chain():
     vt = torch.from_numpy(vf.astype(np.float64)).permute(1, 0, 2).repeat_interleave(g, 0).unsqueeze(0)
     ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=1 / math.sqrt(D)).reshape(Hq, D)
     assert np.max(np.abs(out - ref.numpy())) < 2e-5
+
+
+
+# ---------------------------------------------------------------- direct-reader error bound
+
+
+def _nested_chain(T, H, D, seed, sparse):
+    rng = np.random.default_rng(seed)
+    xs = [rng.standard_normal((T, H, D)).astype(np.float32) * 2.0]
+    for r in range(1, 4):
+        xs.append(xs[-1] + 0.1 * rng.standard_normal((T, H, D)).astype(np.float32))
+    acts = [None, None, None, None]
+    if sparse:
+        a3 = np.sort(rng.choice(T, size=(T + 1) // 2, replace=False)).astype(np.int32)
+        a4 = np.sort(rng.choice(a3, size=(len(a3) + 1) // 2, replace=False)).astype(np.int32)
+        acts = [None, None, a3, a4]
+    return [bf16(x) for x in xs], acts
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+def test_chain_gap_recurrence_bounds_bf16_vs_fp32_chain(sparse):
+    """The per-element gap between the BF16 reconstruction and the FP32 decode
+    stays within the rounding recurrence of tests/reader_bound.py at every
+    depth, and the recurrence is tight (within 2x of the largest gap). A chain
+    read one loop short on the FP32 side breaks it."""
+    xs, acts = _nested_chain(150, 2, 128, 31 + sparse, sparse)
+    for kind in (O.KIND_K, O.KIND_V):
+        st = O.encode_chain(kind, xs, acts)
+        for d in range(1, 5):
+            b = RB.chain_gap_bound(st, d)
+            gap = np.abs(f32(O.reconstruct(st, d)).astype(np.float64) - O.decode_f32(st, d))
+            assert np.all(gap <= b)
+            assert (gap / np.maximum(b, 1e-300)).max() > 0.5
+        short = np.abs(f32(O.reconstruct(st, 4)).astype(np.float64) - O.decode_f32(st, 3))
+        assert np.any(short > RB.chain_gap_bound(st, 4))
+
+
+def test_softmax_shift_bound_holds_for_large_shifts():
+    """The second-order bound on a softmax-weighted sum under score and value
+    shifts, checked against the exact float64 value for shifts up to 0.5."""
+    rng = np.random.default_rng(9)
+    for trial in range(200):
+        T, D = int(rng.integers(1, 300)), 8
+        s = rng.standard_normal(T) * float(rng.choice([0.1, 1.0, 5.0]))
+        e = rng.standard_normal(T) * float(rng.choice([1e-4, 1e-2, 0.1, 0.25]))
+        vf = rng.standard_normal((T, D))
+        vh = vf + rng.standard_normal((T, D)) * 1e-3
+        w0 = np.exp(s - s.max())
+        w0 /= w0.sum()
+        w1 = np.exp(s + e - (s + e).max())
+        w1 /= w1.sum()
+        exact = np.abs(w1 @ vh - w0 @ vf)
+        b = RB.softmax_shift_bound(s, e, vh, vf)
+        assert np.all(exact <= b), trial
+        if np.abs(e).max() <= 1e-2:  # small shifts: the bound is essentially the exact value
+            assert b.max() <= 1.1 * exact.max() + 1e-6, trial
+
+
+@pytest.mark.parametrize("sparse,depth", [(False, 1), (False, 4), (True, 3), (True, 4)])
+def test_reader_error_bound_holds(sparse, depth):
+    """FlashLoop RFC §9: the attention over the BF16 reconstruction and the FP32
+    attention over the FP32 decode differ by at most the derived bound; a V
+    chain read one loop short exceeds it."""
+    xk, acts = _nested_chain(300, 2, 128, 41 + depth, sparse)
+    xv, _ = _nested_chain(300, 2, 128, 51 + depth, sparse)
+    ks = O.encode_chain(O.KIND_K, xk, acts)
+    vs = O.encode_chain(O.KIND_V, xv, acts)
+    q = bf16(np.random.default_rng(3).standard_normal((8, 128)))
+    scale = 1 / math.sqrt(128)
+    o_f32 = O.attention_f32(q, O.decode_f32(ks, depth), O.decode_f32(vs, depth), scale).astype(np.float64)
+    o_bf = O.attention(q, O.reconstruct(ks, depth), O.reconstruct(vs, depth), scale).astype(np.float64)
+    b = RB.reader_error_bound(q, ks, vs, depth, scale)
+    assert np.all(np.abs(o_bf - o_f32) <= b)
+    assert b.max() < 2e-2
+    if depth > 1:
+        o_short = O.attention(q, O.reconstruct(ks, depth), O.reconstruct(vs, depth - 1), scale).astype(np.float64)
+        assert np.any(np.abs(o_short - o_f32) > b)
 
 
 # ---------------------------------------------------------------- BF16 sink and tail segments

@@ -57,7 +57,8 @@ def check_workload(wl, sample=None, depths=(4,), full_recon=True):
                         assert np.array_equal(bf16_bits(rk), khat), f"K reconstruct req {i}"
                         assert np.array_equal(bf16_bits(rv), vhat), f"V reconstruct req {i}"
                 P.assert_attention_close(out[i], o_ref, f"req {i} depth {depth} algo {algo}")
-                P.assert_reader_error_bounded(out[i], khat, vhat, bf16_bits(wl.q[i]), scale, f"req {i} algo {algo}")
+                P.assert_reader_error_bounded(out[i], o_ref, ks, vs, khat, vhat, bf16_bits(wl.q[i]), depth, scale,
+                                              f"req {i} depth {depth} algo {algo}")
     return kc, vc
 
 
