@@ -77,25 +77,29 @@ cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream) {
 
 // ---------------------------------------------------------------- combine
 
-// Grid-stride over the (request, KV head) units. Most units need nothing: their
-// tile range lies inside one CTA's, which wrote the output directly; that is
-// decided from the tile prefix alone. A request with no tiles is read only to
-// tell a refused entry (NaN output) from one without packed tokens (zero output
-// and an empty softmax state).
+// Grid-stride over (request, KV head, query head) items. Most need nothing:
+// their unit's tile range lies inside one CTA's, which wrote the output
+// directly; that is decided from the tile prefix alone. A request with no
+// tiles is read only to tell a refused entry (NaN output) from one without
+// packed tokens (zero output and an empty softmax state). A split unit's
+// query heads are merged by separate blocks, each slot loop unrolled so that
+// the slots' loads overlap.
 __global__ void __launch_bounds__(kD) combine_kernel(AttnArgs a) {
   const int d = threadIdx.x;
   const int g = a.g;
   const long long W = a.prefix[a.n_requests];
   const int C = a.n_ctas;
-  for (int u = blockIdx.x; u < a.n_requests * a.H; u += gridDim.x) {
+  const long long items = (long long)a.n_requests * a.H * g;
+  for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+    const int u = int(it / g), i = int(it % g);
     const int b = u / a.H, h = u % a.H;
-    float* outp = a.out + ((long long)b * a.Hq + (long long)h * g) * kD;
-    float2* stats = a.stats + (long long)b * a.Hq + (long long)h * g;
+    float* outp = a.out + ((long long)b * a.Hq + (long long)h * g + i) * kD;
+    float2* stats = a.stats + (long long)b * a.Hq + (long long)h * g + i;
     const int p0 = a.prefix[b], p1 = a.prefix[b + 1];
     if (p1 <= p0) {
       const bool ok = attn_request_ok(a, a.reqs[b]);
-      for (int i = 0; i < g; ++i) outp[i * kD + d] = ok ? 0.0f : __int_as_float(0x7fc00000);
-      if (ok && d < g) stats[d] = make_float2(-INFINITY, 0.0f);  // no packed tokens: an empty softmax state
+      outp[d] = ok ? 0.0f : __int_as_float(0x7fc00000);
+      if (ok && d == 0) *stats = make_float2(-INFINITY, 0.0f);  // no packed tokens: an empty softmax state
       continue;
     }
     const int nt = (p1 - p0) / a.H;
@@ -103,25 +107,24 @@ __global__ void __launch_bounds__(kD) combine_kernel(AttnArgs a) {
     const long long e = s + nt;
     const int c_lo = cta_of(s, W, C), c_hi = cta_of(e - 1, W, C);
     if (c_lo == c_hi) continue;  // written directly by its only CTA
-    for (int i = 0; i < g; ++i) {
-      float M = -INFINITY;
-      for (int c = c_lo; c <= c_hi; ++c) {
-        if (cta_start(c, W, C) == cta_start(c + 1, W, C)) continue;  // empty range
-        const float* slot = a.partials + (size_t)(c + u) * kSlotFloats;
-        M = fmaxf(M, slot[i]);
-      }
-      float L = 0.0f, acc = 0.0f;
-      for (int c = c_lo; c <= c_hi; ++c) {
-        if (cta_start(c, W, C) == cta_start(c + 1, W, C)) continue;
-        const float* slot = a.partials + (size_t)(c + u) * kSlotFloats;
-        float m = slot[i];
-        float w = (m == -INFINITY) ? 0.0f : exp2f(m - M);
-        L += slot[kMaxG + i] * w;
-        acc += slot[2 * kMaxG + i * kD + d] * w;
-      }
-      outp[i * kD + d] = acc / L;
-      if (d == 0) stats[i] = make_float2(M, L);
+    float M = -INFINITY;
+#pragma unroll 4
+    for (int c = c_lo; c <= c_hi; ++c) {
+      if (cta_start(c, W, C) == cta_start(c + 1, W, C)) continue;  // empty range
+      M = fmaxf(M, a.partials[(size_t)(c + u) * kSlotFloats + i]);
     }
+    float L = 0.0f, acc = 0.0f;
+#pragma unroll 4
+    for (int c = c_lo; c <= c_hi; ++c) {
+      if (cta_start(c, W, C) == cta_start(c + 1, W, C)) continue;
+      const float* slot = a.partials + (size_t)(c + u) * kSlotFloats;
+      const float m = slot[i];
+      const float w = (m == -INFINITY) ? 0.0f : exp2f(m - M);
+      L += slot[kMaxG + i] * w;
+      acc += slot[2 * kMaxG + i * kD + d] * w;
+    }
+    outp[d] = acc / L;
+    if (d == 0) *stats = make_float2(M, L);
   }
 }
 
@@ -135,7 +138,9 @@ static int unit_grid(const AttnArgs& a) {
 
 cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
-  combine_kernel<<<unit_grid(a), kD, 0, stream>>>(a);
+  const long long items = (long long)a.n_requests * a.H * a.g;
+  const long long cap = 4LL * (a.n_ctas > 0 ? a.n_ctas : 1);
+  combine_kernel<<<int(items < cap ? items : cap), kD, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }
