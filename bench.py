@@ -5,8 +5,13 @@ One step = one pass of the whole path over one batch of synthetic requests:
 batched encode of the loop-1 base and the loop-2..4 residuals of K and V,
 batched reconstruction at depth 4 of K and V, and packed-KV GQA decode
 attention at depth 4. Inputs are resident in HBM before the timed region and
-larger than L2. The reported value is algorithmic bytes per second of the
-whole step (every phase's algorithmic bytes, divided by the step time).
+larger than L2. The reported value is the metric's first quantity: the packed
+decode attention's algorithmic bytes (chain payloads to the depth, q, output)
+per second of its phase inside the step; encode and reconstruction GB/s and
+the whole step's rate are reported beside it ("phases"). "e2e" is the same
+attention through the C ABI with the packed chains and q in pinned host memory
+(copied in every step) and the output read back. "configs" times the encode,
+reconstruction and attention of configurations 3, 4 and 5 on their own.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   (the CPU oracle timed on host cores)
@@ -48,6 +53,14 @@ WORKLOADS = {
 }
 
 
+CONFIG_DESCRIPTIONS = {
+    "cfg3": WORKLOADS["cfg3"][2],
+    "cfg4": WORKLOADS["cfg4"][2],
+    "cfg5": "24 layers x 64 requests, lengths uniform 512..16384 (not multiples of 64), H=8 x D=128, Hq=32, 4 loops, "
+            "per request dense or sparse 50%/25% late loops; contiguous per-request buffers and a device request table",
+}
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -55,11 +68,12 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="cfg2x512")
-    ap.add_argument("--algo", choices=["auto", "simt", "mma"], default="auto")
+    ap.add_argument("--algo", choices=["auto", "simt", "mma", "mma_general"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the extra timings (sparse decode, BF16 tail, tile-local K grouping)")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target wall time of the CPU-oracle sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the CPU-oracle sample")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration timings (configs 3, 4, 5)")
     return ap.parse_args(argv)
 
 
@@ -213,22 +227,34 @@ def rank_workload(cfg_idx: int, rank: int, replicate: int, device):
 # ------------------------------------------------------------------ CPU oracle
 
 
-def oracle_sample(reqs, q_rows, depth, scale, threads):
-    """Run the CPU oracle over `reqs` with `threads` host threads; returns seconds."""
+def oracle_attention_sample(reqs, q_rows, depth, scale, threads):
+    """The CPU oracle's packed decode attention over `reqs` with `threads` host
+    threads: the FP32 decode of the K and V chains at `depth`, then FP32
+    attention. The chains are encoded first, untimed. Returns seconds."""
     from oracle import oracle as O
     from quantized_cross_loop_gb300.workloads import bf16_bits
 
     import numpy as np
 
-    host = []
-    for req, q in zip(reqs, q_rows):
-        host.append(([bf16_bits(x) for x in req.xk], [bf16_bits(x) for x in req.xv],
-                     [None if a is None else a.cpu().numpy().astype(np.int32) for a in req.active], bf16_bits(q)))
+    def encode(i):
+        req = reqs[i]
+        act = [None if a is None else a.cpu().numpy().astype(np.int32) for a in req.active]
+        ks = O.encode_chain(O.KIND_K, [bf16_bits(x) for x in req.xk], act)
+        vs = O.encode_chain(O.KIND_V, [bf16_bits(x) for x in req.xv], act)
+        return ks, vs, bf16_bits(q_rows[i])
+
     O.lib()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        chains = list(ex.map(encode, range(len(reqs))))
     t0 = time.perf_counter()
     with ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(lambda h: O.request_path(h[0], h[1], h[2], h[3], depth, scale), host))
+        list(ex.map(lambda c: O.attention_f32(c[2], O.decode_f32(c[0], depth), O.decode_f32(c[1], depth), scale),
+                    chains))
     return time.perf_counter() - t0
+
+
+def attention_bytes(reqs, H, D, Hq, depth, payload):
+    return algorithmic_bytes(reqs, H, D, Hq, depth, payload)["attention"]
 
 
 # ------------------------------------------------------------------ main
@@ -278,7 +304,7 @@ def main():
     q = wl.q.contiguous()
     out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
     ws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(B, H, Hq, D), dtype=torch.uint8, device=dev)
-    algo = {"auto": kvq.ATTN_AUTO, "simt": kvq.ATTN_SIMT, "mma": kvq.ATTN_MMA}[args.algo]
+    algo = {"auto": kvq.ATTN_AUTO, "simt": kvq.ATTN_SIMT, "mma": kvq.ATTN_MMA, "mma_general": kvq.ATTN_MMA_GENERAL}[args.algo]
     stream = torch.cuda.current_stream()
 
     # K and V chains are independent: V runs on a second stream with its own
@@ -368,19 +394,24 @@ def main():
 
     ab = algorithmic_bytes(reqs, H, D, Hq, depth, lambda k, n, s: kvq.payload_bytes(k, n, H, D, s))
     step_bytes = ab["encode"] + ab["reconstruct"] + ab["attention"]
-    value = whole_job_gbs(world, step_bytes, ms_per_step)
+    att_ms_all = max_over_ranks(att_ms, dev)
+    value = whole_job_gbs(world, ab["attention"], att_ms_all)  # the metric's first quantity: packed decode attention
     peak, peak_kind = measured_peak()
     phase_ms = {"encode": enc_ms, "reconstruct": rec_ms, "attention": att_ms}
     phase_gbs = {k: ab[k] / (phase_ms[k] * 1e-3) / 1e9 for k in phase_ms}
 
-    # ---- end to end through the public API with host buffers
-    e2e = None
+    # ---- end to end through the public API with host buffers: the attention
+    # with the packed chains and q copied from host memory every step; beside
+    # it, the whole path with the BF16 sources copied in
+    e2e = e2e_whole = None
     if not args.no_e2e:
-        e2e = run_e2e(args, torch, kvq, src_all, src_chunks, q, out, step, stream, world, dev, step_bytes, dist)
+        e2e = run_e2e_attention(args, torch, kvq, pool, q, out, attend, stream, world, dev, ab["attention"], dist)
+        e2e_whole = run_e2e(args, torch, kvq, src_all, src_chunks, q, out, step, stream, world, dev, step_bytes, dist)
 
     # ---- roofline of the attention kernel call (plan + attention + combine)
     dominant = max(phase_ms, key=phase_ms.get)
-    att_key = {kvq.ATTN_AUTO: "attn_auto", kvq.ATTN_SIMT: "attn_simt", kvq.ATTN_MMA: "attn_mma"}[algo]
+    att_key = {kvq.ATTN_AUTO: "attn_auto", kvq.ATTN_SIMT: "attn_simt", kvq.ATTN_MMA: "attn_mma",
+               kvq.ATTN_MMA_GENERAL: "attn_mma_general"}[algo]
     tr = kernel_traffic(att_key)
     traffic = None
     if tr is not None and tr.get("workload") == args.workload:
@@ -395,6 +426,10 @@ def main():
     if not args.no_extras:
         extras = run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream,
                             (xk_ptrs, xv_ptrs, rk_ptrs, rv_ptrs, rk, rv, offs))
+
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = run_configs(torch, kvq, dev, stream, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -414,16 +449,19 @@ def main():
                        "arithmetic": "codec FP32 with BF16/FP16 rounding (bit-exact), attention FP32 accumulate",
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
                        "streams": "K chain on the launching stream, V chain on a second stream, joined per phase"},
-            "phases": {"encode_gbs": phase_gbs["encode"], "reconstruct_gbs": phase_gbs["reconstruct"],
+            "phases": {"whole_step_gbs": whole_job_gbs(world, step_bytes, ms_per_step),
+                       "encode_gbs": phase_gbs["encode"], "reconstruct_gbs": phase_gbs["reconstruct"],
                        "attention_gbs": phase_gbs["attention"], "encode_ms": enc_ms, "reconstruct_ms": rec_ms,
                        "attention_ms": att_ms, "attention_pct_of_measured_hbm": 100 * phase_gbs["attention"] / peak,
                        "attention_pct_of_8tbs": 100 * phase_gbs["attention"] / NOMINAL_HBM_GBS,
                        "attended_tokens_per_s": ab["tokens"] / (att_ms * 1e-3),
                        "encoded_tokens_per_s": ab["tokens"] / (enc_ms * 1e-3)},
             "roofline": roof,
+            "configs": configs,
             "extras": extras,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "e2e_whole_path": e2e_whole,
             "clocks": clk,
             "gpu_launches": launches,
         }
@@ -718,24 +756,152 @@ def run_e2e(args, torch, kvq, src_all, src_chunks, q, out, step, stream, world, 
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
 
 
+def run_e2e_attention(args, torch, kvq, pool, q, out, attend, stream, world, dev, att_bytes, dist):
+    """The headline metric end to end through the public API with host buffers:
+    every step copies the packed K/V chains (the pool's storage, one pinned
+    host buffer) and q from host memory, runs the packed decode attention and
+    reads the output back."""
+    host_pool = torch.empty(pool.storage.shape, dtype=torch.uint8, pin_memory=True).copy_(pool.storage)
+    host_q = torch.empty(q.shape, dtype=q.dtype, pin_memory=True).copy_(q)
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = host_pool.numel() + host_q.numel() * host_q.element_size()
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        pool.storage.copy_(host_pool, non_blocking=True)
+        q.copy_(host_q, non_blocking=True)
+        attend()
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 10)
+    if world > 1:
+        dist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / n, dev)
+    return {"value": whole_job_gbs(world, att_bytes, ms), "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "path": "pinned host packed chains + q -> kvq_decode_attn_packed -> pinned host output"}
+
+
+def phase_times(torch, kvq, wl, dev, stream, reps):
+    """Encode (every loop of K and V), reconstruction (K and V at full depth)
+    and packed decode attention of one workload resident on the device, on one
+    stream: mean ms per call of each phase over `reps` calls after one warm-up
+    call (the workload's data exceed L2). Returns (ms per phase, algorithmic
+    bytes, error word)."""
+    reqs = wl.requests
+    B, H, D, Hq, depth = wl.n_requests, wl.H, wl.D, wl.Hq, wl.depth
+    lengths = [r.T for r in reqs]
+    pool = kvq.PackedPool(lengths, [r.active for r in reqs], H, D, depth, dev)
+    xk_ptrs = [kvq.pointer_array([r.xk[j] for r in reqs], dev) for j in range(depth)]
+    xv_ptrs = [kvq.pointer_array([r.xv[j] for r in reqs], dev) for j in range(depth)]
+    offs = [0]
+    for t in lengths:
+        offs.append(offs[-1] + t)
+    rk = torch.empty((offs[-1], H, D), dtype=torch.bfloat16, device=dev)
+    rv = torch.empty_like(rk)
+    rk_ptrs = kvq.pointer_array([rk[offs[b]:offs[b + 1]] for b in range(B)], dev)
+    rv_ptrs = kvq.pointer_array([rv[offs[b]:offs[b + 1]] for b in range(B)], dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(B, H, Hq, D), dtype=torch.uint8, device=dev)
+
+    def enc():
+        for j in range(depth):
+            kvq.kvq_encode_batch(pool, kvq.KVQ_K, j, xk_ptrs[j], stream=stream)
+            kvq.kvq_encode_batch(pool, kvq.KVQ_V, j, xv_ptrs[j], stream=stream)
+
+    def rec():
+        kvq.kvq_reconstruct_batch(pool, kvq.KVQ_K, depth, rk_ptrs, stream=stream)
+        kvq.kvq_reconstruct_batch(pool, kvq.KVQ_V, depth, rv_ptrs, stream=stream)
+
+    def att():
+        kvq.kvq_decode_attn_packed(pool.table, wl.q, depth, H, out=out, workspace=ws)
+
+    ms = {}
+    for name, fn in (("encode", enc), ("reconstruct", rec), ("attention", att)):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms[name] = e0.elapsed_time(e1) / reps
+    err = kvq.attn_error_word(ws) | kvq.attn_error_word(pool.workspace)
+    ab = algorithmic_bytes(reqs, H, D, Hq, depth, lambda k, n, sp: kvq.payload_bytes(k, n, H, D, sp))
+    return ms, ab, err
+
+
+def run_configs(torch, kvq, dev, stream, peak):
+    """Encode, reconstruction and attention throughput of the other synthetic
+    configurations, each on its own (timed in this run): 32 x 4096
+    dense, 4 x 32768 sparse GQA 8, and the 24-layer ragged sweep (64 requests
+    per layer, generated, encoded, timed and freed layer by layer; bytes and
+    times summed over the layers)."""
+    from quantized_cross_loop_gb300 import workloads as W
+
+    res = {}
+    for name, idx, layers, reps in (("cfg3", 3, 1, 10), ("cfg4", 4, 1, 10), ("cfg5", 5, 24, 3)):
+        tot_ms = {"encode": 0.0, "reconstruct": 0.0, "attention": 0.0}
+        tot_b = {"encode": 0.0, "reconstruct": 0.0, "attention": 0.0, "tokens": 0}
+        err = 0
+        for layer in range(layers):
+            wl = W.make_workload(idx, device=dev, layer=layer)
+            ms, ab, e = phase_times(torch, kvq, wl, dev, stream, reps)
+            err |= e
+            for k in tot_ms:
+                tot_ms[k] += ms[k]
+            for k in tot_b:
+                tot_b[k] += ab[k]
+            spec = wl.spec
+            del wl
+            torch.cuda.empty_cache()
+        gbs = {k: tot_b[k] / (tot_ms[k] * 1e-3) / 1e9 for k in tot_ms}
+        res[name] = {
+            "description": CONFIG_DESCRIPTIONS[name], "layers": layers,
+            "requests_per_layer": spec.n_requests,
+            "attention_gbs": gbs["attention"], "attention_frac": gbs["attention"] / peak,
+            "attention_frac_of_8tbs": gbs["attention"] / NOMINAL_HBM_GBS, "attention_ms": tot_ms["attention"],
+            "attended_tokens_per_s": tot_b["tokens"] / (tot_ms["attention"] * 1e-3),
+            "encode_gbs": gbs["encode"], "encode_frac": gbs["encode"] / peak, "encode_ms": tot_ms["encode"],
+            "encoded_tokens_per_s": tot_b["tokens"] / (tot_ms["encode"] * 1e-3),
+            "reconstruct_gbs": gbs["reconstruct"], "reconstruct_frac": gbs["reconstruct"] / peak,
+            "reconstruct_ms": tot_ms["reconstruct"],
+            "reconstructed_tokens_per_s": tot_b["tokens"] / (tot_ms["reconstruct"] * 1e-3),
+            "algorithmic_bytes": {k: tot_b[k] for k in ("encode", "reconstruct", "attention")},
+            "timing": f"mean of {reps} calls per phase after one warm-up, one stream, data larger than L2",
+            "error_word": err}
+    return res
+
+
 def run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq):
-    """The CPU oracle as it stands, on the host cores, over a bounded sample of
-    the same requests; same metric and unit."""
+    """The CPU oracle's packed decode attention as it stands, on the host cores,
+    over a bounded sample of the same requests; same metric and unit."""
     cores = os.cpu_count() or 1
     scale = 1.0 / math.sqrt(D)
-    t1 = oracle_sample(reqs[:1], q[:1], depth, scale, 1)
+    t1 = oracle_attention_sample(reqs[:1], q[:1], depth, scale, 1)
     n = max(1, min(len(reqs), int(args.cpu_seconds * cores / max(t1, 1e-3))))
     sample = reqs[:n]
-    secs = oracle_sample(sample, q[:n], depth, scale, cores)
+    secs = oracle_attention_sample(sample, q[:n], depth, scale, cores)
+
     def bytes_of(rs):
-        ab = algorithmic_bytes(rs, H, D, Hq, depth, lambda k, nn, s: kvq.payload_bytes(k, nn, H, D, s))
-        return ab["encode"] + ab["reconstruct"] + ab["attention"]
+        return attention_bytes(rs, H, D, Hq, depth, lambda k, nn, s: kvq.payload_bytes(k, nn, H, D, s))
 
     return {"value": bytes_of(sample) / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "value_1_thread": bytes_of(reqs[:1]) / t1 / 1e9, "cpu_model": cpu_model(),
-            "sample": f"{n} of {len(reqs)} requests of the same workload, whole path (encode K/V 4 loops, "
-                      f"reconstruct, FP32 attention), {secs:.1f} s on {cores} threads; value_1_thread: one "
-                      f"request on one thread, {t1:.2f} s"}
+            "sample": f"{n} of {len(reqs)} requests of the same workload: packed decode attention at depth {depth} "
+                      f"(FP32 decode of the K/V chains, FP32 attention; chains encoded beforehand, untimed), "
+                      f"{secs:.2f} s on {cores} threads; value_1_thread: one request on one thread, {t1:.3f} s"}
 
 
 def cpu_model():
@@ -765,15 +931,16 @@ def cpu_model():
 
 
 def run_reference(args, world, rank, cfg_idx, replicate, desc):
-    """--impl reference: the CPU oracle timed on the host cores, each step a
-    bounded sample of the same workload (rank 0 only under torchrun)."""
+    """--impl reference: the CPU oracle's packed decode attention timed on the
+    host cores, each step a bounded sample of the same workload (rank 0 only
+    under torchrun)."""
     if world > 1 and rank != 0:
         return
     from quantized_cross_loop_gb300 import workloads as W
 
     cores = os.cpu_count() or 1
     spec = W.CONFIGS[cfg_idx]
-    n = min(cores, spec.n_requests * replicate)
+    n = min(4 * cores, spec.n_requests * replicate)
     if replicate > 1:
         wl = W.make_workload(cfg_idx, device="cpu", replicate=math.ceil(n / spec.n_requests))
     else:
@@ -789,13 +956,13 @@ def run_reference(args, world, rank, cfg_idx, replicate, desc):
         return O.stream_bytes(kind, nn, H, D, sparse=sparse)
 
     for _ in range(args.warmup):
-        oracle_sample(reqs[:1], q[:1], depth, scale, 1)
-    times = [oracle_sample(reqs, q, depth, scale, cores) for _ in range(args.steps)]
-    ab = algorithmic_bytes(reqs, H, D, Hq, depth, payload)
-    tot = ab["encode"] + ab["reconstruct"] + ab["attention"]
+        oracle_attention_sample(reqs[:1], q[:1], depth, scale, 1)
+    times = [oracle_attention_sample(reqs, q, depth, scale, cores) for _ in range(args.steps)]
+    tot = attention_bytes(reqs, H, D, Hq, depth, payload)
     ms = 1e3 * sum(times) / len(times)
     value = tot / (ms * 1e-3) / 1e9
-    sample = f"{n} requests of {args.workload} per step (whole path) on {cores} threads"
+    sample = (f"{n} requests of {args.workload} per step: packed decode attention at depth {depth} (FP32 decode "
+              f"of the chains, FP32 attention; chains encoded beforehand, untimed) on {cores} threads")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

@@ -360,7 +360,10 @@ size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_head
 
 #define KVQ_ATTN_AUTO 0 /* tensor-core kernel for depth <= 4, CUDA-core kernel beyond */
 #define KVQ_ATTN_SIMT 1 /* CUDA-core kernel: FP32 decode of the chain per element, FP32 dot products */
-#define KVQ_ATTN_MMA 2  /* tensor-core kernel (depth <= 4): unpack + folded dequant into m16n8k16 MMAs */
+#define KVQ_ATTN_MMA 2  /* tensor-core kernel (depth <= 4): INT4 tables run the subnormal-code kernel (Q' and the
+                           K-min terms built once per tile); NVFP4 tables (with KVQ_ATTN_NVFP4) run the general one */
+#define KVQ_ATTN_MMA_GENERAL 3 /* the general tensor-core kernel (depth <= 4) for every table: codes as FP16 64 + c,
+                                 Q' rebuilt per warp; the form the NVFP4 and sparse-decode paths use */
 #define KVQ_ATTN_NVFP4 8 /* OR-ed into algo: the table may hold NVFP4 residual loops. Without it the
                            tensor-core kernel refuses such a request (NaN output, error bit 64); the
                            CUDA-core kernel reads either format. kvq_decode_attn_packed and the

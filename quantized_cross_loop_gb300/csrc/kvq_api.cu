@@ -784,7 +784,9 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   if (!(softmax_scale > 0.0f) || softmax_scale > 1e30f) return fail(KVQ_ERR_BAD_ARG, "softmax_scale");
   const bool nvfp4_hint = (algo & KVQ_ATTN_NVFP4) != 0;
   algo &= ~KVQ_ATTN_NVFP4;
-  if (algo < KVQ_ATTN_AUTO || algo > KVQ_ATTN_MMA) return fail(KVQ_ERR_BAD_ARG, "algo %d", algo);
+  if (algo < KVQ_ATTN_AUTO || algo > KVQ_ATTN_MMA_GENERAL) return fail(KVQ_ERR_BAD_ARG, "algo %d", algo);
+  const bool general = algo == KVQ_ATTN_MMA_GENERAL;
+  if (general) algo = KVQ_ATTN_MMA;
   if (n_requests == 0) return ok();
   if (!reqs || !q || !out) return fail(KVQ_ERR_BAD_ARG, "NULL reqs, q or out");
   if (!aligned16(reqs) || !aligned16(q) || !aligned16(out))
@@ -804,6 +806,7 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   AttnArgs a;
   attention_args(a, reqs, n_requests, n_heads, n_q_heads, depth, q, softmax_scale, out, static_cast<char*>(workspace),
                  algo, nvfp4_hint, dev, sms);
+  a.general = general ? 1 : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   e = cudaMemsetAsync(a.err, 0, 16, s);
   if (e != cudaSuccess) return cuda_status(e, "clear error word");

@@ -45,6 +45,10 @@ struct AttnArgs {
   // units) of key t < logit_stride to logits[(b * Hq + query head) * logit_stride + t]
   float* logits;
   int32_t logit_stride;
+  // tensor-core calls: 1 runs the general kernel (NVFP4 forms, sparse-decode
+  // masks and logits); 0 runs the INT4 kernel of kvq_attn_tc.cu when the call
+  // has neither NVFP4 loops, masks nor logits
+  int32_t general;
 };
 
 // Workspace layout: [0,16) error word (int32 0) and plan flags (int32 1); then int32 prefix[B+1] (rounded to 16 B);
@@ -130,6 +134,7 @@ cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_segments(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream);
 int attn_ctas(int algo, int device);
 
 }  // namespace kvq

@@ -19,7 +19,7 @@ from tests import pathrun as P
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = [kvq.ATTN_SIMT, kvq.ATTN_MMA]
+ALGOS = [kvq.ATTN_SIMT, kvq.ATTN_MMA, kvq.ATTN_MMA_GENERAL]
 H, D = 8, 128
 
 
