@@ -807,9 +807,8 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   attention_args(a, reqs, n_requests, n_heads, n_q_heads, depth, q, softmax_scale, out, static_cast<char*>(workspace),
                  algo, nvfp4_hint, dev, sms);
   a.general = general ? 1 : 0;
+  a.clear_err = 1;  // the plan kernel clears the error word and flags first
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  e = cudaMemsetAsync(a.err, 0, 16, s);
-  if (e != cudaSuccess) return cuda_status(e, "clear error word");
   return attention_launches(a, algo, true, s);
 }
 

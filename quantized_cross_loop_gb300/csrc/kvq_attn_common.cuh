@@ -11,6 +11,8 @@
 // contiguous), and the combine kernel merges the partials of the unit.
 #pragma once
 
+#include <utility>
+
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -49,7 +51,34 @@ struct AttnArgs {
   // masks and logits); 0 runs the INT4 kernel of kvq_attn_tc.cu when the call
   // has neither NVFP4 loops, masks nor logits
   int32_t general;
+  // 1: the plan kernel clears the error word and the plan flags before its
+  // checks (the call's first launch; no separate memset)
+  int32_t clear_err;
 };
+
+// Programmatic dependent launches: a kernel launched with launch_dependent()
+// may start while its predecessor in the stream finishes; it calls
+// wait_prior_grid() before touching anything the predecessor writes (the wait
+// returns once the predecessor grid has completed and its memory is visible;
+// it does nothing in a kernel launched the ordinary way).
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... P, typename... A>
+inline cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                    A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // Workspace layout: [0,16) error word (int32 0) and plan flags (int32 1); then int32 prefix[B+1] (rounded to 16 B);
 // then (n_ctas + B*H) partial slots of kSlotFloats floats; then float2

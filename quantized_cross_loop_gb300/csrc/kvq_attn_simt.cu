@@ -20,9 +20,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a) {
   __shared__ long long s_carry;
   __shared__ int s_warp[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  allow_dependents();  // the attention kernel may start its prologue; it waits for this grid before reading the plan
   if (threadIdx.x == 0) {
     s_carry = 0;
     a.prefix[0] = 0;
+    if (a.clear_err) {
+      *a.err = 0;
+      *a.flags = 0;
+    }
   }
   __syncthreads();
   for (int base = 0; base < a.n_requests; base += blockDim.x) {
@@ -85,6 +90,8 @@ cudaError_t launch_plan(const AttnArgs& a, cudaStream_t stream) {
 // query heads are merged by separate blocks, each slot loop unrolled so that
 // the slots' loads overlap.
 __global__ void __launch_bounds__(kD) combine_kernel(AttnArgs a) {
+  wait_prior_grid();
+  allow_dependents();
   const int d = threadIdx.x;
   const int g = a.g;
   const long long W = a.prefix[a.n_requests];
@@ -140,9 +147,9 @@ cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
   const long long items = (long long)a.n_requests * a.H * a.g;
   const long long cap = 4LL * (a.n_ctas > 0 ? a.n_ctas : 1);
-  combine_kernel<<<int(items < cap ? items : cap), kD, 0, stream>>>(a);
+  cudaError_t e = launch_dependent(combine_kernel, dim3(unsigned(items < cap ? items : cap)), dim3(kD), 0, stream, a);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 // ---------------------------------------------------------------- BF16 segments
@@ -159,6 +166,7 @@ constexpr float kSegLog2e = 1.4426950408889634f;
 // Grid-stride over the (request, KV head) units; the whole grid leaves at once
 // when the plan saw no request with segments.
 __global__ void __launch_bounds__(32 * kSegWarps) segment_kernel(AttnArgs a) {
+  wait_prior_grid();
   if (!(*a.flags & 1)) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = a.g;
@@ -246,9 +254,9 @@ __global__ void __launch_bounds__(32 * kSegWarps) segment_kernel(AttnArgs a) {
 
 cudaError_t launch_segments(const AttnArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
-  segment_kernel<<<unit_grid(a), 32 * kSegWarps, 0, stream>>>(a);
+  cudaError_t e = launch_dependent(segment_kernel, dim3(unit_grid(a)), dim3(32 * kSegWarps), 0, stream, a);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 // ---------------------------------------------------------------- CUDA-core attention

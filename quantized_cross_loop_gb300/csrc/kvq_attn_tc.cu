@@ -55,7 +55,8 @@ constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kStagesPerGroup = 2;
 constexpr int kStages = kGroups * kStagesPerGroup;
 constexpr int kConsumers = kGroups * kGroupThreads;
-constexpr int kThreads = kConsumers + kGroups * 32;  // + one producer warp per group
+constexpr int kProducers = 2;                         // producer warps per group: one per stage
+constexpr int kThreads = kConsumers + kGroups * kProducers * 32;
 constexpr int kMaxPairs = 1 + 2 * (kLoops - 1);      // (loop, K group) pairs of a tile: loop 1 is dense
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitNs = 2000000000LL;  // bounded waits: 2 s, then flag and leave
@@ -130,12 +131,16 @@ __device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// A waiting thread is suspended for at most kSuspendNs per try (the default,
+// system-dependent limit let a waiter sleep well past the phase completion).
+constexpr uint32_t kSuspendNs = 200;
+
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -182,25 +187,34 @@ __device__ __forceinline__ __half2 u2h(uint32_t v) { return *reinterpret_cast<__
 
 // ---------------------------------------------------------------- producer
 //
-// The group's producer warp stages each tile with one bulk copy per lane: lane
-// 8 j + c moves plane c of loop j (c = 0 K codes, 1 V codes, 2 K mins, 3 K
-// scales, 4 V mins, 5 V scales, 6 the sparse index slice), so a tile's copies
-// leave together instead of one after another. Lane 0 adds the warp's total
-// to the stage's expected transaction count before the copies start and
-// arrives once the metadata is written; the phase completes when every copy
-// has delivered its bytes.
+// A group's two producer warps take alternate tiles (warp p fills stage p of
+// the group's two), so that one warp's copy set-up overlaps the other's. A
+// producer warp stages a tile in two ways. The K and V code blocks
+// (up to 4 KB per loop each) go by 1-D bulk copy, one per lane (lane 8 j + c,
+// c = 0 K, 1 V, of loop j); every bulk copy costs the copy engine a fixed
+// time whatever its size, so the small planes - the K min and scale rows of
+// the tile's groups, its V min and scale rows and a sparse loop's index slice,
+// a few hundred bytes each - go instead as 16-byte asynchronous copies spread
+// over the lanes of the loop. Lane 0 adds the bulk copies' bytes to the
+// stage's expected transaction count before they start; every lane then
+// makes the barrier wait for its 16-byte copies; lane 0 arrives once the
+// metadata is written.
+
+__device__ __forceinline__ void copy16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
 
 template <int DEPTH>
-__device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long long e0, int lane) {
-  const int j = lane >> 3, c = lane & 7;  // this lane's loop and plane
-  const bool jl = j < DEPTH && c < 7;
+__device__ void producer(const AttnArgs& a, Smem& S, int grp, int pw, long long s0, long long e0, int lane) {
+  const int j = lane >> 3, c = lane & 7;  // this lane's loop and slot within it
   int b = request_of(a.prefix, a.n_requests, s0);
   long long us = 0, ue = -1;  // current unit's tile range
   int h = 0, T = 0, unit = -1, nsink = 0;
   int nr = 0, kgr = 0, rs = 0, gs = 0;  // this lane's loop: stored rows, tile K groups, plane strides
   const int32_t* act = nullptr;
   const int32_t* dir = nullptr;
-  const uint8_t* src = nullptr;  // the plane this lane copies
+  const uint8_t* codes = nullptr;  // the code plane this lane copies (c < 2)
+  const uint8_t *kmn = nullptr, *ksc = nullptr, *vmn = nullptr, *vsc = nullptr;
   long long it = 0;
   for (long long x = s0; x < e0; ++x, ++it) {
     if (x >= ue) {  // next unit: request b (skipping empty ones) and KV head h
@@ -222,17 +236,15 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
         gs = L.kgroup_cap > 0 ? L.kgroup_cap : (kgr > 0 ? kgr : (L.n_rows + kG - 1) / kG);
         act = L.active_idx;
         dir = L.tile_dir;
-        const void* pl = c == 0 ? (const void*)L.k_codes
-                         : c == 1 ? (const void*)L.v_codes
-                         : c == 2 ? (const void*)L.k_mins
-                         : c == 3 ? (const void*)L.k_scales
-                         : c == 4 ? (const void*)L.v_mins
-                         : c == 5 ? (const void*)L.v_scales
-                         : c == 6 ? (const void*)L.active_idx
-                                  : nullptr;
-        src = static_cast<const uint8_t*>(pl);
+        codes = c == 0 ? L.k_codes : L.v_codes;
+        kmn = reinterpret_cast<const uint8_t*>(L.k_mins);
+        ksc = reinterpret_cast<const uint8_t*>(L.k_scales);
+        vmn = reinterpret_cast<const uint8_t*>(L.v_mins);
+        vsc = reinterpret_cast<const uint8_t*>(L.v_scales);
       }
     }
+    // the group's two producer warps take alternate tiles: warp pw fills stage pw
+    if (int(it & 1) != pw) continue;
     const int k = int(x - us);
     // directory entries first: their latency overlaps the wait for a free stage
     int c0 = 0, c1 = 0;
@@ -280,47 +292,54 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       ngrp = 0;
       np = 0;
     }
+    const bool live = j < DEPTH && ngrp > 0;
     const long long hr = (long long)h * rs + c0;  // first stored row of this head
-    uint32_t bytes = 0;
-    const void* from = nullptr;
-    void* to = nullptr;
-    int rem = 0;
-    if (jl && ngrp > 0) {
-      LoopStage& LS = st.l[j];
-      if (c < 2) {  // codes
-        from = src + hr * kRowBytes;
-        to = c == 0 ? (void*)LS.kc : (void*)LS.vc;
-        bytes = uint32_t(n * kRowBytes);
-      } else if (c < 4) {  // K params of the tile's groups
-        from = src + ((long long)h * gs + g0) * kD * 2;
-        to = c == 2 ? (void*)LS.kmin : (void*)LS.ksc;
-        bytes = uint32_t(ngrp * kD * 2);
-      } else if (c < 6) {  // V params: 4 B per row and plane, moved in whole 16-byte units
-        const long long off = hr * 4;
-        const long long lo = off & ~15LL;
-        from = src + lo;
-        to = c == 4 ? (void*)LS.vmin : (void*)LS.vsc;
-        bytes = uint32_t(((off + (long long)n * 4 + 15) & ~15LL) - lo);
-        rem = int((off - lo) / 2);
-      } else if (act != nullptr) {  // the index slice
-        const long long off = (long long)c0 * 4;
-        const long long lo = off & ~15LL;
-        from = src + lo;
-        to = (void*)LS.idx;
-        bytes = uint32_t(((off + (long long)n * 4 + 15) & ~15LL) - lo);
-        rem = int((off - lo) / 4);
-      }
-    }
+    // bulk copies of the code blocks
+    const uint32_t bytes = (live && c < 2) ? uint32_t(n * kRowBytes) : 0u;
     uint32_t total = bytes;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
     if (lane == 0) mbar_expect_tx(&S.full[s], total);
     __syncwarp();
-    if (bytes > 0)
+    if (bytes > 0) {
+      LoopStage& LS = st.l[j];
       asm volatile(
-          "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(to)),
-          "l"(from), "r"(bytes), "r"(smem_addr(&S.full[s]))
+          "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              smem_addr(c == 0 ? (void*)LS.kc : (void*)LS.vc)),
+          "l"(codes + hr * kRowBytes), "r"(bytes), "r"(smem_addr(&S.full[s]))
           : "memory");
+    }
+    // 16-byte copies of the small planes: K min and scale rows of the tile's groups (256 B per
+    // group each), V min and scale rows (4 B per row each, in whole 16-byte units), index slice
+    int vrem = 0, irem = 0;
+    if (live) {
+      LoopStage& LS = st.l[j];
+      const long long kb = ((long long)h * gs + g0) * kD * 2;
+      const int nk = ngrp * (kD * 2 / 16);
+      const long long voff = hr * 4, vlo = voff & ~15LL;
+      const int nv = int((((voff + (long long)n * 4 + 15) & ~15LL) - vlo) / 16);
+      vrem = int((voff - vlo) / 2);
+      const long long ioff = (long long)c0 * 4, ilo = ioff & ~15LL;
+      const int ni = act != nullptr ? int((((ioff + (long long)n * 4 + 15) & ~15LL) - ilo) / 16) : 0;
+      irem = int((ioff - ilo) / 4);
+      const int ntot = 2 * nk + 2 * nv + ni;
+      for (int t = c; t < ntot; t += 8) {
+        if (t < nk) {
+          copy16(reinterpret_cast<uint8_t*>(LS.kmin) + 16 * t, kmn + kb + 16 * t);
+        } else if (t < 2 * nk) {
+          copy16(reinterpret_cast<uint8_t*>(LS.ksc) + 16 * (t - nk), ksc + kb + 16 * (t - nk));
+        } else if (t < 2 * nk + nv) {
+          copy16(reinterpret_cast<uint8_t*>(LS.vmin) + 16 * (t - 2 * nk), vmn + vlo + 16 * (t - 2 * nk));
+        } else if (t < 2 * nk + 2 * nv) {
+          copy16(reinterpret_cast<uint8_t*>(LS.vsc) + 16 * (t - 2 * nk - nv), vsc + vlo + 16 * (t - 2 * nk - nv));
+        } else {
+          copy16(reinterpret_cast<uint8_t*>(LS.idx) + 16 * (t - 2 * nk - 2 * nv),
+                 reinterpret_cast<const uint8_t*>(act) + ilo + 16 * (t - 2 * nk - 2 * nv));
+        }
+      }
+    }
+    // the stage's phase also waits for this lane's 16-byte copies
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(&S.full[s])) : "memory");
     // metadata
     if (lane == 0) {
       M[0] = unit;
@@ -339,13 +358,11 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
         LM[1] = kt ? k * kG : c0;
         LM[2] = g0;
         LM[3] = ngrp;
+        LM[4] = vrem;
+        LM[5] = irem;
         LM[6] = act != nullptr;
         LM[7] = pbase;
         if (bad) atomicOr(a.err, 4);
-      } else if (c == 4) {
-        LM[4] = rem;
-      } else if (c == 6) {
-        LM[5] = rem;
       } else if (c == 1 || c == 2) {
         if (c - 1 < ngrp) M[8 + pbase + c - 1] = (j << 1) | (c - 1);
       }
@@ -550,6 +567,10 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
   const int gq = a.g;
   const float lsc = a.scale * kLog2e * 16777216.0f;  // the logits carry 2^-24
   GroupSmem& Gs = S.grp[grp];
+  const uint32_t lowA = (1u << g) - 1u, lowC = (1u << (g + 8)) - 1u;  // slice tokens before g, g + 8
+  uint32_t lowP[4];  // slice tokens before 2q, 2q + 1, 2q + 8, 2q + 9
+#pragma unroll
+  for (int k = 0; k < 4; ++k) lowP[k] = (1u << (2 * q + (k & 1) + 8 * (k >> 1))) - 1u;
   UnitState U;
   int cur_unit = -1;
   UnitInfo Mprev = {-1, 0, 0, 0};
@@ -624,12 +645,11 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       pbits[j] = bits;
       prb[j] = rb;
       if (bits == 0) continue;
+      // stored rows of tokens g and g + 8: the first row of the warp's slice plus the token's rank
+      // among the slice's stored tokens (a dense slice stores them all, so the rank is the token);
+      // an absent token gets a row index <= 64, inside the stage, whose codes its zero A row ignores
       const bool pa = (bits >> g) & 1, pc = (bits >> (g + 8)) & 1;
-      int ra = 16 * w + g, rc = ra + 8;  // dense loops: the token's own row
-      if (sparse) {
-        ra = min(rb + __popc(bits & ((1u << g) - 1u)), KVQ_TILE - 1);
-        rc = min(rb + __popc(bits & ((1u << (g + 8)) - 1u)), KVQ_TILE - 1);
-      }
+      const int ra = rb + __popc(bits & lowA), rc = rb + __popc(bits & lowC);
       const uint4 wa = *reinterpret_cast<const uint4*>(&st.l[j].kc[ra * kRowBytes + 16 * q]);
       const uint4 wb = *reinterpret_cast<const uint4*>(&st.l[j].kc[rc * kRowBytes + 16 * q]);
       const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w}, wB[4] = {wb.x, wb.y, wb.z, wb.w};
@@ -642,8 +662,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         sa = ((c0 + ra) >> 6) - g0;
         sc = ((c0 + rc) >> 6) - g0;
       }
-#pragma unroll 1
-      for (int G = ga; G <= gb; ++G) {
+      auto pass = [&](int G) {
         const bool ka = pa && sa == G, kc = pc && sc == G;
         const uint32_t la_ = ka ? kLoMask : 0u, ha_ = ka ? kHiMask : 0u;
         const uint32_t lc_ = kc ? kLoMask : 0u, hc_ = kc ? kHiMask : 0u;
@@ -668,7 +687,9 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
           const uint32_t kb0 = q == 0 ? uint32_t(Gs.kb[pair][e][g]) : 0u;
           mma16816(C[e][0], kA, kC, 0u, 0u, kb0, 0u);
         }
-      }
+      };
+      pass(ga);
+      if (gb != ga) pass(gb);
     }
 
     // ---- logits in log2 units, this warp's max per head, online softmax
@@ -718,13 +739,8 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       if (bits == 0) continue;
       const int rb = prb[j];
       const int vrem = st.meta[16 + 8 * j + 4];
-      const bool sparse = st.meta[16 + 8 * j + 6] != 0;
       const bool pa = (bits >> g) & 1, pc = (bits >> (g + 8)) & 1;
-      int ra = 16 * w + g, rc = ra + 8;  // dense loops: the token's own row
-      if (sparse) {
-        ra = min(rb + __popc(bits & ((1u << g) - 1u)), KVQ_TILE - 1);
-        rc = min(rb + __popc(bits & ((1u << (g + 8)) - 1u)), KVQ_TILE - 1);
-      }
+      const int ra = rb + __popc(bits & lowA), rc = rb + __popc(bits & lowC);
       // V params of tokens g, g + 8 ({group 0, group 1} pairs), P' = RN16(p * sV) and the V-min
       // terms (a token without a stored row reads nothing: its staged slot may hold stale bits)
       const uint32_t sva = pa ? *reinterpret_cast<const uint32_t*>(&st.l[j].vsc[vrem + 2 * ra]) : 0u;
@@ -744,10 +760,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       const uint8_t* vbase = &st.l[j].vc[0];
       int ro[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int t = 2 * q + (k & 1) + 8 * (k >> 1);
-        ro[k] = (sparse ? min(rb + __popc(bits & ((1u << t) - 1u)), KVQ_TILE - 1) : 16 * w + t) * kRowBytes;
-      }
+      for (int k = 0; k < 4; ++k) ro[k] = (rb + __popc(bits & lowP[k])) * kRowBytes;
       if (G8) {
         // B per V group: columns 2q, 2q + 1 = heads q, q + 4; thread g takes word 8 vg + g of each
         // row (channels 64 vg + 8 g .. + 7); m-tile (vg, e) has rows 8g + 2e and 8g + 2e + 1
@@ -818,7 +831,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int C = a.n_ctas;  // virtual CTAs: two per block
-  const long long W = a.prefix[a.n_requests];
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&S.full[i], 1);
@@ -830,20 +842,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   for (int i = threadIdx.x; i < int(sizeof(GroupSmem) * kGroups / 16); i += kThreads)
     reinterpret_cast<uint4*>(S.grp)[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
-  int grp;
+  wait_prior_grid();  // the plan (tile prefix, error word) is complete and visible from here on
+  const long long W = a.prefix[a.n_requests];
+  int grp, pw = 0;
   bool producer_warp;
   if (threadIdx.x < kConsumers) {
     grp = threadIdx.x / kGroupThreads;
     producer_warp = false;
   } else {
-    grp = (threadIdx.x - kConsumers) >> 5;
+    const int pwarp = (threadIdx.x - kConsumers) >> 5;
+    grp = pwarp / kProducers;
+    pw = pwarp % kProducers;
     producer_warp = true;
   }
   const int vcta = kGroups * blockIdx.x + grp;
   const long long s0 = cta_start(vcta, W, C), e0 = cta_start(vcta + 1, W, C);
   if (s0 >= e0) return;
   if (producer_warp) {
-    producer<DEPTH>(a, S, grp, s0, e0, threadIdx.x & 31);
+    producer<DEPTH>(a, S, grp, pw, s0, e0, threadIdx.x & 31);
     return;
   }
   consumer<DEPTH, G8>(a, S, grp, vcta, s0, e0);
@@ -858,8 +874,7 @@ cudaError_t launch_depth(const AttnArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attn_tc_kernel<DEPTH, G8><<<a.n_ctas / kGroups, kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(attn_tc_kernel<DEPTH, G8>, dim3(a.n_ctas / kGroups), dim3(kThreads), size_t(smem), stream, a);
 }
 
 }  // namespace tc_attn
