@@ -68,7 +68,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="cfg2x512")
-    ap.add_argument("--algo", choices=["auto", "simt", "mma", "mma_general"], default="auto")
+    ap.add_argument("--algo", choices=["auto", "simt", "mma", "mma_general", "tcgen05"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the extra timings (sparse decode, BF16 tail, tile-local K grouping)")
@@ -304,7 +304,8 @@ def main():
     q = wl.q.contiguous()
     out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
     ws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(B, H, Hq, D), dtype=torch.uint8, device=dev)
-    algo = {"auto": kvq.ATTN_AUTO, "simt": kvq.ATTN_SIMT, "mma": kvq.ATTN_MMA, "mma_general": kvq.ATTN_MMA_GENERAL}[args.algo]
+    algo = {"auto": kvq.ATTN_AUTO, "simt": kvq.ATTN_SIMT, "mma": kvq.ATTN_MMA, "mma_general": kvq.ATTN_MMA_GENERAL,
+            "tcgen05": kvq.ATTN_TCGEN05}[args.algo]
     stream = torch.cuda.current_stream()
 
     # K and V chains are independent: V runs on a second stream with its own
@@ -411,7 +412,7 @@ def main():
     # ---- roofline of the attention kernel call (plan + attention + combine)
     dominant = max(phase_ms, key=phase_ms.get)
     att_key = {kvq.ATTN_AUTO: "attn_auto", kvq.ATTN_SIMT: "attn_simt", kvq.ATTN_MMA: "attn_mma",
-               kvq.ATTN_MMA_GENERAL: "attn_mma_general"}[algo]
+               kvq.ATTN_MMA_GENERAL: "attn_mma_general", kvq.ATTN_TCGEN05: "attn_tcgen05"}[algo]
     tr = kernel_traffic(att_key)
     traffic = None
     if tr is not None and tr.get("workload") == args.workload:

@@ -45,7 +45,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="cfg3")
     ap.add_argument("--stage", choices=["encode", "reconstruct", "attention", "sparse", "tail"], default="attention")
-    ap.add_argument("--algo", choices=["auto", "simt", "mma", "mma_general"], default="auto")
+    ap.add_argument("--algo", choices=["auto", "simt", "mma", "mma_general", "tcgen05"], default="auto")
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--kgroup", choices=["compact", "tile"], default="compact")
     ap.add_argument("--residual", choices=["int4", "nvfp4"], default="int4")
@@ -75,7 +75,7 @@ def main():
                 kvq.kvq_reconstruct_batch(pool, kind, wl.depth, ptrs[kind])
     elif args.stage == "attention":
         algo = {"auto": kvq.ATTN_AUTO, "simt": kvq.ATTN_SIMT, "mma": kvq.ATTN_MMA,
-                "mma_general": kvq.ATTN_MMA_GENERAL}[args.algo]
+                "mma_general": kvq.ATTN_MMA_GENERAL, "tcgen05": kvq.ATTN_TCGEN05}[args.algo]
         q = wl.q
         out = torch.empty(q.shape, dtype=torch.float32, device=dev)
         ws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(q.shape[0], wl.H, wl.Hq, wl.D), dtype=torch.uint8,

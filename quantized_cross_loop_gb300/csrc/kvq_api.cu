@@ -755,7 +755,11 @@ static void attention_args(AttnArgs& a, const kvq_request* reqs, int n_requests,
 
 // Plan, attention, split-unit merge and (when asked) the BF16 segments, on a
 // cleared error word.
-static kvq_status attention_launches(const AttnArgs& a, int algo, bool segments, cudaStream_t s) {
+static kvq_status attention_launches(const AttnArgs& a0, int algo, bool segments, cudaStream_t s) {
+  AttnArgs a = a0;
+  // the tcgen05 kernel runs one CTA of the work split per block, one block per SM
+  // (attn_ctas counts two per SM for the tensor-core kernels)
+  if (runs_tcgen05(a, algo == KVQ_ATTN_MMA)) a.n_ctas = a0.n_ctas / 2;
   cudaError_t e = launch_plan(a, s);
   if (e != cudaSuccess) return cuda_status(e, "plan launch");
   e = (algo == KVQ_ATTN_SIMT) ? launch_attn_simt(a, s) : launch_attn_mma(a, s);
@@ -784,9 +788,10 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   if (!(softmax_scale > 0.0f) || softmax_scale > 1e30f) return fail(KVQ_ERR_BAD_ARG, "softmax_scale");
   const bool nvfp4_hint = (algo & KVQ_ATTN_NVFP4) != 0;
   algo &= ~KVQ_ATTN_NVFP4;
-  if (algo < KVQ_ATTN_AUTO || algo > KVQ_ATTN_MMA_GENERAL) return fail(KVQ_ERR_BAD_ARG, "algo %d", algo);
+  if (algo < KVQ_ATTN_AUTO || algo > KVQ_ATTN_TCGEN05) return fail(KVQ_ERR_BAD_ARG, "algo %d", algo);
   const bool general = algo == KVQ_ATTN_MMA_GENERAL;
-  if (general) algo = KVQ_ATTN_MMA;
+  const bool tcgen05 = algo == KVQ_ATTN_TCGEN05;
+  if (general || tcgen05) algo = KVQ_ATTN_MMA;
   if (n_requests == 0) return ok();
   if (!reqs || !q || !out) return fail(KVQ_ERR_BAD_ARG, "NULL reqs, q or out");
   if (!aligned16(reqs) || !aligned16(q) || !aligned16(out))
@@ -807,6 +812,7 @@ kvq_status kvq_decode_attn_packed_ex(const kvq_request* reqs, int n_requests, in
   attention_args(a, reqs, n_requests, n_heads, n_q_heads, depth, q, softmax_scale, out, static_cast<char*>(workspace),
                  algo, nvfp4_hint, dev, sms);
   a.general = general ? 1 : 0;
+  a.tcgen05 = tcgen05 ? 1 : 0;
   a.clear_err = 1;  // the plan kernel clears the error word and flags first
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return attention_launches(a, algo, true, s);

@@ -48,9 +48,11 @@ struct AttnArgs {
   float* logits;
   int32_t logit_stride;
   // tensor-core calls: 1 runs the general kernel (NVFP4 forms, sparse-decode
-  // masks and logits); 0 runs the INT4 kernel of kvq_attn_tc.cu when the call
-  // has neither NVFP4 loops, masks nor logits
+  // masks and logits); 0 runs an INT4 kernel when the call has neither NVFP4
+  // loops, masks nor logits: the mma.sync kernel of kvq_attn_tc.cu, or the
+  // tcgen05 kernel of kvq_attn_tcgen05.cu when tcgen05 is 1
   int32_t general;
+  int32_t tcgen05;
   // 1: the plan kernel clears the error word and the plan flags before its
   // checks (the call's first launch; no separate memset)
   int32_t clear_err;
@@ -164,6 +166,13 @@ cudaError_t launch_segments(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_tcgen05(const AttnArgs& a, cudaStream_t stream);
+
+// The call runs the tcgen05 INT4 kernel (one CTA of the work split per block,
+// where the other tensor-core kernels run two per block).
+inline bool runs_tcgen05(const AttnArgs& a, bool mma_algo) {
+  return mma_algo && !a.general && a.tcgen05 && !a.nvfp4 && a.sel_mask == nullptr && a.logits == nullptr;
+}
 int attn_ctas(int algo, int device);
 
 }  // namespace kvq

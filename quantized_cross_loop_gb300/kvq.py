@@ -25,7 +25,7 @@ KVQ_TILE = 64
 KVQ_MAX_LOOPS = 8
 KVQ_FORMAT_VERSION = 1
 PLANE_CODES, PLANE_MINS, PLANE_SCALES, PLANE_INDEX, PLANE_TILE_DIR = range(5)
-ATTN_AUTO, ATTN_SIMT, ATTN_MMA, ATTN_MMA_GENERAL = 0, 1, 2, 3
+ATTN_AUTO, ATTN_SIMT, ATTN_MMA, ATTN_MMA_GENERAL, ATTN_TCGEN05 = 0, 1, 2, 3, 4
 ATTN_NVFP4 = 8  # OR-ed into algo: the table may hold NVFP4 residual loops
 KVQ_KGROUP_COMPACT, KVQ_KGROUP_TILE = 0, 1  # K groups: 64 stored rows / the stored rows of one 64-token tile
 KVQ_LOOP_K_TILE, KVQ_LOOP_K_NVFP4, KVQ_LOOP_V_NVFP4 = 1, 2, 4

@@ -19,7 +19,7 @@ from tests import pathrun as P
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = [kvq.ATTN_SIMT, kvq.ATTN_MMA, kvq.ATTN_MMA_GENERAL]
+ALGOS = [kvq.ATTN_SIMT, kvq.ATTN_MMA, kvq.ATTN_MMA_GENERAL, kvq.ATTN_TCGEN05]
 H, D = 8, 128
 
 
