@@ -542,6 +542,24 @@ def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, re
                                                         algo=kvq.ATTN_SIMT))
     err = kvq.attn_error_word(st.workspace) | kvq.attn_error_word(dec_ws) | kvq.attn_error_word(pk_ws)
     selected = sum(min(n_select, r.T) for r in reqs) * Hq
+    # budget sweep: the later loop by both kernels against the dense attention at the same depth
+    dws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(B, H, Hq, D), dtype=torch.uint8, device=dev)
+    dense_ms, _ = timed(lambda: kvq.kvq_decode_attn_packed(pool.table, q, depth, H, workspace=dws))
+    err |= kvq.attn_error_word(dws)
+    sweep = []
+    for frac in (0.01, 0.025, 0.05, 0.1, 0.25):
+        ns = max(1, int(round(frac * max_t)))
+        rs_ms, sst = timed(lambda: kvq.kvq_sparse_ref_state(pool.table, q2, 2, H, ns, max_t))
+        m_ms, _ = timed(lambda: kvq.kvq_sparse_decode_attn(pool.table, q, depth, H, sst, workspace=dec_ws,
+                                                           algo=kvq.ATTN_MMA))
+        g_ms, _ = timed(lambda: kvq.kvq_sparse_decode_attn(pool.table, q, depth, H, sst, workspace=pk_ws,
+                                                           algo=kvq.ATTN_SIMT))
+        a_ms, _ = timed(lambda: kvq.kvq_sparse_decode_attn(pool.table, q, depth, H, sst, workspace=dec_ws))
+        err |= kvq.attn_error_word(sst.workspace) | kvq.attn_error_word(dec_ws) | kvq.attn_error_word(pk_ws)
+        sweep.append({"keys_per_query_head": ns, "fraction": frac, "ref_state_ms": rs_ms,
+                      "later_loop_masked_ms": m_ms, "later_loop_gather_ms": g_ms, "later_loop_auto_ms": a_ms,
+                      "later_loop_vs_dense": min(m_ms, g_ms) / dense_ms})
+        del sst
     empty = torch.zeros((0, H, D), dtype=torch.bfloat16, device=dev)
     tail = [(empty, empty, torch.randn((100, H, D), generator=g, device=dev).to(torch.bfloat16),
              torch.randn((100, H, D), generator=g, device=dev).to(torch.bfloat16)) for _ in reqs]
@@ -580,7 +598,8 @@ def run_extras(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, ptrs, re
                               "ref_state_ms": ref_ms, "later_loop_ms": dec_ms,
                               "later_loop_kernel": "key-masked tensor-core attention",
                               "later_loop_ms_per_key_kernel": pk_ms,
-                              "selected_keys_per_s": selected / (dec_ms * 1e-3)},
+                              "selected_keys_per_s": selected / (dec_ms * 1e-3),
+                              "dense_attention_ms": dense_ms, "budget_sweep": sweep},
             "bf16_tail": {"tail_tokens_per_request": 100, "attention_ms": tail_ms},
             "error_word": err}
 

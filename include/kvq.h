@@ -435,7 +435,10 @@ kvq_status kvq_sparse_ref_state(const kvq_request* reqs, int n_requests, int n_h
  *     packed tensor-core attention (kvq_decode_attn_packed) attends with the
  *     unselected keys' logits dropped; a small kernel then applies the
  *     correction;
- *   - otherwise a kernel that gathers the selected keys one by one.
+ *   - otherwise, or when the selection is small (n_select * 64 <= max_tokens:
+ *     the key-masked attention still reads every tile, while gathering so few
+ *     keys one by one reads far fewer bytes), a kernel that gathers the
+ *     selected keys one by one.
  * kvq_sparse_decode_attn reads NVFP4 loops (it passes KVQ_ATTN_NVFP4). */
 kvq_status kvq_sparse_decode_attn(const kvq_request* reqs, int n_requests, int n_heads, int n_q_heads, int head_dim,
                                   int depth, const uint16_t* q, float softmax_scale, int n_select, int max_tokens,
@@ -449,7 +452,7 @@ kvq_status kvq_sparse_decode_attn(const kvq_request* reqs, int n_requests, int n
 size_t kvq_sparse_decode_workspace_bytes(int n_requests, int n_heads, int n_q_heads, int head_dim, int max_tokens);
 
 /* Same as kvq_sparse_decode_attn, choosing the kernel: algo KVQ_ATTN_AUTO (the
- * tensor-core path when the conditions above hold), KVQ_ATTN_SIMT (the per-key
+ * choice above), KVQ_ATTN_SIMT (the per-key
  * kernel) or KVQ_ATTN_MMA (the tensor-core path, or KVQ_ERR_UNSUPPORTED /
  * KVQ_ERR_WORKSPACE when it cannot run), ORed with KVQ_ATTN_NVFP4 when the table
  * may hold NVFP4 loops. Without that flag the tensor-core path refuses requests

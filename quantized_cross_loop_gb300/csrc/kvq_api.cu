@@ -947,7 +947,9 @@ kvq_status kvq_sparse_decode_attn_ex(const kvq_request* reqs, int n_requests, in
                 "aligned out", kMmaMaxDepth);
   if (algo == KVQ_ATTN_MMA && workspace_bytes < need)
     return fail(KVQ_ERR_WORKSPACE, "the tensor-core path needs %zu bytes of workspace", need);
-  const bool tc = algo != KVQ_ATTN_SIMT && tc_ok && workspace_bytes >= need;
+  // a small selection is cheaper gathered key by key than attended through key masks, which read every tile
+  const bool small = (long long)n_select * 64 <= (long long)max_tokens;
+  const bool tc = algo != KVQ_ATTN_SIMT && tc_ok && workspace_bytes >= need && !(algo == KVQ_ATTN_AUTO && small);
   SparseArgs a;
   memset(&a, 0, sizeof a);
   a.reqs = reqs;

@@ -185,6 +185,17 @@ __device__ __forceinline__ void group_sync(int grp) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kGroupThreads) : "memory");
 }
 
+// The group's barrier, returning whether any of its threads passed v = true.
+__device__ __forceinline__ bool group_sync_or(int grp, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, %2, %3, pi; selp.u32 %0, 1, 0, po; }"
+      : "=r"(r)
+      : "r"(uint32_t(v)), "r"(1 + grp), "n"(kGroupThreads)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t m, uint32_t o) {
   uint32_t r;
   asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(a), "r"(m), "r"(o));
@@ -562,8 +573,9 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
   for (long long x = s0; x < e0; ++x, ++it) {
     const int s = grp * kStagesPerGroup + int(it & 1);
     const uint32_t ph = uint32_t((it >> 1) & 1);
-    if (!mbar_wait(&S.full[s], ph)) {
-      if (lane == 0) atomicOr(a.err, 8);
+    // a wait that ran out ends the whole group together (its warps meet at the group's barriers)
+    if (group_sync_or(grp, !mbar_wait(&S.full[s], ph))) {
+      if (gt == 0) atomicOr(a.err, 8);
       return;
     }
     const Stage& st = S.st[s];

@@ -195,3 +195,19 @@ def test_sparse_empty_selection_and_path_choice():
     kvq.kvq_sparse_decode_attn(table, qs[1].cuda(), 4, H, st, workspace=small)
     torch.cuda.synchronize()
     assert kvq.attn_error_word(small) == 0
+
+
+def test_sparse_auto_takes_the_gather_for_small_selections():
+    """With a workspace large enough for the key-masked path, AUTO gathers a
+    selection of at most max_tokens / 64 keys per query head key by key (the
+    masked attention would still read every tile) and attends larger ones
+    through key masks: AUTO's output equals that kernel's bit for bit."""
+    table, reqs, oks, ovs, qs = _setup([1000, 777], True, 32, seed=5)
+    n = kvq.kvq_sparse_decode_workspace_bytes(2, H, 32, D, 1000)
+    for n_select, path in ((15, "per_key"), (16, "tensor_core"), (120, "tensor_core")):
+        st = kvq.kvq_sparse_ref_state(table, qs[0].cuda(), 2, H, n_select, 1000)
+        ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        auto = kvq.kvq_sparse_decode_attn(table, qs[1].cuda(), 4, H, st, workspace=ws).cpu().numpy()
+        assert kvq.attn_error_word(ws) == 0
+        ref, err = _decode(table, qs[1], 4, st, path, 32)
+        assert err == 0 and np.array_equal(auto, ref), (n_select, path)
