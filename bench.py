@@ -227,10 +227,11 @@ def rank_workload(cfg_idx: int, rank: int, replicate: int, device):
 # ------------------------------------------------------------------ CPU oracle
 
 
-def oracle_attention_sample(reqs, q_rows, depth, scale, threads):
+def oracle_attention_sample(reqs, q_rows, depth, scale, threads, outputs=None):
     """The CPU oracle's packed decode attention over `reqs` with `threads` host
     threads: the FP32 decode of the K and V chains at `depth`, then FP32
-    attention. The chains are encoded first, untimed. Returns seconds."""
+    attention. The chains are encoded first, untimed. Returns seconds; the
+    outputs are appended to `outputs` when it is a list."""
     from oracle import oracle as O
     from quantized_cross_loop_gb300.workloads import bf16_bits
 
@@ -248,9 +249,12 @@ def oracle_attention_sample(reqs, q_rows, depth, scale, threads):
         chains = list(ex.map(encode, range(len(reqs))))
     t0 = time.perf_counter()
     with ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(lambda c: O.attention_f32(c[2], O.decode_f32(c[0], depth), O.decode_f32(c[1], depth), scale),
-                    chains))
-    return time.perf_counter() - t0
+        res = list(ex.map(lambda c: O.attention_f32(c[2], O.decode_f32(c[0], depth), O.decode_f32(c[1], depth), scale),
+                          chains))
+    secs = time.perf_counter() - t0
+    if outputs is not None:
+        outputs.extend(res)
+    return secs
 
 
 def attention_bytes(reqs, H, D, Hq, depth, payload):
@@ -434,7 +438,8 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq)
+        gpu_out = kvq.kvq_decode_attn_packed(pool.table, q, depth, H, algo=algo, workspace=ws).cpu().numpy()
+        cpu = run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq, gpu_out)
 
     if rank == 0:
         line = {
@@ -904,15 +909,30 @@ def run_configs(torch, kvq, dev, stream, peak):
     return res
 
 
-def run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq):
+def run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq, gpu_out=None):
     """The CPU oracle's packed decode attention as it stands, on the host cores,
-    over a bounded sample of the same requests; same metric and unit."""
+    over a bounded sample of the same requests; same metric and unit. With the
+    GPU attention output of those requests (gpu_out), the largest absolute and
+    relative differences to the oracle's output on the sample as well."""
+    import numpy as np
+
     cores = os.cpu_count() or 1
     scale = 1.0 / math.sqrt(D)
     t1 = oracle_attention_sample(reqs[:1], q[:1], depth, scale, 1)
     n = max(1, min(len(reqs), int(args.cpu_seconds * cores / max(t1, 1e-3))))
     sample = reqs[:n]
-    secs = oracle_attention_sample(sample, q[:n], depth, scale, cores)
+    ref = []
+    secs = oracle_attention_sample(sample, q[:n], depth, scale, cores, ref)
+    accuracy = None
+    if gpu_out is not None:
+        r = np.stack([np.asarray(x, dtype=np.float64) for x in ref])
+        g = np.asarray(gpu_out[:n], dtype=np.float64).reshape(r.shape)
+        err = np.abs(g - r)
+        big = np.abs(r) >= 0.05  # relative error where it means something
+        accuracy = {"requests": n, "max_abs": float(err.max()),
+                    "max_rel_where_abs_ref_ge_0.05": float((err[big] / np.abs(r[big])).max()) if big.any() else None,
+                    "max_share_of_tolerance": float((err / (2e-3 + 1e-2 * np.abs(r))).max()),
+                    "tolerance": "|gpu - oracle| <= 2e-3 + 1e-2 |oracle| per element"}
 
     def bytes_of(rs):
         return attention_bytes(rs, H, D, Hq, depth, lambda k, nn, s: kvq.payload_bytes(k, nn, H, D, s))
@@ -921,7 +941,8 @@ def run_cpu_baseline(args, reqs, q, depth, D, H, Hq, kvq):
             "value_1_thread": bytes_of(reqs[:1]) / t1 / 1e9, "cpu_model": cpu_model(),
             "sample": f"{n} of {len(reqs)} requests of the same workload: packed decode attention at depth {depth} "
                       f"(FP32 decode of the K/V chains, FP32 attention; chains encoded beforehand, untimed), "
-                      f"{secs:.2f} s on {cores} threads; value_1_thread: one request on one thread, {t1:.3f} s"}
+                      f"{secs:.2f} s on {cores} threads; value_1_thread: one request on one thread, {t1:.3f} s",
+            "gpu_vs_oracle": accuracy}
 
 
 def cpu_model():

@@ -4,7 +4,9 @@ place that sees both, and neither side imports the other."""
 
 from __future__ import annotations
 
+import json
 import math
+import os
 from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
@@ -88,6 +90,30 @@ def assert_attention_close(out_gpu, out_ref, what=""):
     assert not bad.any(), (f"attention out of tolerance {what}: {bad.sum()} elements, max abs err "
                            f"{err.max():.3e}, worst at {np.unravel_index(np.argmax(err - bound), err.shape)}")
     return float(err.max()), float((err / np.maximum(np.abs(b), 1e-30)).max())
+
+
+def accuracy_record(outs, refs):
+    """Largest absolute error, largest relative error where |ref| >= 0.05, and
+    the largest share of the per-element tolerance used, over a set of outputs."""
+    a = np.concatenate([np.asarray(o, dtype=np.float64).ravel() for o in outs])
+    b = np.concatenate([np.asarray(r, dtype=np.float64).ravel() for r in refs])
+    err = np.abs(a - b)
+    big = np.abs(b) >= 0.05
+    return {"max_abs": float(err.max()),
+            "max_rel_where_abs_ref_ge_0.05": float((err[big] / np.abs(b[big])).max()) if big.any() else None,
+            "max_share_of_tolerance": float((err / (ATOL + RTOL * np.abs(b))).max())}
+
+
+def log_accuracy(what, outs, refs):
+    """Appends accuracy_record(outs, refs) as one JSON line to the file named by
+    KVQ_ACCURACY_LOG, when that variable is set (a record of the attention
+    error per configuration beside the pass/fail check)."""
+    path = os.environ.get("KVQ_ACCURACY_LOG")
+    if not path:
+        return
+    rec = {"case": what, **accuracy_record(outs, refs)}
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
 
 
 def assert_reader_error_bounded(out_gpu, o_ref, ks, vs, khat, vhat, q_bits, depth, scale, what=""):

@@ -44,6 +44,9 @@ def check_workload(wl, sample=None, depths=(4,), full_recon=True):
             out, err = P.gpu_attention(wl, kc, vc, depth, algo)
             assert err == 0
             out = out.cpu().numpy()
+            P.log_accuracy(f"{wl.spec.name} layer {wl.layer} x{wl.n_requests} depth {depth} algo {algo} "
+                           f"({len(sample)} requests)", [out[i] for i in sample],
+                           [r[4] for r in ref])
             for j, i in enumerate(sample):
                 ks, vs, khat, vhat, o_ref = ref[j]
                 if depth == depths[0] and algo == _algos()[0]:
