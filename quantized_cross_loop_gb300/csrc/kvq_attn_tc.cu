@@ -9,10 +9,10 @@
 // decode = min + scale * code; §5: FP32 mass and accumulation.
 //
 // Work list, partial slots, plan and merge are those of kvq_attn_common.cuh.
-// A CTA holds two independent groups (virtual CTAs); a group is one producer
-// warp, whose lane 0 stages each 64-token tile's packed planes (codes, min and
-// scale planes, sparse index slices) into a two-stage ring with 1-D bulk
-// copies, and four consumer warps, each owning 16 tokens of the tile.
+// A CTA holds two independent groups (virtual CTAs); a group is two producer
+// warps, which stage alternate 64-token tiles' packed planes (codes, min and
+// scale planes, sparse index slices) into the group's two-stage ring with 1-D
+// bulk copies, and four consumer warps, each owning 16 tokens of the tile.
 //
 // Codes as subnormals. The nibble of channel c sits at bits 0..3 of its byte
 // when c is even and at bits 4..7 when c is odd. AND-ing a 32-bit word of
@@ -188,21 +188,16 @@ __device__ __forceinline__ __half2 u2h(uint32_t v) { return *reinterpret_cast<__
 // ---------------------------------------------------------------- producer
 //
 // A group's two producer warps take alternate tiles (warp p fills stage p of
-// the group's two), so that one warp's copy set-up overlaps the other's. A
-// producer warp stages a tile in two ways. The K and V code blocks
-// (up to 4 KB per loop each) go by 1-D bulk copy, one per lane (lane 8 j + c,
-// c = 0 K, 1 V, of loop j); every bulk copy costs the copy engine a fixed
-// time whatever its size, so the small planes - the K min and scale rows of
-// the tile's groups, its V min and scale rows and a sparse loop's index slice,
-// a few hundred bytes each - go instead as 16-byte asynchronous copies spread
-// over the lanes of the loop. Lane 0 adds the bulk copies' bytes to the
-// stage's expected transaction count before they start; every lane then
-// makes the barrier wait for its 16-byte copies; lane 0 arrives once the
-// metadata is written.
-
-__device__ __forceinline__ void copy16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
+// the group's two), so that one warp's copy set-up overlaps the other's. Lane
+// 8 j + c serves loop j with one 1-D bulk copy: c = 0 the K code block, 1 the
+// V code block (up to 4 KB each), 2 and 3 the K min and scale rows of the
+// tile's groups (256 B per group each), 4 and 5 the V min and scale rows
+// (4 B per row, in whole 16-byte units), 6 a sparse loop's index slice. All
+// per-tile arithmetic - rows, groups, pairs, sizes, the stage's expected byte
+// count - comes before the wait for a free stage; after it the warp only
+// issues the copies and writes the metadata, and lane 0 arrives. (Issuing the
+// small planes as many 16-byte asynchronous copies instead cost the producer
+// warp thousands of cycles per tile, which the consumers waited for.)
 
 template <int DEPTH>
 __device__ void producer(const AttnArgs& a, Smem& S, int grp, int pw, long long s0, long long e0, int lane) {
@@ -213,7 +208,7 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, int pw, long long 
   int nr = 0, kgr = 0, rs = 0, gs = 0;  // this lane's loop: stored rows, tile K groups, plane strides
   const int32_t* act = nullptr;
   const int32_t* dir = nullptr;
-  const uint8_t* codes = nullptr;  // the code plane this lane copies (c < 2)
+  const uint8_t* codes = nullptr;  // the code plane of this lane (c < 2)
   const uint8_t *kmn = nullptr, *ksc = nullptr, *vmn = nullptr, *vsc = nullptr;
   long long it = 0;
   for (long long x = s0; x < e0; ++x, ++it) {
@@ -246,7 +241,6 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, int pw, long long 
     // the group's two producer warps take alternate tiles: warp pw fills stage pw
     if (int(it & 1) != pw) continue;
     const int k = int(x - us);
-    // directory entries first: their latency overlaps the wait for a free stage
     int c0 = 0, c1 = 0;
     if (j < DEPTH) {
       if (act == nullptr) {
@@ -257,16 +251,6 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, int pw, long long 
         c1 = __ldg(dir + k + 1);
       }
     }
-    const int s = grp * kStagesPerGroup + int(it & 1);
-    const uint32_t ph = uint32_t((it >> 1) & 1);
-    int ok = 1;
-    if (lane == 0 && it >= kStagesPerGroup) ok = mbar_wait(&S.empty[s], ph ^ 1u) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, ok, 0)) {
-      if (lane == 0) atomicOr(a.err, 8);
-      return;
-    }
-    Stage& st = S.st[s];
-    int32_t* M = st.meta;
     // this lane's loop: rows of the tile, K groups, pairs
     bool bad = false;
     int n = 0, g0 = 0, ngrp = 0;
@@ -294,52 +278,62 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, int pw, long long 
     }
     const bool live = j < DEPTH && ngrp > 0;
     const long long hr = (long long)h * rs + c0;  // first stored row of this head
-    // bulk copies of the code blocks
-    const uint32_t bytes = (live && c < 2) ? uint32_t(n * kRowBytes) : 0u;
+    // this lane's copy: source, size (16-byte aligned and rounded, as every plane starts on a 16-byte boundary)
+    const long long voff = hr * 4, vlo = voff & ~15LL;
+    const long long ioff = (long long)c0 * 4, ilo = ioff & ~15LL;
+    const int vrem = int((voff - vlo) / 2), irem = int((ioff - ilo) / 4);
+    uint32_t bytes = 0;
+    const uint8_t* src = nullptr;
+    if (live) {
+      const long long kb = ((long long)h * gs + g0) * kD * 2;
+      const uint32_t vbytes = uint32_t(((voff + (long long)n * 4 + 15) & ~15LL) - vlo);
+      switch (c) {
+        case 0:
+        case 1: bytes = uint32_t(n * kRowBytes); src = codes + hr * kRowBytes; break;
+        case 2: bytes = uint32_t(ngrp * kD * 2); src = kmn + kb; break;
+        case 3: bytes = uint32_t(ngrp * kD * 2); src = ksc + kb; break;
+        case 4: bytes = vbytes; src = vmn + vlo; break;
+        case 5: bytes = vbytes; src = vsc + vlo; break;
+        case 6:
+          if (act != nullptr) {
+            bytes = uint32_t(((ioff + (long long)n * 4 + 15) & ~15LL) - ilo);
+            src = reinterpret_cast<const uint8_t*>(act) + ilo;
+          }
+          break;
+        default: break;
+      }
+    }
     uint32_t total = bytes;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
+
+    const int s = grp * kStagesPerGroup + int(it & 1);
+    const uint32_t ph = uint32_t((it >> 1) & 1);
+    int ok = 1;
+    if (lane == 0 && it >= kStagesPerGroup) ok = mbar_wait(&S.empty[s], ph ^ 1u) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+      if (lane == 0) atomicOr(a.err, 8);
+      return;
+    }
+    Stage& st = S.st[s];
+    int32_t* M = st.meta;
     if (lane == 0) mbar_expect_tx(&S.full[s], total);
     __syncwarp();
     if (bytes > 0) {
       LoopStage& LS = st.l[j];
+      void* dst = c == 0 ? (void*)LS.kc
+                  : c == 1 ? (void*)LS.vc
+                  : c == 2 ? (void*)LS.kmin
+                  : c == 3 ? (void*)LS.ksc
+                  : c == 4 ? (void*)LS.vmin
+                  : c == 5 ? (void*)LS.vsc
+                           : (void*)LS.idx;
       asm volatile(
           "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-              smem_addr(c == 0 ? (void*)LS.kc : (void*)LS.vc)),
-          "l"(codes + hr * kRowBytes), "r"(bytes), "r"(smem_addr(&S.full[s]))
+              smem_addr(dst)),
+          "l"(src), "r"(bytes), "r"(smem_addr(&S.full[s]))
           : "memory");
     }
-    // 16-byte copies of the small planes: K min and scale rows of the tile's groups (256 B per
-    // group each), V min and scale rows (4 B per row each, in whole 16-byte units), index slice
-    int vrem = 0, irem = 0;
-    if (live) {
-      LoopStage& LS = st.l[j];
-      const long long kb = ((long long)h * gs + g0) * kD * 2;
-      const int nk = ngrp * (kD * 2 / 16);
-      const long long voff = hr * 4, vlo = voff & ~15LL;
-      const int nv = int((((voff + (long long)n * 4 + 15) & ~15LL) - vlo) / 16);
-      vrem = int((voff - vlo) / 2);
-      const long long ioff = (long long)c0 * 4, ilo = ioff & ~15LL;
-      const int ni = act != nullptr ? int((((ioff + (long long)n * 4 + 15) & ~15LL) - ilo) / 16) : 0;
-      irem = int((ioff - ilo) / 4);
-      const int ntot = 2 * nk + 2 * nv + ni;
-      for (int t = c; t < ntot; t += 8) {
-        if (t < nk) {
-          copy16(reinterpret_cast<uint8_t*>(LS.kmin) + 16 * t, kmn + kb + 16 * t);
-        } else if (t < 2 * nk) {
-          copy16(reinterpret_cast<uint8_t*>(LS.ksc) + 16 * (t - nk), ksc + kb + 16 * (t - nk));
-        } else if (t < 2 * nk + nv) {
-          copy16(reinterpret_cast<uint8_t*>(LS.vmin) + 16 * (t - 2 * nk), vmn + vlo + 16 * (t - 2 * nk));
-        } else if (t < 2 * nk + 2 * nv) {
-          copy16(reinterpret_cast<uint8_t*>(LS.vsc) + 16 * (t - 2 * nk - nv), vsc + vlo + 16 * (t - 2 * nk - nv));
-        } else {
-          copy16(reinterpret_cast<uint8_t*>(LS.idx) + 16 * (t - 2 * nk - 2 * nv),
-                 reinterpret_cast<const uint8_t*>(act) + ilo + 16 * (t - 2 * nk - 2 * nv));
-        }
-      }
-    }
-    // the stage's phase also waits for this lane's 16-byte copies
-    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(&S.full[s])) : "memory");
     // metadata
     if (lane == 0) {
       M[0] = unit;
