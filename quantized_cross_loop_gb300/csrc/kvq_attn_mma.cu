@@ -171,15 +171,6 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t pari
   return true;
 }
 
-// Adds `bytes` to the barrier's expected transaction count, then starts the copy.
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, unsigned long long* bar) {
-  mbar_expect_tx(bar, bytes);
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
 // Named barrier of one consumer group (ids 1, 2).
 __device__ __forceinline__ void group_sync(int grp) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kGroupThreads) : "memory");
@@ -241,24 +232,30 @@ __device__ __forceinline__ uint32_t nv_pair(uint32_t x) {
 }
 
 // ---------------------------------------------------------------- producer
+//
+// One warp per group. Lane 8 j + c serves loop j with one 1-D bulk copy: c = 0
+// the K code block, 1 the V code block, 2 the K min rows of the tile's groups
+// (NVFP4 K: its E4M3 block scales, 8 B per row), 3 the K scale rows, 4 the V
+// min rows (NVFP4 V: its block scales), 5 the V scale rows, 6 a sparse loop's
+// index slice; row planes move in whole 16-byte units. All per-tile arithmetic
+// comes before the wait for a free stage; after it the warp only issues the
+// copies and writes the metadata, and lane 0 arrives (the copies issued one by
+// one from a single thread after the wait kept the consumers waiting).
 
 template <int DEPTH, bool kNv>
-__device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long long e0) {
+__device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long long e0, int lane) {
+  const int j = lane >> 3, c = lane & 7;  // this lane's loop and copy
   int b = request_of(a.prefix, a.n_requests, s0);
   long long us = 0, ue = -1;  // current unit's tile range
   int h = 0, T = 0, unit = -1, nsink = 0;
-  int nr[DEPTH], kgr[DEPTH];  // stored rows; K groups per head (0: compact grouping, else tile grouping)
-  int rs[DEPTH], gs[DEPTH];   // plane strides: rows per head, K groups per head
-  int fl[DEPTH];              // NVFP4 flags per loop (1: K, 2: V); the INT4 form never sees them (plan)
-  float kst[DEPTH], vst[DEPTH];  // their tensor scales
-  const int32_t* act[DEPTH];
-  const int32_t* dir[DEPTH];
-  const uint8_t* kc[DEPTH];
-  const uint16_t* kmn[DEPTH];
-  const uint16_t* ksc[DEPTH];
-  const uint8_t* vc[DEPTH];
-  const uint16_t* vmn[DEPTH];
-  const uint16_t* vsc[DEPTH];
+  int nr = 0, kgr = 0;  // this lane's loop: stored rows; K groups per head (0: compact grouping)
+  int rs = 0, gs = 0;   // plane strides: rows per head, K groups per head
+  int fl = 0;           // NVFP4 flags (1: K, 2: V); the INT4 form never sees them (plan)
+  float kst = 0.0f, vst = 0.0f;  // their tensor scales
+  const int32_t* act = nullptr;
+  const int32_t* dir = nullptr;
+  const uint8_t *kc = nullptr, *vc = nullptr;
+  const uint8_t *kmn = nullptr, *ksc = nullptr, *vmn = nullptr, *vsc = nullptr;
   long long it = 0;
   for (long long x = s0; x < e0; ++x, ++it) {
     if (x >= ue) {  // next unit: request b (skipping empty ones) and KV head h
@@ -272,129 +269,168 @@ __device__ void producer(const AttnArgs& a, Smem& S, int grp, long long s0, long
       us = rb + (long long)h * nt;
       ue = us + nt;
       unit = b * a.H + h;
-#pragma unroll
-      for (int j = 0; j < DEPTH; ++j) {
+      if (j < DEPTH) {
         const kvq_loop_ref& L = R.loop[j];
-        nr[j] = L.n_rows;
-        kgr[j] = (L.flags & KVQ_LOOP_K_TILE) ? k_groups_of(true, L.n_rows, T) : 0;
-        rs[j] = L.row_cap > 0 ? L.row_cap : L.n_rows;
-        gs[j] = L.kgroup_cap > 0 ? L.kgroup_cap : (kgr[j] > 0 ? kgr[j] : (L.n_rows + kG - 1) / kG);
-        fl[j] = kNv ? (((L.flags & KVQ_LOOP_K_NVFP4) ? 1 : 0) | ((L.flags & KVQ_LOOP_V_NVFP4) ? 2 : 0)) : 0;
-        kst[j] = (kNv && (fl[j] & 1) && L.n_rows > 0) ? __ldg(reinterpret_cast<const float*>(L.k_scales)) : 0.0f;
-        vst[j] = (kNv && (fl[j] & 2) && L.n_rows > 0) ? __ldg(reinterpret_cast<const float*>(L.v_scales)) : 0.0f;
-        act[j] = L.active_idx;
-        dir[j] = L.tile_dir;
-        kc[j] = L.k_codes;
-        kmn[j] = L.k_mins;
-        ksc[j] = L.k_scales;
-        vc[j] = L.v_codes;
-        vmn[j] = L.v_mins;
-        vsc[j] = L.v_scales;
+        nr = L.n_rows;
+        kgr = (L.flags & KVQ_LOOP_K_TILE) ? k_groups_of(true, L.n_rows, T) : 0;
+        rs = L.row_cap > 0 ? L.row_cap : L.n_rows;
+        gs = L.kgroup_cap > 0 ? L.kgroup_cap : (kgr > 0 ? kgr : (L.n_rows + kG - 1) / kG);
+        fl = kNv ? (((L.flags & KVQ_LOOP_K_NVFP4) ? 1 : 0) | ((L.flags & KVQ_LOOP_V_NVFP4) ? 2 : 0)) : 0;
+        kst = (kNv && (fl & 1) && L.n_rows > 0 && c == 0) ? __ldg(reinterpret_cast<const float*>(L.k_scales)) : 0.0f;
+        vst = (kNv && (fl & 2) && L.n_rows > 0 && c == 0) ? __ldg(reinterpret_cast<const float*>(L.v_scales)) : 0.0f;
+        act = L.active_idx;
+        dir = L.tile_dir;
+        kc = L.k_codes;
+        vc = L.v_codes;
+        kmn = reinterpret_cast<const uint8_t*>(L.k_mins);
+        ksc = reinterpret_cast<const uint8_t*>(L.k_scales);
+        vmn = reinterpret_cast<const uint8_t*>(L.v_mins);
+        vsc = reinterpret_cast<const uint8_t*>(L.v_scales);
       }
     }
     const int k = int(x - us);
-    // directory entries first: their latency overlaps the wait for a free stage
-    int c0s[DEPTH], c1s[DEPTH];
-#pragma unroll
-    for (int j = 0; j < DEPTH; ++j) {
-      if (act[j] == nullptr) {
-        c0s[j] = k * KVQ_TILE;
-        c1s[j] = min(k * KVQ_TILE + KVQ_TILE, T);
+    int c0 = 0, c1 = 0;
+    bool bad = false;
+    if (j < DEPTH) {
+      if (act == nullptr) {
+        c0 = k * KVQ_TILE;
+        c1 = min(k * KVQ_TILE + KVQ_TILE, T);
       } else {
-        c0s[j] = __ldg(dir[j] + k);
-        c1s[j] = __ldg(dir[j] + k + 1);
+        c0 = __ldg(dir + k);
+        c1 = __ldg(dir + k + 1);
+      }
+      if (c0 < 0 || c1 > nr || c0 > c1 || c1 - c0 > KVQ_TILE) {
+        bad = true;
+        c0 = c1 = 0;
       }
     }
+    const int n = c1 - c0;
+    // K groups of the tile's rows: under tile grouping the tile's own group k,
+    // and word 1 is set so that a consumer's ((word1 + row) >> 6) - g0 is 0
+    const bool kt = kgr > 0;
+    const bool nk = kNv && (fl & 1), nv = kNv && (fl & 2);
+    const int g0 = kt ? k : c0 / kG;
+    const int ngrp = (j < DEPTH && n > 0 && !nk) ? (kt ? 1 : (c1 - 1) / kG - g0 + 1) : 0;  // INT4 K groups
+    int pbase = 0, np = 0;  // pairs of the earlier loops, of all loops
+#pragma unroll
+    for (int jj = 0; jj < DEPTH; ++jj) {
+      const int gj = __shfl_sync(0xffffffffu, ngrp, 8 * jj);
+      pbase += jj < j ? gj : 0;
+      np += gj;
+    }
+    const long long hr = (long long)h * rs + c0;  // first stored row of this head
+    const long long koff = hr * 8, klo = koff & ~15LL;           // NVFP4 K block scales
+    const long long voff = hr * (nv ? 8 : 4), vlo = voff & ~15LL;  // V rows (INT4 params or NVFP4 block scales)
+    const long long ioff = (long long)c0 * 4, ilo = ioff & ~15LL;
+    uint32_t bytes = 0;
+    const uint8_t* src = nullptr;
+    if (j < DEPTH && n > 0) {
+      const long long gb = ((long long)h * gs + g0) * kD * 2;
+      const uint32_t vbytes = uint32_t(((voff + (long long)n * (nv ? 8 : 4) + 15) & ~15LL) - vlo);
+      switch (c) {
+        case 0: bytes = uint32_t(n * kRowBytes); src = kc + hr * kRowBytes; break;
+        case 1: bytes = uint32_t(n * kRowBytes); src = vc + hr * kRowBytes; break;
+        case 2:
+          if (nk) {
+            bytes = uint32_t(((koff + (long long)n * 8 + 15) & ~15LL) - klo);
+            src = kmn + klo;
+          } else {
+            bytes = uint32_t(ngrp * kD * 2);
+            src = kmn + gb;
+          }
+          break;
+        case 3:
+          if (!nk) {
+            bytes = uint32_t(ngrp * kD * 2);
+            src = ksc + gb;
+          }
+          break;
+        case 4: bytes = vbytes; src = vmn + vlo; break;
+        case 5:
+          if (!nv) {
+            bytes = vbytes;
+            src = vsc + vlo;
+          }
+          break;
+        case 6:
+          if (act != nullptr) {
+            bytes = uint32_t(((ioff + (long long)n * 4 + 15) & ~15LL) - ilo);
+            src = reinterpret_cast<const uint8_t*>(act) + ilo;
+          }
+          break;
+        default: break;
+      }
+    }
+    uint32_t total = bytes;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
+
     const int s = grp * kStagesPerGroup + int(it & 1);
     const uint32_t ph = uint32_t((it >> 1) & 1);
-    if (it >= kStagesPerGroup && !mbar_wait(&S.empty[s], ph ^ 1u)) {
-      atomicOr(a.err, 8);
+    int ok = 1;
+    if (lane == 0 && it >= kStagesPerGroup) ok = mbar_wait(&S.empty[s], ph ^ 1u) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+      if (lane == 0) atomicOr(a.err, 8);
       return;
     }
     Stage& st = S.st[s];
     int32_t* M = st.meta;
-    M[0] = unit;
-    M[1] = b;
-    M[2] = h;
-    M[3] = k * KVQ_TILE;
-    M[4] = min(KVQ_TILE, T - k * KVQ_TILE);
-    M[5] = (us >= s0 && ue <= e0) ? 1 : 0;
-    M[7] = max(0, min(KVQ_TILE, nsink - k * KVQ_TILE));
-    int np = 0;
-#pragma unroll
-    for (int j = 0; j < DEPTH; ++j) {
-      int c0 = c0s[j], c1 = c1s[j];
+    if (lane == 0) mbar_expect_tx(&S.full[s], total);
+    __syncwarp();
+    if (bytes > 0) {
+      LoopStage& LS = st.l[j];
+      void* dst = c == 0 ? (void*)LS.kc
+                  : c == 1 ? (void*)LS.vc
+                  : c == 2 ? (void*)LS.kmin
+                  : c == 3 ? (void*)LS.ksc
+                  : c == 4 ? (void*)LS.vmin
+                  : c == 5 ? (void*)LS.vsc
+                           : (void*)LS.idx;
+      asm volatile(
+          "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              smem_addr(dst)),
+          "l"(src), "r"(bytes), "r"(smem_addr(&S.full[s]))
+          : "memory");
+    }
+    // metadata
+    if (lane == 0) {
+      M[0] = unit;
+      M[1] = b;
+      M[2] = h;
+      M[3] = k * KVQ_TILE;
+      M[4] = min(KVQ_TILE, T - k * KVQ_TILE);
+      M[5] = (us >= s0 && ue <= e0) ? 1 : 0;
+      M[6] = np;
+      M[7] = max(0, min(KVQ_TILE, nsink - k * KVQ_TILE));
+    }
+    if (j < DEPTH) {
       int32_t* LM = M + 16 + 8 * j;
-      if (c0 < 0 || c1 > nr[j] || c0 > c1 || c1 - c0 > KVQ_TILE) {
-        atomicOr(a.err, 4);
-        c0 = c1 = 0;
-      }
-      const int n = c1 - c0;
-      // K groups of the tile's rows: under tile grouping the tile's own group k,
-      // and word 1 is set so that a consumer's ((word1 + row) >> 6) - g0 is 0
-      const bool kt = kgr[j] > 0;
-      const bool nk = kNv && (fl[j] & 1), nv = kNv && (fl[j] & 2);
-      const int g0 = kt ? k : c0 / kG;
-      const int ngrp = (n > 0 && !nk) ? (kt ? 1 : (c1 - 1) / kG - g0 + 1) : 0;  // INT4 K groups (NVFP4: none)
-      int32_t* LF = M + kMetaFmt + 4 * j;  // read by the NVFP4 form only
-      if (kNv) {
-        LF[0] = fl[j];
-        LF[1] = __float_as_int(kst[j]);
-        LF[2] = __float_as_int(vst[j]);
-        LF[3] = 0;
-      }
-      LM[0] = n;
-      LM[1] = kt ? k * kG : c0;
-      LM[2] = g0;
-      LM[3] = ngrp;
-      LM[4] = 0;
-      LM[5] = 0;
-      LM[6] = act[j] != nullptr;
-      LM[7] = np;
-      for (int G = 0; G < ngrp; ++G) M[8 + np++] = (j << 1) | G;
-      if (n == 0) continue;
-      const long long hr = (long long)h * rs[j] + c0;  // first stored row of this head
-      bulk_copy(st.l[j].kc, kc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
-      bulk_copy(st.l[j].vc, vc[j] + hr * kRowBytes, n * kRowBytes, &S.full[s]);
-      int krem = 0, vrem = 0;
-      if (nk) {  // E4M3 block scales: 8 B per row, in whole 16-byte units
-        const long long off = hr * 8;
-        const long long lo = off & ~15LL;
-        const uint32_t nb = uint32_t(((off + (long long)n * 8 + 15) & ~15LL) - lo);
-        bulk_copy(st.l[j].kmin, reinterpret_cast<const uint8_t*>(kmn[j]) + lo, nb, &S.full[s]);
-        krem = int(off - lo);
-      } else {
-        const long long gb = ((long long)h * gs[j] + g0) * kD;
-        bulk_copy(st.l[j].kmin, kmn[j] + gb, ngrp * kD * 2, &S.full[s]);
-        bulk_copy(st.l[j].ksc, ksc[j] + gb, ngrp * kD * 2, &S.full[s]);
-      }
-      if (nv) {
-        const long long off = hr * 8;
-        const long long lo = off & ~15LL;
-        const uint32_t nb = uint32_t(((off + (long long)n * 8 + 15) & ~15LL) - lo);
-        bulk_copy(st.l[j].vmin, reinterpret_cast<const uint8_t*>(vmn[j]) + lo, nb, &S.full[s]);
-        vrem = int(off - lo);
-      } else {  // V params: 4 B per row and plane, moved in whole 16-byte units
-        const long long off = hr * 4;
-        const long long lo = off & ~15LL;
-        const uint32_t nb = uint32_t(((off + (long long)n * 4 + 15) & ~15LL) - lo);
-        bulk_copy(st.l[j].vmin, reinterpret_cast<const uint8_t*>(vmn[j]) + lo, nb, &S.full[s]);
-        bulk_copy(st.l[j].vsc, reinterpret_cast<const uint8_t*>(vsc[j]) + lo, nb, &S.full[s]);
-        LM[4] = int((off - lo) / 2);
-      }
-      if (kNv) LF[3] = krem | (vrem << 16);
-      if (act[j] != nullptr) {
-        const long long off = (long long)c0 * 4;
-        const long long lo = off & ~15LL;
-        const uint32_t nb = uint32_t(((off + (long long)n * 4 + 15) & ~15LL) - lo);
-        bulk_copy(st.l[j].idx, reinterpret_cast<const uint8_t*>(act[j]) + lo, nb, &S.full[s]);
-        LM[5] = int((off - lo) / 4);
+      if (c == 0) {
+        LM[0] = n;
+        LM[1] = kt ? k * kG : c0;
+        LM[2] = g0;
+        LM[3] = ngrp;
+        LM[4] = (n > 0 && !nv) ? int((voff - vlo) / 2) : 0;
+        LM[5] = (n > 0 && act != nullptr) ? int((ioff - ilo) / 4) : 0;
+        LM[6] = act != nullptr;
+        LM[7] = pbase;
+        if (kNv) {
+          int32_t* LF = M + kMetaFmt + 4 * j;  // read by the NVFP4 form only
+          LF[0] = fl;
+          LF[1] = __float_as_int(kst);
+          LF[2] = __float_as_int(vst);
+          LF[3] = n > 0 ? (int(nk ? koff - klo : 0) | (int(nv ? voff - vlo : 0) << 16)) : 0;
+        }
+        if (bad) atomicOr(a.err, 4);
+      } else if (c == 1 || c == 2) {
+        if (c - 1 < ngrp) M[8 + pbase + c - 1] = (j << 1) | (c - 1);
       }
     }
-    M[6] = np;
-    // the single expected arrival: releases the metadata; the phase completes
-    // once every copy has delivered its bytes
-    mbar_arrive(&S.full[s]);
+    // the single expected arrival releases the metadata (ordered after every
+    // lane's writes by the warp barrier); the phase completes once every copy
+    // has delivered its bytes
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.full[s]);
   }
 }
 
@@ -940,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a) {
   const long long s0 = cta_start(vcta, W, C), e0 = cta_start(vcta + 1, W, C);
   if (s0 >= e0) return;
   if (producer_warp) {
-    if ((threadIdx.x & 31) == 0) producer<DEPTH, kNv>(a, S, grp, s0, e0);
+    producer<DEPTH, kNv>(a, S, grp, s0, e0, threadIdx.x & 31);
     return;
   }
   consumer<DEPTH, kNv, kSp>(a, S, grp, vcta, s0, e0);
