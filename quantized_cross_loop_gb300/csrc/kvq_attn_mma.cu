@@ -1019,8 +1019,10 @@ int mma_virtual_ctas_per_block() { return mma_attn::kGroups; }
 
 cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream) {
   using namespace mma_attn;
-  if (!a.general && !a.nvfp4 && a.sel_mask == nullptr && a.logits == nullptr)
-    return a.tcgen05 ? launch_attn_tcgen05(a, stream) : launch_attn_tc(a, stream);
+  if (!a.general && !a.nvfp4) {
+    if (a.tcgen05 && a.sel_mask == nullptr && a.logits == nullptr) return launch_attn_tcgen05(a, stream);
+    return launch_attn_tc(a, stream);
+  }
   const cudaError_t e = (a.sel_mask != nullptr || a.logits != nullptr) ? launch_form<true>(a, stream)
                                                                         : launch_form<false>(a, stream);
   if (e == cudaErrorInvalidValue) return e;

@@ -552,7 +552,9 @@ __device__ void finish_unit(const AttnArgs& a, GroupSmem& G, UnitState& U, const
   group_sync(grp);
 }
 
-template <int DEPTH, bool G8>
+// kSp: the sparse-decode branches (key masks of a later loop; every logit of a
+// reference pass), in an instantiation of their own.
+template <int DEPTH, bool G8, bool kSp>
 __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long long s0, long long e0) {
   constexpr int kSlots = G8 ? 2 : 1;
   const int gt = threadIdx.x - grp * kGroupThreads;  // thread within the group
@@ -601,6 +603,21 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         for (int e = 0; e < 4; ++e) U.acc[mt][e] = 0.f;
       load_unit_query(a, Gs, Mprev.b, Mprev.h, gt);
       group_sync(grp);
+    }
+    // sparse decode, later loop: the selection bits of the warp's 16 tokens for this thread's query
+    // heads (one mask word covers them), loaded here so that their latency overlaps the tile's QK;
+    // a request longer than the masks cover (the sparse path refuses it) selects nothing here
+    uint32_t selw[2] = {0u, 0u};
+    if (kSp && a.sel_mask != nullptr) {
+      const int tb = t0 + 16 * w;
+      const bool in = (tb >> 5) < a.mask_words;
+#pragma unroll
+      for (int e = 0; e < kSlots; ++e) {
+        const int hh = head_of<G8>(q, e);
+        if (in && hh < gq)
+          selw[e] = __ldg(a.sel_mask + ((long long)Mprev.b * a.Hq + (long long)Mprev.h * gq + hh) * a.mask_words +
+                          (tb >> 5)) >> (tb & 31);
+      }
     }
     prep_tile<DEPTH, G8>(a, Gs, st, npairs, t0, gt, w, lane);
     group_sync(grp);  // fragments, K-min columns and presence masks ready
@@ -699,8 +716,18 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
         c4[k] = C[e][0][k] + C[e][1][k];
         if (kChains == 4) c4[k] += C[e][2][k] + C[e][3][k];
       }
-      const float sA = (vA && hok) ? (c4[0] + c4[1]) * lsc : -INFINITY;
-      const float sC = (vC && hok) ? (c4[2] + c4[3]) * lsc : -INFINITY;
+      float sA = (vA && hok) ? (c4[0] + c4[1]) * lsc : -INFINITY;
+      float sC = (vC && hok) ? (c4[2] + c4[3]) * lsc : -INFINITY;
+      if (kSp && a.logits != nullptr) {  // sparse decode reference pass: every logit, for the selection
+        float* lr = a.logits + ((long long)Mprev.b * a.Hq + (long long)Mprev.h * gq + head_of<G8>(q, e)) *
+                                   a.logit_stride;
+        if (vA && hok && t0 + tA < a.logit_stride) lr[t0 + tA] = sA;
+        if (vC && hok && t0 + tC < a.logit_stride) lr[t0 + tC] = sC;
+      }
+      if (kSp && a.sel_mask != nullptr) {  // sparse decode later loop: only the query head's selected keys
+        if (!((selw[e] >> g) & 1u)) sA = -INFINITY;
+        if (!((selw[e] >> (g + 8)) & 1u)) sC = -INFINITY;
+      }
       float mt = fmaxf(sA, sC);
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
@@ -820,7 +847,7 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
   if (cur_unit >= 0) finish_unit<G8>(a, Gs, U, Mprev, grp, vcta, w, lane);
 }
 
-template <int DEPTH, bool G8>
+template <int DEPTH, bool G8, bool kSp>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -856,41 +883,50 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
     producer<DEPTH>(a, S, grp, pw, s0, e0, threadIdx.x & 31);
     return;
   }
-  consumer<DEPTH, G8>(a, S, grp, vcta, s0, e0);
+  consumer<DEPTH, G8, kSp>(a, S, grp, vcta, s0, e0);
 }
 
-template <int DEPTH, bool G8>
+template <int DEPTH, bool G8, bool kSp>
 cudaError_t launch_depth(const AttnArgs& a, cudaStream_t stream) {
   const int smem = int(sizeof(Smem));
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<DEPTH, G8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_tc_kernel<DEPTH, G8, kSp>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_dependent(attn_tc_kernel<DEPTH, G8>, dim3(a.n_ctas / kGroups), dim3(kThreads), size_t(smem), stream, a);
+  return launch_dependent(attn_tc_kernel<DEPTH, G8, kSp>, dim3(a.n_ctas / kGroups), dim3(kThreads), size_t(smem),
+                          stream, a);
+}
+
+template <bool kSp>
+cudaError_t launch_form(const AttnArgs& a, cudaStream_t stream) {
+  switch (a.depth * 2 + (a.g == 8 ? 1 : 0)) {
+    case 2: return launch_depth<1, false, kSp>(a, stream);
+    case 3: return launch_depth<1, true, kSp>(a, stream);
+    case 4: return launch_depth<2, false, kSp>(a, stream);
+    case 5: return launch_depth<2, true, kSp>(a, stream);
+    case 6: return launch_depth<3, false, kSp>(a, stream);
+    case 7: return launch_depth<3, true, kSp>(a, stream);
+    case 8: return launch_depth<4, false, kSp>(a, stream);
+    case 9: return launch_depth<4, true, kSp>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace tc_attn
 
 int tc_virtual_ctas_per_block() { return tc_attn::kGroups; }
 
-// The INT4 packed attention (dense calls, depth <= 4, 1/2/4/8 query heads per
-// KV head); the caller refuses requests holding NVFP4 loops in the plan.
+// The INT4 packed attention (depth <= 4, 1/2/4/8 query heads per KV head),
+// dense calls and the sparse-decode passes (key masks, logits); the caller
+// refuses requests holding NVFP4 loops in the plan.
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream) {
   using namespace tc_attn;
-  cudaError_t e;
-  switch (a.depth * 2 + (a.g == 8 ? 1 : 0)) {
-    case 2: e = launch_depth<1, false>(a, stream); break;
-    case 3: e = launch_depth<1, true>(a, stream); break;
-    case 4: e = launch_depth<2, false>(a, stream); break;
-    case 5: e = launch_depth<2, true>(a, stream); break;
-    case 6: e = launch_depth<3, false>(a, stream); break;
-    case 7: e = launch_depth<3, true>(a, stream); break;
-    case 8: e = launch_depth<4, false>(a, stream); break;
-    case 9: e = launch_depth<4, true>(a, stream); break;
-    default: return cudaErrorInvalidValue;
-  }
+  const cudaError_t e = (a.sel_mask != nullptr || a.logits != nullptr) ? launch_form<true>(a, stream)
+                                                                        : launch_form<false>(a, stream);
+  if (e == cudaErrorInvalidValue) return e;
   count_launch();
   return e;
 }
