@@ -706,7 +706,11 @@ def run_nvfp4_extra(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, tim
     att_n, _ = timed(lambda: kvq.kvq_decode_attn_packed(npool.table, q, depth, H, out=out_n, workspace=ws))
     att_i, _ = timed(lambda: kvq.kvq_decode_attn_packed(pool.table, q, depth, H, out=out_i, workspace=ws))
     # the NVFP4-reading form of the tensor-core kernel on the INT4 pool: the cost of carrying both formats
-    att_in, _ = timed(lambda: kvq.kvq_decode_attn_packed(pool.table, q, depth, H, algo=kvq.ATTN_AUTO | kvq.ATTN_NVFP4,
+    att_in, _ = timed(lambda: kvq.kvq_decode_attn_packed(pool.table, q, depth, H,
+                                                         algo=kvq.ATTN_MMA_GENERAL | kvq.ATTN_NVFP4,
+                                                         out=out_i, workspace=ws))
+    # the INT4 pool called with the NVFP4 flag: the plan finds no NVFP4 loop and the INT4 kernel runs
+    att_if, _ = timed(lambda: kvq.kvq_decode_attn_packed(pool.table, q, depth, H, algo=kvq.ATTN_AUTO | kvq.ATTN_NVFP4,
                                                          out=out_i, workspace=ws))
     err = kvq.attn_error_word(ws) | kvq.attn_error_word(npool.workspace)
     # attention error against FP32 attention over the unquantised chain
@@ -723,7 +727,8 @@ def run_nvfp4_extra(torch, kvq, pool, reqs, q, H, Hq, D, depth, dev, stream, tim
     res = {"formats": "INT4 base, NVFP4 loops 2..%d" % depth, "payload_bytes": npool.payload_bytes,
            "payload_bytes_int4": pool.payload_bytes, "encode_ms": enc_n, "encode_ms_int4": enc_i,
            "reconstruct_ms": rec_n, "reconstruct_ms_int4": rec_i, "attention_ms": att_n, "attention_ms_int4": att_i,
-           "attention_ms_int4_in_nvfp4_form": att_in, "sample_requests": len(sample),
+           "attention_ms_int4_in_nvfp4_form": att_in, "attention_ms_int4_with_nvfp4_flag": att_if,
+           "sample_requests": len(sample),
            "recon_rmse_vs_unquantised_chain": rmse, "attn_max_abs_err_vs_unquantised_chain": worst,
            "error_word": err}
     del npool

@@ -361,13 +361,17 @@ size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_head
 #define KVQ_ATTN_AUTO 0 /* tensor-core kernel for depth <= 4, CUDA-core kernel beyond */
 #define KVQ_ATTN_SIMT 1 /* CUDA-core kernel: FP32 decode of the chain per element, FP32 dot products */
 #define KVQ_ATTN_MMA 2  /* tensor-core kernel (depth <= 4): INT4 tables run the subnormal-code kernel (Q' and the
-                           K-min terms built once per tile); NVFP4 tables (with KVQ_ATTN_NVFP4) run the general one */
+                           K-min terms built once per tile). With KVQ_ATTN_NVFP4 both that kernel and the general
+                           one are launched and the plan kernel picks one: a call in which some request holds an
+                           NVFP4 loop within depth runs the general kernel, any other call the subnormal-code one
+                           (the other launch leaves at once) */
 #define KVQ_ATTN_MMA_GENERAL 3 /* the general tensor-core kernel (depth <= 4) for every table: codes as FP16 64 + c,
                                  Q' rebuilt per warp; the form the NVFP4 and sparse-decode paths use */
 #define KVQ_ATTN_TCGEN05 4 /* INT4 tables on the tcgen05 form of the subnormal-code kernel (codes in tensor memory and
                              shared memory, accumulators in tensor memory, warp-specialised, one block per SM; slower
                              than KVQ_ATTN_MMA on decode shapes); NVFP4 tables as KVQ_ATTN_MMA */
-#define KVQ_ATTN_NVFP4 8 /* OR-ed into algo: the table may hold NVFP4 residual loops. Without it the
+#define KVQ_ATTN_NVFP4 8 /* OR-ed into algo: the table may hold NVFP4 residual loops (an INT4 table
+                           passed with it costs one extra, empty kernel launch). Without it the
                            tensor-core kernel refuses such a request (NaN output, error bit 64); the
                            CUDA-core kernel reads either format. kvq_decode_attn_packed and the
                            no-alloc entry run without it (INT4 tables). */

@@ -762,6 +762,16 @@ static kvq_status attention_launches(const AttnArgs& a0, int algo, bool segments
   if (runs_tcgen05(a, algo == KVQ_ATTN_MMA)) a.n_ctas = a0.n_ctas / 2;
   cudaError_t e = launch_plan(a, s);
   if (e != cudaSuccess) return cuda_status(e, "plan launch");
+  if (algo == KVQ_ATTN_MMA && a.nvfp4 && !a.general && !a.tcgen05) {
+    // the table may hold NVFP4 loops: the INT4 kernel, then the NVFP4-reading
+    // one; the plan's flag makes exactly one of them work, the other leaves
+    AttnArgs t = a;
+    t.nvfp4 = 0;
+    t.dispatch = 1;
+    e = launch_attn_mma(t, s);
+    if (e != cudaSuccess) return cuda_status(e, "attention launch");
+    a.dispatch = 2;
+  }
   e = (algo == KVQ_ATTN_SIMT) ? launch_attn_simt(a, s) : launch_attn_mma(a, s);
   if (e != cudaSuccess) return cuda_status(e, "attention launch");
   e = launch_combine(a, s);

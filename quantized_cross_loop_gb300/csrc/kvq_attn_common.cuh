@@ -33,7 +33,8 @@ struct AttnArgs {
   float scale;        // softmax scale (natural-log units)
   float* out;         // FP32 [B][Hq][128]
   int32_t* err;       // error word
-  int32_t* flags;     // word after the error word: bit 0 = some request has BF16 segments (set by the plan)
+  int32_t* flags;     // word after the error word, set by the plan: bit 0 = some request has BF16
+                      // segments; bit 1 = some accepted request holds an NVFP4 loop within depth
   int32_t* prefix;    // [B+1] tile prefix
   float* partials;    // slots
   float2* stats;      // [B][Hq] (max in log2 units, sum of exponentials) of the packed part
@@ -56,6 +57,10 @@ struct AttnArgs {
   // 1: the plan kernel clears the error word and the plan flags before its
   // checks (the call's first launch; no separate memset)
   int32_t clear_err;
+  // a call whose table may hold NVFP4 loops launches two kernels and the plan
+  // picks one: 1 = this INT4 kernel leaves when flags bit 1 is set; 2 = this
+  // NVFP4-reading kernel leaves unless it is set; 0 = the kernel always runs
+  int32_t dispatch;
 };
 
 // Programmatic dependent launches: a kernel launched with launch_dependent()
@@ -150,11 +155,13 @@ __device__ __forceinline__ bool request_ok(const kvq_request& r, int depth) {
 
 // A request this call can attend: a consistent entry, and no NVFP4 loop when
 // the call's kernel does not read them.
-__device__ __forceinline__ bool nvfp4_refused(const AttnArgs& a, const kvq_request& r) {
-  if (!a.refuse_nvfp4) return false;
-  for (int j = 0; j < a.depth && j < KVQ_MAX_LOOPS; ++j)
+__device__ __forceinline__ bool holds_nvfp4(const kvq_request& r, int depth) {
+  for (int j = 0; j < depth && j < KVQ_MAX_LOOPS; ++j)
     if (r.loop[j].flags & (KVQ_LOOP_K_NVFP4 | KVQ_LOOP_V_NVFP4)) return true;
   return false;
+}
+__device__ __forceinline__ bool nvfp4_refused(const AttnArgs& a, const kvq_request& r) {
+  return a.refuse_nvfp4 && holds_nvfp4(r, a.depth);
 }
 __device__ __forceinline__ bool attn_request_ok(const AttnArgs& a, const kvq_request& r) {
   return request_ok(r, a.depth) && !nvfp4_refused(a, r);

@@ -953,6 +953,7 @@ template <int DEPTH, bool kNv, bool kSp>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  if (a.dispatch == 2 && !(*a.flags & 2)) return;  // no NVFP4 loop in the call: the INT4 kernel ran
   const int C = a.n_ctas;  // virtual CTAs: two per block
   const long long W = a.prefix[a.n_requests];
   if (threadIdx.x == 0) {

@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnArgs a) {
       } else {
         v = a.H * n_tiles_of(r.n_tokens);
         if (r.n_sink + r.n_tail > 0) atomicOr(a.flags, 1);
+        if (holds_nvfp4(r, a.depth)) atomicOr(a.flags, 2);
       }
     }
     int x = v;

@@ -864,6 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
     reinterpret_cast<uint4*>(S.grp)[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
   wait_prior_grid();  // the plan (tile prefix, error word) is complete and visible from here on
+  if (a.dispatch == 1 && (*a.flags & 2)) return;  // the plan found NVFP4 loops: the NVFP4-reading kernel runs
   const long long W = a.prefix[a.n_requests];
   int grp, pw = 0;
   bool producer_warp;

@@ -13,8 +13,8 @@
 //   sparse_logits_kernel  block = (request, KV head, 64-token tile): the FP32
 //                         logits (log2 units) of every key for the g query heads
 //   sparse_select_kernel  block = (request, query head): softmax max and sum,
-//                         exact top-k by a 4-pass radix select on
-//                         order-preserving keys (ties: lower position), the
+//                         exact top-k by a radix select of up to four passes
+//                         on order-preserving keys (ties: lower position), the
 //                         selected indices in ascending order, m and C_ref
 //   sparse_attn_kernel    block = (request, query head): the later loop
 #include "kvq_attn_common.cuh"
@@ -93,6 +93,14 @@ __global__ void __launch_bounds__(128) sparse_logits_kernel(SparseArgs a) {
 // ---------------------------------------------------------------- selection, m and C_ref
 
 constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
+static_assert(kSelThreads == 256, "one histogram bin per thread");
+// Requests of up to this many keys keep their order-preserving keys in shared
+// memory for the selection's passes; longer ones re-read the logits.
+constexpr int kSelStageMax = 12288;
+// The first this many selected positions also go to shared memory, from which
+// the C_ref gather reads them.
+constexpr int kSelListMax = 1024;
 
 // Block-wide exclusive scan of one flag per thread; returns the prefix and
 // writes the total to *total (every thread).
@@ -103,7 +111,7 @@ __device__ __forceinline__ int block_scan(int flag, int* s_warp, int* total) {
   if (lane == 0) s_warp[warp] = __popc(ball);
   __syncthreads();
   int before = 0, sum = 0;
-  for (int w = 0; w < kSelThreads / 32; ++w) {
+  for (int w = 0; w < kSelWarps; ++w) {
     const int c = s_warp[w];
     if (w < warp) before += c;
     sum += c;
@@ -113,7 +121,58 @@ __device__ __forceinline__ int block_scan(int flag, int* s_warp, int* total) {
   return before + within;
 }
 
-__global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseArgs a) {
+// The float of an order-preserving key.
+__device__ __forceinline__ float okey_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// The FP32 chain of V at a stored-row set over channels c0 .. c0 + 15 (c0 a
+// multiple of 16: one V group, one NVFP4 block): the arithmetic of
+// chain4_f32, with one 8-byte codes load and one parameter pair per loop. The
+// decode min + scale * c is one FMA: scale * c is exact (an FP16 significand
+// times a 4-bit code), so the FMA rounds once where chain4_f32 rounds the sum.
+__device__ __forceinline__ void chain16_v_f32(const Chain& C, int depth, const int* rows, int h, int c0,
+                                              float out[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) out[e] = 0.0f;
+  for (int j = 0; j < depth; ++j) {
+    const int row = rows[j];
+    if (row < 0) continue;
+    const LoopPlanes& L = C.loop[j];
+    const long long rr = (long long)h * L.stride + row;
+    const uint2 cw = __ldg(reinterpret_cast<const uint2*>(L.codes + rr * kRowBytes + c0 / 2));
+    if (L.fmt == KVQ_FMT_NVFP4) {
+      const float sb = nvfp4_block_scale(L, h, row, c0 / 16), st = nvfp4_tensor_scale(L);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float dq = nvfp4_dequant(((e < 8 ? cw.x : cw.y) >> (4 * (e & 7))) & 0xFu, sb, st);
+        out[e] = (j == 0) ? dq : __fadd_rn(out[e], dq);
+      }
+      continue;
+    }
+    const long long pi = rr * (kD / kG) + c0 / kG;
+    const float mn = f16_bits_to_f32(__ldg(L.mins + pi)), sc = f16_bits_to_f32(__ldg(L.scales + pi));
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint32_t nib = ((e < 8 ? cw.x : cw.y) >> (4 * (e & 7))) & 0xFu;
+      const float dq = __fmaf_rn(sc, __uint_as_float(nib | 0x4B000000u) - 8388608.0f, mn);
+      out[e] = (j == 0) ? dq : __fadd_rn(out[e], dq);
+    }
+  }
+}
+
+// Block = (request, query head). The logits become order-preserving keys
+// (staged in shared memory when the request fits); the K-th largest key comes
+// from up to four radix passes over the key bytes, most significant first: a
+// block histogram of the keys that share the prefix found so far (increments
+// aggregated per warp and bin), then one warp finds the bin holding the K-th
+// key by a suffix sum over its lanes. When that bin is taken whole the
+// threshold is its lowest key and the passes stop early. Positions are then
+// compacted in order (ties at the threshold: lower positions first), and C_ref
+// gathers the selected V rows, four keys per warp at a time (eight lanes per
+// key, sixteen channels per lane).
+__global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseArgs a, int staged) {
+  extern __shared__ uint32_t s_key[];  // [max_tokens] when staged
   const int bq = blockIdx.x;
   const int b = bq / a.Hq, hq = bq % a.Hq;
   const int h = hq / a.g;
@@ -139,76 +198,100 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseArgs a
     return;
   }
   const float* s = a.logits + (long long)bq * a.max_tokens;
-  __shared__ float s_red[kSelThreads / 32];
-  __shared__ int s_warp[kSelThreads / 32];
+  __shared__ float s_red[kSelWarps];
+  __shared__ int s_warp[kSelWarps];
   __shared__ unsigned s_hist[256];
-  __shared__ unsigned s_prefix, s_need;
+  __shared__ unsigned s_prefix, s_need, s_whole;
   __shared__ Chain C;
-  __shared__ float s_acc[kSelThreads / 32][kD];
+  __shared__ float s_acc[kSelWarps][kD];
+  __shared__ int s_sel[kSelListMax];
+  auto key_at = [&](int t) -> uint32_t { return staged ? s_key[t] : okey(s[t]); };
 
-  // softmax max and sum (log2 units)
+  // softmax max (and the staged keys), then the sum (log2 units)
   float mx = -INFINITY;
-  for (int t = tid; t < T; t += kSelThreads) mx = fmaxf(mx, s[t]);
+  for (int t = tid; t < T; t += kSelThreads) {
+    const float v = s[t];
+    if (staged) s_key[t] = okey(v);
+    mx = fmaxf(mx, v);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   if (lane == 0) s_red[warp] = mx;
+  if (tid == 0) {
+    s_prefix = 0;
+    s_need = unsigned(K);  // keys still to take at and below the current prefix
+    s_whole = 0;
+  }
   __syncthreads();
   float M = s_red[0];
-  for (int w = 1; w < kSelThreads / 32; ++w) M = fmaxf(M, s_red[w]);
+  for (int w = 1; w < kSelWarps; ++w) M = fmaxf(M, s_red[w]);
   __syncthreads();
   float sum = 0.0f;
-  for (int t = tid; t < T; t += kSelThreads) sum += exp2f(s[t] - M);
+  for (int t = tid; t < T; t += kSelThreads) sum += exp2f(okey_value(key_at(t)) - M);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
   if (lane == 0) s_red[warp] = sum;
   __syncthreads();
   float L = 0.0f;
-  for (int w = 0; w < kSelThreads / 32; ++w) L += s_red[w];
-  __syncthreads();
+  for (int w = 0; w < kSelWarps; ++w) L += s_red[w];
 
-  // the K-th largest key: four passes over the key bytes, most significant first
-  if (tid == 0) {
-    s_prefix = 0;
-    s_need = unsigned(K);  // keys still to take at and below the current prefix
-  }
+  // the threshold key
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kSelThreads) s_hist[i] = 0;
+    s_hist[tid] = 0;  // kSelThreads == 256 bins
     __syncthreads();
     const unsigned prefix = s_prefix;
     const unsigned hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
-    // warp-aggregated increments: logits of one request crowd a few bins (the top
-    // byte is the sign and most of the exponent), so one atomic per bin and warp
+    // logits of one request crowd a few bins (the top byte is the sign and most
+    // of the exponent): one shared atomic per warp and bin
     for (int base = 0; base < T; base += kSelThreads) {
       const int t = base + tid;
-      const uint32_t key = t < T ? okey(s[t]) : 0u;
+      const uint32_t key = t < T ? key_at(t) : 0u;
       const bool in = t < T && (key & hmask) == (prefix & hmask);
-      const unsigned bin = (key >> shift) & 0xFFu;
-      const unsigned peers = __match_any_sync(0xffffffffu, in ? bin : 256u + unsigned(lane));
-      if (in && __ffs(peers) - 1 == lane) atomicAdd(&s_hist[bin], unsigned(__popc(peers)));
-    }
-    __syncthreads();
-    if (tid == 0) {
-      unsigned need = s_need, acc = 0;
-      int bin = 255;
-      for (; bin > 0; --bin) {
-        if (acc + s_hist[bin] >= need) break;
-        acc += s_hist[bin];
+      if (__ballot_sync(0xffffffffu, in) != 0u) {
+        const unsigned bin = (key >> shift) & 0xFFu;
+        const unsigned peers = __match_any_sync(0xffffffffu, in ? bin : 256u + unsigned(lane));
+        if (in && __ffs(peers) - 1 == lane) atomicAdd(&s_hist[bin], unsigned(__popc(peers)));
       }
-      s_prefix = prefix | (unsigned(bin) << shift);
-      s_need = need - acc;  // keys to take equal to the prefix so far
     }
     __syncthreads();
+    if (warp == 0) {  // lane l holds bins 8l .. 8l + 7; the suffix sums run from the top bin down
+      const unsigned need = s_need;
+      unsigned mine = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mine += s_hist[8 * lane + k];
+      unsigned suf = mine;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const unsigned v = __shfl_down_sync(0xffffffffu, suf, off);
+        if (lane + off < 32) suf += v;
+      }
+      const unsigned reach = __ballot_sync(0xffffffffu, suf >= need);  // lanes 0 .. l*
+      const int ls = reach ? 31 - __clz(reach) : 0;
+      if (lane == ls) {
+        unsigned acc = suf - mine;  // keys in the bins above this lane's
+        int bin = 8 * lane + 7;
+        for (; bin > 8 * lane; --bin) {
+          if (acc + s_hist[bin] >= need) break;
+          acc += s_hist[bin];
+        }
+        s_prefix = prefix | (unsigned(bin) << shift);
+        s_need = need - acc;  // keys to take equal to the prefix so far
+        s_whole = (acc + s_hist[bin] == need) ? 1u : 0u;
+      }
+    }
+    __syncthreads();
+    if (s_whole) break;
   }
-  const uint32_t tau = s_prefix;    // the K-th largest key
-  const unsigned take_eq = s_need;  // keys equal to tau to take, lowest positions first
+  const uint32_t tau = s_prefix;  // the K-th largest key, or the lowest key of a bin taken whole
+  const unsigned take_eq = s_whole ? 0xFFFFFFFFu : s_need;  // keys equal to tau to take, lowest positions first
 
   // compaction in position order; m from the selected probabilities
   int written = 0, eq_seen = 0;
   float msum = 0.0f;
   for (int base = 0; base < T; base += kSelThreads) {
     const int t = base + tid;
-    const uint32_t key = t < T ? okey(s[t]) : 0u;
+    const uint32_t key = t < T ? key_at(t) : 0u;
     const int is_eq = (t < T && key == tau) ? 1 : 0;
     int eq_total = 0;
     const int eq_before = eq_seen + block_scan(is_eq, s_warp, &eq_total);
@@ -217,7 +300,8 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseArgs a
     const int pos = written + block_scan(take, s_warp, &n_take);
     if (take) {
       sel[pos] = t;
-      msum += exp2f(s[t] - M);
+      if (pos < kSelListMax) s_sel[pos] = t;
+      msum += exp2f(okey_value(key) - M);
     }
     written += n_take;
     eq_seen += eq_total;
@@ -226,31 +310,45 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseArgs a
   for (int off = 16; off > 0; off >>= 1) msum += __shfl_xor_sync(0xffffffffu, msum, off);
   if (lane == 0) s_red[warp] = msum;
   if (tid == 0) chain_of(r, KVQ_V, a.depth, a.H, C);
-  __syncthreads();
+  __syncthreads();  // also orders the selected positions before their reads below
   if (tid == 0) {
     float ms = 0.0f;
-    for (int w = 0; w < kSelThreads / 32; ++w) ms += s_red[w];
+    for (int w = 0; w < kSelWarps; ++w) ms += s_red[w];
     a.mass[bq] = ms / L;
   }
 
-  // C_ref: the selected rows of V at the reference depth, weighted by p
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int i = warp; i < K; i += kSelThreads / 32) {
-    const int t = sel[i];
-    int rows[KVQ_MAX_LOOPS];
-    rows_of(C, a.depth, t, rows);
-    float vv[4];
-    chain4_f32(C, a.depth, rows, t, h, 4 * lane, vv);
-    const float p = exp2f(s[t] - M) / L;
+  // C_ref: the selected rows of V at the reference depth, weighted by p; a
+  // warp takes four keys at a time, eight lanes per key
+  const int ks = lane >> 3, sub = lane & 7;
+  float acc[16];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] = fmaf(p, vv[e], acc[e]);
+  for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
+  for (int i0 = 4 * warp; i0 < K; i0 += 4 * kSelWarps) {
+    const int i = i0 + ks;
+    if (i < K) {
+      const int t = i < kSelListMax ? s_sel[i] : sel[i];
+      int rows[KVQ_MAX_LOOPS];
+      rows_of(C, a.depth, t, rows);
+      float vv[16];
+      chain16_v_f32(C, a.depth, rows, h, 16 * sub, vv);
+      const float p = exp2f(okey_value(key_at(t)) - M) / L;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e] = fmaf(p, vv[e], acc[e]);
+    }
   }
 #pragma unroll
-  for (int e = 0; e < 4; ++e) s_acc[warp][4 * lane + e] = acc[e];
+  for (int e = 0; e < 16; ++e) {
+    acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 8);
+    acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
+  }
+  if (ks == 0) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) s_acc[warp][16 * sub + e] = acc[e];
+  }
   __syncthreads();
   if (tid < kD) {
     float c = 0.0f;
-    for (int w = 0; w < kSelThreads / 32; ++w) c += s_acc[w][tid];
+    for (int w = 0; w < kSelWarps; ++w) c += s_acc[w][tid];
     cref[tid] = c;
   }
 }
@@ -408,14 +506,21 @@ cudaError_t launch_sparse_select_path(const SparseArgs& a, cudaStream_t stream) 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  sparse_select_kernel<<<a.n_requests * a.Hq, kSelThreads, 0, stream>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_sparse_select(a, stream);
 }
 
 cudaError_t launch_sparse_select(const SparseArgs& a, cudaStream_t stream) {
   if (a.n_requests == 0) return cudaSuccess;
-  sparse_select_kernel<<<a.n_requests * a.Hq, kSelThreads, 0, stream>>>(a);
+  const int staged = a.max_tokens <= kSelStageMax ? 1 : 0;
+  const size_t smem = staged ? size_t(a.max_tokens) * 4 : 0;
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(sparse_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kSelStageMax * 4);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  sparse_select_kernel<<<a.n_requests * a.Hq, kSelThreads, smem, stream>>>(a, staged);
   count_launch();
   return cudaGetLastError();
 }

@@ -204,6 +204,42 @@ def test_int4_tensor_core_kernel_refuses_nvfp4():
     P.assert_attention_close(o[1], ref, "INT4 request")
 
 
+def test_nvfp4_flag_picks_the_kernel_on_the_device():
+    """With KVQ_ATTN_NVFP4 the call launches the INT4 kernel and the NVFP4-reading
+    one, and the plan picks the one that works: an INT4 table gives the bits of
+    the call without the flag, a table holding an NVFP4 loop those of the general
+    kernel (which reads both formats); either within the attention tolerance of
+    the oracle."""
+    H, Hq = 8, 32
+    _, kc, vc, oks, ovs, _ = _nvfp4_requests([300], Hq, 720)
+    _, kc4, vc4, oks4, ovs4, _ = _nvfp4_requests([200, 77], Hq, 721, (I4, I4, I4, I4))
+    q3 = torch.randn((3, Hq, D), generator=torch.Generator().manual_seed(722)).to(torch.bfloat16).cuda()
+    L = kvq.lib()
+
+    def call(table, n, algo):
+        ws = torch.empty(kvq.kvq_decode_attn_workspace_bytes(n, H, Hq, D), dtype=torch.uint8, device="cuda")
+        out = torch.empty((n, Hq, D), dtype=torch.float32, device="cuda")
+        st = L.kvq_decode_attn_packed_ex(kvq._dptr(table.table), n, H, Hq, D, 4, kvq._dptr(q3[:n].contiguous()),
+                                         ctypes.c_float(0.088), kvq._dptr(out), kvq._dptr(ws), ws.numel(), algo, None)
+        torch.cuda.synchronize()
+        assert st == 0 and kvq.attn_error_word(ws) == 0, algo
+        return out.cpu().numpy()
+
+    int4 = kvq.RequestTable(kc4, vc4, torch.device("cuda"))
+    plain = call(int4, 2, kvq.ATTN_MMA)
+    assert np.array_equal(call(int4, 2, kvq.ATTN_MMA | kvq.ATTN_NVFP4), plain)
+    assert np.array_equal(call(int4, 2, kvq.ATTN_AUTO | kvq.ATTN_NVFP4), plain)
+    mixed = kvq.RequestTable(kc4[:1] + kc + kc4[1:], vc4[:1] + vc + vc4[1:], torch.device("cuda"))
+    flagged = call(mixed, 3, kvq.ATTN_MMA | kvq.ATTN_NVFP4)
+    assert np.array_equal(flagged, call(mixed, 3, kvq.ATTN_MMA_GENERAL | kvq.ATTN_NVFP4))
+    ref = lambda b, ok_, ov_: O.attention_f32(bf16_bits(q3[b].cpu()), O.decode_f32(ok_, 4),  # noqa: E731
+                                              O.decode_f32(ov_, 4), 0.088)
+    for b, (ok_, ov_) in enumerate([(oks4[0], ovs4[0]), (oks[0], ovs[0]), (oks4[1], ovs4[1])]):
+        P.assert_attention_close(flagged[b], ref(b, ok_, ov_), f"mixed table, request {b}")
+    for b in range(2):
+        P.assert_attention_close(plain[b], ref(b, oks4[b], ovs4[b]), f"INT4 table, request {b}")
+
+
 def test_sparse_later_loop_without_the_nvfp4_flag_refuses_nvfp4():
     """The tensor-core sparse later loop called without KVQ_ATTN_NVFP4: the request
     holding NVFP4 loops is refused (NaN, bit 64), the INT4 request beside it agrees

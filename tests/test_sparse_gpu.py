@@ -90,6 +90,8 @@ def _check_selection(sel, q_bits, kf, Hq, g, K, scale):
     ([4096], False, 1024, 32),
     ([777, 64, 1], True, 100, 64),
     ([200], False, 500, 32),  # more than T: every key
+    ([1000, 300], True, 10, 32),  # at most max_tokens / 64 keys: C_ref gathered key by key
+    ([12300, 40], False, 400, 32),  # beyond the staged length: keys re-read, C_ref key by key
 ])
 def test_sparse_reference_and_later_loops(Ts, sparse, n_select, Hq):
     table, reqs, oks, ovs, qs = _setup(Ts, sparse, Hq, seed=sum(Ts) + n_select)
