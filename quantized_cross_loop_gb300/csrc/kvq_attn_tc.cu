@@ -564,9 +564,17 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
   const float lsc = a.scale * kLog2e * 16777216.0f;  // the logits carry 2^-24
   GroupSmem& Gs = S.grp[grp];
   const uint32_t lowA = (1u << g) - 1u, lowC = (1u << (g + 8)) - 1u;  // slice tokens before g, g + 8
-  uint32_t lowP[4];  // slice tokens before 2q, 2q + 1, 2q + 8, 2q + 9
+  // PV takes the warp's 16 tokens in the order t(kk) = s(kk) for kk < 8 and s(kk - 8) + 8 beyond,
+  // s(x) = x ^ ((x >> 1) & 1): the four rows that the q lanes load for one A register (rows 2q of
+  // the slice in plain order, all 128 bytes apart, so in the same banks) then alternate between the
+  // two 64-byte halves of the bank line (rows 0, 3, 4, 7 and 1, 2, 5, 6). B takes P' of the same
+  // tokens: lane group g holds the p of token s(g) (a shuffle from lane group s(g), s being its own
+  // inverse), which the transposition turns into the rows of tokens s(2q), s(2q + 1).
+  const int gs = g ^ ((g >> 1) & 1);
+  const uint32_t lowAs = (1u << gs) - 1u, lowCs = (1u << (gs + 8)) - 1u;  // slice tokens before s(g), s(g) + 8
+  uint32_t lowP[4];  // slice tokens before s(2q), s(2q + 1), s(2q) + 8, s(2q + 1) + 8
 #pragma unroll
-  for (int k = 0; k < 4; ++k) lowP[k] = (1u << (2 * q + (k & 1) + 8 * (k >> 1))) - 1u;
+  for (int k = 0; k < 4; ++k) lowP[k] = (1u << (((2 * q + (k & 1)) ^ (q & 1)) + 8 * (k >> 1))) - 1u;
   UnitState U;
   int cur_unit = -1;
   UnitInfo Mprev = {-1, 0, 0, 0};
@@ -753,16 +761,22 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       }
     }
 
-    // ---- PV over every loop
+    // ---- PV over every loop (tokens s(g), s(g) + 8 in this lane group's B rows)
+    float pAs[2], pCs[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      pAs[e] = __shfl_sync(0xffffffffu, pA[e], 4 * gs + q);
+      pCs[e] = __shfl_sync(0xffffffffu, pC[e], 4 * gs + q);
+    }
 #pragma unroll
     for (int j = 0; j < DEPTH; ++j) {
       const uint32_t bits = pbits[j];
       if (bits == 0) continue;
       const int rb = prb[j];
       const int vrem = st.meta[16 + 8 * j + 4];
-      const bool pa = (bits >> g) & 1, pc = (bits >> (g + 8)) & 1;
-      const int ra = rb + __popc(bits & lowA), rc = rb + __popc(bits & lowC);
-      // V params of tokens g, g + 8 ({group 0, group 1} pairs), P' = RN16(p * sV) and the V-min
+      const bool pa = (bits >> gs) & 1, pc = (bits >> (gs + 8)) & 1;
+      const int ra = rb + __popc(bits & lowAs), rc = rb + __popc(bits & lowCs);
+      // V params of tokens s(g), s(g) + 8 ({group 0, group 1} pairs), P' = RN16(p * sV) and the V-min
       // terms (a token without a stored row reads nothing: its staged slot may hold stale bits)
       const uint32_t sva = pa ? *reinterpret_cast<const uint32_t*>(&st.l[j].vsc[vrem + 2 * ra]) : 0u;
       const uint32_t svc = pc ? *reinterpret_cast<const uint32_t*>(&st.l[j].vsc[vrem + 2 * rc]) : 0u;
@@ -773,11 +787,11 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
       float qa[2], qc[2];  // p of the slots, zero for a token without a row in this loop
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        qa[e] = pa ? pA[e] : 0.f;
-        qc[e] = pc ? pC[e] : 0.f;
+        qa[e] = pa ? pAs[e] : 0.f;
+        qc[e] = pc ? pCs[e] : 0.f;
       }
-      // A: V codes of tokens 2q, 2q + 1, 2q + 8, 2q + 9 (a token without a row reads a valid
-      // row against a zero P')
+      // A: V codes of tokens s(2q), s(2q + 1), s(2q) + 8, s(2q + 1) + 8 (a token without a row
+      // reads a valid row against a zero P')
       const uint8_t* vbase = &st.l[j].vc[0];
       int ro[4];
 #pragma unroll
