@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(kSelThreads) sparse_select_kernel(SparseArgs a
     const int t = base + tid;
     const uint32_t key = t < T ? key_at(t) : 0u;
     const int is_eq = (t < T && key == tau) ? 1 : 0;
-    int eq_total = 0;
-    const int eq_before = eq_seen + block_scan(is_eq, s_warp, &eq_total);
+    int eq_total = 0, eq_before = 0;  // keys equal to tau are counted only when some are left out
+    if (take_eq != 0xFFFFFFFFu) eq_before = eq_seen + block_scan(is_eq, s_warp, &eq_total);
     const int take = (t < T) && (key > tau || (is_eq && unsigned(eq_before) < take_eq));
     int n_take = 0;
     const int pos = written + block_scan(take, s_warp, &n_take);
