@@ -138,6 +138,47 @@ def test_sparse_reference_and_later_loops(Ts, sparse, n_select, Hq):
                     P.assert_attention_close(outs[path, depth][b], dense, f"dense req {b} depth {depth} {path}")
 
 
+@pytest.mark.parametrize("n_select", [10, 64, 70])
+def test_sparse_selection_breaks_exact_ties_by_position(n_select):
+    """Keys with exactly equal logits: tokens 64-127 of each KV head share one K
+    row (a constant K group, so equal codes and parameters), built to outscore
+    every other key for each of the head's query heads. The selection takes the
+    lowest positions among them (RFC §3.2 top-k with the position tie-break);
+    beyond 64 keys it takes the whole tied group, then the best of the rest, as
+    the oracle's logits rank them."""
+    T, Hq = 256, 32
+    g = Hq // H
+    gen = torch.Generator().manual_seed(77)
+    q = torch.randn((1, Hq, D), generator=gen).to(torch.bfloat16)
+    xk = torch.randn((T, H, D), generator=gen) * 0.5
+    xv = torch.randn((T, H, D), generator=gen)
+    for h in range(H):  # the tied row: along the sum of the head's queries
+        xk[64:128, h] = 0.25 * q[0, g * h:g * h + g].float().sum(0)
+    xk, xv = xk.to(torch.bfloat16), xv.to(torch.bfloat16)
+    kc = [kvq.kvq_encode_base(xk.cuda(), kvq.KVQ_K)]
+    vc = [kvq.kvq_encode_base(xv.cuda(), kvq.KVQ_V)]
+    table = kvq.RequestTable([kc], [vc], torch.device("cuda"))
+    st = kvq.kvq_sparse_ref_state(table, q.cuda(), 1, H, n_select, T)
+    torch.cuda.synchronize()
+    assert kvq.attn_error_word(st.workspace) == 0
+    sel = st.sel_idx.cpu().numpy()[0]
+    ok = O.encode_chain(O.KIND_K, [bf16_bits(xk)], [None])
+    kf = O.decode_f32(ok, 1)
+    qb = bf16_bits(q[0])
+    for hq in range(Hq):
+        s64 = _logits64(qb, kf, hq, g, 1.0 / math.sqrt(D))
+        assert np.all(s64[64:128] == s64[64]) and s64[64] > np.delete(s64, np.arange(64, 128)).max()
+        if n_select <= 64:
+            assert np.array_equal(sel[hq], np.arange(64, 64 + n_select)), hq
+            continue
+        S = sel[hq]
+        assert len(S) == n_select and np.all(np.diff(S) > 0) and np.all(np.isin(np.arange(64, 128), S)), hq
+        rest = np.delete(np.arange(T), np.arange(64, 128))
+        picked = np.isin(rest, S)
+        tol = 1e-5 * max(1.0, float(np.abs(s64).max()))  # FP32 logits on the GPU, float64 here
+        assert picked.sum() == n_select - 64 and s64[rest[picked]].min() >= s64[rest[~picked]].max() - tol, hq
+
+
 def test_sparse_refuses_segments_and_bad_selections():
     table, reqs, oks, ovs, qs = _setup([100, 100], False, 32, seed=9)
     seg = tuple(torch.randn((n, H, D)).to(torch.bfloat16).cuda() for n in (2, 2, 0, 0))
