@@ -640,30 +640,29 @@ __device__ void consumer(const AttnArgs& a, Smem& S, int grp, int vcta, long lon
     for (int e = 0; e < kSlots; ++e)
 #pragma unroll
       for (int ch = 0; ch < kChains; ++ch) C[e][ch][0] = C[e][ch][1] = C[e][ch][2] = C[e][ch][3] = 0.f;
-    uint32_t pbits[DEPTH];  // per loop: presence of the warp's 16 tokens, and the first stored row
+    // per loop: presence of the warp's 16 tokens and the first stored row of its slice, for every
+    // loop before the contractions (a dense loop stores the tile's first nrows tokens at rows
+    // 0 .. nrows - 1; a sparse loop's presence mask was built with the fragments; the branch-free
+    // form lets the loops' loads issue together)
+    uint32_t pbits[DEPTH];
     int prb[DEPTH];
 #pragma unroll
     for (int j = 0; j < DEPTH; ++j) {
+      const int nrows = st.meta[16 + 8 * j], sparse = st.meta[22 + 8 * j];
+      const unsigned long long mk = Gs.mask[j];  // stale for a dense loop, and then unused
+      const int cnt = max(0, min(16, nrows - 16 * w));
+      const uint32_t dense_bits = cnt >= 16 ? 0xFFFFu : ((1u << cnt) - 1u);
+      pbits[j] = nrows == 0 ? 0u : (sparse ? uint32_t(mk >> (16 * w)) & 0xFFFFu : dense_bits);
+      prb[j] = nrows == 0 ? 0 : (sparse ? __popcll(mk & ((1ull << (16 * w)) - 1ull)) : 16 * w);
+    }
+#pragma unroll
+    for (int j = 0; j < DEPTH; ++j) {
+      const uint32_t bits = pbits[j];
+      if (bits == 0) continue;
+      const int rb = prb[j];
       const int4 la = *reinterpret_cast<const int4*>(&st.meta[16 + 8 * j]);
       const int4 lb = *reinterpret_cast<const int4*>(&st.meta[20 + 8 * j]);
-      const int c0 = la.y, g0 = la.z, ngrp = la.w, sparse = lb.z, pbase = lb.w;
-      uint32_t bits;
-      int rb;
-      if (la.x == 0) {
-        bits = 0;
-        rb = 0;
-      } else if (!sparse) {  // the tile's first la.x tokens, rows 0 .. la.x - 1
-        const int cnt = max(0, min(16, la.x - 16 * w));
-        bits = cnt >= 16 ? 0xFFFFu : ((1u << cnt) - 1u);
-        rb = 16 * w;
-      } else {
-        const unsigned long long mk = Gs.mask[j];
-        bits = uint32_t(mk >> (16 * w)) & 0xFFFFu;
-        rb = __popcll(mk & ((1ull << (16 * w)) - 1ull));
-      }
-      pbits[j] = bits;
-      prb[j] = rb;
-      if (bits == 0) continue;
+      const int c0 = la.y, g0 = la.z, ngrp = la.w, pbase = lb.w;
       // stored rows of tokens g and g + 8: the first row of the warp's slice plus the token's rank
       // among the slice's stored tokens (a dense slice stores them all, so the rank is the token);
       // an absent token gets a row index <= 64, inside the stage, whose codes its zero A row ignores
