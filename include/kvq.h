@@ -366,7 +366,7 @@ size_t kvq_decode_attn_workspace_bytes(int n_requests, int n_heads, int n_q_head
                            NVFP4 loop within depth runs the general kernel, any other call the subnormal-code one
                            (the other launch leaves at once) */
 #define KVQ_ATTN_MMA_GENERAL 3 /* the general tensor-core kernel (depth <= 4) for every table: codes as FP16 64 + c,
-                                 Q' rebuilt per warp; the form the NVFP4 and sparse-decode paths use */
+                                 Q' rebuilt per warp; the form that reads NVFP4 loops */
 #define KVQ_ATTN_TCGEN05 4 /* INT4 tables on the tcgen05 form of the subnormal-code kernel (codes in tensor memory and
                              shared memory, accumulators in tensor memory, warp-specialised, one block per SM; slower
                              than KVQ_ATTN_MMA on decode shapes); NVFP4 tables as KVQ_ATTN_MMA */

@@ -48,10 +48,11 @@ struct AttnArgs {
   // units) of key t < logit_stride to logits[(b * Hq + query head) * logit_stride + t]
   float* logits;
   int32_t logit_stride;
-  // tensor-core calls: 1 runs the general kernel (NVFP4 forms, sparse-decode
-  // masks and logits); 0 runs an INT4 kernel when the call has neither NVFP4
-  // loops, masks nor logits: the mma.sync kernel of kvq_attn_tc.cu, or the
-  // tcgen05 kernel of kvq_attn_tcgen05.cu when tcgen05 is 1
+  // tensor-core calls: 1 runs the general kernel (64 + c codes, the NVFP4
+  // form when nvfp4 is set); 0 runs the mma.sync kernel of kvq_attn_tc.cu for
+  // INT4 calls (sparse-decode masks and logits included), or, when tcgen05 is
+  // 1 and the call has neither masks nor logits, the tcgen05 kernel of
+  // kvq_attn_tcgen05.cu
   int32_t general;
   int32_t tcgen05;
   // 1: the plan kernel clears the error word and the plan flags before its
