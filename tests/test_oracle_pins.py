@@ -790,6 +790,25 @@ def test_sparse_all_keys_is_dense_attention():
     assert np.max(np.abs(out - _sdpa64_rows(q, k1, v1, 0.09, Hq))) < 1e-9
 
 
+def test_sparse_later_loop_on_the_reference_keys_returns_o_ref():
+    """A later loop that reads the reference loop's own K and V with the same
+    query attends S with the probabilities p_t / m, so m * softmax_S(V) = C_ref
+    and O = O_ref - C_ref + C_ref = O_ref, whatever the budget (RFC §3.2). A
+    dropped correction term, a wrong sign or a mass not taken over S breaks it."""
+    rng = np.random.default_rng(14)
+    T, H, Hq, D = 37, 2, 8, 128
+    q = bf16(rng.standard_normal((Hq, D)))
+    k, v = rng.standard_normal((T, H, D)), rng.standard_normal((T, H, D))
+    for K in (1, 5, 20, 36):
+        S, m, o_ref, c_ref = O.sparse_reference(q, k, v, 0.09, K)
+        assert np.all((m > 0) & (m < 1))
+        out = O.sparse_decode(q, k, v, 0.09, S, m, o_ref, c_ref)
+        assert np.max(np.abs(out - o_ref)) < 1e-9, K
+        # and the output moves when the later loop's values do
+        out2 = O.sparse_decode(q, k, v + 1.0, 0.09, S, m, o_ref, c_ref)
+        assert np.allclose(out2 - o_ref, m[:, None]), K
+
+
 def test_sparse_selection_is_top_k_with_position_ties():
     rng = np.random.default_rng(13)
     T, H, Hq, D = 40, 1, 2, 128
